@@ -1,0 +1,222 @@
+/*
+ * kvarn.h -- C ABI of the KVarN hot path on GB300 (sm_103a).
+ *
+ * KVarN stores the KV cache of a transformer as 4-bit keys and 2-bit values.
+ * Every 128-token tile of each KV head is compressed on its own:
+ *   1. an orthonormal Walsh-Hadamard rotation of every K and V row along
+ *      head_dim                       (SharpInference issue #180, "Algorithm
+ *                                      (per 128-token tile)" step 1;
+ *                                      SharpInference PR #434, commit 82efc4f);
+ *   2. a dual-axis "Sinkhorn" variance normalisation that alternates
+ *      per-channel and per-token std scaling, accumulated in log space
+ *                                     (issue #180, Algorithm step 2);
+ *   3. asymmetric round-to-nearest quantisation: keys 4-bit per channel over
+ *      the tile's tokens, values 2-bit per token over 128-channel groups,
+ *      keys packed channel-major and values token-major
+ *                                     (issue #180, Algorithm steps 3-4;
+ *                                      PR #434, commit 82efc4f).
+ * Attention reads the packed tiles directly: the query is rotated once, the
+ * scales are folded into the dequant-dot at read time, one streaming softmax
+ * runs over the tiles and the FP32 staging window of not-yet-full tiles, and
+ * a single inverse rotation is applied at the end (issue #180 step 4; PR #434,
+ * commits 0d7cd28 and 99c3773; SharpInference issue #433, item 2, which
+ * describes the split-tile decode with an LSE combine).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array argument is a DEVICE pointer owned by the caller, unless the
+ *    argument says "host". The library never allocates device memory and keeps
+ *    no state between calls: scratch space is passed in as a workspace.
+ *  - Work is enqueued asynchronously on the given stream; nothing synchronises.
+ *  - All floating-point data is IEEE fp32, little-endian.
+ *  - The return value is a kvarn_status_t. Argument errors are detected on the
+ *    host before anything is launched and nothing is enqueued in that case.
+ *    A launch failure reported by the CUDA runtime returns KVARN_ERR_CUDA.
+ *    Faults inside a kernel surface at the caller's next synchronisation.
+ *  - head_dim D must be a power of two in [64, 256]; the pages' CUDA path
+ *    supports power-of-two head dims up to 256 (PR #434, "Scope notes").
+ *  - The GQA mapping is contiguous: query head h reads KV head h / G with
+ *    G = Hq / Hkv (the pages do not state it; this is the usual grouping).
+ */
+#ifndef KVARN_H_
+#define KVARN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. 0 = legacy default stream. */
+typedef struct CUstream_st* kvarn_stream_t;
+
+typedef enum kvarn_status {
+  KVARN_OK = 0,
+  KVARN_ERR_NULL = -1,        /* a required pointer is NULL                        */
+  KVARN_ERR_ALIGN = -2,       /* a pointer, stride or offset breaks 16-byte alignment */
+  KVARN_ERR_UNSUPPORTED = -3, /* head_dim, GQA group or iteration count out of range */
+  KVARN_ERR_BAD_ARG = -4,     /* a size or count is negative or inconsistent       */
+  KVARN_ERR_WORKSPACE = -5,   /* the workspace is smaller than the _workspace_bytes query */
+  KVARN_ERR_CUDA = -6         /* the CUDA runtime rejected a launch                */
+} kvarn_status_t;
+
+/* Tokens per compressed tile. Tile i of a sequence always covers token
+ * positions [128 i, 128 i + 128), whatever chunking produced it, so
+ * re-chunking yields byte-identical tiles (PR #434, commit 99c3773; issue #433
+ * item 1, "re-chunking oracle"). */
+#define KVARN_TILE_TOKENS 128
+#define KVARN_K_BITS 4
+#define KVARN_V_BITS 2
+#define KVARN_LAYOUT_VERSION 1
+#define KVARN_DEFAULT_SINKHORN_ITERS 4
+
+/*
+ * Packed tile record: one record per (tile, KV head), headerless, all fields
+ * at 16-byte aligned offsets. The pages fix only channel-major K codes,
+ * token-major V codes and fp32 scales stored beside the codes (PR #434,
+ * commit 82efc4f; issue #433 item 3 names f16 scales as a later saving);
+ * the bit and field order below are this library's own.
+ * With T = 128, D = head_dim, Gv = D / min(D, 128) value groups per token:
+ *
+ *   off_k_codes  u8 [D][T/2]   K code of token t, channel c: byte c*64 + t/2,
+ *                              low nibble for even t, high nibble for odd t
+ *   off_v_codes  u8 [T][D/4]   V code of token t, channel c: byte t*(D/4) + c/4,
+ *                              bits 2*(c%4) .. 2*(c%4)+1
+ *   off_k_delta  f32 [D]       K step per channel
+ *   off_k_lo     f32 [D]       K offset (zero point, the group minimum) per channel
+ *   off_k_s      f32 [D]       K Sinkhorn channel factor s_c = exp(alpha_c)
+ *   off_k_r      f32 [T]       K Sinkhorn token factor r_t = exp(beta_t)
+ *   off_v_delta  f32 [T][Gv]   V step per token and group
+ *   off_v_lo     f32 [T][Gv]   V offset per token and group
+ *   off_v_r      f32 [T]       V Sinkhorn token factor
+ *   off_v_s      f32 [D]       V Sinkhorn channel factor
+ *
+ * Reconstruction in the rotated space: K~[t][c] = r_t s_c (delta_c code + lo_c),
+ * V~[t][c] = r_t s_c (delta_{t,g(c)} code + lo_{t,g(c)}); the token's K or V
+ * row is H times that row, H the orthonormal Sylvester Walsh-Hadamard matrix.
+ * record_bytes = 112 D + 1024 + 1024 Gv: 9216 at D=64, 16384 at D=128,
+ * 31744 at D=256.
+ */
+typedef struct kvarn_layout {
+  int32_t version;        /* KVARN_LAYOUT_VERSION                           */
+  int32_t head_dim;       /* D                                              */
+  int32_t tile_tokens;    /* 128                                            */
+  int32_t sinkhorn_iters; /* n, the fixed Sinkhorn round count (default 4)  */
+  int32_t k_bits;         /* 4                                              */
+  int32_t v_bits;         /* 2                                              */
+  int32_t v_group;        /* min(D, 128) channels per V quantisation group  */
+  int32_t v_groups;       /* D / v_group                                    */
+  int64_t record_bytes;
+  int64_t off_k_codes, off_v_codes;
+  int64_t off_k_delta, off_k_lo, off_k_s, off_k_r;
+  int64_t off_v_delta, off_v_lo, off_v_r, off_v_s;
+} kvarn_layout_t;
+
+/* Fills *out (host pointer) for head_dim and sinkhorn_iters (1..16).
+ * Returns KVARN_ERR_UNSUPPORTED for other head dims or iteration counts. */
+int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char* kvarn_status_string(int status);
+
+/*
+ * Query rotation (PR #434, commit 0d7cd28, llm_kvarn_rotate_query; issue #180
+ * Algorithm step 1): q_rot[i] = H q[i] for every row i, H the orthonormal
+ * Sylvester Walsh-Hadamard matrix of order D (symmetric, so self-inverse).
+ * Because H is orthonormal, (H q) . (H k) = q . k.
+ *   q, q_rot : fp32 [n_rows][D], contiguous, 16-byte aligned. q_rot == q
+ *              (in place) is allowed; any other overlap is not.
+ *   n_rows   : >= 0; 0 enqueues nothing.
+ */
+int kvarn_rotate_query(const float* q, float* q_rot, int64_t n_rows, int head_dim,
+                       kvarn_stream_t stream);
+
+/*
+ * Tile compression (issue #180, Algorithm steps 1-3; PR #434, commits 82efc4f
+ * and 0d7cd28, llm_kvarn_compress_tile). Each unit u turns 128 consecutive raw
+ * K rows and the matching 128 V rows into one packed record:
+ *   K rows  k_raw[(src_row0[u] + t) * row_stride + c], t < 128, c < D
+ *   V rows  v_raw[(same index)]
+ *   record  tiles + dst_record[u] (byte offset), layout->record_bytes long.
+ * A unit is a pure function of its 256 input rows, so the result does not
+ * depend on which other units share the launch or on their order.
+ *   k_raw, v_raw  : fp32, n_rows rows of row_stride elements, 16-byte aligned.
+ *   row_stride    : elements between rows, >= D and a multiple of 4.
+ *   n_rows        : rows in k_raw and v_raw; every src_row0[u] + 128 <= n_rows
+ *                   is the caller's promise (not checked on the device).
+ *   src_row0      : int64 [n_units], device.
+ *   tiles         : u8 base of the record pool, 16-byte aligned.
+ *   dst_record    : int64 [n_units] byte offsets, device, multiples of 16;
+ *                   records of one launch must not overlap.
+ *   layout        : host pointer from kvarn_layout().
+ */
+int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stride,
+                        int64_t n_rows, const int64_t* src_row0, uint8_t* tiles,
+                        const int64_t* dst_record, int64_t n_units,
+                        const kvarn_layout_t* layout, kvarn_stream_t stream);
+
+/*
+ * FP32 staging window append (PR #434, commit 6040076: the FP32 window is the
+ * staging area and whole 128-token tiles are promoted out of it). Copies n_new
+ * new raw K and V tokens of every sequence into that sequence's ring window:
+ *   k_new, v_new  : fp32 [n_seq][n_new][Hkv][D] (the projection's layout).
+ *   win_k, win_v  : fp32 [n_seq][Hkv][win_capacity][D] ring buffers.
+ *   win_start,
+ *   win_len       : int32 [n_seq], device. New token i of sequence s goes to
+ *                   ring slot (win_start[s] + win_len[s] + i) % win_capacity.
+ *                   The caller guarantees win_len[s] + n_new <= win_capacity.
+ * The library does not change win_start or win_len: the caller applies the
+ * promotion rule (while win_len >= W, compress the oldest 128 tokens with
+ * kvarn_compress_tile, then win_start += 128, win_len -= 128) and advances
+ * them. With win_capacity a multiple of 128 and win_start kept a multiple of
+ * 128, the oldest 128 tokens are always contiguous rows of the ring.
+ */
+int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new,
+                        float* win_k, float* win_v, int win_capacity,
+                        const int32_t* win_start, const int32_t* win_len,
+                        int n_seq, int n_kv_heads, int head_dim,
+                        kvarn_stream_t stream);
+
+/*
+ * Decode attention over the compressed cache (PR #434, commits 0d7cd28 and
+ * e43f3f0, llm_kvarn_attention; issue #433 item 2: a fixed worst-case grid
+ * over (head, tile range) with early exit, followed by an LSE combine, with
+ * the deferred inverse rotation applied after combining the rotated
+ * partials). Two launches: a split kernel over (sequence, KV head, tile range)
+ * that also runs the window, then a combine kernel over (sequence, query head).
+ *
+ * For query head h of sequence b the result is exact softmax attention
+ *   out[b][h] = sum_j softmax_j(scale * q[b][h] . k_j) v_j
+ * over every cached token j of KV head h / G: the tiles' tokens (k_j, v_j
+ * reconstructed as described at kvarn_layout_t) and then the window's raw rows.
+ *   q          : fp32 [B][Hq][D], unrotated.
+ *   tiles      : u8 base of the record pool.
+ *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets (multiples of
+ *                16); entries at or past n_tiles[b] are never read.
+ *   n_tiles    : int32 [B], 0 <= n_tiles[b] <= max_tiles (clamped on device).
+ *   win_k/v    : fp32 [B][Hkv][win_capacity][D]; win_start/win_len int32 [B]
+ *                as in kvarn_append_window (win_len clamped to win_capacity).
+ *   out        : fp32 [B][Hq][D]. A head with no tokens at all gets zeros.
+ *   softmax_scale : usually 1/sqrt(D) (the pages do not state it).
+ *   ws         : device workspace of at least kvarn_decode_workspace_bytes()
+ *                bytes, 256-byte aligned; it holds per-split partials and
+ *                needs no initialisation. Calls sharing ws must not overlap.
+ * The grid depends only on (B, Hkv, max_tiles, device), so the call can be
+ * captured in a CUDA graph and replayed while n_tiles and the windows change.
+ * Results are deterministic: the same inputs give bit-identical outputs.
+ */
+int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                                 size_t* bytes);
+int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
+                           const int32_t* n_tiles, const float* win_k, const float* win_v,
+                           const int32_t* win_start, const int32_t* win_len,
+                           int win_capacity, int B, int Hq, int Hkv, int head_dim,
+                           int max_tiles, float softmax_scale, const kvarn_layout_t* layout,
+                           void* ws, size_t ws_bytes, float* out, kvarn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H_ */

@@ -1,0 +1,371 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle
+itself: textbook matrices, closed forms, invariants of the algebra, hand-worked
+examples and library routines the oracle does not use.
+
+Each test names the step of the method it pins (SharpInference issue #180,
+"Algorithm (per 128-token tile)"; PR #434 commit 82efc4f for packing) and the
+plausible mistake it is there to catch.
+"""
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+
+from kv_cache_quantization_token_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+# ------------------------------------------------------------------ c1: WHT
+def test_wht_order4_matches_textbook_matrix(oracle):
+    """Issue #180 step 1. H_4 from the Sylvester recursion, typed in the golden
+    file by hand; catches sequency/bit-reversed ordering and sign slips."""
+    rows = _read_golden("hadamard4.txt")
+    H4 = np.array([[float(x) for x in r.split()] for r in rows]) / 2.0
+    got = oracle.wht_rows(np.eye(4))  # row i of the result is H e_i = column i
+    np.testing.assert_allclose(got.T, H4, atol=1e-15)
+    H2 = oracle.wht_rows(np.eye(2)).T
+    np.testing.assert_allclose(H2, np.array([[1, 1], [1, -1]]) / np.sqrt(2), atol=1e-15)
+
+
+@pytest.mark.parametrize("D", [2, 8, 64, 128, 256])
+def test_wht_matches_scipy_sylvester(oracle, D):
+    """scipy.linalg.hadamard builds the Sylvester matrix; the oracle does not use it."""
+    H = scipy.linalg.hadamard(D) / np.sqrt(D)
+    np.testing.assert_allclose(oracle.wht_rows(np.eye(D)).T, H, atol=1e-14)
+
+
+@pytest.mark.parametrize("D", [4, 64, 128, 256])
+def test_wht_orthonormal_self_inverse_preserves_dot(oracle, D):
+    """H orthonormal and symmetric: H(Hx) = x, |Hx| = |x|, (Hq).(Hk) = q.k."""
+    rng = np.random.default_rng(D)
+    x = rng.standard_normal((5, D))
+    y = oracle.wht_rows(x)
+    np.testing.assert_allclose(oracle.wht_rows(y), x, atol=1e-12)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    hq, hk = oracle.wht_rows(q[None])[0], oracle.wht_rows(k[None])[0]
+    assert abs(hq @ hk - q @ k) <= 1e-12 * (np.abs(q) @ np.abs(k))
+
+
+# ------------------------------------------------------------- c2: Sinkhorn
+def _balanced_pm1(T, D, seed):
+    """A +-1 matrix whose every row and every column has mean 0 and std 1."""
+    rng = np.random.default_rng(seed)
+    a = np.where(rng.permutation(T) < T // 2, 1.0, -1.0)
+    b = np.where(rng.permutation(D) < D // 2, 1.0, -1.0)
+    return np.outer(a, b)
+
+
+def test_sinkhorn_closed_form_column_scaled_fixed_point(oracle):
+    """Issue #180 step 2. Y = Z diag(b) with Z balanced +-1: the first channel
+    step gives s = b exactly and every later std is 1, so r = 1 and Yn = Z.
+    Catches exp(+alpha) for exp(-alpha), ln(var) for ln(std), and a sample
+    (N-1) std, each of which moves s, r or Yn off the closed form."""
+    T, D = 128, 64
+    Z = _balanced_pm1(T, D, 3)
+    b = np.exp(np.random.default_rng(4).standard_normal(D))
+    for iters in (1, 4):
+        s, r, yn = oracle.sinkhorn(Z * b[None, :], iters)
+        np.testing.assert_allclose(s, b, rtol=1e-13)
+        np.testing.assert_allclose(r, 1.0, rtol=1e-13)
+        np.testing.assert_allclose(yn, Z, atol=1e-13)
+
+
+def test_sinkhorn_channel_step_comes_first(oracle):
+    """Channel step first (issue #180 step 2 names per-channel before per-token):
+    then any positive per-channel scaling of Y is absorbed by s exactly and
+    leaves r and Yn unchanged at every iteration count. With the token step
+    first this only holds in the limit."""
+    k, _ = synth.kv_stream(0, 1, 0, 128, 128)
+    Y = oracle.wht_rows(k.astype(np.float64))
+    b = np.exp(np.random.default_rng(5).standard_normal(128))
+    for iters in (1, 2, 4):
+        s0, r0, y0 = oracle.sinkhorn(Y, iters)
+        s1, r1, y1 = oracle.sinkhorn(Y * b[None, :], iters)
+        np.testing.assert_allclose(s1, s0 * b, rtol=1e-12)
+        np.testing.assert_allclose(r1, r0, rtol=1e-12)
+        np.testing.assert_allclose(y1, y0, atol=1e-12)
+
+
+@pytest.mark.parametrize("cfg,D", [(0, 128), (2, 128), (4, 256), (2, 64)])
+def test_sinkhorn_normalises_rows_and_converges_on_columns(oracle, cfg, D):
+    """After the last (token) step every token std of Yn is 1; the worst
+    channel |ln std| never grows with more rounds and is below 0.05 at n = 4
+    on the synthetic workloads' distributions."""
+    k, v = synth.kv_stream(cfg, 2, 1, 128, D)
+    for x in (k, v):
+        Y = oracle.wht_rows(x.astype(np.float64))
+        prev = np.inf
+        for iters in (1, 2, 3, 4, 6):
+            s, r, yn = oracle.sinkhorn(Y, iters)
+            np.testing.assert_allclose(yn.std(axis=1), 1.0, rtol=1e-12)
+            np.testing.assert_allclose(yn, Y / np.outer(r, s), rtol=1e-12)
+            worst = np.abs(np.log(yn.std(axis=0))).max()
+            assert worst <= prev * (1 + 1e-9)
+            prev = worst
+            if iters == 4:
+                assert worst < 0.05
+
+
+def test_sinkhorn_global_scale_moves_only_s(oracle):
+    """Y -> cY: s -> c s, r and Yn unchanged (the channel step sees c first)."""
+    _, v = synth.kv_stream(2, 0, 3, 128, 128)
+    Y = oracle.wht_rows(v.astype(np.float64))
+    s0, r0, y0 = oracle.sinkhorn(Y, 4)
+    s1, r1, y1 = oracle.sinkhorn(3.7 * Y, 4)
+    np.testing.assert_allclose(s1, 3.7 * s0, rtol=1e-12)
+    np.testing.assert_allclose(r1, r0, rtol=1e-12)
+    np.testing.assert_allclose(y1, y0, atol=1e-12)
+
+
+def test_sinkhorn_skips_degenerate_groups(oracle):
+    """Skip rule (a reading; the pages are silent): an all-zero tensor keeps
+    s = r = 1; a constant channel is skipped although fp64 rounding leaves a
+    std of ~1e-17 (an absolute 1e-30 guard would take ln of it)."""
+    s, r, yn = oracle.sinkhorn(np.zeros((128, 64)), 4)
+    assert np.all(s == 1.0) and np.all(r == 1.0) and np.all(yn == 0.0)
+    rng = np.random.default_rng(9)
+    Y = rng.standard_normal((128, 64))
+    Y[:, 5] = 0.1  # constant channel: in round 1 its std is pure rounding
+    Y[:, 9] = 0.0  # zero channel: skipped in every round
+    s, r, yn = oracle.sinkhorn(Y, 1)
+    assert s[5] == 1.0 and s[9] == 1.0
+    # after a token step the constant channel is divided by varying r_t, so
+    # later rounds update it like any other channel
+    s, r, yn = oracle.sinkhorn(Y, 4)
+    assert s[9] == 1.0 and np.all(yn[:, 9] == 0.0)
+    assert s[5] != 1.0
+    assert np.all(np.isfinite(yn))
+
+
+# ------------------------------------------------------------------- c3: RTN
+def test_rtn_hand_worked_cases(oracle):
+    """Issue #180 step 3, asymmetric RTN with ties rounding half up. Each golden
+    line: bits, values ; expected codes, worked by hand from
+    code = floor((y - min) / ((max - min) / (2^bits - 1)) + 1/2)."""
+    for line in _read_golden("rtn_cases.txt"):
+        lhs, rhs = line.split(";")
+        bits, *vals = lhs.split()
+        want = [int(c) for c in rhs.split()]
+        d, lo, codes, _ = oracle.rtn_group(np.array([float(x) for x in vals]), int(bits))
+        assert list(codes) == want, line
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_rtn_error_bound_and_extremes(oracle, bits):
+    """|y - (delta code + lo)| <= delta/2; argmin -> 0; argmax -> 2^b - 1."""
+    rng = np.random.default_rng(bits)
+    for _ in range(20):
+        y = rng.standard_normal(128) * np.exp(rng.standard_normal())
+        d, lo, codes, vpre = oracle.rtn_group(y, bits)
+        assert codes.max() <= (1 << bits) - 1
+        assert codes[np.argmin(y)] == 0 and codes[np.argmax(y)] == (1 << bits) - 1
+        err = np.abs(y - (d * codes + lo))
+        assert np.all(err <= d / 2 * (1 + 1e-12))
+        np.testing.assert_allclose(vpre, (y - lo) / d, rtol=1e-15, atol=1e-15)
+
+
+def test_rtn_constant_group_gives_zero_codes(oracle):
+    d, lo, codes, _ = oracle.rtn_group(np.full(128, -1.25), 4)
+    assert d == 0.0 and lo == -1.25 and np.all(codes == 0)
+
+
+# --------------------------------------------------------------- c4: packing
+@pytest.mark.parametrize("D,size", [(64, 9216), (128, 16384), (256, 31744)])
+def test_record_size(oracle, D, size):
+    """K 4 bit + V 2 bit + fp32 scales: 112 D + 1024 + 1024 Gv bytes."""
+    assert oracle.record_bytes(D) == size
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_pack_unpack_roundtrip(oracle, D):
+    rng = np.random.default_rng(D + 1)
+    gv = D // min(D, 128)
+    f32 = lambda n: rng.standard_normal(n).astype(np.float32).astype(np.float64)
+    args = dict(k_codes=rng.integers(0, 16, (128, D)).astype(np.uint8),
+                v_codes=rng.integers(0, 4, (128, D)).astype(np.uint8),
+                k_delta=f32(D), k_lo=f32(D), k_s=f32(D), k_r=f32(128),
+                v_delta=f32(128 * gv), v_lo=f32(128 * gv), v_r=f32(128), v_s=f32(D))
+    rec = oracle.pack_record(D, **args)
+    back = oracle.unpack_record(rec, D)
+    for name, val in args.items():
+        np.testing.assert_array_equal(back[name], val, err_msg=name)
+
+
+def test_pack_bit_order_hand_built(oracle):
+    """Channel-major K: token 2i in the low nibble of byte i of channel row c;
+    token-major V: channel 4j+k in bits 2k..2k+1 of byte j of token row t."""
+    D = 64
+    kc = np.zeros((128, D), np.uint8)
+    vc = np.zeros((128, D), np.uint8)
+    kc[1, 0] = 0xA          # token 1, channel 0 -> high nibble of byte 0
+    kc[2, 3] = 0x5          # token 2, channel 3 -> low nibble of byte 3*64 + 1
+    vc[0, 1] = 2            # token 0, channel 1 -> bits 2..3 of V byte 0
+    vc[5, 63] = 3           # token 5, channel 63 -> bits 6..7 of byte 5*16 + 15
+    z = np.zeros
+    rec = oracle.pack_record(D, kc, vc, z(D), z(D), z(D), z(128), z(128), z(128), z(128), z(D))
+    assert rec[0] == 0xA0 and rec[3 * 64 + 1] == 0x05
+    voff = 64 * D
+    assert rec[voff] == 0x08 and rec[voff + 5 * 16 + 15] == 0xC0
+    assert np.count_nonzero(rec) == 4
+
+
+# --------------------------------------------------------- c5: reconstruction
+@pytest.mark.parametrize("cfg,D", [(0, 128), (2, 128), (4, 256), (2, 64)])
+def test_compress_dequant_distortion_bound(oracle, cfg, D):
+    """Per element of the rotated tile |Yn r s - recon| <= r s delta / 2, so by
+    orthonormality each unrotated row error is at most the norm of those
+    bounds. Pins compress and dequant against each other: a swapped factor,
+    a wrong group index or a missing inverse rotation breaks it."""
+    k, v = synth.kv_stream(cfg, 0, 0, 128, D)
+    o = oracle.compress_unit(k, v)
+    kh, vh = oracle.dequant_record(o["record"], D)
+    gv = D // min(D, 128)
+    f = lambda a: a.astype(np.float32).astype(np.float64)  # stored scales are fp32
+    kbound = f(o["k_r"])[:, None] * f(o["k_s"])[None, :] * f(o["k_delta"])[None, :] / 2
+    vd = np.repeat(f(o["v_delta"]).reshape(128, gv), D // gv, axis=1)
+    vbound = f(o["v_r"])[:, None] * f(o["v_s"])[None, :] * vd / 2
+    for x, xh, bnd in ((k, kh, kbound), (v, vh, vbound)):
+        err = np.linalg.norm(xh - x.astype(np.float64), axis=1)
+        assert np.all(err <= np.linalg.norm(bnd, axis=1) * (1 + 1e-5) + 1e-6)
+
+
+def test_fold_identity(oracle):
+    """Issue #180 step 4, scales folded at read time: for a key row of a tile,
+    q . (H K~_t) = r_t (sum_c q'_c s_c delta_c code_tc + sum_c q'_c s_c lo_c)
+    with q' = H q. The explicit dequantisation is on the left."""
+    D = 128
+    k, v = synth.kv_stream(2, 0, 0, 128, D)
+    rec = oracle.compress_unit(k, v)["record"]
+    kh, _ = oracle.dequant_record(rec, D)
+    u = oracle.unpack_record(rec, D)
+    q = np.random.default_rng(0).standard_normal(D)
+    qr = oracle.wht_rows(q[None])[0]
+    folded = u["k_r"] * ((u["k_codes"] * (qr * u["k_s"] * u["k_delta"])[None, :]).sum(1)
+                         + (qr * u["k_s"] * u["k_lo"]).sum())
+    np.testing.assert_allclose(kh @ q, folded, rtol=1e-11, atol=1e-11)
+
+
+def test_compress_invariant_to_global_scale(oracle):
+    """X -> cX (c > 0) leaves every code unchanged and moves only s."""
+    k, v = synth.kv_stream(2, 3, 0, 128, 128)
+    a = oracle.compress_unit(k, v)
+    b = oracle.compress_unit(k * np.float32(4.0), v * np.float32(0.25))
+    ua, ub = oracle.unpack_record(a["record"], 128), oracle.unpack_record(b["record"], 128)
+    np.testing.assert_array_equal(ua["k_codes"], ub["k_codes"])
+    np.testing.assert_array_equal(ua["v_codes"], ub["v_codes"])
+    np.testing.assert_allclose(b["k_s"], 4.0 * a["k_s"], rtol=1e-12)
+    np.testing.assert_allclose(b["v_s"], 0.25 * a["v_s"], rtol=1e-12)
+
+
+def test_zero_tile(oracle):
+    z = np.zeros((128, 128), np.float32)
+    o = oracle.compress_unit(z, z)
+    kh, vh = oracle.dequant_record(o["record"], 128)
+    assert np.all(kh == 0) and np.all(vh == 0)
+    u = oracle.unpack_record(o["record"], 128)
+    assert np.all(u["k_s"] == 1) and np.all(u["v_r"] == 1) and np.all(u["k_delta"] == 0)
+
+
+# ------------------------------------------------------- c6: state machine
+@pytest.mark.parametrize("W", [128, 256])
+def test_rechunking_gives_identical_tiles(oracle, W):
+    """PR #434 commit 99c3773 and issue #433 item 1: tiles do not depend on the
+    chunking. Chunk sizes 1, 17 and 512 over 700 tokens."""
+    Hkv, D, n = 2, 64, 700
+    ks, vs = synth.kv_layer(0, 0, Hkv, n, D)
+    k_tok, v_tok = ks.transpose(1, 0, 2), vs.transpose(1, 0, 2)
+    results = []
+    for chunk in (1, 17, 512):
+        sm = oracle.CacheStateMachine(Hkv, D, W=W)
+        for i0 in range(0, n, chunk):
+            sm.append(k_tok[i0:i0 + chunk], v_tok[i0:i0 + chunk])
+            if chunk == 1:
+                lo = 0 if W == 128 else (128 if sm.n_tokens >= W else 0)
+                assert lo <= sm.win_len < W
+        results.append(sm)
+    for sm in results[1:]:
+        assert sm.n_tiles == results[0].n_tiles == (n - W) // 128 + 1
+        for t in range(sm.n_tiles):
+            for h in range(Hkv):
+                assert np.array_equal(sm.records[t][h], results[0].records[t][h])
+        np.testing.assert_array_equal(sm.window(1)[0], results[0].window(1)[0])
+
+
+# ------------------------------------------------------- c7/c8: attention
+def test_attend_reduces_to_textbook_softmax(oracle):
+    """With no tiles, decode is plain softmax attention (scipy.special.softmax)."""
+    rng = np.random.default_rng(11)
+    q, K, V = rng.standard_normal(64), rng.standard_normal((40, 64)), rng.standard_normal((40, 64))
+    p = scipy.special.softmax(0.125 * (K @ q))
+    np.testing.assert_allclose(oracle.attend(q, K, V, 0.125), p @ V, rtol=1e-12, atol=1e-14)
+
+
+def test_attend_special_cases(oracle):
+    rng = np.random.default_rng(12)
+    K, V = rng.standard_normal((30, 32)), rng.standard_normal((30, 32))
+    np.testing.assert_allclose(oracle.attend(np.zeros(32), K, V, 1.0), V.mean(0), atol=1e-13)
+    np.testing.assert_allclose(oracle.attend(rng.standard_normal(32), K[:1], V[:1], 0.3), V[0],
+                               atol=1e-15)
+    assert np.all(oracle.attend(np.ones(32), K[:0], V[:0], 1.0) == 0.0)
+    q = 1000.0 * K[7] / np.linalg.norm(K[7])
+    np.testing.assert_allclose(oracle.attend(q, K, V, 1.0), V[7], atol=1e-9)
+
+
+def test_decode_independent_of_tile_order(oracle):
+    """Permuting the order of tiles in the table leaves the output unchanged."""
+    D, n_t = 64, 3
+    k, v = synth.kv_stream(0, 0, 0, 128 * n_t + 5, D)
+    pool = np.concatenate([oracle.compress_unit(k[128 * i:128 * i + 128],
+                                                v[128 * i:128 * i + 128])["record"]
+                           for i in range(n_t)])
+    rb = oracle.record_bytes(D)
+    win_k = np.zeros((1, 1, 128, D), np.float32)
+    win_v = np.zeros((1, 1, 128, D), np.float32)
+    win_k[0, 0, :5], win_v[0, 0, :5] = k[-5:], v[-5:]
+    q = synth.queries(0, 0, (1, 1, D))
+    outs = []
+    for perm in ([0, 1, 2], [2, 0, 1]):
+        table = (np.array(perm, np.int64) * rb)[None, None, :]
+        outs.append(oracle.decode_attention(q, pool, table, [n_t], win_k, win_v, [0], [5],
+                                            1 / 8)[(0, 0)])
+    np.testing.assert_allclose(outs[0], outs[1], rtol=1e-12, atol=1e-14)
+
+
+def test_prefill_chunk_of_one_equals_decode(oracle):
+    """c8: causal prefill restricted to a single query is decode (c7) at that
+    step; query i of a chunk sees exactly pos0 + i + 1 tokens."""
+    Hkv, Hq, D, n = 1, 2, 64, 300
+    ks, vs = synth.kv_layer(2, 0, Hkv, n, D)
+    qs = synth.queries(2, 0, (n, Hq, D))
+    sm = oracle.CacheStateMachine(Hkv, D, W=128)
+    rb = oracle.record_bytes(D)
+    full_chunk = None
+    for pos in range(n):
+        sm.append(ks[:, pos:pos + 1].transpose(1, 0, 2), vs[:, pos:pos + 1].transpose(1, 0, 2))
+        if pos in (0, 127, 128, 255, 299):
+            pool = np.concatenate([r[0] for r in sm.records]) if sm.records else np.zeros(rb, np.uint8)
+            table = (np.arange(max(sm.n_tiles, 1), dtype=np.int64) * rb)[None, :]
+            wk, wv = sm.window(0)
+            win_k = np.zeros((1, 256, D), np.float32)
+            win_v = np.zeros((1, 256, D), np.float32)
+            win_k[0, :len(wk)], win_v[0, :len(wv)] = wk, wv
+            dec = oracle.decode_attention(qs[pos][None], pool, table[None], [sm.n_tiles],
+                                          win_k[None], win_v[None], [0], [sm.win_len], 1 / 8)
+            pre = oracle.prefill_attention(qs[pos:pos + 1], pos, pool, table, sm.n_tiles, win_k,
+                                           win_v, 0, sm.win_len, 1 / 8)
+            for h in range(Hq):
+                np.testing.assert_allclose(pre[(0, h)], dec[(0, h)], rtol=1e-13, atol=1e-15)
