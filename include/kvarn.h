@@ -207,7 +207,7 @@ int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new,
  * Results are deterministic: the same inputs give bit-identical outputs.
  */
 int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_tiles,
-                                 size_t* bytes);
+                                 int win_capacity, size_t* bytes);
 int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
                            const int32_t* n_tiles, const float* win_k, const float* win_v,
                            const int32_t* win_start, const int32_t* win_len,

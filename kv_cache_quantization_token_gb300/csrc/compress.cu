@@ -1,0 +1,437 @@
+// compress.cu -- KVarN tile compression on sm_103a.
+//
+// Per (128-token tile, KV head) unit and per tensor (K or V), as the method
+// states it (SharpInference issue #180, "Algorithm (per 128-token tile)",
+// steps 1-3; SharpInference PR #434, commit 82efc4f):
+//   1. Walsh-Hadamard rotation of each token row along head_dim,
+//   2. n rounds of dual-axis std normalisation, channel step first,
+//   3. asymmetric RTN: K 4-bit per channel over the tile's tokens, V 2-bit per
+//      token over 128-channel groups; codes packed into the record.
+//
+// GPU formulation (same result up to rounding as the log-space statement):
+//  - The rotation is computed unnormalised (entries +-1); the 1/sqrt(D) factor
+//    is carried by the channel factor s' = sqrt(D) s, which the normalisation
+//    is invariant to.
+//  - Log-space accumulation telescopes: after a channel step,
+//    alpha_c = ln std_t(Y_tc e^{-beta_t}), and after a token step
+//    beta_t = ln std_c(Y_tc e^{-alpha_c}). So the kernel keeps s' and r
+//    directly and never evaluates log or exp; a skipped step (std not larger
+//    than 2^-20 times the group's RMS) keeps the previous factor, which is
+//    what ln(sigma) := 0 does in log space.
+//  - Each std is a two-pass (mean, M2) per thread followed by Chan pairwise
+//    merges across threads, so large group means do not cancel.
+//
+// Work decomposition: one CTA of 2*D threads per (unit, tensor); every thread
+// holds an 8-token x 8-channel block of the tile in registers (64 floats).
+//   phase 1: each thread loads 16-byte chunks of 512/D tokens straight from
+//            global memory (fully coalesced) and runs the butterflies of the
+//            channel bits it holds (bits 0,1 and 5..log2D-1);
+//   phase 2: a swizzled shared-memory transpose gives the block layout, whose
+//            in-thread channel bits 2..4 take the remaining butterflies.
+// In the block layout token reductions run across lanes with shuffles only,
+// channel reductions across lanes and then across warps through shared memory.
+#include "kvarn_common.cuh"
+
+namespace kvarn {
+namespace {
+
+template <int D>
+struct CC {
+  static constexpr int L = (D == 64) ? 6 : (D == 128) ? 7 : 8;
+  static constexpr int NT = 2 * D;          // threads per CTA
+  static constexpr int NCG = D / 8;         // channel groups (lanes sharing a token group)
+  static constexpr int CG_BITS = L - 3;     // lane bits that index the channel group
+  static constexpr int WARPS = NT / 32;
+  static constexpr int TGW = 5 - CG_BITS;   // token-group bits inside a warp
+  static constexpr int P1_TOK = 512 / D;    // tokens per thread in phase 1
+  static constexpr int P1_K = D / 32;       // 16-byte chunks per token per thread in phase 1
+  static constexpr int TOK_PER_WARP = 8 << TGW;
+  // dynamic shared memory: tile, channel-reduction partials, two channel arrays
+  static constexpr int OFF_RED = 128 * D * 4;
+  static constexpr int OFF_CH = OFF_RED + WARPS * D * 8;
+  static constexpr int SMEM = OFF_CH + 2 * D * 4;
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+};
+
+// 16-byte chunk swizzle of the tile in shared memory: chunk J of token t is
+// stored at J ^ sigma(t, J). It keeps the phase-1 128-byte row segments intact
+// and makes the phase-2 scalar reads hit 32 distinct banks.
+template <int L>
+__device__ __forceinline__ int swz(int t, int J) {
+  return J ^ (((J >> 3) | ((t >> 3) << (L - 5))) & 7);
+}
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+
+// In-register butterflies over the two low bits of a float4.
+__device__ __forceinline__ void fwht4(float4& v) {
+  const float a = v.x + v.y, b = v.x - v.y, c = v.z + v.w, d = v.z - v.w;
+  v.x = a + c; v.y = b + d; v.z = a - c; v.w = b - d;
+}
+__device__ __forceinline__ void bfly(float4& a, float4& b) {
+  const float4 s = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+  b = make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+  a = s;
+}
+
+// Equal-count merge of (mean, M2) summaries; symmetric in its two arguments,
+// so both lanes of a full exchange get bit-identical results.
+__device__ __forceinline__ void merge_eq(float& mean, float& m2, float mb, float m2b, float cnt) {
+  const float d = mb - mean;
+  mean = (mean + mb) * 0.5f;
+  m2 = (m2 + m2b) + d * d * (cnt * 0.5f);
+}
+
+// Halving stage over one lane bit for N (mean, M2) pairs: the lane keeps the
+// lower half of its pairs when its lane bit is 0, the upper half otherwise,
+// and merges in the partner's copy of the half it keeps.
+template <int N>
+__device__ __forceinline__ void halve_mv(float (&mn)[8], float (&m2)[8], int mask, bool upper,
+                                         float cnt) {
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const float sm = upper ? mn[j] : mn[j + N / 2];
+    const float sq = upper ? m2[j] : m2[j + N / 2];
+    const float km = upper ? mn[j + N / 2] : mn[j];
+    const float kq = upper ? m2[j + N / 2] : m2[j];
+    const float rm = shfl_xor(sm, mask), rq = shfl_xor(sq, mask);
+    mn[j] = km; m2[j] = kq;
+    merge_eq(mn[j], m2[j], rm, rq, cnt);
+  }
+}
+template <int N>
+__device__ __forceinline__ void halve_mm(float (&lo)[8], float (&hi)[8], int mask, bool upper) {
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const float sl = upper ? lo[j] : lo[j + N / 2];
+    const float sh = upper ? hi[j] : hi[j + N / 2];
+    const float kl = upper ? lo[j + N / 2] : lo[j];
+    const float kh = upper ? hi[j + N / 2] : hi[j];
+    lo[j] = fminf(kl, shfl_xor(sl, mask));
+    hi[j] = fmaxf(kh, shfl_xor(sh, mask));
+  }
+}
+
+// Usable std: larger than 2^-20 times the RMS of the same group (false for NaN).
+__device__ __forceinline__ bool usable(float var, float mean) {
+  const float sd = sqrtf(var);
+  return sd > ldexpf(sqrtf(var + mean * mean), -20);
+}
+
+template <int D>
+__global__ void __launch_bounds__(CC<D>::NT, (D == 256) ? 1 : 2)
+compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw,
+                int64_t row_stride, const int64_t* __restrict__ src_row0,
+                uint8_t* __restrict__ tiles, const int64_t* __restrict__ dst_record,
+                int iters) {
+  using C = CC<D>;
+  using R = Rec<D>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* xs = reinterpret_cast<float*>(smem);
+  float2* red = reinterpret_cast<float2*>(smem + C::OFF_RED);
+  float* ch_a = reinterpret_cast<float*>(smem + C::OFF_CH);
+  float* ch_b = ch_a + D;
+  unsigned char* stage = smem;  // output staging aliases the tile (used after it is consumed)
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t unit = blockIdx.x >> 1;
+  const bool is_v = blockIdx.x & 1;
+  const float* src = (is_v ? v_raw : k_raw) + src_row0[unit] * row_stride;
+
+  // ---------------- phase 1: coalesced loads + butterflies of bits 0,1,5.. --
+  {
+    const int j0 = tid & 7, trow = tid >> 3;
+    float4 x[C::P1_TOK][C::P1_K];
+#pragma unroll
+    for (int i = 0; i < C::P1_TOK; ++i) {
+      const float4* row = reinterpret_cast<const float4*>(src + (int64_t)(trow + (D / 4) * i) * row_stride);
+#pragma unroll
+      for (int k = 0; k < C::P1_K; ++k) x[i][k] = ld_stream(row + j0 + 8 * k);
+    }
+#pragma unroll
+    for (int i = 0; i < C::P1_TOK; ++i) {
+#pragma unroll
+      for (int k = 0; k < C::P1_K; ++k) fwht4(x[i][k]);
+#pragma unroll
+      for (int h = 1; h < C::P1_K; h <<= 1)
+#pragma unroll
+        for (int k = 0; k < C::P1_K; ++k)
+          if (!(k & h)) bfly(x[i][k], x[i][k | h]);
+      const int t = trow + (D / 4) * i;
+#pragma unroll
+      for (int k = 0; k < C::P1_K; ++k)
+        *reinterpret_cast<float4*>(xs + t * D + 4 * swz<C::L>(t, j0 + 8 * k)) = x[i][k];
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 2: block layout + butterflies of bits 2..4 --------
+  const int cg = tid % C::NCG, tg = tid / C::NCG;
+  float y[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = 8 * tg + i;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int J = ((cg >> 2) << 3) + m;
+      y[i][m] = xs[t * D + 4 * swz<C::L>(t, J) + (cg & 3)];
+    }
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (!(m & h)) {
+          const float a = y[i][m], b = y[i][m | h];
+          y[i][m] = a + b;
+          y[i][m | h] = a - b;
+        }
+  }
+
+  // Sinkhorn state. sinv[m] = 1/s'_c for the thread's channels, rinv[i] = 1/r_t
+  // for its tokens; s_own is owned by the thread pair (2p, 2p+1) of permuted
+  // channel p, r_own by the lanes whose channel-group bits 0..2 encode token i.
+  const float sqrt_d = sqrtf((float)D);
+  float sinv[8], rinv[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) sinv[m] = 1.0f / sqrt_d;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rinv[i] = 1.0f;
+  float s_own = sqrt_d, r_own = 1.0f;
+  const int p_own = tid >> 1, h_own = tid & 1;
+  // token held by this lane after the row halving: bits (cg&1, cg>>1&1, cg>>2&1) -> 4,2,1
+  const int tau = ((cg & 1) << 2) | (((cg >> 1) & 1) << 1) | ((cg >> 2) & 1);
+  auto src_lane = [&](int i) {  // a lane of this token group that owns token i
+    return (lane & ~7) | ((i >> 2) & 1) | (((i >> 1) & 1) << 1) | ((i & 1) << 2);
+  };
+  // channel index of permuted slot p = m * NCG + cg
+  auto chan_of = [&](int p) {
+    const int g = p % C::NCG, m = p / C::NCG;
+    return (g & 3) | (m << 2) | ((g >> 2) << 5);
+  };
+  // which channels m a lane keeps after the in-warp token-group halving
+  const int m_keep0 = (C::TGW == 0) ? 0
+                    : (C::TGW == 1) ? 4 * ((lane >> 4) & 1)
+                                    : 4 * ((lane >> 3) & 1) + 2 * ((lane >> 4) & 1);
+  constexpr int KEEP = 8 >> C::TGW;
+
+  for (int it = 0; it < iters; ++it) {
+    // ---- channel step: std over the 128 tokens of Y' / r ----
+    float cm[8], cq[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(y[i][m], rinv[i], s);
+      const float mean = s * 0.125f;
+      float q = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { const float d = fmaf(y[i][m], rinv[i], -mean); q = fmaf(d, d, q); }
+      cm[m] = mean; cq[m] = q;
+    }
+    if (C::TGW >= 1) halve_mv<8>(cm, cq, 1 << C::CG_BITS, (lane >> C::CG_BITS) & 1, 8.f);
+    if (C::TGW >= 2) halve_mv<4>(cm, cq, 1 << (C::CG_BITS + 1), (lane >> (C::CG_BITS + 1)) & 1, 16.f);
+#pragma unroll
+    for (int j = 0; j < KEEP; ++j)
+      red[warp * D + (m_keep0 + j) * C::NCG + cg] = make_float2(cm[j], cq[j]);
+    __syncthreads();
+    {
+      constexpr int HW = C::WARPS / 2;
+      const float n1 = (float)C::TOK_PER_WARP;
+      float2 a = red[(h_own * HW) * D + p_own];
+      float mean = a.x, m2 = a.y, n = n1;
+#pragma unroll
+      for (int w = 1; w < HW; ++w) {
+        const float2 b = red[(h_own * HW + w) * D + p_own];
+        chan_merge(mean, m2, n, b.x, b.y, n1);
+        n += n1;
+      }
+      merge_eq(mean, m2, shfl_xor(mean, 1), shfl_xor(m2, 1), 64.f);
+      const float var = m2 * (1.0f / 128.0f);
+      if (usable(var, mean)) s_own = sqrtf(var);
+      if (h_own == 0) ch_a[p_own] = 1.0f / s_own;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) sinv[m] = ch_a[m * C::NCG + cg];
+
+    // ---- token step: std over the D channels of Y' / s' ----
+    float rm[8], rq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) s = fmaf(y[i][m], sinv[m], s);
+      const float mean = s * 0.125f;
+      float q = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) { const float d = fmaf(y[i][m], sinv[m], -mean); q = fmaf(d, d, q); }
+      rm[i] = mean; rq[i] = q;
+    }
+    halve_mv<8>(rm, rq, 1, lane & 1, 8.f);
+    halve_mv<4>(rm, rq, 2, (lane >> 1) & 1, 16.f);
+    halve_mv<2>(rm, rq, 4, (lane >> 2) & 1, 32.f);
+    if (C::CG_BITS >= 4) merge_eq(rm[0], rq[0], shfl_xor(rm[0], 8), shfl_xor(rq[0], 8), 64.f);
+    if (C::CG_BITS >= 5) merge_eq(rm[0], rq[0], shfl_xor(rm[0], 16), shfl_xor(rq[0], 16), 128.f);
+    {
+      const float var = rq[0] * (1.0f / (float)D);
+      if (usable(var, rm[0])) r_own = sqrtf(var);
+      const float ri = 1.0f / r_own;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rinv[i] = __shfl_sync(0xffffffffu, ri, src_lane(i));
+    }
+  }
+
+  // ---------------- normalised values -------------------------------------
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int m = 0; m < 8; ++m) y[i][m] = (y[i][m] * sinv[m]) * rinv[i];
+
+  const int t_own = 8 * tg + tau;
+  const bool tok_writer = (C::CG_BITS == 3) || ((cg >> 3) & 1) == 0;
+
+  if (!is_v) {
+    // ---------------- K: 4-bit RTN per channel over the 128 tokens ----------
+    float lo[8], hi[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      lo[m] = y[0][m]; hi[m] = y[0][m];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) { lo[m] = fminf(lo[m], y[i][m]); hi[m] = fmaxf(hi[m], y[i][m]); }
+    }
+    if (C::TGW >= 1) halve_mm<8>(lo, hi, 1 << C::CG_BITS, (lane >> C::CG_BITS) & 1);
+    if (C::TGW >= 2) halve_mm<4>(lo, hi, 1 << (C::CG_BITS + 1), (lane >> (C::CG_BITS + 1)) & 1);
+#pragma unroll
+    for (int j = 0; j < KEEP; ++j) red[warp * D + (m_keep0 + j) * C::NCG + cg] = make_float2(lo[j], hi[j]);
+    __syncthreads();  // also: every thread is past its last read of the tile
+    {
+      constexpr int HW = C::WARPS / 2;
+      float2 a = red[(h_own * HW) * D + p_own];
+      float l = a.x, h = a.y;
+#pragma unroll
+      for (int w = 1; w < HW; ++w) {
+        const float2 b = red[(h_own * HW + w) * D + p_own];
+        l = fminf(l, b.x); h = fmaxf(h, b.y);
+      }
+      l = fminf(l, shfl_xor(l, 1));
+      h = fmaxf(h, shfl_xor(h, 1));
+      const float delta = (h - l) / 15.0f;
+      const float inv = delta > 0.f ? 1.0f / delta : 0.f;
+      if (h_own == 0) {
+        ch_a[p_own] = l;
+        ch_b[p_own] = inv;
+        const int c = chan_of(p_own);
+        reinterpret_cast<float*>(stage + R::kKDelta)[c] = delta;
+        reinterpret_cast<float*>(stage + R::kKLo)[c] = l;
+        reinterpret_cast<float*>(stage + R::kKS)[c] = s_own / sqrt_d;
+      }
+    }
+    if (tok_writer) reinterpret_cast<float*>(stage + R::kKR)[t_own] = r_own;
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float l = ch_a[m * C::NCG + cg], inv = ch_b[m * C::NCG + cg];
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int code = __float2int_rd((y[i][m] - l) * inv + 0.5f);
+        code = min(15, max(0, code));
+        w |= (uint32_t)code << (4 * i);
+      }
+      const int c = (cg & 3) | (m << 2) | ((cg >> 2) << 5);
+      *reinterpret_cast<uint32_t*>(stage + R::kKCodes + c * (kTile / 2) + 4 * tg) = w;
+    }
+  } else {
+    // ---------------- V: 2-bit RTN per token over 128-channel groups ---------
+    float lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lo[i] = y[i][0]; hi[i] = y[i][0];
+#pragma unroll
+      for (int m = 1; m < 8; ++m) { lo[i] = fminf(lo[i], y[i][m]); hi[i] = fmaxf(hi[i], y[i][m]); }
+    }
+    halve_mm<8>(lo, hi, 1, lane & 1);
+    halve_mm<4>(lo, hi, 2, (lane >> 1) & 1);
+    halve_mm<2>(lo, hi, 4, (lane >> 2) & 1);
+    if (C::CG_BITS >= 4) {  // channel bit 5 (lane bit 3) stays inside one 128-channel group
+      lo[0] = fminf(lo[0], shfl_xor(lo[0], 8));
+      hi[0] = fmaxf(hi[0], shfl_xor(hi[0], 8));
+    }
+    const float delta = (hi[0] - lo[0]) / 3.0f;
+    const float inv = delta > 0.f ? 1.0f / delta : 0.f;
+    const int g = (D == 256) ? ((cg >> 4) & 1) : 0;
+    __syncthreads();  // every thread is past its last read of the tile
+    if (tok_writer) {
+      reinterpret_cast<float*>(stage + R::kVDelta)[t_own * R::kGv + g] = delta;
+      reinterpret_cast<float*>(stage + R::kVLo)[t_own * R::kGv + g] = lo[0];
+      if (g == 0) reinterpret_cast<float*>(stage + R::kVR)[t_own] = r_own;
+    }
+    if (h_own == 0) reinterpret_cast<float*>(stage + R::kVS)[chan_of(p_own)] = s_own / sqrt_d;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float l = __shfl_sync(0xffffffffu, lo[0], src_lane(i));
+      const float iv = __shfl_sync(0xffffffffu, inv, src_lane(i));
+      unsigned long long w = 0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        int code = __float2int_rd((y[i][m] - l) * iv + 0.5f);
+        code = min(3, max(0, code));
+        w |= (unsigned long long)code << (8 * m + 2 * (cg & 3));
+      }
+      w |= __shfl_xor_sync(0xffffffffu, w, 1);
+      w |= __shfl_xor_sync(0xffffffffu, w, 2);
+      if ((i & 3) == (cg & 3)) {
+        const int t = 8 * tg + i;
+        *reinterpret_cast<unsigned long long*>(stage + R::kVCodes + t * (D / 4) + 8 * (cg >> 2)) = w;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---------------- copy the staged halves of the record out --------------
+  uint8_t* rec = tiles + dst_record[unit];
+  const int a0 = is_v ? R::kVCodes : R::kKCodes;
+  const int a1 = is_v ? R::kKDelta : R::kVCodes;
+  const int b0 = is_v ? R::kVDelta : R::kKDelta;
+  const int b1 = is_v ? R::kBytes : R::kVDelta;
+  for (int o = a0 + 16 * tid; o < a1; o += 16 * C::NT)
+    __stcs(reinterpret_cast<uint4*>(rec + o), *reinterpret_cast<const uint4*>(stage + o));
+  for (int o = b0 + 16 * tid; o < b1; o += 16 * C::NT)
+    __stcs(reinterpret_cast<uint4*>(rec + o), *reinterpret_cast<const uint4*>(stage + o));
+}
+
+template <int D>
+cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw, int64_t row_stride,
+                              const int64_t* src_row0, uint8_t* tiles, const int64_t* dst_record,
+                              int64_t n_units, cudaStream_t st) {
+  using C = CC<D>;
+  static bool configured[64] = {};  // the smem opt-in is set once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const int64_t blocks = 2 * n_units;
+  compress_kernel<D><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(k_raw, v_raw, row_stride, src_row0,
+                                                               tiles, dst_record, iters);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compress(int D, int iters, const float* k_raw, const float* v_raw,
+                            int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
+                            const int64_t* dst_record, int64_t n_units, cudaStream_t st) {
+  switch (D) {
+    case 64: return launch_compress_d<64>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 128: return launch_compress_d<128>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 256: return launch_compress_d<256>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvarn

@@ -1,0 +1,172 @@
+// kvarn_abi.cu -- the extern "C" entry points of libkvarn.so.
+//
+// Each entry point validates its arguments on the host, returns a
+// kvarn_status_t without enqueuing anything when they are wrong, and otherwise
+// launches the kernels of compress.cu, window.cu or decode.cu on the stream.
+#include <stdint.h>
+#include <string.h>
+
+#include "kvarn_common.cuh"
+
+namespace {
+
+bool supported_dim(int D) { return D == 64 || D == 128 || D == 256; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA; }
+
+int fill_layout(int D, int iters, kvarn_layout_t* L) {
+  memset(L, 0, sizeof(*L));
+  L->version = KVARN_LAYOUT_VERSION;
+  L->head_dim = D;
+  L->tile_tokens = KVARN_TILE_TOKENS;
+  L->sinkhorn_iters = iters;
+  L->k_bits = KVARN_K_BITS;
+  L->v_bits = KVARN_V_BITS;
+  L->v_group = D < 128 ? D : 128;
+  L->v_groups = D / L->v_group;
+  const int64_t T = KVARN_TILE_TOKENS, gv = L->v_groups;
+  L->off_k_codes = 0;
+  L->off_v_codes = L->off_k_codes + (int64_t)D * (T / 2);
+  L->off_k_delta = L->off_v_codes + T * (D / 4);
+  L->off_k_lo = L->off_k_delta + 4LL * D;
+  L->off_k_s = L->off_k_lo + 4LL * D;
+  L->off_k_r = L->off_k_s + 4LL * D;
+  L->off_v_delta = L->off_k_r + 4 * T;
+  L->off_v_lo = L->off_v_delta + 4 * T * gv;
+  L->off_v_r = L->off_v_lo + 4 * T * gv;
+  L->off_v_s = L->off_v_r + 4 * T;
+  L->record_bytes = L->off_v_s + 4LL * D;
+  return KVARN_OK;
+}
+
+// A layout handed back by the caller must be one this library produced.
+bool layout_ok(const kvarn_layout_t* L) {
+  if (!L || L->version != KVARN_LAYOUT_VERSION || !supported_dim(L->head_dim)) return false;
+  if (L->sinkhorn_iters < 1 || L->sinkhorn_iters > 16) return false;
+  kvarn_layout_t ref;
+  fill_layout(L->head_dim, L->sinkhorn_iters, &ref);
+  return memcmp(&ref, L, sizeof(ref)) == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out) {
+  if (!out) return KVARN_ERR_NULL;
+  if (!supported_dim(head_dim) || sinkhorn_iters < 1 || sinkhorn_iters > 16)
+    return KVARN_ERR_UNSUPPORTED;
+  return fill_layout(head_dim, sinkhorn_iters, out);
+}
+
+const char* kvarn_status_string(int status) {
+  switch (status) {
+    case KVARN_OK: return "ok";
+    case KVARN_ERR_NULL: return "a required pointer is NULL";
+    case KVARN_ERR_ALIGN: return "a pointer, stride or offset is not 16-byte aligned";
+    case KVARN_ERR_UNSUPPORTED: return "unsupported head_dim, GQA group or iteration count";
+    case KVARN_ERR_BAD_ARG: return "a size or count is negative or inconsistent";
+    case KVARN_ERR_WORKSPACE: return "workspace smaller than the _workspace_bytes query";
+    case KVARN_ERR_CUDA: return "the CUDA runtime rejected a launch";
+    default: return "unknown kvarn status";
+  }
+}
+
+int kvarn_rotate_query(const float* q, float* q_rot, int64_t n_rows, int head_dim,
+                       kvarn_stream_t stream) {
+  if (!supported_dim(head_dim)) return KVARN_ERR_UNSUPPORTED;
+  if (n_rows < 0 || n_rows > (int64_t)8 * 0x7fffffff) return KVARN_ERR_BAD_ARG;
+  if (n_rows == 0) return KVARN_OK;
+  if (!q || !q_rot) return KVARN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(q_rot)) return KVARN_ERR_ALIGN;
+  if (q != q_rot) {  // only exact in-place use may overlap
+    const char *a = reinterpret_cast<const char*>(q), *b = reinterpret_cast<const char*>(q_rot);
+    const int64_t bytes = n_rows * head_dim * 4;
+    if (a < b + bytes && b < a + bytes) return KVARN_ERR_BAD_ARG;
+  }
+  return from_cuda(kvarn::launch_rotate(q, q_rot, n_rows, head_dim, (cudaStream_t)stream));
+}
+
+int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stride,
+                        int64_t n_rows, const int64_t* src_row0, uint8_t* tiles,
+                        const int64_t* dst_record, int64_t n_units, const kvarn_layout_t* layout,
+                        kvarn_stream_t stream) {
+  if (!layout) return KVARN_ERR_NULL;
+  if (!layout_ok(layout)) return KVARN_ERR_UNSUPPORTED;
+  const int D = layout->head_dim;
+  if (n_units < 0 || n_units > 0x3fffffff || n_rows < 0) return KVARN_ERR_BAD_ARG;
+  if (n_units == 0) return KVARN_OK;
+  if (!k_raw || !v_raw || !src_row0 || !tiles || !dst_record) return KVARN_ERR_NULL;
+  if (row_stride < D || n_rows < KVARN_TILE_TOKENS) return KVARN_ERR_BAD_ARG;
+  if ((row_stride & 3) || !aligned16(k_raw) || !aligned16(v_raw) || !aligned16(tiles))
+    return KVARN_ERR_ALIGN;
+  return from_cuda(kvarn::launch_compress(D, layout->sinkhorn_iters, k_raw, v_raw, row_stride,
+                                          src_row0, tiles, dst_record, n_units,
+                                          (cudaStream_t)stream));
+}
+
+int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
+                        float* win_v, int win_capacity, const int32_t* win_start,
+                        const int32_t* win_len, int n_seq, int n_kv_heads, int head_dim,
+                        kvarn_stream_t stream) {
+  if (!supported_dim(head_dim)) return KVARN_ERR_UNSUPPORTED;
+  if (n_new < 0 || n_seq < 0 || n_kv_heads <= 0 || win_capacity <= 0) return KVARN_ERR_BAD_ARG;
+  if (n_new > win_capacity) return KVARN_ERR_BAD_ARG;
+  if (n_new == 0 || n_seq == 0) return KVARN_OK;
+  if (!k_new || !v_new || !win_k || !win_v || !win_start || !win_len) return KVARN_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(win_k) || !aligned16(win_v))
+    return KVARN_ERR_ALIGN;
+  return from_cuda(kvarn::launch_append(k_new, v_new, n_new, win_k, win_v, win_capacity,
+                                        win_start, win_len, n_seq, n_kv_heads, head_dim,
+                                        (cudaStream_t)stream));
+}
+
+static int decode_check(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity) {
+  if (!supported_dim(D)) return KVARN_ERR_UNSUPPORTED;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_tiles < 0 || win_capacity < 0) return KVARN_ERR_BAD_ARG;
+  if (Hq % Hkv) return KVARN_ERR_BAD_ARG;
+  if (Hq / Hkv > 8) return KVARN_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535) return KVARN_ERR_BAD_ARG;
+  return KVARN_OK;
+}
+
+int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                                 int win_capacity, size_t* bytes) {
+  if (!bytes) return KVARN_ERR_NULL;
+  const int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
+  if (rc != KVARN_OK) return rc;
+  kvarn::DecodePlan p;
+  kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &p);
+  *bytes = p.ws_bytes;
+  return KVARN_OK;
+}
+
+int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
+                           const int32_t* n_tiles, const float* win_k, const float* win_v,
+                           const int32_t* win_start, const int32_t* win_len, int win_capacity,
+                           int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                           float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                           size_t ws_bytes, float* out, kvarn_stream_t stream) {
+  int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
+  if (rc != KVARN_OK) return rc;
+  if (!layout) return KVARN_ERR_NULL;
+  if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
+  if (B == 0) return KVARN_OK;
+  kvarn::DecodePlan p;
+  kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &p);
+  if (!q || !out || !n_tiles) return KVARN_ERR_NULL;
+  if (max_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
+  if (win_capacity > 0 && (!win_k || !win_v || !win_start || !win_len)) return KVARN_ERR_NULL;
+  if (p.ws_bytes > 0 && !ws) return KVARN_ERR_NULL;
+  if (ws_bytes < p.ws_bytes) return KVARN_ERR_WORKSPACE;
+  if (!aligned16(q) || !aligned16(out) || (max_tiles > 0 && !aligned16(tiles)) ||
+      (win_capacity > 0 && (!aligned16(win_k) || !aligned16(win_v))) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
+    return KVARN_ERR_ALIGN;
+  if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
+  return from_cuda(kvarn::launch_decode(p, q, tiles, tile_table, n_tiles, win_k, win_v,
+                                        win_start, win_len, win_capacity, B, Hq, Hkv, head_dim,
+                                        max_tiles, softmax_scale, ws, out, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// window.cu -- query rotation and FP32 staging-window append.
+//
+// Query rotation: q' = H q per query head, H the orthonormal Sylvester
+// Walsh-Hadamard matrix (SharpInference PR #434, commit 0d7cd28,
+// llm_kvarn_rotate_query; issue #180, "Algorithm (per 128-token tile)" step 1).
+// Window append: raw K/V rows go into the per-sequence FP32 ring that stages
+// tokens until a whole 128-token tile is promoted (PR #434, commit 6040076).
+#include "kvarn_common.cuh"
+
+namespace kvarn {
+namespace {
+
+// One warp per row; lane l holds elements l*E .. l*E+E-1 (E = D/32). The
+// butterflies of the low log2(E) bits run in registers, the other five across
+// lanes with shuffles; the result is scaled by 1/sqrt(D).
+template <int D>
+__global__ void __launch_bounds__(256) rotate_kernel(const float* q, float* q_rot, int64_t n_rows) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  float x[E];
+  const float* src = q + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] = src[e];
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (!(e & h)) {
+        const float a = x[e], b = x[e | h];
+        x[e] = a + b;
+        x[e | h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = lane & m;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = upper ? (o - x[e]) : (x[e] + o);
+    }
+  }
+  const float sc = 1.0f / sqrtf((float)D);
+  float* dst = q_rot + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[e] = x[e] * sc;
+}
+
+__global__ void append_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v_new,
+                              int64_t n_new, float4* __restrict__ win_k, float4* __restrict__ win_v,
+                              int cap, const int32_t* __restrict__ win_start,
+                              const int32_t* __restrict__ win_len, int n_seq, int hkv, int d4) {
+  const int64_t total = (int64_t)n_seq * n_new * hkv * d4;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int c4 = (int)(idx % d4);
+    int64_t r = idx / d4;
+    const int h = (int)(r % hkv);
+    r /= hkv;
+    const int64_t i = r % n_new;
+    const int s = (int)(r / n_new);
+    int64_t slot = ((int64_t)win_start[s] + win_len[s] + i) % cap;
+    if (slot < 0) slot += cap;
+    const int64_t dst = (((int64_t)s * hkv + h) * cap + slot) * d4 + c4;
+    win_k[dst] = k_new[idx];
+    win_v[dst] = v_new[idx];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, cudaStream_t st) {
+  const unsigned blocks = (unsigned)((n_rows + 7) / 8);
+  switch (D) {
+    case 64: rotate_kernel<64><<<blocks, 256, 0, st>>>(q, q_rot, n_rows); break;
+    case 128: rotate_kernel<128><<<blocks, 256, 0, st>>>(q, q_rot, n_rows); break;
+    case 256: rotate_kernel<256><<<blocks, 256, 0, st>>>(q, q_rot, n_rows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
+                          float* win_v, int win_capacity, const int32_t* win_start,
+                          const int32_t* win_len, int n_seq, int n_kv_heads, int D,
+                          cudaStream_t st) {
+  const int64_t total = (int64_t)n_seq * n_new * n_kv_heads * (D / 4);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      reinterpret_cast<const float4*>(k_new), reinterpret_cast<const float4*>(v_new), n_new,
+      reinterpret_cast<float4*>(win_k), reinterpret_cast<float4*>(win_v), win_capacity, win_start,
+      win_len, n_seq, n_kv_heads, D / 4);
+  return cudaGetLastError();
+}
+
+}  // namespace kvarn

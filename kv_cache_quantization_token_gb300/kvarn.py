@@ -1,0 +1,188 @@
+"""Thin ctypes binding of libkvarn.so (include/kvarn.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. There is no
+fallback: if the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import _build
+
+TILE = 128
+DEFAULT_ITERS = 4
+
+_lib = None
+
+
+class KvarnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _L().kvarn_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+class Layout(ctypes.Structure):
+    """Mirror of kvarn_layout_t."""
+    _fields_ = [("version", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("tile_tokens", ctypes.c_int32), ("sinkhorn_iters", ctypes.c_int32),
+                ("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32),
+                ("v_group", ctypes.c_int32), ("v_groups", ctypes.c_int32),
+                ("record_bytes", ctypes.c_int64),
+                ("off_k_codes", ctypes.c_int64), ("off_v_codes", ctypes.c_int64),
+                ("off_k_delta", ctypes.c_int64), ("off_k_lo", ctypes.c_int64),
+                ("off_k_s", ctypes.c_int64), ("off_k_r", ctypes.c_int64),
+                ("off_v_delta", ctypes.c_int64), ("off_v_lo", ctypes.c_int64),
+                ("off_v_r", ctypes.c_int64), ("off_v_s", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkvarn.so is not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, i64, c_int, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.kvarn_status_string.restype = ctypes.c_char_p
+        lib.kvarn_status_string.argtypes = [c_int]
+        lib.kvarn_layout.argtypes = [c_int, c_int, ctypes.POINTER(Layout)]
+        lib.kvarn_rotate_query.argtypes = [vp, vp, i64, c_int, vp]
+        lib.kvarn_compress_tile.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, ctypes.POINTER(Layout), vp]
+        lib.kvarn_append_window.argtypes = [vp, vp, i64, vp, vp, c_int, vp, vp, c_int, c_int, c_int, vp]
+        lib.kvarn_decode_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int,
+                                                     ctypes.POINTER(sz)]
+        lib.kvarn_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
+                                               c_int, c_int, c_int, ctypes.c_float,
+                                               ctypes.POINTER(Layout), vp, sz, vp, vp]
+        for name in ("kvarn_layout", "kvarn_rotate_query", "kvarn_compress_tile",
+                     "kvarn_append_window", "kvarn_decode_workspace_bytes",
+                     "kvarn_decode_attention"):
+            getattr(lib, name).restype = c_int
+        _lib = lib
+    return _lib
+
+
+def declared_functions(header: str) -> list:
+    """Names of the functions include/kvarn.h declares."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(kvarn_\w+)\s*\(", text, flags=re.M)))
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise KvarnError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def layout(head_dim: int, iters: int = DEFAULT_ITERS) -> Layout:
+    L = Layout()
+    _check("kvarn_layout", _L().kvarn_layout(head_dim, iters, ctypes.byref(L)))
+    return L
+
+
+def rotate_query(q: torch.Tensor, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """H q for every row (last axis = head_dim)."""
+    _dev(q, "q", torch.float32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.float32)
+    D = q.shape[-1]
+    _check("kvarn_rotate_query",
+           _L().kvarn_rotate_query(_ptr(q), _ptr(out), q.numel() // D, D, _stream(stream)))
+    return out
+
+
+def compress_tile(k_raw, v_raw, src_row0, tiles, dst_record, lay: Layout, stream=None):
+    """k_raw, v_raw: fp32 [n_rows][row_stride] (2-D view of any row-major
+    buffer); src_row0, dst_record: int64 [n_units] on the device."""
+    for n, t in (("k_raw", k_raw), ("v_raw", v_raw)):
+        _dev(t, n, torch.float32)
+    _dev(src_row0, "src_row0", torch.int64)
+    _dev(dst_record, "dst_record", torch.int64)
+    _dev(tiles, "tiles", torch.uint8)
+    if k_raw.shape != v_raw.shape:
+        raise ValueError("k_raw and v_raw must have the same shape")
+    row_stride = k_raw.shape[-1]
+    n_rows = k_raw.numel() // row_stride
+    _check("kvarn_compress_tile",
+           _L().kvarn_compress_tile(_ptr(k_raw), _ptr(v_raw), row_stride, n_rows, _ptr(src_row0),
+                                    _ptr(tiles), _ptr(dst_record), src_row0.numel(),
+                                    ctypes.byref(lay), _stream(stream)))
+
+
+def append_window(k_new, v_new, win_k, win_v, win_start, win_len, stream=None):
+    """k_new, v_new: fp32 [n_seq][n_new][Hkv][D]; win_k, win_v: fp32
+    [n_seq][Hkv][cap][D]; win_start, win_len: int32 [n_seq]."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("win_k", win_k), ("win_v", win_v)):
+        _dev(t, n, torch.float32)
+    _dev(win_start, "win_start", torch.int32)
+    _dev(win_len, "win_len", torch.int32)
+    n_seq, n_new, hkv, D = k_new.shape
+    cap = win_k.shape[2]
+    _check("kvarn_append_window",
+           _L().kvarn_append_window(_ptr(k_new), _ptr(v_new), n_new, _ptr(win_k), _ptr(win_v), cap,
+                                    _ptr(win_start), _ptr(win_len), n_seq, hkv, D, _stream(stream)))
+
+
+def decode_workspace_bytes(B, Hq, Hkv, head_dim, max_tiles, win_capacity) -> int:
+    n = ctypes.c_size_t()
+    _check("kvarn_decode_workspace_bytes",
+           _L().kvarn_decode_workspace_bytes(B, Hq, Hkv, head_dim, max_tiles, win_capacity,
+                                             ctypes.byref(n)))
+    return n.value
+
+
+def decode_attention(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
+                     lay: Layout, softmax_scale=None, ws=None, out=None, stream=None):
+    """q fp32 [B][Hq][D]; tile_table int64 [B][Hkv][max_tiles]; n_tiles int32
+    [B]; win_k/v fp32 [B][Hkv][cap][D]; win_start/len int32 [B]."""
+    _dev(q, "q", torch.float32)
+    B, Hq, D = q.shape
+    _dev(tile_table, "tile_table", torch.int64)
+    Hkv, max_tiles = tile_table.shape[1], tile_table.shape[2]
+    cap = win_k.shape[2]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    need = decode_workspace_bytes(B, Hq, Hkv, D, max_tiles, cap)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("kvarn_decode_attention",
+           _L().kvarn_decode_attention(_ptr(q), _ptr(tiles), _ptr(tile_table), _ptr(n_tiles),
+                                       _ptr(win_k), _ptr(win_v), _ptr(win_start), _ptr(win_len),
+                                       cap, B, Hq, Hkv, D, max_tiles, float(softmax_scale),
+                                       ctypes.byref(lay), _ptr(ws), ws.numel(), _ptr(out),
+                                       _stream(stream)))
+    return out

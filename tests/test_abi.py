@@ -1,0 +1,80 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function
+include/kvarn.h declares, and rejects bad arguments on the host before any
+launch (no GPU needed: validation precedes every CUDA call)."""
+import ctypes
+import os
+
+import pytest
+
+import oracle
+from kv_cache_quantization_token_gb300 import _build, kvarn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvarn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kvarn._L()
+
+
+def test_library_exports_every_declared_function(lib):
+    names = kvarn.declared_functions(HEADER)
+    assert {"kvarn_layout", "kvarn_compress_tile", "kvarn_decode_attention",
+            "kvarn_rotate_query", "kvarn_append_window"} <= set(names)
+    raw = ctypes.CDLL(_build.LIB)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in kvarn.h but not exported"
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_layout_agrees_with_oracle_record_size(lib, D):
+    L = kvarn.layout(D)
+    assert L.record_bytes == oracle.record_bytes(D)
+    assert L.version == 1 and L.tile_tokens == 128 and L.sinkhorn_iters == 4
+    assert (L.k_bits, L.v_bits, L.v_group) == (4, 2, min(D, 128))
+    offs = [L.off_k_codes, L.off_v_codes, L.off_k_delta, L.off_k_lo, L.off_k_s, L.off_k_r,
+            L.off_v_delta, L.off_v_lo, L.off_v_r, L.off_v_s]
+    assert offs == sorted(offs) and all(o % 16 == 0 for o in offs)
+    assert L.off_v_codes == 64 * D and L.off_k_delta == 96 * D
+
+
+def test_layout_rejects_unsupported(lib):
+    L = kvarn.Layout()
+    for D, it in ((96, 4), (32, 4), (512, 4), (128, 0), (128, 17)):
+        assert lib.kvarn_layout(D, it, ctypes.byref(L)) == -3
+    assert lib.kvarn_layout(128, 4, None) == -1
+
+
+def test_status_strings(lib):
+    for s in range(-7, 1):
+        assert lib.kvarn_status_string(s)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    L = kvarn.layout(128)
+    p = ctypes.c_void_p(16)
+    bad = ctypes.c_void_p(8)
+    # compress: null, misaligned, bad stride
+    assert lib.kvarn_compress_tile(None, p, 128, 256, p, p, p, 1, ctypes.byref(L), None) == -1
+    assert lib.kvarn_compress_tile(bad, p, 128, 256, p, p, p, 1, ctypes.byref(L), None) == -2
+    assert lib.kvarn_compress_tile(p, p, 130, 256, p, p, p, 1, ctypes.byref(L), None) == -2
+    assert lib.kvarn_compress_tile(p, p, 64, 256, p, p, p, 1, ctypes.byref(L), None) == -4
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, p, 0, ctypes.byref(L), None) == 0
+    tampered = kvarn.layout(128)
+    tampered.record_bytes += 16
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, p, 1, ctypes.byref(tampered), None) == -3
+    # rotate: unsupported dim, overlap
+    assert lib.kvarn_rotate_query(p, p, 4, 96, None) == -3
+    assert lib.kvarn_rotate_query(ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 256), 4, 128, None) == -4
+    # append: too many new tokens for the ring
+    assert lib.kvarn_append_window(p, p, 300, p, p, 256, p, p, 1, 8, 128, None) == -4
+    # decode: GQA group too large, non-divisible heads, workspace too small
+    n = ctypes.c_size_t()
+    assert lib.kvarn_decode_workspace_bytes(1, 32, 2, 128, 8, 128, ctypes.byref(n)) == -3
+    assert lib.kvarn_decode_workspace_bytes(1, 30, 8, 128, 8, 128, ctypes.byref(n)) == -4
+    assert lib.kvarn_decode_workspace_bytes(1, 32, 8, 128, 8, 128, ctypes.byref(n)) == 0
+    assert n.value > 0
+    args = [p] * 8 + [128, 1, 32, 8, 128, 8, ctypes.c_float(0.088), ctypes.byref(L), p, 16, p, None]
+    assert lib.kvarn_decode_attention(*args) == -5

@@ -1,0 +1,99 @@
+"""GPU tile compression vs the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_quantization_token_gb300 import kvarn, synth
+from tests.kvarn_helpers import compare_record
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _compress(k_rows, v_rows, units, D, iters=4, row_stride=None):
+    """k_rows/v_rows: fp32 [n][D]; units: list of first rows. Returns records."""
+    lay = kvarn.layout(D, iters)
+    rb = lay.record_bytes
+    n = k_rows.shape[0]
+    if row_stride is not None and row_stride != D:
+        kp = np.zeros((n, row_stride), np.float32)
+        vp = np.zeros((n, row_stride), np.float32)
+        kp[:, :D], vp[:, :D] = k_rows, v_rows
+        kp[:, D:], vp[:, D:] = 1e30, -1e30  # padding must never be read
+        k_rows, v_rows = kp, vp
+    tiles = torch.full((len(units) * rb,), 0xAB, dtype=torch.uint8, device=DEV)
+    # records go to a permuted order of slots: placement must not matter
+    slots = np.random.default_rng(len(units)).permutation(len(units))
+    kvarn.compress_tile(torch.from_numpy(k_rows).to(DEV), torch.from_numpy(v_rows).to(DEV),
+                        torch.tensor(units, dtype=torch.int64, device=DEV), tiles,
+                        torch.tensor(slots * rb, dtype=torch.int64, device=DEV), lay)
+    host = tiles.cpu().numpy()
+    return [host[s * rb:(s + 1) * rb] for s in slots]
+
+
+@pytest.mark.parametrize("cfg,D,n_heads,n_tiles", [(0, 128, 1, 1), (1, 128, 2, 4), (2, 128, 2, 4),
+                                                    (4, 256, 2, 3), (2, 64, 2, 3), (0, 64, 1, 2),
+                                                    (4, 128, 1, 2)])
+def test_compress_matches_oracle(cfg, D, n_heads, n_tiles):
+    ks, vs = synth.kv_layer(cfg, 3, n_heads, 128 * n_tiles, D)
+    k_rows, v_rows = ks.reshape(-1, D), vs.reshape(-1, D)
+    units = [128 * i for i in range(n_heads * n_tiles)]
+    recs = _compress(k_rows, v_rows, units, D)
+    flips = total = 0
+    for u, rec in zip(units, recs):
+        ref = oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128])
+        st = compare_record(rec, ref, D)
+        flips += st["band_flips"]
+        total += st["codes"]
+    print(f"cfg{cfg} D{D}: {flips} boundary-band flips of {total} codes")
+
+
+def test_compress_strided_rows_and_offsets():
+    D = 128
+    ks, vs = synth.kv_layer(2, 5, 1, 128 * 3 + 40, D)
+    k_rows, v_rows = ks[0], vs[0]
+    units = [0, 40, 128 + 40, 256]  # overlapping and unaligned-to-128 starts
+    recs = _compress(k_rows, v_rows, units, D, row_stride=D + 8)
+    for u, rec in zip(units, recs):
+        compare_record(rec, oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128]), D)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 7])
+def test_compress_other_iteration_counts(iters):
+    D = 128
+    ks, vs = synth.kv_layer(0, 2, 1, 256, D)
+    recs = _compress(ks[0], vs[0], [0, 128], D, iters=iters)
+    for u, rec in zip([0, 128], recs):
+        compare_record(rec, oracle.compress_unit(ks[0, u:u + 128], vs[0, u:u + 128], iters), D)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_compress_degenerate_tiles(D):
+    """All-zero tile; a tile of identical tokens (every channel constant); a
+    tile with zero tokens and a zero channel."""
+    rng = np.random.default_rng(D)
+    zero = np.zeros((128, D), np.float32)
+    same = np.tile(rng.standard_normal(D).astype(np.float32), (128, 1))
+    holes = rng.standard_normal((128, D)).astype(np.float32)
+    holes[::7] = 0.0
+    holes[:, 3] = 0.0
+    k_rows = np.concatenate([zero, same, holes])
+    v_rows = np.concatenate([zero, same[::-1] * 2, holes * 0.5])
+    recs = _compress(k_rows, v_rows, [0, 128, 256], D)
+    for u, rec in zip([0, 128, 256], recs):
+        compare_record(rec, oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128]), D)
+    z = oracle.unpack_record(recs[0], D)
+    assert np.all(z["k_codes"] == 0) and np.all(z["k_delta"] == 0) and np.all(z["k_s"] == 1)
+
+
+def test_compress_is_deterministic_and_schedule_independent():
+    D = 128
+    ks, vs = synth.kv_layer(2, 9, 1, 128 * 8, D)
+    units = [128 * i for i in range(8)]
+    a = _compress(ks[0], vs[0], units, D)
+    b = _compress(ks[0], vs[0], units[::-1], D)[::-1]
+    c = _compress(ks[0], vs[0], units[3:4], D)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert np.array_equal(a[3], c[0])
