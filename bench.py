@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""KVarN hot-path benchmark on GB300: decode attention over the compressed
+cache at 16k context, and bulk tile compression.
+
+Decode step (the timed unit): one new token of a Qwen3-8B-like model (32 query
+heads, 8 KV heads, head_dim 128, batch 1) through 36 layers, each layer with
+its own 16k-token compressed cache (128 packed tiles per KV head plus the FP32
+window): per layer the split-tile decode kernel and the LSE combine, then the
+append of the layer's next K/V token into the window; one device-side window
+advance per step. The step is captured once as a CUDA graph and replayed.
+Whenever the window reaches 128 tokens the oldest 128 are promoted (compressed
+into a tile) between replays, as the decode loop of the pages does with its
+promotion hoisted out of the graph.
+
+After the decode timing the bulk compression of config 2's 32k caches
+(256 tiles x 8 KV heads = 2048 tile-heads per launch) is timed on its own.
+
+Prints one JSON line (see the keys at the end of main()).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KVarN decode-attn tokens/s & HBM GB/s at 16k ctx; tile-compress tiles/s"
+L2_BYTES = 129 * 1024 * 1024
+
+# Decode workload (Qwen3-8B-like, config 2 at 16k)
+CFG, HQ, HKV, D, LAYERS, CTX0, W = 2, 32, 8, 128, 36, 16384, 128
+# Compress bulk workload (config 2's 32k caches)
+C_TILES, C_HEADS = 256, 8
+
+# DRAM bytes per launch from an ncu capture, keyed by the kernel source they
+# were measured on (None until captured; ignored once the source changes).
+NCU_TRAFFIC = {
+    "decode_split": {"src_sha": None, "bytes": None},
+    "compress": {"src_sha": None, "bytes": None},
+}
+
+
+def src_sha(name: str) -> str:
+    with open(os.path.join(ROOT, "kv_cache_quantization_token_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx, self.proc, self.lines = gpu_index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+class OracleDecodeSample:
+    """The fp64 oracle (as it stands) on a bounded sample of the decode step:
+    layer 0's 8 KV heads, each over its first `n_tiles` tiles, every query
+    head of the KV head's group, on host threads (the oracle's C code
+    releases the GIL). Its inputs are the oracle's own compressed tiles."""
+
+    def __init__(self, n_tiles: int):
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        from kv_cache_quantization_token_gb300 import synth
+        self.oracle, self.n_tiles = oracle, n_tiles
+        self.threads = max(1, min(len(os.sched_getaffinity(0)), HKV))
+        self.pool = ThreadPoolExecutor(self.threads)
+        rb = oracle.record_bytes(D)
+        self.table = (np.arange(n_tiles, dtype=np.int64) * rb)[None, None, :]
+        self.q = synth.queries(CFG, 0, (1, HQ, D))
+        n_tok = 128 * n_tiles
+
+        def setup(h):
+            k, v = synth.kv_stream(CFG, 0, h, n_tok, D)
+            return np.concatenate([oracle.compress_unit(k[128 * i:128 * i + 128],
+                                                        v[128 * i:128 * i + 128])["record"]
+                                   for i in range(n_tiles)])
+        self.recs = list(self.pool.map(setup, range(HKV)))
+        self.sample = (f"layer 0 of {LAYERS}: {HKV} KV heads x {HQ // HKV} query heads over "
+                       f"{n_tok} of {CTX0} tokens, scaled to the full step")
+
+    def _head(self, h):
+        G = HQ // HKV
+        wk = np.zeros((1, 1, 128, D), np.float32)
+        return self.oracle.decode_attention(self.q[:, h * G:(h + 1) * G], self.recs[h], self.table,
+                                            [self.n_tiles], wk, wk, [0], [0], D ** -0.5,
+                                            heads=[(0, g) for g in range(G)])
+
+    def run(self) -> float:
+        """Seconds of one sample; tokens/s of the full step = 1 / (that x scale)."""
+        t0 = time.perf_counter()
+        list(self.pool.map(self._head, range(HKV)))
+        return time.perf_counter() - t0
+
+    @property
+    def scale(self) -> float:
+        return LAYERS * CTX0 / (128.0 * self.n_tiles)
+
+
+def run_reference(args, rank):
+    """--impl reference: the oracle timed on the host cores on this arm's metric,
+    one bounded sample (every KV head of one layer over one tile) per step."""
+    if rank != 0:
+        return
+    smp = OracleDecodeSample(1)
+    for _ in range(args.warmup):
+        smp.run()
+    secs = [smp.run() for _ in range(args.steps)]
+    value = 1.0 / (float(np.mean(secs)) * smp.scale)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1000.0 * float(np.mean(secs)), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(),
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.threads,
+                            "kind": "oracle", "sample": smp.sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def workload_config():
+    return {"workload": f"Qwen3-8B-like KVarN decode attention: batch 1, {HQ}q/{HKV}kv heads, "
+                        f"head_dim {D}, {LAYERS} layers of distinct caches at "
+                        f"{CTX0}+ tokens (K4/V2 tiles + FP32 window, W={W}); "
+                        f"plus bulk compress of {C_TILES}x{C_HEADS} tile-heads (32k ctx)",
+            "global_batch": 1, "seq_len": CTX0, "layers": LAYERS, "head_dim": D,
+            "q_heads": HQ, "kv_heads": HKV, "parallelism": "replicas",
+            "l2": "inputs larger than L2: 36 distinct layer caches (>576 MiB) read per step"}
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from kv_cache_quantization_token_gb300 import _build, kvarn, synth
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    lay = kvarn.layout(D)
+    rb = lay.record_bytes
+    B = 1
+    cap = 128
+    # the window starts part-filled so promotions fall inside the timed steps
+    w0 = 64
+    e2e_steps = max(10, args.steps // 5)
+    total_steps = 1 + args.warmup + args.steps + e2e_steps
+    max_tiles = CTX0 // 128 + (w0 + total_steps) // 128 + 1
+
+    # ---- caches: raw synthetic K/V per layer, compressed on the GPU --------
+    tiles = torch.empty(LAYERS * HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
+    table = torch.empty(LAYERS, B, HKV, max_tiles, dtype=torch.int64, device=dev)
+    win_k = torch.zeros(LAYERS, B, HKV, cap, D, device=dev)
+    win_v = torch.zeros_like(win_k)
+    n0 = CTX0 // 128
+    for l in range(LAYERS):
+        ks, vs = synth.kv_layer(CFG, l, HKV, CTX0 + w0, D)
+        base = (l * HKV) * max_tiles
+        tab = (base + np.arange(HKV)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
+        table[l, 0] = torch.from_numpy(tab.astype(np.int64))
+        kd = torch.from_numpy(ks.reshape(-1, D)).to(dev)
+        vd = torch.from_numpy(vs.reshape(-1, D)).to(dev)
+        src = (np.arange(HKV)[:, None] * (CTX0 + w0) + 128 * np.arange(n0)[None, :]).reshape(-1)
+        kvarn.compress_tile(kd, vd, torch.from_numpy(src.astype(np.int64)).to(dev), tiles,
+                            torch.from_numpy(tab[:, :n0].reshape(-1).astype(np.int64)).to(dev), lay)
+        win_k[l, 0, :, :w0] = torch.from_numpy(ks[:, CTX0:]).to(dev)
+        win_v[l, 0, :, :w0] = torch.from_numpy(vs[:, CTX0:]).to(dev)
+        del kd, vd
+    win_start = torch.zeros(B, dtype=torch.int32, device=dev)
+    win_len = torch.full((B,), w0, dtype=torch.int32, device=dev)
+    n_tiles = torch.full((B,), n0, dtype=torch.int32, device=dev)
+    q = torch.from_numpy(synth.queries(CFG, 0, (LAYERS, B, HQ, D))).to(dev)
+    kn = torch.from_numpy(synth.queries(CFG, 1, (LAYERS, B, 1, HKV, D))).to(dev)
+    vn = torch.from_numpy(synth.queries(CFG, 2, (LAYERS, B, 1, HKV, D))).to(dev)
+    out = torch.empty(LAYERS, B, HQ, D, device=dev)
+    ws = torch.empty(kvarn.decode_workspace_bytes(B, HQ, HKV, D, max_tiles, cap) + 256,
+                     dtype=torch.uint8, device=dev)
+    # promotion: the oldest 128 window rows of every (layer, head) -> next tile slot
+    win_rows_k = win_k.view(-1, D)
+    win_rows_v = win_v.view(-1, D)
+    torch.cuda.synchronize()
+
+    host = {"start": 0, "len": w0, "n_tiles": n0}
+    launches = {"n": 0}
+
+    def promote_if_due():
+        if host["len"] < W:
+            return
+        if host["n_tiles"] >= max_tiles:
+            raise RuntimeError("tile slots exhausted")
+        src = ((np.arange(LAYERS * HKV) * cap) + host["start"]).astype(np.int64)
+        lh = np.arange(LAYERS * HKV)
+        dst = (((lh // HKV) * HKV + lh % HKV) * max_tiles + host["n_tiles"]) * rb
+        kvarn.compress_tile(win_rows_k, win_rows_v, torch.from_numpy(src).to(dev, non_blocking=True),
+                            tiles, torch.from_numpy(dst.astype(np.int64)).to(dev, non_blocking=True),
+                            lay)
+        kvarn.window_advance(win_start, win_len, n_tiles, 0, 1, cap)
+        host["start"] = (host["start"] + 128) % cap
+        host["len"] -= 128
+        host["n_tiles"] += 1
+        launches["n"] += 2
+
+    # ---- capture one decode step ----------------------------------------
+    try:
+        ev_split = [(torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True)) for _ in range(LAYERS)]
+        timed_in_graph = True
+    except TypeError:
+        ev_split, timed_in_graph = None, False
+
+    def step_body(record_events):
+        for l in range(LAYERS):
+            if record_events:
+                ev_split[l][0].record()
+            kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
+                               win_len, lay, ws)
+            if record_events:
+                ev_split[l][1].record()
+            kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
+            kvarn.append_window(kn[l], vn[l], win_k[l], win_v[l], win_start, win_len)
+        kvarn.window_advance(win_start, win_len, None, 1, 0, cap)
+
+    per_step_launches = 3 * LAYERS + 1
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step_body(False)  # warm the function attributes outside capture
+        host["len"] += 1
+        promote_if_due()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_body(timed_in_graph)
+
+    def run_steps(n):
+        for _ in range(n):
+            graph.replay()
+            host["len"] += 1
+            launches["n"] += per_step_launches
+            with torch.cuda.stream(stream):
+                promote_if_due()
+
+    with torch.cuda.stream(stream):
+        run_steps(args.warmup)
+    torch.cuda.synchronize()
+
+    # ---- timed region ----------------------------------------------------
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches["n"] = 0
+    with torch.cuda.stream(stream):
+        t_start.record()
+        run_steps(args.steps)
+        t_end.record()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    gpu_launches = launches["n"]
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_s = world * B * args.steps / (elapsed_ms / 1000.0)
+
+    # split-kernel durations of the last replay (events captured in the graph)
+    if timed_in_graph:
+        split_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_split]))
+        split_how = "CUDA events captured around each split launch in the graph (last timed replay)"
+    else:
+        with torch.cuda.stream(stream):
+            evs = []
+            for l in range(LAYERS):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
+                                   win_len, lay, ws)
+                b.record()
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        split_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        split_how = "CUDA events around eager split launches after the timed region"
+    ctx_now = 128 * host["n_tiles"] + host["len"]
+    packed = B * HKV * host["n_tiles"] * rb
+    window_bytes = B * HKV * host["len"] * D * 4 * 2
+    split_bytes = packed + window_bytes + B * HQ * D * 4
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC["decode_split"]
+    traffic = tr["bytes"] if tr["src_sha"] == src_sha("decode.cu") else None
+
+    # ---- e2e: host buffers through the public API ---------------------------
+    q_h = q.cpu().pin_memory()
+    kn_h, vn_h = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = q.numel() * 4 + kn.numel() * 4 + vn.numel() * 4
+    d2h = out.numel() * 4
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(e2e_steps):
+            q.copy_(q_h, non_blocking=True)
+            kn.copy_(kn_h, non_blocking=True)
+            vn.copy_(vn_h, non_blocking=True)
+            graph.replay()
+            host["len"] += 1
+            promote_if_due()
+            out_h.copy_(out, non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_tps = world * B * e2e_steps / (e0.elapsed_time(e1) / 1000.0)
+    assert np.isfinite(out_h.numpy()).all(), "decode produced non-finite output"
+
+    # ---- compress bulk (config 2's 32k caches) ------------------------------
+    n_units = C_TILES * C_HEADS
+    ks, vs = synth.kv_layer(CFG, 99, C_HEADS, 128 * C_TILES, D)
+    ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
+    cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
+    del ks, vs
+    csrc = torch.arange(n_units, dtype=torch.int64, device=dev) * 128
+    cdst = torch.arange(n_units, dtype=torch.int64, device=dev) * rb
+    ctiles = torch.empty(n_units * rb, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
+        c_reps = 20
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(c_reps)]
+        for a, b in cev:  # input (256 MiB) is larger than L2
+            a.record()
+            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
+            b.record()
+    torch.cuda.synchronize()
+    comp_ms = float(np.mean([a.elapsed_time(b) for a, b in cev]))
+    comp_bytes = n_units * (2 * 128 * D * 4 + rb)
+    comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
+    trc = NCU_TRAFFIC["compress"]
+    ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        smp = OracleDecodeSample(32)
+        sec = smp.run()
+        cpu = {"value": 1.0 / (sec * smp.scale), "unit": "tokens/s", "cores": smp.threads,
+               "kind": "oracle", "sample": smp.sample, "sample_seconds": sec}
+
+    if rank == 0:
+        res = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(),
+            "decode": {"ctx_end": ctx_now, "split_kernel_ms": split_ms, "split_gbs": split_gbs,
+                       "split_bytes_per_launch": split_bytes, "timing": split_how},
+            "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": split_gbs / hbm, "traffic": traffic,
+                         "kernel": "decode_split_kernel", "peak_source": peak_kind},
+            "compress": {"tile_heads_per_launch": n_units, "ms_per_launch": comp_ms,
+                         "tiles_per_s": n_units / (comp_ms * 1e-3), "gbs": comp_gbs,
+                         "bytes_per_launch": comp_bytes,
+                         "roofline": {"bound": "hbm", "achieved": comp_gbs, "peak": hbm,
+                                      "unit": "GB/s", "frac": comp_gbs / hbm,
+                                      "traffic": ctraffic, "kernel": "compress_kernel<128>",
+                                      "peak_source": peak_kind}},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": gpu_launches,
+            "clocks": clock_info,
+        }
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

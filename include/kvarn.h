@@ -179,35 +179,69 @@ int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new,
                         kvarn_stream_t stream);
 
 /*
+ * Device-side window bookkeeping (PR #434, commit 6040076: whole-tile
+ * promotion out of the FP32 staging window; commit e43f3f0: promotion is
+ * hoisted out of the CUDA-graph decode step). For every sequence s < n_seq:
+ *   win_len[s] += d_len                      (tokens appended since the last call)
+ *   then, if promote > 0:
+ *   win_start[s] = (win_start[s] + 128 * promote) % win_capacity
+ *   win_len[s]  -= 128 * promote,  n_tiles[s] += promote
+ * The caller decides `promote` under the rule "while win_len >= W, compress
+ * the oldest 128 tokens" and has already compressed those tokens with
+ * kvarn_compress_tile. win_start, win_len, n_tiles: int32 [n_seq], device
+ * (n_tiles may be NULL when promote == 0). win_capacity must be a positive
+ * multiple of 128. One tiny launch; it lets a whole decode step be captured.
+ */
+int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
+                         int d_len, int promote, int win_capacity, kvarn_stream_t stream);
+
+/*
  * Decode attention over the compressed cache (PR #434, commits 0d7cd28 and
  * e43f3f0, llm_kvarn_attention; issue #433 item 2: a fixed worst-case grid
  * over (head, tile range) with early exit, followed by an LSE combine, with
  * the deferred inverse rotation applied after combining the rotated
- * partials). Two launches: a split kernel over (sequence, KV head, tile range)
- * that also runs the window, then a combine kernel over (sequence, query head).
+ * partials). Two kernels:
+ *   kvarn_decode_split    grid over (item, KV head, sequence): each item is a
+ *                         fixed range of packed tiles, or a fixed range of
+ *                         128-token chunks of the FP32 window; it writes the
+ *                         item's softmax max, sum and (rotated for tiles, raw
+ *                         for the window) value accumulator into ws.
+ *   kvarn_decode_combine  grid over (query head, sequence): LSE merge of the
+ *                         items, one inverse rotation of the merged tile
+ *                         accumulator, plus the window accumulator, / sum.
+ * kvarn_decode_attention enqueues both.
  *
  * For query head h of sequence b the result is exact softmax attention
  *   out[b][h] = sum_j softmax_j(scale * q[b][h] . k_j) v_j
  * over every cached token j of KV head h / G: the tiles' tokens (k_j, v_j
  * reconstructed as described at kvarn_layout_t) and then the window's raw rows.
- *   q          : fp32 [B][Hq][D], unrotated.
+ *   q          : fp32 [B][Hq][D], unrotated. Hq / Hkv = G must be 1..8.
  *   tiles      : u8 base of the record pool.
  *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets (multiples of
- *                16); entries at or past n_tiles[b] are never read.
+ *                16; an unaligned offset makes that head's output NaN);
+ *                entries at or past n_tiles[b] are never read.
  *   n_tiles    : int32 [B], 0 <= n_tiles[b] <= max_tiles (clamped on device).
  *   win_k/v    : fp32 [B][Hkv][win_capacity][D]; win_start/win_len int32 [B]
  *                as in kvarn_append_window (win_len clamped to win_capacity).
  *   out        : fp32 [B][Hq][D]. A head with no tokens at all gets zeros.
  *   softmax_scale : usually 1/sqrt(D) (the pages do not state it).
  *   ws         : device workspace of at least kvarn_decode_workspace_bytes()
- *                bytes, 256-byte aligned; it holds per-split partials and
+ *                bytes, 256-byte aligned; it holds the per-item partials and
  *                needs no initialisation. Calls sharing ws must not overlap.
- * The grid depends only on (B, Hkv, max_tiles, device), so the call can be
- * captured in a CUDA graph and replayed while n_tiles and the windows change.
- * Results are deterministic: the same inputs give bit-identical outputs.
+ * The grids depend only on (B, Hq, Hkv, D, max_tiles, win_capacity, device),
+ * so the calls can be captured in a CUDA graph and replayed while n_tiles and
+ * the windows change. Results are deterministic (bit-identical on repeat).
  */
 int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_tiles,
                                  int win_capacity, size_t* bytes);
+int kvarn_decode_split(const float* q, const uint8_t* tiles, const int64_t* tile_table,
+                       const int32_t* n_tiles, const float* win_k, const float* win_v,
+                       const int32_t* win_start, const int32_t* win_len, int win_capacity, int B,
+                       int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
+                       const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
+                       kvarn_stream_t stream);
+int kvarn_decode_combine(const void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int head_dim,
+                         int max_tiles, int win_capacity, float* out, kvarn_stream_t stream);
 int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
                            const int32_t* n_tiles, const float* win_k, const float* win_v,
                            const int32_t* win_start, const int32_t* win_len,

@@ -4,9 +4,10 @@
 // grid over (head, tile range) with early exit, followed by an LSE combine;
 // the deferred inverse WHT is applied after combining the rotated partials):
 //
-//   split kernel   grid (item, KV head, sequence). Items 0..tile_items-1 each
-//                  own TPS consecutive tiles, one warp per tile; the remaining
-//                  items each own 128 tokens of the FP32 window.
+//   split kernel   grid (item, KV head, sequence) of TPS warps per CTA. Items
+//                  0..tile_items-1 own TPS consecutive packed tiles, one warp
+//                  per tile; the remaining items own TPS 128-token chunks of
+//                  the FP32 window (raw rows, unrotated query), one per warp.
 //   combine kernel grid (query head, sequence): LSE merge of the items, one
 //                  inverse rotation of the merged tile accumulator, plus the
 //                  (unrotated) window accumulator, divided by the softmax sum.
@@ -131,20 +132,32 @@ struct DC {
 
 template <int D, int GP, int TPS>
 __global__ void __launch_bounds__(32 * TPS)
-decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
-                   const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
-                   int Hq, int Hkv, int G, int max_tiles, int items, float scale,
-                   float* __restrict__ ws_ml, float* __restrict__ ws_acc) {
+decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
+                    const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
+                    const float* __restrict__ win_k, const float* __restrict__ win_v,
+                    const int32_t* __restrict__ win_start, const int32_t* __restrict__ win_len,
+                    int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
+                    float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc) {
   using C = DC<D, GP, TPS>;
   using R = Rec<D>;
   extern __shared__ __align__(16) unsigned char smem[];
   const int item = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nt = min(max(n_tiles[b], 0), max_tiles);
-  const int tile0 = item * TPS;
-  const int ntile = min(max(nt - tile0, 0), TPS);
+  const bool is_win = item >= tile_items;
   const int64_t part = ((int64_t)b * Hq + (int64_t)kvh * G) * items + item;
-  if (ntile == 0) {
+
+  // slots of this item: packed tiles, or 128-token chunks of the window
+  int nslot, wlen = 0, wstart = 0, wj0 = 0;
+  if (!is_win) {
+    const int nt = min(max(n_tiles[b], 0), max_tiles);
+    nslot = min(max(nt - item * TPS, 0), TPS);
+  } else {
+    wlen = min(max(win_len[b], 0), cap);
+    wstart = ((win_start[b] % cap) + cap) % cap;
+    wj0 = 128 * TPS * (item - tile_items);
+    nslot = min(max((wlen - wj0 + 127) / 128, 0), TPS);
+  }
+  if (nslot == 0) {
     if (tid < G) {
       ws_ml[(part + (int64_t)tid * items) * 2 + 0] = kNegInf;
       ws_ml[(part + (int64_t)tid * items) * 2 + 1] = 0.f;
@@ -157,43 +170,56 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
   float* red_l = red_max + TPS * GP;
   int* okf = reinterpret_cast<int*>(smem + C::OFF_FLG);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + tile0;
-
-  if (tid == 0) {
-    for (int k = 0; k < ntile; ++k) mbar_init(&bar[k], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    for (int k = 0; k < ntile; ++k) {
-      const int64_t off = trow[k];
-      const bool aligned = (off & 15) == 0 && off >= 0;
-      okf[k] = aligned;
-      if (aligned) {
-        mbar_expect_tx(&bar[k], C::RB);
-        bulk_g2s(smem + k * C::RB, tiles + off, C::RB, &bar[k]);
-      }
-    }
-  }
-  // the rotated, scaled query of every head of the GQA group
-  for (int h = warp; h < GP; h += TPS)
-    rotate_head_to_smem<D, GP>(q + ((int64_t)b * Hq + (int64_t)kvh * G + h) * D, h < G, scale, qs, h,
-                               lane);
-  __syncthreads();
 
   const int k = warp;
-  const bool have = k < ntile;
-  bool ok = have && okf[k];
-  if (ok) ok = mbar_wait(&bar[k], 0);
-  const unsigned char* Rk = smem + k * C::RB;
-
-  // ---------------- phase A: scores of this warp's tile -------------------
+  const bool have = k < nslot;
+  bool ok = have;
+  const int tw = lane & 15, cs = lane >> 4;
   float zr[4][GP];
   float mx[GP];
 #pragma unroll
   for (int h = 0; h < GP; ++h) mx[h] = kNegInf;
-  const int tw = lane & 15, cs = lane >> 4;
-  if (ok) {
+
+  if (!is_win) {
+    const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + item * TPS;
+    if (tid == 0) {
+      for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int kk = 0; kk < nslot; ++kk) {
+        const int64_t off = trow[kk];
+        const bool aligned = (off & 15) == 0 && off >= 0;
+        okf[kk] = aligned;
+        if (aligned) {
+          mbar_expect_tx(&bar[kk], C::RB);
+          bulk_g2s(smem + kk * C::RB, tiles + off, C::RB, &bar[kk]);
+        }
+      }
+    }
+    // the rotated, scaled query of every head of the GQA group
+    for (int h = warp; h < GP; h += TPS)
+      rotate_head_to_smem<D, GP>(q + ((int64_t)b * Hq + (int64_t)kvh * G + h) * D, h < G, scale,
+                                 qs, h, lane);
+    __syncthreads();
+    ok = have && okf[k];
+    if (ok) ok = mbar_wait(&bar[k], 0);
+  } else {
+    // the unrotated, scaled query: window rows are raw
+    for (int idx = tid; idx < D * GP; idx += 32 * TPS) {
+      const int c = idx / GP, h = idx % GP;
+      qs[idx] = h < G ? scale * q[((int64_t)b * Hq + (int64_t)kvh * G + h) * D + c] : 0.f;
+    }
+    if (tid < TPS) okf[tid] = 1;
+    __syncthreads();
+  }
+  const unsigned char* Rk = smem + k * C::RB;
+  const int64_t head_base = ((int64_t)b * Hkv + kvh) * cap;          // window rows of this head
+  const int wn = is_win ? min(128, wlen - (wj0 + 128 * k)) : 0;      // tokens in this warp's chunk
+
+  // ---------------- phase A: scores of this warp's slot -------------------
+  if (ok && !is_win) {
     const float* kS = reinterpret_cast<const float*>(Rk + R::kKS);
     const float* kD = reinterpret_cast<const float*>(Rk + R::kKDelta);
     const float* kL = reinterpret_cast<const float*>(Rk + R::kKLo);
@@ -254,16 +280,43 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
         mx[h] = fmaxf(mx[h], z);
       }
     }
+  } else if (ok) {
+    // window chunk: lane owns tokens 4*lane .. 4*lane+3 of the chunk
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = 4 * lane + j;
+#pragma unroll
+      for (int h = 0; h < GP; ++h) zr[j][h] = kNegInf;
+      if (t < wn) {
+        const int slot = (wstart + wj0 + 128 * k + t) % cap;
+        const float4* kr = reinterpret_cast<const float4*>(win_k + (head_base + slot) * D);
+        float z[GP];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) z[h] = 0.f;
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 kv = kr[c4];
+          const float kx[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int h = 0; h < GP; ++h) z[h] = fmaf(qs[(4 * c4 + e) * GP + h], kx[e], z[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+          zr[j][h] = z[h];
+          mx[h] = fmaxf(mx[h], z[h]);
+        }
+      }
+    }
   }
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
     mx[h] = warp_max(mx[h]);
     if (lane == 0) red_max[k * GP + h] = mx[h];
   }
-  if (lane == 0 && have && !ok) red_l[k * GP] = NAN;  // poison marker, checked below
   __syncthreads();
   bool poison = false;
-  for (int kk = 0; kk < ntile; ++kk) poison |= !okf[kk];
+  for (int kk = 0; kk < nslot; ++kk) poison |= !okf[kk];
   float M[GP];
 #pragma unroll
   for (int h = 0; h < GP; ++h) {
@@ -276,10 +329,10 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
   if (ok) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int t = 8 * tw + 4 * cs + j;
+      const int t = is_win ? 4 * lane + j : 8 * tw + 4 * cs + j;
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        const float p = expf(zr[j][h] - M[h]);
+        const float p = (is_win && t >= wn) ? 0.f : expf(zr[j][h] - M[h]);
         l[h] += p;
         sc[(k * 128 + t) * GP + h] = p;
       }
@@ -292,8 +345,9 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
   }
   __syncwarp();
 
-  // ---------------- phase B: value aggregate of this warp's tile ----------
-  if (ok) {
+  // ---------------- phase B: value aggregate of this warp's slot ----------
+  float* vred = reinterpret_cast<float*>(smem + k * C::RB);  // [GP][D] partial of slot k
+  if (ok && !is_win) {
     const float* vR = reinterpret_cast<const float*>(Rk + R::kVR);
     const float* vD = reinterpret_cast<const float*>(Rk + R::kVDelta);
     const float* vL = reinterpret_cast<const float*>(Rk + R::kVLo);
@@ -324,8 +378,8 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
       for (int h = 0; h < GP; ++h) Lg[g][h] = warp_sum(Lg[g][h]);
     __syncwarp();
     const unsigned char* vc = Rk + R::kVCodes;
-    constexpr int COLS = D / 4;                  // bytes per token row
-    constexpr int CPL = COLS >= 32 ? COLS / 32 : 1;  // byte columns per lane
+    constexpr int COLS = D / 4;                        // bytes per token row
+    constexpr int CPL = COLS >= 32 ? COLS / 32 : 1;    // byte columns per lane
     constexpr int TSTEP = COLS >= 32 ? 1 : 32 / COLS;  // lanes sharing a column (token split)
     const int jb0 = COLS >= 32 ? lane : (lane % COLS);
     const int tpar = COLS >= 32 ? 0 : (lane / COLS);
@@ -370,7 +424,6 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
 #pragma unroll
       for (int e = 0; e < 4; ++e) sv[u][e] = vS[4 * (jb0 + 32 * u) + e];
     __syncwarp();  // the record slot is reused for this tile's value partials
-    float* vred = reinterpret_cast<float*>(smem + k * C::RB);  // [GP][D]
     if (tpar == 0) {
 #pragma unroll
       for (int u = 0; u < CPL; ++u) {
@@ -382,117 +435,48 @@ decode_tile_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tile
           for (int h = 0; h < GP; ++h) vred[h * D + 4 * jb + e] = sv[u][e] * (acc[u][e][h] + Lg[g][h]);
       }
     }
+  } else if (ok) {
+    // window chunk: lane owns channels lane*E .. lane*E+E-1 of the raw rows
+    constexpr int E = D / 32;
+    float acc[E][GP];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+#pragma unroll
+      for (int h = 0; h < GP; ++h) acc[e][h] = 0.f;
+    for (int t = 0; t < wn; ++t) {
+      const int slot = (wstart + wj0 + 128 * k + t) % cap;
+      const float* vr = win_v + (head_base + slot) * D + lane * E;
+      float pv[GP];
+#pragma unroll
+      for (int h = 0; h < GP; ++h) pv[h] = sc[(k * 128 + t) * GP + h];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float x = vr[e];
+#pragma unroll
+        for (int h = 0; h < GP; ++h) acc[e][h] = fmaf(pv[h], x, acc[e][h]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+#pragma unroll
+      for (int h = 0; h < GP; ++h) vred[h * D + lane * E + e] = acc[e][h];
   }
   __syncthreads();
 
   for (int idx = tid; idx < G * D; idx += 32 * TPS) {
     const int h = idx / D, c = idx % D;
     float s = 0.f;
-    for (int kk = 0; kk < ntile; ++kk) s += reinterpret_cast<const float*>(smem + kk * C::RB)[h * D + c];
+    for (int kk = 0; kk < nslot; ++kk) s += reinterpret_cast<const float*>(smem + kk * C::RB)[h * D + c];
     ws_acc[(part + (int64_t)h * items) * D + c] = poison ? NAN : s;
   }
   if (tid < G) {
     float M0 = kNegInf, L0 = 0.f;
     for (int kk = 0; kk < TPS; ++kk) {
       M0 = fmaxf(M0, red_max[kk * GP + tid]);
-      if (kk < ntile) L0 += red_l[kk * GP + tid];
+      if (kk < nslot) L0 += red_l[kk * GP + tid];
     }
     ws_ml[(part + (int64_t)tid * items) * 2 + 0] = poison ? NAN : M0;
     ws_ml[(part + (int64_t)tid * items) * 2 + 1] = poison ? NAN : L0;
-  }
-}
-
-// Window items: up to 128 raw FP32 tokens of the ring, unrotated query.
-template <int D, int GP>
-__global__ void __launch_bounds__(128)
-decode_window_kernel(const float* __restrict__ q, const float* __restrict__ win_k,
-                     const float* __restrict__ win_v, const int32_t* __restrict__ win_start,
-                     const int32_t* __restrict__ win_len, int cap, int Hq, int Hkv, int G, int items,
-                     int tile_items, float scale, float* __restrict__ ws_ml,
-                     float* __restrict__ ws_acc) {
-  __shared__ float qs[D * GP];
-  __shared__ float sc[128 * GP];
-  __shared__ float red[4 * GP];
-  const int witem = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int item = tile_items + witem;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wlen = min(max(win_len[b], 0), cap);
-  const int start = ((win_start[b] % cap) + cap) % cap;
-  const int j0 = 128 * witem;
-  const int n = min(128, wlen - j0);
-  const int64_t part = ((int64_t)b * Hq + (int64_t)kvh * G) * items + item;
-  if (n <= 0) {
-    if (tid < G) {
-      ws_ml[(part + (int64_t)tid * items) * 2 + 0] = kNegInf;
-      ws_ml[(part + (int64_t)tid * items) * 2 + 1] = 0.f;
-    }
-    return;
-  }
-  for (int idx = tid; idx < D * GP; idx += 128) {
-    const int c = idx / GP, h = idx % GP;
-    qs[idx] = h < G ? scale * q[((int64_t)b * Hq + (int64_t)kvh * G + h) * D + c] : 0.f;
-  }
-  __syncthreads();
-  const int64_t head_base = ((int64_t)b * Hkv + kvh) * cap;
-  float z[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) z[h] = kNegInf;
-  if (tid < n) {
-    const int slot = (start + j0 + tid) % cap;
-    const float4* kr = reinterpret_cast<const float4*>(win_k + (head_base + slot) * D);
-#pragma unroll
-    for (int h = 0; h < GP; ++h) z[h] = 0.f;
-    for (int c4 = 0; c4 < D / 4; ++c4) {
-      const float4 kv = kr[c4];
-      const float kx[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-#pragma unroll
-        for (int h = 0; h < GP; ++h) z[h] = fmaf(qs[(4 * c4 + e) * GP + h], kx[e], z[h]);
-    }
-  }
-  float M[GP], l[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    const float m = warp_max(z[h]);
-    if (lane == 0) red[warp * GP + h] = m;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < GP; ++h)
-    M[h] = fmaxf(fmaxf(red[h], red[GP + h]), fmaxf(red[2 * GP + h], red[3 * GP + h]));
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    const float p = tid < n ? expf(z[h] - M[h]) : 0.f;
-    sc[tid * GP + h] = p;
-    const float s = warp_sum(p);
-    if (lane == 0) red[warp * GP + h] = s;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int h = 0; h < GP; ++h) l[h] = (red[h] + red[GP + h]) + (red[2 * GP + h] + red[3 * GP + h]);
-  for (int c = tid; c < D; c += 128) {
-    float acc[GP];
-#pragma unroll
-    for (int h = 0; h < GP; ++h) acc[h] = 0.f;
-    for (int t = 0; t < n; ++t) {
-      const int slot = (start + j0 + t) % cap;
-      const float v = win_v[(head_base + slot) * D + c];
-#pragma unroll
-      for (int h = 0; h < GP; ++h) acc[h] = fmaf(sc[t * GP + h], v, acc[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-      if (h < G) ws_acc[(part + (int64_t)h * items) * D + c] = acc[h];
-  }
-  if (tid < G) {
-    float Mh = M[0], lh = l[0];
-#pragma unroll
-    for (int h = 1; h < GP; ++h)
-      if (h == tid) { Mh = M[h]; lh = l[h]; }
-    ws_ml[(part + (int64_t)tid * items) * 2 + 0] = Mh;
-    ws_ml[(part + (int64_t)tid * items) * 2 + 1] = lh;
   }
 }
 
@@ -538,67 +522,55 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
 }
 
 template <int D, int GP, int TPS>
-cudaError_t launch_tile(const DecodePlan& p, const float* q, const uint8_t* tiles,
-                        const int64_t* tile_table, const int32_t* n_tiles, int B, int Hq, int Hkv,
-                        int max_tiles, float scale, float* ws_ml, float* ws_acc, cudaStream_t st) {
+cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
+                           cudaStream_t st) {
   using C = DC<D, GP, TPS>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_tile_kernel<D, GP, TPS>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, TPS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  dim3 grid(p.tile_items, Hkv, B);
-  decode_tile_kernel<D, GP, TPS><<<grid, 32 * TPS, C::SMEM, st>>>(
-      q, tiles, tile_table, n_tiles, Hq, Hkv, Hq / Hkv, max_tiles, p.items, scale, ws_ml, ws_acc);
+  dim3 grid(p.items, a.Hkv, a.B);
+  decode_split_kernel<D, GP, TPS><<<grid, 32 * TPS, C::SMEM, st>>>(
+      a.q, a.tiles, a.tile_table, a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len,
+      a.win_capacity, a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale, ws_ml,
+      ws_acc);
   return cudaGetLastError();
 }
 
 template <int D, int GP>
-cudaError_t launch_dg(const DecodePlan& p, const float* q, const uint8_t* tiles,
-                      const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
-                      const float* win_v, const int32_t* win_start, const int32_t* win_len,
-                      int win_capacity, int B, int Hq, int Hkv, int max_tiles, float scale,
-                      float* ws_ml, float* ws_acc, float* out, cudaStream_t st) {
-  cudaError_t e = cudaSuccess;
-  if (p.tile_items > 0) {
-    switch (p.tiles_per_item) {
-      case 1: e = launch_tile<D, GP, 1>(p, q, tiles, tile_table, n_tiles, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, st); break;
-      case 2: e = launch_tile<D, GP, 2>(p, q, tiles, tile_table, n_tiles, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, st); break;
-      case 4: e = launch_tile<D, GP, 4>(p, q, tiles, tile_table, n_tiles, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, st); break;
-      default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess) return e;
+cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
+                           cudaStream_t st) {
+  switch (p.tiles_per_item) {
+    case 1: return launch_split_t<D, GP, 1>(p, a, ws_ml, ws_acc, st);
+    case 2: return launch_split_t<D, GP, 2>(p, a, ws_ml, ws_acc, st);
+    case 4: return launch_split_t<D, GP, 4>(p, a, ws_ml, ws_acc, st);
+    default: return cudaErrorInvalidValue;
   }
-  if (p.win_items > 0) {
-    dim3 grid(p.win_items, Hkv, B);
-    decode_window_kernel<D, GP><<<grid, 128, 0, st>>>(q, win_k, win_v, win_start, win_len,
-                                                      win_capacity, Hq, Hkv, Hq / Hkv, p.items,
-                                                      p.tile_items, scale, ws_ml, ws_acc);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  decode_combine_kernel<D><<<dim3(Hq, B), D, 0, st>>>(ws_ml, ws_acc, Hq, p.items, p.tile_items, out);
-  return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const DecodePlan& p, const float* q, const uint8_t* tiles,
-                     const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
-                     const float* win_v, const int32_t* win_start, const int32_t* win_len,
-                     int win_capacity, int B, int Hq, int Hkv, int max_tiles, float scale,
-                     float* ws_ml, float* ws_acc, float* out, cudaStream_t st) {
+cudaError_t launch_split_d(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
+                           cudaStream_t st) {
   switch (p.g_pad) {
-    case 1: return launch_dg<D, 1>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
-    case 2: return launch_dg<D, 2>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
-    case 4: return launch_dg<D, 4>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
-    case 8: return launch_dg<D, 8>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
+    case 1: return launch_split_g<D, 1>(p, a, ws_ml, ws_acc, st);
+    case 2: return launch_split_g<D, 2>(p, a, ws_ml, ws_acc, st);
+    case 4: return launch_split_g<D, 4>(p, a, ws_ml, ws_acc, st);
+    case 8: return launch_split_g<D, 8>(p, a, ws_ml, ws_acc, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** acc) {
+  const size_t parts = (size_t)B * Hq * p.items;
+  const size_t mlb = (parts * 2 * sizeof(float) + 255) / 256 * 256;
+  *ml = reinterpret_cast<float*>(ws);
+  *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
 int sm_count() {
@@ -625,7 +597,7 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
   if (tps > cap) tps = cap;
   p->tiles_per_item = tps;
   p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
-  p->win_items = win_capacity > 0 ? (win_capacity + 127) / 128 : 0;
+  p->win_items = win_capacity > 0 ? (win_capacity + 128 * tps - 1) / (128 * tps) : 0;
   p->items = p->tile_items + p->win_items;
   const size_t parts = (size_t)B * Hq * p->items;
   const size_t ml = (parts * 2 * sizeof(float) + 255) / 256 * 256;
@@ -633,21 +605,31 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
   return 0;
 }
 
-cudaError_t launch_decode(const DecodePlan& p, const float* q, const uint8_t* tiles,
-                          const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
-                          const float* win_v, const int32_t* win_start, const int32_t* win_len,
-                          int win_capacity, int B, int Hq, int Hkv, int D, int max_tiles,
-                          float scale, void* ws, float* out, cudaStream_t st) {
-  const size_t parts = (size_t)B * Hq * p.items;
-  const size_t ml = (parts * 2 * sizeof(float) + 255) / 256 * 256;
-  float* ws_ml = reinterpret_cast<float*>(ws);
-  float* ws_acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ml);
-  switch (D) {
-    case 64: return launch_d<64>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
-    case 128: return launch_d<128>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
-    case 256: return launch_d<256>(p, q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, win_capacity, B, Hq, Hkv, max_tiles, scale, ws_ml, ws_acc, out, st);
+cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                cudaStream_t st) {
+  if (p.items == 0) return cudaSuccess;
+  float *ml, *acc;
+  ws_split(p, a.B, a.Hq, ws, &ml, &acc);
+  switch (a.D) {
+    case 64: return launch_split_d<64>(p, a, ml, acc, st);
+    case 128: return launch_split_d<128>(p, a, ml, acc, st);
+    case 256: return launch_split_d<256>(p, a, ml, acc, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
+                                  float* out, cudaStream_t st) {
+  float *ml, *acc;
+  ws_split(p, B, Hq, const_cast<void*>(ws), &ml, &acc);
+  const dim3 grid(Hq, B);
+  switch (D) {
+    case 64: decode_combine_kernel<64><<<grid, 64, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 128: decode_combine_kernel<128><<<grid, 128, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 256: decode_combine_kernel<256><<<grid, 256, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace kvarn

@@ -141,32 +141,88 @@ int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_t
   return KVARN_OK;
 }
 
+static int decode_prepare(const float* q, const uint8_t* tiles, const int64_t* tile_table,
+                          const int32_t* n_tiles, const float* win_k, const float* win_v,
+                          const int32_t* win_start, const int32_t* win_len, int win_capacity,
+                          int B, int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
+                          const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
+                          kvarn::DecodePlan* p, kvarn::DecodeArgs* a) {
+  int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
+  if (rc != KVARN_OK) return rc;
+  if (!layout) return KVARN_ERR_NULL;
+  if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
+  kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, p);
+  if (B == 0) return KVARN_OK;
+  if (!q || !n_tiles) return KVARN_ERR_NULL;
+  if (max_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
+  if (win_capacity > 0 && (!win_k || !win_v || !win_start || !win_len)) return KVARN_ERR_NULL;
+  if (p->ws_bytes > 0 && !ws) return KVARN_ERR_NULL;
+  if (ws_bytes < p->ws_bytes) return KVARN_ERR_WORKSPACE;
+  if (!aligned16(q) || (max_tiles > 0 && !aligned16(tiles)) ||
+      (win_capacity > 0 && (!aligned16(win_k) || !aligned16(win_v))) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
+    return KVARN_ERR_ALIGN;
+  if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
+  *a = kvarn::DecodeArgs{q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
+                         win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale};
+  return KVARN_OK;
+}
+
+int kvarn_decode_split(const float* q, const uint8_t* tiles, const int64_t* tile_table,
+                       const int32_t* n_tiles, const float* win_k, const float* win_v,
+                       const int32_t* win_start, const int32_t* win_len, int win_capacity, int B,
+                       int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
+                       const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
+                       kvarn_stream_t stream) {
+  kvarn::DecodePlan p;
+  kvarn::DecodeArgs a;
+  const int rc = decode_prepare(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
+                                win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
+                                layout, ws, ws_bytes, &p, &a);
+  if (rc != KVARN_OK || B == 0) return rc;
+  return from_cuda(kvarn::launch_decode_split(p, a, ws, (cudaStream_t)stream));
+}
+
+int kvarn_decode_combine(const void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int head_dim,
+                         int max_tiles, int win_capacity, float* out, kvarn_stream_t stream) {
+  const int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
+  if (rc != KVARN_OK) return rc;
+  if (B == 0) return KVARN_OK;
+  kvarn::DecodePlan p;
+  kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &p);
+  if (!out || (p.ws_bytes > 0 && !ws)) return KVARN_ERR_NULL;
+  if (ws_bytes < p.ws_bytes) return KVARN_ERR_WORKSPACE;
+  if (!aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255)) return KVARN_ERR_ALIGN;
+  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
+}
+
 int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
                            const int32_t* n_tiles, const float* win_k, const float* win_v,
                            const int32_t* win_start, const int32_t* win_len, int win_capacity,
                            int B, int Hq, int Hkv, int head_dim, int max_tiles,
                            float softmax_scale, const kvarn_layout_t* layout, void* ws,
                            size_t ws_bytes, float* out, kvarn_stream_t stream) {
-  int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
-  if (rc != KVARN_OK) return rc;
-  if (!layout) return KVARN_ERR_NULL;
-  if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
-  if (B == 0) return KVARN_OK;
   kvarn::DecodePlan p;
-  kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &p);
-  if (!q || !out || !n_tiles) return KVARN_ERR_NULL;
-  if (max_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
-  if (win_capacity > 0 && (!win_k || !win_v || !win_start || !win_len)) return KVARN_ERR_NULL;
-  if (p.ws_bytes > 0 && !ws) return KVARN_ERR_NULL;
-  if (ws_bytes < p.ws_bytes) return KVARN_ERR_WORKSPACE;
-  if (!aligned16(q) || !aligned16(out) || (max_tiles > 0 && !aligned16(tiles)) ||
-      (win_capacity > 0 && (!aligned16(win_k) || !aligned16(win_v))) ||
-      (reinterpret_cast<uintptr_t>(ws) & 255))
-    return KVARN_ERR_ALIGN;
-  if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
-  return from_cuda(kvarn::launch_decode(p, q, tiles, tile_table, n_tiles, win_k, win_v,
-                                        win_start, win_len, win_capacity, B, Hq, Hkv, head_dim,
-                                        max_tiles, softmax_scale, ws, out, (cudaStream_t)stream));
+  kvarn::DecodeArgs a;
+  int rc = decode_prepare(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
+                          win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale, layout, ws,
+                          ws_bytes, &p, &a);
+  if (rc != KVARN_OK || B == 0) return rc;
+  if (!out) return KVARN_ERR_NULL;
+  if (!aligned16(out)) return KVARN_ERR_ALIGN;
+  rc = from_cuda(kvarn::launch_decode_split(p, a, ws, (cudaStream_t)stream));
+  if (rc != KVARN_OK) return rc;
+  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
+}
+
+int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
+                         int d_len, int promote, int win_capacity, kvarn_stream_t stream) {
+  if (n_seq < 0 || promote < 0 || win_capacity <= 0 || (win_capacity % KVARN_TILE_TOKENS))
+    return KVARN_ERR_BAD_ARG;
+  if (n_seq == 0 || (d_len == 0 && promote == 0)) return KVARN_OK;
+  if (!win_start || !win_len || (promote > 0 && !n_tiles)) return KVARN_ERR_NULL;
+  return from_cuda(kvarn::launch_window_advance(win_start, win_len, n_tiles, n_seq, d_len, promote,
+                                                win_capacity, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -61,17 +61,31 @@ cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new,
                           cudaStream_t st);
 
 struct DecodePlan {
-  int tiles_per_item;  // tiles handled by one split CTA
+  int tiles_per_item;  // tiles (or 128-token window chunks) handled by one split CTA
   int tile_items;      // ceil(max_tiles / tiles_per_item)
-  int win_items;       // ceil(win_capacity / 128) window CTAs (0 when capacity is 0)
+  int win_items;       // ceil(win_capacity / (128 * tiles_per_item))
   int items;           // tile_items + win_items
   int g_pad;           // query heads per KV head rounded up to 1, 2, 4 or 8
   size_t ws_bytes;
 };
+struct DecodeArgs {
+  const float* q;
+  const uint8_t* tiles;
+  const int64_t* tile_table;
+  const int32_t* n_tiles;
+  const float* win_k;
+  const float* win_v;
+  const int32_t* win_start;
+  const int32_t* win_len;
+  int win_capacity, B, Hq, Hkv, D, max_tiles;
+  float scale;
+};
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p);
-cudaError_t launch_decode(const DecodePlan& p, const float* q, const uint8_t* tiles,
-                          const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
-                          const float* win_v, const int32_t* win_start, const int32_t* win_len,
-                          int win_capacity, int B, int Hq, int Hkv, int D, int max_tiles,
-                          float scale, void* ws, float* out, cudaStream_t st);
+cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                cudaStream_t st);
+cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
+                                  float* out, cudaStream_t st);
+cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
+                                  int n_seq, int d_len, int promote, int win_capacity,
+                                  cudaStream_t st);
 }  // namespace kvarn

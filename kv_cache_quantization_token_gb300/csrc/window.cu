@@ -5,6 +5,8 @@
 // llm_kvarn_rotate_query; issue #180, "Algorithm (per 128-token tile)" step 1).
 // Window append: raw K/V rows go into the per-sequence FP32 ring that stages
 // tokens until a whole 128-token tile is promoted (PR #434, commit 6040076).
+// Window advance: the ring's start/length and the tile count move on the
+// device after an append or a promotion.
 #include "kvarn_common.cuh"
 
 namespace kvarn {
@@ -68,7 +70,30 @@ __global__ void append_kernel(const float4* __restrict__ k_new, const float4* __
   }
 }
 
+// Window bookkeeping on the device, so that a decode step (append, attend,
+// advance) can be captured in a CUDA graph and replayed.
+__global__ void advance_kernel(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
+                               int d_len, int promote, int cap) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  int len = win_len[s] + d_len;
+  if (promote > 0) {
+    win_start[s] = (int)(((int64_t)win_start[s] + 128LL * promote) % cap);
+    len -= 128 * promote;
+    n_tiles[s] += promote;
+  }
+  win_len[s] = len;
+}
+
 }  // namespace
+
+cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
+                                  int n_seq, int d_len, int promote, int win_capacity,
+                                  cudaStream_t st) {
+  advance_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(win_start, win_len, n_tiles, n_seq, d_len,
+                                                       promote, win_capacity);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, cudaStream_t st) {
   const unsigned blocks = (unsigned)((n_rows + 7) / 8);

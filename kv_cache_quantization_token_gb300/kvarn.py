@@ -64,9 +64,15 @@ def _L():
         lib.kvarn_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                c_int, c_int, c_int, ctypes.c_float,
                                                ctypes.POINTER(Layout), vp, sz, vp, vp]
+        lib.kvarn_decode_split.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
+                                           c_int, c_int, c_int, ctypes.c_float,
+                                           ctypes.POINTER(Layout), vp, sz, vp]
+        lib.kvarn_decode_combine.argtypes = [vp, sz, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]
+        lib.kvarn_window_advance.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, vp]
         for name in ("kvarn_layout", "kvarn_rotate_query", "kvarn_compress_tile",
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
-                     "kvarn_decode_attention"):
+                     "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
+                     "kvarn_window_advance"):
             getattr(lib, name).restype = c_int
         _lib = lib
     return _lib
@@ -186,3 +192,39 @@ def decode_attention(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win
                                        ctypes.byref(lay), _ptr(ws), ws.numel(), _ptr(out),
                                        _stream(stream)))
     return out
+
+
+def decode_split(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len, lay: Layout,
+                 ws, softmax_scale=None, stream=None):
+    """First decode kernel: per-item partials into ws (see decode_attention)."""
+    _dev(q, "q", torch.float32)
+    B, Hq, D = q.shape
+    Hkv, max_tiles = tile_table.shape[1], tile_table.shape[2]
+    cap = win_k.shape[2]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    _check("kvarn_decode_split",
+           _L().kvarn_decode_split(_ptr(q), _ptr(tiles), _ptr(tile_table), _ptr(n_tiles),
+                                   _ptr(win_k), _ptr(win_v), _ptr(win_start), _ptr(win_len), cap,
+                                   B, Hq, Hkv, D, max_tiles, float(softmax_scale),
+                                   ctypes.byref(lay), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def decode_combine(ws, out, Hkv, max_tiles, win_capacity, stream=None):
+    """Second decode kernel: LSE combine of the partials in ws into out [B][Hq][D]."""
+    _dev(out, "out", torch.float32)
+    B, Hq, D = out.shape
+    _check("kvarn_decode_combine",
+           _L().kvarn_decode_combine(_ptr(ws), ws.numel(), B, Hq, Hkv, D, max_tiles, win_capacity,
+                                     _ptr(out), _stream(stream)))
+    return out
+
+
+def window_advance(win_start, win_len, n_tiles, d_len, promote, win_capacity, stream=None):
+    """Device-side window bookkeeping (length += d_len, then promote tiles)."""
+    _dev(win_start, "win_start", torch.int32)
+    _dev(win_len, "win_len", torch.int32)
+    _check("kvarn_window_advance",
+           _L().kvarn_window_advance(_ptr(win_start), _ptr(win_len), _ptr(n_tiles),
+                                     win_start.numel(), int(d_len), int(promote),
+                                     int(win_capacity), _stream(stream)))

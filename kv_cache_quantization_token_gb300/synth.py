@@ -16,7 +16,7 @@ outliers in keys, heavy-tailed per-token scales in values):
     V = N(0,1) * per-token |t_4| (Student-t, 4 degrees of freedom)
   queries: N(0,1) fp32.
 
-Seeds: numpy PCG64 with seed = base + 1000 * config + 37 * layer + kv_head for
+Draws are fp32 (numpy's float32 normal sampler). Seeds: numpy PCG64 with seed = base + 1000 * config + 37 * layer + kv_head for
 K/V streams; queries use a separate stream keyed the same way plus 500_000.
 """
 from __future__ import annotations
@@ -40,13 +40,15 @@ def kv_stream(config: int, layer: int, kv_head: int, n_tokens: int, head_dim: in
     ch_scale = np.exp(rng.standard_normal(D))
     outliers = rng.choice(D, size=n_out, replace=False)
     ch_scale[outliers] *= 20.0
-    k = rng.standard_normal((n_tokens, D)) * ch_scale[None, :]
+    k = rng.standard_normal((n_tokens, D), dtype=np.float32)
+    k *= ch_scale.astype(np.float32)[None, :]
     if fam == "lognormal":
         tok_scale = np.exp(0.5 * rng.standard_normal(n_tokens))
     else:
         tok_scale = np.abs(rng.standard_t(4.0, n_tokens))
-    v = rng.standard_normal((n_tokens, D)) * tok_scale[:, None]
-    return k.astype(np.float32), v.astype(np.float32)
+    v = rng.standard_normal((n_tokens, D), dtype=np.float32)
+    v *= tok_scale.astype(np.float32)[:, None]
+    return k, v
 
 
 def kv_layer(config: int, layer: int, n_kv_heads: int, n_tokens: int, head_dim: int,
