@@ -249,6 +249,35 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
                            int max_tiles, float softmax_scale, const kvarn_layout_t* layout,
                            void* ws, size_t ws_bytes, float* out, kvarn_stream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory. The pages
+ * have no counterpart to this entry point; it exists for embedders that may
+ * not call cudaMalloc where attention runs (code inside another runtime's
+ * memory arena, or a host framework that owns every allocation).
+ * Same arguments and result as kvarn_decode_attention, minus the workspace:
+ * the partials go to a scratch array of KVARN_NOALLOC_SCRATCH_BYTES that the
+ * library keeps in its own device memory. Every GPU that loads the library
+ * holds that array until the process exits.
+ *  - Returns KVARN_ERR_WORKSPACE (nothing enqueued) when
+ *    kvarn_decode_workspace_bytes() for these sizes exceeds the array; with
+ *    head_dim 128 and GQA 4 that is about B * 2,000 tiles.
+ *  - The first call on a device (that device current) looks up the array's
+ *    device address with cudaGetSymbolAddress and caches it; make that first
+ *    call before any stream capture. It never calls cudaMalloc or cudaFree.
+ *  - Every call on a device shares the one array and leaves its last contents
+ *    there; nothing in it needs to start at zero. Calls that overlap on the
+ *    GPU (different streams, or different host threads) race on it.
+ */
+#define KVARN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int kvarn_decode_attention_noalloc(const float* q, const uint8_t* tiles,
+                                   const int64_t* tile_table, const int32_t* n_tiles,
+                                   const float* win_k, const float* win_v,
+                                   const int32_t* win_start, const int32_t* win_len,
+                                   int win_capacity, int B, int Hq, int Hkv, int head_dim,
+                                   int max_tiles, float softmax_scale,
+                                   const kvarn_layout_t* layout, float* out,
+                                   kvarn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

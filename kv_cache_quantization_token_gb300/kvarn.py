@@ -228,3 +228,31 @@ def window_advance(win_start, win_len, n_tiles, d_len, promote, win_capacity, st
            _L().kvarn_window_advance(_ptr(win_start), _ptr(win_len), _ptr(n_tiles),
                                      win_start.numel(), int(d_len), int(promote),
                                      int(win_capacity), _stream(stream)))
+
+
+def decode_attention_noalloc(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
+                             lay: Layout, softmax_scale=None, out=None, stream=None):
+    """decode_attention for callers that cannot allocate device memory: the
+    partials go to the library's own fixed scratch array instead of a
+    workspace (see kvarn_decode_attention_noalloc in include/kvarn.h).
+    `out` must be passed by such callers; it is created here only as a
+    convenience for everyone else."""
+    _dev(q, "q", torch.float32)
+    B, Hq, D = q.shape
+    Hkv, max_tiles = tile_table.shape[1], tile_table.shape[2]
+    cap = win_k.shape[2]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    lib = _L()
+    fn = lib.kvarn_decode_attention_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6 + [ctypes.c_float,
+                                                               ctypes.POINTER(Layout),
+                                                               ctypes.c_void_p, ctypes.c_void_p]
+    _check("kvarn_decode_attention_noalloc",
+           fn(_ptr(q), _ptr(tiles), _ptr(tile_table), _ptr(n_tiles), _ptr(win_k), _ptr(win_v),
+              _ptr(win_start), _ptr(win_len), cap, B, Hq, Hkv, D, max_tiles,
+              float(softmax_scale), ctypes.byref(lay), _ptr(out), _stream(stream)))
+    return out
