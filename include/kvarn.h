@@ -250,6 +250,35 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
                            void* ws, size_t ws_bytes, float* out, kvarn_stream_t stream);
 
 /*
+ * Chunked-prefill attention (PR #434, commit 99c3773, llm_kvarn_prefill_attention:
+ * a single streaming softmax over the compressed tiles plus the FP32 window
+ * with a deferred inverse WHT; issue #433 item 1: run the K-score and
+ * V-aggregate contractions on tensor cores). For one sequence, after the
+ * chunk's K/V were appended to the window and whole tiles promoted:
+ *   out[i][h] = sum_j softmax_j(scale * q[i][h] . k_j) v_j
+ * over the keys j of KV head h / G whose position is <= pos0 + i, where tile
+ * k holds positions [128 k, 128 k + 128) and window token w (w < win_len)
+ * sits at position 128 * n_tiles + w.
+ * The two contractions run on tcgen05 tensor cores with fp16 operands and
+ * fp32 accumulation: tiles are dequantised to fp16 in shared memory (never to
+ * global memory), window rows are rotated into the same space on the fly,
+ * and the softmax, causal mask and final inverse rotation run on CUDA cores.
+ *   q_chunk    : fp32 [C][Hq][D], unrotated; out: fp32 [C][Hq][D].
+ *   tile_table : int64 [Hkv][table_stride] record byte offsets (multiples of
+ *                16) of this sequence's tiles; table_stride >= n_tiles.
+ *   win_k/v    : fp32 [Hkv][win_capacity][D] ring of this sequence;
+ *                win_start, win_len, n_tiles: host integers.
+ * Requires pos0 + C <= 128 * n_tiles + win_len (the chunk's own keys are in
+ * the cache), head_dim 64 or 128 (256 returns KVARN_ERR_UNSUPPORTED) and
+ * Hq / Hkv <= 8. Needs no workspace.
+ */
+int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                            const int64_t* tile_table, int table_stride, int n_tiles,
+                            const float* win_k, const float* win_v, int win_start, int win_len,
+                            int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
+                            const kvarn_layout_t* layout, float* out, kvarn_stream_t stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it exists for embedders that may
  * not call cudaMalloc where attention runs (code inside another runtime's

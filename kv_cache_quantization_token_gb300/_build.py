@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkvarn.so")
-SOURCES = ["kvarn_abi.cu", "compress.cu", "window.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["kvarn_abi.cu", "compress.cu", "window.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu"]
 HEADERS = [os.path.join(CSRC, "kvarn_common.cuh"), os.path.join(ROOT, "include", "kvarn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

@@ -6,8 +6,9 @@
 //
 //   split kernel   grid (item, KV head, sequence) of TPS warps per CTA. Items
 //                  0..tile_items-1 own TPS consecutive packed tiles, one warp
-//                  per tile; the remaining items own TPS 128-token chunks of
-//                  the FP32 window (raw rows, unrotated query), one per warp.
+//                  per tile; the remaining items own TPS chunks of 16 (8 at
+//                  head_dim 256) FP32 window rows, one per warp, staged by
+//                  bulk copies (raw rows, unrotated query).
 //   combine kernel grid (query head, sequence): LSE merge of the items, one
 //                  inverse rotation of the merged tile accumulator, plus the
 //                  (unrotated) window accumulator, divided by the softmax sum.
@@ -78,6 +79,34 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int m = 16; m; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
   return v;
 }
+// Sums v[j] over the 32 lanes for every j < N (N a power of two <= 32) with
+// halving exchanges; returns the total of row win_row_of_lane<N>(lane).
+template <int N>
+__device__ __forceinline__ int win_row_of_lane(int lane) {
+  int r = 0;
+#pragma unroll
+  for (int s = 0; (1 << s) < N; ++s) r |= ((lane >> s) & 1) * (N >> (s + 1));
+  return r;
+}
+template <int N>
+__device__ __forceinline__ float warp_reduce_rows(float (&v)[N], int lane) {
+#pragma unroll
+  for (int s = 0; (1 << s) < N; ++s) {
+    const int n = N >> s, m = 1 << s;
+    const bool up = lane & m;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float send = up ? v[j] : v[j + n / 2];
+      const float keep = up ? v[j + n / 2] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = N; m < 32; m <<= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+  return r;
+}
+
 // exact small-integer to float: the code sits in the mantissa of 2^23
 __device__ __forceinline__ float code_f(uint32_t c) {
   return __int_as_float((int)(c | 0x4B000000u)) - 8388608.0f;
@@ -119,6 +148,7 @@ template <int D, int GP, int TPS>
 struct DC {
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
+  static constexpr int WCH = D >= 256 ? 8 : 16;  // window tokens per warp (K+V rows fit a slot)
   static constexpr int WK = (D > 128 * GV ? D : 128 * GV) * GP;  // floats of per-warp scratch
   static constexpr int OFF_SC = TPS * RB;                         // [TPS][128][GP] scores
   static constexpr int OFF_WK = OFF_SC + TPS * 128 * GP * 4;      // [TPS][WK]
@@ -128,6 +158,7 @@ struct DC {
   static constexpr int OFF_BAR = (OFF_FLG + TPS * 4 + 7) / 8 * 8;
   static constexpr int SMEM = (OFF_BAR + TPS * 8 + 15) / 16 * 16;
   static_assert(GP * D * 4 <= RB, "value partials must fit in a record slot");
+  static_assert(2 * WCH * D * 4 <= RB, "a window chunk must fit in a record slot");
 };
 
 template <int D, int GP, int TPS>
@@ -154,8 +185,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   } else {
     wlen = min(max(win_len[b], 0), cap);
     wstart = ((win_start[b] % cap) + cap) % cap;
-    wj0 = 128 * TPS * (item - tile_items);
-    nslot = min(max((wlen - wj0 + 127) / 128, 0), TPS);
+    wj0 = C::WCH * TPS * (item - tile_items);
+    nslot = min(max((wlen - wj0 + C::WCH - 1) / C::WCH, 0), TPS);
   }
   if (nslot == 0) {
     if (tid < G) {
@@ -206,17 +237,42 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     ok = have && okf[k];
     if (ok) ok = mbar_wait(&bar[k], 0);
   } else {
-    // the unrotated, scaled query: window rows are raw
+    // window rows are raw FP32: stage each warp's chunk of WCH rows of K and V
+    // (contiguous D-float rows of the ring) into its slot with bulk copies
+    const int64_t head_base = ((int64_t)b * Hkv + kvh) * cap;
+    if (tid == 0) {
+      for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int kk = 0; kk < nslot; ++kk) {
+        const int n = min(C::WCH, wlen - (wj0 + C::WCH * kk));
+        okf[kk] = 1;
+        mbar_expect_tx(&bar[kk], (uint32_t)(n * D * 4 * 2));
+        unsigned char* dst = smem + kk * C::RB;
+        for (int j = 0; j < n; ++j) {
+          const int slot = (wstart + wj0 + C::WCH * kk + j) % cap;
+          bulk_g2s(dst + j * D * 4, win_k + (head_base + slot) * D, D * 4, &bar[kk]);
+          bulk_g2s(dst + (C::WCH + j) * D * 4, win_v + (head_base + slot) * D, D * 4, &bar[kk]);
+        }
+      }
+    }
+    // the unrotated, scaled query
     for (int idx = tid; idx < D * GP; idx += 32 * TPS) {
       const int c = idx / GP, h = idx % GP;
       qs[idx] = h < G ? scale * q[((int64_t)b * Hq + (int64_t)kvh * G + h) * D + c] : 0.f;
     }
-    if (tid < TPS) okf[tid] = 1;
     __syncthreads();
+    if (ok) ok = mbar_wait(&bar[k], 0);
   }
   const unsigned char* Rk = smem + k * C::RB;
-  const int64_t head_base = ((int64_t)b * Hkv + kvh) * cap;          // window rows of this head
-  const int wn = is_win ? min(128, wlen - (wj0 + 128 * k)) : 0;      // tokens in this warp's chunk
+  const int wn = is_win ? min(C::WCH, wlen - (wj0 + C::WCH * k)) : 0;  // tokens in this warp's chunk
+  // window chunk: lane owns channels lane*E .. lane*E+E-1; after the row
+  // reduction it holds the score of token wtok(lane) (lanes >= WCH repeat)
+  constexpr int E = D / 32;
+  const int wtok = win_row_of_lane<C::WCH>(lane);
+  float zw[GP];
 
   // ---------------- phase A: scores of this warp's slot -------------------
   if (ok && !is_win) {
@@ -281,32 +337,24 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
   } else if (ok) {
-    // window chunk: lane owns tokens 4*lane .. 4*lane+3 of the chunk
+    const float* Kw = reinterpret_cast<const float*>(Rk);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int t = 4 * lane + j;
+    for (int h = 0; h < GP; ++h) {
+      float qv[E];
 #pragma unroll
-      for (int h = 0; h < GP; ++h) zr[j][h] = kNegInf;
-      if (t < wn) {
-        const int slot = (wstart + wj0 + 128 * k + t) % cap;
-        const float4* kr = reinterpret_cast<const float4*>(win_k + (head_base + slot) * D);
-        float z[GP];
+      for (int e = 0; e < E; ++e) qv[e] = qs[(lane * E + e) * GP + h];
+      float part[C::WCH];
 #pragma unroll
-        for (int h = 0; h < GP; ++h) z[h] = 0.f;
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 kv = kr[c4];
-          const float kx[4] = {kv.x, kv.y, kv.z, kv.w};
+      for (int j = 0; j < C::WCH; ++j) {
+        float a = 0.f;
+        if (j < wn) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-#pragma unroll
-            for (int h = 0; h < GP; ++h) z[h] = fmaf(qs[(4 * c4 + e) * GP + h], kx[e], z[h]);
+          for (int e = 0; e < E; ++e) a = fmaf(qv[e], Kw[j * D + lane * E + e], a);
         }
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-          zr[j][h] = z[h];
-          mx[h] = fmaxf(mx[h], z[h]);
-        }
+        part[j] = a;
       }
+      zw[h] = warp_reduce_rows<C::WCH>(part, lane);
+      if (wtok < wn) mx[h] = zw[h];
     }
   }
 #pragma unroll
@@ -326,16 +374,23 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   float l[GP];
 #pragma unroll
   for (int h = 0; h < GP; ++h) l[h] = 0.f;
-  if (ok) {
+  if (ok && !is_win) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int t = is_win ? 4 * lane + j : 8 * tw + 4 * cs + j;
+      const int t = 8 * tw + 4 * cs + j;
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
-        const float p = (is_win && t >= wn) ? 0.f : expf(zr[j][h] - M[h]);
+        const float p = expf(zr[j][h] - M[h]);
         l[h] += p;
         sc[(k * 128 + t) * GP + h] = p;
       }
+    }
+  } else if (ok && lane < C::WCH) {
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      const float p = wtok < wn ? expf(zw[h] - M[h]) : 0.f;
+      l[h] += p;
+      sc[(k * 128 + wtok) * GP + h] = p;
     }
   }
 #pragma unroll
@@ -436,26 +491,28 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
   } else if (ok) {
-    // window chunk: lane owns channels lane*E .. lane*E+E-1 of the raw rows
-    constexpr int E = D / 32;
+    const float* Vw = reinterpret_cast<const float*>(Rk) + C::WCH * D;
     float acc[E][GP];
 #pragma unroll
     for (int e = 0; e < E; ++e)
 #pragma unroll
       for (int h = 0; h < GP; ++h) acc[e][h] = 0.f;
-    for (int t = 0; t < wn; ++t) {
-      const int slot = (wstart + wj0 + 128 * k + t) % cap;
-      const float* vr = win_v + (head_base + slot) * D + lane * E;
-      float pv[GP];
+    __syncwarp();  // the chunk's probabilities are in sc
 #pragma unroll
-      for (int h = 0; h < GP; ++h) pv[h] = sc[(k * 128 + t) * GP + h];
+    for (int j = 0; j < C::WCH; ++j) {
+      if (j < wn) {
+        float pv[GP];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float x = vr[e];
+        for (int h = 0; h < GP; ++h) pv[h] = sc[(k * 128 + j) * GP + h];
 #pragma unroll
-        for (int h = 0; h < GP; ++h) acc[e][h] = fmaf(pv[h], x, acc[e][h]);
+        for (int e = 0; e < E; ++e) {
+          const float x = Vw[j * D + lane * E + e];
+#pragma unroll
+          for (int h = 0; h < GP; ++h) acc[e][h] = fmaf(pv[h], x, acc[e][h]);
+        }
       }
     }
+    __syncwarp();  // the slot's rows are overwritten by the partials below
 #pragma unroll
     for (int e = 0; e < E; ++e)
 #pragma unroll
@@ -480,34 +537,67 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 }
 
-// LSE combine: one CTA of D threads per (query head, sequence).
+// LSE combine: one CTA of D threads per (query head, sequence). The items'
+// (max, sum) pairs are reduced cooperatively, their weights kept in shared
+// memory, then each thread sums its channel over the items with independent,
+// coalesced loads.
 template <int D>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_acc, int Hq,
                       int items, int tile_items, float* __restrict__ out) {
+  constexpr int NW = D / 32;
+  constexpr int CH = 1024;  // items per weight chunk in shared memory
   __shared__ float x[D];
-  const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+  __shared__ float wgt[CH];
+  __shared__ float redf[NW];
+  __shared__ int redi[NW];
+  const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x, lane = c & 31, wid = c >> 5;
   const int64_t base = ((int64_t)b * Hq + hq) * items;
   float M = kNegInf;
-  bool poison = false;
-  for (int j = 0; j < items; ++j) {
+  int poison = 0;
+  for (int j = c; j < items; j += D) {
     const float lj = ws_ml[(base + j) * 2 + 1];
-    if (!(lj >= 0.f)) poison = true;
+    if (!(lj >= 0.f)) poison = 1;
     if (lj > 0.f) M = fmaxf(M, ws_ml[(base + j) * 2]);
   }
+  M = warp_max(M);
+  poison = __any_sync(0xffffffffu, poison);
+  if (lane == 0) { redf[wid] = M; redi[wid] = poison; }
+  __syncthreads();
+  M = redf[0];
+  poison = redi[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) { M = fmaxf(M, redf[w]); poison |= redi[w]; }
+  __syncthreads();
   float L = 0.f, arot = 0.f, awin = 0.f;
-  for (int j = 0; j < items; ++j) {
-    const float lj = ws_ml[(base + j) * 2 + 1];
-    if (lj > 0.f) {
-      const float w = expf(ws_ml[(base + j) * 2] - M);
-      L = fmaf(lj, w, L);
-      const float a = ws_acc[(base + j) * D + c];
-      if (j < tile_items) arot = fmaf(w, a, arot);
-      else awin = fmaf(w, a, awin);
+  for (int j0 = 0; j0 < items; j0 += CH) {
+    const int n = min(CH, items - j0);
+    for (int j = c; j < n; j += D) {
+      const float lj = ws_ml[(base + j0 + j) * 2 + 1];
+      const float w = lj > 0.f ? expf(ws_ml[(base + j0 + j) * 2] - M) : 0.f;
+      wgt[j] = w;
+      L = fmaf(lj > 0.f ? lj : 0.f, w, L);
     }
+    __syncthreads();
+    const float* a = ws_acc + (base + j0) * D + c;
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) {
+      const float w = wgt[j];
+      if (w != 0.f) {
+        const float v = a[(int64_t)j * D];
+        if (j0 + j < tile_items) arot = fmaf(w, v, arot);
+        else awin = fmaf(w, v, awin);
+      }
+    }
+    __syncthreads();
   }
+  L = warp_sum(L);
+  if (lane == 0) redf[wid] = L;
   x[c] = arot;
   __syncthreads();
+  L = redf[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) L += redf[w];
 #pragma unroll
   for (int h = 1; h < D; h <<= 1) {
     const float v = x[c], o = x[c ^ h];
@@ -597,7 +687,8 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
   if (tps > cap) tps = cap;
   p->tiles_per_item = tps;
   p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
-  p->win_items = win_capacity > 0 ? (win_capacity + 128 * tps - 1) / (128 * tps) : 0;
+  const int wch = D >= 256 ? 8 : 16;  // window tokens per warp, as in DC<>::WCH
+  p->win_items = win_capacity > 0 ? (win_capacity + wch * tps - 1) / (wch * tps) : 0;
   p->items = p->tile_items + p->win_items;
   const size_t parts = (size_t)B * Hq * p->items;
   const size_t ml = (parts * 2 * sizeof(float) + 255) / 256 * 256;

@@ -215,6 +215,34 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
   return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
 }
 
+int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                            const int64_t* tile_table, int table_stride, int n_tiles,
+                            const float* win_k, const float* win_v, int win_start, int win_len,
+                            int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
+                            const kvarn_layout_t* layout, float* out, kvarn_stream_t stream) {
+  if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
+  if (!layout) return KVARN_ERR_NULL;
+  if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hkv > 65535) return KVARN_ERR_BAD_ARG;
+  if (Hq / Hkv > 8) return KVARN_ERR_UNSUPPORTED;
+  if (C < 0 || pos0 < 0 || n_tiles < 0 || win_len < 0 || win_capacity < 0 ||
+      table_stride < n_tiles || win_len > win_capacity)
+    return KVARN_ERR_BAD_ARG;
+  if (pos0 + C > (int64_t)KVARN_TILE_TOKENS * n_tiles + win_len) return KVARN_ERR_BAD_ARG;
+  if (C == 0) return KVARN_OK;
+  if (!q_chunk || !out) return KVARN_ERR_NULL;
+  if (n_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
+  if (win_len > 0 && (!win_k || !win_v)) return KVARN_ERR_NULL;
+  if (!aligned16(q_chunk) || !aligned16(out) || (n_tiles > 0 && !aligned16(tiles)) ||
+      (win_len > 0 && (!aligned16(win_k) || !aligned16(win_v))))
+    return KVARN_ERR_ALIGN;
+  if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
+  return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
+                                         n_tiles, win_k, win_v, win_start, win_len, win_capacity,
+                                         Hq, Hkv, head_dim, softmax_scale, out,
+                                         (cudaStream_t)stream));
+}
+
 int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
                          int d_len, int promote, int win_capacity, kvarn_stream_t stream) {
   if (n_seq < 0 || promote < 0 || win_capacity <= 0 || (win_capacity % KVARN_TILE_TOKENS))

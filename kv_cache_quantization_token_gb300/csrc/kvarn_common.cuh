@@ -85,6 +85,11 @@ cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* 
                                 cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
                                   float* out, cudaStream_t st);
+cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
+                           const int64_t* tile_table, int table_stride, int n_tiles,
+                           const float* win_k, const float* win_v, int win_start, int win_len,
+                           int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
+                           float* out, cudaStream_t st);
 cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
                                   int n_seq, int d_len, int promote, int win_capacity,
                                   cudaStream_t st);

@@ -1,0 +1,578 @@
+// prefill.cu -- KVarN chunked-prefill attention on sm_103a tensor cores.
+//
+// Per chunk of C query positions of one sequence (SharpInference PR #434,
+// commit 99c3773: a single streaming softmax over the compressed tiles plus
+// the FP32 window with a deferred inverse WHT; issue #433 item 1: run the
+// K-score and V-aggregate contractions on tensor cores), after the chunk's
+// tokens were appended and whole tiles promoted:
+//   out[i][h] = sum_j softmax_j(scale * q[i][h] . k_j) v_j  over keys j with
+//   position(j) <= pos0 + i,
+// tile k holding positions [128k, 128k+128) and window token w position
+// 128 * n_tiles + w.
+//
+// One CTA (4 warps) owns a KV head and 128 score rows: the G query heads of
+// the GQA group times 128/G consecutive positions, so every dequantised tile
+// serves the whole group. All keys live in the rotated space: the query is
+// q' = H q (times scale * log2 e), packed tiles dequantise to
+// K~ = r_t s_c (delta code + lo) and V~ likewise, and window rows are rotated
+// when staged (H k, H v). Per 128-key block:
+//   1. the block is dequantised (or rotated) into fp16 K~ [key][channel] and
+//      V~^T [channel][key] in shared memory, 128-byte swizzled, K-major;
+//   2. S = Q' K~^T on tcgen05 (kind::f16, fp32 accumulate) into TMEM, with
+//      Q' and K~ each split into fp16 hi + lo parts and S = Qh Kh + Qh Kl +
+//      Ql Kh: one fp16 rounding of either operand costs up to 1e-2 in the
+//      output through cancellation in q.k (rotated keys are large), the
+//      split keeps the scores to about 2^-22;
+//   3. each thread owns one score row: causal mask, online softmax in base 2
+//      (the running max is only moved, and O rescaled in TMEM, when a score
+//      exceeds it by more than 8), P written as fp16 to shared memory;
+//   4. O += P V~ on tcgen05 into TMEM.
+// At the end each thread divides its O row by the row sum and applies the one
+// inverse rotation (H is its own inverse). Every wait is bounded; a CTA that
+// gives up writes NaN rows, frees its TMEM and returns.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kvarn_common.cuh"
+
+namespace kvarn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of element (row, k) of a K-major fp16 operand of `rows` rows in
+// the 128-byte-swizzled canonical layout: 64-element K blocks, each `rows`
+// x 128 bytes, 16-byte chunks XOR-swizzled by (row & 7).
+__device__ __forceinline__ uint32_t sw_off(int row, int k, int rows) {
+  return (uint32_t)((k >> 6) * rows * 128 + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) +
+                    (k & 7) * 2);
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row
+// groups 1024 bytes apart (stride byte offset), version bits 46-48 = 0b001.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D f32, A and B f16, both K-major, M = 128.
+template <int N>
+__device__ __forceinline__ uint32_t idesc() {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init1(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 22); ++i)
+    if (mbar_poll(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// x = hi + lo with hi, lo fp16: the pair carries about 22 significant bits.
+__device__ __forceinline__ void split2(float x0, float x1, __half2& hi, __half2& lo) {
+  hi = __floats2half2_rn(x0, x1);
+  lo = __floats2half2_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+}
+
+// In-register orthonormal Walsh-Hadamard transform of N values (N a power of 2).
+template <int N>
+__device__ __forceinline__ void fwht_reg(float (&x)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (!(i & h)) {
+        const float a = x[i], b = x[i | h];
+        x[i] = a + b;
+        x[i | h] = a - b;
+      }
+  const float s = 1.0f / sqrtf((float)N);
+#pragma unroll
+  for (int i = 0; i < N; ++i) x[i] *= s;
+}
+
+template <int D>
+struct PC {
+  static constexpr int OFF_QH = 0;                     // fp16 Q' hi [128 rows][D]
+  static constexpr int OFF_QL = OFF_QH + 128 * D * 2;  // fp16 Q' lo (Q' - hi)
+  static constexpr int OFF_KH = OFF_QL + 128 * D * 2;  // fp16 K~ hi [128 keys][D]
+  static constexpr int OFF_KL = OFF_KH + 128 * D * 2;  // fp16 K~ lo
+  static constexpr int OFF_V = OFF_KL + 128 * D * 2;   // fp16 V~^T [D][128 keys]
+  static constexpr int OFF_P = OFF_V + D * 128 * 2;  // fp16 P   [128 rows][128 keys]
+  static constexpr int OFF_REC = OFF_P + 128 * 128 * 2;  // two packed records (prefetch)
+  static constexpr int RB = Rec<D>::kBytes;
+  static constexpr int OFF_BAR = OFF_REC + 2 * RB;   // mbarriers: rec[2], s, o
+  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack to align the base to 1024
+  static constexpr int TMEM_COLS = 256;              // S: columns 0..127, O: 128..128+D-1
+  static_assert(D == 64 || D == 128, "prefill head_dim");
+};
+
+struct PrefillArgs {
+  const float* q;
+  const uint8_t* tiles;
+  const int64_t* tile_table;  // [Hkv][table_stride]
+  const float* win_k;
+  const float* win_v;
+  float* out;
+  int64_t pos0;
+  int C, Hq, Hkv, G, n_tiles, table_stride, win_start, win_len, win_cap;
+  float qscale;  // softmax_scale * log2(e)
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
+  using P = PC<D>;
+  using R = Rec<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                       ~uintptr_t(1023));
+  unsigned char* sQh = sm + P::OFF_QH;
+  unsigned char* sQl = sm + P::OFF_QL;
+  unsigned char* sKh = sm + P::OFF_KH;
+  unsigned char* sKl = sm + P::OFF_KL;
+  unsigned char* sV = sm + P::OFF_V;
+  unsigned char* sP = sm + P::OFF_P;
+  unsigned char* sRec = sm + P::OFF_REC;
+  uint64_t* bar_rec = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // [2]
+  uint64_t* bar_s = bar_rec + 2;
+  uint64_t* bar_o = bar_rec + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
+  int* fail = reinterpret_cast<int*>(sm + P::OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int kvh = blockIdx.y;
+  const int ppc = 128 / a.G;                 // positions per CTA
+  const int i0 = blockIdx.x * ppc;           // first chunk row of this CTA
+  // score row `tid` <-> (head g = tid / ppc, chunk position i0 + tid % ppc)
+  const int my_g = tid / ppc, my_i = i0 + tid % ppc;
+  const bool my_valid = my_i < a.C && my_g < a.G;
+  const int64_t my_pos = a.pos0 + my_i;
+  const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
+  const int hq = kvh * a.G + min(my_g, a.G - 1);
+
+  // key blocks visible to some row of this CTA: tiles, then 128-token window blocks
+  const int64_t win_pos0 = 128LL * a.n_tiles;
+  int n_tile_blk = a.n_tiles;
+  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
+  n_tile_blk = min(n_tile_blk, a.n_tiles);
+  int n_win_blk = 0;
+  for (int w = 0; 128 * w < a.win_len; ++w)
+    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
+  const int n_blk = n_tile_blk + n_win_blk;
+
+  // every record offset must be 16-byte aligned for the bulk copies; a CTA
+  // that finds one that is not writes NaN rows and does nothing else
+  {
+    int bad = 0;
+    const int64_t* tr = a.tile_table + (int64_t)kvh * a.table_stride;
+    for (int t = tid; t < n_tile_blk; t += 128) bad |= (tr[t] & 15) != 0 || tr[t] < 0;
+    if (__syncthreads_or(bad)) {
+      if (my_valid)
+        for (int c = 0; c < D; ++c) a.out[((int64_t)my_i * a.Hq + hq) * D + c] = NAN;
+      return;
+    }
+  }
+  if (tid == 0) {
+    mbar_init1(&bar_rec[0]);
+    mbar_init1(&bar_rec[1]);
+    mbar_init1(bar_s);
+    mbar_init1(bar_o);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *fail = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_slot)),
+                 "r"(P::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // Q' row: rotate, scale, fp16 into the swizzled A operand
+  {
+    float x[D];
+    if (my_valid) {
+      const float4* src = reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 v = src[c4];
+        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < D; ++c) x[c] = 0.f;
+    }
+    fwht_reg<D>(x);
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        split2(x[8 * c8 + 2 * e] * a.qscale, x[8 * c8 + 2 * e + 1] * a.qscale, hi[e], lo[e]);
+      *reinterpret_cast<uint4*>(sQh + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+      *reinterpret_cast<uint4*>(sQl + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem, t_o = tmem + 128;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int64_t* trow = a.tile_table + (int64_t)kvh * a.table_stride;
+
+  // prefetch the first packed record
+  if (tid == 0 && n_tile_blk > 0) bulk_load(sRec, a.tiles + trow[0], P::RB, &bar_rec[0]);
+
+  float m_ref = -INFINITY, l_sum = 0.f;
+  bool ok = true;
+  int issued_s = 0, issued_o = 0, issued_rec = n_tile_blk > 0 ? 1 : 0;
+  for (int j = 0; j < n_blk; ++j) {
+    const bool is_tile = j < n_tile_blk;
+    // ---- 1. the PV MMA of block j-1 has consumed V~^T and P
+    if (j > 0) {
+      const bool w = mbar_wait_bounded(bar_o, (j - 1) & 1);
+      if (!w) *fail = 1;
+    }
+    int nkeys = 128;
+    int64_t kpos0;
+    if (is_tile) {
+      kpos0 = 128LL * j;
+      if (!mbar_wait_bounded(&bar_rec[j & 1], (j >> 1) & 1)) *fail = 1;
+      // prefetch the next record into the other buffer (its previous user, block j-1, is done)
+      if (j + 1 < n_tile_blk) {
+        if (tid == 0)
+          bulk_load(sRec + ((j + 1) & 1) * P::RB, a.tiles + trow[j + 1], P::RB, &bar_rec[(j + 1) & 1]);
+        ++issued_rec;
+      }
+      const unsigned char* rec = sRec + (j & 1) * P::RB;
+      const float* kS = reinterpret_cast<const float*>(rec + R::kKS);
+      const float* kD = reinterpret_cast<const float*>(rec + R::kKDelta);
+      const float* kL = reinterpret_cast<const float*>(rec + R::kKLo);
+      const float* kR = reinterpret_cast<const float*>(rec + R::kKR);
+      const float* vS = reinterpret_cast<const float*>(rec + R::kVS);
+      const float* vR = reinterpret_cast<const float*>(rec + R::kVR);
+      const float* vD = reinterpret_cast<const float*>(rec + R::kVDelta);
+      const float* vL = reinterpret_cast<const float*>(rec + R::kVLo);
+      // K~: thread -> channel(s), all 128 keys of the channel row
+      for (int c = tid; c < D; c += 128) {
+        const float s = kS[c], d = kD[c] * s, lo = kL[c] * s;
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
+#pragma unroll 4
+        for (int w4 = 0; w4 < 16; ++w4) {
+          const uint32_t wd = row[w4];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int t = 8 * w4 + i;
+            const float v = kR[t] * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
+            const __half h = __float2half_rn(v);
+            const uint32_t o = sw_off(t, c, 128);
+            *reinterpret_cast<__half*>(sKh + o) = h;
+            *reinterpret_cast<__half*>(sKl + o) = __float2half_rn(v - __half2float(h));
+          }
+        }
+      }
+      // V~^T: thread -> key t, all D channels of the token row
+      {
+        const int t = tid;
+        const float r = vR[t];
+        const unsigned char* row = rec + R::kVCodes + t * (D / 4);
+#pragma unroll 4
+        for (int jb = 0; jb < D / 4; ++jb) {
+          const uint32_t byte = row[jb];
+          const int g = (4 * jb) / R::kVGroup;
+          const float d = vD[t * R::kGv + g] * r, lo = vL[t * R::kGv + g] * r;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * jb + e;
+            const float v = vS[c] * fmaf(d, (float)((byte >> (2 * e)) & 3u), lo);
+            *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
+          }
+        }
+      }
+    } else {
+      // window block: rotate raw rows on the fly
+      const int wb = j - n_tile_blk;
+      kpos0 = win_pos0 + 128LL * wb;
+      nkeys = min(128, a.win_len - 128 * wb);
+      const int t = tid;
+      float x[D];
+      const bool have = t < nkeys;
+      const int64_t slot = ((int64_t)a.win_start + 128 * wb + t) % a.win_cap;
+      const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
+      // K row
+      if (have) {
+        const float4* src = reinterpret_cast<const float4*>(a.win_k + rbase);
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 v = src[c4];
+          x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+        }
+        fwht_reg<D>(x);
+      } else {
+#pragma unroll
+        for (int c = 0; c < D; ++c) x[c] = 0.f;
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
+        *reinterpret_cast<uint4*>(sKh + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+        *reinterpret_cast<uint4*>(sKl + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+      }
+      // V row -> column t of V~^T
+      if (have) {
+        const float4* src = reinterpret_cast<const float4*>(a.win_v + rbase);
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 v = src[c4];
+          x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+        }
+        fwht_reg<D>(x);
+      } else {
+#pragma unroll
+        for (int c = 0; c < D; ++c) x[c] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(x[c]);
+    }
+    // ---- 2. S = Q' K~^T
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (*fail) { ok = false; break; }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+        mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKh) + off), idesc<128>(), kk > 0);
+        mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKl) + off), idesc<128>(), 1);
+        mma_f16(t_s, sdesc(su32(sQl) + off), sdesc(su32(sKh) + off), idesc<128>(), 1);
+      }
+      mma_commit(bar_s);
+    }
+    ++issued_s;
+    if (!mbar_wait_bounded(bar_s, j & 1)) *fail = 1;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // ---- 3. softmax of this thread's row
+    float s[128];
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      float v[32];
+      tmem_ld32(t_s + lane_base + c0, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[c0 + i] = v[i];
+    }
+    float mblk = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 128; ++t) {
+      const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
+      s[t] = vis ? s[t] : -INFINITY;
+      mblk = fmaxf(mblk, s[t]);
+    }
+    // move the reference max (and rescale O) only when a score exceeds it by > 8
+    const bool need = mblk > m_ref + 8.0f;
+    const float m_new = need ? mblk : m_ref;
+    const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
+    if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_o + lane_base + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        tmem_st32(t_o + lane_base + c0, v);
+      }
+    }
+    l_sum *= alpha;
+    m_ref = m_new;
+    float rs = 0.f;
+#pragma unroll
+    for (int c8 = 0; c8 < 16; ++c8) {
+      __align__(16) __half2 h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * c8 + 2 * e] - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * c8 + 2 * e + 1] - m_ref);
+        const __half2 hp = __floats2half2_rn(p0, p1);
+        rs += __low2float(hp) + __high2float(hp);  // the sum of what the MMA will add
+        h[e] = hp;
+      }
+      *reinterpret_cast<uint4*>(sP + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(h);
+    }
+    l_sum += rs;
+    // ---- 4. O += P V~
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (*fail) { ok = false; break; }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tid == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+        const uint32_t off_b = (kk >> 2) * D * 128 + (kk & 3) * 32;
+        mma_f16(t_o, sdesc(su32(sP) + off_a), sdesc(su32(sV) + off_b), idesc<D>(), (j > 0 || kk > 0));
+      }
+      mma_commit(bar_o);
+    }
+    ++issued_o;
+  }
+  if (!ok) {
+    // a wait gave up: let the work already issued finish (bounded) before
+    // the shared memory and TMEM are released
+    if (issued_s > 0) mbar_wait_bounded(bar_s, (issued_s - 1) & 1);
+    if (issued_o > 0) mbar_wait_bounded(bar_o, (issued_o - 1) & 1);
+    for (int r = 0; r < 2; ++r) {
+      const int uses = issued_rec / 2 + (r < issued_rec % 2 ? 1 : 0);
+      if (uses > 0) mbar_wait_bounded(&bar_rec[r], (uses - 1) & 1);
+    }
+  }
+  if (ok && n_blk > 0) {
+    if (!mbar_wait_bounded(bar_o, (n_blk - 1) & 1)) ok = false;
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  // ---- epilogue: O / l, one inverse rotation, store
+  {
+    float o[D];
+    if (n_blk > 0) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_o + lane_base + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c0 + i] = v[i];
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < D; ++c) o[c] = 0.f;
+    }
+    const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+#pragma unroll
+    for (int c = 0; c < D; ++c) o[c] *= inv;
+    fwht_reg<D>(o);
+    if (my_valid) {
+      float4* dst = reinterpret_cast<float4*>(a.out + ((int64_t)my_i * a.Hq + hq) * D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        float4 v;
+        v.x = ok ? o[4 * c4] : NAN; v.y = ok ? o[4 * c4 + 1] : NAN;
+        v.z = ok ? o[4 * c4 + 2] : NAN; v.w = ok ? o[4 * c4 + 3] : NAN;
+        dst[c4] = v;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
+  using P = PC<D>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const int ppc = 128 / a.G;
+  dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
+  prefill_kernel<D><<<grid, 128, P::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
+                           const int64_t* tile_table, int table_stride, int n_tiles,
+                           const float* win_k, const float* win_v, int win_start, int win_len,
+                           int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
+                           float* out, cudaStream_t st) {
+  PrefillArgs a;
+  a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
+  a.out = out; a.pos0 = pos0; a.C = C; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
+  a.n_tiles = n_tiles; a.table_stride = table_stride; a.win_start = win_start;
+  a.win_len = win_len; a.win_cap = win_capacity; a.qscale = softmax_scale * kLog2e;
+  switch (D) {
+    case 64: return launch_prefill_d<64>(a, st);
+    case 128: return launch_prefill_d<128>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace kvarn

@@ -69,10 +69,13 @@ def _L():
                                            ctypes.POINTER(Layout), vp, sz, vp]
         lib.kvarn_decode_combine.argtypes = [vp, sz, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp]
         lib.kvarn_window_advance.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, vp]
+        lib.kvarn_prefill_attention.argtypes = [vp, c_int, i64, vp, vp, c_int, c_int, vp, vp,
+                                                c_int, c_int, c_int, c_int, c_int, c_int,
+                                                ctypes.c_float, ctypes.POINTER(Layout), vp, vp]
         for name in ("kvarn_layout", "kvarn_rotate_query", "kvarn_compress_tile",
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
                      "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
-                     "kvarn_window_advance"):
+                     "kvarn_window_advance", "kvarn_prefill_attention"):
             getattr(lib, name).restype = c_int
         _lib = lib
     return _lib
@@ -228,6 +231,29 @@ def window_advance(win_start, win_len, n_tiles, d_len, promote, win_capacity, st
            _L().kvarn_window_advance(_ptr(win_start), _ptr(win_len), _ptr(n_tiles),
                                      win_start.numel(), int(d_len), int(promote),
                                      int(win_capacity), _stream(stream)))
+
+
+def prefill_attention(q_chunk, pos0, tiles, tile_table, n_tiles, win_k, win_v, win_start,
+                      win_len, lay: Layout, softmax_scale=None, out=None, stream=None):
+    """Causal attention of a chunk of one sequence: q_chunk fp32 [C][Hq][D] at
+    positions pos0 + i; tile_table int64 [Hkv][stride]; win_k/v fp32
+    [Hkv][cap][D]; n_tiles, win_start, win_len host ints."""
+    _dev(q_chunk, "q_chunk", torch.float32)
+    C, Hq, D = q_chunk.shape
+    _dev(tile_table, "tile_table", torch.int64)
+    Hkv, stride = tile_table.shape
+    cap = win_k.shape[1]
+    if softmax_scale is None:
+        softmax_scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q_chunk)
+    _check("kvarn_prefill_attention",
+           _L().kvarn_prefill_attention(_ptr(q_chunk), C, int(pos0), _ptr(tiles), _ptr(tile_table),
+                                        stride, int(n_tiles), _ptr(win_k), _ptr(win_v),
+                                        int(win_start), int(win_len), cap, Hq, Hkv, D,
+                                        float(softmax_scale), ctypes.byref(lay), _ptr(out),
+                                        _stream(stream)))
+    return out
 
 
 def decode_attention_noalloc(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,

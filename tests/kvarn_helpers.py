@@ -151,3 +151,72 @@ def rel_l2(got: np.ndarray, want: np.ndarray) -> float:
     if den == 0:
         return float(np.linalg.norm(got))
     return float(np.linalg.norm(got.astype(np.float64) - want) / den)
+
+
+PREFILL_RTOL = 2e-3  # tensor-core prefill (fp16 operands, fp32 accumulation)
+
+
+class PrefillRun:
+    """A prompt streamed through the C ABI in chunks: append -> promote (while
+    the window holds >= W tokens) -> chunked-prefill attention. Keeps, for the
+    chunks listed in `keep`, a copy of the window and the outputs so the
+    oracle can be evaluated on the same state."""
+
+    def __init__(self, cfg, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
+                 dev="cuda:0", scale=None):
+        dev = torch.device(dev)
+        self.Hq, self.Hkv, self.D, self.W = Hq, Hkv, D, W
+        self.k, self.v = synth.kv_layer(cfg, layer, Hkv, n_tokens, D)
+        self.q = synth.queries(cfg, layer, (n_tokens, Hq, D))
+        self.lay = kvarn.layout(D)
+        rb = self.rb = self.lay.record_bytes
+        self.cap = cap = TILE * ((W - 1 + chunk + TILE - 1) // TILE)
+        max_tiles = n_tokens // TILE + 1
+        self.tiles = torch.zeros(Hkv * max_tiles * rb, dtype=torch.uint8, device=dev)
+        table = (np.arange(Hkv)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
+        self.table = torch.from_numpy(table.astype(np.int64)).to(dev)
+        win_k = torch.zeros(1, Hkv, cap, D, device=dev)
+        win_v = torch.zeros_like(win_k)
+        start, length, n_tiles = 0, 0, 0
+        self.snap = {}
+        keep = set(keep if keep is not None else range(0, n_tokens, chunk))
+        for pos0 in range(0, n_tokens, chunk):
+            C = min(chunk, n_tokens - pos0)
+            kn = np.ascontiguousarray(self.k[:, pos0:pos0 + C].transpose(1, 0, 2))[None]
+            vn = np.ascontiguousarray(self.v[:, pos0:pos0 + C].transpose(1, 0, 2))[None]
+            kvarn.append_window(torch.from_numpy(kn).to(dev), torch.from_numpy(vn).to(dev),
+                                win_k, win_v, torch.tensor([start], dtype=torch.int32, device=dev),
+                                torch.tensor([length], dtype=torch.int32, device=dev))
+            length += C
+            while length >= W:
+                src = torch.tensor([h * cap + start for h in range(Hkv)], dtype=torch.int64,
+                                   device=dev)
+                dst = self.table[:, n_tiles].contiguous()
+                kvarn.compress_tile(win_k.view(-1, D), win_v.view(-1, D), src, self.tiles, dst,
+                                    self.lay)
+                n_tiles += 1
+                start = (start + TILE) % cap
+                length -= TILE
+            out = kvarn.prefill_attention(torch.from_numpy(self.q[pos0:pos0 + C]).to(dev), pos0,
+                                          self.tiles, self.table, n_tiles, win_k[0], win_v[0],
+                                          start, length, self.lay, softmax_scale=scale)
+            if pos0 in keep:
+                self.snap[pos0] = dict(C=C, n_tiles=n_tiles, start=start, length=length,
+                                       win_k=win_k[0].cpu().numpy(), win_v=win_v[0].cpu().numpy(),
+                                       out=out.cpu().numpy())
+        self.n_tiles = n_tiles
+        self.scale = D ** -0.5 if scale is None else scale
+
+    def check(self, pos0, rows):
+        """rel-L2 per (i, h) of the chunk at pos0 against the oracle; returns the worst."""
+        s = self.snap[pos0]
+        pool = self.tiles.cpu().numpy()
+        ref = oracle.prefill_attention(self.q[pos0:pos0 + s["C"]], pos0, pool,
+                                       self.table.cpu().numpy(), s["n_tiles"], s["win_k"],
+                                       s["win_v"], s["start"], s["length"], self.scale, rows=rows)
+        worst = 0.0
+        for (i, h), r in ref.items():
+            e = rel_l2(s["out"][i, h], r)
+            worst = max(worst, e)
+            assert e <= PREFILL_RTOL, f"chunk {pos0} row {i} head {h}: rel-L2 {e:.3e}"
+        return worst

@@ -78,3 +78,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert n.value > 0
     args = [p] * 8 + [128, 1, 32, 8, 128, 8, ctypes.c_float(0.088), ctypes.byref(L), p, 16, p, None]
     assert lib.kvarn_decode_attention(*args) == -5
+
+
+def test_prefill_host_validation(lib):
+    L = kvarn.layout(128)
+    p = ctypes.c_void_p(4096)
+    args = lambda C, pos0, nt, wl, D=128, Hq=32, lay=L: (p, C, pos0, p, p, 64, nt, p, p, 0, wl, 768,
+                                                        Hq, 8, D, ctypes.c_float(0.088),
+                                                        ctypes.byref(lay), p, None)
+    f = lib.kvarn_prefill_attention
+    assert f(*args(512, 2000, 10, 300)) == -4          # chunk beyond the cache
+    L256 = kvarn.layout(256)
+    assert f(*args(16, 0, 1, 16, D=256, lay=L256)) == -3  # head_dim 256 not yet supported
+    assert f(*args(16, 0, 1, 16, Hq=80)) == -3            # GQA group of 10
+    assert f(*args(0, 0, 0, 0)) == 0                      # empty chunk enqueues nothing

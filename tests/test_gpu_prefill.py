@@ -1,0 +1,63 @@
+"""GPU chunked-prefill attention (tcgen05) vs the fp64 oracle's causal
+attention, evaluated on the GPU's own tiles and window."""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_quantization_token_gb300 import kvarn, synth
+from tests.kvarn_helpers import ATTN_RTOL, Cache, PrefillRun, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(C, heads, step=37):
+    idx = sorted(set([0, 1, 2, 63, 64, 127, 128, 255, 256, 511, C - 1] + list(range(0, C, step))))
+    return [(i, h) for i in idx if i < C for h in heads]
+
+
+def test_prefill_config3_prefix_chunks():
+    """32q/8kv, D=128, W=256, 512-token chunks over a 2188-token prefix."""
+    run = PrefillRun(3, 0, 2048 + 140, Hq=32, Hkv=8, D=128)
+    worst = max(run.check(p, _rows(run.snap[p]["C"], (0, 5, 18, 31))) for p in run.snap)
+    print(f"prefill D128 worst rel-L2 {worst:.2e}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W", [(8, 8, 64, 700, 256, 128), (16, 2, 128, 900, 300, 256),
+                                                 (12, 4, 64, 650, 200, 128), (4, 4, 128, 300, 96, 128)])
+def test_prefill_shapes(Hq, Hkv, D, n, chunk, W):
+    """GQA groups 1, 8 and 3 (padded rows), D=64, ragged chunks, windows that wrap."""
+    run = PrefillRun(2, 1, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk)
+    for p in run.snap:
+        run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=19))
+
+
+def test_prefill_chunk_of_one_equals_decode():
+    """A one-token chunk is a decode step over the same cache."""
+    n = 128 * 3 + 40
+    run = PrefillRun(2, 2, n, Hq=8, Hkv=2, D=128, W=128, chunk=1, keep=[n - 1])
+    s = run.snap[n - 1]
+    dev = torch.device("cuda:0")
+    q = torch.from_numpy(run.q[n - 1:n]).to(dev)
+    dec = kvarn.decode_attention(q, run.tiles, run.table[None], torch.tensor([s["n_tiles"]],
+                                 dtype=torch.int32, device=dev),
+                                 torch.from_numpy(s["win_k"])[None].to(dev),
+                                 torch.from_numpy(s["win_v"])[None].to(dev),
+                                 torch.tensor([s["start"]], dtype=torch.int32, device=dev),
+                                 torch.tensor([s["length"]], dtype=torch.int32, device=dev),
+                                 run.lay).cpu().numpy()
+    for h in range(8):
+        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-3
+    run.check(n - 1, [(0, h) for h in range(8)])
+
+
+def test_prefill_config3_full_prompt_sampled():
+    """15,500 tokens = 30 x 512 + 140; every 64th row of the last chunk and a
+    middle chunk, two KV heads' query heads."""
+    n = 15500
+    run = PrefillRun(3, 3, n, Hq=32, Hkv=8, D=128, keep=[512 * 15, 512 * 30])
+    assert run.n_tiles == (n - 256) // 128 + 1
+    for p in run.snap:
+        C = run.snap[p]["C"]
+        rows = [(i, h) for i in list(range(0, C, 64)) + [C - 1] for h in (0, 3, 28, 31)]
+        w = run.check(p, rows)
+        print(f"15.5k chunk {p}: worst rel-L2 {w:.2e}")
