@@ -184,6 +184,93 @@ def run_reference(args, rank):
     print(json.dumps(out), flush=True)
 
 
+def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512, Wp=256, reps=3):
+    """One layer of config 3's prompt: per chunk append, promote, prefill
+    attention (tcgen05). Reports prompt tokens/s of the attention path scaled
+    to 36 layers, and the contraction throughput against the dense fp16
+    tensor peak (the algorithmic Q.K and P.V multiply-adds, counted once)."""
+    import torch
+    from kv_cache_quantization_token_gb300 import kvarn, synth
+    ks, vs = synth.kv_layer(3, 0, HKV, n_tok, D)
+    q = torch.from_numpy(synth.queries(3, 0, (n_tok, HQ, D))).to(dev)
+    kn_all = torch.from_numpy(np.ascontiguousarray(ks.transpose(1, 0, 2))).to(dev)  # [n][Hkv][D]
+    vn_all = torch.from_numpy(np.ascontiguousarray(vs.transpose(1, 0, 2))).to(dev)
+    rb = lay.record_bytes
+    cap = 128 * ((Wp - 1 + chunk + 127) // 128)
+    max_tiles = n_tok // 128 + 1
+    tiles = torch.empty(HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
+    tab = (np.arange(HKV)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
+    table = torch.from_numpy(tab.astype(np.int64)).to(dev)
+    dst_by_tile = [table[:, t].contiguous() for t in range(max_tiles)]
+    src_by_start = {s0: torch.tensor([h * cap + s0 for h in range(HKV)], dtype=torch.int64,
+                                     device=dev) for s0 in range(0, cap, 128)}
+    win_k = torch.zeros(1, HKV, cap, D, device=dev)
+    win_v = torch.zeros_like(win_k)
+    ws_start = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_len = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_nt = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(n_tok, HQ, D, device=dev)
+    ev = []
+
+    def prompt(record):
+        start = length = n_tiles = 0
+        ws_start.zero_()
+        ws_len.zero_()
+        ws_nt.zero_()
+        for pos0 in range(0, n_tok, chunk):
+            C = min(chunk, n_tok - pos0)
+            kvarn.append_window(kn_all[pos0:pos0 + C][None], vn_all[pos0:pos0 + C][None],
+                                win_k, win_v, ws_start, ws_len)
+            kvarn.window_advance(ws_start, ws_len, None, C, 0, cap)
+            length += C
+            while length >= Wp:
+                kvarn.compress_tile(win_k.view(-1, D), win_v.view(-1, D), src_by_start[start],
+                                    tiles, dst_by_tile[n_tiles], lay)
+                n_tiles += 1
+                start = (start + 128) % cap
+                length -= 128
+                kvarn.window_advance(ws_start, ws_len, ws_nt, 0, 1, cap)
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+            kvarn.prefill_attention(q[pos0:pos0 + C], pos0, tiles, table, n_tiles, win_k[0],
+                                    win_v[0], start, length, lay, out=out[pos0:pos0 + C])
+            if record:
+                b.record()
+                ev.append((a, b))
+
+    with torch.cuda.stream(stream):
+        prompt(False)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            prompt(False)
+        t1.record()
+        prompt(True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all().item(), "prefill produced non-finite output"
+    layer_ms = t0.elapsed_time(t1) / reps
+    attn_ms = float(sum(a.elapsed_time(b) for a, b in ev))
+    # algorithmic multiply-adds: every visible (query, key) pair, Q.K and P.V
+    vis = sum((p + 1) for p in range(n_tok))
+    macs = 2.0 * vis * HQ * D
+    tflops = 2.0 * macs / (attn_ms * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops", 1900.0))
+    return {"workload": f"config 3: {n_tok}-token prompt, {chunk}-token chunks, W={Wp}, "
+                        f"{HQ}q/{HKV}kv, head_dim {D}, causal; one layer",
+            "layer_ms": layer_ms, "attention_ms": attn_ms,
+            "prompt_tokens_per_s_36_layers": n_tok / (LAYERS * layer_ms * 1e-3),
+            "algorithmic_macs": macs, "achieved_tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": tflops / peak_tf, "traffic": None,
+                         "kernel": "prefill_kernel<128>",
+                         "peak_source": peak_kind + " (dense bf16 burst; fp16 runs at the bf16 rate)"},
+            "mma": "tcgen05 kind::f16, Q and K split hi+lo (3 MMAs for Q.K, 1 for P.V)"}
+
+
 def workload_config():
     return {"workload": f"Qwen3-8B-like KVarN decode attention: batch 1, {HQ}q/{HKV}kv heads, "
                         f"head_dim {D}, {LAYERS} layers of distinct caches at "
@@ -432,6 +519,9 @@ def main():
     trc = NCU_TRAFFIC["compress"]
     ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
 
+    # ---- chunked prefill (config 3: 15,500-token prompt, 512-token chunks, W=256)
+    prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleDecodeSample(32)
@@ -457,6 +547,7 @@ def main():
                                       "unit": "GB/s", "frac": comp_gbs / hbm,
                                       "traffic": ctraffic, "kernel": "compress_kernel<128>",
                                       "peak_source": peak_kind}},
+            "prefill": prefill,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
