@@ -12,7 +12,7 @@ Whenever the window reaches 128 tokens the oldest 128 are promoted (compressed
 into a tile) between replays, as the decode loop of the pages does with its
 promotion hoisted out of the graph.
 
-After the decode timing the bulk compression of config 2's 32k caches
+After the decode timing the bulk compression of 32k-token 8B-like caches
 (256 tiles x 8 KV heads = 2048 tile-heads per launch) is timed on its own.
 
 Prints one JSON line (see the keys at the end of main()).
@@ -37,16 +37,17 @@ if ROOT not in sys.path:
 METRIC = "KVarN decode-attn tokens/s & HBM GB/s at 16k ctx; tile-compress tiles/s"
 L2_BYTES = 129 * 1024 * 1024
 
-# Decode workload (Qwen3-8B-like, config 2 at 16k)
-CFG, HQ, HKV, D, LAYERS, CTX0, W = 2, 32, 8, 128, 36, 16384, 128
-# Compress bulk workload (config 2's 32k caches)
+# Decode workload: Qwen3-8B-like, batch 1, 32q/8kv heads, head_dim 128, 16k context
+WORKLOAD, HQ, HKV, D, LAYERS, CTX0, W = "qwen3_8b_decode", 32, 8, 128, 36, 16384, 128
+# Compress bulk workload: 32k-token caches of the same model, 8 KV heads
 C_TILES, C_HEADS = 256, 8
 
 # DRAM bytes per launch from an ncu capture, keyed by the kernel source they
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
     "decode_split": {"src_sha": None, "bytes": None},
-    "compress": {"src_sha": None, "bytes": None},
+    # 2 x (134.30 MB read + 5.99 MB written) for 1024 tile-heads, scaled to 2048
+    "compress": {"src_sha": "278c323257dc925a", "bytes": 280588800},
 }
 
 
@@ -132,11 +133,11 @@ class OracleDecodeSample:
         self.pool = ThreadPoolExecutor(self.threads)
         rb = oracle.record_bytes(D)
         self.table = (np.arange(n_tiles, dtype=np.int64) * rb)[None, None, :]
-        self.q = synth.queries(CFG, 0, (1, HQ, D))
+        self.q = synth.queries(WORKLOAD, 0, (1, HQ, D))
         n_tok = 128 * n_tiles
 
         def setup(h):
-            k, v = synth.kv_stream(CFG, 0, h, n_tok, D)
+            k, v = synth.kv_stream(WORKLOAD, 0, h, n_tok, D)
             return np.concatenate([oracle.compress_unit(k[128 * i:128 * i + 128],
                                                         v[128 * i:128 * i + 128])["record"]
                                    for i in range(n_tiles)])
@@ -185,14 +186,14 @@ def run_reference(args, rank):
 
 
 def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512, Wp=256, reps=3):
-    """One layer of config 3's prompt: per chunk append, promote, prefill
+    """One layer of the 15,500-token 8B-like prompt: per chunk append, promote, prefill
     attention (tcgen05). Reports prompt tokens/s of the attention path scaled
     to 36 layers, and the contraction throughput against the dense fp16
     tensor peak (the algorithmic Q.K and P.V multiply-adds, counted once)."""
     import torch
     from kv_cache_quantization_token_gb300 import kvarn, synth
-    ks, vs = synth.kv_layer(3, 0, HKV, n_tok, D)
-    q = torch.from_numpy(synth.queries(3, 0, (n_tok, HQ, D))).to(dev)
+    ks, vs = synth.kv_layer("qwen3_8b_prefill", 0, HKV, n_tok, D)
+    q = torch.from_numpy(synth.queries("qwen3_8b_prefill", 0, (n_tok, HQ, D))).to(dev)
     kn_all = torch.from_numpy(np.ascontiguousarray(ks.transpose(1, 0, 2))).to(dev)  # [n][Hkv][D]
     vn_all = torch.from_numpy(np.ascontiguousarray(vs.transpose(1, 0, 2))).to(dev)
     rb = lay.record_bytes
@@ -259,7 +260,7 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
     macs = 2.0 * vis * HQ * D
     tflops = 2.0 * macs / (attn_ms * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", 1900.0))
-    return {"workload": f"config 3: {n_tok}-token prompt, {chunk}-token chunks, W={Wp}, "
+    return {"workload": f"Qwen3-8B-like chunked prefill: {n_tok}-token prompt, {chunk}-token chunks, W={Wp}, "
                         f"{HQ}q/{HKV}kv, head_dim {D}, causal; one layer",
             "layer_ms": layer_ms, "attention_ms": attn_ms,
             "prompt_tokens_per_s_36_layers": n_tok / (LAYERS * layer_ms * 1e-3),
@@ -327,7 +328,7 @@ def main():
     win_v = torch.zeros_like(win_k)
     n0 = CTX0 // 128
     for l in range(LAYERS):
-        ks, vs = synth.kv_layer(CFG, l, HKV, CTX0 + w0, D)
+        ks, vs = synth.kv_layer(WORKLOAD, l, HKV, CTX0 + w0, D)
         base = (l * HKV) * max_tiles
         tab = (base + np.arange(HKV)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
         table[l, 0] = torch.from_numpy(tab.astype(np.int64))
@@ -342,9 +343,9 @@ def main():
     win_start = torch.zeros(B, dtype=torch.int32, device=dev)
     win_len = torch.full((B,), w0, dtype=torch.int32, device=dev)
     n_tiles = torch.full((B,), n0, dtype=torch.int32, device=dev)
-    q = torch.from_numpy(synth.queries(CFG, 0, (LAYERS, B, HQ, D))).to(dev)
-    kn = torch.from_numpy(synth.queries(CFG, 1, (LAYERS, B, 1, HKV, D))).to(dev)
-    vn = torch.from_numpy(synth.queries(CFG, 2, (LAYERS, B, 1, HKV, D))).to(dev)
+    q = torch.from_numpy(synth.queries(WORKLOAD, 0, (LAYERS, B, HQ, D))).to(dev)
+    kn = torch.from_numpy(synth.queries(WORKLOAD, 1, (LAYERS, B, 1, HKV, D))).to(dev)
+    vn = torch.from_numpy(synth.queries(WORKLOAD, 2, (LAYERS, B, 1, HKV, D))).to(dev)
     out = torch.empty(LAYERS, B, HQ, D, device=dev)
     ws = torch.empty(kvarn.decode_workspace_bytes(B, HQ, HKV, D, max_tiles, cap) + 256,
                      dtype=torch.uint8, device=dev)
@@ -493,9 +494,9 @@ def main():
     e2e_tps = world * B * e2e_steps / (e0.elapsed_time(e1) / 1000.0)
     assert np.isfinite(out_h.numpy()).all(), "decode produced non-finite output"
 
-    # ---- compress bulk (config 2's 32k caches) ------------------------------
+    # ---- compress bulk (32k-token 8B-like caches) ------------------------------
     n_units = C_TILES * C_HEADS
-    ks, vs = synth.kv_layer(CFG, 99, C_HEADS, 128 * C_TILES, D)
+    ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * C_TILES, D)
     ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
     cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
     del ks, vs
@@ -519,7 +520,7 @@ def main():
     trc = NCU_TRAFFIC["compress"]
     ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
 
-    # ---- chunked prefill (config 3: 15,500-token prompt, 512-token chunks, W=256)
+    # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256)
     prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
 
     cpu = None

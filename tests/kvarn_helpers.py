@@ -80,9 +80,9 @@ def n_tiles_for(ctx: int, W: int) -> int:
 class Cache:
     """A batch of KVarN caches built on the GPU through the C ABI."""
 
-    def __init__(self, cfg, layer, ctxs, Hkv, D, W=128, cap=None, win_start=None, dev="cuda:0",
+    def __init__(self, workload, layer, ctxs, Hkv, D, W=128, cap=None, win_start=None, dev="cuda:0",
                  iters=4):
-        self.cfg, self.layer, self.Hkv, self.D, self.W = cfg, layer, Hkv, D, W
+        self.workload, self.layer, self.Hkv, self.D, self.W = workload, layer, Hkv, D, W
         self.dev = torch.device(dev)
         self.B = len(ctxs)
         self.ctxs = list(ctxs)
@@ -93,7 +93,7 @@ class Cache:
         self.wl = [c - TILE * n for c, n in zip(ctxs, self.nt)]
         self.cap = cap if cap is not None else max(W, TILE * ((max(self.wl) + TILE - 1) // TILE), TILE)
         starts = win_start if win_start is not None else [0] * self.B
-        kv = [synth.kv_layer(cfg, layer + 1000 * b, Hkv, c, D) for b, c in enumerate(ctxs)]
+        kv = [synth.kv_layer(workload, layer + 1000 * b, Hkv, c, D) for b, c in enumerate(ctxs)]
         self.k = [x[0] for x in kv]
         self.v = [x[1] for x in kv]
         # compress every full tile of every (sequence, head) in one launch
@@ -162,12 +162,12 @@ class PrefillRun:
     chunks listed in `keep`, a copy of the window and the outputs so the
     oracle can be evaluated on the same state."""
 
-    def __init__(self, cfg, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
+    def __init__(self, workload, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
                  dev="cuda:0", scale=None):
         dev = torch.device(dev)
         self.Hq, self.Hkv, self.D, self.W = Hq, Hkv, D, W
-        self.k, self.v = synth.kv_layer(cfg, layer, Hkv, n_tokens, D)
-        self.q = synth.queries(cfg, layer, (n_tokens, Hq, D))
+        self.k, self.v = synth.kv_layer(workload, layer, Hkv, n_tokens, D)
+        self.q = synth.queries(workload, layer, (n_tokens, Hq, D))
         self.lay = kvarn.layout(D)
         rb = self.rb = self.lay.record_bytes
         self.cap = cap = TILE * ((W - 1 + chunk + TILE - 1) // TILE)

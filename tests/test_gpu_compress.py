@@ -32,11 +32,11 @@ def _compress(k_rows, v_rows, units, D, iters=4, row_stride=None):
     return [host[s * rb:(s + 1) * rb] for s in slots]
 
 
-@pytest.mark.parametrize("cfg,D,n_heads,n_tiles", [(0, 128, 1, 1), (1, 128, 2, 4), (2, 128, 2, 4),
-                                                    (4, 256, 2, 3), (2, 64, 2, 3), (0, 64, 1, 2),
-                                                    (4, 128, 1, 2)])
-def test_compress_matches_oracle(cfg, D, n_heads, n_tiles):
-    ks, vs = synth.kv_layer(cfg, 3, n_heads, 128 * n_tiles, D)
+@pytest.mark.parametrize("workload,D,n_heads,n_tiles", [("single_tile", 128, 1, 1), ("qwen3_0p6b_decode", 128, 2, 4), ("qwen3_8b_decode", 128, 2, 4),
+                                                    ("batched_d256_decode", 256, 2, 3), ("qwen3_8b_decode", 64, 2, 3), ("single_tile", 64, 1, 2),
+                                                    ("batched_d256_decode", 128, 1, 2)])
+def test_compress_matches_oracle(workload, D, n_heads, n_tiles):
+    ks, vs = synth.kv_layer(workload, 3, n_heads, 128 * n_tiles, D)
     k_rows, v_rows = ks.reshape(-1, D), vs.reshape(-1, D)
     units = [128 * i for i in range(n_heads * n_tiles)]
     recs = _compress(k_rows, v_rows, units, D)
@@ -46,12 +46,12 @@ def test_compress_matches_oracle(cfg, D, n_heads, n_tiles):
         st = compare_record(rec, ref, D)
         flips += st["band_flips"]
         total += st["codes"]
-    print(f"cfg{cfg} D{D}: {flips} boundary-band flips of {total} codes")
+    print(f"{workload} D{D}: {flips} boundary-band flips of {total} codes")
 
 
 def test_compress_strided_rows_and_offsets():
     D = 128
-    ks, vs = synth.kv_layer(2, 5, 1, 128 * 3 + 40, D)
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 5, 1, 128 * 3 + 40, D)
     k_rows, v_rows = ks[0], vs[0]
     units = [0, 40, 128 + 40, 256]  # overlapping and unaligned-to-128 starts
     recs = _compress(k_rows, v_rows, units, D, row_stride=D + 8)
@@ -62,7 +62,7 @@ def test_compress_strided_rows_and_offsets():
 @pytest.mark.parametrize("iters", [1, 2, 7])
 def test_compress_other_iteration_counts(iters):
     D = 128
-    ks, vs = synth.kv_layer(0, 2, 1, 256, D)
+    ks, vs = synth.kv_layer("single_tile", 2, 1, 256, D)
     recs = _compress(ks[0], vs[0], [0, 128], D, iters=iters)
     for u, rec in zip([0, 128], recs):
         compare_record(rec, oracle.compress_unit(ks[0, u:u + 128], vs[0, u:u + 128], iters), D)
@@ -89,7 +89,7 @@ def test_compress_degenerate_tiles(D):
 
 def test_compress_is_deterministic_and_schedule_independent():
     D = 128
-    ks, vs = synth.kv_layer(2, 9, 1, 128 * 8, D)
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 9, 1, 128 * 8, D)
     units = [128 * i for i in range(8)]
     a = _compress(ks[0], vs[0], units, D)
     b = _compress(ks[0], vs[0], units[::-1], D)[::-1]

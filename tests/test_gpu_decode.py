@@ -12,7 +12,7 @@ DEV = "cuda:0"
 
 
 def _check(cache, Hq, heads=None, scale=None, seed=0):
-    q = synth.queries(cache.cfg, seed, (cache.B, Hq, cache.D))
+    q = synth.queries(cache.workload, seed, (cache.B, Hq, cache.D))
     out = cache.decode(torch.from_numpy(q).to(DEV), scale=scale).cpu().numpy()
     ref = cache.oracle_decode(q, heads=heads, scale=scale)
     worst = 0.0
@@ -23,57 +23,57 @@ def _check(cache, Hq, heads=None, scale=None, seed=0):
     return out, worst
 
 
-def test_config0_one_tile_plus_17_window():
-    c = Cache(0, 0, [128 + 17], Hkv=1, D=128)
+def test_single_tile_plus_17_window():
+    c = Cache("single_tile", 0, [128 + 17], Hkv=1, D=128)
     _check(c, Hq=1)
 
 
 @pytest.mark.parametrize("w", [0, 1, 127, 77])
-def test_config1_qwen06b_like(w):
+def test_qwen3_0p6b_like_3k(w):
     """16q/8kv, D=128, 3072 + w tokens (24 tiles + w-token window)."""
-    c = Cache(1, 4, [3072 + w], Hkv=8, D=128)
+    c = Cache("qwen3_0p6b_decode", 4, [3072 + w], Hkv=8, D=128)
     _check(c, Hq=16, heads=[(0, h) for h in (0, 5, 10, 15)])
 
 
 @pytest.mark.parametrize("ctx", [4096, 4096 + 77])
-def test_config2_qwen8b_like(ctx):
-    c = Cache(2, 1, [ctx], Hkv=8, D=128)
+def test_qwen3_8b_like(ctx):
+    c = Cache("qwen3_8b_decode", 1, [ctx], Hkv=8, D=128)
     _check(c, Hq=32, heads=[(0, h) for h in (0, 3, 17, 31)])
 
 
-def test_config2_16k_sampled_heads():
-    c = Cache(2, 2, [16384], Hkv=8, D=128)
+def test_qwen3_8b_like_16k_sampled_heads():
+    c = Cache("qwen3_8b_decode", 2, [16384], Hkv=8, D=128)
     _check(c, Hq=32, heads=[(0, 0), (0, 13), (0, 30)])
 
 
-def test_config4_ragged_batch_d256():
+def test_ragged_batch32_d256():
     ctxs = [900, 128 * 5 + 3, 256, 1500]
-    c = Cache(4, 0, ctxs, Hkv=4, D=256)
+    c = Cache("batched_d256_decode", 0, ctxs, Hkv=4, D=256)
     _check(c, Hq=16, heads=[(b, h) for b in range(4) for h in (0, 7, 15)])
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (24, 8), (8, 1)])
 def test_gqa_groups(Hq, Hkv):
     """G = 1, 3 (padded group of 4) and 8."""
-    c = Cache(2, 6, [600], Hkv=Hkv, D=128)
+    c = Cache("qwen3_8b_decode", 6, [600], Hkv=Hkv, D=128)
     _check(c, Hq=Hq)
 
 
 def test_d64_and_window_wraparound():
-    c = Cache(0, 7, [128 * 3 + 200], Hkv=2, D=64, W=256, cap=384, win_start=[256])
+    c = Cache("single_tile", 7, [128 * 3 + 200], Hkv=2, D=64, W=256, cap=384, win_start=[256])
     assert c.wl == [200] and c.cap == 384
     _check(c, Hq=4)
 
 
 def test_empty_and_window_only_and_tiles_only():
-    c = Cache(2, 8, [0, 50, 256, 128], Hkv=2, D=128)
+    c = Cache("qwen3_8b_decode", 8, [0, 50, 256, 128], Hkv=2, D=128)
     out, _ = _check(c, Hq=4)
     assert np.all(out[0] == 0.0)
 
 
 def test_custom_scale_and_determinism():
-    c = Cache(2, 9, [1000], Hkv=2, D=128)
-    q = torch.from_numpy(synth.queries(2, 1, (1, 8, 128))).to(DEV)
+    c = Cache("qwen3_8b_decode", 9, [1000], Hkv=2, D=128)
+    q = torch.from_numpy(synth.queries("qwen3_8b_decode", 1, (1, 8, 128))).to(DEV)
     a = c.decode(q, scale=0.3)
     b = c.decode(q, scale=0.3)
     assert torch.equal(a, b)

@@ -15,9 +15,9 @@ def _rows(C, heads, step=37):
     return [(i, h) for i in idx if i < C for h in heads]
 
 
-def test_prefill_config3_prefix_chunks():
+def test_prefill_15k_prompt_prefix_chunks():
     """32q/8kv, D=128, W=256, 512-token chunks over a 2188-token prefix."""
-    run = PrefillRun(3, 0, 2048 + 140, Hq=32, Hkv=8, D=128)
+    run = PrefillRun("qwen3_8b_prefill", 0, 2048 + 140, Hq=32, Hkv=8, D=128)
     worst = max(run.check(p, _rows(run.snap[p]["C"], (0, 5, 18, 31))) for p in run.snap)
     print(f"prefill D128 worst rel-L2 {worst:.2e}")
 
@@ -26,7 +26,7 @@ def test_prefill_config3_prefix_chunks():
                                                  (12, 4, 64, 650, 200, 128), (4, 4, 128, 300, 96, 128)])
 def test_prefill_shapes(Hq, Hkv, D, n, chunk, W):
     """GQA groups 1, 8 and 3 (padded rows), D=64, ragged chunks, windows that wrap."""
-    run = PrefillRun(2, 1, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk)
+    run = PrefillRun("qwen3_8b_decode", 1, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk)
     for p in run.snap:
         run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=19))
 
@@ -34,7 +34,7 @@ def test_prefill_shapes(Hq, Hkv, D, n, chunk, W):
 def test_prefill_chunk_of_one_equals_decode():
     """A one-token chunk is a decode step over the same cache."""
     n = 128 * 3 + 40
-    run = PrefillRun(2, 2, n, Hq=8, Hkv=2, D=128, W=128, chunk=1, keep=[n - 1])
+    run = PrefillRun("qwen3_8b_decode", 2, n, Hq=8, Hkv=2, D=128, W=128, chunk=1, keep=[n - 1])
     s = run.snap[n - 1]
     dev = torch.device("cuda:0")
     q = torch.from_numpy(run.q[n - 1:n]).to(dev)
@@ -50,11 +50,11 @@ def test_prefill_chunk_of_one_equals_decode():
     run.check(n - 1, [(0, h) for h in range(8)])
 
 
-def test_prefill_config3_full_prompt_sampled():
+def test_prefill_15k_prompt_full_sampled():
     """15,500 tokens = 30 x 512 + 140; every 64th row of the last chunk and a
     middle chunk, two KV heads' query heads."""
     n = 15500
-    run = PrefillRun(3, 3, n, Hq=32, Hkv=8, D=128, keep=[512 * 15, 512 * 30])
+    run = PrefillRun("qwen3_8b_prefill", 3, n, Hq=32, Hkv=8, D=128, keep=[512 * 15, 512 * 30])
     assert run.n_tiles == (n - 256) // 128 + 1
     for p in run.snap:
         C = run.snap[p]["C"]

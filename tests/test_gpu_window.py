@@ -14,7 +14,7 @@ DEV = "cuda:0"
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_rotate_query_matches_oracle(D):
-    q = synth.queries(2, 0, (3, 5, D))
+    q = synth.queries("qwen3_8b_decode", 0, (3, 5, D))
     got = kvarn.rotate_query(torch.from_numpy(q).to(DEV)).cpu().numpy()
     want = oracle.wht_rows(q.reshape(-1, D).astype(np.float64)).reshape(q.shape)
     assert np.max(np.abs(got - want)) <= 1e-5 * np.max(np.abs(want))
@@ -45,7 +45,7 @@ def test_state_machine_through_the_abi(W, chunk):
     the oracle state machine's within the rounding band, for any chunking."""
     D, hkv, n = 64, 2, 700
     cap = 128 * ((W + chunk + 127) // 128)
-    ks, vs = synth.kv_layer(0, 11, hkv, n, D)
+    ks, vs = synth.kv_layer("single_tile", 11, hkv, n, D)
     lay = kvarn.layout(D)
     rb = lay.record_bytes
     wk = torch.zeros(1, hkv, cap, D, device=DEV)

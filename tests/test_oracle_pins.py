@@ -89,7 +89,7 @@ def test_sinkhorn_channel_step_comes_first(oracle):
     then any positive per-channel scaling of Y is absorbed by s exactly and
     leaves r and Yn unchanged at every iteration count. With the token step
     first this only holds in the limit."""
-    k, _ = synth.kv_stream(0, 1, 0, 128, 128)
+    k, _ = synth.kv_stream("single_tile", 1, 0, 128, 128)
     Y = oracle.wht_rows(k.astype(np.float64))
     b = np.exp(np.random.default_rng(5).standard_normal(128))
     for iters in (1, 2, 4):
@@ -100,12 +100,12 @@ def test_sinkhorn_channel_step_comes_first(oracle):
         np.testing.assert_allclose(y1, y0, atol=1e-12)
 
 
-@pytest.mark.parametrize("cfg,D", [(0, 128), (2, 128), (4, 256), (2, 64)])
-def test_sinkhorn_normalises_rows_and_converges_on_columns(oracle, cfg, D):
+@pytest.mark.parametrize("workload,D", [("single_tile", 128), ("qwen3_8b_decode", 128), ("batched_d256_decode", 256), ("qwen3_8b_decode", 64)])
+def test_sinkhorn_normalises_rows_and_converges_on_columns(oracle, workload, D):
     """After the last (token) step every token std of Yn is 1; the worst
     channel |ln std| never grows with more rounds and is below 0.05 at n = 4
     on the synthetic workloads' distributions."""
-    k, v = synth.kv_stream(cfg, 2, 1, 128, D)
+    k, v = synth.kv_stream(workload, 2, 1, 128, D)
     for x in (k, v):
         Y = oracle.wht_rows(x.astype(np.float64))
         prev = np.inf
@@ -122,7 +122,7 @@ def test_sinkhorn_normalises_rows_and_converges_on_columns(oracle, cfg, D):
 
 def test_sinkhorn_global_scale_moves_only_s(oracle):
     """Y -> cY: s -> c s, r and Yn unchanged (the channel step sees c first)."""
-    _, v = synth.kv_stream(2, 0, 3, 128, 128)
+    _, v = synth.kv_stream("qwen3_8b_decode", 0, 3, 128, 128)
     Y = oracle.wht_rows(v.astype(np.float64))
     s0, r0, y0 = oracle.sinkhorn(Y, 4)
     s1, r1, y1 = oracle.sinkhorn(3.7 * Y, 4)
@@ -224,13 +224,13 @@ def test_pack_bit_order_hand_built(oracle):
 
 
 # --------------------------------------------------------- c5: reconstruction
-@pytest.mark.parametrize("cfg,D", [(0, 128), (2, 128), (4, 256), (2, 64)])
-def test_compress_dequant_distortion_bound(oracle, cfg, D):
+@pytest.mark.parametrize("workload,D", [("single_tile", 128), ("qwen3_8b_decode", 128), ("batched_d256_decode", 256), ("qwen3_8b_decode", 64)])
+def test_compress_dequant_distortion_bound(oracle, workload, D):
     """Per element of the rotated tile |Yn r s - recon| <= r s delta / 2, so by
     orthonormality each unrotated row error is at most the norm of those
     bounds. Pins compress and dequant against each other: a swapped factor,
     a wrong group index or a missing inverse rotation breaks it."""
-    k, v = synth.kv_stream(cfg, 0, 0, 128, D)
+    k, v = synth.kv_stream(workload, 0, 0, 128, D)
     o = oracle.compress_unit(k, v)
     kh, vh = oracle.dequant_record(o["record"], D)
     gv = D // min(D, 128)
@@ -248,7 +248,7 @@ def test_fold_identity(oracle):
     q . (H K~_t) = r_t (sum_c q'_c s_c delta_c code_tc + sum_c q'_c s_c lo_c)
     with q' = H q. The explicit dequantisation is on the left."""
     D = 128
-    k, v = synth.kv_stream(2, 0, 0, 128, D)
+    k, v = synth.kv_stream("qwen3_8b_decode", 0, 0, 128, D)
     rec = oracle.compress_unit(k, v)["record"]
     kh, _ = oracle.dequant_record(rec, D)
     u = oracle.unpack_record(rec, D)
@@ -261,7 +261,7 @@ def test_fold_identity(oracle):
 
 def test_compress_invariant_to_global_scale(oracle):
     """X -> cX (c > 0) leaves every code unchanged and moves only s."""
-    k, v = synth.kv_stream(2, 3, 0, 128, 128)
+    k, v = synth.kv_stream("qwen3_8b_decode", 3, 0, 128, 128)
     a = oracle.compress_unit(k, v)
     b = oracle.compress_unit(k * np.float32(4.0), v * np.float32(0.25))
     ua, ub = oracle.unpack_record(a["record"], 128), oracle.unpack_record(b["record"], 128)
@@ -286,7 +286,7 @@ def test_rechunking_gives_identical_tiles(oracle, W):
     """PR #434 commit 99c3773 and issue #433 item 1: tiles do not depend on the
     chunking. Chunk sizes 1, 17 and 512 over 700 tokens."""
     Hkv, D, n = 2, 64, 700
-    ks, vs = synth.kv_layer(0, 0, Hkv, n, D)
+    ks, vs = synth.kv_layer("single_tile", 0, Hkv, n, D)
     k_tok, v_tok = ks.transpose(1, 0, 2), vs.transpose(1, 0, 2)
     results = []
     for chunk in (1, 17, 512):
@@ -328,7 +328,7 @@ def test_attend_special_cases(oracle):
 def test_decode_independent_of_tile_order(oracle):
     """Permuting the order of tiles in the table leaves the output unchanged."""
     D, n_t = 64, 3
-    k, v = synth.kv_stream(0, 0, 0, 128 * n_t + 5, D)
+    k, v = synth.kv_stream("single_tile", 0, 0, 128 * n_t + 5, D)
     pool = np.concatenate([oracle.compress_unit(k[128 * i:128 * i + 128],
                                                 v[128 * i:128 * i + 128])["record"]
                            for i in range(n_t)])
@@ -336,7 +336,7 @@ def test_decode_independent_of_tile_order(oracle):
     win_k = np.zeros((1, 1, 128, D), np.float32)
     win_v = np.zeros((1, 1, 128, D), np.float32)
     win_k[0, 0, :5], win_v[0, 0, :5] = k[-5:], v[-5:]
-    q = synth.queries(0, 0, (1, 1, D))
+    q = synth.queries("single_tile", 0, (1, 1, D))
     outs = []
     for perm in ([0, 1, 2], [2, 0, 1]):
         table = (np.array(perm, np.int64) * rb)[None, None, :]
@@ -349,8 +349,8 @@ def test_prefill_chunk_of_one_equals_decode(oracle):
     """c8: causal prefill restricted to a single query is decode (c7) at that
     step; query i of a chunk sees exactly pos0 + i + 1 tokens."""
     Hkv, Hq, D, n = 1, 2, 64, 300
-    ks, vs = synth.kv_layer(2, 0, Hkv, n, D)
-    qs = synth.queries(2, 0, (n, Hq, D))
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 0, Hkv, n, D)
+    qs = synth.queries("qwen3_8b_decode", 0, (n, Hq, D))
     sm = oracle.CacheStateMachine(Hkv, D, W=128)
     rb = oracle.record_bytes(D)
     full_chunk = None

@@ -20,9 +20,9 @@ DEV = "cuda:0"
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    c = Cache(2, 21, [2000, 777], Hkv=8, D=128)
+    c = Cache("qwen3_8b_decode", 21, [2000, 777], Hkv=8, D=128)
     for call in range(2):  # the scratch keeps the previous call's contents
-        q = torch.from_numpy(synth.queries(2, 40 + call, (2, 32, 128))).to(DEV)
+        q = torch.from_numpy(synth.queries("qwen3_8b_decode", 40 + call, (2, 32, 128))).to(DEV)
         want = c.decode(q).cpu().numpy()
         got = kvarn.decode_attention_noalloc(q, c.tiles, c.tile_table, c.n_tiles, c.win_k,
                                              c.win_v, c.win_start, c.win_len, c.lay)
