@@ -217,8 +217,10 @@ int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
  * reconstructed as described at kvarn_layout_t) and then the window's raw rows.
  *   q          : fp32 [B][Hq][D], unrotated. Hq / Hkv = G must be 1..8.
  *   tiles      : u8 base of the record pool.
- *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets (multiples of
- *                16; an unaligned offset makes that head's output NaN);
+ *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets, multiples of
+ *                128 (record_bytes is a multiple of 1024, so a pool of whole
+ *                records qualifies; another offset makes that head's output
+ *                NaN);
  *                entries at or past n_tiles[b] are never read.
  *   n_tiles    : int32 [B], 0 <= n_tiles[b] <= max_tiles (clamped on device).
  *   win_k/v    : fp32 [B][Hkv][win_capacity][D]; win_start/win_len int32 [B]

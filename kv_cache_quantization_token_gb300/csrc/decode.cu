@@ -5,12 +5,15 @@
 // the deferred inverse WHT is applied after combining the rotated partials):
 //
 //   split kernel   grid (item, KV head, sequence), 4 warps per CTA. Items
-//                  0..tile_items-1 own TPS consecutive packed tiles: the four
-//                  warps share each tile, the scores and the value aggregate
-//                  run as mma.sync m16n8k16 contractions whose A fragments
-//                  are built straight from the packed codes. The remaining
-//                  items own 4 chunks of FP32 window rows (raw rows,
-//                  unrotated query), one per warp, staged by bulk copies.
+//                  0..tile_items-1 own TPS consecutive packed tiles, staged in
+//                  shared memory by bulk async copies. Warp w takes tokens
+//                  32w..32w+31 of every tile: the score and value contractions
+//                  run as mma.sync m16n8k16 with A fragments built straight
+//                  from the packed codes; the warps share only the folded
+//                  query (one named barrier per tile) and keep their own
+//                  streaming-softmax state, merged once per item. The
+//                  remaining items own 4 chunks of FP32 window rows (raw rows,
+//                  unrotated query), one per warp.
 //   combine kernel grid (query head, sequence): LSE merge of the items, one
 //                  inverse rotation of the merged tile accumulator, plus the
 //                  (unrotated) window accumulator, divided by the softmax sum.
@@ -22,10 +25,13 @@
 // and the value aggregate stays in the rotated space:
 //   acc_c = s_c * (sum_t p_t r_t delta_tg code_tc + sum_t p_t r_t lo_tg).
 // Every query head of a KV head's GQA group is served from one pass over the
-// packed codes. Records are staged in shared memory with bulk async copies
-// (cp.async.bulk, mbarrier completion); every wait is bounded.
+// packed codes. Every wait on a copy is bounded.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "kvarn_common.cuh"
 
@@ -112,11 +118,6 @@ __device__ __forceinline__ float warp_reduce_rows(float (&v)[N], int lane) {
   return r;
 }
 
-// exact small-integer to float: the code sits in the mantissa of 2^23
-__device__ __forceinline__ float code_f(uint32_t c) {
-  return __int_as_float((int)(c | 0x4B000000u)) - 8388608.0f;
-}
-
 // One warp rotates one query head: x = scale/sqrt(D) * H q, written to
 // qs[c * GP + h]. Heads h >= G (padding of the GQA group) are zero.
 template <int D, int GP>
@@ -159,11 +160,6 @@ __device__ __forceinline__ void rotate_head_to_smem(const float* qh, bool valid,
 //          sum_t pd_t code_tc = 4 (O - sum_t pd_t)
 // Columns n are (query head, hi/lo part) pairs, 8 per n-tile. Each B operand is
 // scaled by a power of two per head (exact) so the fp16 parts stay in range.
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -172,14 +168,38 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// {fp16(1 + n_a/16), fp16(1 + n_b/16)} from byte `byte` of words wa, wb; the
-// nibble is the low one when sh == 6 and the high one when sh == 2.
-__device__ __forceinline__ uint32_t nib_pair(uint32_t wa, uint32_t wb, uint32_t sel, int sh) {
-  return ((prmt(wa, wb, sel) << sh) & 0x03C003C0u) | 0x3C003C00u;
+// fp16 pair {1 + c_lo/16, 1 + c_hi/16} from nibble j of the low and of the high
+// 16-bit half of x (the code sits in mantissa bits 9..6).
+__device__ __forceinline__ uint32_t k_frag(uint32_t x, int j) {
+  const uint32_t y = j == 0 ? (x << 6) : j == 1 ? (x << 2) : j == 2 ? (x >> 2) : (x >> 6);
+  return (y & 0x03C003C0u) | 0x3C003C00u;
 }
-// {fp16(1 + c_a/4), fp16(1 + c_b/4)}: 2-bit fields at bit `2*f` of the selected bytes.
-__device__ __forceinline__ uint32_t crumb_pair(uint32_t wa, uint32_t wb, uint32_t sel, int sh) {
-  return ((prmt(wa, wb, sel) << sh) & 0x03000300u) | 0x3C003C00u;
+// fp16 pair {1 + c_lo/4, 1 + c_hi/4} from 2-bit field m of each 16-bit half of x
+// (the code sits in mantissa bits 9..8).
+__device__ __forceinline__ uint32_t v_frag(uint32_t x, int m) {
+  const uint32_t y = m < 4 ? (x << (8 - 2 * m)) : (x >> (2 * m - 8));
+  return (y & 0x03000300u) | 0x3C003C00u;
+}
+// Physical offset of logical byte o of a 1024-byte aligned region written by a
+// TMA copy with 128-byte swizzling (16-byte chunk index XOR 128-byte line index).
+__device__ __forceinline__ uint32_t swz128(uint32_t o) { return o ^ (((o >> 7) & 7u) << 4); }
+// Four 8x8 matrices of 16-bit elements, transposed: lanes 8i..8i+7 give the
+// row addresses of matrix i, whose fragment lands in r[i].
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+// 2D tensor copy (box of the tensor map) into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 // Packed fp16 pair of the hi (odd == false) or lo parts of (x0, x1): x = hi + lo
 // to about 22 bits.
@@ -203,30 +223,103 @@ __device__ __forceinline__ void pow2_scale(float m, float k, float& scale, float
   inv_k = k * __int_as_float((127 - e) << 23);
 }
 
+// Transposes an 8x8 matrix of 16-bit pairs held one row pair per lane (lane
+// 4g + q holds row g, columns 2q and 2q+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// Barrier 1 among the n threads of the CTA that execute it (barrier 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int n) {
+  asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
+// {fp16(x), fp16(x - fp16(x))} packed low/high; adds the value the pair represents to sum.
+__device__ __forceinline__ uint32_t hilo_one(float x, float& sum) {
+  const __half h = __float2half_rn(x);
+  const float hf = __half2float(h);
+  const __half l = __float2half_rn(x - hf);
+  sum += hf + __half2float(l);
+  const __half2 r = __halves2half2(h, l);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// One warp rotates one query head for the tile path: x = f / sqrt(D) * H q,
+// stored as channel pairs interleaved by head (qs[((c/2) * GP + h) * 2 + c % 2])
+// so that the lanes of a fragment read their pairs without bank conflicts,
+// plus max_c |x_c| in qmax[h].
+template <int D, int GP>
+__device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, float f_scale,
+                                                  float* qs, float* qmax, int h, int lane) {
+  constexpr int E = D / 32;
+  float x[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] = valid ? qh[lane * E + e] : 0.f;
+#pragma unroll
+  for (int s = 1; s < E; s <<= 1)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (!(e & s)) {
+        const float a = x[e], b = x[e | s];
+        x[e] = a + b;
+        x[e | s] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool up = lane & m;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = up ? (o - x[e]) : (x[e] + o);
+    }
+  }
+  const float f = f_scale / sqrtf((float)D);
+  float mx = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const int c = lane * E + e;
+    const float2 v = make_float2(x[e] * f, x[e + 1] * f);
+    *reinterpret_cast<float2*>(qs + ((c >> 1) * GP + h) * 2) = v;
+    mx = fmaxf(mx, fmaxf(fabsf(v.x), fabsf(v.y)));
+  }
+  mx = warp_max(mx);
+  if (lane == 0) qmax[h] = mx;
+}
+
 template <int D, int GP, int TPS>
 struct DC {
   static constexpr int NW = 4;                                  // warps per CTA
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
+  static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
+  static constexpr int CODE_BYTES = 96 * D;                     // K + V codes, one TMA box
+  static constexpr int CODE_LINES = CODE_BYTES / 128;           // 128-byte lines of that box
   static constexpr int NT = GP > 4 ? 2 : 1;                     // n8-tiles of (head, part) columns
   static constexpr int NCB = D / 16;                            // 16-channel blocks
-  static constexpr int CBA = NCB / NW;                          // channel blocks per warp (phase A)
+  static constexpr int CBA = NCB / NW;                          // blocks whose B fragments a warp builds
   // window rows staged per warp (K and V rows of one chunk fit the record region)
   static constexpr int WCH0 = (TPS * RB) / (NW * 2 * D * 4);
   static constexpr int WCH = WCH0 >= 16 ? 16 : WCH0 >= 8 ? 8 : WCH0 >= 4 ? 4 : 2;
-  static constexpr int OFF_SC = TPS * RB;                       // f32 [TPS][128][GP]
-  static constexpr int OFF_QS = OFF_SC + TPS * 128 * GP * 4;    // f32 [D][GP] query
-  // score shares [TPS][NW][128][GP]; reused for the value partials [NW][GP][D]
-  static constexpr int PART = (TPS * NW * 128 * GP > NW * GP * D ? TPS * NW * 128 * GP : NW * GP * D) * 4;
-  static constexpr int OFF_PART = OFF_QS + D * GP * 4;
-  static constexpr int OFF_RED = OFF_PART + PART;               // f32 reduction scratch [NW][32]
+  static constexpr int DP = D + 8;                              // padded channel stride of the merge
+  static constexpr int MRG = NW * GP * DP * 4;                  // merge region [NW][GP][DP], over records
+  static constexpr int REC_REGION = TPS * RB > MRG ? TPS * RB : MRG;
+  static constexpr int OFF_QS = (REC_REGION + 15) / 16 * 16;    // f32 query [D/2][GP][2] (window: [D][GP])
+  static constexpr int OFF_QMAX = OFF_QS + D * GP * 4;          // f32 [8]
+  static constexpr int OFF_BX = OFF_QMAX + 32;                  // B fragments [2][NCB][NT][32] x u32x2
+  static constexpr int BX = 2 * NCB * NT * 32 * 8;              //   (window items: scores [4 WCH][GP])
+  static constexpr int OFF_PT = OFF_BX + BX;                    // per-warp (sum wd, bias) [2][NW][GP]
+  static constexpr int OFF_RED = OFF_PT + 2 * NW * GP * 8;      // f32 reduction scratch [NW][32]
   static constexpr int OFF_FLG = OFF_RED + NW * 32 * 4;         // int [TPS]
+  static constexpr int NBAR = TPS > NW ? TPS : NW;               // one per tile, or per window chunk
   static constexpr int OFF_BAR = (OFF_FLG + TPS * 4 + 7) / 8 * 8;
-  static constexpr int SMEM = (OFF_BAR + TPS * 8 + 15) / 16 * 16;
+  static constexpr int SMEM = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
-  static_assert(CBA >= 1, "channel blocks per warp");
+  static_assert(RB % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
+  static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D>::kKDelta, "code box");
+  static_assert(CBA >= 1 && CBA * NW == NCB, "channel blocks per warp");
   static_assert(2 * WCH * D * 4 * NW <= TPS * RB, "window chunks must fit the record region");
-  static_assert(NW * GP * D * 4 <= OFF_QS, "window partials fit below the query (over dead scores)");
+  static_assert(NW * WCH * GP * 4 <= BX, "window scores fit the fragment region");
+  static_assert(NW * GP * D * 4 <= REC_REGION, "window partials fit the record region");
 };
 
 // Sum over the CTA (NW warps) of per-thread vectors v[N]; every thread gets the totals.
@@ -272,11 +365,14 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     const float* __restrict__ win_k, const float* __restrict__ win_v,
                     const int32_t* __restrict__ win_start, const int32_t* __restrict__ win_len,
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
-                    float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc) {
+                    float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
+                    const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, TPS>;
   using R = Rec<D>;
-  constexpr int NW = C::NW, NT = C::NT, GV = C::GV;
-  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the swizzled TMA boxes need 1024-byte aligned slots (the launch adds the slack)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int item = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = lane >> 2, q4 = lane & 3;  // mma fragment coordinates
@@ -301,7 +397,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
     return;
   }
-  float* sc = reinterpret_cast<float*>(smem + C::OFF_SC);
+  float* sc = reinterpret_cast<float*>(smem + C::OFF_BX);
   float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   int* okf = reinterpret_cast<int*>(smem + C::OFF_FLG);
@@ -427,7 +523,20 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 
   // ========================= packed tiles, tensor cores ======================
+  // Warp w owns tokens 32w .. 32w+31 of every tile of the item and keeps its
+  // own streaming-softmax state (m, l, acc) per query head; the four warps'
+  // states are merged once, at the end of the item.
+  //
+  // Each record slot holds the K and V codes as one 128B-swizzled TMA box
+  // (K: channel rows of 64 bytes, V: token rows of D/4 bytes) followed by the
+  // scales. ldmatrix.trans reads 8 rows x 16 bytes of codes and leaves in lane
+  // (g8, q4) rows 2q4 and 2q4+1 at byte pair g8: two channels x four tokens
+  // (K) or two tokens x eight channels (V), which is a fragment's worth of
+  // codes for the mma.sync layout below.
   const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + item * TPS;
+  float* qmax = reinterpret_cast<float*>(smem + C::OFF_QMAX);
+  uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [2][NCB][NT][32]
+  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [2][NW][GP]
   if (tid == 0) {
     for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
     fence_mbar_init();
@@ -436,290 +545,290 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   if (tid == 0) {
     for (int kk = 0; kk < nslot; ++kk) {
       const int64_t off = trow[kk];
-      const bool aligned = (off & 15) == 0 && off >= 0;
+      const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
       okf[kk] = aligned;
       if (aligned) {
         mbar_expect_tx(&bar[kk], C::RB);
-        bulk_g2s(smem + kk * C::RB, tiles + off, C::RB, &bar[kk]);
+        tma_load_2d(smem + kk * C::RB, &tmap, 0, (int)(off >> 7), &bar[kk]);
+        bulk_g2s(smem + kk * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
+                 C::RB - C::CODE_BYTES, &bar[kk]);
       }
     }
   }
   // scores are kept in base-2 units (scale * log2 e folded into the query); the
   // item's (max, sum) pair is converted back to natural-log units when stored
   for (int h = warp; h < GP; h += NW)
-    rotate_head_to_smem<D, GP>(q + ((int64_t)b * Hq + (int64_t)kvh * G + h) * D, h < G,
-                               scale * kLog2eD, qs, h, lane);
+    rotate_head_pairs<D, GP>(q + ((int64_t)b * Hq + (int64_t)kvh * G + h) * D, h < G,
+                             scale * kLog2eD, qs, qmax, h, lane);
   __syncthreads();
   int bad = 0;
   for (int kk = 0; kk < nslot; ++kk) bad |= !okf[kk];
-  // the 8 lanes of one query head in a fragment: g8 in {2h', 2h'+1} (hi, lo), any q4
-  const int hcol = g8 >> 1;      // head within an n-tile
-  const bool is_hi = !(g8 & 1);  // this lane's B column holds the hi part
 
-  // ---------------- phase A: warp w contracts channel blocks CBA*w.. ------
-  // share[k][w][t][h]: this warp's share of the score of token t, head h
-  float* share = reinterpret_cast<float*>(smem + C::OFF_PART);
+  // B view (fragment column g8): head 4nt + hb, hi part when is_hi.
+  // Accumulator view (columns 2q4, 2q4+1): head 4nt + q4, hi + lo parts.
+  const int hb = g8 >> 1;
+  const bool is_hi = !(g8 & 1);
+  float qmB[NT], qmA[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    qmB[nt] = 4 * nt + hb < GP ? qmax[4 * nt + hb] : 0.f;
+    qmA[nt] = 4 * nt + q4 < GP ? qmax[4 * nt + q4] : 0.f;
+  }
+  constexpr int NS = D / 64;  // 64-channel slices of a V row
+  float m_run[NT], l_run[NT];
+  float out_acc[NS][4][2][NT];  // channel 64s + 8 g8 + 2 mu + rr, head 4nt + q4
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) { m_run[nt] = kNegInf; l_run[nt] = 0.f; }
+#pragma unroll
+  for (int sl = 0; sl < NS; ++sl)
+#pragma unroll
+    for (int mu = 0; mu < 4; ++mu)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) out_acc[sl][mu][rr][nt] = 0.f;
+  // ldmatrix row addresses of this lane (matrix lane >> 3, row lane & 7)
+  const int mi = lane >> 3, ri = lane & 7;
+  const uint32_t kaddr0 = (uint32_t)((16 * (mi >> 1) + 8 * (mi & 1) + ri) * 64 + 16 * warp);
+  const uint32_t vaddr0 =
+      (uint32_t)(C::K_BYTES + (32 * warp + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
+
   for (int k = 0; k < nslot; ++k) {
+    const int buf = k & 1;
     const unsigned char* Rk = smem + k * C::RB;
+    const uint32_t rk = smem_u32(Rk);
+    // a CTA whose copy failed or timed out still runs every step (on whatever the
+    // buffer holds) so that all warps meet every barrier; its output is NaN
     if (!bad && !mbar_wait(&bar[k], 0)) bad = 1;
-    if (__any_sync(0xffffffffu, bad)) { bad = 1; continue; }
     const float* kS = reinterpret_cast<const float*>(Rk + R::kKS);
     const float* kD = reinterpret_cast<const float*>(Rk + R::kKDelta);
     const float* kL = reinterpret_cast<const float*>(Rk + R::kKLo);
-    // B fragments of this warp's channels, in registers: channels 16cb + 2q4 + {0,1,8,9}
-    float wdv[C::CBA][4][NT];
-    float amax[NT], bsum[NT];
+    const float* kR = reinterpret_cast<const float*>(Rk + R::kKR);
+
+    // ---- folded query wd_c = q'_c s_c delta_c, one power-of-two scale per head
+    // from the bound max|q'| * max_c s_c delta_c (the same in every warp)
+    float mf = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) { amax[nt] = 0.f; bsum[nt] = 0.f; }
+    for (int i = 0; i < D / 32; ++i) mf = fmaxf(mf, fabsf(kS[lane + 32 * i] * kD[lane + 32 * i]));
+    mf = warp_max(mf);
+    float scB[NT], invA[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float s_, i_;
+      pow2_scale(qmB[nt] * mf, 16.0f, scB[nt], i_);
+      pow2_scale(qmA[nt] * mf, 16.0f, s_, invA[nt]);
+    }
+    // this warp's channel blocks: B fragments to shared memory, per-head partial sums
+    float ssum[NT], bsum[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) { ssum[nt] = 0.f; bsum[nt] = 0.f; }
 #pragma unroll
     for (int u = 0; u < C::CBA; ++u) {
-      const int cbase = 16 * (C::CBA * warp + u) + 2 * q4;
+      const int cb = C::CBA * warp + u;
+      uint32_t fr[NT][2];
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
-        const int c = cbase + 8 * hlf;
+        const int c = 16 * cb + 2 * q4 + 8 * hlf;
         const float2 s = *reinterpret_cast<const float2*>(kS + c);
         const float2 dd = *reinterpret_cast<const float2*>(kD + c);
         const float2 lo = *reinterpret_cast<const float2*>(kL + c);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float w0 = qs[c * GP + 4 * nt + hcol] * s.x;
-          const float w1 = qs[(c + 1) * GP + 4 * nt + hcol] * s.y;
-          wdv[u][2 * hlf][nt] = w0 * dd.x;
-          wdv[u][2 * hlf + 1][nt] = w1 * dd.y;
-          amax[nt] = fmaxf(amax[nt], fmaxf(fabsf(w0 * dd.x), fabsf(w1 * dd.y)));
+          const int h = 4 * nt + hb;
+          const float2 qv = h < GP ? *reinterpret_cast<const float2*>(qs + ((c >> 1) * GP + h) * 2)
+                                   : make_float2(0.f, 0.f);
+          const float w0 = qv.x * s.x, w1 = qv.y * s.y;
+          fr[nt][hlf] = hilo_pair(w0 * dd.x * scB[nt], w1 * dd.y * scB[nt], !is_hi);
+          ssum[nt] += pair_sum(fr[nt][hlf]);
           if (is_hi) bsum[nt] = fmaf(w1, lo.y, fmaf(w0, lo.x, bsum[nt]));
         }
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        bx[((buf * NCB + cb) * NT + nt) * 32 + lane] = make_uint2(fr[nt][0], fr[nt][1]);
     }
-    uint32_t bfr[C::CBA][NT][2];
-    float sumwd[NT], inv[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int m = 1; m <= 4; m <<= 1) amax[nt] = fmaxf(amax[nt], __shfl_xor_sync(0xffffffffu, amax[nt], m));
-      float sc2;
-      pow2_scale(amax[nt], 16.0f, sc2, inv[nt]);
-      float ssum = 0.f;
-#pragma unroll
-      for (int u = 0; u < C::CBA; ++u) {
-        bfr[u][nt][0] = hilo_pair(wdv[u][0][nt] * sc2, wdv[u][1][nt] * sc2, !is_hi);
-        bfr[u][nt][1] = hilo_pair(wdv[u][2][nt] * sc2, wdv[u][3][nt] * sc2, !is_hi);
-        ssum += pair_sum(bfr[u][nt][0]) + pair_sum(bfr[u][nt][1]);
-      }
-#pragma unroll
-      for (int m = 1; m <= 4; m <<= 1) {
-        ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
+      for (int m = 1; m <= 4; m <<= 1) {  // over q4 (channels), then the hi/lo pair of lanes
+        ssum[nt] += __shfl_xor_sync(0xffffffffu, ssum[nt], m);
         bsum[nt] += __shfl_xor_sync(0xffffffffu, bsum[nt], m);
       }
-      sumwd[nt] = ssum;
+      if (q4 == 0 && is_hi && 4 * nt + hb < GP)
+        pt[(buf * NW + warp) * GP + 4 * nt + hb] = make_float2(ssum[nt], bsum[nt]);
     }
-    float acc[8][NT][4];
+    named_bar_sync(NW * 32);
+
+    // ---- phase A: scores of this warp's 32 tokens against all channels.
+    // M-block j: row g8 <-> token 32w + 4 g8 + 2j, row g8 + 8 <-> that token + 1.
+    float swd[NT], bia[NT];
 #pragma unroll
-    for (int tb = 0; tb < 8; ++tb)
+    for (int nt = 0; nt < NT; ++nt) {
+      float a = 0.f, c = 0.f;
+      if (4 * nt + q4 < GP) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float2 v = pt[(buf * NW + w) * GP + 4 * nt + q4];
+          a += v.x;
+          c += v.y;
+        }
+      }
+      swd[nt] = a;
+      bia[nt] = c;
+    }
+    float acc[2][NT][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[tb][nt][e] = 0.f;
-    const uint32_t sel = (uint32_t)(g8 >> 1) | ((uint32_t)((g8 >> 1) + 4) << 8);
-    const int sh = (g8 & 1) ? 2 : 6;
+        for (int e = 0; e < 4; ++e) acc[j][nt][e] = 0.f;
 #pragma unroll
-    for (int u = 0; u < C::CBA; ++u) {
-      const int r0 = 16 * (C::CBA * warp + u) + 2 * q4;
-      const uint4* row0 = reinterpret_cast<const uint4*>(Rk + R::kKCodes + (r0 + 0) * 64);
-      const uint4* row1 = reinterpret_cast<const uint4*>(Rk + R::kKCodes + (r0 + 1) * 64);
-      const uint4* row8 = reinterpret_cast<const uint4*>(Rk + R::kKCodes + (r0 + 8) * 64);
-      const uint4* row9 = reinterpret_cast<const uint4*>(Rk + R::kKCodes + (r0 + 9) * 64);
+    for (int cp = 0; cp < NCB; cp += 2) {
+      uint32_t x[4];  // channel blocks cp, cp+1; channels +0..7 and +8..15 of each
+      ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64)), x[0], x[1], x[2], x[3]);
 #pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {  // 16-byte quarter of the rows: token blocks 2qd, 2qd+1
-        const uint4 w0 = row0[qd], w1 = row1[qd], w8 = row8[qd], w9 = row9[qd];
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t xl = x[2 * u], xh = x[2 * u + 1];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          mma16816(acc[2 * qd][nt], nib_pair(w0.x, w1.x, sel, sh), nib_pair(w0.y, w1.y, sel, sh),
-                   nib_pair(w8.x, w9.x, sel, sh), nib_pair(w8.y, w9.y, sel, sh), bfr[u][nt][0],
-                   bfr[u][nt][1]);
-          mma16816(acc[2 * qd + 1][nt], nib_pair(w0.z, w1.z, sel, sh), nib_pair(w0.w, w1.w, sel, sh),
-                   nib_pair(w8.z, w9.z, sel, sh), nib_pair(w8.w, w9.w, sel, sh), bfr[u][nt][0],
-                   bfr[u][nt][1]);
+          const uint2 bf = bx[((buf * NCB + cp + u) * NT + nt) * 32 + lane];
+          mma16816(acc[0][nt], k_frag(xl, 0), k_frag(xl, 1), k_frag(xh, 0), k_frag(xh, 1), bf.x,
+                   bf.y);
+          mma16816(acc[1][nt], k_frag(xl, 2), k_frag(xl, 3), k_frag(xh, 2), k_frag(xh, 3), bf.x,
+                   bf.y);
         }
       }
     }
-    // this warp's share: sum_c (wd code + w lo) over its channels = 16 (S - sum wd) 2^-e + bias
+    // z = r_t (sum_c wd_c code_tc + bias) for token 32w + 4 g8 + 2j + rr, head 4nt + q4
+    const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * warp + 4 * g8);
+    const float rt[2][2] = {{r4.x, r4.y}, {r4.z, r4.w}};
+    float z[2][2][NT];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          z[j][rr][nt] = rt[j][rr] * fmaf(acc[j][nt][2 * rr] + acc[j][nt][2 * rr + 1] - swd[nt],
+                                          invA[nt], bia[nt]);
+
+    // ---- streaming softmax of this warp (per head)
+    float alpha[NT], p[2][2][NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int h = 4 * nt + q4;
-      // lanes hold heads q4 of the accumulator columns; sum wd / bias of head h live in
-      // the lanes whose fragment column is head h: fetch them from lane 8*(h%4)
-      const float swd = __shfl_sync(0xffffffffu, sumwd[nt], 8 * q4);
-      const float bia = __shfl_sync(0xffffffffu, bsum[nt], 8 * q4);
-      const float iv = __shfl_sync(0xffffffffu, inv[nt], 8 * q4);
-      if (h < GP) {
+      float mx = fmaxf(fmaxf(z[0][0][nt], z[0][1][nt]), fmaxf(z[1][0][nt], z[1][1][nt]));
 #pragma unroll
-        for (int tb = 0; tb < 8; ++tb)
+      for (int m = 4; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      const float mn = fmaxf(m_run[nt], mx);
+      alpha[nt] = exp2f(m_run[nt] - mn);
+      m_run[nt] = mn;
+      float ls = 0.f;
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int t = 16 * tb + g8 + 8 * rr;
-            const float S = acc[tb][nt][2 * rr] + acc[tb][nt][2 * rr + 1];
-            share[((k * NW + warp) * 128 + t) * GP + h] = fmaf(S - swd, iv, bia);
-          }
-      }
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          p[j][rr][nt] = exp2f(z[j][rr][nt] - mn);
+          ls += p[j][rr][nt];
+        }
+      l_run[nt] = fmaf(l_run[nt], alpha[nt], ls);
     }
-  }
-  bad = __syncthreads_or(bad);
 
-  // ---------------- scores and the item's softmax maximum ------------------
-  float M[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) M[h] = kNegInf;
-  if (!bad) {
-    const int t = tid;
-    for (int k = 0; k < nslot; ++k) {
-      const float r = reinterpret_cast<const float*>(smem + k * C::RB + R::kKR)[t];
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        float z = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) z += share[((k * NW + w) * 128 + t) * GP + h];
-        z *= r;
-        sc[(k * 128 + t) * GP + h] = z;
-        M[h] = fmaxf(M[h], z);
-      }
-    }
-  }
-  cta_max<GP, NW>(M, red, tid);  // its barriers also publish sc
-
-  // ---------------- phase B: warp w aggregates tokens 32w .. 32w+31 --------
-  // out_acc: this warp's share of acc_rot for channels 16cb + g8 (+8), head q4 (+4 nt)
-  float out_acc[C::NCB][2][NT];
-#pragma unroll
-  for (int cb = 0; cb < C::NCB; ++cb)
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) out_acc[cb][rr][nt] = 0.f;
-  float lsum[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) lsum[nt] = 0.f;
-  const uint32_t sel0 = (uint32_t)(g8 >> 2) | ((uint32_t)((g8 >> 2) + 4) << 8);
-  const uint32_t sel1 = sel0 + 0x0202u;  // channel g8 + 8
-  const int shc = 8 - 2 * (g8 & 3);
-  for (int k = 0; k < nslot && !bad; ++k) {
-    const unsigned char* Rk = smem + k * C::RB;
+    // ---- value side: pd_t = p_t r_t delta_tg as fp16 hi + lo, transposed into
+    // B fragments (tokens x (head, part)) with movmatrix. K-block j of phase B
+    // holds tokens 32w + 8 q4 + 2j + {0, 4} (b0) and + {1, 5} (b1).
     const float* vR = reinterpret_cast<const float*>(Rk + R::kVR);
     const float* vD = reinterpret_cast<const float*>(Rk + R::kVDelta);
     const float* vL = reinterpret_cast<const float*>(Rk + R::kVLo);
     const float* vS = reinterpret_cast<const float*>(Rk + R::kVS);
-    // B fragments: tokens 16tb + 2q4 + {0,1,8,9} of tb = 2w, 2w+1, column g8
-    uint32_t bfr[GV][2][NT][2];
-    float sumpd[GV][NT], Lw[GV][NT], invp[GV][NT];
+    const float4 vr4 = *reinterpret_cast<const float4*>(vR + 32 * warp + 4 * g8);
+    const float vrt[2][2] = {{vr4.x, vr4.y}, {vr4.z, vr4.w}};
+    uint32_t bB[GV][2][NT][2];
+    float spd[GV][NT], lterm[GV][NT], invp[GV][NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h = 4 * nt + hcol;
-      const bool hv_ok = h < GP;
-      const float Mh = M[hv_ok ? h : 0];
-      float pdv[GV][2][4], pm[GV], ls[GV];
+    for (int gv = 0; gv < GV; ++gv) {
+      float pdv[2][2][NT], pm[NT], lt[NT];
 #pragma unroll
-      for (int g = 0; g < GV; ++g) { pm[g] = 0.f; ls[g] = 0.f; }
+      for (int nt = 0; nt < NT; ++nt) { pm[nt] = 0.f; lt[nt] = 0.f; }
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int t = 16 * (2 * warp + j) + 2 * q4 + 8 * hlf;
-          const float2 r = *reinterpret_cast<const float2*>(vR + t);
-          const float p0 = hv_ok ? exp2f(sc[(k * 128 + t) * GP + h] - Mh) : 0.f;
-          const float p1 = hv_ok ? exp2f(sc[(k * 128 + t + 1) * GP + h] - Mh) : 0.f;
-          const float pv0 = p0 * r.x, pv1 = p1 * r.y;
-          if (is_hi) lsum[nt] += p0 + p1;
+        for (int rr = 0; rr < 2; ++rr) {
+          const int t = 32 * warp + 4 * g8 + 2 * j + rr;
+          const float d = vD[t * GV + gv], lo = vL[t * GV + gv];
 #pragma unroll
-          for (int g = 0; g < GV; ++g) {
-            const float d0 = vD[t * GV + g], d1 = vD[(t + 1) * GV + g];
-            pdv[g][j][2 * hlf] = pv0 * d0;
-            pdv[g][j][2 * hlf + 1] = pv1 * d1;
-            pm[g] = fmaxf(pm[g], fmaxf(fabsf(pv0 * d0), fabsf(pv1 * d1)));
-            if (is_hi) ls[g] = fmaf(pv1, vL[(t + 1) * GV + g], fmaf(pv0, vL[t * GV + g], ls[g]));
+          for (int nt = 0; nt < NT; ++nt) {
+            const float pv = p[j][rr][nt] * vrt[j][rr];
+            pdv[j][rr][nt] = pv * d;
+            pm[nt] = fmaxf(pm[nt], fabsf(pv * d));
+            lt[nt] = fmaf(pv, lo, lt[nt]);
           }
         }
 #pragma unroll
-      for (int g = 0; g < GV; ++g) {
+      for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int m = 1; m <= 4; m <<= 1) pm[g] = fmaxf(pm[g], __shfl_xor_sync(0xffffffffu, pm[g], m));
+        for (int m = 4; m < 32; m <<= 1) pm[nt] = fmaxf(pm[nt], __shfl_xor_sync(0xffffffffu, pm[nt], m));
         float sc2;
-        pow2_scale(pm[g], 4.0f, sc2, invp[g][nt]);
-        float ssum = 0.f;
+        pow2_scale(pm[nt], 4.0f, sc2, invp[gv][nt]);
+        float sp = 0.f;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          bfr[g][j][nt][0] = hilo_pair(pdv[g][j][0] * sc2, pdv[g][j][1] * sc2, !is_hi);
-          bfr[g][j][nt][1] = hilo_pair(pdv[g][j][2] * sc2, pdv[g][j][3] * sc2, !is_hi);
-          ssum += pair_sum(bfr[g][j][nt][0]) + pair_sum(bfr[g][j][nt][1]);
+          const uint32_t xl = hilo_one(pdv[j][0][nt] * sc2, sp);  // row g8: token 4 g8 + 2j
+          const uint32_t xh = hilo_one(pdv[j][1][nt] * sc2, sp);  // token 4 g8 + 2j + 1
+          bB[gv][j][nt][0] = movmatrix_t(xl);
+          bB[gv][j][nt][1] = movmatrix_t(xh);
         }
+        float l2 = lt[nt];
 #pragma unroll
-        for (int m = 1; m <= 4; m <<= 1) {
-          ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
-          ls[g] += __shfl_xor_sync(0xffffffffu, ls[g], m);
+        for (int m = 4; m < 32; m <<= 1) {
+          sp += __shfl_xor_sync(0xffffffffu, sp, m);
+          l2 += __shfl_xor_sync(0xffffffffu, l2, m);
         }
-        sumpd[g][nt] = ssum;
-        Lw[g][nt] = ls[g];
+        spd[gv][nt] = sp;
+        lterm[gv][nt] = l2;
       }
     }
-    // the accumulator column of lane (g8, q4) is head q4: fetch its scalars from lane 8*q4
-    float swd_o[GV][NT], lw_o[GV][NT], iv_o[GV][NT];
+
+    // ---- phase B: this warp's 32 tokens against all channels, one 64-channel
+    // slice of the V rows at a time. M-block mu of slice sl: row g8 <-> channel
+    // 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1.
 #pragma unroll
-    for (int g = 0; g < GV; ++g)
+    for (int sl = 0; sl < NS; ++sl) {
+      const int gv = (64 * sl) / R::kVGroup;
+      uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
+      ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(16 * sl)), y[0], y[1], y[2], y[3]);
+      float o[4][NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        swd_o[g][nt] = __shfl_sync(0xffffffffu, sumpd[g][nt], 8 * q4);
-        lw_o[g][nt] = __shfl_sync(0xffffffffu, Lw[g][nt], 8 * q4);
-        iv_o[g][nt] = __shfl_sync(0xffffffffu, invp[g][nt], 8 * q4);
-      }
-    constexpr int CH = C::NCB < 8 ? C::NCB : 8;  // channel blocks per accumulator pass
-#pragma unroll
-    for (int cb0 = 0; cb0 < C::NCB; cb0 += CH) {
-      float o[CH][NT][4];
-#pragma unroll
-      for (int u = 0; u < CH; ++u)
+      for (int mu = 0; mu < 4; ++mu)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[u][nt][e] = 0.f;
-      const int g = (16 * cb0) / Rec<D>::kVGroup;
+          for (int e = 0; e < 4; ++e) o[mu][nt][e] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int t0 = 16 * (2 * warp + j) + 2 * q4;
-        const unsigned char* v0 = Rk + R::kVCodes + (t0 + 0) * (D / 4) + 4 * cb0;
-        const unsigned char* v1 = Rk + R::kVCodes + (t0 + 1) * (D / 4) + 4 * cb0;
-        const unsigned char* v8 = Rk + R::kVCodes + (t0 + 8) * (D / 4) + 4 * cb0;
-        const unsigned char* v9 = Rk + R::kVCodes + (t0 + 9) * (D / 4) + 4 * cb0;
+      for (int mu = 0; mu < 4; ++mu)
 #pragma unroll
-        for (int u = 0; u < CH; u += 2) {
-          const uint2 a0 = reinterpret_cast<const uint2*>(v0)[u / 2];
-          const uint2 a1 = reinterpret_cast<const uint2*>(v1)[u / 2];
-          const uint2 a8 = reinterpret_cast<const uint2*>(v8)[u / 2];
-          const uint2 a9 = reinterpret_cast<const uint2*>(v9)[u / 2];
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t a0 = v_frag(y[2 * j], 2 * mu), a1 = v_frag(y[2 * j], 2 * mu + 1);
+          const uint32_t a2 = v_frag(y[2 * j + 1], 2 * mu), a3 = v_frag(y[2 * j + 1], 2 * mu + 1);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816(o[u][nt], crumb_pair(a0.x, a1.x, sel0, shc), crumb_pair(a0.x, a1.x, sel1, shc),
-                     crumb_pair(a8.x, a9.x, sel0, shc), crumb_pair(a8.x, a9.x, sel1, shc),
-                     bfr[g][j][nt][0], bfr[g][j][nt][1]);
-            mma16816(o[u + 1][nt], crumb_pair(a0.y, a1.y, sel0, shc), crumb_pair(a0.y, a1.y, sel1, shc),
-                     crumb_pair(a8.y, a9.y, sel0, shc), crumb_pair(a8.y, a9.y, sel1, shc),
-                     bfr[g][j][nt][0], bfr[g][j][nt][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][j][nt][0], bB[gv][j][nt][1]);
+        }
+      // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
+      const float4 s0 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8);
+      const float4 s1 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8 + 4);
+      const float sv[4][2] = {{s0.x, s0.y}, {s0.z, s0.w}, {s1.x, s1.y}, {s1.z, s1.w}};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mu = 0; mu < 4; ++mu)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
+            out_acc[sl][mu][rr][nt] =
+                fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
+                     sv[mu][rr] * fmaf(O - spd[gv][nt], invp[gv][nt], lterm[gv][nt]));
           }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (4 * nt + q4 < GP) {
-#pragma unroll
-          for (int u = 0; u < CH; ++u)
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const int cb = cb0 + u;
-              const int c = 16 * cb + g8 + 8 * rr;
-              const float O = o[u][nt][2 * rr] + o[u][nt][2 * rr + 1];
-              out_acc[cb][rr][nt] = fmaf(vS[c], fmaf(O - swd_o[g][nt], iv_o[g][nt], lw_o[g][nt]),
-                                         out_acc[cb][rr][nt]);
-            }
-        }
-      }
     }
   }
   bad = __syncthreads_or(bad);
@@ -727,32 +836,33 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int kk = 0; kk < nslot; ++kk)
       if (okf[kk]) mbar_wait(&bar[kk], 0);
 
-  // ---------------- cross-warp sum of the value partials, softmax sum ------
-  float L[GP];
-#pragma unroll
-  for (int h = 0; h < GP; ++h) L[h] = 0.f;
+  // ---------------- merge the four warps' (m, l, acc) ----------------------
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    // lsum of head 4nt + hcol: summed over the column's lanes (lo lanes hold 0), then
-    // one lane per head adds it
 #pragma unroll
-    for (int m = 1; m <= 4; m <<= 1) lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], m);
-    const float v = (q4 == 0 && is_hi) ? lsum[nt] : 0.f;
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-      if (h == 4 * nt + hcol) L[h] += v;
+    for (int m = 4; m < 32; m <<= 1) l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], m);
+    const int h = 4 * nt + q4;
+    if (g8 == 0 && h < GP) {
+      red[warp * 32 + h] = m_run[nt];
+      red[warp * 32 + 8 + h] = l_run[nt];
+    }
   }
-  cta_sum<GP, NW>(L, red, tid);
-  float* vred = reinterpret_cast<float*>(smem + C::OFF_PART);  // [NW][GP][D]
+  __syncthreads();
+  float* vred = reinterpret_cast<float*>(smem);  // [NW][GP][DP], over the dead records
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h = 4 * nt + q4;
     if (h < GP) {
+      float M = kNegInf;
 #pragma unroll
-      for (int cb = 0; cb < C::NCB; ++cb)
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
+      const float f = exp2f(m_run[nt] - M);
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-          vred[(warp * GP + h) * D + 16 * cb + g8 + 8 * rr] = out_acc[cb][rr][nt];
+      for (int sl = 0; sl < NS; ++sl)
+#pragma unroll
+        for (int mu = 0; mu < 4; ++mu)
+          *reinterpret_cast<float2*>(vred + (warp * GP + h) * C::DP + 64 * sl + 8 * g8 + 2 * mu) =
+              make_float2(out_acc[sl][mu][0][nt] * f, out_acc[sl][mu][1][nt] * f);
     }
   }
   __syncthreads();
@@ -760,38 +870,40 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     const int h = idx / D, c = idx % D;
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) s += vred[(w * GP + h) * D + c];
+    for (int w = 0; w < NW; ++w) s += vred[(w * GP + h) * C::DP + c];
     ws_acc[(part + (int64_t)h * items) * D + c] = bad ? NAN : s;
   }
   if (tid < G) {
-    float Mh = M[0], lh = L[0];
+    float M = kNegInf, L = 0.f;
 #pragma unroll
-    for (int h = 1; h < GP; ++h)
-      if (h == tid) { Mh = M[h]; lh = L[h]; }
-    ws_ml[(part + (int64_t)tid * items) * 2 + 0] = bad ? NAN : Mh * kLn2D;
-    ws_ml[(part + (int64_t)tid * items) * 2 + 1] = bad ? NAN : lh;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + tid]);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) L += red[w * 32 + 8 + tid] * exp2f(red[w * 32 + tid] - M);
+    ws_ml[(part + (int64_t)tid * items) * 2 + 0] = bad ? NAN : M * kLn2D;
+    ws_ml[(part + (int64_t)tid * items) * 2 + 1] = bad ? NAN : L;
   }
 }
 
-// LSE combine: one CTA of D threads per (query head, sequence). The items'
-// (max, sum) pairs are reduced cooperatively, their weights kept in shared
-// memory, then each thread sums its channel over the items with independent,
-// coalesced loads.
+// LSE combine: one CTA of 512 threads per (query head, sequence). Each group of
+// D/4 threads reads whole item rows (float4 per thread, coalesced) for every
+// (512/(D/4))-th item; the groups are summed in shared memory, the tile part is
+// rotated back with one FWHT, the window part added, and the result divided by
+// the softmax sum.
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(512)
 decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_acc, int Hq,
                       int items, int tile_items, float* __restrict__ out) {
-  constexpr int NW = D / 32;
-  constexpr int CH = 1024;  // items per weight chunk in shared memory
+  constexpr int NTH = 512, TPR = D / 4, NG = NTH / TPR, NWC = NTH / 32;
+  __shared__ float4 grp[2][NG][TPR];
   __shared__ float x[D];
-  __shared__ float wgt[CH];
-  __shared__ float redf[NW];
-  __shared__ int redi[NW];
-  const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x, lane = c & 31, wid = c >> 5;
+  __shared__ float redf[NWC];
+  __shared__ float redl[NWC];
+  __shared__ int redi[NWC];
+  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t base = ((int64_t)b * Hq + hq) * items;
   float M = kNegInf;
   int poison = 0;
-  for (int j = c; j < items; j += D) {
+  for (int j = tid; j < items; j += NTH) {
     const float lj = ws_ml[(base + j) * 2 + 1];
     if (!(lj >= 0.f)) poison = 1;
     if (lj > 0.f) M = fmaxf(M, ws_ml[(base + j) * 2]);
@@ -803,48 +915,101 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   M = redf[0];
   poison = redi[0];
 #pragma unroll
-  for (int w = 1; w < NW; ++w) { M = fmaxf(M, redf[w]); poison |= redi[w]; }
-  __syncthreads();
-  float L = 0.f, arot = 0.f, awin = 0.f;
-  for (int j0 = 0; j0 < items; j0 += CH) {
-    const int n = min(CH, items - j0);
-    for (int j = c; j < n; j += D) {
-      const float lj = ws_ml[(base + j0 + j) * 2 + 1];
-      const float w = lj > 0.f ? expf(ws_ml[(base + j0 + j) * 2] - M) : 0.f;
-      wgt[j] = w;
-      L = fmaf(lj > 0.f ? lj : 0.f, w, L);
-    }
-    __syncthreads();
-    const float* a = ws_acc + (base + j0) * D + c;
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) {
-      const float w = wgt[j];
-      if (w != 0.f) {
-        const float v = a[(int64_t)j * D];
-        if (j0 + j < tile_items) arot = fmaf(w, v, arot);
-        else awin = fmaf(w, v, awin);
-      }
-    }
-    __syncthreads();
+  for (int w = 1; w < NWC; ++w) { M = fmaxf(M, redf[w]); poison |= redi[w]; }
+  const int gi = tid / TPR, c4 = tid % TPR;
+  float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), aw = ar;
+  float L = 0.f;
+#pragma unroll 4
+  for (int j = gi; j < items; j += NG) {
+    const float mj = ws_ml[(base + j) * 2], lj = ws_ml[(base + j) * 2 + 1];
+    const float w = lj > 0.f ? expf(mj - M) : 0.f;
+    if (c4 == 0) L = fmaf(lj > 0.f ? lj : 0.f, w, L);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (w != 0.f) v = reinterpret_cast<const float4*>(ws_acc + (base + j) * D)[c4];
+    float4& a = j < tile_items ? ar : aw;
+    a.x = fmaf(w, v.x, a.x);
+    a.y = fmaf(w, v.y, a.y);
+    a.z = fmaf(w, v.z, a.z);
+    a.w = fmaf(w, v.w, a.w);
   }
+  grp[0][gi][c4] = ar;
+  grp[1][gi][c4] = aw;
   L = warp_sum(L);
-  if (lane == 0) redf[wid] = L;
-  x[c] = arot;
+  if (lane == 0) redl[wid] = L;
   __syncthreads();
-  L = redf[0];
+  L = 0.f;
 #pragma unroll
-  for (int w = 1; w < NW; ++w) L += redf[w];
+  for (int w = 0; w < NWC; ++w) L += redl[w];
+  float xr = 0.f, xw = 0.f;
+  if (tid < D) {
+    const float* g0 = reinterpret_cast<const float*>(grp[0]);
+    const float* g1 = reinterpret_cast<const float*>(grp[1]);
 #pragma unroll
-  for (int h = 1; h < D; h <<= 1) {
-    const float v = x[c], o = x[c ^ h];
+    for (int g = 0; g < NG; ++g) {
+      xr += g0[g * D + tid];
+      xw += g1[g * D + tid];
+    }
+    // FWHT: butterflies within the warp by shuffles, across warps through x[]
+#pragma unroll
+    for (int h = 1; h < 32 && h < D; h <<= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, xr, h);
+      xr = (tid & h) ? (o - xr) : (xr + o);
+    }
+  }
+  for (int h = 32; h < D; h <<= 1) {
+    if (tid < D) x[tid] = xr;
     __syncthreads();
-    x[c] = (c & h) ? (o - v) : (v + o);
+    if (tid < D) {
+      const float o = x[tid ^ h];
+      xr = (tid & h) ? (o - xr) : (xr + o);
+    }
     __syncthreads();
   }
-  float r = 0.f;
-  if (L > 0.f) r = (x[c] * (1.0f / sqrtf((float)D)) + awin) / L;
-  if (poison) r = NAN;
-  out[((int64_t)b * Hq + hq) * D + c] = r;
+  if (tid < D) {
+    float r = 0.f;
+    if (L > 0.f) r = (xr * (1.0f / sqrtf((float)D)) + xw) / L;
+    if (poison) r = NAN;
+    out[((int64_t)b * Hq + hq) * D + tid] = r;
+  }
+}
+
+// cuTensorMapEncodeTiled, fetched once from the driver (the library links the
+// static CUDA runtime only).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tensor map over the record pool seen as rows of 128 bytes: a box of
+// code_lines rows starting at row offset/128 is the K and V codes of the
+// record at that offset, copied with 128-byte swizzling. The row count is the
+// largest a coordinate can address; only rows of real records are read.
+cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
+  memset(m, 0, sizeof(*m));
+  if (!tiles) return cudaSuccess;  // no tile items: the map is never used
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {128, 0x7FFFFFFFull};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)code_lines};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(tiles), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <int D, int GP, int TPS>
@@ -857,15 +1022,18 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(decode_split_kernel<D, GP, TPS>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM + 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  CUtensorMap tmap;
+  e = code_map(&tmap, p.tile_items > 0 ? a.tiles : nullptr, C::CODE_LINES);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.items, a.Hkv, a.B);
-  decode_split_kernel<D, GP, TPS><<<grid, 128, C::SMEM, st>>>(
+  decode_split_kernel<D, GP, TPS><<<grid, 128, C::SMEM + 1024, st>>>(
       a.q, a.tiles, a.tile_table, a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len,
       a.win_capacity, a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale, ws_ml,
-      ws_acc);
+      ws_acc, tmap);
   return cudaGetLastError();
 }
 
@@ -954,9 +1122,9 @@ cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, con
   ws_split(p, B, Hq, const_cast<void*>(ws), &ml, &acc);
   const dim3 grid(Hq, B);
   switch (D) {
-    case 64: decode_combine_kernel<64><<<grid, 64, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
-    case 128: decode_combine_kernel<128><<<grid, 128, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
-    case 256: decode_combine_kernel<256><<<grid, 256, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 64: decode_combine_kernel<64><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 128: decode_combine_kernel<128><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 256: decode_combine_kernel<256><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
