@@ -395,6 +395,10 @@ def main():
         kvarn.window_advance(win_start, win_len, None, 1, 0, cap)
 
     per_step_launches = 3 * LAYERS + 1
+    # kernels of a step chain by programmatic dependent launch; the split kernels
+    # stream their records in before waiting on the previous kernel (nothing in
+    # the step writes records, tables or tile counts: promotions run between steps)
+    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
@@ -404,7 +408,18 @@ def main():
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        step_body(timed_in_graph)
+        step_body(False)
+    if timed_in_graph:  # the same step with events around each split launch
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            step_body(True)
+    # the split kernels of all layers back to back (one graph), for their
+    # sustained per-launch time
+    graph_split = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_split, stream=stream):
+        for l in range(LAYERS):
+            kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
+                               win_len, lay, ws)
 
     def run_steps(n):
         for _ in range(n):
@@ -444,10 +459,16 @@ def main():
     ms_per_step = elapsed_ms / args.steps
     tokens_per_s = world * B * args.steps / (elapsed_ms / 1000.0)
 
-    # split-kernel durations of the last replay (events captured in the graph)
+    # split-kernel durations: one more decode step with events around each split
+    # launch, then the splits of all layers back to back
     if timed_in_graph:
+        with torch.cuda.stream(stream):
+            graph_ev.replay()
+            host["len"] += 1
+            promote_if_due()
+        torch.cuda.synchronize()
         split_ms = float(np.mean([a.elapsed_time(b) for a, b in ev_split]))
-        split_how = "CUDA events captured around each split launch in the graph (last timed replay)"
+        split_how = "CUDA events captured around each split launch of one decode step (graph)"
     else:
         with torch.cuda.stream(stream):
             evs = []
@@ -461,6 +482,16 @@ def main():
         torch.cuda.synchronize()
         split_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
         split_how = "CUDA events around eager split launches after the timed region"
+    reps = 20
+    with torch.cuda.stream(stream):
+        graph_split.replay()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(reps):
+            graph_split.replay()
+        s1.record()
+    torch.cuda.synchronize()
+    split_seq_ms = s0.elapsed_time(s1) / (reps * LAYERS)
     ctx_now = 128 * host["n_tiles"] + host["len"]
     packed = B * HKV * host["n_tiles"] * rb
     window_bytes = B * HKV * host["len"] * D * 4 * 2
@@ -537,7 +568,13 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": workload_config(),
             "decode": {"ctx_end": ctx_now, "split_kernel_ms": split_ms, "split_gbs": split_gbs,
-                       "split_bytes_per_launch": split_bytes, "timing": split_how},
+                       "split_bytes_per_launch": split_bytes, "timing": split_how,
+                       "split_back_to_back_ms": split_seq_ms,
+                       "split_back_to_back_gbs": split_bytes / (split_seq_ms * 1e-3) / 1e9,
+                       "back_to_back_timing": f"CUDA events around {reps} replays of a graph of "
+                                              f"the {LAYERS} layers' split launches (programmatic "
+                                              f"dependent launch, records prefetched)",
+                       "launch_flags": "PDL|PREFETCH"},
             "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": split_gbs / hbm, "traffic": traffic,
                          "kernel": "decode_split_kernel", "peak_source": peak_kind},

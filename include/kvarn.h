@@ -196,6 +196,33 @@ int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
                          int d_len, int promote, int win_capacity, kvarn_stream_t stream);
 
 /*
+ * Launch mode of the decode-path kernels (kvarn_append_window,
+ * kvarn_window_advance, kvarn_decode_split, kvarn_decode_combine,
+ * kvarn_decode_attention). Process-wide; applies to launches enqueued after
+ * the call, including launches captured into CUDA graphs. The pages have no
+ * counterpart: this is how the kernels are chained on this GPU.
+ *   0                      plain stream-ordered launches (the default).
+ *   KVARN_LAUNCH_PDL       programmatic dependent launch: each kernel may be
+ *                          scheduled while the previous kernel on the stream
+ *                          is still running and waits for it on the device
+ *                          before touching memory, which hides the launch
+ *                          gap. Results are identical to mode 0.
+ *   KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH
+ *                          as above, and the split kernel reads n_tiles, the
+ *                          tile table and the packed records BEFORE that wait
+ *                          (so a layer's records stream in while the previous
+ *                          kernels finish). The caller guarantees that no
+ *                          kernel still running ahead of it on the stream
+ *                          writes those three (e.g. promotions are enqueued
+ *                          between graph replays, not inside the step).
+ * Returns KVARN_ERR_BAD_ARG for unknown bits or PREFETCH without PDL.
+ */
+#define KVARN_LAUNCH_PDL 1u
+#define KVARN_LAUNCH_PREFETCH 2u
+int kvarn_set_launch_flags(unsigned flags);
+unsigned kvarn_get_launch_flags(void);
+
+/*
  * Decode attention over the compressed cache (PR #434, commits 0d7cd28 and
  * e43f3f0, llm_kvarn_attention; issue #433 item 2: a fixed worst-case grid
  * over (head, tile range) with early exit, followed by an LSE combine, with

@@ -366,7 +366,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     const int32_t* __restrict__ win_start, const int32_t* __restrict__ win_len,
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
-                    const __grid_constant__ CUtensorMap tmap) {
+                    int prefetch, const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, TPS>;
   using R = Rec<D>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB;
@@ -378,6 +378,12 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   const int g8 = lane >> 2, q4 = lane & 3;  // mma fragment coordinates
   const bool is_win = item >= tile_items;
   const int64_t part = ((int64_t)b * Hq + (int64_t)kvh * G) * items + item;
+  // Under programmatic dependent launch, wait for the previous kernel on the
+  // stream before touching memory; with prefetch, tile items first read
+  // n_tiles, the tile table and their records (which, by the caller's
+  // guarantee, no earlier kernel still running writes) and wait afterwards.
+  const bool early = prefetch && !is_win;
+  if (!early) pdl_wait();
 
   // slots of this item: packed tiles, or window chunks of WCH rows (one per warp)
   int nslot, wlen = 0, wstart = 0, wj0 = 0;
@@ -391,6 +397,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     nslot = min(max((wlen - wj0 + C::WCH - 1) / C::WCH, 0), NW);
   }
   if (nslot == 0) {
+    if (early) pdl_wait();
+    pdl_trigger();
     if (tid < G) {
       ws_ml[(part + (int64_t)tid * items) * 2 + 0] = kNegInf;
       ws_ml[(part + (int64_t)tid * items) * 2 + 1] = 0.f;
@@ -405,22 +413,26 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 
   if (is_win) {
     // ===================== window chunk: raw rows, SIMT =====================
+    pdl_trigger();
     const int64_t head_base = ((int64_t)b * Hkv + kvh) * cap;
     if (tid == 0) {
       for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
       fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-      for (int kk = 0; kk < nslot; ++kk) {
-        const int n = min(C::WCH, wlen - (wj0 + C::WCH * kk));
-        mbar_expect_tx(&bar[kk], (uint32_t)(n * D * 4 * 2));
-        unsigned char* dst = smem + kk * (2 * C::WCH * D * 4);
-        for (int j = 0; j < n; ++j) {
-          const int slot = (wstart + wj0 + C::WCH * kk + j) % cap;
-          bulk_g2s(dst + j * D * 4, win_k + (head_base + slot) * D, D * 4, &bar[kk]);
-          bulk_g2s(dst + (C::WCH + j) * D * 4, win_v + (head_base + slot) * D, D * 4, &bar[kk]);
-        }
+    if (lane == 0 && warp < nslot) {
+      // this warp's chunk: n consecutive ring slots from s0, in at most two pieces
+      const int kk = warp;
+      const int n = min(C::WCH, wlen - (wj0 + C::WCH * kk));
+      const int s0 = (wstart + wj0 + C::WCH * kk) % cap;
+      const int n1 = min(n, cap - s0);
+      mbar_expect_tx(&bar[kk], (uint32_t)(n * D * 4 * 2));
+      unsigned char* dst = smem + kk * (2 * C::WCH * D * 4);
+      bulk_g2s(dst, win_k + (head_base + s0) * D, n1 * D * 4, &bar[kk]);
+      bulk_g2s(dst + C::WCH * D * 4, win_v + (head_base + s0) * D, n1 * D * 4, &bar[kk]);
+      if (n1 < n) {
+        bulk_g2s(dst + n1 * D * 4, win_k + head_base * D, (n - n1) * D * 4, &bar[kk]);
+        bulk_g2s(dst + (C::WCH + n1) * D * 4, win_v + head_base * D, (n - n1) * D * 4, &bar[kk]);
       }
     }
     for (int idx = tid; idx < D * GP; idx += 128) {
@@ -555,6 +567,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
   }
+  if (early) pdl_wait();
+  pdl_trigger();
   // scores are kept in base-2 units (scale * log2 e folded into the query); the
   // item's (max, sum) pair is converted back to natural-log units when stored
   for (int h = warp; h < GP; h += NW)
@@ -901,6 +915,8 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   __shared__ int redi[NWC];
   const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t base = ((int64_t)b * Hq + hq) * items;
+  pdl_trigger();
+  pdl_wait();
   float M = kNegInf;
   int poison = 0;
   for (int j = tid; j < items; j += NTH) {
@@ -1029,12 +1045,13 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   CUtensorMap tmap;
   e = code_map(&tmap, p.tile_items > 0 ? a.tiles : nullptr, C::CODE_LINES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.items, a.Hkv, a.B);
-  decode_split_kernel<D, GP, TPS><<<grid, 128, C::SMEM + 1024, st>>>(
-      a.q, a.tiles, a.tile_table, a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len,
-      a.win_capacity, a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale, ws_ml,
-      ws_acc, tmap);
-  return cudaGetLastError();
+  const unsigned fl = launch_flags();
+  const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
+  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(128), C::SMEM + 1024, st);
+  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, TPS>, a.q, a.tiles, a.tile_table,
+                            a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
+                            a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale,
+                            ws_ml, ws_acc, prefetch, tmap);
 }
 
 template <int D, int GP>
@@ -1120,14 +1137,15 @@ cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, con
                                   float* out, cudaStream_t st) {
   float *ml, *acc;
   ws_split(p, B, Hq, const_cast<void*>(ws), &ml, &acc);
-  const dim3 grid(Hq, B);
+  LaunchCfg L(dim3(Hq, B), dim3(512), 0, st);
+  const float* cml = ml;
+  const float* cacc = acc;
   switch (D) {
-    case 64: decode_combine_kernel<64><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
-    case 128: decode_combine_kernel<128><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
-    case 256: decode_combine_kernel<256><<<grid, 512, 0, st>>>(ml, acc, Hq, p.items, p.tile_items, out); break;
+    case 64: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<64>, cml, cacc, Hq, p.items, p.tile_items, out);
+    case 128: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<128>, cml, cacc, Hq, p.items, p.tile_items, out);
+    case 256: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<256>, cml, cacc, Hq, p.items, p.tile_items, out);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace kvarn

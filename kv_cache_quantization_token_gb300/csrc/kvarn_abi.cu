@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kvarn_common.cuh"
 
 namespace {
@@ -48,9 +50,24 @@ bool layout_ok(const kvarn_layout_t* L) {
   return memcmp(&ref, L, sizeof(ref)) == 0;
 }
 
+std::atomic<unsigned> g_launch_flags{0};
+
 }  // namespace
 
+namespace kvarn {
+unsigned launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+}  // namespace kvarn
+
 extern "C" {
+
+int kvarn_set_launch_flags(unsigned flags) {
+  if (flags & ~(KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH)) return KVARN_ERR_BAD_ARG;
+  if ((flags & KVARN_LAUNCH_PREFETCH) && !(flags & KVARN_LAUNCH_PDL)) return KVARN_ERR_BAD_ARG;
+  g_launch_flags.store(flags, std::memory_order_relaxed);
+  return KVARN_OK;
+}
+
+unsigned kvarn_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
 int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out) {
   if (!out) return KVARN_ERR_NULL;

@@ -46,6 +46,36 @@ __device__ __forceinline__ void chan_merge(float& mean, float& m2, float na, flo
   m2 = m2 + m2_b + d * d * (na * nb / n);
 }
 
+// Programmatic dependent launch: wait for the previous grid on the stream
+// (no-op when the kernel was launched without the attribute) and let the
+// next grid be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Current kvarn_set_launch_flags() value.
+unsigned launch_flags();
+
+// cudaLaunchKernelEx configuration honouring KVARN_LAUNCH_PDL.
+struct LaunchCfg {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_flags() & KVARN_LAUNCH_PDL) ? 1 : 0;
+  }
+  LaunchCfg(const LaunchCfg&) = delete;
+  LaunchCfg& operator=(const LaunchCfg&) = delete;
+};
+
 }  // namespace kvarn
 
 // Launchers implemented in the .cu files; kvarn_abi.cu validates arguments

@@ -53,6 +53,8 @@ __global__ void append_kernel(const float4* __restrict__ k_new, const float4* __
                               int64_t n_new, float4* __restrict__ win_k, float4* __restrict__ win_v,
                               int cap, const int32_t* __restrict__ win_start,
                               const int32_t* __restrict__ win_len, int n_seq, int hkv, int d4) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t total = (int64_t)n_seq * n_new * hkv * d4;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -74,6 +76,8 @@ __global__ void append_kernel(const float4* __restrict__ k_new, const float4* __
 // advance) can be captured in a CUDA graph and replayed.
 __global__ void advance_kernel(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
                                int d_len, int promote, int cap) {
+  pdl_trigger();
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= n_seq) return;
   int len = win_len[s] + d_len;
@@ -90,9 +94,9 @@ __global__ void advance_kernel(int32_t* win_start, int32_t* win_len, int32_t* n_
 cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
                                   int n_seq, int d_len, int promote, int win_capacity,
                                   cudaStream_t st) {
-  advance_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(win_start, win_len, n_tiles, n_seq, d_len,
-                                                       promote, win_capacity);
-  return cudaGetLastError();
+  LaunchCfg L(dim3((n_seq + 127) / 128), dim3(128), 0, st);
+  return cudaLaunchKernelEx(&L.cfg, advance_kernel, win_start, win_len, n_tiles, n_seq, d_len,
+                            promote, win_capacity);
 }
 
 cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, cudaStream_t st) {
@@ -113,11 +117,11 @@ cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new,
   const int64_t total = (int64_t)n_seq * n_new * n_kv_heads * (D / 4);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
-  append_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-      reinterpret_cast<const float4*>(k_new), reinterpret_cast<const float4*>(v_new), n_new,
-      reinterpret_cast<float4*>(win_k), reinterpret_cast<float4*>(win_v), win_capacity, win_start,
-      win_len, n_seq, n_kv_heads, D / 4);
-  return cudaGetLastError();
+  LaunchCfg L(dim3((unsigned)blocks), dim3(256), 0, st);
+  return cudaLaunchKernelEx(&L.cfg, append_kernel, reinterpret_cast<const float4*>(k_new),
+                            reinterpret_cast<const float4*>(v_new), n_new,
+                            reinterpret_cast<float4*>(win_k), reinterpret_cast<float4*>(win_v),
+                            win_capacity, win_start, win_len, n_seq, n_kv_heads, D / 4);
 }
 
 }  // namespace kvarn

@@ -16,6 +16,8 @@ from . import _build
 
 TILE = 128
 DEFAULT_ITERS = 4
+LAUNCH_PDL = 1       # KVARN_LAUNCH_PDL
+LAUNCH_PREFETCH = 2  # KVARN_LAUNCH_PREFETCH
 
 _lib = None
 
@@ -72,10 +74,13 @@ def _L():
         lib.kvarn_prefill_attention.argtypes = [vp, c_int, i64, vp, vp, c_int, c_int, vp, vp,
                                                 c_int, c_int, c_int, c_int, c_int, c_int,
                                                 ctypes.c_float, ctypes.POINTER(Layout), vp, vp]
+        lib.kvarn_set_launch_flags.argtypes = [ctypes.c_uint]
+        lib.kvarn_get_launch_flags.argtypes = []
+        lib.kvarn_get_launch_flags.restype = ctypes.c_uint
         for name in ("kvarn_layout", "kvarn_rotate_query", "kvarn_compress_tile",
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
                      "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
-                     "kvarn_window_advance", "kvarn_prefill_attention"):
+                     "kvarn_window_advance", "kvarn_prefill_attention", "kvarn_set_launch_flags"):
             getattr(lib, name).restype = c_int
         _lib = lib
     return _lib
@@ -282,3 +287,12 @@ def decode_attention_noalloc(q, tiles, tile_table, n_tiles, win_k, win_v, win_st
               _ptr(win_start), _ptr(win_len), cap, B, Hq, Hkv, D, max_tiles,
               float(softmax_scale), ctypes.byref(lay), _ptr(out), _stream(stream)))
     return out
+
+
+def set_launch_flags(flags: int):
+    """Process-wide launch mode of the decode-path kernels (kvarn_set_launch_flags)."""
+    _check("kvarn_set_launch_flags", _L().kvarn_set_launch_flags(int(flags)))
+
+
+def get_launch_flags() -> int:
+    return int(_L().kvarn_get_launch_flags())

@@ -92,3 +92,15 @@ def test_prefill_host_validation(lib):
     assert f(*args(16, 0, 1, 16, D=256, lay=L256)) == -3  # head_dim 256 not yet supported
     assert f(*args(16, 0, 1, 16, Hq=80)) == -3            # GQA group of 10
     assert f(*args(0, 0, 0, 0)) == 0                      # empty chunk enqueues nothing
+
+
+def test_launch_flags_validation():
+    assert kvarn.get_launch_flags() == 0
+    with pytest.raises(kvarn.KvarnError):
+        kvarn.set_launch_flags(kvarn.LAUNCH_PREFETCH)  # prefetch needs programmatic launch
+    with pytest.raises(kvarn.KvarnError):
+        kvarn.set_launch_flags(8)
+    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
+    assert kvarn.get_launch_flags() == 3
+    kvarn.set_launch_flags(0)
+    assert kvarn.get_launch_flags() == 0

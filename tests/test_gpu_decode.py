@@ -78,3 +78,19 @@ def test_custom_scale_and_determinism():
     b = c.decode(q, scale=0.3)
     assert torch.equal(a, b)
     _check(c, Hq=8, scale=0.3, seed=1)
+
+
+def test_offset_not_multiple_of_128_poisons_only_that_head():
+    c = Cache("qwen3_8b_decode", 11, [128 * 3 + 10], Hkv=2, D=128)
+    q = torch.from_numpy(synth.queries("qwen3_8b_decode", 11, (1, 8, 128))).to(DEV)
+    good = c.decode(q).cpu().numpy()
+    n = c.tiles.numel()
+    pool = torch.zeros(n + c.rb + 256, dtype=torch.uint8, device=DEV)
+    pool[:n] = c.tiles
+    pool[n + 16:n + 16 + c.rb] = c.tiles[int(c.tile_table[0, 1, 0]):int(c.tile_table[0, 1, 0]) + c.rb]
+    table = c.tile_table.clone()
+    table[0, 1, 0] = n + 16  # 16-byte aligned, not a multiple of 128
+    out = kvarn.decode_attention(q, pool, table, c.n_tiles, c.win_k, c.win_v, c.win_start,
+                                 c.win_len, c.lay).cpu().numpy()
+    assert np.isnan(out[0, 4:]).all()          # query heads of KV head 1
+    assert np.array_equal(out[0, :4], good[0, :4])
