@@ -5,15 +5,14 @@
 // the deferred inverse WHT is applied after combining the rotated partials):
 //
 //   split kernel   grid (item, KV head, sequence), 4 warps per CTA. Items
-//                  0..tile_items-1 own TPS consecutive packed tiles, staged in
-//                  shared memory by bulk async copies. Warp w takes tokens
-//                  32w..32w+31 of every tile: the score and value contractions
-//                  run as mma.sync m16n8k16 with A fragments built straight
-//                  from the packed codes; the warps share only the folded
-//                  query (one named barrier per tile) and keep their own
-//                  streaming-softmax state, merged once per item. The
-//                  remaining items own 4 chunks of FP32 window rows (raw rows,
-//                  unrotated query), one per warp.
+//                  0..tile_items-1 own 2 consecutive packed tiles, staged in
+//                  shared memory by TMA, one per warp pair; each warp takes 64
+//                  tokens of its tile: the score and value contractions run
+//                  as mma.sync m16n8k16 with A fragments built straight from
+//                  the packed codes, and the warp keeps its own streaming-
+//                  softmax state, merged with the others' once per item. The
+//                  remaining items own chunks of FP32 window rows (raw rows,
+//                  unrotated query), one chunk per warp.
 //   combine kernel grid (query head, sequence): LSE merge of the items, one
 //                  inverse rotation of the merged tile accumulator, plus the
 //                  (unrotated) window accumulator, divided by the softmax sum.
@@ -209,10 +208,6 @@ __device__ __forceinline__ uint32_t hilo_pair(float x0, float x1, bool lo_part) 
   const __half2 r = lo_part ? __floats2half2_rn(x0 - hf.x, x1 - hf.y) : hi;
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-__device__ __forceinline__ float pair_sum(uint32_t v) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
-  return f.x + f.y;
-}
 // 2^e for the power-of-two scale that brings max |x| = m into [2^10, 2^11)
 // (1 when m is zero or not finite), and its inverse times `k`.
 __device__ __forceinline__ void pow2_scale(float m, float k, float& scale, float& inv_k) {
@@ -229,10 +224,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
-}
-// Barrier 1 among the n threads of the CTA that execute it (barrier 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int n) {
-  asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
 }
 // {fp16(x), fp16(x - fp16(x))} packed low/high; adds the value the pair represents to sum.
 __device__ __forceinline__ uint32_t hilo_one(float x, float& sum) {
@@ -286,9 +277,11 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
   if (lane == 0) qmax[h] = mx;
 }
 
-template <int D, int GP, int TPS>
+template <int D, int GP>
 struct DC {
   static constexpr int NW = 4;                                  // warps per CTA
+  static constexpr int NTHR = 32 * NW;
+  static constexpr int TPS = 2;                                 // tiles per item, one per warp pair
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
   static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
@@ -296,7 +289,8 @@ struct DC {
   static constexpr int CODE_LINES = CODE_BYTES / 128;           // 128-byte lines of that box
   static constexpr int NT = GP > 4 ? 2 : 1;                     // n8-tiles of (head, part) columns
   static constexpr int NCB = D / 16;                            // 16-channel blocks
-  static constexpr int CBA = NCB / NW;                          // blocks whose B fragments a warp builds
+  static constexpr int HB = NCB / 2;                            // blocks whose B fragments a warp builds
+  static constexpr int NS = D / 64;                             // 64-channel slices of a V row
   // window rows staged per warp (K and V rows of one chunk fit the record region)
   static constexpr int WCH0 = (TPS * RB) / (NW * 2 * D * 4);
   static constexpr int WCH = WCH0 >= 16 ? 16 : WCH0 >= 8 ? 8 : WCH0 >= 4 ? 4 : 2;
@@ -304,11 +298,11 @@ struct DC {
   static constexpr int MRG = NW * GP * DP * 4;                  // merge region [NW][GP][DP], over records
   static constexpr int REC_REGION = TPS * RB > MRG ? TPS * RB : MRG;
   static constexpr int OFF_QS = (REC_REGION + 15) / 16 * 16;    // f32 query [D/2][GP][2] (window: [D][GP])
-  static constexpr int OFF_QMAX = OFF_QS + D * GP * 4;          // f32 [8]
-  static constexpr int OFF_BX = OFF_QMAX + 32;                  // B fragments [2][NCB][NT][32] x u32x2
-  static constexpr int BX = 2 * NCB * NT * 32 * 8;              //   (window items: scores [4 WCH][GP])
-  static constexpr int OFF_PT = OFF_BX + BX;                    // per-warp (sum wd, bias) [2][NW][GP]
-  static constexpr int OFF_RED = OFF_PT + 2 * NW * GP * 8;      // f32 reduction scratch [NW][32]
+  static constexpr int OFF_QMAX = OFF_QS + D * GP * 4;          // f32 [8] max |q'| per head
+  static constexpr int OFF_BX = OFF_QMAX + 32;                  // B fragments [TPS][NCB][NT][32] x u32x2
+  static constexpr int OFF_PT = OFF_BX + TPS * NCB * NT * 32 * 8;  // (sum wd, bias) [TPS][2][GP]
+  static constexpr int OFF_SCW = OFF_PT + TPS * 2 * GP * 8;     // window probabilities [NW WCH][GP]
+  static constexpr int OFF_RED = OFF_SCW + (NW * WCH * GP * 4 + 15) / 16 * 16;  // f32 [NW][32]
   static constexpr int OFF_FLG = OFF_RED + NW * 32 * 4;         // int [TPS]
   static constexpr int NBAR = TPS > NW ? TPS : NW;               // one per tile, or per window chunk
   static constexpr int OFF_BAR = (OFF_FLG + TPS * 4 + 7) / 8 * 8;
@@ -316,9 +310,8 @@ struct DC {
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(RB % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
   static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D>::kKDelta, "code box");
-  static_assert(CBA >= 1 && CBA * NW == NCB, "channel blocks per warp");
+  static_assert(HB >= 1 && 2 * HB == NCB, "channel blocks per warp");
   static_assert(2 * WCH * D * 4 * NW <= TPS * RB, "window chunks must fit the record region");
-  static_assert(NW * WCH * GP * 4 <= BX, "window scores fit the fragment region");
   static_assert(NW * GP * D * 4 <= REC_REGION, "window partials fit the record region");
 };
 
@@ -358,7 +351,7 @@ __device__ __forceinline__ void cta_max(float (&v)[N], float* red, int tid) {
   }
 }
 
-template <int D, int GP, int TPS>
+template <int D, int GP>
 __global__ void __launch_bounds__(128)
 decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
                     const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
@@ -367,9 +360,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
-  using C = DC<D, GP, TPS>;
+  using C = DC<D, GP>;
   using R = Rec<D>;
-  constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB;
+  constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
+  constexpr int HB = C::HB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled TMA boxes need 1024-byte aligned slots (the launch adds the slack)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -405,7 +399,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
     return;
   }
-  float* sc = reinterpret_cast<float*>(smem + C::OFF_BX);
+  float* sc = reinterpret_cast<float*>(smem + C::OFF_SCW);
   float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   int* okf = reinterpret_cast<int*>(smem + C::OFF_FLG);
@@ -435,7 +429,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         bulk_g2s(dst + (C::WCH + n1) * D * 4, win_v + head_base * D, (n - n1) * D * 4, &bar[kk]);
       }
     }
-    for (int idx = tid; idx < D * GP; idx += 128) {
+    for (int idx = tid; idx < D * GP; idx += C::NTHR) {
       const int c = idx / GP, h = idx % GP;
       qs[idx] = h < G ? scale * q[((int64_t)b * Hq + (int64_t)kvh * G + h) * D + c] : 0.f;
     }
@@ -516,7 +510,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
       for (int h = 0; h < GP; ++h) vred[(warp * GP + h) * D + lane * E + e] = acc[e][h];
     __syncthreads();
-    for (int idx = tid; idx < G * D; idx += 128) {
+    for (int idx = tid; idx < G * D; idx += C::NTHR) {
       const int h = idx / D, c = idx % D;
       float s = 0.f;
 #pragma unroll
@@ -535,36 +529,37 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 
   // ========================= packed tiles, tensor cores ======================
-  // Warp w owns tokens 32w .. 32w+31 of every tile of the item and keeps its
-  // own streaming-softmax state (m, l, acc) per query head; the four warps'
-  // states are merged once, at the end of the item.
+  // Warp pair p = warp / 2 owns tile p of the item; warp w of the pair takes
+  // its tokens 64 (w % 2) .. +63. The pair shares the folded query (each warp
+  // builds half of its channel blocks; one pair barrier per tile), each warp
+  // contracts scores and values of its tokens on mma.sync and keeps its own
+  // streaming-softmax state (m, l, acc) per query head; the four warps'
+  // states are merged at the end of the item.
   //
   // Each record slot holds the K and V codes as one 128B-swizzled TMA box
   // (K: channel rows of 64 bytes, V: token rows of D/4 bytes) followed by the
   // scales. ldmatrix.trans reads 8 rows x 16 bytes of codes and leaves in lane
   // (g8, q4) rows 2q4 and 2q4+1 at byte pair g8: two channels x four tokens
-  // (K) or two tokens x eight channels (V), which is a fragment's worth of
-  // codes for the mma.sync layout below.
+  // (K) or two tokens x eight channels (V), a fragment's worth of codes.
   const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + item * TPS;
+  const int pair = warp >> 1, half = warp & 1;
   float* qmax = reinterpret_cast<float*>(smem + C::OFF_QMAX);
-  uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [2][NCB][NT][32]
-  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [2][NW][GP]
+  uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [TPS][NCB][NT][32]
+  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [TPS][2][GP]
   if (tid == 0) {
     for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    for (int kk = 0; kk < nslot; ++kk) {
-      const int64_t off = trow[kk];
-      const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
-      okf[kk] = aligned;
-      if (aligned) {
-        mbar_expect_tx(&bar[kk], C::RB);
-        tma_load_2d(smem + kk * C::RB, &tmap, 0, (int)(off >> 7), &bar[kk]);
-        bulk_g2s(smem + kk * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
-                 C::RB - C::CODE_BYTES, &bar[kk]);
-      }
+  if (lane == 0 && half == 0 && pair < nslot) {
+    const int64_t off = trow[pair];
+    const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
+    okf[pair] = aligned;
+    if (aligned) {
+      mbar_expect_tx(&bar[pair], C::RB);
+      tma_load_2d(smem + pair * C::RB, &tmap, 0, (int)(off >> 7), &bar[pair]);
+      bulk_g2s(smem + pair * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
+               C::RB - C::CODE_BYTES, &bar[pair]);
     }
   }
   if (early) pdl_wait();
@@ -576,21 +571,13 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                              scale * kLog2eD, qs, qmax, h, lane);
   __syncthreads();
   int bad = 0;
-  for (int kk = 0; kk < nslot; ++kk) bad |= !okf[kk];
 
   // B view (fragment column g8): head 4nt + hb, hi part when is_hi.
   // Accumulator view (columns 2q4, 2q4+1): head 4nt + q4, hi + lo parts.
   const int hb = g8 >> 1;
   const bool is_hi = !(g8 & 1);
-  float qmB[NT], qmA[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    qmB[nt] = 4 * nt + hb < GP ? qmax[4 * nt + hb] : 0.f;
-    qmA[nt] = 4 * nt + q4 < GP ? qmax[4 * nt + q4] : 0.f;
-  }
-  constexpr int NS = D / 64;  // 64-channel slices of a V row
   float m_run[NT], l_run[NT];
-  float out_acc[NS][4][2][NT];  // channel 64s + 8 g8 + 2 mu + rr, head 4nt + q4
+  float out_acc[NS][4][2][NT];  // channel 64 sl + 8 g8 + 2 mu + rr, head 4nt + q4
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) { m_run[nt] = kNegInf; l_run[nt] = 0.f; }
 #pragma unroll
@@ -601,26 +588,19 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) out_acc[sl][mu][rr][nt] = 0.f;
-  // ldmatrix row addresses of this lane (matrix lane >> 3, row lane & 7)
-  const int mi = lane >> 3, ri = lane & 7;
-  const uint32_t kaddr0 = (uint32_t)((16 * (mi >> 1) + 8 * (mi & 1) + ri) * 64 + 16 * warp);
-  const uint32_t vaddr0 =
-      (uint32_t)(C::K_BYTES + (32 * warp + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
 
-  for (int k = 0; k < nslot; ++k) {
-    const int buf = k & 1;
-    const unsigned char* Rk = smem + k * C::RB;
+  if (pair < nslot) {  // both warps of the pair agree
+    const int kk = pair;
+    const unsigned char* Rk = smem + kk * C::RB;
     const uint32_t rk = smem_u32(Rk);
-    // a CTA whose copy failed or timed out still runs every step (on whatever the
-    // buffer holds) so that all warps meet every barrier; its output is NaN
-    if (!bad && !mbar_wait(&bar[k], 0)) bad = 1;
+    if (!okf[kk] || !mbar_wait(&bar[kk], 0)) bad = 1;  // computed on, result poisoned
     const float* kS = reinterpret_cast<const float*>(Rk + R::kKS);
     const float* kD = reinterpret_cast<const float*>(Rk + R::kKDelta);
     const float* kL = reinterpret_cast<const float*>(Rk + R::kKLo);
     const float* kR = reinterpret_cast<const float*>(Rk + R::kKR);
 
     // ---- folded query wd_c = q'_c s_c delta_c, one power-of-two scale per head
-    // from the bound max|q'| * max_c s_c delta_c (the same in every warp)
+    // from the bound max|q'| * max_c s_c delta_c (the same in both warps)
     float mf = 0.f;
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) mf = fmaxf(mf, fabsf(kS[lane + 32 * i] * kD[lane + 32 * i]));
@@ -629,16 +609,19 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float s_, i_;
-      pow2_scale(qmB[nt] * mf, 16.0f, scB[nt], i_);
-      pow2_scale(qmA[nt] * mf, 16.0f, s_, invA[nt]);
+      const float qb = 4 * nt + hb < GP ? qmax[4 * nt + hb] : 0.f;
+      const float qa = 4 * nt + q4 < GP ? qmax[4 * nt + q4] : 0.f;
+      pow2_scale(qb * mf, 16.0f, scB[nt], i_);
+      pow2_scale(qa * mf, 16.0f, s_, invA[nt]);
     }
-    // this warp's channel blocks: B fragments to shared memory, per-head partial sums
-    float ssum[NT], bsum[NT];
+    // this warp's half of the channel blocks: B fragments to shared memory, and
+    // per-head partial sums of wd (fp32) and of the bias q' s lo
+    float wsum[NT], bsum[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) { ssum[nt] = 0.f; bsum[nt] = 0.f; }
+    for (int nt = 0; nt < NT; ++nt) { wsum[nt] = 0.f; bsum[nt] = 0.f; }
 #pragma unroll
-    for (int u = 0; u < C::CBA; ++u) {
-      const int cb = C::CBA * warp + u;
+    for (int u = 0; u < HB; ++u) {
+      const int cb = HB * half + u;
       uint32_t fr[NT][2];
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
@@ -652,86 +635,108 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           const float2 qv = h < GP ? *reinterpret_cast<const float2*>(qs + ((c >> 1) * GP + h) * 2)
                                    : make_float2(0.f, 0.f);
           const float w0 = qv.x * s.x, w1 = qv.y * s.y;
-          fr[nt][hlf] = hilo_pair(w0 * dd.x * scB[nt], w1 * dd.y * scB[nt], !is_hi);
-          ssum[nt] += pair_sum(fr[nt][hlf]);
-          if (is_hi) bsum[nt] = fmaf(w1, lo.y, fmaf(w0, lo.x, bsum[nt]));
+          const float x0 = w0 * dd.x, x1 = w1 * dd.y;
+          fr[nt][hlf] = hilo_pair(x0 * scB[nt], x1 * scB[nt], !is_hi);
+          wsum[nt] += x0 + x1;
+          bsum[nt] = fmaf(w1, lo.y, fmaf(w0, lo.x, bsum[nt]));
         }
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
-        bx[((buf * NCB + cb) * NT + nt) * 32 + lane] = make_uint2(fr[nt][0], fr[nt][1]);
+        bx[((kk * NCB + cb) * NT + nt) * 32 + lane] = make_uint2(fr[nt][0], fr[nt][1]);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int m = 1; m <= 4; m <<= 1) {  // over q4 (channels), then the hi/lo pair of lanes
-        ssum[nt] += __shfl_xor_sync(0xffffffffu, ssum[nt], m);
+      for (int m = 1; m <= 2; m <<= 1) {  // over q4: all channels of this warp's half
+        wsum[nt] += __shfl_xor_sync(0xffffffffu, wsum[nt], m);
         bsum[nt] += __shfl_xor_sync(0xffffffffu, bsum[nt], m);
       }
       if (q4 == 0 && is_hi && 4 * nt + hb < GP)
-        pt[(buf * NW + warp) * GP + 4 * nt + hb] = make_float2(ssum[nt], bsum[nt]);
+        pt[(kk * 2 + half) * GP + 4 * nt + hb] = make_float2(wsum[nt], bsum[nt]);
     }
-    named_bar_sync(NW * 32);
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");  // the pair's barrier
 
-    // ---- phase A: scores of this warp's 32 tokens against all channels.
-    // M-block j: row g8 <-> token 32w + 4 g8 + 2j, row g8 + 8 <-> that token + 1.
-    float swd[NT], bia[NT];
+    // sum_c wd_c code_tc = S inv - 16 sum_c wd_c: per-head constants of the
+    // accumulator view (head 4nt + q4)
+    float cstA[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float a = 0.f, c = 0.f;
+      float ws = 0.f, bs = 0.f;
       if (4 * nt + q4 < GP) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float2 v = pt[(buf * NW + w) * GP + 4 * nt + q4];
-          a += v.x;
-          c += v.y;
-        }
+        const float2 v0 = pt[(kk * 2 + 0) * GP + 4 * nt + q4];
+        const float2 v1 = pt[(kk * 2 + 1) * GP + 4 * nt + q4];
+        ws = v0.x + v1.x;
+        bs = v0.y + v1.y;
       }
-      swd[nt] = a;
-      bia[nt] = c;
+      cstA[nt] = bs - 16.0f * ws;
     }
-    float acc[2][NT][4];
+
+    // ---- phase A: scores of this warp's 64 tokens. Chunk w4 = tokens 32 w4 ..
+    // +31 (w4 = 2 half, 2 half + 1); M-block j: row g8 <-> token 32 w4 + 4 g8 + 2j,
+    // row g8 + 8 <-> that token + 1.
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint32_t kaddr0 =
+        (uint32_t)((16 * (mi >> 1) + 8 * (mi & 1) + ri) * 64 + 16 * (2 * half));
+    float acc[2][2][NT][4];
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int w2 = 0; w2 < 2; ++w2)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][nt][e] = 0.f;
-#pragma unroll
-    for (int cp = 0; cp < NCB; cp += 2) {
-      uint32_t x[4];  // channel blocks cp, cp+1; channels +0..7 and +8..15 of each
-      ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64)), x[0], x[1], x[2], x[3]);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t xl = x[2 * u], xh = x[2 * u + 1];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint2 bf = bx[((buf * NCB + cp + u) * NT + nt) * 32 + lane];
-          mma16816(acc[0][nt], k_frag(xl, 0), k_frag(xl, 1), k_frag(xh, 0), k_frag(xh, 1), bf.x,
-                   bf.y);
-          mma16816(acc[1][nt], k_frag(xl, 2), k_frag(xl, 3), k_frag(xh, 2), k_frag(xh, 3), bf.x,
-                   bf.y);
-        }
-      }
-    }
-    // z = r_t (sum_c wd_c code_tc + bias) for token 32w + 4 g8 + 2j + rr, head 4nt + q4
-    const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * warp + 4 * g8);
-    const float rt[2][2] = {{r4.x, r4.y}, {r4.z, r4.w}};
-    float z[2][2][NT];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          z[j][rr][nt] = rt[j][rr] * fmaf(acc[j][nt][2 * rr] + acc[j][nt][2 * rr + 1] - swd[nt],
-                                          invA[nt], bia[nt]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[w2][j][nt][e] = 0.f;
+#pragma unroll
+    for (int cp = 0; cp < NCB; cp += 2) {
+      uint2 bf[2][NT];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bf[u][nt] = bx[((kk * NCB + cp + u) * NT + nt) * 32 + lane];
+#pragma unroll
+      for (int w2 = 0; w2 < 2; ++w2) {
+        uint32_t x[4];  // channel blocks cp, cp+1; channels +0..7 and +8..15 of each
+        ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64 + 16 * w2)), x[0], x[1], x[2], x[3]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t xl = x[2 * u], xh = x[2 * u + 1];
+          const uint32_t a00 = k_frag(xl, 0), a01 = k_frag(xl, 1), a02 = k_frag(xh, 0), a03 = k_frag(xh, 1);
+          const uint32_t a10 = k_frag(xl, 2), a11 = k_frag(xl, 3), a12 = k_frag(xh, 2), a13 = k_frag(xh, 3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(acc[w2][0][nt], a00, a01, a02, a03, bf[u][nt].x, bf[u][nt].y);
+            mma16816(acc[w2][1][nt], a10, a11, a12, a13, bf[u][nt].x, bf[u][nt].y);
+          }
+        }
+      }
+    }
 
-    // ---- streaming softmax of this warp (per head)
-    float alpha[NT], p[2][2][NT];
+    // ---- scores z = r_t (sum_c wd_c code_tc + bias) and the warp's softmax
+    float z[2][2][2][NT];
+#pragma unroll
+    for (int w2 = 0; w2 < 2; ++w2) {
+      const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * (2 * half + w2) + 4 * g8);
+      const float rt[2][2] = {{r4.x, r4.y}, {r4.z, r4.w}};
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            z[w2][j][rr][nt] = rt[j][rr] * fmaf(acc[w2][j][nt][2 * rr] + acc[w2][j][nt][2 * rr + 1],
+                                                invA[nt], cstA[nt]);
+    }
+    float alpha[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float mx = fmaxf(fmaxf(z[0][0][nt], z[0][1][nt]), fmaxf(z[1][0][nt], z[1][1][nt]));
+      float mx = kNegInf;
+#pragma unroll
+      for (int w2 = 0; w2 < 2; ++w2)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) mx = fmaxf(mx, z[w2][j][rr][nt]);
 #pragma unroll
       for (int m = 4; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
       const float mn = fmaxf(m_run[nt], mx);
@@ -739,78 +744,83 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       m_run[nt] = mn;
       float ls = 0.f;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int w2 = 0; w2 < 2; ++w2)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          p[j][rr][nt] = exp2f(z[j][rr][nt] - mn);
-          ls += p[j][rr][nt];
-        }
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            z[w2][j][rr][nt] = exp2f(z[w2][j][rr][nt] - mn);  // now p
+            ls += z[w2][j][rr][nt];
+          }
       l_run[nt] = fmaf(l_run[nt], alpha[nt], ls);
     }
 
     // ---- value side: pd_t = p_t r_t delta_tg as fp16 hi + lo, transposed into
-    // B fragments (tokens x (head, part)) with movmatrix. K-block j of phase B
-    // holds tokens 32w + 8 q4 + 2j + {0, 4} (b0) and + {1, 5} (b1).
+    // B fragments with movmatrix. K-block (w2, j) of phase B holds tokens
+    // 32 w4 + 8 q4 + 2j + {0, 4} (b0) and + {1, 5} (b1).
     const float* vR = reinterpret_cast<const float*>(Rk + R::kVR);
     const float* vD = reinterpret_cast<const float*>(Rk + R::kVDelta);
     const float* vL = reinterpret_cast<const float*>(Rk + R::kVLo);
     const float* vS = reinterpret_cast<const float*>(Rk + R::kVS);
-    const float4 vr4 = *reinterpret_cast<const float4*>(vR + 32 * warp + 4 * g8);
-    const float vrt[2][2] = {{vr4.x, vr4.y}, {vr4.z, vr4.w}};
-    uint32_t bB[GV][2][NT][2];
-    float spd[GV][NT], lterm[GV][NT], invp[GV][NT];
+    uint32_t bB[GV][2][2][NT][2];
+    float invP[GV][NT], cstP[GV][NT];
 #pragma unroll
     for (int gv = 0; gv < GV; ++gv) {
-      float pdv[2][2][NT], pm[NT], lt[NT];
+      float pd[2][2][2][NT], pm[NT], lt[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) { pm[nt] = 0.f; lt[nt] = 0.f; }
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int w2 = 0; w2 < 2; ++w2) {
+        const int t0 = 32 * (2 * half + w2) + 4 * g8;
+        const float4 vr4 = *reinterpret_cast<const float4*>(vR + t0);
+        const float vrt[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int t = 32 * warp + 4 * g8 + 2 * j + rr;
-          const float d = vD[t * GV + gv], lo = vL[t * GV + gv];
+        for (int e = 0; e < 4; ++e) {
+          const float d = vD[(t0 + e) * GV + gv], lo = vL[(t0 + e) * GV + gv];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float pv = p[j][rr][nt] * vrt[j][rr];
-            pdv[j][rr][nt] = pv * d;
+            const float pv = z[w2][e >> 1][e & 1][nt] * vrt[e];
+            pd[w2][e >> 1][e & 1][nt] = pv * d;
             pm[nt] = fmaxf(pm[nt], fabsf(pv * d));
             lt[nt] = fmaf(pv, lo, lt[nt]);
           }
         }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int m = 4; m < 32; m <<= 1) pm[nt] = fmaxf(pm[nt], __shfl_xor_sync(0xffffffffu, pm[nt], m));
-        float sc2;
-        pow2_scale(pm[nt], 4.0f, sc2, invp[gv][nt]);
+        float sc2, inv2;
+        pow2_scale(pm[nt], 4.0f, sc2, inv2);
         float sp = 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t xl = hilo_one(pdv[j][0][nt] * sc2, sp);  // row g8: token 4 g8 + 2j
-          const uint32_t xh = hilo_one(pdv[j][1][nt] * sc2, sp);  // token 4 g8 + 2j + 1
-          bB[gv][j][nt][0] = movmatrix_t(xl);
-          bB[gv][j][nt][1] = movmatrix_t(xh);
-        }
+        for (int w2 = 0; w2 < 2; ++w2)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t xl = hilo_one(pd[w2][j][0][nt] * sc2, sp);  // row g8: token 4 g8 + 2j
+            const uint32_t xh = hilo_one(pd[w2][j][1][nt] * sc2, sp);  // token 4 g8 + 2j + 1
+            bB[gv][w2][j][nt][0] = movmatrix_t(xl);
+            bB[gv][w2][j][nt][1] = movmatrix_t(xh);
+          }
         float l2 = lt[nt];
 #pragma unroll
         for (int m = 4; m < 32; m <<= 1) {
           sp += __shfl_xor_sync(0xffffffffu, sp, m);
           l2 += __shfl_xor_sync(0xffffffffu, l2, m);
         }
-        spd[gv][nt] = sp;
-        lterm[gv][nt] = l2;
+        invP[gv][nt] = inv2;
+        cstP[gv][nt] = fmaf(-sp, inv2, l2);
       }
     }
 
-    // ---- phase B: this warp's 32 tokens against all channels, one 64-channel
+    // ---- phase B: this warp's 64 tokens against all channels, one 64-channel
     // slice of the V rows at a time. M-block mu of slice sl: row g8 <-> channel
     // 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1.
+    const uint32_t vaddr0 =
+        (uint32_t)(C::K_BYTES + (64 * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
 #pragma unroll
     for (int sl = 0; sl < NS; ++sl) {
       const int gv = (64 * sl) / R::kVGroup;
-      uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
-      ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(16 * sl)), y[0], y[1], y[2], y[3]);
       float o[4][NT][4];
 #pragma unroll
       for (int mu = 0; mu < 4; ++mu)
@@ -819,15 +829,21 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[mu][nt][e] = 0.f;
 #pragma unroll
-      for (int mu = 0; mu < 4; ++mu)
+      for (int w2 = 0; w2 < 2; ++w2) {
+        uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
+        ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * (D / 4) + 16 * sl)), y[0], y[1], y[2],
+                  y[3]);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t a0 = v_frag(y[2 * j], 2 * mu), a1 = v_frag(y[2 * j], 2 * mu + 1);
-          const uint32_t a2 = v_frag(y[2 * j + 1], 2 * mu), a3 = v_frag(y[2 * j + 1], 2 * mu + 1);
+        for (int mu = 0; mu < 4; ++mu)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][j][nt][0], bB[gv][j][nt][1]);
-        }
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t a0 = v_frag(y[2 * j], 2 * mu), a1 = v_frag(y[2 * j], 2 * mu + 1);
+            const uint32_t a2 = v_frag(y[2 * j + 1], 2 * mu), a3 = v_frag(y[2 * j + 1], 2 * mu + 1);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
+          }
+      }
       // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
       const float4 s0 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8);
       const float4 s1 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8 + 4);
@@ -839,9 +855,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
-            out_acc[sl][mu][rr][nt] =
-                fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
-                     sv[mu][rr] * fmaf(O - spd[gv][nt], invp[gv][nt], lterm[gv][nt]));
+            out_acc[sl][mu][rr][nt] = fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
+                                           sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]));
           }
     }
   }
@@ -850,7 +865,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int kk = 0; kk < nslot; ++kk)
       if (okf[kk]) mbar_wait(&bar[kk], 0);
 
-  // ---------------- merge the four warps' (m, l, acc) ----------------------
+  // ---------------- merge the warps' (m, l, acc) ---------------------------
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -870,7 +885,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       float M = kNegInf;
 #pragma unroll
       for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
-      const float f = exp2f(m_run[nt] - M);
+      const float f = m_run[nt] == kNegInf ? 0.f : exp2f(m_run[nt] - M);  // a warp without a tile
 #pragma unroll
       for (int sl = 0; sl < NS; ++sl)
 #pragma unroll
@@ -880,7 +895,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += 128) {
+  for (int idx = tid; idx < G * D; idx += C::NTHR) {
     const int h = idx / D, c = idx % D;
     float s = 0.f;
 #pragma unroll
@@ -892,7 +907,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + tid]);
 #pragma unroll
-    for (int w = 0; w < NW; ++w) L += red[w * 32 + 8 + tid] * exp2f(red[w * 32 + tid] - M);
+    for (int w = 0; w < NW; ++w)
+      if (red[w * 32 + tid] != kNegInf) L += red[w * 32 + 8 + tid] * exp2f(red[w * 32 + tid] - M);
     ws_ml[(part + (int64_t)tid * items) * 2 + 0] = bad ? NAN : M * kLn2D;
     ws_ml[(part + (int64_t)tid * items) * 2 + 1] = bad ? NAN : L;
   }
@@ -1028,16 +1044,16 @@ cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int GP, int TPS>
+template <int D, int GP>
 cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  using C = DC<D, GP, TPS>;
+  using C = DC<D, GP>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, TPS>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, GP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM + 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -1047,8 +1063,8 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   if (e != cudaSuccess) return e;
   const unsigned fl = launch_flags();
   const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
-  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(128), C::SMEM + 1024, st);
-  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, TPS>, a.q, a.tiles, a.tile_table,
+  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::SMEM + 1024, st);
+  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP>, a.q, a.tiles, a.tile_table,
                             a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
                             a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale,
                             ws_ml, ws_acc, prefetch, tmap);
@@ -1057,12 +1073,8 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
 template <int D, int GP>
 cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  switch (p.tiles_per_item) {
-    case 1: return launch_split_t<D, GP, 1>(p, a, ws_ml, ws_acc, st);
-    case 2: return launch_split_t<D, GP, 2>(p, a, ws_ml, ws_acc, st);
-    case 4: return launch_split_t<D, GP, 4>(p, a, ws_ml, ws_acc, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.tiles_per_item != DC<D, GP>::TPS) return cudaErrorInvalidValue;
+  return launch_split_t<D, GP>(p, a, ws_ml, ws_acc, st);
 }
 
 template <int D>
@@ -1084,31 +1096,16 @@ void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** 
   *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
-int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
-}
-
 }  // namespace
 
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  const int cap = D >= 256 ? 2 : 4;  // tiles staged per CTA (shared memory)
-  const int64_t total = (int64_t)B * Hkv * max_tiles;
-  const int64_t target = 4LL * sm_count();
-  int tps = (int)((total + target - 1) / (target > 0 ? target : 1));
-  tps = tps <= 1 ? 1 : tps <= 2 ? 2 : 4;
-  if (tps > cap) tps = cap;
+  // four warps per CTA, a warp pair per tile (DC<D, GP>)
+  const int tps = 2;
   p->tiles_per_item = tps;
   p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
-  // window rows per warp and chunks per item, as DC<D, GP, TPS>::WCH and its 4 warps
+  // window rows per warp and per item, as DC<D, GP>::WCH and its 4 warps
   const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
   const int w0 = (tps * rb) / (4 * 2 * D * 4);
   const int wch = w0 >= 16 ? 16 : w0 >= 8 ? 8 : w0 >= 4 ? 4 : 2;

@@ -91,9 +91,9 @@ cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new,
                           cudaStream_t st);
 
 struct DecodePlan {
-  int tiles_per_item;  // tiles (or 128-token window chunks) handled by one split CTA
+  int tiles_per_item;  // packed tiles handled by one split CTA (2 warps)
   int tile_items;      // ceil(max_tiles / tiles_per_item)
-  int win_items;       // ceil(win_capacity / (128 * tiles_per_item))
+  int win_items;       // window items: ceil(win_capacity / window rows per item)
   int items;           // tile_items + win_items
   int g_pad;           // query heads per KV head rounded up to 1, 2, 4 or 8
   size_t ws_bytes;
