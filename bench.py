@@ -5,9 +5,11 @@ cache at 16k context, and bulk tile compression.
 Decode step (the timed unit): one new token of a Qwen3-8B-like model (32 query
 heads, 8 KV heads, head_dim 128, batch 1) through 36 layers, each layer with
 its own 16k-token compressed cache (128 packed tiles per KV head plus the FP32
-window): per layer the split-tile decode kernel and the LSE combine, then the
-append of the layer's next K/V token into the window; one device-side window
-advance per step. The step is captured once as a CUDA graph and replayed.
+window): per layer the split-tile decode kernel and the LSE combine, and the
+append of the layer's next K/V token into the window (on a forked stream: it
+writes a slot no attention of the step reads); one device-side window advance
+per step. The step is captured once as a CUDA graph and replayed, its kernels
+chained by programmatic dependent launch.
 Whenever the window reaches 128 tokens the oldest 128 are promoted (compressed
 into a tile) between replays, as the decode loop of the pages does with its
 promotion hoisted out of the graph.
@@ -382,7 +384,20 @@ def main():
     except TypeError:
         ev_split, timed_in_graph = None, False
 
+    side = torch.cuda.Stream(device=dev)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+
     def step_body(record_events):
+        # The layers' new K/V rows go into window slot start + len, which no
+        # attention of this step reads, so the appends run on a forked stream
+        # and join before the window advance (len += 1).
+        cur = torch.cuda.current_stream()
+        ev_fork.record(cur)
+        side.wait_event(ev_fork)
+        with torch.cuda.stream(side):
+            for l in range(LAYERS):
+                kvarn.append_window(kn[l], vn[l], win_k[l], win_v[l], win_start, win_len)
+        ev_join.record(side)
         for l in range(LAYERS):
             if record_events:
                 ev_split[l][0].record()
@@ -391,7 +406,7 @@ def main():
             if record_events:
                 ev_split[l][1].record()
             kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
-            kvarn.append_window(kn[l], vn[l], win_k[l], win_v[l], win_start, win_len)
+        cur.wait_event(ev_join)
         kvarn.window_advance(win_start, win_len, None, 1, 0, cap)
 
     per_step_launches = 3 * LAYERS + 1

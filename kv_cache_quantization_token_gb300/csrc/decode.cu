@@ -914,72 +914,65 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 }
 
-// LSE combine: one CTA of 512 threads per (query head, sequence). Each group of
-// D/4 threads reads whole item rows (float4 per thread, coalesced) for every
-// (512/(D/4))-th item; the groups are summed in shared memory, the tile part is
-// rotated back with one FWHT, the window part added, and the result divided by
-// the softmax sum.
+// LSE combine: one CTA of 512 threads per (query head, sequence). Each group
+// of D/4 threads reads whole item rows (float4 per thread, coalesced) of
+// every (512/(D/4))-th item in one pass, keeping its own running maximum; the
+// groups are merged in shared memory, the tile part is rotated back with one
+// FWHT, the window part added, and the result divided by the softmax sum.
 template <int D>
 __global__ void __launch_bounds__(512)
 decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__ ws_acc, int Hq,
                       int items, int tile_items, float* __restrict__ out) {
-  constexpr int NTH = 512, TPR = D / 4, NG = NTH / TPR, NWC = NTH / 32;
+  constexpr int NTH = 512, TPR = D / 4, NG = NTH / TPR;
   __shared__ float4 grp[2][NG][TPR];
+  __shared__ float gm[NG], gl[NG];
   __shared__ float x[D];
-  __shared__ float redf[NWC];
-  __shared__ float redl[NWC];
-  __shared__ int redi[NWC];
-  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int64_t base = ((int64_t)b * Hq + hq) * items;
   pdl_trigger();
   pdl_wait();
-  float M = kNegInf;
-  int poison = 0;
-  for (int j = tid; j < items; j += NTH) {
-    const float lj = ws_ml[(base + j) * 2 + 1];
-    if (!(lj >= 0.f)) poison = 1;
-    if (lj > 0.f) M = fmaxf(M, ws_ml[(base + j) * 2]);
-  }
-  M = warp_max(M);
-  poison = __any_sync(0xffffffffu, poison);
-  if (lane == 0) { redf[wid] = M; redi[wid] = poison; }
-  __syncthreads();
-  M = redf[0];
-  poison = redi[0];
-#pragma unroll
-  for (int w = 1; w < NWC; ++w) { M = fmaxf(M, redf[w]); poison |= redi[w]; }
   const int gi = tid / TPR, c4 = tid % TPR;
+  float m = kNegInf, L = 0.f;
   float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), aw = ar;
-  float L = 0.f;
+  int poison = 0;
 #pragma unroll 4
   for (int j = gi; j < items; j += NG) {
     const float mj = ws_ml[(base + j) * 2], lj = ws_ml[(base + j) * 2 + 1];
-    const float w = lj > 0.f ? expf(mj - M) : 0.f;
-    if (c4 == 0) L = fmaf(lj > 0.f ? lj : 0.f, w, L);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (w != 0.f) v = reinterpret_cast<const float4*>(ws_acc + (base + j) * D)[c4];
-    float4& a = j < tile_items ? ar : aw;
-    a.x = fmaf(w, v.x, a.x);
-    a.y = fmaf(w, v.y, a.y);
-    a.z = fmaf(w, v.z, a.z);
-    a.w = fmaf(w, v.w, a.w);
+    if (!(lj >= 0.f)) poison = 1;  // NaN partial (a failed split item)
+    if (lj > 0.f) {
+      const float4 v = reinterpret_cast<const float4*>(ws_acc + (base + j) * D)[c4];
+      const float mn = fmaxf(m, mj);
+      const float a = expf(m - mn), w = expf(mj - mn);  // a = 0 while m = -inf
+      const bool tile = j < tile_items;
+      const float wt = tile ? w : 0.f, ww = tile ? 0.f : w;
+      ar = make_float4(fmaf(ar.x, a, wt * v.x), fmaf(ar.y, a, wt * v.y), fmaf(ar.z, a, wt * v.z),
+                       fmaf(ar.w, a, wt * v.w));
+      aw = make_float4(fmaf(aw.x, a, ww * v.x), fmaf(aw.y, a, ww * v.y), fmaf(aw.z, a, ww * v.z),
+                       fmaf(aw.w, a, ww * v.w));
+      L = fmaf(L, a, w * lj);
+      m = mn;
+    }
   }
   grp[0][gi][c4] = ar;
   grp[1][gi][c4] = aw;
-  L = warp_sum(L);
-  if (lane == 0) redl[wid] = L;
-  __syncthreads();
-  L = 0.f;
-#pragma unroll
-  for (int w = 0; w < NWC; ++w) L += redl[w];
-  float xr = 0.f, xw = 0.f;
+  if (c4 == 0) {
+    gm[gi] = m;
+    gl[gi] = L;
+  }
+  poison = __syncthreads_or(poison);
+  float xr = 0.f, xw = 0.f, Lt = 0.f;
   if (tid < D) {
+    float M = kNegInf;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) M = fmaxf(M, gm[g]);
     const float* g0 = reinterpret_cast<const float*>(grp[0]);
     const float* g1 = reinterpret_cast<const float*>(grp[1]);
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      xr += g0[g * D + tid];
-      xw += g1[g * D + tid];
+      const float f = gm[g] == kNegInf ? 0.f : expf(gm[g] - M);
+      xr = fmaf(f, g0[g * D + tid], xr);
+      xw = fmaf(f, g1[g * D + tid], xw);
+      Lt = fmaf(f, gl[g], Lt);
     }
     // FWHT: butterflies within the warp by shuffles, across warps through x[]
 #pragma unroll
@@ -999,7 +992,7 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   }
   if (tid < D) {
     float r = 0.f;
-    if (L > 0.f) r = (xr * (1.0f / sqrtf((float)D)) + xw) / L;
+    if (Lt > 0.f) r = (xr * (1.0f / sqrtf((float)D)) + xw) / Lt;
     if (poison) r = NAN;
     out[((int64_t)b * Hq + hq) * D + tid] = r;
   }
