@@ -167,17 +167,24 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// fp16 pair {1 + c_lo/16, 1 + c_hi/16} from nibble j of the low and of the high
-// 16-bit half of x (the code sits in mantissa bits 9..6).
-__device__ __forceinline__ uint32_t k_frag(uint32_t x, int j) {
-  const uint32_t y = j == 0 ? (x << 6) : j == 1 ? (x << 2) : j == 2 ? (x >> 2) : (x >> 6);
-  return (y & 0x03C003C0u) | 0x3C003C00u;
+// y * m + c on the integer multiply-add unit (keeps these off the logic pipe,
+// which the masks already occupy).
+__device__ __forceinline__ uint32_t imad(uint32_t y, uint32_t m, uint32_t c) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(y), "r"(m), "r"(c));
+  return r;
 }
-// fp16 pair {1 + c_lo/4, 1 + c_hi/4} from 2-bit field m of each 16-bit half of x
-// (the code sits in mantissa bits 9..8).
+// fp16 pair {1 + c_lo/16, 1 + c_hi/16} from nibble j (0 or 1) of the low and of
+// the high 16-bit half of x (the code goes to mantissa bits 9..6); nibbles 2
+// and 3 are taken as nibbles 0 and 1 of x >> 8.
+__device__ __forceinline__ uint32_t k_frag(uint32_t x, int j) {
+  return imad(x & (j == 0 ? 0x000F000Fu : 0x00F000F0u), j == 0 ? 64u : 4u, 0x3C003C00u);
+}
+// fp16 pair {1 + c_lo/4, 1 + c_hi/4} from 2-bit field m (0..3) of each 16-bit
+// half of x (the code goes to mantissa bits 9..8); fields 4..7 are taken as
+// fields 0..3 of x >> 8.
 __device__ __forceinline__ uint32_t v_frag(uint32_t x, int m) {
-  const uint32_t y = m < 4 ? (x << (8 - 2 * m)) : (x >> (2 * m - 8));
-  return (y & 0x03000300u) | 0x3C003C00u;
+  return imad(x & (0x00030003u << (2 * m)), 1u << (8 - 2 * m), 0x3C003C00u);
 }
 // Physical offset of logical byte o of a 1024-byte aligned region written by a
 // TMA copy with 128-byte swizzling (16-byte chunk index XOR 128-byte line index).
@@ -700,9 +707,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64 + 16 * w2)), x[0], x[1], x[2], x[3]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const uint32_t xl = x[2 * u], xh = x[2 * u + 1];
+          const uint32_t xl = x[2 * u], xh = x[2 * u + 1], xl8 = xl >> 8, xh8 = xh >> 8;
           const uint32_t a00 = k_frag(xl, 0), a01 = k_frag(xl, 1), a02 = k_frag(xh, 0), a03 = k_frag(xh, 1);
-          const uint32_t a10 = k_frag(xl, 2), a11 = k_frag(xl, 3), a12 = k_frag(xh, 2), a13 = k_frag(xh, 3);
+          const uint32_t a10 = k_frag(xl8, 0), a11 = k_frag(xl8, 1), a12 = k_frag(xh8, 0), a13 = k_frag(xh8, 1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(acc[w2][0][nt], a00, a01, a02, a03, bf[u][nt].x, bf[u][nt].y);
@@ -833,12 +840,17 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
         ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * (D / 4) + 16 * sl)), y[0], y[1], y[2],
                   y[3]);
+        const uint32_t y8[4] = {y[0] >> 8, y[1] >> 8, y[2] >> 8, y[3] >> 8};
 #pragma unroll
         for (int mu = 0; mu < 4; ++mu)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const uint32_t a0 = v_frag(y[2 * j], 2 * mu), a1 = v_frag(y[2 * j], 2 * mu + 1);
-            const uint32_t a2 = v_frag(y[2 * j + 1], 2 * mu), a3 = v_frag(y[2 * j + 1], 2 * mu + 1);
+            // fields 2 mu and 2 mu + 1: fields 0..3 of y, or of y >> 8 for mu >= 2
+            const uint32_t ya = mu < 2 ? y[2 * j] : y8[2 * j];
+            const uint32_t yb = mu < 2 ? y[2 * j + 1] : y8[2 * j + 1];
+            const int f = 2 * (mu & 1);
+            const uint32_t a0 = v_frag(ya, f), a1 = v_frag(ya, f + 1);
+            const uint32_t a2 = v_frag(yb, f), a3 = v_frag(yb, f + 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
@@ -935,22 +947,37 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   float m = kNegInf, L = 0.f;
   float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), aw = ar;
   int poison = 0;
-#pragma unroll 4
-  for (int j = gi; j < items; j += NG) {
-    const float mj = ws_ml[(base + j) * 2], lj = ws_ml[(base + j) * 2 + 1];
-    if (!(lj >= 0.f)) poison = 1;  // NaN partial (a failed split item)
-    if (lj > 0.f) {
-      const float4 v = reinterpret_cast<const float4*>(ws_acc + (base + j) * D)[c4];
-      const float mn = fmaxf(m, mj);
-      const float a = expf(m - mn), w = expf(mj - mn);  // a = 0 while m = -inf
-      const bool tile = j < tile_items;
-      const float wt = tile ? w : 0.f, ww = tile ? 0.f : w;
-      ar = make_float4(fmaf(ar.x, a, wt * v.x), fmaf(ar.y, a, wt * v.y), fmaf(ar.z, a, wt * v.z),
-                       fmaf(ar.w, a, wt * v.w));
-      aw = make_float4(fmaf(aw.x, a, ww * v.x), fmaf(aw.y, a, ww * v.y), fmaf(aw.z, a, ww * v.z),
-                       fmaf(aw.w, a, ww * v.w));
-      L = fmaf(L, a, w * lj);
-      m = mn;
+  constexpr int U = 8;  // items per thread whose loads are issued together
+  for (int j0 = gi; j0 < items; j0 += U * NG) {
+    float2 mlv[U];
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * NG;
+      mlv[u] = make_float2(kNegInf, 0.f);
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < items) {
+        mlv[u] = reinterpret_cast<const float2*>(ws_ml)[base + j];
+        v[u] = reinterpret_cast<const float4*>(ws_acc + (base + j) * D)[c4];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u * NG;
+      const float mj = mlv[u].x, lj = mlv[u].y;
+      if (j < items && !(lj >= 0.f)) poison = 1;  // NaN partial (a failed split item)
+      if (lj > 0.f) {  // empty items (never written) are skipped before any arithmetic
+        const float mn = fmaxf(m, mj);
+        const float a = expf(m - mn), w = expf(mj - mn);  // a = 0 while m = -inf
+        const bool tile = j < tile_items;
+        const float wt = tile ? w : 0.f, ww = tile ? 0.f : w;
+        ar = make_float4(fmaf(ar.x, a, wt * v[u].x), fmaf(ar.y, a, wt * v[u].y),
+                         fmaf(ar.z, a, wt * v[u].z), fmaf(ar.w, a, wt * v[u].w));
+        aw = make_float4(fmaf(aw.x, a, ww * v[u].x), fmaf(aw.y, a, ww * v[u].y),
+                         fmaf(aw.z, a, ww * v[u].z), fmaf(aw.w, a, ww * v[u].w));
+        L = fmaf(L, a, w * lj);
+        m = mn;
+      }
     }
   }
   grp[0][gi][c4] = ar;
