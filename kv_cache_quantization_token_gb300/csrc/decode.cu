@@ -4,9 +4,9 @@
 // grid over (head, tile range) with early exit, followed by an LSE combine;
 // the deferred inverse WHT is applied after combining the rotated partials):
 //
-//   split kernel   grid (item, KV head, sequence), 4 warps per CTA. Items
-//                  0..tile_items-1 own 2 consecutive packed tiles, staged in
-//                  shared memory by TMA, one per warp pair; each warp takes 64
+//   split kernel   grid (item, KV head, sequence), 4 or 8 warps per CTA.
+//                  Items 0..tile_items-1 own 2 or 4 consecutive packed tiles,
+//                  staged in shared memory by TMA, one per warp pair; each warp takes 64
 //                  tokens of its tile: the score and value contractions run
 //                  as mma.sync m16n8k16 with A fragments built straight from
 //                  the packed codes, and the warp keeps its own streaming-
@@ -284,11 +284,11 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
   if (lane == 0) qmax[h] = mx;
 }
 
-template <int D, int GP>
+template <int D, int GP, int NW_>
 struct DC {
-  static constexpr int NW = 4;                                  // warps per CTA
+  static constexpr int NW = NW_;                                // warps per CTA (4 or 8)
   static constexpr int NTHR = 32 * NW;
-  static constexpr int TPS = 2;                                 // tiles per item, one per warp pair
+  static constexpr int TPS = NW / 2;                            // tiles per item, one per warp pair
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
   static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
@@ -358,8 +358,8 @@ __device__ __forceinline__ void cta_max(float (&v)[N], float* red, int tid) {
   }
 }
 
-template <int D, int GP>
-__global__ void __launch_bounds__(128)
+template <int D, int GP, int NW_>
+__global__ void __launch_bounds__(32 * NW_)
 decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
                     const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
                     const float* __restrict__ win_k, const float* __restrict__ win_v,
@@ -367,7 +367,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
-  using C = DC<D, GP>;
+  using C = DC<D, GP, NW_>;
   using R = Rec<D>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
   constexpr int HB = C::HB;
@@ -1064,16 +1064,16 @@ cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int GP>
+template <int D, int GP, int NW>
 cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  using C = DC<D, GP>;
+  using C = DC<D, GP, NW>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_split_kernel<D, GP>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, NW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM + 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -1084,7 +1084,7 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   const unsigned fl = launch_flags();
   const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
   LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::SMEM + 1024, st);
-  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP>, a.q, a.tiles, a.tile_table,
+  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW>, a.q, a.tiles, a.tile_table,
                             a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
                             a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale,
                             ws_ml, ws_acc, prefetch, tmap);
@@ -1093,8 +1093,13 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
 template <int D, int GP>
 cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  if (p.tiles_per_item != DC<D, GP>::TPS) return cudaErrorInvalidValue;
-  return launch_split_t<D, GP>(p, a, ws_ml, ws_acc, st);
+  switch (p.tiles_per_item) {  // a warp pair per tile
+    case 2: return launch_split_t<D, GP, 4>(p, a, ws_ml, ws_acc, st);
+    case 4:
+      if constexpr (D <= 128) return launch_split_t<D, GP, 8>(p, a, ws_ml, ws_acc, st);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int D>
@@ -1116,20 +1121,35 @@ void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** 
   *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 }  // namespace
 
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  // four warps per CTA, a warp pair per tile (DC<D, GP>)
-  const int tps = 2;
+  // a warp pair per tile (DC<D, GP, NW>): 2 tiles per CTA, or 4 (eight warps)
+  // once the grid has at least 4 tiles per SM, which halves the partials the
+  // combine reads and the per-CTA set-up (head_dim 256 keeps 2: shared memory)
+  const int64_t total = (int64_t)B * Hkv * max_tiles;
+  const int tps = (D <= 128 && total >= 4LL * sm_count()) ? 4 : 2;
+  const int nw = 2 * tps;
   p->tiles_per_item = tps;
   p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
-  // window rows per warp and per item, as DC<D, GP>::WCH and its 4 warps
+  // window rows per warp and per item, as DC<D, GP, NW>::WCH and its NW warps
   const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
-  const int w0 = (tps * rb) / (4 * 2 * D * 4);
+  const int w0 = (tps * rb) / (nw * 2 * D * 4);
   const int wch = w0 >= 16 ? 16 : w0 >= 8 ? 8 : w0 >= 4 ? 4 : 2;
-  p->win_items = win_capacity > 0 ? (win_capacity + 4 * wch - 1) / (4 * wch) : 0;
+  p->win_items = win_capacity > 0 ? (win_capacity + nw * wch - 1) / (nw * wch) : 0;
   p->items = p->tile_items + p->win_items;
   const size_t parts = (size_t)B * Hq * p->items;
   const size_t ml = (parts * 2 * sizeof(float) + 255) / 256 * 256;
