@@ -514,6 +514,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
+    seq_gbs = split_bytes / (split_seq_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC["decode_split"]
     traffic = tr["bytes"] if tr["src_sha"] == src_sha("decode.cu") else None
 
@@ -582,17 +583,22 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": workload_config(),
-            "decode": {"ctx_end": ctx_now, "split_kernel_ms": split_ms, "split_gbs": split_gbs,
-                       "split_bytes_per_launch": split_bytes, "timing": split_how,
-                       "split_back_to_back_ms": split_seq_ms,
-                       "split_back_to_back_gbs": split_bytes / (split_seq_ms * 1e-3) / 1e9,
+            "decode": {"ctx_end": ctx_now, "split_bytes_per_launch": split_bytes,
+                       "split_back_to_back_ms": split_seq_ms, "split_back_to_back_gbs": seq_gbs,
                        "back_to_back_timing": f"CUDA events around {reps} replays of a graph of "
                                               f"the {LAYERS} layers' split launches (programmatic "
-                                              f"dependent launch, records prefetched)",
+                                              f"dependent launch, records prefetched); each "
+                                              f"launch reads its own layer's cache from HBM",
+                       "split_isolated_ms": split_ms, "split_isolated_gbs": split_gbs,
+                       "isolated_timing": split_how + "; includes the launch latency",
+                       "step_attention_gbs": LAYERS * split_bytes / (ms_per_step * 1e-3) / 1e9,
+                       "step_attention_frac": LAYERS * split_bytes / (ms_per_step * 1e-3) / 1e9 / hbm,
                        "launch_flags": "PDL|PREFETCH"},
-            "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": split_gbs / hbm, "traffic": traffic,
-                         "kernel": "decode_split_kernel", "peak_source": peak_kind},
+            "roofline": {"bound": "hbm", "achieved": seq_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": seq_gbs / hbm, "traffic": traffic,
+                         "kernel": "decode_split_kernel",
+                         "timing": "average launch duration over back-to-back launches (see "
+                                   "decode.back_to_back_timing)", "peak_source": peak_kind},
             "compress": {"tile_heads_per_launch": n_units, "ms_per_launch": comp_ms,
                          "tiles_per_s": n_units / (comp_ms * 1e-3), "gbs": comp_gbs,
                          "bytes_per_launch": comp_bytes,

@@ -22,7 +22,8 @@
 //    merges across threads, so large group means do not cancel.
 //
 // Work decomposition: one CTA of 2*D threads per (unit, tensor); every thread
-// holds an 8-token x 8-channel block of the tile in registers (64 floats).
+// holds an 8-token x 8-channel block of the tile in registers (64 floats, as
+// channel pairs: the per-element arithmetic uses packed fp32x2 instructions).
 //   phase 1: each thread loads 16-byte chunks of 512/D tokens straight from
 //            global memory (fully coalesced) and runs the butterflies of the
 //            channel bits it holds (bits 0,1 and 5..log2D-1);
@@ -62,6 +63,13 @@ __device__ __forceinline__ int swz(int t, int J) {
 }
 
 __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+
+// Packed fp32x2 arithmetic (one instruction for two IEEE round-to-nearest
+// results): the per-element work below runs on channel pairs.
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 // In-register butterflies over the two low bits of a float4.
 __device__ __forceinline__ void fwht4(float4& v) {
@@ -167,23 +175,28 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 
   // ---------------- phase 2: block layout + butterflies of bits 2..4 --------
   const int cg = tid % C::NCG, tg = tid / C::NCG;
-  float y[8][8];
+  // y2[i][k] = (channel slot 2k, 2k+1) of token 8 tg + i
+  float2 y2[8][4];
+  const float2 neg1 = f2(-1.f, -1.f);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = 8 * tg + i;
+    float v[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int J = ((cg >> 2) << 3) + m;
-      y[i][m] = xs[t * D + 4 * swz<C::L>(t, J) + (cg & 3)];
+      v[m] = xs[t * D + 4 * swz<C::L>(t, J) + (cg & 3)];
     }
 #pragma unroll
-    for (int h = 1; h < 8; h <<= 1)
+    for (int k = 0; k < 4; ++k) y2[i][k] = f2(v[2 * k] + v[2 * k + 1], v[2 * k] - v[2 * k + 1]);
 #pragma unroll
-      for (int m = 0; m < 8; ++m)
-        if (!(m & h)) {
-          const float a = y[i][m], b = y[i][m | h];
-          y[i][m] = a + b;
-          y[i][m | h] = a - b;
+    for (int h = 1; h < 4; h <<= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (!(k & h)) {
+          const float2 a = y2[i][k], b = y2[i][k | h];
+          y2[i][k] = add2(a, b);
+          y2[i][k | h] = fma2(b, neg1, a);  // a - b, exactly
         }
   }
 
@@ -191,11 +204,11 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
   // for its tokens; s_own is owned by the thread pair (2p, 2p+1) of permuted
   // channel p, r_own by the lanes whose channel-group bits 0..2 encode token i.
   const float sqrt_d = sqrtf((float)D);
-  float sinv[8], rinv[8];
+  float2 sinv2[4], rinv2[8];  // (1/s') of channel pairs; (1/r, 1/r) per token
 #pragma unroll
-  for (int m = 0; m < 8; ++m) sinv[m] = 1.0f / sqrt_d;
+  for (int k = 0; k < 4; ++k) sinv2[k] = f2(1.0f / sqrt_d, 1.0f / sqrt_d);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) rinv[i] = 1.0f;
+  for (int i = 0; i < 8; ++i) rinv2[i] = f2(1.0f, 1.0f);
   float s_own = sqrt_d, r_own = 1.0f;
   const int p_own = tid >> 1, h_own = tid & 1;
   // token held by this lane after the row halving: bits (cg&1, cg>>1&1, cg>>2&1) -> 4,2,1
@@ -218,15 +231,19 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     // ---- channel step: std over the 128 tokens of Y' / r ----
     float cm[8], cq[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      float s = 0.f;
+    for (int k = 0; k < 4; ++k) {
+      float2 s2 = f2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s = fmaf(y[i][m], rinv[i], s);
-      const float mean = s * 0.125f;
-      float q = 0.f;
+      for (int i = 0; i < 8; ++i) s2 = fma2(y2[i][k], rinv2[i], s2);
+      const float2 nmean = mul2(s2, f2(-0.125f, -0.125f));
+      float2 q2 = f2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { const float d = fmaf(y[i][m], rinv[i], -mean); q = fmaf(d, d, q); }
-      cm[m] = mean; cq[m] = q;
+      for (int i = 0; i < 8; ++i) {
+        const float2 d = fma2(y2[i][k], rinv2[i], nmean);
+        q2 = fma2(d, d, q2);
+      }
+      cm[2 * k] = -nmean.x; cm[2 * k + 1] = -nmean.y;
+      cq[2 * k] = q2.x; cq[2 * k + 1] = q2.y;
     }
     if (C::TGW >= 1) halve_mv<8>(cm, cq, 1 << C::CG_BITS, (lane >> C::CG_BITS) & 1, 8.f);
     if (C::TGW >= 2) halve_mv<4>(cm, cq, 1 << (C::CG_BITS + 1), (lane >> (C::CG_BITS + 1)) & 1, 16.f);
@@ -252,20 +269,24 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     }
     __syncthreads();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) sinv[m] = ch_a[m * C::NCG + cg];
+    for (int k = 0; k < 4; ++k) sinv2[k] = f2(ch_a[(2 * k) * C::NCG + cg], ch_a[(2 * k + 1) * C::NCG + cg]);
 
     // ---- token step: std over the D channels of Y' / s' ----
     float rm[8], rq[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float s = 0.f;
+      float2 s2 = f2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) s = fmaf(y[i][m], sinv[m], s);
-      const float mean = s * 0.125f;
-      float q = 0.f;
+      for (int k = 0; k < 4; ++k) s2 = fma2(y2[i][k], sinv2[k], s2);
+      const float mean = (s2.x + s2.y) * 0.125f;
+      const float2 nmean = f2(-mean, -mean);
+      float2 q2 = f2(0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) { const float d = fmaf(y[i][m], sinv[m], -mean); q = fmaf(d, d, q); }
-      rm[i] = mean; rq[i] = q;
+      for (int k = 0; k < 4; ++k) {
+        const float2 d = fma2(y2[i][k], sinv2[k], nmean);
+        q2 = fma2(d, d, q2);
+      }
+      rm[i] = mean; rq[i] = q2.x + q2.y;
     }
     halve_mv<8>(rm, rq, 1, lane & 1, 8.f);
     halve_mv<4>(rm, rq, 2, (lane >> 1) & 1, 16.f);
@@ -277,7 +298,10 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       if (usable(var, rm[0])) r_own = sqrtf(var);
       const float ri = 1.0f / r_own;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rinv[i] = __shfl_sync(0xffffffffu, ri, src_lane(i));
+      for (int i = 0; i < 8; ++i) {
+        const float r = __shfl_sync(0xffffffffu, ri, src_lane(i));
+        rinv2[i] = f2(r, r);
+      }
     }
   }
 
@@ -285,7 +309,9 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int m = 0; m < 8; ++m) y[i][m] = (y[i][m] * sinv[m]) * rinv[i];
+    for (int k = 0; k < 4; ++k) y2[i][k] = mul2(mul2(y2[i][k], sinv2[k]), rinv2[i]);
+  // scalar view of the normalised block: y(i, m)
+  auto y = [&](int i, int m) -> float { return (m & 1) ? y2[i][m >> 1].y : y2[i][m >> 1].x; };
 
   const int t_own = 8 * tg + tau;
   const bool tok_writer = (C::CG_BITS == 3) || ((cg >> 3) & 1) == 0;
@@ -295,9 +321,9 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     float lo[8], hi[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      lo[m] = y[0][m]; hi[m] = y[0][m];
+      lo[m] = y(0, m); hi[m] = y(0, m);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) { lo[m] = fminf(lo[m], y[i][m]); hi[m] = fmaxf(hi[m], y[i][m]); }
+      for (int i = 1; i < 8; ++i) { lo[m] = fminf(lo[m], y(i, m)); hi[m] = fmaxf(hi[m], y(i, m)); }
     }
     if (C::TGW >= 1) halve_mm<8>(lo, hi, 1 << C::CG_BITS, (lane >> C::CG_BITS) & 1);
     if (C::TGW >= 2) halve_mm<4>(lo, hi, 1 << (C::CG_BITS + 1), (lane >> (C::CG_BITS + 1)) & 1);
@@ -329,26 +355,32 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     if (tok_writer) reinterpret_cast<float*>(stage + R::kKR)[t_own] = r_own;
     __syncthreads();
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float l = ch_a[m * C::NCG + cg], inv = ch_b[m * C::NCG + cg];
-      uint32_t w = 0;
+    for (int k = 0; k < 4; ++k) {
+      // code = floor((y - lo) / delta + 1/2) for channel slots 2k, 2k+1
+      const float2 nl = f2(-ch_a[(2 * k) * C::NCG + cg], -ch_a[(2 * k + 1) * C::NCG + cg]);
+      const float2 inv = f2(ch_b[(2 * k) * C::NCG + cg], ch_b[(2 * k + 1) * C::NCG + cg]);
+      uint32_t w0 = 0, w1 = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        int code = __float2int_rd((y[i][m] - l) * inv + 0.5f);
-        code = min(15, max(0, code));
-        w |= (uint32_t)code << (4 * i);
+        const float2 u = fma2(add2(y2[i][k], nl), inv, f2(0.5f, 0.5f));
+        const int c0 = min(15, max(0, __float2int_rd(u.x)));
+        const int c1 = min(15, max(0, __float2int_rd(u.y)));
+        w0 |= (uint32_t)c0 << (4 * i);
+        w1 |= (uint32_t)c1 << (4 * i);
       }
-      const int c = (cg & 3) | (m << 2) | ((cg >> 2) << 5);
-      *reinterpret_cast<uint32_t*>(stage + R::kKCodes + c * (kTile / 2) + 4 * tg) = w;
+      const int ca = (cg & 3) | ((2 * k) << 2) | ((cg >> 2) << 5);
+      const int cb = (cg & 3) | ((2 * k + 1) << 2) | ((cg >> 2) << 5);
+      *reinterpret_cast<uint32_t*>(stage + R::kKCodes + ca * (kTile / 2) + 4 * tg) = w0;
+      *reinterpret_cast<uint32_t*>(stage + R::kKCodes + cb * (kTile / 2) + 4 * tg) = w1;
     }
   } else {
     // ---------------- V: 2-bit RTN per token over 128-channel groups ---------
     float lo[8], hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      lo[i] = y[i][0]; hi[i] = y[i][0];
+      lo[i] = y(i, 0); hi[i] = y(i, 0);
 #pragma unroll
-      for (int m = 1; m < 8; ++m) { lo[i] = fminf(lo[i], y[i][m]); hi[i] = fmaxf(hi[i], y[i][m]); }
+      for (int m = 1; m < 8; ++m) { lo[i] = fminf(lo[i], y(i, m)); hi[i] = fmaxf(hi[i], y(i, m)); }
     }
     halve_mm<8>(lo, hi, 1, lane & 1);
     halve_mm<4>(lo, hi, 2, (lane >> 1) & 1);
@@ -372,11 +404,14 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       const float l = __shfl_sync(0xffffffffu, lo[0], src_lane(i));
       const float iv = __shfl_sync(0xffffffffu, inv, src_lane(i));
       unsigned long long w = 0;
+      const float2 nl = f2(-l, -l), iv2 = f2(iv, iv);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        int code = __float2int_rd((y[i][m] - l) * iv + 0.5f);
-        code = min(3, max(0, code));
-        w |= (unsigned long long)code << (8 * m + 2 * (cg & 3));
+      for (int k = 0; k < 4; ++k) {
+        const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
+        const int c0 = min(3, max(0, __float2int_rd(u.x)));
+        const int c1 = min(3, max(0, __float2int_rd(u.y)));
+        w |= (unsigned long long)c0 << (8 * (2 * k) + 2 * (cg & 3));
+        w |= (unsigned long long)c1 << (8 * (2 * k + 1) + 2 * (cg & 3));
       }
       w |= __shfl_xor_sync(0xffffffffu, w, 1);
       w |= __shfl_xor_sync(0xffffffffu, w, 2);
