@@ -10,9 +10,10 @@
 // tile k holding positions [128k, 128k+128) and window token w position
 // 128 * n_tiles + w.
 //
-// One CTA (4 warps) owns a KV head and 128 score rows: the G query heads of
+// One CTA (8 warps) owns a KV head and 128 score rows: the G query heads of
 // the GQA group times 128/G consecutive positions, so every dequantised tile
-// serves the whole group. All keys live in the rotated space: the query is
+// serves the whole group. Two threads share each score row (one per half of
+// the 128 keys of a block), and the dequantisation is split the same way. All keys live in the rotated space: the query is
 // q' = H q (times scale * log2 e), packed tiles dequantise to
 // K~ = r_t s_c (delta code + lo) and V~ likewise, and window rows are rotated
 // when staged (H k, H v). Per 128-key block:
@@ -23,12 +24,13 @@
 //      Ql Kh: one fp16 rounding of either operand costs up to 1e-2 in the
 //      output through cancellation in q.k (rotated keys are large), the
 //      split keeps the scores to about 2^-22;
-//   3. each thread owns one score row: causal mask, online softmax in base 2
-//      (the running max is only moved, and O rescaled in TMEM, when a score
-//      exceeds it by more than 8), P written as fp16 to shared memory;
+//   3. two threads own each score row (64 keys each): causal mask, online
+//      softmax in base 2 (the running max is only moved, and O rescaled in
+//      TMEM, when a score exceeds it by more than 8), P written as fp16 to
+//      shared memory;
 //   4. O += P V~ on tcgen05 into TMEM.
-// At the end each thread divides its O row by the row sum and applies the one
-// inverse rotation (H is its own inverse). Every wait is bounded; a CTA that
+// At the end one thread per row divides the O row by the row sum and applies
+// the one inverse rotation (H is its own inverse). Every wait is bounded; a CTA that
 // gives up writes NaN rows, frees its TMEM and returns.
 #include <cuda_fp16.h>
 #include <math.h>
@@ -172,7 +174,9 @@ struct PC {
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int OFF_BAR = OFF_REC + 2 * RB;   // mbarriers: rec[2], s, o
   static constexpr int OFF_MISC = OFF_BAR + 64;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack to align the base to 1024
+  static constexpr int OFF_XCH = OFF_MISC + 64;      // f32 [2][128] row max / sum exchange
+  static constexpr int SMEM = OFF_XCH + 2 * 128 * 4 + 1024;  // + slack to align the base to 1024
+  static constexpr int NTHR = 256;                   // two threads per score row
   static constexpr int TMEM_COLS = 256;              // S: columns 0..127, O: 128..128+D-1
   static_assert(D == 64 || D == 128, "prefill head_dim");
 };
@@ -190,7 +194,7 @@ struct PrefillArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
   using P = PC<D>;
   using R = Rec<D>;
   extern __shared__ unsigned char smem_raw[];
@@ -208,13 +212,17 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
   uint64_t* bar_o = bar_rec + 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
   int* fail = reinterpret_cast<int*>(sm + P::OFF_MISC + 4);
+  float* xch = reinterpret_cast<float*>(sm + P::OFF_XCH);  // [2][128]
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  // score row of this thread and its half of the key block (TMEM lanes of warp
+  // w are 32 (w % 4) .. +31, so rows and TMEM lanes agree)
+  const int row = tid & 127, half = tid >> 7;
   const int kvh = blockIdx.y;
   const int ppc = 128 / a.G;                 // positions per CTA
   const int i0 = blockIdx.x * ppc;           // first chunk row of this CTA
-  // score row `tid` <-> (head g = tid / ppc, chunk position i0 + tid % ppc)
-  const int my_g = tid / ppc, my_i = i0 + tid % ppc;
+  // score row `row` <-> (head g = row / ppc, chunk position i0 + row % ppc)
+  const int my_g = row / ppc, my_i = i0 + row % ppc;
   const bool my_valid = my_i < a.C && my_g < a.G;
   const int64_t my_pos = a.pos0 + my_i;
   const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
@@ -235,9 +243,9 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
   {
     int bad = 0;
     const int64_t* tr = a.tile_table + (int64_t)kvh * a.table_stride;
-    for (int t = tid; t < n_tile_blk; t += 128) bad |= (tr[t] & 15) != 0 || tr[t] < 0;
+    for (int t = tid; t < n_tile_blk; t += P::NTHR) bad |= (tr[t] & 15) != 0 || tr[t] < 0;
     if (__syncthreads_or(bad)) {
-      if (my_valid)
+      if (my_valid && half == 0)
         for (int c = 0; c < D; ++c) a.out[((int64_t)my_i * a.Hq + hq) * D + c] = NAN;
       return;
     }
@@ -256,8 +264,8 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
                  "r"(P::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // Q' row: rotate, scale, fp16 into the swizzled A operand
-  {
+  // Q' row: rotate, scale, fp16 into the swizzled A operand (one thread per row)
+  if (half == 0) {
     float x[D];
     if (my_valid) {
       const float4* src = reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D);
@@ -277,8 +285,8 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         split2(x[8 * c8 + 2 * e] * a.qscale, x[8 * c8 + 2 * e + 1] * a.qscale, hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(sQh + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-      *reinterpret_cast<uint4*>(sQl + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+      *reinterpret_cast<uint4*>(sQh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+      *reinterpret_cast<uint4*>(sQl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s = tmem, t_o = tmem + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // TMEM lanes of this warp
   const int64_t* trow = a.tile_table + (int64_t)kvh * a.table_stride;
 
   // prefetch the first packed record
@@ -322,13 +330,15 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
       const float* vR = reinterpret_cast<const float*>(rec + R::kVR);
       const float* vD = reinterpret_cast<const float*>(rec + R::kVDelta);
       const float* vL = reinterpret_cast<const float*>(rec + R::kVLo);
-      // K~: thread -> channel(s), all 128 keys of the channel row
-      for (int c = tid; c < D; c += 128) {
+      // K~: thread -> channel tid % D and a contiguous share of its 128 keys
+      {
+        constexpr int NKG = P::NTHR / D, WPG = 16 / NKG;  // key groups, 8-key words per group
+        const int c = tid % D, kg = tid / D;
         const float s = kS[c], d = kD[c] * s, lo = kL[c] * s;
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
+        const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
 #pragma unroll 4
-        for (int w4 = 0; w4 < 16; ++w4) {
-          const uint32_t wd = row[w4];
+        for (int w4 = WPG * kg; w4 < WPG * (kg + 1); ++w4) {
+          const uint32_t wd = crow[w4];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int t = 8 * w4 + i;
@@ -340,14 +350,14 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
           }
         }
       }
-      // V~^T: thread -> key t, all D channels of the token row
+      // V~^T: thread -> key t, half of the D channels of the token row
       {
-        const int t = tid;
+        const int t = row;
         const float r = vR[t];
-        const unsigned char* row = rec + R::kVCodes + t * (D / 4);
+        const unsigned char* vrow = rec + R::kVCodes + t * (D / 4);
 #pragma unroll 4
-        for (int jb = 0; jb < D / 4; ++jb) {
-          const uint32_t byte = row[jb];
+        for (int jb = half * (D / 8); jb < (half + 1) * (D / 8); ++jb) {
+          const uint32_t byte = vrow[jb];
           const int g = (4 * jb) / R::kVGroup;
           const float d = vD[t * R::kGv + g] * r, lo = vL[t * R::kGv + g] * r;
 #pragma unroll
@@ -363,12 +373,13 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
       const int wb = j - n_tile_blk;
       kpos0 = win_pos0 + 128LL * wb;
       nkeys = min(128, a.win_len - 128 * wb);
-      const int t = tid;
+      const int t = row;
       float x[D];
       const bool have = t < nkeys;
       const int64_t slot = ((int64_t)a.win_start + 128 * wb + t) % a.win_cap;
       const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
-      // K row
+      // K row (threads of the first half)
+      if (half == 0) {
       if (have) {
         const float4* src = reinterpret_cast<const float4*>(a.win_k + rbase);
 #pragma unroll
@@ -389,7 +400,8 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
         *reinterpret_cast<uint4*>(sKh + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
         *reinterpret_cast<uint4*>(sKl + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
       }
-      // V row -> column t of V~^T
+      } else {
+      // V row -> column t of V~^T (threads of the second half)
       if (have) {
         const float4* src = reinterpret_cast<const float4*>(a.win_v + rbase);
 #pragma unroll
@@ -404,6 +416,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
       }
 #pragma unroll
       for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(x[c]);
+      }
     }
     // ---- 2. S = Q' K~^T
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -424,53 +437,57 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
     ++issued_s;
     if (!mbar_wait_bounded(bar_s, j & 1)) *fail = 1;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // ---- 3. softmax of this thread's row
-    float s[128];
+    // ---- 3. softmax of this thread's half row (keys 64 half .. 64 half + 63)
+    float sv[64];
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+    for (int c0 = 0; c0 < 64; c0 += 32) {
       float v[32];
-      tmem_ld32(t_s + lane_base + c0, v);
+      tmem_ld32(t_s + lane_base + 64 * half + c0, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[c0 + i] = v[i];
+      for (int i = 0; i < 32; ++i) sv[c0 + i] = v[i];
     }
     float mblk = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < 128; ++t) {
+    for (int u = 0; u < 64; ++u) {
+      const int t = 64 * half + u;
       const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
-      s[t] = vis ? s[t] : -INFINITY;
-      mblk = fmaxf(mblk, s[t]);
+      sv[u] = vis ? sv[u] : -INFINITY;
+      mblk = fmaxf(mblk, sv[u]);
     }
+    xch[half * 128 + row] = mblk;
+    __syncthreads();
+    mblk = fmaxf(xch[row], xch[128 + row]);  // the row's block maximum, same in both threads
     // move the reference max (and rescale O) only when a score exceeds it by > 8
     const bool need = mblk > m_ref + 8.0f;
     const float m_new = need ? mblk : m_ref;
     const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
     if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         float v[32];
-        tmem_ld32(t_o + lane_base + c0, v);
+        tmem_ld32(t_o + lane_base + half * (D / 2) + c0, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(t_o + lane_base + c0, v);
+        tmem_st32(t_o + lane_base + half * (D / 2) + c0, v);
       }
     }
     l_sum *= alpha;
     m_ref = m_new;
     float rs = 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < 16; ++c8) {
+    for (int c8 = 0; c8 < 8; ++c8) {
       __align__(16) __half2 h[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * c8 + 2 * e] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(s[8 * c8 + 2 * e + 1] - m_ref);
+        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * e] - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * e + 1] - m_ref);
         const __half2 hp = __floats2half2_rn(p0, p1);
         rs += __low2float(hp) + __high2float(hp);  // the sum of what the MMA will add
         h[e] = hp;
       }
-      *reinterpret_cast<uint4*>(sP + sw_off(tid, 8 * c8, 128)) = *reinterpret_cast<uint4*>(h);
+      *reinterpret_cast<uint4*>(sP + sw_off(row, 64 * half + 8 * c8, 128)) = *reinterpret_cast<uint4*>(h);
     }
-    l_sum += rs;
+    l_sum += rs;  // this thread's share of the row sum
     // ---- 4. O += P V~
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -502,8 +519,11 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
     if (!mbar_wait_bounded(bar_o, (n_blk - 1) & 1)) ok = false;
   }
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  // ---- epilogue: O / l, one inverse rotation, store
-  {
+  // ---- epilogue: O / l, one inverse rotation, store (one thread per row)
+  xch[half * 128 + row] = l_sum;
+  __syncthreads();
+  if (half == 0) {
+    const float l_row = xch[row] + xch[128 + row];
     float o[D];
     if (n_blk > 0) {
 #pragma unroll
@@ -517,7 +537,7 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
       for (int c = 0; c < D; ++c) o[c] = 0.f;
     }
-    const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+    const float inv = l_row > 0.f ? 1.0f / l_row : 0.f;
 #pragma unroll
     for (int c = 0; c < D; ++c) o[c] *= inv;
     fwht_reg<D>(o);
@@ -552,7 +572,7 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
-  prefill_kernel<D><<<grid, 128, P::SMEM, st>>>(a);
+  prefill_kernel<D><<<grid, P::NTHR, P::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
