@@ -47,9 +47,10 @@ C_TILES, C_HEADS = 256, 8
 # DRAM bytes per launch from an ncu capture, keyed by the kernel source they
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
-    "decode_split": {"src_sha": None, "bytes": None},
-    # 2 x (134.30 MB read + 5.99 MB written) for 1024 tile-heads, scaled to 2048
-    "compress": {"src_sha": "278c323257dc925a", "bytes": 280588800},
+    # one 16k-context layer: 17.39 MB read, nothing written back within the launch
+    "decode_split": {"src_sha": "4ee725ce3260e326", "bytes": 17392896},
+    # 2 x (134.30 MB read + 5.88 MB written) for 1024 tile-heads, scaled to 2048
+    "compress": {"src_sha": "92c82f58b708b8f7", "bytes": 280351744},
 }
 
 
