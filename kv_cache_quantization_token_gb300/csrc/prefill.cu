@@ -336,9 +336,16 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
         const int c = tid % D, kg = tid / D;
         const float s = kS[c], d = kD[c] * s, lo = kL[c] * s;
         const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
-#pragma unroll 4
-        for (int w4 = WPG * kg; w4 < WPG * (kg + 1); ++w4) {
-          const uint32_t wd = crow[w4];
+        uint32_t wds[WPG];  // this thread's share of the channel row, read with 16-byte loads
+#pragma unroll
+        for (int q4 = 0; q4 < WPG / 4; ++q4) {
+          const uint4 u = reinterpret_cast<const uint4*>(crow + WPG * kg)[q4];
+          wds[4 * q4] = u.x; wds[4 * q4 + 1] = u.y; wds[4 * q4 + 2] = u.z; wds[4 * q4 + 3] = u.w;
+        }
+#pragma unroll
+        for (int u = 0; u < WPG; ++u) {
+          const int w4 = WPG * kg + u;
+          const uint32_t wd = wds[u];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int t = 8 * w4 + i;
@@ -355,9 +362,22 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
         const int t = row;
         const float r = vR[t];
         const unsigned char* vrow = rec + R::kVCodes + t * (D / 4);
-#pragma unroll 4
-        for (int jb = half * (D / 8); jb < (half + 1) * (D / 8); ++jb) {
-          const uint32_t byte = vrow[jb];
+        constexpr int HB = D / 8;  // code bytes of half a token row (16 at D=128, 8 at D=64)
+        uint32_t vw[HB / 4];       // read with one or two wide loads
+        if constexpr (HB >= 16) {
+#pragma unroll
+          for (int q4 = 0; q4 < HB / 16; ++q4) {
+            const uint4 u = reinterpret_cast<const uint4*>(vrow + half * HB)[q4];
+            vw[4 * q4] = u.x; vw[4 * q4 + 1] = u.y; vw[4 * q4 + 2] = u.z; vw[4 * q4 + 3] = u.w;
+          }
+        } else {
+          const uint2 u = *reinterpret_cast<const uint2*>(vrow + half * HB);
+          vw[0] = u.x; vw[1] = u.y;
+        }
+#pragma unroll
+        for (int ub = 0; ub < HB; ++ub) {
+          const int jb = half * HB + ub;
+          const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
           const int g = (4 * jb) / R::kVGroup;
           const float d = vD[t * R::kGv + g] * r, lo = vL[t * R::kGv + g] * r;
 #pragma unroll

@@ -94,3 +94,13 @@ def test_offset_not_multiple_of_128_poisons_only_that_head():
                                  c.win_len, c.lay).cpu().numpy()
     assert np.isnan(out[0, 4:]).all()          # query heads of KV head 1
     assert np.array_equal(out[0, :4], good[0, :4])
+
+
+@pytest.mark.parametrize("workload,Hq,Hkv,D,ctx", [("single_tile", 8, 8, 64, 128 * 80 + 33),
+                                                  ("qwen3_8b_decode", 8, 1, 128, 128 * 620 + 5)])
+def test_four_tiles_per_item_path(workload, Hq, Hkv, D, ctx):
+    """Grids with at least 4 tiles per SM take the 8-warp, 4-tiles-per-item
+    split kernel: head_dim 64, and a GQA group of 8 (two n8-tiles of columns)."""
+    c = Cache(workload, 12, [ctx], Hkv=Hkv, D=D)
+    assert Hkv * c.max_tiles >= 4 * 152
+    _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 3)])
