@@ -190,9 +190,10 @@ def run_reference(args, rank):
 
 def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512, Wp=256, reps=3):
     """One layer of the 15,500-token 8B-like prompt: per chunk append, promote, prefill
-    attention (tcgen05). Reports prompt tokens/s of the attention path scaled
-    to 36 layers, and the contraction throughput against the dense fp16
-    tensor peak (the algorithmic Q.K and P.V multiply-adds, counted once)."""
+    attention (block dequantisation + tcgen05 attention). Reports prompt tokens/s
+    of the attention path scaled to 36 layers, and the contraction throughput
+    against the dense fp16 tensor peak (the algorithmic Q.K and P.V
+    multiply-adds, counted once)."""
     import torch
     from kv_cache_quantization_token_gb300 import kvarn, synth
     ks, vs = synth.kv_layer("qwen3_8b_prefill", 0, HKV, n_tok, D)
@@ -214,6 +215,8 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
     ws_len = torch.zeros(1, dtype=torch.int32, device=dev)
     ws_nt = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty(n_tok, HQ, D, device=dev)
+    ws_p = torch.empty(kvarn.prefill_workspace_bytes(max_tiles, cap, HKV, D), dtype=torch.uint8,
+                       device=dev)
     ev = []
 
     def prompt(record):
@@ -239,7 +242,7 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
             kvarn.prefill_attention(q[pos0:pos0 + C], pos0, tiles, table, n_tiles, win_k[0],
-                                    win_v[0], start, length, lay, out=out[pos0:pos0 + C])
+                                    win_v[0], start, length, lay, ws=ws_p, out=out[pos0:pos0 + C])
             if record:
                 b.record()
                 ev.append((a, b))

@@ -289,23 +289,31 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
  * k holds positions [128 k, 128 k + 128) and window token w (w < win_len)
  * sits at position 128 * n_tiles + w.
  * The two contractions run on tcgen05 tensor cores with fp16 operands and
- * fp32 accumulation: tiles are dequantised to fp16 in shared memory (never to
- * global memory), window rows are rotated into the same space on the fly,
- * and the softmax, causal mask and final inverse rotation run on CUDA cores.
+ * fp32 accumulation. Two kernels: every 128-key block the chunk sees (packed
+ * tiles dequantised, window rows rotated into the same space) is written once
+ * per KV head into ws as fp16 operand images, then one attention kernel per
+ * (KV head, 128 score rows) streams those images through shared memory; the
+ * softmax, causal mask and final inverse rotation run on CUDA cores.
  *   q_chunk    : fp32 [C][Hq][D], unrotated; out: fp32 [C][Hq][D].
  *   tile_table : int64 [Hkv][table_stride] record byte offsets (multiples of
- *                16) of this sequence's tiles; table_stride >= n_tiles.
+ *                16; another offset makes the keys of that tile NaN) of this
+ *                sequence's tiles; table_stride >= n_tiles.
  *   win_k/v    : fp32 [Hkv][win_capacity][D] ring of this sequence;
  *                win_start, win_len, n_tiles: host integers.
+ *   ws         : device workspace of at least kvarn_prefill_workspace_bytes(
+ *                n_tiles, win_len, Hkv, head_dim) bytes, 256-byte aligned; no
+ *                initialisation needed. Calls sharing ws must not overlap.
  * Requires pos0 + C <= 128 * n_tiles + win_len (the chunk's own keys are in
  * the cache), head_dim 64 or 128 (256 returns KVARN_ERR_UNSUPPORTED) and
- * Hq / Hkv <= 8. Needs no workspace.
+ * Hq / Hkv <= 8.
  */
+int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes);
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
                             const int64_t* tile_table, int table_stride, int n_tiles,
                             const float* win_k, const float* win_v, int win_start, int win_len,
                             int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
-                            const kvarn_layout_t* layout, float* out, kvarn_stream_t stream);
+                            const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
+                            kvarn_stream_t stream);
 
 /*
  * Decode attention for callers that cannot allocate device memory. The pages

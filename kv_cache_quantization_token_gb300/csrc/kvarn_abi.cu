@@ -232,11 +232,21 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
   return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
 }
 
+int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes) {
+  if (!bytes) return KVARN_ERR_NULL;
+  if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
+  if (n_tiles < 0 || win_len < 0 || Hkv <= 0) return KVARN_ERR_BAD_ARG;
+  const size_t blocks = (size_t)n_tiles + (size_t)(win_len + KVARN_TILE_TOKENS - 1) / KVARN_TILE_TOKENS;
+  *bytes = blocks * (size_t)Hkv * kvarn::prefill_block_bytes(head_dim);
+  return KVARN_OK;
+}
+
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
                             const int64_t* tile_table, int table_stride, int n_tiles,
                             const float* win_k, const float* win_v, int win_start, int win_len,
                             int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
-                            const kvarn_layout_t* layout, float* out, kvarn_stream_t stream) {
+                            const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
+                            kvarn_stream_t stream) {
   if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
@@ -250,13 +260,19 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
   if (!q_chunk || !out) return KVARN_ERR_NULL;
   if (n_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
   if (win_len > 0 && (!win_k || !win_v)) return KVARN_ERR_NULL;
+  int n_tblk = 0, n_blk = 0;
+  kvarn::prefill_blocks(pos0, C, n_tiles, win_len, &n_tblk, &n_blk);
+  const size_t need = (size_t)n_blk * (size_t)Hkv * kvarn::prefill_block_bytes(head_dim);
+  if (need > 0 && !ws) return KVARN_ERR_NULL;
+  if (ws_bytes < need) return KVARN_ERR_WORKSPACE;
   if (!aligned16(q_chunk) || !aligned16(out) || (n_tiles > 0 && !aligned16(tiles)) ||
-      (win_len > 0 && (!aligned16(win_k) || !aligned16(win_v))))
+      (win_len > 0 && (!aligned16(win_k) || !aligned16(win_v))) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255))
     return KVARN_ERR_ALIGN;
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
   return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
                                          n_tiles, win_k, win_v, win_start, win_len, win_capacity,
-                                         Hq, Hkv, head_dim, softmax_scale, out,
+                                         Hq, Hkv, head_dim, softmax_scale, ws, out,
                                          (cudaStream_t)stream));
 }
 

@@ -10,28 +10,31 @@
 // tile k holding positions [128k, 128k+128) and window token w position
 // 128 * n_tiles + w.
 //
-// One CTA (8 warps) owns a KV head and 128 score rows: the G query heads of
-// the GQA group times 128/G consecutive positions, so every dequantised tile
-// serves the whole group. Two threads share each score row (one per half of
-// the 128 keys of a block), and the dequantisation is split the same way. All keys live in the rotated space: the query is
-// q' = H q (times scale * log2 e), packed tiles dequantise to
-// K~ = r_t s_c (delta code + lo) and V~ likewise, and window rows are rotated
-// when staged (H k, H v). Per 128-key block:
-//   1. the block is dequantised (or rotated) into fp16 K~ [key][channel] and
-//      V~^T [channel][key] in shared memory, 128-byte swizzled, K-major;
-//   2. S = Q' K~^T on tcgen05 (kind::f16, fp32 accumulate) into TMEM, with
-//      Q' and K~ each split into fp16 hi + lo parts and S = Qh Kh + Qh Kl +
-//      Ql Kh: one fp16 rounding of either operand costs up to 1e-2 in the
-//      output through cancellation in q.k (rotated keys are large), the
-//      split keeps the scores to about 2^-22;
-//   3. two threads own each score row (64 keys each): causal mask, online
-//      softmax in base 2 (the running max is only moved, and O rescaled in
-//      TMEM, when a score exceeds it by more than 8), P written as fp16 to
-//      shared memory;
-//   4. O += P V~ on tcgen05 into TMEM.
-// At the end one thread per row divides the O row by the row sum and applies
-// the one inverse rotation (H is its own inverse). Every wait is bounded; a CTA that
-// gives up writes NaN rows, frees its TMEM and returns.
+// Two kernels per chunk:
+//   dequant   one CTA per (visible 128-key block, KV head): a packed tile is
+//             dequantised (K~ = r_t s_c (delta code + lo), V~ likewise) or a
+//             block of window rows rotated (H k, H v), into fp16 K~ hi + lo
+//             [key][channel] and V~^T [channel][key] in the 128-byte-swizzled
+//             K-major image the tensor-core operands use, built in shared
+//             memory and written to the workspace with one bulk copy. Each
+//             block is dequantised once per chunk, not once per query CTA.
+//   attention one CTA (8 warps) per KV head and 128 score rows (the G query
+//             heads of the GQA group times 128/G positions). Per visible
+//             block: the block image is bulk-copied into shared memory (the
+//             next block's K~ while this block's softmax runs, this block's
+//             V~ while its scores are computed); S = Q' K~^T on tcgen05
+//             (kind::f16, fp32 accumulate into TMEM) with Q' and K~ each
+//             split into fp16 hi + lo and S = Qh Kh + Qh Kl + Ql Kh (one fp16
+//             rounding of either operand costs up to 1e-2 in the output
+//             through cancellation in q.k; the split keeps the scores to
+//             about 2^-22); two threads per score row apply the causal mask
+//             and an online softmax in base 2 (the running max is only moved,
+//             and O rescaled in TMEM, when a score exceeds it by more than
+//             8); P goes to shared memory as fp16 and O += P V~ on tcgen05.
+//             At the end one thread per row divides by the row sum and
+//             applies the one inverse rotation (H is its own inverse).
+// Every wait is bounded; a CTA that gives up writes NaN rows, frees its TMEM
+// and returns.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -104,6 +107,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Shared -> global bulk copy; the CTA waits until the source has been read.
+__device__ __forceinline__ void bulk_store_wait(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(su32(ssrc)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // 32 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -164,21 +176,28 @@ __device__ __forceinline__ void fwht_reg(float (&x)[N]) {
 
 template <int D>
 struct PC {
-  static constexpr int OFF_QH = 0;                     // fp16 Q' hi [128 rows][D]
-  static constexpr int OFF_QL = OFF_QH + 128 * D * 2;  // fp16 Q' lo (Q' - hi)
-  static constexpr int OFF_KH = OFF_QL + 128 * D * 2;  // fp16 K~ hi [128 keys][D]
-  static constexpr int OFF_KL = OFF_KH + 128 * D * 2;  // fp16 K~ lo
-  static constexpr int OFF_V = OFF_KL + 128 * D * 2;   // fp16 V~^T [D][128 keys]
-  static constexpr int OFF_P = OFF_V + D * 128 * 2;  // fp16 P   [128 rows][128 keys]
-  static constexpr int OFF_REC = OFF_P + 128 * 128 * 2;  // two packed records (prefetch)
   static constexpr int RB = Rec<D>::kBytes;
-  static constexpr int OFF_BAR = OFF_REC + 2 * RB;   // mbarriers: rec[2], s, o
+  static constexpr int OPB = 128 * D * 2;                // one fp16 operand image: 128 rows x D
+  static constexpr int BLK = 3 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T
+  // attention kernel shared memory
+  static constexpr int OFF_QH = 0;                       // fp16 Q' hi [128 rows][D]
+  static constexpr int OFF_QL = OFF_QH + OPB;            // fp16 Q' lo (Q' - hi)
+  static constexpr int OFF_KH = OFF_QL + OPB;            // fp16 K~ hi [128 keys][D]
+  static constexpr int OFF_KL = OFF_KH + OPB;            // fp16 K~ lo (contiguous with hi)
+  static constexpr int OFF_V = OFF_KL + OPB;             // fp16 V~^T [D][128 keys]
+  static constexpr int OFF_P = OFF_V + OPB;              // fp16 P [128 rows][128 keys]
+  static constexpr int OFF_BAR = OFF_P + 128 * 128 * 2;  // mbarriers: k, v, s, o
   static constexpr int OFF_MISC = OFF_BAR + 64;
-  static constexpr int OFF_XCH = OFF_MISC + 64;      // f32 [2][128] row max / sum exchange
+  static constexpr int OFF_XCH = OFF_MISC + 64;          // f32 [2][128] row max / sum exchange
   static constexpr int SMEM = OFF_XCH + 2 * 128 * 4 + 1024;  // + slack to align the base to 1024
-  static constexpr int NTHR = 256;                   // two threads per score row
-  static constexpr int TMEM_COLS = 256;              // S: columns 0..127, O: 128..128+D-1
+  // dequant kernel shared memory: the packed record, then the block image
+  static constexpr int DQ_OFF_OUT = RB;                  // RB is a multiple of 1024
+  static constexpr int DQ_OFF_BAR = DQ_OFF_OUT + BLK;
+  static constexpr int DQ_SMEM = DQ_OFF_BAR + 64 + 1024;
+  static constexpr int NTHR = 256;                       // two threads per score row
+  static constexpr int TMEM_COLS = 256;                  // S: columns 0..127, O: 128..128+D-1
   static_assert(D == 64 || D == 128, "prefill head_dim");
+  static_assert(RB % 1024 == 0 && OPB % 1024 == 0, "swizzled images on 1024-byte boundaries");
 };
 
 struct PrefillArgs {
@@ -187,141 +206,47 @@ struct PrefillArgs {
   const int64_t* tile_table;  // [Hkv][table_stride]
   const float* win_k;
   const float* win_v;
+  uint8_t* ws;                // [Hkv][n_blk] block images
   float* out;
   int64_t pos0;
   int C, Hq, Hkv, G, n_tiles, table_stride, win_start, win_len, win_cap;
-  float qscale;  // softmax_scale * log2(e)
+  int n_tblk, n_blk;          // tiles, and tiles + window blocks, visible to the chunk
+  float qscale;               // softmax_scale * log2(e)
 };
 
+// ---------------------------------------------------------------------------
+// dequant: block j (tile j, or window block j - n_tblk) of KV head blockIdx.y
 template <int D>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillArgs a) {
   using P = PC<D>;
   using R = Rec<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
-  unsigned char* sQh = sm + P::OFF_QH;
-  unsigned char* sQl = sm + P::OFF_QL;
-  unsigned char* sKh = sm + P::OFF_KH;
-  unsigned char* sKl = sm + P::OFF_KL;
-  unsigned char* sV = sm + P::OFF_V;
-  unsigned char* sP = sm + P::OFF_P;
-  unsigned char* sRec = sm + P::OFF_REC;
-  uint64_t* bar_rec = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // [2]
-  uint64_t* bar_s = bar_rec + 2;
-  uint64_t* bar_o = bar_rec + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
-  int* fail = reinterpret_cast<int*>(sm + P::OFF_MISC + 4);
-  float* xch = reinterpret_cast<float*>(sm + P::OFF_XCH);  // [2][128]
-
-  const int tid = threadIdx.x, warp = tid >> 5;
-  // score row of this thread and its half of the key block (TMEM lanes of warp
-  // w are 32 (w % 4) .. +31, so rows and TMEM lanes agree)
-  const int row = tid & 127, half = tid >> 7;
-  const int kvh = blockIdx.y;
-  const int ppc = 128 / a.G;                 // positions per CTA
-  const int i0 = blockIdx.x * ppc;           // first chunk row of this CTA
-  // score row `row` <-> (head g = row / ppc, chunk position i0 + row % ppc)
-  const int my_g = row / ppc, my_i = i0 + row % ppc;
-  const bool my_valid = my_i < a.C && my_g < a.G;
-  const int64_t my_pos = a.pos0 + my_i;
-  const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
-  const int hq = kvh * a.G + min(my_g, a.G - 1);
-
-  // key blocks visible to some row of this CTA: tiles, then 128-token window blocks
-  const int64_t win_pos0 = 128LL * a.n_tiles;
-  int n_tile_blk = a.n_tiles;
-  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
-  n_tile_blk = min(n_tile_blk, a.n_tiles);
-  int n_win_blk = 0;
-  for (int w = 0; 128 * w < a.win_len; ++w)
-    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
-  const int n_blk = n_tile_blk + n_win_blk;
-
-  // every record offset must be 16-byte aligned for the bulk copies; a CTA
-  // that finds one that is not writes NaN rows and does nothing else
-  {
-    int bad = 0;
-    const int64_t* tr = a.tile_table + (int64_t)kvh * a.table_stride;
-    for (int t = tid; t < n_tile_blk; t += P::NTHR) bad |= (tr[t] & 15) != 0 || tr[t] < 0;
-    if (__syncthreads_or(bad)) {
-      if (my_valid && half == 0)
-        for (int c = 0; c < D; ++c) a.out[((int64_t)my_i * a.Hq + hq) * D + c] = NAN;
-      return;
+  const unsigned char* rec = sm;
+  unsigned char* sKh = sm + P::DQ_OFF_OUT;
+  unsigned char* sKl = sKh + P::OPB;
+  unsigned char* sV = sKl + P::OPB;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::DQ_OFF_BAR);
+  const int j = blockIdx.x, kvh = blockIdx.y;
+  const int tid = threadIdx.x, row = tid & 127, half = tid >> 7;
+  bool poison = false;
+  if (j < a.n_tblk) {
+    const int64_t off = a.tile_table[(int64_t)kvh * a.table_stride + j];
+    const bool aligned = (off & 15) == 0 && off >= 0;
+    if (tid == 0) {
+      mbar_init1(bar);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-  }
-  if (tid == 0) {
-    mbar_init1(&bar_rec[0]);
-    mbar_init1(&bar_rec[1]);
-    mbar_init1(bar_s);
-    mbar_init1(bar_o);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    *fail = 0;
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     su32(tmem_slot)),
-                 "r"(P::TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  // Q' row: rotate, scale, fp16 into the swizzled A operand (one thread per row)
-  if (half == 0) {
-    float x[D];
-    if (my_valid) {
-      const float4* src = reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D);
-#pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4) {
-        const float4 v = src[c4];
-        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
-      }
+    __syncthreads();
+    if (aligned && tid == 0) bulk_load(sm, a.tiles + off, P::RB, bar);
+    poison = !aligned || !mbar_wait_bounded(bar, 0);
+    if (__syncthreads_or(poison)) {
+      // an unusable record: NaN keys make every score of this block NaN
+      if (aligned && tid == 0) mbar_wait_bounded(bar, 0);  // let the copy land (bounded)
+      for (int o = tid * 8; o < P::BLK / 2; o += 8 * P::NTHR)
+        *reinterpret_cast<uint4*>(sKh + 2 * o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
     } else {
-#pragma unroll
-      for (int c = 0; c < D; ++c) x[c] = 0.f;
-    }
-    fwht_reg<D>(x);
-#pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-      __align__(16) __half2 hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        split2(x[8 * c8 + 2 * e] * a.qscale, x[8 * c8 + 2 * e + 1] * a.qscale, hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(sQh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-      *reinterpret_cast<uint4*>(sQl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
-    }
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + 128;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // TMEM lanes of this warp
-  const int64_t* trow = a.tile_table + (int64_t)kvh * a.table_stride;
-
-  // prefetch the first packed record
-  if (tid == 0 && n_tile_blk > 0) bulk_load(sRec, a.tiles + trow[0], P::RB, &bar_rec[0]);
-
-  float m_ref = -INFINITY, l_sum = 0.f;
-  bool ok = true;
-  int issued_s = 0, issued_o = 0, issued_rec = n_tile_blk > 0 ? 1 : 0;
-  for (int j = 0; j < n_blk; ++j) {
-    const bool is_tile = j < n_tile_blk;
-    // ---- 1. the PV MMA of block j-1 has consumed V~^T and P
-    if (j > 0) {
-      const bool w = mbar_wait_bounded(bar_o, (j - 1) & 1);
-      if (!w) *fail = 1;
-    }
-    int nkeys = 128;
-    int64_t kpos0;
-    if (is_tile) {
-      kpos0 = 128LL * j;
-      if (!mbar_wait_bounded(&bar_rec[j & 1], (j >> 1) & 1)) *fail = 1;
-      // prefetch the next record into the other buffer (its previous user, block j-1, is done)
-      if (j + 1 < n_tile_blk) {
-        if (tid == 0)
-          bulk_load(sRec + ((j + 1) & 1) * P::RB, a.tiles + trow[j + 1], P::RB, &bar_rec[(j + 1) & 1]);
-        ++issued_rec;
-      }
-      const unsigned char* rec = sRec + (j & 1) * P::RB;
       const float* kS = reinterpret_cast<const float*>(rec + R::kKS);
       const float* kD = reinterpret_cast<const float*>(rec + R::kKDelta);
       const float* kL = reinterpret_cast<const float*>(rec + R::kKLo);
@@ -388,11 +313,11 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
           }
         }
       }
-    } else {
-      // window block: rotate raw rows on the fly
-      const int wb = j - n_tile_blk;
-      kpos0 = win_pos0 + 128LL * wb;
-      nkeys = min(128, a.win_len - 128 * wb);
+    }
+  } else {
+      // window block: rotate raw rows (K into K~ hi/lo, V into V~^T)
+      const int wb = j - a.n_tblk;
+      const int nkeys = min(128, a.win_len - 128 * wb);
       const int t = row;
       float x[D];
       const bool have = t < nkeys;
@@ -437,9 +362,132 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
       for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(x[c]);
       }
+  }
+  // the image goes out with one bulk copy (async proxy: fence the generic writes)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (tid == 0)
+    bulk_store_wait(a.ws + ((int64_t)kvh * a.n_blk + j) * P::BLK, sKh, P::BLK);
+}
+
+// ---------------------------------------------------------------------------
+// attention over the block images of the chunk
+template <int D>
+__global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
+  using P = PC<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                       ~uintptr_t(1023));
+  unsigned char* sQh = sm + P::OFF_QH;
+  unsigned char* sQl = sm + P::OFF_QL;
+  unsigned char* sKh = sm + P::OFF_KH;
+  unsigned char* sKl = sm + P::OFF_KL;
+  unsigned char* sV = sm + P::OFF_V;
+  unsigned char* sP = sm + P::OFF_P;
+  uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);
+  uint64_t* bar_v = bar_k + 1;
+  uint64_t* bar_s = bar_k + 2;
+  uint64_t* bar_o = bar_k + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
+  int* fail = reinterpret_cast<int*>(sm + P::OFF_MISC + 4);
+  float* xch = reinterpret_cast<float*>(sm + P::OFF_XCH);  // [2][128]
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // score row of this thread and its half of the key block (TMEM lanes of warp
+  // w are 32 (w % 4) .. +31, so rows and TMEM lanes agree)
+  const int row = tid & 127, half = tid >> 7;
+  const int kvh = blockIdx.y;
+  const int ppc = 128 / a.G;                 // positions per CTA
+  const int i0 = blockIdx.x * ppc;           // first chunk row of this CTA
+  // score row `row` <-> (head g = row / ppc, chunk position i0 + row % ppc)
+  const int my_g = row / ppc, my_i = i0 + row % ppc;
+  const bool my_valid = my_i < a.C && my_g < a.G;
+  const int64_t my_pos = a.pos0 + my_i;
+  const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
+  const int hq = kvh * a.G + min(my_g, a.G - 1);
+
+  // key blocks visible to some row of this CTA: tiles, then 128-token window
+  // blocks (a CTA that sees a window block sees every tile)
+  const int64_t win_pos0 = 128LL * a.n_tiles;
+  int n_tile_blk = a.n_tiles;
+  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
+  n_tile_blk = min(n_tile_blk, a.n_tiles);
+  int n_win_blk = 0;
+  for (int w = 0; 128 * w < a.win_len; ++w)
+    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
+  const int n_blk = n_tile_blk + n_win_blk;
+  auto image = [&](int jj) -> const uint8_t* {  // workspace image of this CTA's block jj
+    const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
+    return a.ws + ((int64_t)kvh * a.n_blk + widx) * P::BLK;
+  };
+
+  if (tid == 0) {
+    mbar_init1(bar_k);
+    mbar_init1(bar_v);
+    mbar_init1(bar_s);
+    mbar_init1(bar_o);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *fail = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_slot)),
+                 "r"(P::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // Q' row: rotate, scale, fp16 into the swizzled A operand (one thread per row)
+  if (half == 0) {
+    float x[D];
+    if (my_valid) {
+      const float4* src = reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 v = src[c4];
+        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < D; ++c) x[c] = 0.f;
+    }
+    fwht_reg<D>(x);
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        split2(x[8 * c8 + 2 * e] * a.qscale, x[8 * c8 + 2 * e + 1] * a.qscale, hi[e], lo[e]);
+      *reinterpret_cast<uint4*>(sQh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+      *reinterpret_cast<uint4*>(sQl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem, t_o = tmem + 128;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // TMEM lanes of this warp
+
+  // first block: K~ hi + lo (contiguous in the image and in shared memory), V~^T
+  if (tid == 0 && n_blk > 0) {
+    bulk_load(sKh, image(0), 2 * P::OPB, bar_k);
+    bulk_load(sV, image(0) + 2 * P::OPB, P::OPB, bar_v);
+  }
+
+  float m_ref = -INFINITY, l_sum = 0.f;
+  bool ok = true;
+  int issued_k = n_blk > 0 ? 1 : 0, issued_v = issued_k, issued_s = 0, issued_o = 0;
+  for (int j = 0; j < n_blk; ++j) {
+    const bool is_tile = j < n_tile_blk;
+    const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
+    const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
+    // ---- 1. the PV MMA of block j-1 is done: P and V~ are free; V~ of block j in
+    if (j > 0) {
+      if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) *fail = 1;
+      if (tid == 0) bulk_load(sV, image(j) + 2 * P::OPB, P::OPB, bar_v);
+      ++issued_v;
     }
     // ---- 2. S = Q' K~^T
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (!mbar_wait_bounded(bar_k, j & 1)) *fail = 1;
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (*fail) { ok = false; break; }
@@ -457,6 +505,11 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
     ++issued_s;
     if (!mbar_wait_bounded(bar_s, j & 1)) *fail = 1;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // K~ is free: the next block's K~ streams in while this block's softmax runs
+    if (j + 1 < n_blk) {
+      if (tid == 0) bulk_load(sKh, image(j + 1), 2 * P::OPB, bar_k);
+      ++issued_k;
+    }
     // ---- 3. softmax of this thread's half row (keys 64 half .. 64 half + 63)
     float sv[64];
 #pragma unroll
@@ -509,6 +562,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
     }
     l_sum += rs;  // this thread's share of the row sum
     // ---- 4. O += P V~
+    if (!mbar_wait_bounded(bar_v, j & 1)) *fail = 1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -530,10 +584,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
     // the shared memory and TMEM are released
     if (issued_s > 0) mbar_wait_bounded(bar_s, (issued_s - 1) & 1);
     if (issued_o > 0) mbar_wait_bounded(bar_o, (issued_o - 1) & 1);
-    for (int r = 0; r < 2; ++r) {
-      const int uses = issued_rec / 2 + (r < issued_rec % 2 ? 1 : 0);
-      if (uses > 0) mbar_wait_bounded(&bar_rec[r], (uses - 1) & 1);
-    }
+    if (issued_k > 0) mbar_wait_bounded(bar_k, (issued_k - 1) & 1);
+    if (issued_v > 0) mbar_wait_bounded(bar_v, (issued_v - 1) & 1);
   }
   if (ok && n_blk > 0) {
     if (!mbar_wait_bounded(bar_o, (n_blk - 1) & 1)) ok = false;
@@ -588,7 +640,15 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_dequant_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P::DQ_SMEM);
+    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  if (a.n_blk > 0) {
+    prefill_dequant_kernel<D><<<dim3(a.n_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
@@ -598,16 +658,33 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+// Blocks visible to some position of the chunk [pos0, pos0 + C): tiles whose
+// first position is <= the last one, then the window's 128-token blocks likewise.
+void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, int* n_blk) {
+  const int64_t pmax = pos0 + C - 1;
+  int nt = n_tiles;
+  if (nt > 0 && 128LL * (nt - 1) > pmax) nt = (int)(pmax / 128) + 1;
+  int nw = 0;
+  for (int w = 0; 128 * w < win_len; ++w)
+    if (128LL * n_tiles + 128 * w <= pmax) nw = w + 1;
+  *n_tblk = nt;
+  *n_blk = nt + nw;
+}
+
+size_t prefill_block_bytes(int D) { return (size_t)3 * 128 * D * 2; }
+
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           float* out, cudaStream_t st) {
+                           void* ws, float* out, cudaStream_t st) {
   PrefillArgs a;
   a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
+  a.ws = reinterpret_cast<uint8_t*>(ws);
   a.out = out; a.pos0 = pos0; a.C = C; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
   a.n_tiles = n_tiles; a.table_stride = table_stride; a.win_start = win_start;
   a.win_len = win_len; a.win_cap = win_capacity; a.qscale = softmax_scale * kLog2e;
+  prefill_blocks(pos0, C, n_tiles, win_len, &a.n_tblk, &a.n_blk);
   switch (D) {
     case 64: return launch_prefill_d<64>(a, st);
     case 128: return launch_prefill_d<128>(a, st);

@@ -73,14 +73,17 @@ def _L():
         lib.kvarn_window_advance.argtypes = [vp, vp, vp, c_int, c_int, c_int, c_int, vp]
         lib.kvarn_prefill_attention.argtypes = [vp, c_int, i64, vp, vp, c_int, c_int, vp, vp,
                                                 c_int, c_int, c_int, c_int, c_int, c_int,
-                                                ctypes.c_float, ctypes.POINTER(Layout), vp, vp]
+                                                ctypes.c_float, ctypes.POINTER(Layout), vp, sz, vp,
+                                                vp]
+        lib.kvarn_prefill_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, ctypes.POINTER(sz)]
         lib.kvarn_set_launch_flags.argtypes = [ctypes.c_uint]
         lib.kvarn_get_launch_flags.argtypes = []
         lib.kvarn_get_launch_flags.restype = ctypes.c_uint
         for name in ("kvarn_layout", "kvarn_rotate_query", "kvarn_compress_tile",
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
                      "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
-                     "kvarn_window_advance", "kvarn_prefill_attention", "kvarn_set_launch_flags"):
+                     "kvarn_window_advance", "kvarn_prefill_attention", "kvarn_set_launch_flags",
+                     "kvarn_prefill_workspace_bytes"):
             getattr(lib, name).restype = c_int
         _lib = lib
     return _lib
@@ -238,11 +241,20 @@ def window_advance(win_start, win_len, n_tiles, d_len, promote, win_capacity, st
                                      int(win_capacity), _stream(stream)))
 
 
+def prefill_workspace_bytes(n_tiles, win_len, Hkv, head_dim) -> int:
+    n = ctypes.c_size_t()
+    _check("kvarn_prefill_workspace_bytes",
+           _L().kvarn_prefill_workspace_bytes(int(n_tiles), int(win_len), Hkv, head_dim,
+                                              ctypes.byref(n)))
+    return n.value
+
+
 def prefill_attention(q_chunk, pos0, tiles, tile_table, n_tiles, win_k, win_v, win_start,
-                      win_len, lay: Layout, softmax_scale=None, out=None, stream=None):
+                      win_len, lay: Layout, softmax_scale=None, ws=None, out=None, stream=None):
     """Causal attention of a chunk of one sequence: q_chunk fp32 [C][Hq][D] at
     positions pos0 + i; tile_table int64 [Hkv][stride]; win_k/v fp32
-    [Hkv][cap][D]; n_tiles, win_start, win_len host ints."""
+    [Hkv][cap][D]; n_tiles, win_start, win_len host ints; ws a uint8 device
+    workspace of prefill_workspace_bytes() (allocated here when None)."""
     _dev(q_chunk, "q_chunk", torch.float32)
     C, Hq, D = q_chunk.shape
     _dev(tile_table, "tile_table", torch.int64)
@@ -252,12 +264,15 @@ def prefill_attention(q_chunk, pos0, tiles, tile_table, n_tiles, win_k, win_v, w
         softmax_scale = D ** -0.5
     if out is None:
         out = torch.empty_like(q_chunk)
+    if ws is None:
+        need = prefill_workspace_bytes(n_tiles, win_len, Hkv, D)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q_chunk.device)
     _check("kvarn_prefill_attention",
            _L().kvarn_prefill_attention(_ptr(q_chunk), C, int(pos0), _ptr(tiles), _ptr(tile_table),
                                         stride, int(n_tiles), _ptr(win_k), _ptr(win_v),
                                         int(win_start), int(win_len), cap, Hq, Hkv, D,
-                                        float(softmax_scale), ctypes.byref(lay), _ptr(out),
-                                        _stream(stream)))
+                                        float(softmax_scale), ctypes.byref(lay), _ptr(ws),
+                                        ws.numel(), _ptr(out), _stream(stream)))
     return out
 
 

@@ -83,15 +83,24 @@ def test_host_validation_rejects_before_launch(lib):
 def test_prefill_host_validation(lib):
     L = kvarn.layout(128)
     p = ctypes.c_void_p(4096)
-    args = lambda C, pos0, nt, wl, D=128, Hq=32, lay=L: (p, C, pos0, p, p, 64, nt, p, p, 0, wl, 768,
-                                                        Hq, 8, D, ctypes.c_float(0.088),
-                                                        ctypes.byref(lay), p, None)
+    args = lambda C, pos0, nt, wl, D=128, Hq=32, lay=L, wsb=1 << 40: (
+        p, C, pos0, p, p, 64, nt, p, p, 0, wl, 768, Hq, 8, D, ctypes.c_float(0.088),
+        ctypes.byref(lay), p, ctypes.c_size_t(wsb), p, None)
     f = lib.kvarn_prefill_attention
+    f.argtypes = None
     assert f(*args(512, 2000, 10, 300)) == -4          # chunk beyond the cache
     L256 = kvarn.layout(256)
     assert f(*args(16, 0, 1, 16, D=256, lay=L256)) == -3  # head_dim 256 not yet supported
     assert f(*args(16, 0, 1, 16, Hq=80)) == -3            # GQA group of 10
     assert f(*args(0, 0, 0, 0)) == 0                      # empty chunk enqueues nothing
+    # the workspace bound covers every tile and window block of 8 KV heads ...
+    need = ctypes.c_size_t()
+    assert lib.kvarn_prefill_workspace_bytes(10, 300, 8, 128, ctypes.byref(need)) == 0
+    blk = 3 * 128 * 128 * 2
+    assert need.value == (10 + 3) * 8 * blk
+    # ... a chunk at 1000..1511 sees the 10 tiles and 2 of the window's 3 blocks
+    assert f(*args(512, 1000, 10, 300, wsb=12 * 8 * blk - 1)) == -5
+
 
 
 def test_launch_flags_validation():
