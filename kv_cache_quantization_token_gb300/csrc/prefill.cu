@@ -157,6 +157,13 @@ __device__ __forceinline__ void split2(float x0, float x1, __half2& hi, __half2&
   lo = __floats2half2_rn(x0 - __low2float(hi), x1 - __high2float(hi));
 }
 
+// 2^x on the special-function unit (results below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // In-register orthonormal Walsh-Hadamard transform of N values (N a power of 2).
 template <int N>
 __device__ __forceinline__ void fwht_reg(float (&x)[N]) {
@@ -404,6 +411,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
   const bool my_valid = my_i < a.C && my_g < a.G;
   const int64_t my_pos = a.pos0 + my_i;
   const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
+  const int64_t pmin = a.pos0 + i0;                       // smallest
   const int hq = kvh * a.G + min(my_g, a.G - 1);
 
   // key blocks visible to some row of this CTA: tiles, then 128-token window
@@ -480,6 +488,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
     const bool is_tile = j < n_tile_blk;
     const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
     const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
+    const bool full_vis = kpos0 + 127 <= pmin;  // the same in every thread of the CTA
     // ---- 1. the PV MMA of block j-1 is done: P and V~ are free; V~ of block j in
     if (j > 0) {
       if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) *fail = 1;
@@ -520,12 +529,18 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
       for (int i = 0; i < 32; ++i) sv[c0 + i] = v[i];
     }
     float mblk = -INFINITY;
+    if (full_vis && nkeys == 128) {  // every row of the CTA sees every key of the block
 #pragma unroll
-    for (int u = 0; u < 64; ++u) {
-      const int t = 64 * half + u;
-      const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
-      sv[u] = vis ? sv[u] : -INFINITY;
-      mblk = fmaxf(mblk, sv[u]);
+      for (int u = 0; u < 64; ++u) mblk = fmaxf(mblk, sv[u]);
+      if (!my_valid) mblk = -INFINITY;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 64; ++u) {
+        const int t = 64 * half + u;
+        const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
+        sv[u] = vis ? sv[u] : -INFINITY;
+        mblk = fmaxf(mblk, sv[u]);
+      }
     }
     xch[half * 128 + row] = mblk;
     __syncthreads();
@@ -552,8 +567,11 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
       __align__(16) __half2 h[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * e] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * e + 1] - m_ref);
+        // exp2 of a non-positive argument (up to +8); results below 2^-126 flush to
+        // zero (they are below fp16 resolution too); a row with no visible key
+        // yet (m_ref = -inf) gets exp2(-inf) = 0 from the NaN-free guard below
+        const float p0 = m_ref == -INFINITY ? 0.f : ex2_ftz(sv[8 * c8 + 2 * e] - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : ex2_ftz(sv[8 * c8 + 2 * e + 1] - m_ref);
         const __half2 hp = __floats2half2_rn(p0, p1);
         rs += __low2float(hp) + __high2float(hp);  // the sum of what the MMA will add
         h[e] = hp;
