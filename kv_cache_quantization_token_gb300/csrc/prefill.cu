@@ -18,21 +18,26 @@
 //             K-major image the tensor-core operands use, built in shared
 //             memory and written to the workspace with one bulk copy. Each
 //             block is dequantised once per chunk, not once per query CTA.
-//   attention one CTA (8 warps) per KV head and 128 score rows (the G query
-//             heads of the GQA group times 128/G positions). Per visible
-//             block: the block image is bulk-copied into shared memory (the
-//             next block's K~ while this block's softmax runs, this block's
-//             V~ while its scores are computed); S = Q' K~^T on tcgen05
+//   attention one CTA (10 warps) per KV head and 128 score rows (the G query
+//             heads of the GQA group times 128/G positions): 8 softmax warps,
+//             one MMA warp, one copy warp, handing off through mbarriers.
+//             Per visible block: the block image is bulk-copied into shared
+//             memory (K~ hi and lo on separate barriers, each as soon as the
+//             previous block's MMAs have read it); S = Q' K~^T on tcgen05
 //             (kind::f16, fp32 accumulate into TMEM) with Q' and K~ each
 //             split into fp16 hi + lo and S = Qh Kh + Qh Kl + Ql Kh (one fp16
 //             rounding of either operand costs up to 1e-2 in the output
 //             through cancellation in q.k; the split keeps the scores to
-//             about 2^-22); two threads per score row apply the causal mask
-//             and an online softmax in base 2 (the running max is only moved,
-//             and O rescaled in TMEM, when a score exceeds it by more than
-//             8); P goes to shared memory as fp16 and O += P V~ on tcgen05.
-//             At the end one thread per row divides by the row sum and
-//             applies the one inverse rotation (H is its own inverse).
+//             about 2^-22), double-buffered in TMEM so that the scores of
+//             block j+1 are computed while the softmax of block j runs; two
+//             threads per score row apply the causal mask and an online
+//             softmax in base 2 (the running max is only moved, and O
+//             rescaled in TMEM, when a score exceeds it by more than 8); P
+//             goes to shared memory as fp16 and [O | l] += P [V~ | 1] on
+//             tcgen05, the ones column giving the row sums of exactly the
+//             fp16 P the MMA adds. At the end one thread per row divides by
+//             the row sum and applies the one inverse rotation (H is its own
+//             inverse).
 // Every wait is bounded; a CTA that gives up writes NaN rows, frees its TMEM
 // and returns.
 #include <cuda_fp16.h>
@@ -97,6 +102,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (mbar_poll(bar, parity)) return true;
   return false;
 }
+// Bounded wait that also gives up once another thread of the CTA has raised
+// `fail`; a wait that runs out raises it.
+__device__ __forceinline__ bool mbar_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  for (int i = 0; i < (1 << 22); ++i) {
+    if (mbar_poll(bar, parity)) return true;
+    if ((i & 63) == 63 && *fail) return false;
+  }
+  *fail = 1;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+// TMEM lane field of the 32 lanes warp `w` may access (lanes 32 (w % 4) ..).
+__device__ __forceinline__ uint32_t lane_base_of(int w) { return (uint32_t)((w & 3) * 32) << 16; }
+
+// Bulk copy whose bytes count against a transaction count announced earlier.
+__device__ __forceinline__ void bulk_copy_tx(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
                : "memory");
@@ -151,6 +185,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// One fp32 TMEM column of this thread's lane.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v))
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // x = hi + lo with hi, lo fp16: the pair carries about 22 significant bits.
 __device__ __forceinline__ void split2(float x0, float x1, __half2& hi, __half2& lo) {
   hi = __floats2half2_rn(x0, x1);
@@ -191,20 +244,23 @@ struct PC {
   static constexpr int OFF_QL = OFF_QH + OPB;            // fp16 Q' lo (Q' - hi)
   static constexpr int OFF_KH = OFF_QL + OPB;            // fp16 K~ hi [128 keys][D]
   static constexpr int OFF_KL = OFF_KH + OPB;            // fp16 K~ lo (contiguous with hi)
-  static constexpr int OFF_V = OFF_KL + OPB;             // fp16 V~^T [D][128 keys]
-  static constexpr int OFF_P = OFF_V + OPB;              // fp16 P [128 rows][128 keys]
-  static constexpr int OFF_BAR = OFF_P + 128 * 128 * 2;  // mbarriers: k, v, s, o
+  static constexpr int NV = D + 16;                      // V~^T rows + a ones row + 15 zero rows
+  static constexpr int VKB = NV * 128;                   // one 64-key block of the V operand
+  static constexpr int OFF_V = OFF_KL + OPB;             // fp16 [V~^T; 1; 0] [NV][128 keys]
+  static constexpr int OFF_P = OFF_V + 2 * VKB;          // fp16 P [128 rows][128 keys]
+  static constexpr int OFF_BAR = OFF_P + 128 * 128 * 2;  // 8 mbarriers
   static constexpr int OFF_MISC = OFF_BAR + 64;
-  static constexpr int OFF_XCH = OFF_MISC + 64;          // f32 [2][128] row max / sum exchange
-  static constexpr int SMEM = OFF_XCH + 2 * 128 * 4 + 1024;  // + slack to align the base to 1024
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;     // + slack to align the base to 1024
   // dequant kernel shared memory: the packed record, then the block image
   static constexpr int DQ_OFF_OUT = RB;                  // RB is a multiple of 1024
   static constexpr int DQ_OFF_BAR = DQ_OFF_OUT + BLK;
   static constexpr int DQ_SMEM = DQ_OFF_BAR + 64 + 1024;
-  static constexpr int NTHR = 256;                       // two threads per score row
-  static constexpr int TMEM_COLS = 256;                  // S: columns 0..127, O: 128..128+D-1
+  static constexpr int NTHR = 256;                       // dequant: two threads per key row
+  static constexpr int NTHR_ATT = 320;                   // attention: 8 softmax warps, MMA, loads
+  static constexpr int TMEM_COLS = 512;                  // S: 0..127 and 128..255, O|l: 256..256+D
   static_assert(D == 64 || D == 128, "prefill head_dim");
-  static_assert(RB % 1024 == 0 && OPB % 1024 == 0, "swizzled images on 1024-byte boundaries");
+  static_assert(RB % 1024 == 0 && OPB % 1024 == 0 && VKB % 1024 == 0,
+                "swizzled images on 1024-byte boundaries");
 };
 
 struct PrefillArgs {
@@ -379,8 +435,16 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
 
 // ---------------------------------------------------------------------------
 // attention over the block images of the chunk
+//
+// Warp roles: warps 0-7 run the softmax (two threads per score row) and the
+// epilogue, warp 8 issues the tcgen05 MMAs (one thread), warp 9 the bulk
+// copies (one thread). Scores are double-buffered in TMEM, so S of block j+1
+// is computed while the softmax of block j runs. The tensor pipe runs, in
+// order, S(0), S(1), PV(0), S(2), PV(1), ...; K~ hi and K~ lo have their own
+// barriers, so the next block's hi half streams in while this block's
+// Qh Kl product is still being accumulated.
 template <int D>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   using P = PC<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -391,18 +455,20 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
   unsigned char* sKl = sm + P::OFF_KL;
   unsigned char* sV = sm + P::OFF_V;
   unsigned char* sP = sm + P::OFF_P;
-  uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);
-  uint64_t* bar_v = bar_k + 1;
-  uint64_t* bar_s = bar_k + 2;
-  uint64_t* bar_o = bar_k + 3;
+  uint64_t* bar_kh = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // K~ hi landed
+  uint64_t* bar_kl = bar_kh + 1;   // K~ lo landed
+  uint64_t* bar_v = bar_kh + 2;    // V~^T landed
+  uint64_t* bar_s = bar_kh + 3;    // [2] S(j) complete (TMEM buffer j & 1); K~ lo free
+  uint64_t* bar_khf = bar_kh + 5;  // the K~ hi products of S(j) complete: K~ hi free
+  uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: P and V~ free, O current
+  uint64_t* bar_p = bar_kh + 7;    // P(j) written and O rescaled (one arrival per softmax warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
-  int* fail = reinterpret_cast<int*>(sm + P::OFF_MISC + 4);
-  float* xch = reinterpret_cast<float*>(sm + P::OFF_XCH);  // [2][128]
+  volatile int* fail = reinterpret_cast<volatile int*>(sm + P::OFF_MISC + 4);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  // score row of this thread and its half of the key block (TMEM lanes of warp
-  // w are 32 (w % 4) .. +31, so rows and TMEM lanes agree)
-  const int row = tid & 127, half = tid >> 7;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // score row of a softmax thread and its half of the key block (TMEM lanes of
+  // warp w are 32 (w % 4) .. +31, so rows and TMEM lanes agree)
+  const int row = tid & 127, half = (tid >> 7) & 1;
   const int kvh = blockIdx.y;
   const int ppc = 128 / a.G;                 // positions per CTA
   const int i0 = blockIdx.x * ppc;           // first chunk row of this CTA
@@ -430,10 +496,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
   };
 
   if (tid == 0) {
-    mbar_init1(bar_k);
-    mbar_init1(bar_v);
-    mbar_init1(bar_s);
-    mbar_init1(bar_o);
+    for (int i = 0; i < 7; ++i) mbar_init1(bar_kh + i);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
   }
@@ -444,7 +508,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // Q' row: rotate, scale, fp16 into the swizzled A operand (one thread per row)
-  if (half == 0) {
+  if (tid < 128) {
     float x[D];
     if (my_valid) {
       const float4* src = reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D);
@@ -467,162 +531,222 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const PrefillArgs a) {
       *reinterpret_cast<uint4*>(sQh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
       *reinterpret_cast<uint4*>(sQl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
     }
+    // the MMA (async proxy) reads what these generic stores wrote
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else if (tid < 256) {
+    // rows D .. D+15 of both key blocks of the V operand: a row of ones (the
+    // PV MMA then also sums P into column D of O) and zeros
+    for (int idx = tid - 128; idx < 2 * 16 * 8; idx += 128) {
+      const int kb = idx >> 7, r = (idx >> 3) & 15, c16 = idx & 7;
+      const uint32_t w = r == 0 ? 0x3C003C00u : 0u;
+      *reinterpret_cast<uint4*>(sV + kb * P::VKB + (D + r) * 128 + c16 * 16) = make_uint4(w, w, w, w);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_o = tmem + 128;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;  // TMEM lanes of this warp
+  const uint32_t t_o = tmem + 256;
 
-  // first block: K~ hi + lo (contiguous in the image and in shared memory), V~^T
-  if (tid == 0 && n_blk > 0) {
-    bulk_load(sKh, image(0), 2 * P::OPB, bar_k);
-    bulk_load(sV, image(0) + 2 * P::OPB, P::OPB, bar_v);
+  if (warp == 9) {
+    // ---------------- loader: block images into shared memory
+    if (lane == 0 && n_blk > 0) {
+      int nkh = 1, nkl = 1, nv = 1;
+      auto load_v = [&](int jj) {  // the image holds two 64-key blocks of D rows each
+        mbar_expect_tx(bar_v, P::OPB);
+        bulk_copy_tx(sV, image(jj) + 2 * P::OPB, P::OPB / 2, bar_v);
+        bulk_copy_tx(sV + P::VKB, image(jj) + 2 * P::OPB + P::OPB / 2, P::OPB / 2, bar_v);
+      };
+      bulk_load(sKh, image(0), P::OPB, bar_kh);
+      bulk_load(sKl, image(0) + P::OPB, P::OPB, bar_kl);
+      load_v(0);
+      // waits follow the tensor pipe's completion order: S(j-1) hi part,
+      // S(j-1), PV(j-2)
+      for (int j = 1; j <= n_blk; ++j) {
+        if (j < n_blk) {
+          if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail)) break;
+          bulk_load(sKh, image(j), P::OPB, bar_kh);
+          ++nkh;
+          if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail)) break;
+          bulk_load(sKl, image(j) + P::OPB, P::OPB, bar_kl);
+          ++nkl;
+        }
+        if (j >= 2) {
+          if (!mbar_wait_flag(bar_o, (uint32_t)(j - 2) & 1u, fail)) break;
+          load_v(j - 1);
+          ++nv;
+        }
+      }
+      // every copy issued has landed before the CTA can retire
+      mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u);
+      mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u);
+      mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ---------------- MMA issuer
+    if (lane == 0 && n_blk > 0) {
+      uint64_t* last = nullptr;  // the most recent commit, drained on the way out
+      uint32_t last_par = 0;
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t t_s = tmem + 128 * (j & 1);
+        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+          mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKh) + off), idesc<128>(), kk > 0);
+          mma_f16(t_s, sdesc(su32(sQl) + off), sdesc(su32(sKh) + off), idesc<128>(), 1);
+        }
+        mma_commit(bar_khf);
+        last = bar_khf; last_par = (uint32_t)j & 1u;
+        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+          mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKl) + off), idesc<128>(), 1);
+        }
+        mma_commit(bar_s + (j & 1));
+        last = bar_s + (j & 1); last_par = (uint32_t)(j >> 1) & 1u;
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int j = 0; ok && j < n_blk; ++j) {
+        // S(j+1) goes in ahead of PV(j): its TMEM buffer was read by the softmax
+        // of block j-1, which PV(j-1) already waited for
+        if (j + 1 < n_blk && !issue_s(j + 1)) break;
+        if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * P::VKB + (kk & 3) * 32;
+          mma_f16(t_o, sdesc(su32(sP) + off_a), sdesc(su32(sV) + off_b), idesc<P::NV>(),
+                  (j > 0 || kk > 0));
+        }
+        mma_commit(bar_o);
+        last = bar_o; last_par = (uint32_t)j & 1u;
+      }
+      // the tensor pipe completes in order: the last commit covers everything
+      if (last != nullptr && !mbar_wait_bounded(last, last_par)) *fail = 1;
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax (warps 0-7)
+    // Each thread reads its whole score row for the row maximum (no exchange
+    // between the two threads of a row) and exponentiates its half. Row sums
+    // come out of the PV MMA (column D of O, from the ones row of the V operand).
+    float m_ref = -INFINITY;
+    const uint32_t lb = lane_base_of(warp);
+    for (int j = 0; j < n_blk; ++j) {
+      const bool is_tile = j < n_tile_blk;
+      const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
+      const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
+      const bool full_vis = kpos0 + 127 <= pmin && nkeys == 128;  // uniform over the CTA
+      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
+      if (__any_sync(0xffffffffu, bad || *fail != 0)) break;  // the warp leaves together
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t t_s = tmem + 128 * (j & 1) + lb;
+      float sv[64];
+      tmem_ld32(t_s + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
+      tmem_ld32(t_s + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+      float mblk = -INFINITY;
+      if (full_vis) {
+#pragma unroll
+        for (int u = 0; u < 64; u += 2) mblk = fmax3(mblk, sv[u], sv[u + 1]);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {  // the other half of the row
+          float v[32];
+          tmem_ld32(t_s + 64 * (1 - half) + c0, v);
+#pragma unroll
+          for (int u = 0; u < 32; u += 2) mblk = fmax3(mblk, v[u], v[u + 1]);
+        }
+        if (!my_valid) mblk = -INFINITY;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          const int t = 64 * half + u;
+          const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
+          sv[u] = vis ? sv[u] : -INFINITY;
+          mblk = fmaxf(mblk, sv[u]);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          float v[32];
+          tmem_ld32(t_s + 64 * (1 - half) + c0, v);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const int t = 64 * (1 - half) + c0 + u;
+            const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
+            mblk = vis ? fmaxf(mblk, v[u]) : mblk;
+          }
+        }
+      }
+      // move the reference max (and rescale O and l) only when a score exceeds
+      // it by more than 8; both threads of a row see the same values
+      const bool need = mblk > m_ref + 8.0f;
+      const float m_new = need ? mblk : m_ref;
+      const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
+      m_ref = m_new;
+      // exp2 of a non-positive argument (up to +8); results below 2^-126 flush to
+      // zero (they are below fp16 resolution too); a row with no visible key yet
+      // subtracts +inf and gets 0
+      const float msub = m_ref == -INFINITY ? INFINITY : m_ref;
+      uint32_t h[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const __half2 hp = __floats2half2_rn(ex2_ftz(sv[2 * e] - msub), ex2_ftz(sv[2 * e + 1] - msub));
+        h[e] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      // P and O belong to PV(j-1) until it completes
+      if (j == 0 || mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            float v[32];
+            tmem_ld32(t_o + lb + half * (D / 2) + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(t_o + lb + half * (D / 2) + c0, v);
+          }
+          if (half == 0) {
+            const float l = tmem_ld1(t_o + lb + D);
+            tmem_st1(t_o + lb + D, l * alpha);
+          }
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(sP + sw_off(row, 64 * half + 8 * c8, 128)) =
+              make_uint4(h[4 * c8], h[4 * c8 + 1], h[4 * c8 + 2], h[4 * c8 + 3]);
+      }
+      // (a failed wait leaves P and O alone; the next block's check stops the warp)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+    }
   }
-
-  float m_ref = -INFINITY, l_sum = 0.f;
-  bool ok = true;
-  int issued_k = n_blk > 0 ? 1 : 0, issued_v = issued_k, issued_s = 0, issued_o = 0;
-  for (int j = 0; j < n_blk; ++j) {
-    const bool is_tile = j < n_tile_blk;
-    const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
-    const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
-    const bool full_vis = kpos0 + 127 <= pmin;  // the same in every thread of the CTA
-    // ---- 1. the PV MMA of block j-1 is done: P and V~ are free; V~ of block j in
-    if (j > 0) {
-      if (!mbar_wait_bounded(bar_o, (j - 1) & 1)) *fail = 1;
-      if (tid == 0) bulk_load(sV, image(j) + 2 * P::OPB, P::OPB, bar_v);
-      ++issued_v;
-    }
-    // ---- 2. S = Q' K~^T
-    if (!mbar_wait_bounded(bar_k, j & 1)) *fail = 1;
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    if (*fail) { ok = false; break; }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-        mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKh) + off), idesc<128>(), kk > 0);
-        mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKl) + off), idesc<128>(), 1);
-        mma_f16(t_s, sdesc(su32(sQl) + off), sdesc(su32(sKh) + off), idesc<128>(), 1);
-      }
-      mma_commit(bar_s);
-    }
-    ++issued_s;
-    if (!mbar_wait_bounded(bar_s, j & 1)) *fail = 1;
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // K~ is free: the next block's K~ streams in while this block's softmax runs
-    if (j + 1 < n_blk) {
-      if (tid == 0) bulk_load(sKh, image(j + 1), 2 * P::OPB, bar_k);
-      ++issued_k;
-    }
-    // ---- 3. softmax of this thread's half row (keys 64 half .. 64 half + 63)
-    float sv[64];
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-      float v[32];
-      tmem_ld32(t_s + lane_base + 64 * half + c0, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sv[c0 + i] = v[i];
-    }
-    float mblk = -INFINITY;
-    if (full_vis && nkeys == 128) {  // every row of the CTA sees every key of the block
-#pragma unroll
-      for (int u = 0; u < 64; ++u) mblk = fmaxf(mblk, sv[u]);
-      if (!my_valid) mblk = -INFINITY;
-    } else {
-#pragma unroll
-      for (int u = 0; u < 64; ++u) {
-        const int t = 64 * half + u;
-        const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
-        sv[u] = vis ? sv[u] : -INFINITY;
-        mblk = fmaxf(mblk, sv[u]);
-      }
-    }
-    xch[half * 128 + row] = mblk;
-    __syncthreads();
-    mblk = fmaxf(xch[row], xch[128 + row]);  // the row's block maximum, same in both threads
-    // move the reference max (and rescale O) only when a score exceeds it by > 8
-    const bool need = mblk > m_ref + 8.0f;
-    const float m_new = need ? mblk : m_ref;
-    const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
-    if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        float v[32];
-        tmem_ld32(t_o + lane_base + half * (D / 2) + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(t_o + lane_base + half * (D / 2) + c0, v);
-      }
-    }
-    l_sum *= alpha;
-    m_ref = m_new;
-    float rs = 0.f;
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      __align__(16) __half2 h[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // exp2 of a non-positive argument (up to +8); results below 2^-126 flush to
-        // zero (they are below fp16 resolution too); a row with no visible key
-        // yet (m_ref = -inf) gets exp2(-inf) = 0 from the NaN-free guard below
-        const float p0 = m_ref == -INFINITY ? 0.f : ex2_ftz(sv[8 * c8 + 2 * e] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : ex2_ftz(sv[8 * c8 + 2 * e + 1] - m_ref);
-        const __half2 hp = __floats2half2_rn(p0, p1);
-        rs += __low2float(hp) + __high2float(hp);  // the sum of what the MMA will add
-        h[e] = hp;
-      }
-      *reinterpret_cast<uint4*>(sP + sw_off(row, 64 * half + 8 * c8, 128)) = *reinterpret_cast<uint4*>(h);
-    }
-    l_sum += rs;  // this thread's share of the row sum
-    // ---- 4. O += P V~
-    if (!mbar_wait_bounded(bar_v, j & 1)) *fail = 1;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    if (*fail) { ok = false; break; }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-        const uint32_t off_b = (kk >> 2) * D * 128 + (kk & 3) * 32;
-        mma_f16(t_o, sdesc(su32(sP) + off_a), sdesc(su32(sV) + off_b), idesc<D>(), (j > 0 || kk > 0));
-      }
-      mma_commit(bar_o);
-    }
-    ++issued_o;
-  }
-  if (!ok) {
-    // a wait gave up: let the work already issued finish (bounded) before
-    // the shared memory and TMEM are released
-    if (issued_s > 0) mbar_wait_bounded(bar_s, (issued_s - 1) & 1);
-    if (issued_o > 0) mbar_wait_bounded(bar_o, (issued_o - 1) & 1);
-    if (issued_k > 0) mbar_wait_bounded(bar_k, (issued_k - 1) & 1);
-    if (issued_v > 0) mbar_wait_bounded(bar_v, (issued_v - 1) & 1);
-  }
-  if (ok && n_blk > 0) {
-    if (!mbar_wait_bounded(bar_o, (n_blk - 1) & 1)) ok = false;
-  }
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  // ---- epilogue: O / l, one inverse rotation, store (one thread per row)
-  xch[half * 128 + row] = l_sum;
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (half == 0) {
-    const float l_row = xch[row] + xch[128 + row];
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const bool ok = *fail == 0;
+  // ---- epilogue: O / l, one inverse rotation, store (one thread per row)
+  if (tid < 128) {
     float o[D];
-    if (n_blk > 0) {
+    float l_row = 0.f;
+    if (n_blk > 0 && ok) {
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float v[32];
-        tmem_ld32(t_o + lane_base + c0, v);
+        tmem_ld32(t_o + lane_base_of(warp) + c0, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c0 + i] = v[i];
       }
+      l_row = tmem_ld1(t_o + lane_base_of(warp) + D);
     } else {
 #pragma unroll
       for (int c = 0; c < D; ++c) o[c] = 0.f;
@@ -670,7 +794,7 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
-  prefill_kernel<D><<<grid, P::NTHR, P::SMEM, st>>>(a);
+  prefill_kernel<D><<<grid, P::NTHR_ATT, P::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
