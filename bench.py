@@ -48,7 +48,7 @@ C_TILES, C_HEADS = 256, 8
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
     # one 16k-context layer: 17.39 MB read, nothing written back within the launch
-    "decode_split": {"src_sha": "4ee725ce3260e326", "bytes": 17392896},
+    "decode_split": {"src_sha": "19ca5db96362b892", "bytes": 17394432},
     # 2 x (134.30 MB read + 5.88 MB written) for 1024 tile-heads, scaled to 2048
     "compress": {"src_sha": "92c82f58b708b8f7", "bytes": 280351744},
 }
@@ -276,6 +276,175 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
                          "kernel": "prefill_kernel<128>",
                          "peak_source": peak_kind + " (dense bf16 burst; fp16 runs at the bf16 rate)"},
             "mma": "tcgen05 kind::f16, Q and K split hi+lo (3 MMAs for Q.K, 1 for P.V)"}
+
+
+def run_decode_sweeps(dev, lay, peaks, peak_kind):
+    """Decode split throughput beyond the headline configuration: the 8B-like
+    model at 4k and 32k context (36 layers of distinct caches, split launches
+    back to back as in the headline roofline), and batched decode with large
+    heads (32 ragged sequences with contexts uniform in [8k, 32k], 16q/4kv,
+    head_dim 256; one layer's cache is 0.6 GB), timed as back-to-back split
+    launches and as decode steps (split + combine) with a concurrent compress
+    stream promoting one tile per sequence per step."""
+    import torch
+    from kv_cache_quantization_token_gb300 import kvarn, synth
+    hbm = float(peaks["hbm_gbs"])
+    res = {}
+    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
+    stream = torch.cuda.Stream(device=dev)
+
+    def back_to_back(launch, n_launch, reps=10):
+        with torch.cuda.stream(stream):
+            launch()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * n_launch)
+
+    # ---- 8B-like decode at 4k and 32k ------------------------------------------
+    for ctx in (4096, 32768):
+        n0, w0, cap = ctx // 128, 64, 128
+        rb = lay.record_bytes
+        max_tiles = n0 + 1
+        tiles = torch.empty(LAYERS * HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
+        table = torch.empty(LAYERS, 1, HKV, max_tiles, dtype=torch.int64, device=dev)
+        win_k = torch.zeros(LAYERS, 1, HKV, cap, D, device=dev)
+        win_v = torch.zeros_like(win_k)
+        raw = []
+        for r in range(2):  # two distinct layers of values, stored at 36 distinct addresses
+            ks, vs = synth.kv_layer(WORKLOAD, 200 + r, HKV, ctx + w0, D)
+            raw.append((torch.from_numpy(ks.reshape(-1, D)).to(dev),
+                        torch.from_numpy(vs.reshape(-1, D)).to(dev), ks[:, ctx:], vs[:, ctx:]))
+            del ks, vs
+        src = torch.from_numpy((np.arange(HKV)[:, None] * (ctx + w0)
+                                + 128 * np.arange(n0)[None, :]).reshape(-1).astype(np.int64)).to(dev)
+        for l in range(LAYERS):
+            tab = ((l * HKV) * max_tiles + np.arange(HKV)[:, None] * max_tiles
+                   + np.arange(max_tiles)[None, :]) * rb
+            table[l, 0] = torch.from_numpy(tab.astype(np.int64))
+            kd, vd, kw, vw = raw[l % 2]
+            kvarn.compress_tile(kd, vd, src, tiles,
+                                torch.from_numpy(tab[:, :n0].reshape(-1).astype(np.int64)).to(dev), lay)
+            win_k[l, 0, :, :w0] = torch.from_numpy(kw).to(dev)
+            win_v[l, 0, :, :w0] = torch.from_numpy(vw).to(dev)
+        del raw
+        q = torch.from_numpy(synth.queries(WORKLOAD, 3, (LAYERS, 1, HQ, D))).to(dev)
+        ws = torch.empty(kvarn.decode_workspace_bytes(1, HQ, HKV, D, max_tiles, cap) + 256,
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty(LAYERS, 1, HQ, D, device=dev)
+        wst = torch.zeros(1, dtype=torch.int32, device=dev)
+        wl = torch.full((1,), w0, dtype=torch.int32, device=dev)
+        nt = torch.full((1,), n0, dtype=torch.int32, device=dev)
+
+        def splits():
+            for l in range(LAYERS):
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay, ws)
+
+        def steps():
+            for l in range(LAYERS):
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay, ws)
+                kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
+
+        split_ms = back_to_back(splits, LAYERS)
+        layer_ms = back_to_back(steps, LAYERS)
+        assert torch.isfinite(out).all().item(), "decode produced non-finite output"
+        nbytes = HKV * n0 * rb + HKV * w0 * D * 8 + HQ * D * 4
+        gbs = nbytes / (split_ms * 1e-3) / 1e9
+        res[f"qwen3_8b_ctx{ctx}"] = {
+            "split_back_to_back_ms": split_ms, "split_bytes_per_launch": nbytes,
+            "split_gbs": gbs, "split_frac": gbs / hbm,
+            "attention_ms_per_layer": layer_ms,
+            "tokens_per_s_36_layers": 1.0 / (LAYERS * layer_ms * 1e-3)}
+        del tiles, table, win_k, win_v, ws
+
+    # ---- batched decode, head_dim 256 ------------------------------------------
+    Bb, Hqb, Hkvb, Db, capb = 32, 16, 4, 256, 128
+    layb = kvarn.layout(Db)
+    rbb = layb.record_bytes
+    ctxs = synth.uniform_ints(4242, 8192, 32768, Bb)
+    ntl = ctxs // 128
+    wlen = ctxs % 128
+    max_tiles = int(ntl.max()) + 1
+    pool_tiles = 64  # distinct tile values per head, stored at every sequence's slots
+    ks, vs = synth.kv_layer("batched_d256_decode", 0, Hkvb, 128 * pool_tiles + capb, Db)
+    kd = torch.from_numpy(ks.reshape(-1, Db)).to(dev)
+    vd = torch.from_numpy(vs.reshape(-1, Db)).to(dev)
+    tiles = torch.empty(Bb * Hkvb * max_tiles * rbb, dtype=torch.uint8, device=dev)
+    tab = ((np.arange(Bb)[:, None, None] * Hkvb + np.arange(Hkvb)[None, :, None]) * max_tiles
+           + np.arange(max_tiles)[None, None, :]) * rbb
+    table = torch.from_numpy(tab.astype(np.int64)).to(dev)
+    src_l, dst_l = [], []
+    for b in range(Bb):
+        for h in range(Hkvb):
+            t = np.arange(ntl[b])
+            src_l.append(h * (128 * pool_tiles + capb) + 128 * (t % pool_tiles))
+            dst_l.append(tab[b, h, :ntl[b]])
+    kvarn.compress_tile(kd, vd, torch.from_numpy(np.concatenate(src_l).astype(np.int64)).to(dev),
+                        tiles, torch.from_numpy(np.concatenate(dst_l).astype(np.int64)).to(dev), layb)
+    win_k = torch.zeros(Bb, Hkvb, capb, Db, device=dev)
+    win_v = torch.zeros_like(win_k)
+    tail = torch.from_numpy(ks[:, 128 * pool_tiles:]).to(dev)
+    tailv = torch.from_numpy(vs[:, 128 * pool_tiles:]).to(dev)
+    win_k[:] = tail[None]
+    win_v[:] = tailv[None]
+    del ks, vs
+    q = torch.from_numpy(synth.queries("batched_d256_decode", 0, (Bb, Hqb, Db))).to(dev)
+    wst = torch.zeros(Bb, dtype=torch.int32, device=dev)
+    wl = torch.from_numpy(wlen.astype(np.int32)).to(dev)
+    nt = torch.from_numpy(ntl.astype(np.int32)).to(dev)
+    ws = torch.empty(kvarn.decode_workspace_bytes(Bb, Hqb, Hkvb, Db, max_tiles, capb) + 256,
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(Bb, Hqb, Db, device=dev)
+    # promotion work of one step: one tile per sequence and KV head, into scratch records
+    n_prom = Bb * Hkvb
+    psrc = torch.from_numpy((np.arange(n_prom) % Hkvb * (128 * pool_tiles + capb)
+                             + 128 * (np.arange(n_prom) % pool_tiles)).astype(np.int64)).to(dev)
+    pdst = torch.arange(n_prom, dtype=torch.int64, device=dev) * rbb
+    ptiles = torch.empty(n_prom * rbb, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    ev_f, ev_j = torch.cuda.Event(), torch.cuda.Event()
+
+    def split1():
+        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws)
+
+    def step_conc():
+        cur = torch.cuda.current_stream()
+        ev_f.record(cur)
+        side.wait_event(ev_f)
+        with torch.cuda.stream(side):
+            kvarn.compress_tile(kd, vd, psrc, ptiles, pdst, layb)
+        ev_j.record(side)
+        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws)
+        kvarn.decode_combine(ws, out, Hkvb, max_tiles, capb)
+        cur.wait_event(ev_j)
+
+    split_ms = back_to_back(lambda: [split1() for _ in range(8)], 8)
+    step_ms = back_to_back(step_conc, 1, reps=40)
+    assert torch.isfinite(out).all().item(), "decode produced non-finite output"
+    nbytes = int(ntl.sum()) * Hkvb * rbb + int(wlen.sum()) * Hkvb * Db * 8 + Bb * Hqb * Db * 4
+    gbs = nbytes / (split_ms * 1e-3) / 1e9
+    res["batched_d256"] = {
+        "workload": f"batch {Bb}, contexts uniform in [8192, 32768] (seeded; sum {int(ctxs.sum())}), "
+                    f"{Hqb}q/{Hkvb}kv heads, head_dim {Db}, K4/V2 tiles + FP32 window (W=128); "
+                    f"one layer",
+        "split_back_to_back_ms": split_ms, "split_bytes_per_launch": nbytes,
+        "split_gbs": gbs, "split_frac": gbs / hbm,
+        "step_ms_with_concurrent_compress": step_ms,
+        "tokens_per_s_per_layer": Bb / (step_ms * 1e-3),
+        "concurrent_compress_tile_heads_per_step": n_prom,
+        "peak_source": peak_kind}
+    kvarn.set_launch_flags(0)
+    return res
 
 
 def workload_config():
@@ -573,6 +742,8 @@ def main():
 
     # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256)
     prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
+    # ---- decode at other contexts and batched large-head decode
+    sweeps = run_decode_sweeps(dev, lay, peaks, peak_kind)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -611,6 +782,7 @@ def main():
                                       "traffic": ctraffic, "kernel": "compress_kernel<128>",
                                       "peak_source": peak_kind}},
             "prefill": prefill,
+            "decode_sweeps": sweeps,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

@@ -284,11 +284,13 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
   if (lane == 0) qmax[h] = mx;
 }
 
-template <int D, int GP, int NW_>
+template <int D, int GP, int NW_, int WPT_>
 struct DC {
   static constexpr int NW = NW_;                                // warps per CTA (4 or 8)
   static constexpr int NTHR = 32 * NW;
-  static constexpr int TPS = NW / 2;                            // tiles per item, one per warp pair
+  static constexpr int WPT = WPT_;                              // warps per tile (2 or 4)
+  static constexpr int TPS = NW / WPT;                          // tiles per item
+  static constexpr int CH = 4 / WPT;                            // 32-token chunks per warp
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
   static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
@@ -296,7 +298,7 @@ struct DC {
   static constexpr int CODE_LINES = CODE_BYTES / 128;           // 128-byte lines of that box
   static constexpr int NT = GP > 4 ? 2 : 1;                     // n8-tiles of (head, part) columns
   static constexpr int NCB = D / 16;                            // 16-channel blocks
-  static constexpr int HB = NCB / 2;                            // blocks whose B fragments a warp builds
+  static constexpr int HB = NCB / WPT;                          // blocks whose B fragments a warp builds
   static constexpr int NS = D / 64;                             // 64-channel slices of a V row
   // window rows staged per warp (K and V rows of one chunk fit the record region)
   static constexpr int WCH0 = (TPS * RB) / (NW * 2 * D * 4);
@@ -307,8 +309,8 @@ struct DC {
   static constexpr int OFF_QS = (REC_REGION + 15) / 16 * 16;    // f32 query [D/2][GP][2] (window: [D][GP])
   static constexpr int OFF_QMAX = OFF_QS + D * GP * 4;          // f32 [8] max |q'| per head
   static constexpr int OFF_BX = OFF_QMAX + 32;                  // B fragments [TPS][NCB][NT][32] x u32x2
-  static constexpr int OFF_PT = OFF_BX + TPS * NCB * NT * 32 * 8;  // (sum wd, bias) [TPS][2][GP]
-  static constexpr int OFF_SCW = OFF_PT + TPS * 2 * GP * 8;     // window probabilities [NW WCH][GP]
+  static constexpr int OFF_PT = OFF_BX + TPS * NCB * NT * 32 * 8;  // (sum wd, bias) [TPS][WPT][GP]
+  static constexpr int OFF_SCW = OFF_PT + TPS * WPT * GP * 8;   // window probabilities [NW WCH][GP]
   static constexpr int OFF_RED = OFF_SCW + (NW * WCH * GP * 4 + 15) / 16 * 16;  // f32 [NW][32]
   static constexpr int OFF_FLG = OFF_RED + NW * 32 * 4;         // int [TPS]
   static constexpr int NBAR = TPS > NW ? TPS : NW;               // one per tile, or per window chunk
@@ -317,7 +319,7 @@ struct DC {
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(RB % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
   static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D>::kKDelta, "code box");
-  static_assert(HB >= 1 && 2 * HB == NCB, "channel blocks per warp");
+  static_assert(HB >= 1 && WPT * HB == NCB && (WPT == 2 || WPT == 4), "channel blocks per warp");
   static_assert(2 * WCH * D * 4 * NW <= TPS * RB, "window chunks must fit the record region");
   static_assert(NW * GP * D * 4 <= REC_REGION, "window partials fit the record region");
 };
@@ -358,7 +360,7 @@ __device__ __forceinline__ void cta_max(float (&v)[N], float* red, int tid) {
   }
 }
 
-template <int D, int GP, int NW_>
+template <int D, int GP, int NW_, int WPT_>
 __global__ void __launch_bounds__(32 * NW_)
 decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
                     const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
@@ -367,10 +369,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
-  using C = DC<D, GP, NW_>;
+  using C = DC<D, GP, NW_, WPT_>;
   using R = Rec<D>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
-  constexpr int HB = C::HB;
+  constexpr int HB = C::HB, WPT = C::WPT, CH = C::CH;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled TMA boxes need 1024-byte aligned slots (the launch adds the slack)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -536,12 +538,13 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 
   // ========================= packed tiles, tensor cores ======================
-  // Warp pair p = warp / 2 owns tile p of the item; warp w of the pair takes
-  // its tokens 64 (w % 2) .. +63. The pair shares the folded query (each warp
-  // builds half of its channel blocks; one pair barrier per tile), each warp
-  // contracts scores and values of its tokens on mma.sync and keeps its own
-  // streaming-softmax state (m, l, acc) per query head; the four warps'
-  // states are merged at the end of the item.
+  // Warp group p = warp / WPT owns tile p of the item; warp w of the group
+  // takes the tile's tokens 32 CH (w % WPT) .. +32 CH - 1 (CH = 4 / WPT
+  // chunks of 32). The group shares the folded query (each warp builds 1/WPT
+  // of its channel blocks; one group barrier per tile), each warp contracts
+  // scores and values of its tokens on mma.sync and keeps its own
+  // streaming-softmax state (m, l, acc) per query head; the NW warps' states
+  // are merged at the end of the item.
   //
   // Each record slot holds the K and V codes as one 128B-swizzled TMA box
   // (K: channel rows of 64 bytes, V: token rows of D/4 bytes) followed by the
@@ -549,10 +552,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   // (g8, q4) rows 2q4 and 2q4+1 at byte pair g8: two channels x four tokens
   // (K) or two tokens x eight channels (V), a fragment's worth of codes.
   const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + item * TPS;
-  const int pair = warp >> 1, half = warp & 1;
+  const int pair = warp / WPT, half = warp % WPT;  // tile of the item, warp within its group
   float* qmax = reinterpret_cast<float*>(smem + C::OFF_QMAX);
   uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [TPS][NCB][NT][32]
-  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [TPS][2][GP]
+  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [TPS][WPT][GP]
   if (tid == 0) {
     for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
     fence_mbar_init();
@@ -621,7 +624,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       pow2_scale(qb * mf, 16.0f, scB[nt], i_);
       pow2_scale(qa * mf, 16.0f, s_, invA[nt]);
     }
-    // this warp's half of the channel blocks: B fragments to shared memory, and
+    // this warp's share of the channel blocks: B fragments to shared memory, and
     // per-head partial sums of wd (fp32) and of the bias q' s lo
     float wsum[NT], bsum[NT];
 #pragma unroll
@@ -655,14 +658,14 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int m = 1; m <= 2; m <<= 1) {  // over q4: all channels of this warp's half
+      for (int m = 1; m <= 2; m <<= 1) {  // over q4: all channels of this warp's share
         wsum[nt] += __shfl_xor_sync(0xffffffffu, wsum[nt], m);
         bsum[nt] += __shfl_xor_sync(0xffffffffu, bsum[nt], m);
       }
       if (q4 == 0 && is_hi && 4 * nt + hb < GP)
-        pt[(kk * 2 + half) * GP + 4 * nt + hb] = make_float2(wsum[nt], bsum[nt]);
+        pt[(kk * WPT + half) * GP + 4 * nt + hb] = make_float2(wsum[nt], bsum[nt]);
     }
-    asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");  // the pair's barrier
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");  // the group's barrier
 
     // sum_c wd_c code_tc = S inv - 16 sum_c wd_c: per-head constants of the
     // accumulator view (head 4nt + q4)
@@ -671,23 +674,25 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int nt = 0; nt < NT; ++nt) {
       float ws = 0.f, bs = 0.f;
       if (4 * nt + q4 < GP) {
-        const float2 v0 = pt[(kk * 2 + 0) * GP + 4 * nt + q4];
-        const float2 v1 = pt[(kk * 2 + 1) * GP + 4 * nt + q4];
-        ws = v0.x + v1.x;
-        bs = v0.y + v1.y;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) {
+          const float2 v = pt[(kk * WPT + w) * GP + 4 * nt + q4];
+          ws += v.x;
+          bs += v.y;
+        }
       }
       cstA[nt] = bs - 16.0f * ws;
     }
 
-    // ---- phase A: scores of this warp's 64 tokens. Chunk w4 = tokens 32 w4 ..
-    // +31 (w4 = 2 half, 2 half + 1); M-block j: row g8 <-> token 32 w4 + 4 g8 + 2j,
+    // ---- phase A: scores of this warp's 32 CH tokens. Chunk w4 = tokens 32 w4 ..
+    // +31 (w4 = CH half + w2); M-block j: row g8 <-> token 32 w4 + 4 g8 + 2j,
     // row g8 + 8 <-> that token + 1.
     const int mi = lane >> 3, ri = lane & 7;
     const uint32_t kaddr0 =
-        (uint32_t)((16 * (mi >> 1) + 8 * (mi & 1) + ri) * 64 + 16 * (2 * half));
-    float acc[2][2][NT][4];
+        (uint32_t)((16 * (mi >> 1) + 8 * (mi & 1) + ri) * 64 + 16 * (CH * half));
+    float acc[CH][2][NT][4];
 #pragma unroll
-    for (int w2 = 0; w2 < 2; ++w2)
+    for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -702,7 +707,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) bf[u][nt] = bx[((kk * NCB + cp + u) * NT + nt) * 32 + lane];
 #pragma unroll
-      for (int w2 = 0; w2 < 2; ++w2) {
+      for (int w2 = 0; w2 < CH; ++w2) {
         uint32_t x[4];  // channel blocks cp, cp+1; channels +0..7 and +8..15 of each
         ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64 + 16 * w2)), x[0], x[1], x[2], x[3]);
 #pragma unroll
@@ -720,10 +725,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
 
     // ---- scores z = r_t (sum_c wd_c code_tc + bias) and the warp's softmax
-    float z[2][2][2][NT];
+    float z[CH][2][2][NT];
 #pragma unroll
-    for (int w2 = 0; w2 < 2; ++w2) {
-      const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * (2 * half + w2) + 4 * g8);
+    for (int w2 = 0; w2 < CH; ++w2) {
+      const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * (CH * half + w2) + 4 * g8);
       const float rt[2][2] = {{r4.x, r4.y}, {r4.z, r4.w}};
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -739,7 +744,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int nt = 0; nt < NT; ++nt) {
       float mx = kNegInf;
 #pragma unroll
-      for (int w2 = 0; w2 < 2; ++w2)
+      for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -751,7 +756,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       m_run[nt] = mn;
       float ls = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < 2; ++w2)
+      for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -769,16 +774,16 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     const float* vD = reinterpret_cast<const float*>(Rk + R::kVDelta);
     const float* vL = reinterpret_cast<const float*>(Rk + R::kVLo);
     const float* vS = reinterpret_cast<const float*>(Rk + R::kVS);
-    uint32_t bB[GV][2][2][NT][2];
+    uint32_t bB[GV][CH][2][NT][2];
     float invP[GV][NT], cstP[GV][NT];
 #pragma unroll
     for (int gv = 0; gv < GV; ++gv) {
-      float pd[2][2][2][NT], pm[NT], lt[NT];
+      float pd[CH][2][2][NT], pm[NT], lt[NT];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) { pm[nt] = 0.f; lt[nt] = 0.f; }
 #pragma unroll
-      for (int w2 = 0; w2 < 2; ++w2) {
-        const int t0 = 32 * (2 * half + w2) + 4 * g8;
+      for (int w2 = 0; w2 < CH; ++w2) {
+        const int t0 = 32 * (CH * half + w2) + 4 * g8;
         const float4 vr4 = *reinterpret_cast<const float4*>(vR + t0);
         const float vrt[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
 #pragma unroll
@@ -801,7 +806,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         pow2_scale(pm[nt], 4.0f, sc2, inv2);
         float sp = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < 2; ++w2)
+        for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const uint32_t xl = hilo_one(pd[w2][j][0][nt] * sc2, sp);  // row g8: token 4 g8 + 2j
@@ -820,11 +825,11 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
 
-    // ---- phase B: this warp's 64 tokens against all channels, one 64-channel
+    // ---- phase B: this warp's 32 CH tokens against all channels, one 64-channel
     // slice of the V rows at a time. M-block mu of slice sl: row g8 <-> channel
     // 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1.
     const uint32_t vaddr0 =
-        (uint32_t)(C::K_BYTES + (64 * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
+        (uint32_t)(C::K_BYTES + (32 * CH * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
 #pragma unroll
     for (int sl = 0; sl < NS; ++sl) {
       const int gv = (64 * sl) / R::kVGroup;
@@ -836,7 +841,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[mu][nt][e] = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < 2; ++w2) {
+      for (int w2 = 0; w2 < CH; ++w2) {
         uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
         ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * (D / 4) + 16 * sl)), y[0], y[1], y[2],
                   y[3]);
@@ -1064,16 +1069,16 @@ cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int GP, int NW>
+template <int D, int GP, int NW, int WPT>
 cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  using C = DC<D, GP, NW>;
+  using C = DC<D, GP, NW, WPT>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, NW>,
+    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, NW, WPT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM + 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
@@ -1084,7 +1089,7 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   const unsigned fl = launch_flags();
   const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
   LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::SMEM + 1024, st);
-  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW>, a.q, a.tiles, a.tile_table,
+  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW, WPT>, a.q, a.tiles, a.tile_table,
                             a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
                             a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale,
                             ws_ml, ws_acc, prefetch, tmap);
@@ -1093,10 +1098,14 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
 template <int D, int GP>
 cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  switch (p.tiles_per_item) {  // a warp pair per tile
-    case 2: return launch_split_t<D, GP, 4>(p, a, ws_ml, ws_acc, st);
-    case 4:
-      if constexpr (D <= 128) return launch_split_t<D, GP, 8>(p, a, ws_ml, ws_acc, st);
+  // (tiles per item, warps per tile)
+  const int key = 10 * p.tiles_per_item + p.warps_per_tile;
+  switch (key) {
+    case 22: return launch_split_t<D, GP, 4, 2>(p, a, ws_ml, ws_acc, st);
+    case 14: return launch_split_t<D, GP, 4, 4>(p, a, ws_ml, ws_acc, st);
+    case 24: return launch_split_t<D, GP, 8, 4>(p, a, ws_ml, ws_acc, st);
+    case 42:
+      if constexpr (D <= 128) return launch_split_t<D, GP, 8, 2>(p, a, ws_ml, ws_acc, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
@@ -1137,15 +1146,20 @@ int sm_count() {
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  // a warp pair per tile (DC<D, GP, NW>): 2 tiles per CTA, or 4 (eight warps)
+  // head_dim <= 128: a warp pair per tile, 2 tiles per CTA, or 4 (eight warps)
   // once the grid has at least 4 tiles per SM, which halves the partials the
-  // combine reads and the per-CTA set-up (head_dim 256 keeps 2: shared memory)
+  // combine reads and the per-CTA set-up. head_dim 256: four warps per tile
+  // (32 tokens each) and one tile per CTA, whose record is twice as large;
+  // the extra warps per SM hide more of each warp's mma.sync / shuffle chain
+  // (a warp pair per tile leaves 12 warps per SM there).
   const int64_t total = (int64_t)B * Hkv * max_tiles;
-  const int tps = (D <= 128 && total >= 4LL * sm_count()) ? 4 : 2;
-  const int nw = 2 * tps;
+  const int wpt = D <= 128 ? 2 : 4;
+  const int tps = D <= 128 ? ((total >= 4LL * sm_count()) ? 4 : 2) : 1;
+  const int nw = wpt * tps;
   p->tiles_per_item = tps;
+  p->warps_per_tile = wpt;
   p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
-  // window rows per warp and per item, as DC<D, GP, NW>::WCH and its NW warps
+  // window rows per warp and per item, as DC<D, GP, NW, WPT>::WCH and its NW warps
   const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
   const int w0 = (tps * rb) / (nw * 2 * D * 4);
   const int wch = w0 >= 16 ? 16 : w0 >= 8 ? 8 : w0 >= 4 ? 4 : 2;
