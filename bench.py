@@ -465,6 +465,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--section", default="all", choices=["all", "prefill", "decode-sweeps"],
+                    help="run one secondary measurement alone and print its JSON (for profiling)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -487,6 +489,15 @@ def main():
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     lay = kvarn.layout(D)
+    if args.section != "all":
+        peaks, peak_kind = measured_peaks()
+        if args.section == "prefill":
+            sec = run_prefill_bench(dev, torch.cuda.Stream(device=dev), lay, peaks, peak_kind)
+        else:
+            sec = run_decode_sweeps(dev, lay, peaks, peak_kind)
+        if rank == 0:
+            print(json.dumps({"section": args.section, "result": sec}), flush=True)
+        return
     rb = lay.record_bytes
     B = 1
     cap = 128
