@@ -207,14 +207,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// Packed fp16 pair of the hi (odd == false) or lo parts of (x0, x1): x = hi + lo
-// to about 22 bits.
-__device__ __forceinline__ uint32_t hilo_pair(float x0, float x1, bool lo_part) {
-  const __half2 hi = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(hi);
-  const __half2 r = lo_part ? __floats2half2_rn(x0 - hf.x, x1 - hf.y) : hi;
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
 // 2^e for the power-of-two scale that brings max |x| = m into [2^10, 2^11)
 // (1 when m is zero or not finite), and its inverse times `k`.
 __device__ __forceinline__ void pow2_scale(float m, float k, float& scale, float& inv_k) {
@@ -232,14 +224,17 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
-// {fp16(x), fp16(x - fp16(x))} packed low/high; adds the value the pair represents to sum.
-__device__ __forceinline__ uint32_t hilo_one(float x, float& sum) {
-  const __half h = __float2half_rn(x);
-  const float hf = __half2float(h);
-  const __half l = __float2half_rn(x - hf);
-  sum += hf + __half2float(l);
-  const __half2 r = __halves2half2(h, l);
+// {fp16(x), fp16(x - fp16(x))} packed low/high: x to about 22 bits.
+__device__ __forceinline__ uint32_t hilo_one(float x) {
+  const float hf = __half2float(__float2half_rn(x));
+  const __half2 r = __floats2half2_rn(x, x - hf);
   return *reinterpret_cast<const uint32_t*>(&r);
+}
+// 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // One warp rotates one query head for the tile path: x = f / sqrt(D) * H q,
@@ -361,7 +356,7 @@ __device__ __forceinline__ void cta_max(float (&v)[N], float* red, int tid) {
 }
 
 template <int D, int GP, int NW_, int WPT_>
-__global__ void __launch_bounds__(32 * NW_)
+__global__ void __launch_bounds__(32 * NW_, GP <= 4 ? (NW_ == 8 ? 3 : 6) : 1)
 decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
                     const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
                     const float* __restrict__ win_k, const float* __restrict__ win_v,
@@ -625,45 +620,51 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       pow2_scale(qa * mf, 16.0f, s_, invA[nt]);
     }
     // this warp's share of the channel blocks: B fragments to shared memory, and
-    // per-head partial sums of wd (fp32) and of the bias q' s lo
-    float wsum[NT], bsum[NT];
+    // per-head partial sums of wd (fp32) and of the bias q' s lo. In block cb,
+    // lane (g8, q4) forms both fp16 parts of wd for head 4nt + hb on the channel
+    // pair 16 cb + 2 q4 + 8 (g8 & 1) and swaps one part with lane ^ 4, which
+    // took the other pair of the same head: the hi lane keeps both hi parts,
+    // the lo lane both lo parts.
+    const int hl = g8 & 1;
+    float2 wsum[NT], bsum[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) { wsum[nt] = 0.f; bsum[nt] = 0.f; }
+    for (int nt = 0; nt < NT; ++nt) { wsum[nt] = make_float2(0.f, 0.f); bsum[nt] = wsum[nt]; }
 #pragma unroll
     for (int u = 0; u < HB; ++u) {
       const int cb = HB * half + u;
-      uint32_t fr[NT][2];
+      const int c = 16 * cb + 2 * q4 + 8 * hl;
+      const float2 s = *reinterpret_cast<const float2*>(kS + c);
+      const float2 dd = *reinterpret_cast<const float2*>(kD + c);
+      const float2 lo = *reinterpret_cast<const float2*>(kL + c);
+      const float2 sd = __fmul2_rn(s, dd), sl = __fmul2_rn(s, lo);
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        const int c = 16 * cb + 2 * q4 + 8 * hlf;
-        const float2 s = *reinterpret_cast<const float2*>(kS + c);
-        const float2 dd = *reinterpret_cast<const float2*>(kD + c);
-        const float2 lo = *reinterpret_cast<const float2*>(kL + c);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int h = 4 * nt + hb;
-          const float2 qv = h < GP ? *reinterpret_cast<const float2*>(qs + ((c >> 1) * GP + h) * 2)
-                                   : make_float2(0.f, 0.f);
-          const float w0 = qv.x * s.x, w1 = qv.y * s.y;
-          const float x0 = w0 * dd.x, x1 = w1 * dd.y;
-          fr[nt][hlf] = hilo_pair(x0 * scB[nt], x1 * scB[nt], !is_hi);
-          wsum[nt] += x0 + x1;
-          bsum[nt] = fmaf(w1, lo.y, fmaf(w0, lo.x, bsum[nt]));
-        }
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = 4 * nt + hb;
+        const float2 qv = h < GP ? *reinterpret_cast<const float2*>(qs + ((c >> 1) * GP + h) * 2)
+                                 : make_float2(0.f, 0.f);
+        const float2 x = __fmul2_rn(qv, sd);
+        wsum[nt] = __fadd2_rn(wsum[nt], x);
+        bsum[nt] = __ffma2_rn(qv, sl, bsum[nt]);
+        const float2 xs = __fmul2_rn(x, make_float2(scB[nt], scB[nt]));
+        const __half2 hi = __floats2half2_rn(xs.x, xs.y);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo16 = __floats2half2_rn(xs.x - hf.x, xs.y - hf.y);
+        const uint32_t hu = *reinterpret_cast<const uint32_t*>(&hi);
+        const uint32_t lu = *reinterpret_cast<const uint32_t*>(&lo16);
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, hl ? hu : lu, 4);
+        bx[((kk * NCB + cb) * NT + nt) * 32 + lane] = hl ? make_uint2(got, lu) : make_uint2(hu, got);
       }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        bx[((kk * NCB + cb) * NT + nt) * 32 + lane] = make_uint2(fr[nt][0], fr[nt][1]);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+      float ws = wsum[nt].x + wsum[nt].y, bs = bsum[nt].x + bsum[nt].y;
 #pragma unroll
-      for (int m = 1; m <= 2; m <<= 1) {  // over q4: all channels of this warp's share
-        wsum[nt] += __shfl_xor_sync(0xffffffffu, wsum[nt], m);
-        bsum[nt] += __shfl_xor_sync(0xffffffffu, bsum[nt], m);
+      for (int m = 1; m <= 4; m <<= 1) {  // over q4 and the hi/lo lane: all channels of this warp's share
+        ws += __shfl_xor_sync(0xffffffffu, ws, m);
+        bs += __shfl_xor_sync(0xffffffffu, bs, m);
       }
       if (q4 == 0 && is_hi && 4 * nt + hb < GP)
-        pt[(kk * WPT + half) * GP + 4 * nt + hb] = make_float2(wsum[nt], bsum[nt]);
+        pt[(kk * WPT + half) * GP + 4 * nt + hb] = make_float2(ws, bs);
     }
     asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");  // the group's barrier
 
@@ -739,7 +740,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
             z[w2][j][rr][nt] = rt[j][rr] * fmaf(acc[w2][j][nt][2 * rr] + acc[w2][j][nt][2 * rr + 1],
                                                 invA[nt], cstA[nt]);
     }
-    float alpha[NT];
+    // each warp takes one tile, so its streaming state starts here: no rescale
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float mx = kNegInf;
@@ -751,9 +752,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           for (int rr = 0; rr < 2; ++rr) mx = fmaxf(mx, z[w2][j][rr][nt]);
 #pragma unroll
       for (int m = 4; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      const float mn = fmaxf(m_run[nt], mx);
-      alpha[nt] = exp2f(m_run[nt] - mn);
-      m_run[nt] = mn;
+      m_run[nt] = mx;
       float ls = 0.f;
 #pragma unroll
       for (int w2 = 0; w2 < CH; ++w2)
@@ -761,10 +760,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
-            z[w2][j][rr][nt] = exp2f(z[w2][j][rr][nt] - mn);  // now p
+            z[w2][j][rr][nt] = ex2_approx(z[w2][j][rr][nt] - mx);  // now p
             ls += z[w2][j][rr][nt];
           }
-      l_run[nt] = fmaf(l_run[nt], alpha[nt], ls);
+      l_run[nt] = ls;
     }
 
     // ---- value side: pd_t = p_t r_t delta_tg as fp16 hi + lo, transposed into
@@ -786,9 +785,19 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         const int t0 = 32 * (CH * half + w2) + 4 * g8;
         const float4 vr4 = *reinterpret_cast<const float4*>(vR + t0);
         const float vrt[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
+        float dv[4], lv[4];
+        if constexpr (GV == 1) {
+          const float4 d4 = *reinterpret_cast<const float4*>(vD + t0);
+          const float4 l4 = *reinterpret_cast<const float4*>(vL + t0);
+          dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
+          lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { dv[e] = vD[(t0 + e) * GV + gv]; lv[e] = vL[(t0 + e) * GV + gv]; }
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float d = vD[(t0 + e) * GV + gv], lo = vL[(t0 + e) * GV + gv];
+          const float d = dv[e], lo = lv[e];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const float pv = z[w2][e >> 1][e & 1][nt] * vrt[e];
@@ -809,8 +818,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const uint32_t xl = hilo_one(pd[w2][j][0][nt] * sc2, sp);  // row g8: token 4 g8 + 2j
-            const uint32_t xh = hilo_one(pd[w2][j][1][nt] * sc2, sp);  // token 4 g8 + 2j + 1
+            const float xa = pd[w2][j][0][nt] * sc2, xb = pd[w2][j][1][nt] * sc2;
+            sp += xa + xb;
+            const uint32_t xl = hilo_one(xa);  // row g8: token 4 g8 + 2j
+            const uint32_t xh = hilo_one(xb);  // token 4 g8 + 2j + 1
             bB[gv][w2][j][nt][0] = movmatrix_t(xl);
             bB[gv][w2][j][nt][1] = movmatrix_t(xh);
           }
@@ -861,7 +872,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
               mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
           }
       }
-      // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
+      // acc_c = s_c (4 2^-e (O - sum pd) + sum p r lo)
       const float4 s0 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8);
       const float4 s1 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8 + 4);
       const float sv[4][2] = {{s0.x, s0.y}, {s0.z, s0.w}, {s1.x, s1.y}, {s1.z, s1.w}};
@@ -872,8 +883,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
-            out_acc[sl][mu][rr][nt] = fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
-                                           sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]));
+            out_acc[sl][mu][rr][nt] = sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]);
           }
     }
   }
