@@ -30,6 +30,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvarn_common.cuh"
@@ -281,10 +282,10 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
 
 template <int D, int GP, int NW_, int WPT_>
 struct DC {
-  static constexpr int NW = NW_;                                // warps per CTA (4 or 8)
+  static constexpr int NW = NW_;                                // warps per CTA (2, 4 or 8)
   static constexpr int NTHR = 32 * NW;
   static constexpr int WPT = WPT_;                              // warps per tile (2 or 4)
-  static constexpr int TPS = NW / WPT;                          // tiles per item
+  static constexpr int TPS = NW / WPT;                          // tiles per round
   static constexpr int CH = 4 / WPT;                            // 32-token chunks per warp
   static constexpr int RB = Rec<D>::kBytes;
   static constexpr int GV = Rec<D>::kGv;
@@ -300,23 +301,36 @@ struct DC {
   static constexpr int WCH = WCH0 >= 16 ? 16 : WCH0 >= 8 ? 8 : WCH0 >= 4 ? 4 : 2;
   static constexpr int DP = D + 8;                              // padded channel stride of the merge
   static constexpr int MRG = NW * GP * DP * 4;                  // merge region [NW][GP][DP], over records
-  static constexpr int REC_REGION = TPS * RB > MRG ? TPS * RB : MRG;
-  static constexpr int OFF_QS = (REC_REGION + 15) / 16 * 16;    // f32 query [D/2][GP][2] (window: [D][GP])
+  // Small regions first, then the record slots (1024-byte aligned for the
+  // swizzled boxes): TPS slots, or 2 TPS when the warp groups take several
+  // tiles in turn.
+  static constexpr int OFF_QS = 0;                              // f32 query [D/2][GP][2] (window: [D][GP])
   static constexpr int OFF_QMAX = OFF_QS + D * GP * 4;          // f32 [8] max |q'| per head
-  static constexpr int OFF_BX = OFF_QMAX + 32;                  // B fragments [TPS][NCB][NT][32] x u32x2
-  static constexpr int OFF_PT = OFF_BX + TPS * NCB * NT * 32 * 8;  // (sum wd, bias) [TPS][WPT][GP]
-  static constexpr int OFF_SCW = OFF_PT + TPS * WPT * GP * 8;   // window probabilities [NW WCH][GP]
-  static constexpr int OFF_RED = OFF_SCW + (NW * WCH * GP * 4 + 15) / 16 * 16;  // f32 [NW][32]
-  static constexpr int OFF_FLG = OFF_RED + NW * 32 * 4;         // int [TPS]
-  static constexpr int NBAR = TPS > NW ? TPS : NW;               // one per tile, or per window chunk
-  static constexpr int OFF_BAR = (OFF_FLG + TPS * 4 + 7) / 8 * 8;
-  static constexpr int SMEM = (OFF_BAR + NBAR * 8 + 15) / 16 * 16;
+  // tile items: B fragments [TPS][NCB][NT][32] x u32x2; window items: their
+  // probabilities [NW WCH][GP] and reduction slots [NW][32] in the same bytes
+  static constexpr int BX_BYTES = TPS * NCB * NT * 32 * 8;
+  static constexpr int SCW_BYTES = (NW * WCH * GP * 4 + 15) / 16 * 16;
+  static constexpr int WIN_BYTES = SCW_BYTES + NW * 32 * 4;
+  static constexpr int OFF_BX = OFF_QMAX + 32;
+  static constexpr int OFF_SCW = OFF_BX;
+  static constexpr int OFF_WRED = OFF_BX + SCW_BYTES;
+  static constexpr int OFF_PT = OFF_BX + (BX_BYTES > WIN_BYTES ? BX_BYTES : WIN_BYTES);  // (sum wd, bias) [TPS][WPT][GP]
+  static constexpr int OFF_FLG = OFF_PT + TPS * WPT * GP * 8;   // int [2 TPS]: slot copy issued / parity pending
+  static constexpr int NBAR = 2 * TPS > NW ? 2 * TPS : NW;       // one per record slot, or per window chunk
+  static constexpr int OFF_BAR = (OFF_FLG + 2 * TPS * 4 + 7) / 8 * 8;
+  static constexpr int OFF_REC = (OFF_BAR + NBAR * 8 + 1023) / 1024 * 1024;
+  static constexpr int REC_MIN = TPS * RB > MRG + NW * 128 ? TPS * RB : MRG + NW * 128;
+  static constexpr int OFF_TRED = MRG;                          // tile items' reduction slots (record-relative)
+  // dynamic shared memory for `slots` record slots (without the alignment slack)
+  static constexpr int smem_bytes(int slots) {
+    return OFF_REC + (slots * RB > REC_MIN ? slots * RB : REC_MIN);
+  }
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(RB % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
   static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D>::kKDelta, "code box");
   static_assert(HB >= 1 && WPT * HB == NCB && (WPT == 2 || WPT == 4), "channel blocks per warp");
   static_assert(2 * WCH * D * 4 * NW <= TPS * RB, "window chunks must fit the record region");
-  static_assert(NW * GP * D * 4 <= REC_REGION, "window partials fit the record region");
+  static_assert(NW * GP * D * 4 <= REC_MIN, "window partials fit the record region");
 };
 
 // Sum over the CTA (NW warps) of per-thread vectors v[N]; every thread gets the totals.
@@ -355,14 +369,16 @@ __device__ __forceinline__ void cta_max(float (&v)[N], float* red, int tid) {
   }
 }
 
-template <int D, int GP, int NW_, int WPT_>
-__global__ void __launch_bounds__(32 * NW_, GP <= 4 ? (NW_ == 8 ? 3 : 6) : 1)
+// MR: multi-round items (each warp group takes several tiles in turn, records
+// double-buffered); without it every group takes at most one tile.
+template <int D, int GP, int NW_, int WPT_, bool MR>
+__global__ void __launch_bounds__(32 * NW_, GP <= 4 ? (MR || NW_ == 8 ? 3 : 6) : 1)
 decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ tiles,
                     const int64_t* __restrict__ tile_table, const int32_t* __restrict__ n_tiles,
                     const float* __restrict__ win_k, const float* __restrict__ win_v,
                     const int32_t* __restrict__ win_start, const int32_t* __restrict__ win_len,
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
-                    float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
+                    int rounds_arg, float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, NW_, WPT_>;
   using R = Rec<D>;
@@ -371,11 +387,14 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled TMA boxes need 1024-byte aligned slots (the launch adds the slack)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* rec = smem + C::OFF_REC;
   const int item = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = lane >> 2, q4 = lane & 3;  // mma fragment coordinates
   const bool is_win = item >= tile_items;
   const int64_t part = ((int64_t)b * Hq + (int64_t)kvh * G) * items + item;
+  const int rounds = MR ? rounds_arg : 1;
+  const int span = TPS * rounds;  // packed tiles of a tile item
   // Under programmatic dependent launch, wait for the previous kernel on the
   // stream before touching memory; with prefetch, tile items first read
   // n_tiles, the tile table and their records (which, by the caller's
@@ -383,11 +402,11 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   const bool early = prefetch && !is_win;
   if (!early) pdl_wait();
 
-  // slots of this item: packed tiles, or window chunks of WCH rows (one per warp)
+  // work of this item: packed tiles, or window chunks of WCH rows (one per warp)
   int nslot, wlen = 0, wstart = 0, wj0 = 0;
   if (!is_win) {
     const int nt = min(max(n_tiles[b], 0), max_tiles);
-    nslot = min(max(nt - item * TPS, 0), TPS);
+    nslot = min(max(nt - item * span, 0), span);
   } else {
     wlen = min(max(win_len[b], 0), cap);
     wstart = ((win_start[b] % cap) + cap) % cap;
@@ -405,7 +424,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
   float* sc = reinterpret_cast<float*>(smem + C::OFF_SCW);
   float* qs = reinterpret_cast<float*>(smem + C::OFF_QS);
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  float* red = reinterpret_cast<float*>(is_win ? smem + C::OFF_WRED : rec + C::OFF_TRED);
   int* okf = reinterpret_cast<int*>(smem + C::OFF_FLG);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
 
@@ -425,7 +444,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       const int s0 = (wstart + wj0 + C::WCH * kk) % cap;
       const int n1 = min(n, cap - s0);
       mbar_expect_tx(&bar[kk], (uint32_t)(n * D * 4 * 2));
-      unsigned char* dst = smem + kk * (2 * C::WCH * D * 4);
+      unsigned char* dst = rec + kk * (2 * C::WCH * D * 4);
       bulk_g2s(dst, win_k + (head_base + s0) * D, n1 * D * 4, &bar[kk]);
       bulk_g2s(dst + C::WCH * D * 4, win_v + (head_base + s0) * D, n1 * D * 4, &bar[kk]);
       if (n1 < n) {
@@ -441,7 +460,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     const int k = warp;
     const bool have = k < nslot;
     bool ok = have && mbar_wait(&bar[k], 0);
-    const float* Kw = reinterpret_cast<const float*>(smem + k * (2 * C::WCH * D * 4));
+    const float* Kw = reinterpret_cast<const float*>(rec + k * (2 * C::WCH * D * 4));
     const float* Vw = Kw + C::WCH * D;
     const int wn = min(C::WCH, wlen - (wj0 + C::WCH * k));
     constexpr int E = D / 32;
@@ -507,7 +526,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     bad = __syncthreads_or(bad);
     cta_sum<GP, NW>(l, red, tid);
     // the partial acc of the warps is summed through the (now free) staging region
-    float* vred = reinterpret_cast<float*>(smem);
+    float* vred = reinterpret_cast<float*>(rec);
     __syncthreads();
 #pragma unroll
     for (int e = 0; e < E; ++e)
@@ -546,26 +565,39 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   // scales. ldmatrix.trans reads 8 rows x 16 bytes of codes and leaves in lane
   // (g8, q4) rows 2q4 and 2q4+1 at byte pair g8: two channels x four tokens
   // (K) or two tokens x eight channels (V), a fragment's worth of codes.
-  const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + item * TPS;
-  const int pair = warp / WPT, half = warp % WPT;  // tile of the item, warp within its group
+  const int64_t* trow = tile_table + ((int64_t)b * Hkv + kvh) * max_tiles + (int64_t)item * span;
+  const int pair = warp / WPT, half = warp % WPT;  // warp group, warp within the group
+  const bool dbuf = MR && rounds > 1;              // two record slots per group
   float* qmax = reinterpret_cast<float*>(smem + C::OFF_QMAX);
   uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [TPS][NCB][NT][32]
   float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [TPS][WPT][GP]
+  const bool issuer = lane == 0 && half == 0;                 // the group's copy issuer
+  // Copies a packed tile into a record slot (one TMA box of codes plus one bulk
+  // copy of the scales, completing on the slot's barrier); okf[slot] tells
+  // the group whether a copy was issued (record offsets must be multiples of
+  // 128 bytes; others poison the result).
+  auto issue = [&](int li, int slot) {
+    const int64_t off = trow[li];
+    const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
+    okf[slot] = aligned;
+    if (aligned) {
+      mbar_expect_tx(&bar[slot], C::RB);
+      tma_load_2d(rec + slot * C::RB, &tmap, 0, (int)(off >> 7), &bar[slot]);
+      bulk_g2s(rec + slot * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
+               C::RB - C::CODE_BYTES, &bar[slot]);
+    }
+    return aligned;
+  };
   if (tid == 0) {
-    for (int kk = 0; kk < nslot; ++kk) mbar_init(&bar[kk], 1);
+    for (int kk = 0; kk < (dbuf ? 2 * TPS : TPS); ++kk) mbar_init(&bar[kk], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (lane == 0 && half == 0 && pair < nslot) {
-    const int64_t off = trow[pair];
-    const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
-    okf[pair] = aligned;
-    if (aligned) {
-      mbar_expect_tx(&bar[pair], C::RB);
-      tma_load_2d(smem + pair * C::RB, &tmap, 0, (int)(off >> 7), &bar[pair]);
-      bulk_g2s(smem + pair * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
-               C::RB - C::CODE_BYTES, &bar[pair]);
-    }
+  // copies in flight that this issuer has not seen land: parity + 1, per slot of its group
+  int pend0 = 0, pend1 = 0;
+  if (issuer) {
+    if (pair < nslot && issue(pair, pair)) pend0 = 1;
+    if (dbuf && pair + TPS < nslot && issue(pair + TPS, pair + TPS)) pend1 = 1;
   }
   if (early) pdl_wait();
   pdl_trigger();
@@ -594,11 +626,18 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) out_acc[sl][mu][rr][nt] = 0.f;
 
-  if (pair < nslot) {  // both warps of the pair agree
+  // group `pair` takes the item's tiles pair, pair + TPS, ... in turn
+  for (int k = 0; k < rounds && pair + TPS * k < nslot; ++k) {  // uniform over the group
     const int kk = pair;
-    const unsigned char* Rk = smem + kk * C::RB;
+    const int slot = pair + (dbuf ? TPS * (k & 1) : 0);
+    const uint32_t par = dbuf ? (uint32_t)((k >> 1) & 1) : 0u;
+    const unsigned char* Rk = rec + slot * C::RB;
     const uint32_t rk = smem_u32(Rk);
-    if (!okf[kk] || !mbar_wait(&bar[kk], 0)) bad = 1;  // computed on, result poisoned
+    const bool landed = okf[slot] && mbar_wait(&bar[slot], par);
+    if (!landed) bad = 1;  // computed on, result poisoned
+    if (issuer && landed) {
+      if (k & 1) pend1 = 0; else pend0 = 0;
+    }
     const float* kS = reinterpret_cast<const float*>(Rk + R::kKS);
     const float* kD = reinterpret_cast<const float*>(Rk + R::kKDelta);
     const float* kL = reinterpret_cast<const float*>(Rk + R::kKLo);
@@ -740,7 +779,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
             z[w2][j][rr][nt] = rt[j][rr] * fmaf(acc[w2][j][nt][2 * rr] + acc[w2][j][nt][2 * rr + 1],
                                                 invA[nt], cstA[nt]);
     }
-    // each warp takes one tile, so its streaming state starts here: no rescale
+    // streaming state of the warp: the running maximum moves to mn, earlier
+    // sums are rescaled by alpha (0 on the group's first tile)
+    float alpha[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float mx = kNegInf;
@@ -752,7 +793,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           for (int rr = 0; rr < 2; ++rr) mx = fmaxf(mx, z[w2][j][rr][nt]);
 #pragma unroll
       for (int m = 4; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      m_run[nt] = mx;
+      const float mn = fmaxf(m_run[nt], mx);
+      alpha[nt] = ex2_approx(m_run[nt] - mn);
+      m_run[nt] = mn;
       float ls = 0.f;
 #pragma unroll
       for (int w2 = 0; w2 < CH; ++w2)
@@ -760,10 +803,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
-            z[w2][j][rr][nt] = ex2_approx(z[w2][j][rr][nt] - mx);  // now p
+            z[w2][j][rr][nt] = ex2_approx(z[w2][j][rr][nt] - mn);  // now p
             ls += z[w2][j][rr][nt];
           }
-      l_run[nt] = ls;
+      l_run[nt] = k == 0 ? ls : fmaf(l_run[nt], alpha[nt], ls);
     }
 
     // ---- value side: pd_t = p_t r_t delta_tg as fp16 hi + lo, transposed into
@@ -872,61 +915,87 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
               mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
           }
       }
-      // acc_c = s_c (4 2^-e (O - sum pd) + sum p r lo)
+      // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
       const float4 s0 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8);
       const float4 s1 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8 + 4);
       const float sv[4][2] = {{s0.x, s0.y}, {s0.z, s0.w}, {s1.x, s1.y}, {s1.z, s1.w}};
+      if (k == 0) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int mu = 0; mu < 4; ++mu)
+          for (int mu = 0; mu < 4; ++mu)
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
-            out_acc[sl][mu][rr][nt] = sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]);
-          }
+            for (int rr = 0; rr < 2; ++rr) {
+              const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
+              out_acc[sl][mu][rr][nt] = sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]);
+            }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int mu = 0; mu < 4; ++mu)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
+              out_acc[sl][mu][rr][nt] = fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
+                                             sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]));
+            }
+      }
+    }
+    if (dbuf) {
+      // the group is done with this slot (and with its fragments): refill it
+      // with the group's tile two turns ahead, unless its copy never landed
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");
+      const int nxt = pair + TPS * (k + 2);
+      if (issuer && k + 2 < rounds && nxt < nslot && landed && issue(nxt, slot)) {
+        const int pv = (int)(((k + 2) >> 1) & 1) + 1;
+        if (k & 1) pend1 = pv; else pend0 = pv;
+      }
+      if (issuer && k + 2 < rounds && nxt < nslot && !landed) okf[slot] = 0;
     }
   }
   bad = __syncthreads_or(bad);
-  if (bad)  // let every copy that was issued land before the CTA exits (bounded)
-    for (int kk = 0; kk < nslot; ++kk)
-      if (okf[kk]) mbar_wait(&bar[kk], 0);
+  if (bad && issuer)  // let every copy that was issued land before the CTA exits (bounded)
+  {
+    if (pend0) mbar_wait(&bar[pair], (uint32_t)(pend0 - 1));
+    if (pend1) mbar_wait(&bar[pair + TPS], (uint32_t)(pend1 - 1));
+  }
 
   // ---------------- merge the warps' (m, l, acc) ---------------------------
+  // Every warp stores its own (m, l) per head and its unscaled accumulator
+  // (over the dead records); each output then takes the maximum over the
+  // warps and sums their accumulators rescaled to it.
+  float* vred = reinterpret_cast<float*>(rec);  // [NW][GP][DP], over the dead records
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], m);
     const int h = 4 * nt + q4;
-    if (g8 == 0 && h < GP) {
-      red[warp * 32 + h] = m_run[nt];
-      red[warp * 32 + 8 + h] = l_run[nt];
-    }
-  }
-  __syncthreads();
-  float* vred = reinterpret_cast<float*>(smem);  // [NW][GP][DP], over the dead records
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int h = 4 * nt + q4;
     if (h < GP) {
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
-      const float f = m_run[nt] == kNegInf ? 0.f : exp2f(m_run[nt] - M);  // a warp without a tile
+      if (g8 == 0) {
+        red[warp * 32 + h] = m_run[nt];
+        red[warp * 32 + 8 + h] = l_run[nt];
+      }
 #pragma unroll
       for (int sl = 0; sl < NS; ++sl)
 #pragma unroll
         for (int mu = 0; mu < 4; ++mu)
           *reinterpret_cast<float2*>(vred + (warp * GP + h) * C::DP + 64 * sl + 8 * g8 + 2 * mu) =
-              make_float2(out_acc[sl][mu][0][nt] * f, out_acc[sl][mu][1][nt] * f);
+              make_float2(out_acc[sl][mu][0][nt], out_acc[sl][mu][1][nt]);
     }
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += C::NTHR) {
     const int h = idx / D, c = idx % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) s += vred[(w * GP + h) * C::DP + c];
+    for (int w = 0; w < NW; ++w) {
+      const float mw = red[w * 32 + h];  // -inf: a warp without a tile
+      if (mw != kNegInf) s = fmaf(vred[(w * GP + h) * C::DP + c], ex2_approx(mw - M), s);
+    }
     ws_acc[(part + (int64_t)h * items) * D + c] = bad ? NAN : s;
   }
   if (tid < G) {
@@ -935,7 +1004,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + tid]);
 #pragma unroll
     for (int w = 0; w < NW; ++w)
-      if (red[w * 32 + tid] != kNegInf) L += red[w * 32 + 8 + tid] * exp2f(red[w * 32 + tid] - M);
+      if (red[w * 32 + tid] != kNegInf) L += red[w * 32 + 8 + tid] * ex2_approx(red[w * 32 + tid] - M);
     ws_ml[(part + (int64_t)tid * items) * 2 + 0] = bad ? NAN : M * kLn2D;
     ws_ml[(part + (int64_t)tid * items) * 2 + 1] = bad ? NAN : L;
   }
@@ -1079,17 +1148,18 @@ cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int GP, int NW, int WPT>
+template <int D, int GP, int NW, int WPT, bool MR>
 cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
   using C = DC<D, GP, NW, WPT>;
+  constexpr int kMaxSmem = C::smem_bytes(MR ? 2 * C::TPS : C::TPS) + 1024;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, NW, WPT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM + 1024);
+    e = cudaFuncSetAttribute(decode_split_kernel<D, GP, NW, WPT, MR>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
@@ -1098,24 +1168,30 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
   if (e != cudaSuccess) return e;
   const unsigned fl = launch_flags();
   const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
-  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::SMEM + 1024, st);
-  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW, WPT>, a.q, a.tiles, a.tile_table,
+  const int slots = MR && p.rounds > 1 ? 2 * C::TPS : C::TPS;
+  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::smem_bytes(slots) + 1024, st);
+  return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW, WPT, MR>, a.q, a.tiles, a.tile_table,
                             a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
-                            a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, a.scale,
-                            ws_ml, ws_acc, prefetch, tmap);
+                            a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, p.rounds,
+                            a.scale, ws_ml, ws_acc, prefetch, tmap);
 }
 
 template <int D, int GP>
 cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  // (tiles per item, warps per tile)
-  const int key = 10 * p.tiles_per_item + p.warps_per_tile;
+  // (tiles per round, warps per tile); several rounds only with four warps
+  const int key = 10 * p.tiles_per_round + p.warps_per_tile;
+  if (p.rounds > 1) {
+    if (key == 22) return launch_split_t<D, GP, 4, 2, true>(p, a, ws_ml, ws_acc, st);
+    if (key == 14) return launch_split_t<D, GP, 4, 4, true>(p, a, ws_ml, ws_acc, st);
+    return cudaErrorInvalidValue;
+  }
   switch (key) {
-    case 22: return launch_split_t<D, GP, 4, 2>(p, a, ws_ml, ws_acc, st);
-    case 14: return launch_split_t<D, GP, 4, 4>(p, a, ws_ml, ws_acc, st);
-    case 24: return launch_split_t<D, GP, 8, 4>(p, a, ws_ml, ws_acc, st);
+    case 22: return launch_split_t<D, GP, 4, 2, false>(p, a, ws_ml, ws_acc, st);
+    case 14: return launch_split_t<D, GP, 4, 4, false>(p, a, ws_ml, ws_acc, st);
+    case 24: return launch_split_t<D, GP, 8, 4, false>(p, a, ws_ml, ws_acc, st);
     case 42:
-      if constexpr (D <= 128) return launch_split_t<D, GP, 8, 2>(p, a, ws_ml, ws_acc, st);
+      if constexpr (D <= 128) return launch_split_t<D, GP, 8, 2, false>(p, a, ws_ml, ws_acc, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
@@ -1156,19 +1232,33 @@ int sm_count() {
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-  // head_dim <= 128: a warp pair per tile, 2 tiles per CTA, or 4 (eight warps)
-  // once the grid has at least 4 tiles per SM, which halves the partials the
-  // combine reads and the per-CTA set-up. head_dim 256: four warps per tile
-  // (32 tokens each) and one tile per CTA, whose record is twice as large;
-  // the extra warps per SM hide more of each warp's mma.sync / shuffle chain
-  // (a warp pair per tile leaves 12 warps per SM there).
+  // head_dim <= 128: a warp pair per tile, 2 tiles per CTA at a time, or 4
+  // (eight warps) once the grid has at least 4 tiles per SM, which halves the
+  // partials the combine reads and the per-CTA set-up. head_dim 256: four
+  // warps per tile (32 tokens each) and one tile per CTA at a time, whose
+  // record is twice as large; the extra warps per SM hide more of each warp's
+  // mma.sync / shuffle chain. When there are many more tiles than the SMs hold
+  // at once, each warp group takes several tiles in turn (rounds), its next
+  // record streaming into a second slot while it works on the current one:
+  // the query rotation, the merge of the warps and the partial written for
+  // the combine are then paid once per item instead of once per tile.
   const int64_t total = (int64_t)B * Hkv * max_tiles;
+  const int64_t per_sm = total / sm_count();
   const int wpt = D <= 128 ? 2 : 4;
-  const int tps = D <= 128 ? ((total >= 4LL * sm_count()) ? 4 : 2) : 1;
+  int tps, rounds = 1;
+  if (D <= 128) {
+    tps = per_sm > 8 ? 2 : total >= 4LL * sm_count() ? 4 : 2;
+    if (per_sm > 8) rounds = (int)std::min<int64_t>(8, std::max<int64_t>(2, per_sm / 6));
+  } else {
+    tps = 1;
+    if (per_sm >= 12) rounds = (int)std::min<int64_t>(8, per_sm / 3);
+  }
   const int nw = wpt * tps;
-  p->tiles_per_item = tps;
+  p->tiles_per_round = tps;
+  p->rounds = rounds;
+  p->tiles_per_item = tps * rounds;
   p->warps_per_tile = wpt;
-  p->tile_items = max_tiles > 0 ? (max_tiles + tps - 1) / tps : 0;
+  p->tile_items = max_tiles > 0 ? (max_tiles + p->tiles_per_item - 1) / p->tiles_per_item : 0;
   // window rows per warp and per item, as DC<D, GP, NW, WPT>::WCH and its NW warps
   const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
   const int w0 = (tps * rb) / (nw * 2 * D * 4);

@@ -91,9 +91,11 @@ cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new,
                           cudaStream_t st);
 
 struct DecodePlan {
-  int tiles_per_item;  // packed tiles handled by one split CTA
-  int warps_per_tile;  // 2 or 4 (64 or 32 tokens per warp)
-  int tile_items;      // ceil(max_tiles / tiles_per_item)
+  int tiles_per_round;  // packed tiles a split CTA works on at once (one per warp group)
+  int rounds;           // tiles each warp group takes in turn (records double-buffered when > 1)
+  int tiles_per_item;   // tiles_per_round * rounds: packed tiles handled by one split CTA
+  int warps_per_tile;   // 2 or 4 (64 or 32 tokens per warp)
+  int tile_items;       // ceil(max_tiles / tiles_per_item)
   int win_items;       // window items: ceil(win_capacity / window rows per item)
   int items;           // tile_items + win_items
   int g_pad;           // query heads per KV head rounded up to 1, 2, 4 or 8

@@ -104,3 +104,18 @@ def test_four_tiles_per_item_path(workload, Hq, Hkv, D, ctx):
     c = Cache(workload, 12, [ctx], Hkv=Hkv, D=D)
     assert Hkv * c.max_tiles >= 4 * 152
     _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 3)])
+
+
+@pytest.mark.parametrize("workload,Hq,Hkv,D,ctx", [("qwen3_8b_decode", 8, 1, 128, 128 * 1400 + 9),
+                                                  ("qwen3_8b_decode", 16, 2, 128, 128 * 1330 + 100),
+                                                  ("batched_d256_decode", 16, 4, 256, 128 * 460 + 77)])
+def test_multi_round_items(workload, Hq, Hkv, D, ctx):
+    """Grids with many more tiles than the SMs hold at once take the split
+    kernel in which each warp group works through several tiles in turn while
+    its next record is copied into a second slot (head_dim 128: more than 8
+    tiles per SM; head_dim 256: at least 12). Tile counts leave the last item
+    and the last round of some groups partly empty."""
+    c = Cache(workload, 13, [ctx], Hkv=Hkv, D=D)
+    per_sm = Hkv * c.max_tiles // 152
+    assert per_sm > (8 if D == 128 else 11)
+    _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])
