@@ -211,52 +211,100 @@ int orc_quantize_tensor(const float* x, int64_t row_stride, int D, int iters, in
 /* ---------------------------------------------------------------------------
  * c4: packed record (layout of include/kvarn.h, restated here on purpose so
  * that the oracle does not include the library's header).
+ * Scale fields are stored as IEEE binary32 (sw = 4 bytes, the default
+ * layout) or as IEEE binary16 (sw = 2: the f16-scale layout that
+ * SharpInference issue #433, item 3 names as a later saving). The codes are
+ * the same in both: only the stored precision of the scales differs.
  */
 typedef struct {
   int64_t bytes, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s;
-  int gv;
+  int gv, sw;
 } orc_layout;
 
-static orc_layout orc_record_layout(int D) {
+static orc_layout orc_record_layout(int D, int sw) {
   orc_layout L;
   L.gv = D / (D < 128 ? D : 128);
+  L.sw = sw;
   L.k_codes = 0;
   L.v_codes = L.k_codes + (int64_t)D * (ORC_T / 2);     /* 4-bit K codes        */
   L.k_delta = L.v_codes + (int64_t)ORC_T * (D / 4);     /* 2-bit V codes        */
-  L.k_lo = L.k_delta + 4LL * D;
-  L.k_s = L.k_lo + 4LL * D;
-  L.k_r = L.k_s + 4LL * D;
-  L.v_delta = L.k_r + 4LL * ORC_T;
-  L.v_lo = L.v_delta + 4LL * ORC_T * L.gv;
-  L.v_r = L.v_lo + 4LL * ORC_T * L.gv;
-  L.v_s = L.v_r + 4LL * ORC_T;
-  L.bytes = L.v_s + 4LL * D;
+  L.k_lo = L.k_delta + (int64_t)sw * D;
+  L.k_s = L.k_lo + (int64_t)sw * D;
+  L.k_r = L.k_s + (int64_t)sw * D;
+  L.v_delta = L.k_r + (int64_t)sw * ORC_T;
+  L.v_lo = L.v_delta + (int64_t)sw * ORC_T * L.gv;
+  L.v_r = L.v_lo + (int64_t)sw * ORC_T * L.gv;
+  L.v_s = L.v_r + (int64_t)sw * ORC_T;
+  L.bytes = L.v_s + (int64_t)sw * D;
   return L;
 }
 
-int64_t orc_record_bytes(int D) {
-  if (!orc_pow2_dim(D) || D < 4) return -3;
-  return orc_record_layout(D).bytes;
+static int orc_sw_ok(int sw) { return sw == 4 || sw == 2; }
+
+int64_t orc_record_bytes_sw(int D, int sw) {
+  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
+  return orc_record_layout(D, sw).bytes;
+}
+int64_t orc_record_bytes(int D) { return orc_record_bytes_sw(D, 4); }
+
+/* IEEE binary16 encoding of v, rounded to nearest with ties to even, from the
+ * format's definition: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; subnormals have the quantum 2^-24, a normal number 2^E (1 + f/1024)
+ * the quantum 2^(E-10); results above 65504 after rounding are infinite. */
+uint16_t orc_f64_to_f16_bits(double v) {
+  if (isnan(v)) return 0x7E00;
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return (uint16_t)(sign | 0x7C00);
+  int e;
+  frexp(a, &e);                  /* a = m 2^e, m in [0.5, 1): a = 1.f 2^(e-1) */
+  int E = e - 1;
+  if (E < -14) E = -14;          /* subnormal range shares the quantum 2^-24 */
+  const double ulp = ldexp(1.0, E - 10);
+  const double n = rint(a / ulp); /* exact scaling; ties to even (default mode) */
+  const double bits = ldexp((double)(E + 14), 10) + n;
+  if (bits >= 31744.0) return (uint16_t)(sign | 0x7C00); /* 0x7C00: overflow */
+  return (uint16_t)(sign | (uint16_t)bits);
 }
 
-static void orc_put_f32(uint8_t* dst, double v) {
-  float f = (float)v;
-  memcpy(dst, &f, 4);
+double orc_f16_bits_to_f64(uint16_t h) {
+  const int sign = h >> 15, ex = (h >> 10) & 0x1F, fr = h & 0x3FF;
+  double m;
+  if (ex == 0x1F) m = fr ? NAN : INFINITY;
+  else if (ex == 0) m = ldexp((double)fr, -24);
+  else m = ldexp(1024.0 + fr, ex - 25);
+  return sign ? -m : m;
 }
-static double orc_get_f32(const uint8_t* src) {
-  float f;
-  memcpy(&f, src, 4);
-  return (double)f;
+
+static void orc_put_scale(uint8_t* dst, double v, int sw) {
+  if (sw == 4) {
+    float f = (float)v;
+    memcpy(dst, &f, 4);
+  } else {
+    const uint16_t h = orc_f64_to_f16_bits(v);
+    memcpy(dst, &h, 2);
+  }
+}
+static double orc_get_scale(const uint8_t* src, int sw) {
+  if (sw == 4) {
+    float f;
+    memcpy(&f, src, 4);
+    return (double)f;
+  }
+  uint16_t h;
+  memcpy(&h, src, 2);
+  return orc_f16_bits_to_f64(h);
 }
 
 /* Writes the record from unpacked codes ([128][D], one per byte) and fp64
- * scales, which are stored rounded to fp32. */
-int orc_pack_record(int D, const uint8_t* k_codes, const uint8_t* v_codes,
-                    const double* k_delta, const double* k_lo, const double* k_s,
-                    const double* k_r, const double* v_delta, const double* v_lo,
-                    const double* v_r, const double* v_s, uint8_t* rec) {
-  if (!orc_pow2_dim(D) || D < 4) return -3;
-  const orc_layout L = orc_record_layout(D);
+ * scales, which are stored rounded to the layout's scale format. */
+int orc_pack_record_sw(int D, int sw, const uint8_t* k_codes, const uint8_t* v_codes,
+                       const double* k_delta, const double* k_lo, const double* k_s,
+                       const double* k_r, const double* v_delta, const double* v_lo,
+                       const double* v_r, const double* v_s, uint8_t* rec) {
+  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
+  const orc_layout L = orc_record_layout(D, sw);
   memset(rec, 0, (size_t)L.bytes);
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t) {
@@ -269,28 +317,35 @@ int orc_pack_record(int D, const uint8_t* k_codes, const uint8_t* v_codes,
       rec[L.v_codes + (int64_t)t * (D / 4) + c / 4] |= (uint8_t)(code << (2 * (c % 4)));
     }
   for (int c = 0; c < D; ++c) {
-    orc_put_f32(rec + L.k_delta + 4LL * c, k_delta[c]);
-    orc_put_f32(rec + L.k_lo + 4LL * c, k_lo[c]);
-    orc_put_f32(rec + L.k_s + 4LL * c, k_s[c]);
-    orc_put_f32(rec + L.v_s + 4LL * c, v_s[c]);
+    orc_put_scale(rec + L.k_delta + (int64_t)sw * c, k_delta[c], sw);
+    orc_put_scale(rec + L.k_lo + (int64_t)sw * c, k_lo[c], sw);
+    orc_put_scale(rec + L.k_s + (int64_t)sw * c, k_s[c], sw);
+    orc_put_scale(rec + L.v_s + (int64_t)sw * c, v_s[c], sw);
   }
   for (int t = 0; t < ORC_T; ++t) {
-    orc_put_f32(rec + L.k_r + 4LL * t, k_r[t]);
-    orc_put_f32(rec + L.v_r + 4LL * t, v_r[t]);
+    orc_put_scale(rec + L.k_r + (int64_t)sw * t, k_r[t], sw);
+    orc_put_scale(rec + L.v_r + (int64_t)sw * t, v_r[t], sw);
     for (int g = 0; g < L.gv; ++g) {
-      orc_put_f32(rec + L.v_delta + 4LL * (t * L.gv + g), v_delta[t * L.gv + g]);
-      orc_put_f32(rec + L.v_lo + 4LL * (t * L.gv + g), v_lo[t * L.gv + g]);
+      orc_put_scale(rec + L.v_delta + (int64_t)sw * (t * L.gv + g), v_delta[t * L.gv + g], sw);
+      orc_put_scale(rec + L.v_lo + (int64_t)sw * (t * L.gv + g), v_lo[t * L.gv + g], sw);
     }
   }
   return 0;
 }
+int orc_pack_record(int D, const uint8_t* k_codes, const uint8_t* v_codes,
+                    const double* k_delta, const double* k_lo, const double* k_s,
+                    const double* k_r, const double* v_delta, const double* v_lo,
+                    const double* v_r, const double* v_s, uint8_t* rec) {
+  return orc_pack_record_sw(D, 4, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta, v_lo,
+                            v_r, v_s, rec);
+}
 
-/* Inverse of orc_pack_record: unpacked codes and the stored fp32 scales. */
-int orc_unpack_record(int D, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
-                      double* k_delta, double* k_lo, double* k_s, double* k_r,
-                      double* v_delta, double* v_lo, double* v_r, double* v_s) {
-  if (!orc_pow2_dim(D) || D < 4) return -3;
-  const orc_layout L = orc_record_layout(D);
+/* Inverse of orc_pack_record_sw: unpacked codes and the stored scales. */
+int orc_unpack_record_sw(int D, int sw, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
+                         double* k_delta, double* k_lo, double* k_s, double* k_r,
+                         double* v_delta, double* v_lo, double* v_r, double* v_s) {
+  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
+  const orc_layout L = orc_record_layout(D, sw);
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t)
       k_codes[(int64_t)t * D + c] =
@@ -300,29 +355,36 @@ int orc_unpack_record(int D, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_co
       v_codes[(int64_t)t * D + c] =
           (rec[L.v_codes + (int64_t)t * (D / 4) + c / 4] >> (2 * (c % 4))) & 0x3;
   for (int c = 0; c < D; ++c) {
-    k_delta[c] = orc_get_f32(rec + L.k_delta + 4LL * c);
-    k_lo[c] = orc_get_f32(rec + L.k_lo + 4LL * c);
-    k_s[c] = orc_get_f32(rec + L.k_s + 4LL * c);
-    v_s[c] = orc_get_f32(rec + L.v_s + 4LL * c);
+    k_delta[c] = orc_get_scale(rec + L.k_delta + (int64_t)sw * c, sw);
+    k_lo[c] = orc_get_scale(rec + L.k_lo + (int64_t)sw * c, sw);
+    k_s[c] = orc_get_scale(rec + L.k_s + (int64_t)sw * c, sw);
+    v_s[c] = orc_get_scale(rec + L.v_s + (int64_t)sw * c, sw);
   }
   for (int t = 0; t < ORC_T; ++t) {
-    k_r[t] = orc_get_f32(rec + L.k_r + 4LL * t);
-    v_r[t] = orc_get_f32(rec + L.v_r + 4LL * t);
+    k_r[t] = orc_get_scale(rec + L.k_r + (int64_t)sw * t, sw);
+    v_r[t] = orc_get_scale(rec + L.v_r + (int64_t)sw * t, sw);
     for (int g = 0; g < L.gv; ++g) {
-      v_delta[t * L.gv + g] = orc_get_f32(rec + L.v_delta + 4LL * (t * L.gv + g));
-      v_lo[t * L.gv + g] = orc_get_f32(rec + L.v_lo + 4LL * (t * L.gv + g));
+      v_delta[t * L.gv + g] = orc_get_scale(rec + L.v_delta + (int64_t)sw * (t * L.gv + g), sw);
+      v_lo[t * L.gv + g] = orc_get_scale(rec + L.v_lo + (int64_t)sw * (t * L.gv + g), sw);
     }
   }
   return 0;
 }
+int orc_unpack_record(int D, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
+                      double* k_delta, double* k_lo, double* k_s, double* k_r,
+                      double* v_delta, double* v_lo, double* v_r, double* v_s) {
+  return orc_unpack_record_sw(D, 4, rec, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta,
+                              v_lo, v_r, v_s);
+}
 
 /* Full compression of one (tile, KV head) unit into a record; also returns the
- * fp64 scales and the pre-rounding values for the parity checks. */
-int orc_compress_unit(const float* k, const float* v, int64_t row_stride, int D, int iters,
-                      uint8_t* rec, double* k_s, double* k_r, double* k_delta, double* k_lo,
-                      double* k_vpre, double* v_s, double* v_r, double* v_delta,
-                      double* v_lo, double* v_vpre) {
-  if (!orc_pow2_dim(D) || D < 4) return -3;
+ * fp64 scales and the pre-rounding values for the parity checks. The codes
+ * come from the fp64 scales whatever the stored scale format. */
+int orc_compress_unit_sw(const float* k, const float* v, int64_t row_stride, int D, int iters,
+                         int sw, uint8_t* rec, double* k_s, double* k_r, double* k_delta,
+                         double* k_lo, double* k_vpre, double* v_s, double* v_r,
+                         double* v_delta, double* v_lo, double* v_vpre) {
+  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
   uint8_t* kc = (uint8_t*)malloc((size_t)ORC_T * D);
   uint8_t* vc = (uint8_t*)malloc((size_t)ORC_T * D);
   if (!kc || !vc) { free(kc); free(vc); return -7; }
@@ -332,19 +394,28 @@ int orc_compress_unit(const float* k, const float* v, int64_t row_stride, int D,
     rc = orc_quantize_tensor(v, row_stride, D, iters, 0, 2, v_s, v_r, v_delta, v_lo, vc,
                              v_vpre);
   if (rc == 0)
-    rc = orc_pack_record(D, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s, rec);
+    rc = orc_pack_record_sw(D, sw, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s,
+                            rec);
   free(kc); free(vc);
   return rc;
+}
+int orc_compress_unit(const float* k, const float* v, int64_t row_stride, int D, int iters,
+                      uint8_t* rec, double* k_s, double* k_r, double* k_delta, double* k_lo,
+                      double* k_vpre, double* v_s, double* v_r, double* v_delta,
+                      double* v_lo, double* v_vpre) {
+  return orc_compress_unit_sw(k, v, row_stride, D, iters, 4, rec, k_s, k_r, k_delta, k_lo,
+                              k_vpre, v_s, v_r, v_delta, v_lo, v_vpre);
 }
 
 /* ---------------------------------------------------------------------------
  * c5: reconstruction of one record to unrotated K and V rows ([128][D] each).
  * K~[t][c] = r_t s_c (delta_c code + lo_c), V~[t][c] = r_t s_c (delta_tg code
- * + lo_tg), then each row is multiplied by H (H is its own inverse).
+ * + lo_tg) with the stored scales, then each row is multiplied by H (H is its
+ * own inverse).
  */
-int orc_dequant_record(int D, const uint8_t* rec, double* k_out, double* v_out) {
-  if (!orc_pow2_dim(D) || D < 4) return -3;
-  const orc_layout L = orc_record_layout(D);
+int orc_dequant_record_sw(int D, int sw, const uint8_t* rec, double* k_out, double* v_out) {
+  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
+  const orc_layout L = orc_record_layout(D, sw);
   const int T = ORC_T;
   uint8_t* kc = (uint8_t*)malloc((size_t)T * D);
   uint8_t* vc = (uint8_t*)malloc((size_t)T * D);
@@ -357,7 +428,7 @@ int orc_dequant_record(int D, const uint8_t* rec, double* k_out, double* v_out) 
   }
   double *k_delta = buf, *k_lo = k_delta + D, *k_s = k_lo + D, *v_s = k_s + D;
   double *k_r = v_s + D, *v_r = k_r + T, *v_delta = v_r + T, *v_lo = v_delta + T * L.gv;
-  orc_unpack_record(D, rec, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s);
+  orc_unpack_record_sw(D, sw, rec, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s);
   const int gw = D < 128 ? D : 128;
   for (int t = 0; t < T; ++t)
     for (int c = 0; c < D; ++c) {
@@ -370,6 +441,9 @@ int orc_dequant_record(int D, const uint8_t* rec, double* k_out, double* v_out) 
   orc_wht_rows(vt, v_out, T, D);
   free(kc); free(vc); free(buf); free(kt); free(vt);
   return 0;
+}
+int orc_dequant_record(int D, const uint8_t* rec, double* k_out, double* v_out) {
+  return orc_dequant_record_sw(D, 4, rec, k_out, v_out);
 }
 
 /* ---------------------------------------------------------------------------

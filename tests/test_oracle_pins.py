@@ -369,3 +369,82 @@ def test_prefill_chunk_of_one_equals_decode(oracle):
                                            win_v, 0, sm.win_len, 1 / 8)
             for h in range(Hq):
                 np.testing.assert_allclose(pre[(0, h)], dec[(0, h)], rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------- c4 variant: f16-scale layout
+def test_f16_rounding_matches_numpy(oracle):
+    """The oracle's binary16 encoder (written from the format's definition)
+    against numpy's float16 conversion, an independent implementation of the
+    same IEEE rounding: random magnitudes over the whole range, exact ties
+    between neighbours (ties go to the even fraction), subnormals, the
+    overflow threshold 65520, and every one of the 65536 bit patterns decoded."""
+    rng = np.random.default_rng(16)
+    mags = np.ldexp(rng.random(4000) + 0.5, rng.integers(-30, 18, 4000))
+    vals = np.concatenate([mags, -mags])
+    h = np.arange(0, 0x7C00, 37, dtype=np.uint16).view(np.float16).astype(np.float64)
+    ties = (h[:-1] + np.nextafter(h[:-1].astype(np.float16), np.float16(np.inf)).astype(np.float64)) / 2
+    edge = np.array([0.0, -0.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -25, 2.0 ** -14, 65504.0,
+                     65519.999, 65520.0, 1e9, -1e9, np.inf, -np.inf])
+    with np.errstate(over="ignore"):
+        for v in np.concatenate([vals, ties, edge]):
+            want = int(np.array(v).astype(np.float16).view(np.uint16))
+            assert oracle.f16_bits(v) == want, (v, hex(oracle.f16_bits(v)), hex(want))
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_value(int(b)) for b in allbits])
+    fin = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[fin], ref[fin])
+    assert np.isnan(got[~fin]).all()
+
+
+@pytest.mark.parametrize("D,size", [(64, 7680), (128, 14336), (256, 28160)])
+def test_f16_record_size(oracle, D, size):
+    """Codes as in the fp32 layout (96 D bytes), every scale field 2 bytes:
+    96 D + 2 (4 D + 256 + 256 Gv); all multiples of 128."""
+    assert oracle.record_bytes(D, 16) == size and size % 128 == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_f16_pack_unpack_roundtrip(oracle, D):
+    rng = np.random.default_rng(D + 16)
+    gv = D // min(D, 128)
+    f16 = lambda n: rng.standard_normal(n).astype(np.float16).astype(np.float64)
+    args = dict(k_codes=rng.integers(0, 16, (128, D)).astype(np.uint8),
+                v_codes=rng.integers(0, 4, (128, D)).astype(np.uint8),
+                k_delta=f16(D), k_lo=f16(D), k_s=f16(D), k_r=f16(128),
+                v_delta=f16(128 * gv), v_lo=f16(128 * gv), v_r=f16(128), v_s=f16(D))
+    rec = oracle.pack_record(D, scale_bits=16, **args)
+    back = oracle.unpack_record(rec, D, scale_bits=16)
+    for name, val in args.items():
+        np.testing.assert_array_equal(back[name], val, err_msg=name)
+    # the scale fields sit right after the codes, low byte first
+    assert int(rec[96 * D]) | (int(rec[96 * D + 1]) << 8) == oracle.f16_bits(args["k_delta"][0])
+
+
+@pytest.mark.parametrize("workload,D", [("qwen3_8b_decode", 128), ("batched_d256_decode", 256)])
+def test_f16_layout_keeps_codes_and_rounds_scales(oracle, workload, D):
+    """The f16-scale record holds the fp32 layout's codes and every scale
+    rounded once from fp64 to binary16; dequantisation uses the stored
+    values (checked against the same algebra with the rounded scales and
+    scipy's Sylvester matrix)."""
+    from scipy.linalg import hadamard
+    k, v = synth.kv_stream(workload, 0, 1, 128, D)
+    a = oracle.compress_unit(k, v)
+    b = oracle.compress_unit(k, v, scale_bits=16)
+    ua = oracle.unpack_record(a["record"], D)
+    ub = oracle.unpack_record(b["record"], D, scale_bits=16)
+    for t in ("k_codes", "v_codes"):
+        np.testing.assert_array_equal(ua[t], ub[t])
+    for name in ("k_delta", "k_lo", "k_s", "k_r", "v_delta", "v_lo", "v_r", "v_s"):
+        want = np.asarray(b[name], np.float64).astype(np.float16).astype(np.float64)
+        np.testing.assert_array_equal(ub[name], want, err_msg=name)
+    kk, vv = oracle.dequant_record(b["record"], D, scale_bits=16)
+    H = hadamard(D) / np.sqrt(D)
+    gv = D // min(D, 128)
+    gidx = np.arange(D) // min(D, 128)
+    kt = ub["k_r"][:, None] * ub["k_s"][None, :] * (ub["k_delta"][None, :] * ub["k_codes"] + ub["k_lo"][None, :])
+    vd = ub["v_delta"].reshape(128, gv)[:, gidx]
+    vl = ub["v_lo"].reshape(128, gv)[:, gidx]
+    vt = ub["v_r"][:, None] * ub["v_s"][None, :] * (vd * ub["v_codes"] + vl)
+    np.testing.assert_allclose(kk, kt @ H, rtol=0, atol=1e-12 * np.abs(kt).max())
+    np.testing.assert_allclose(vv, vt @ H, rtol=0, atol=1e-12 * np.abs(vt).max())
