@@ -97,3 +97,49 @@ def test_compress_is_deterministic_and_schedule_independent():
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
     assert np.array_equal(a[3], c[0])
+
+
+def test_compress_bulk_launch_sampled():
+    """The benchmarked bulk launch: 256 tiles x 8 KV heads of 32k-token
+    8B-like caches (2048 units, 256 MiB of input) in one call; a seeded sample
+    of the units is checked against the oracle."""
+    D, n_tiles, n_heads = 128, 256, 8
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 99, n_heads, 128 * n_tiles, D)
+    k_rows, v_rows = ks.reshape(-1, D), vs.reshape(-1, D)
+    units = [128 * i for i in range(n_heads * n_tiles)]
+    lay = kvarn.layout(D)
+    rb = lay.record_bytes
+    tiles = torch.zeros(len(units) * rb, dtype=torch.uint8, device=DEV)
+    kvarn.compress_tile(torch.from_numpy(k_rows).to(DEV), torch.from_numpy(v_rows).to(DEV),
+                        torch.tensor(units, dtype=torch.int64, device=DEV), tiles,
+                        torch.arange(len(units), dtype=torch.int64, device=DEV) * rb, lay)
+    host = tiles.cpu().numpy()
+    pick = np.random.default_rng(2048).choice(len(units), 12, replace=False)
+    for i in sorted(pick.tolist()) + [0, len(units) - 1]:
+        u = units[i]
+        compare_record(host[i * rb:(i + 1) * rb],
+                       oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128]), D)
+
+
+@pytest.mark.parametrize("workload,D,n_heads,n_tiles", [("qwen3_8b_decode", 128, 2, 4),
+                                                       ("batched_d256_decode", 256, 2, 3),
+                                                       ("single_tile", 64, 1, 2)])
+def test_compress_f16_scales_matches_oracle(workload, D, n_heads, n_tiles):
+    """The f16-scale layout: the same codes, every scale field binary16."""
+    from tests.kvarn_helpers import compare_record_f16
+    ks, vs = synth.kv_layer(workload, 4, n_heads, 128 * n_tiles, D)
+    k_rows, v_rows = ks.reshape(-1, D), vs.reshape(-1, D)
+    units = [128 * i for i in range(n_heads * n_tiles)]
+    lay = kvarn.layout(D, scale_bits=16)
+    rb = lay.record_bytes
+    assert rb == oracle.record_bytes(D, 16)
+    tiles = torch.full((len(units) * rb,), 0xAB, dtype=torch.uint8, device=DEV)
+    kvarn.compress_tile(torch.from_numpy(k_rows).to(DEV), torch.from_numpy(v_rows).to(DEV),
+                        torch.tensor(units, dtype=torch.int64, device=DEV), tiles,
+                        torch.arange(len(units), dtype=torch.int64, device=DEV) * rb, lay)
+    host = tiles.cpu().numpy()
+    flips = 0
+    for i, u in enumerate(units):
+        ref = oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128], scale_bits=16)
+        flips += compare_record_f16(host[i * rb:(i + 1) * rb], ref, D)["scale_flips"]
+    print(f"{workload} D{D} f16 scales: {flips} binary16 rounding-midpoint flips")

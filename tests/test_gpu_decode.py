@@ -119,3 +119,67 @@ def test_multi_round_items(workload, Hq, Hkv, D, ctx):
     per_sm = Hkv * c.max_tiles // 152
     assert per_sm > (8 if D == 128 else 11)
     _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])
+
+
+def test_qwen3_8b_like_32k_sampled_heads():
+    """The 32k point of the 8B-like sweep (32q/8kv, 257 tiles per KV head):
+    the multi-round split kernel on one GB300."""
+    c = Cache("qwen3_8b_decode", 3, [32768 + 77], Hkv=8, D=128)
+    _check(c, Hq=32, heads=[(0, 0), (0, 11), (0, 29)])
+
+
+def test_batched_d256_full_config_sampled():
+    """The benchmarked batched decode: 32 sequences with contexts uniform in
+    [8192, 32768] (the same seeded draw), 16q/4kv, head_dim 256. Every
+    sequence's tiles repeat a pool of 64 compressed tiles per KV head (as in
+    the benchmark); sampled (sequence, head) outputs against the oracle."""
+    import oracle
+    B, Hq, Hkv, D, cap, pool_tiles = 32, 16, 4, 256, 128, 64
+    ctxs = synth.uniform_ints(4242, 8192, 32768, B)
+    ntl, wlen = ctxs // 128, ctxs % 128
+    mt = int(ntl.max()) + 1
+    lay = kvarn.layout(D)
+    rb = lay.record_bytes
+    ks, vs = synth.kv_layer("batched_d256_decode", 0, Hkv, 128 * pool_tiles + cap, D)
+    pool = torch.zeros(Hkv * pool_tiles * rb, dtype=torch.uint8, device=DEV)
+    src = np.array([h * (128 * pool_tiles + cap) + 128 * t for h in range(Hkv) for t in range(pool_tiles)])
+    kvarn.compress_tile(torch.from_numpy(ks.reshape(-1, D)).to(DEV), torch.from_numpy(vs.reshape(-1, D)).to(DEV),
+                        torch.from_numpy(src.astype(np.int64)).to(DEV), pool,
+                        torch.arange(Hkv * pool_tiles, dtype=torch.int64, device=DEV) * rb, lay)
+    table = ((np.arange(Hkv)[None, :, None] * pool_tiles + (np.arange(mt)[None, None, :] % pool_tiles))
+             * rb * np.ones((B, 1, 1), np.int64)).astype(np.int64)
+    win_k = np.broadcast_to(ks[None, :, 128 * pool_tiles:], (B, Hkv, cap, D)).copy()
+    win_v = np.broadcast_to(vs[None, :, 128 * pool_tiles:], (B, Hkv, cap, D)).copy()
+    q = synth.queries("batched_d256_decode", 0, (B, Hq, D))
+    out = kvarn.decode_attention(torch.from_numpy(q).to(DEV), pool, torch.from_numpy(table).to(DEV),
+                                 torch.from_numpy(ntl.astype(np.int32)).to(DEV),
+                                 torch.from_numpy(win_k).to(DEV), torch.from_numpy(win_v).to(DEV),
+                                 torch.zeros(B, dtype=torch.int32, device=DEV),
+                                 torch.from_numpy(wlen.astype(np.int32)).to(DEV), lay).cpu().numpy()
+    heads = [(b, h) for b in (0, 7, 19, 31) for h in (0, 9, 15)]
+    ref = oracle.decode_attention(q, pool.cpu().numpy(), table, [int(x) for x in ntl], win_k, win_v,
+                                  [0] * B, [int(x) for x in wlen], D ** -0.5, heads=heads)
+    for (b, h), r in ref.items():
+        e = rel_l2(out[b, h], r)
+        assert e <= ATTN_RTOL, f"(b={b}, h={h}) rel-L2 {e:.3e}"
+
+
+@pytest.mark.parametrize("workload,ctxs,Hq,Hkv,D", [("single_tile", [128 + 17], 1, 1, 128),
+                                                   ("qwen3_8b_decode", [16384 + 40], 32, 8, 128),
+                                                   ("qwen3_8b_decode", [600, 1000], 8, 1, 128),
+                                                   ("batched_d256_decode", [900, 128 * 5 + 3], 16, 4, 256),
+                                                   ("single_tile", [128 * 3 + 50], 4, 2, 64)])
+def test_f16_scale_records(workload, ctxs, Hq, Hkv, D):
+    """Decode over records of the f16-scale layout (binary16 scale fields,
+    14,336-byte records at head_dim 128): the oracle dequantises the same
+    records with the stored binary16 values."""
+    c = Cache(workload, 14, ctxs, Hkv=Hkv, D=D, scale_bits=16)
+    assert c.rb == 96 * D + 2 * (4 * D + 256 + 256 * (D // min(D, 128)))
+    heads = [(b, h) for b in range(len(ctxs)) for h in range(0, Hq, max(1, Hq // 4))]
+    _check(c, Hq=Hq, heads=heads)
+
+
+def test_f16_scale_records_multi_round():
+    """The multi-round split kernel (more than 8 tiles per SM) on f16-scale records."""
+    c = Cache("qwen3_8b_decode", 15, [128 * 1400 + 9], Hkv=1, D=128, scale_bits=16)
+    _check(c, Hq=8, heads=[(0, h) for h in range(0, 8, 3)])
