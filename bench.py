@@ -280,8 +280,9 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
 
 def run_decode_sweeps(dev, lay, peaks, peak_kind):
     """Decode split throughput beyond the headline configuration: the 8B-like
-    model at 4k and 32k context (36 layers of distinct caches, split launches
-    back to back as in the headline roofline), and batched decode with large
+    model at 4k and 32k context, and at 16k on records of the f16-scale layout
+    (36 layers of distinct caches, split launches back to back as in the
+    headline roofline), and batched decode with large
     heads (32 ragged sequences with contexts uniform in [8k, 32k], 16q/4kv,
     head_dim 256; one layer's cache is 0.6 GB), timed as back-to-back split
     launches and as decode steps (split + combine) with a concurrent compress
@@ -311,10 +312,11 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / (reps * n_launch)
 
-    # ---- 8B-like decode at 4k and 32k ------------------------------------------
-    for ctx in (4096, 32768):
+    # ---- 8B-like decode at 4k and 32k, and at 16k on f16-scale records --------
+    for ctx, sb in ((4096, 32), (32768, 32), (16384, 16)):
+        lay_s = lay if sb == 32 else kvarn.layout(D, scale_bits=sb)
         n0, w0, cap = ctx // 128, 64, 128
-        rb = lay.record_bytes
+        rb = lay_s.record_bytes
         max_tiles = n0 + 1
         tiles = torch.empty(LAYERS * HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
         table = torch.empty(LAYERS, 1, HKV, max_tiles, dtype=torch.int64, device=dev)
@@ -334,7 +336,7 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
             table[l, 0] = torch.from_numpy(tab.astype(np.int64))
             kd, vd, kw, vw = raw[l % 2]
             kvarn.compress_tile(kd, vd, src, tiles,
-                                torch.from_numpy(tab[:, :n0].reshape(-1).astype(np.int64)).to(dev), lay)
+                                torch.from_numpy(tab[:, :n0].reshape(-1).astype(np.int64)).to(dev), lay_s)
             win_k[l, 0, :, :w0] = torch.from_numpy(kw).to(dev)
             win_v[l, 0, :, :w0] = torch.from_numpy(vw).to(dev)
         del raw
@@ -348,11 +350,11 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
 
         def splits():
             for l in range(LAYERS):
-                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay, ws)
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws)
 
         def steps():
             for l in range(LAYERS):
-                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay, ws)
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws)
                 kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
 
         split_ms = back_to_back(splits, LAYERS)
@@ -360,7 +362,8 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         assert torch.isfinite(out).all().item(), "decode produced non-finite output"
         nbytes = HKV * n0 * rb + HKV * w0 * D * 8 + HQ * D * 4
         gbs = nbytes / (split_ms * 1e-3) / 1e9
-        res[f"qwen3_8b_ctx{ctx}"] = {
+        res[f"qwen3_8b_ctx{ctx}" + ("" if sb == 32 else "_f16_scales")] = {
+            "record_bytes": rb,
             "split_back_to_back_ms": split_ms, "split_bytes_per_launch": nbytes,
             "split_gbs": gbs, "split_frac": gbs / hbm,
             "attention_ms_per_layer": layer_ms,

@@ -69,6 +69,7 @@ typedef enum kvarn_status {
 #define KVARN_K_BITS 4
 #define KVARN_V_BITS 2
 #define KVARN_LAYOUT_VERSION 1
+#define KVARN_LAYOUT_VERSION_F16_SCALES 2
 #define KVARN_DEFAULT_SINKHORN_ITERS 4
 
 /*
@@ -116,6 +117,24 @@ typedef struct kvarn_layout {
 /* Fills *out (host pointer) for head_dim and sinkhorn_iters (1..16).
  * Returns KVARN_ERR_UNSUPPORTED for other head dims or iteration counts. */
 int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out);
+
+/*
+ * The record layout with scale fields of scale_bits bits: 32 gives the layout
+ * above (version KVARN_LAYOUT_VERSION); 16 gives the f16-scale layout
+ * (version KVARN_LAYOUT_VERSION_F16_SCALES; SharpInference issue #433, item 3
+ * names f16 scales as a saving of the record): the same fields in the same
+ * order, every scale field (delta, lo, s, r of K and V) an IEEE binary16
+ * value rounded to nearest from the fp32 one, and the same codes, which are
+ * computed from the unrounded scales. record_bytes = 96 D + 2 (4 D + 256 +
+ * 256 Gv): 7680 at D=64, 14336 at D=128, 28160 at D=256 (multiples of 128).
+ * Reconstruction reads the stored binary16 values. Scales whose magnitude
+ * exceeds 65504 (group ranges or stds that large) do not fit the format;
+ * use the fp32 layout for such data. Every entry point taking a layout
+ * accepts either version.
+ * Returns KVARN_ERR_UNSUPPORTED for other head dims, iteration counts or
+ * scale_bits.
+ */
+int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_layout_t* out);
 
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* kvarn_status_string(int status);
@@ -245,7 +264,7 @@ unsigned kvarn_get_launch_flags(void);
  *   q          : fp32 [B][Hq][D], unrotated. Hq / Hkv = G must be 1..8.
  *   tiles      : u8 base of the record pool.
  *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets, multiples of
- *                128 (record_bytes is a multiple of 1024, so a pool of whole
+ *                128 (record_bytes is a multiple of 128, so a pool of whole
  *                records qualifies; another offset makes that head's output
  *                NaN);
  *                entries at or past n_tiles[b] are never read.

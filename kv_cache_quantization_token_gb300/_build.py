@@ -11,7 +11,13 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkvarn.so")
-SOURCES = ["kvarn_abi.cu", "compress.cu", "window.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu"]
+# (source, object, extra flags): decode.cu is built twice, for records with
+# fp32 and with binary16 scale fields.
+UNITS = [("kvarn_abi.cu", "kvarn_abi.o", []), ("compress.cu", "compress.o", []),
+         ("window.cu", "window.o", []), ("decode.cu", "decode.o", []),
+         ("decode.cu", "decode_sb2.o", ["-DKVARN_SCALE_BYTES=2"]),
+         ("decode_noalloc.cu", "decode_noalloc.o", []), ("prefill.cu", "prefill.o", [])]
+SOURCES = sorted({u[0] for u in UNITS})
 HEADERS = [os.path.join(CSRC, "kvarn_common.cuh"), os.path.join(ROOT, "include", "kvarn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
@@ -34,12 +40,12 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     objs, procs = [], []
-    for src in SOURCES:
+    for src, obj, extra in UNITS:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(OUT_DIR, obj)
         objs.append(o)
         if force or _stale(o, [s] + HEADERS):
-            cmd = [nvcc()] + ARCH + FLAGS + ["-c", s, "-o", o]
+            cmd = [nvcc()] + ARCH + FLAGS + extra + ["-c", s, "-o", o]
             if verbose:
                 print(" ".join(cmd))
             procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

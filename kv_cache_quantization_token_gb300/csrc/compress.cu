@@ -126,14 +126,14 @@ __device__ __forceinline__ bool usable(float var, float mean) {
   return sd > ldexpf(sqrtf(var + mean * mean), -20);
 }
 
-template <int D>
+template <int D, int SB>
 __global__ void __launch_bounds__(CC<D>::NT, (D == 256) ? 1 : 2)
 compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw,
                 int64_t row_stride, const int64_t* __restrict__ src_row0,
                 uint8_t* __restrict__ tiles, const int64_t* __restrict__ dst_record,
                 int iters) {
   using C = CC<D>;
-  using R = Rec<D>;
+  using R = Rec<D, SB>;
   extern __shared__ __align__(16) unsigned char smem[];
   float* xs = reinterpret_cast<float*>(smem);
   float2* red = reinterpret_cast<float2*>(smem + C::OFF_RED);
@@ -347,12 +347,12 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
         ch_a[p_own] = l;
         ch_b[p_own] = inv;
         const int c = chan_of(p_own);
-        reinterpret_cast<float*>(stage + R::kKDelta)[c] = delta;
-        reinterpret_cast<float*>(stage + R::kKLo)[c] = l;
-        reinterpret_cast<float*>(stage + R::kKS)[c] = s_own / sqrt_d;
+        sc_st<SB>(stage + R::kKDelta, c, delta);
+        sc_st<SB>(stage + R::kKLo, c, l);
+        sc_st<SB>(stage + R::kKS, c, s_own / sqrt_d);
       }
     }
-    if (tok_writer) reinterpret_cast<float*>(stage + R::kKR)[t_own] = r_own;
+    if (tok_writer) sc_st<SB>(stage + R::kKR, t_own, r_own);
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -394,11 +394,11 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     const int g = (D == 256) ? ((cg >> 4) & 1) : 0;
     __syncthreads();  // every thread is past its last read of the tile
     if (tok_writer) {
-      reinterpret_cast<float*>(stage + R::kVDelta)[t_own * R::kGv + g] = delta;
-      reinterpret_cast<float*>(stage + R::kVLo)[t_own * R::kGv + g] = lo[0];
-      if (g == 0) reinterpret_cast<float*>(stage + R::kVR)[t_own] = r_own;
+      sc_st<SB>(stage + R::kVDelta, t_own * R::kGv + g, delta);
+      sc_st<SB>(stage + R::kVLo, t_own * R::kGv + g, lo[0]);
+      if (g == 0) sc_st<SB>(stage + R::kVR, t_own, r_own);
     }
-    if (h_own == 0) reinterpret_cast<float*>(stage + R::kVS)[chan_of(p_own)] = s_own / sqrt_d;
+    if (h_own == 0) sc_st<SB>(stage + R::kVS, chan_of(p_own), s_own / sqrt_d);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float l = __shfl_sync(0xffffffffu, lo[0], src_lane(i));
@@ -435,7 +435,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     __stcs(reinterpret_cast<uint4*>(rec + o), *reinterpret_cast<const uint4*>(stage + o));
 }
 
-template <int D>
+template <int D, int SB>
 cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw, int64_t row_stride,
                               const int64_t* src_row0, uint8_t* tiles, const int64_t* dst_record,
                               int64_t n_units, cudaStream_t st) {
@@ -445,28 +445,42 @@ cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(compress_kernel<D, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   const int64_t blocks = 2 * n_units;
-  compress_kernel<D><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(k_raw, v_raw, row_stride, src_row0,
-                                                               tiles, dst_record, iters);
+  compress_kernel<D, SB><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(
+      k_raw, v_raw, row_stride, src_row0, tiles, dst_record, iters);
   return cudaGetLastError();
+}
+
+template <int SB>
+cudaError_t launch_compress_sb(int D, int iters, const float* k_raw, const float* v_raw,
+                               int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
+                               const int64_t* dst_record, int64_t n_units, cudaStream_t st) {
+  switch (D) {
+    case 64: return launch_compress_d<64, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 128: return launch_compress_d<128, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 256: return launch_compress_d<256, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_compress(int D, int iters, const float* k_raw, const float* v_raw,
-                            int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
-                            const int64_t* dst_record, int64_t n_units, cudaStream_t st) {
-  switch (D) {
-    case 64: return launch_compress_d<64>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 128: return launch_compress_d<128>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 256: return launch_compress_d<256>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_compress(int D, int iters, int scale_bytes, const float* k_raw,
+                            const float* v_raw, int64_t row_stride, const int64_t* src_row0,
+                            uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
+                            cudaStream_t st) {
+  if (scale_bytes == 2)
+    return launch_compress_sb<2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
+                                 n_units, st);
+  if (scale_bytes == 4)
+    return launch_compress_sb<4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
+                                 n_units, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvarn

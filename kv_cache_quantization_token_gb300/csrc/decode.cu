@@ -35,8 +35,17 @@
 
 #include "kvarn_common.cuh"
 
+// Built twice: for records with fp32 scale fields (KVARN_SCALE_BYTES 4, the
+// default; this unit also holds the plan, the combine kernel and the
+// dispatch) and with binary16 scale fields (2).
+#ifndef KVARN_SCALE_BYTES
+#define KVARN_SCALE_BYTES 4
+#endif
+
 namespace kvarn {
 namespace {
+
+constexpr int kSB = KVARN_SCALE_BYTES;
 
 constexpr float kNegInf = -INFINITY;
 constexpr float kLog2eD = 1.4426950408889634f;
@@ -287,8 +296,9 @@ struct DC {
   static constexpr int WPT = WPT_;                              // warps per tile (2 or 4)
   static constexpr int TPS = NW / WPT;                          // tiles per round
   static constexpr int CH = 4 / WPT;                            // 32-token chunks per warp
-  static constexpr int RB = Rec<D>::kBytes;
-  static constexpr int GV = Rec<D>::kGv;
+  static constexpr int RB = Rec<D, kSB>::kBytes;                // record bytes
+  static constexpr int SLOT = Rec<D, kSB>::kSlot;               // record slot stride in shared memory
+  static constexpr int GV = Rec<D, kSB>::kGv;
   static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
   static constexpr int CODE_BYTES = 96 * D;                     // K + V codes, one TMA box
   static constexpr int CODE_LINES = CODE_BYTES / 128;           // 128-byte lines of that box
@@ -296,8 +306,8 @@ struct DC {
   static constexpr int NCB = D / 16;                            // 16-channel blocks
   static constexpr int HB = NCB / WPT;                          // blocks whose B fragments a warp builds
   static constexpr int NS = D / 64;                             // 64-channel slices of a V row
-  // window rows staged per warp (K and V rows of one chunk fit the record region)
-  static constexpr int WCH0 = (TPS * RB) / (NW * 2 * D * 4);
+  // window rows staged per warp (sized by the fp32 record, whatever the scale width)
+  static constexpr int WCH0 = (TPS * Rec<D, 4>::kBytes) / (NW * 2 * D * 4);
   static constexpr int WCH = WCH0 >= 16 ? 16 : WCH0 >= 8 ? 8 : WCH0 >= 4 ? 4 : 2;
   static constexpr int DP = D + 8;                              // padded channel stride of the merge
   static constexpr int MRG = NW * GP * DP * 4;                  // merge region [NW][GP][DP], over records
@@ -319,17 +329,18 @@ struct DC {
   static constexpr int NBAR = 2 * TPS > NW ? 2 * TPS : NW;       // one per record slot, or per window chunk
   static constexpr int OFF_BAR = (OFF_FLG + 2 * TPS * 4 + 7) / 8 * 8;
   static constexpr int OFF_REC = (OFF_BAR + NBAR * 8 + 1023) / 1024 * 1024;
-  static constexpr int REC_MIN = TPS * RB > MRG + NW * 128 ? TPS * RB : MRG + NW * 128;
+  static constexpr int WSTAGE = 2 * WCH * D * 4 * NW;           // window rows of one item
+  static constexpr int REC_MIN0 = TPS * SLOT > MRG + NW * 128 ? TPS * SLOT : MRG + NW * 128;
+  static constexpr int REC_MIN = REC_MIN0 > WSTAGE ? REC_MIN0 : WSTAGE;
   static constexpr int OFF_TRED = MRG;                          // tile items' reduction slots (record-relative)
   // dynamic shared memory for `slots` record slots (without the alignment slack)
   static constexpr int smem_bytes(int slots) {
-    return OFF_REC + (slots * RB > REC_MIN ? slots * RB : REC_MIN);
+    return OFF_REC + (slots * SLOT > REC_MIN ? slots * SLOT : REC_MIN);
   }
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
-  static_assert(RB % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
-  static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D>::kKDelta, "code box");
+  static_assert(SLOT % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
+  static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D, kSB>::kKDelta, "code box");
   static_assert(HB >= 1 && WPT * HB == NCB && (WPT == 2 || WPT == 4), "channel blocks per warp");
-  static_assert(2 * WCH * D * 4 * NW <= TPS * RB, "window chunks must fit the record region");
   static_assert(NW * GP * D * 4 <= REC_MIN, "window partials fit the record region");
 };
 
@@ -381,7 +392,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int rounds_arg, float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, NW_, WPT_>;
-  using R = Rec<D>;
+  using R = Rec<D, kSB>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
   constexpr int HB = C::HB, WPT = C::WPT, CH = C::CH;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -582,8 +593,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     okf[slot] = aligned;
     if (aligned) {
       mbar_expect_tx(&bar[slot], C::RB);
-      tma_load_2d(rec + slot * C::RB, &tmap, 0, (int)(off >> 7), &bar[slot]);
-      bulk_g2s(rec + slot * C::RB + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
+      tma_load_2d(rec + slot * C::SLOT, &tmap, 0, (int)(off >> 7), &bar[slot]);
+      bulk_g2s(rec + slot * C::SLOT + C::CODE_BYTES, tiles + off + C::CODE_BYTES,
                C::RB - C::CODE_BYTES, &bar[slot]);
     }
     return aligned;
@@ -631,23 +642,24 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     const int kk = pair;
     const int slot = pair + (dbuf ? TPS * (k & 1) : 0);
     const uint32_t par = dbuf ? (uint32_t)((k >> 1) & 1) : 0u;
-    const unsigned char* Rk = rec + slot * C::RB;
+    const unsigned char* Rk = rec + slot * C::SLOT;
     const uint32_t rk = smem_u32(Rk);
     const bool landed = okf[slot] && mbar_wait(&bar[slot], par);
     if (!landed) bad = 1;  // computed on, result poisoned
     if (issuer && landed) {
       if (k & 1) pend1 = 0; else pend0 = 0;
     }
-    const float* kS = reinterpret_cast<const float*>(Rk + R::kKS);
-    const float* kD = reinterpret_cast<const float*>(Rk + R::kKDelta);
-    const float* kL = reinterpret_cast<const float*>(Rk + R::kKLo);
-    const float* kR = reinterpret_cast<const float*>(Rk + R::kKR);
+    const unsigned char* kS = Rk + R::kKS;  // scale fields (fp32 or binary16)
+    const unsigned char* kD = Rk + R::kKDelta;
+    const unsigned char* kL = Rk + R::kKLo;
+    const unsigned char* kR = Rk + R::kKR;
 
     // ---- folded query wd_c = q'_c s_c delta_c, one power-of-two scale per head
     // from the bound max|q'| * max_c s_c delta_c (the same in both warps)
     float mf = 0.f;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) mf = fmaxf(mf, fabsf(kS[lane + 32 * i] * kD[lane + 32 * i]));
+    for (int i = 0; i < D / 32; ++i)
+      mf = fmaxf(mf, fabsf(sc_ld<kSB>(kS, lane + 32 * i) * sc_ld<kSB>(kD, lane + 32 * i)));
     mf = warp_max(mf);
     float scB[NT], invA[NT];
 #pragma unroll
@@ -672,9 +684,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     for (int u = 0; u < HB; ++u) {
       const int cb = HB * half + u;
       const int c = 16 * cb + 2 * q4 + 8 * hl;
-      const float2 s = *reinterpret_cast<const float2*>(kS + c);
-      const float2 dd = *reinterpret_cast<const float2*>(kD + c);
-      const float2 lo = *reinterpret_cast<const float2*>(kL + c);
+      const float2 s = sc_ld2<kSB>(kS, c);
+      const float2 dd = sc_ld2<kSB>(kD, c);
+      const float2 lo = sc_ld2<kSB>(kL, c);
       const float2 sd = __fmul2_rn(s, dd), sl = __fmul2_rn(s, lo);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -768,7 +780,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     float z[CH][2][2][NT];
 #pragma unroll
     for (int w2 = 0; w2 < CH; ++w2) {
-      const float4 r4 = *reinterpret_cast<const float4*>(kR + 32 * (CH * half + w2) + 4 * g8);
+      const float4 r4 = sc_ld4<kSB>(kR, 32 * (CH * half + w2) + 4 * g8);
       const float rt[2][2] = {{r4.x, r4.y}, {r4.z, r4.w}};
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -812,10 +824,10 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     // ---- value side: pd_t = p_t r_t delta_tg as fp16 hi + lo, transposed into
     // B fragments with movmatrix. K-block (w2, j) of phase B holds tokens
     // 32 w4 + 8 q4 + 2j + {0, 4} (b0) and + {1, 5} (b1).
-    const float* vR = reinterpret_cast<const float*>(Rk + R::kVR);
-    const float* vD = reinterpret_cast<const float*>(Rk + R::kVDelta);
-    const float* vL = reinterpret_cast<const float*>(Rk + R::kVLo);
-    const float* vS = reinterpret_cast<const float*>(Rk + R::kVS);
+    const unsigned char* vR = Rk + R::kVR;
+    const unsigned char* vD = Rk + R::kVDelta;
+    const unsigned char* vL = Rk + R::kVLo;
+    const unsigned char* vS = Rk + R::kVS;
     uint32_t bB[GV][CH][2][NT][2];
     float invP[GV][NT], cstP[GV][NT];
 #pragma unroll
@@ -826,17 +838,20 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
       for (int w2 = 0; w2 < CH; ++w2) {
         const int t0 = 32 * (CH * half + w2) + 4 * g8;
-        const float4 vr4 = *reinterpret_cast<const float4*>(vR + t0);
+        const float4 vr4 = sc_ld4<kSB>(vR, t0);
         const float vrt[4] = {vr4.x, vr4.y, vr4.z, vr4.w};
         float dv[4], lv[4];
         if constexpr (GV == 1) {
-          const float4 d4 = *reinterpret_cast<const float4*>(vD + t0);
-          const float4 l4 = *reinterpret_cast<const float4*>(vL + t0);
+          const float4 d4 = sc_ld4<kSB>(vD, t0);
+          const float4 l4 = sc_ld4<kSB>(vL, t0);
           dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
           lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
         } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) { dv[e] = vD[(t0 + e) * GV + gv]; lv[e] = vL[(t0 + e) * GV + gv]; }
+          for (int e = 0; e < 4; ++e) {
+            dv[e] = sc_ld<kSB>(vD, (t0 + e) * GV + gv);
+            lv[e] = sc_ld<kSB>(vL, (t0 + e) * GV + gv);
+          }
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -916,8 +931,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           }
       }
       // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
-      const float4 s0 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8);
-      const float4 s1 = *reinterpret_cast<const float4*>(vS + 64 * sl + 8 * g8 + 4);
+      const float4 s0 = sc_ld4<kSB>(vS, 64 * sl + 8 * g8);
+      const float4 s1 = sc_ld4<kSB>(vS, 64 * sl + 8 * g8 + 4);
       const float sv[4][2] = {{s0.x, s0.y}, {s0.z, s0.w}, {s1.x, s1.y}, {s1.z, s1.w}};
       if (k == 0) {
 #pragma unroll
@@ -1010,6 +1025,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 }
 
+#if KVARN_SCALE_BYTES == 4
 // LSE combine: one CTA of 512 threads per (query head, sequence). Each group
 // of D/4 threads reads whole item rows (float4 per thread, coalesced) of
 // every (512/(D/4))-th item in one pass, keeping its own running maximum; the
@@ -1109,6 +1125,8 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   }
 }
 
+#endif  // KVARN_SCALE_BYTES == 4
+
 // cuTensorMapEncodeTiled, fetched once from the driver (the library links the
 // static CUDA runtime only).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1179,22 +1197,22 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
 template <int D, int GP>
 cudaError_t launch_split_g(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  // (tiles per round, warps per tile); several rounds only with four warps
-  const int key = 10 * p.tiles_per_round + p.warps_per_tile;
-  if (p.rounds > 1) {
-    if (key == 22) return launch_split_t<D, GP, 4, 2, true>(p, a, ws_ml, ws_acc, st);
-    if (key == 14) return launch_split_t<D, GP, 4, 4, true>(p, a, ws_ml, ws_acc, st);
-    return cudaErrorInvalidValue;
+  // The plans decode_plan() makes: head_dim <= 128 takes a warp pair per
+  // tile, 4 tiles per round (one round) or 2 (one or more rounds); head_dim
+  // 256 four warps per tile, one tile per round.
+  if constexpr (D <= 128) {
+    if (p.warps_per_tile != 2) return cudaErrorInvalidValue;
+    if (p.tiles_per_round == 4 && p.rounds == 1)
+      return launch_split_t<D, GP, 8, 2, false>(p, a, ws_ml, ws_acc, st);
+    if (p.tiles_per_round == 2)
+      return p.rounds > 1 ? launch_split_t<D, GP, 4, 2, true>(p, a, ws_ml, ws_acc, st)
+                          : launch_split_t<D, GP, 4, 2, false>(p, a, ws_ml, ws_acc, st);
+  } else {
+    if (p.warps_per_tile == 4 && p.tiles_per_round == 1)
+      return p.rounds > 1 ? launch_split_t<D, GP, 4, 4, true>(p, a, ws_ml, ws_acc, st)
+                          : launch_split_t<D, GP, 4, 4, false>(p, a, ws_ml, ws_acc, st);
   }
-  switch (key) {
-    case 22: return launch_split_t<D, GP, 4, 2, false>(p, a, ws_ml, ws_acc, st);
-    case 14: return launch_split_t<D, GP, 4, 4, false>(p, a, ws_ml, ws_acc, st);
-    case 24: return launch_split_t<D, GP, 8, 4, false>(p, a, ws_ml, ws_acc, st);
-    case 42:
-      if constexpr (D <= 128) return launch_split_t<D, GP, 8, 2, false>(p, a, ws_ml, ws_acc, st);
-      return cudaErrorInvalidValue;
-    default: return cudaErrorInvalidValue;
-  }
+  return cudaErrorInvalidValue;
 }
 
 template <int D>
@@ -1216,6 +1234,7 @@ void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** 
   *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
+#if KVARN_SCALE_BYTES == 4
 int sm_count() {
   static int cached[64] = {};
   int dev = 0;
@@ -1227,8 +1246,11 @@ int sm_count() {
   return n;
 }
 
+#endif
+
 }  // namespace
 
+#if KVARN_SCALE_BYTES == 4
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
@@ -1273,15 +1295,9 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
 
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                 cudaStream_t st) {
-  if (p.items == 0) return cudaSuccess;
-  float *ml, *acc;
-  ws_split(p, a.B, a.Hq, ws, &ml, &acc);
-  switch (a.D) {
-    case 64: return launch_split_d<64>(p, a, ml, acc, st);
-    case 128: return launch_split_d<128>(p, a, ml, acc, st);
-    case 256: return launch_split_d<256>(p, a, ml, acc, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.scale_bytes == 4) return launch_decode_split_sb4(p, a, ws, st);
+  if (a.scale_bytes == 2) return launch_decode_split_sb2(p, a, ws, st);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
@@ -1295,6 +1311,26 @@ cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, con
     case 64: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<64>, cml, cacc, Hq, p.items, p.tile_items, out);
     case 128: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<128>, cml, cacc, Hq, p.items, p.tile_items, out);
     case 256: return cudaLaunchKernelEx(&L.cfg, decode_combine_kernel<256>, cml, cacc, Hq, p.items, p.tile_items, out);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+#endif  // KVARN_SCALE_BYTES == 4
+
+#if KVARN_SCALE_BYTES == 4
+cudaError_t launch_decode_split_sb4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                    cudaStream_t st) {
+#else
+cudaError_t launch_decode_split_sb2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                    cudaStream_t st) {
+#endif
+  if (p.items == 0) return cudaSuccess;
+  float *ml, *acc;
+  ws_split(p, a.B, a.Hq, ws, &ml, &acc);
+  switch (a.D) {
+    case 64: return launch_split_d<64>(p, a, ml, acc, st);
+    case 128: return launch_split_d<128>(p, a, ml, acc, st);
+    case 256: return launch_split_d<256>(p, a, ml, acc, st);
     default: return cudaErrorInvalidValue;
   }
 }

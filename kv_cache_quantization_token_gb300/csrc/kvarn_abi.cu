@@ -16,9 +16,11 @@ bool supported_dim(int D) { return D == 64 || D == 128 || D == 256; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA; }
 
-int fill_layout(int D, int iters, kvarn_layout_t* L) {
+// sb: bytes of each scale field, 4 (fp32, layout version 1) or 2 (binary16,
+// layout version 2); the code fields are the same in both.
+int fill_layout(int D, int iters, int sb, kvarn_layout_t* L) {
   memset(L, 0, sizeof(*L));
-  L->version = KVARN_LAYOUT_VERSION;
+  L->version = sb == 2 ? KVARN_LAYOUT_VERSION_F16_SCALES : KVARN_LAYOUT_VERSION;
   L->head_dim = D;
   L->tile_tokens = KVARN_TILE_TOKENS;
   L->sinkhorn_iters = iters;
@@ -30,23 +32,30 @@ int fill_layout(int D, int iters, kvarn_layout_t* L) {
   L->off_k_codes = 0;
   L->off_v_codes = L->off_k_codes + (int64_t)D * (T / 2);
   L->off_k_delta = L->off_v_codes + T * (D / 4);
-  L->off_k_lo = L->off_k_delta + 4LL * D;
-  L->off_k_s = L->off_k_lo + 4LL * D;
-  L->off_k_r = L->off_k_s + 4LL * D;
-  L->off_v_delta = L->off_k_r + 4 * T;
-  L->off_v_lo = L->off_v_delta + 4 * T * gv;
-  L->off_v_r = L->off_v_lo + 4 * T * gv;
-  L->off_v_s = L->off_v_r + 4 * T;
-  L->record_bytes = L->off_v_s + 4LL * D;
+  L->off_k_lo = L->off_k_delta + (int64_t)sb * D;
+  L->off_k_s = L->off_k_lo + (int64_t)sb * D;
+  L->off_k_r = L->off_k_s + (int64_t)sb * D;
+  L->off_v_delta = L->off_k_r + sb * T;
+  L->off_v_lo = L->off_v_delta + sb * T * gv;
+  L->off_v_r = L->off_v_lo + sb * T * gv;
+  L->off_v_s = L->off_v_r + sb * T;
+  L->record_bytes = L->off_v_s + (int64_t)sb * D;
   return KVARN_OK;
+}
+
+// Bytes of each scale field of a layout this library produced.
+int scale_bytes_of(const kvarn_layout_t* L) {
+  return L->version == KVARN_LAYOUT_VERSION_F16_SCALES ? 2 : 4;
 }
 
 // A layout handed back by the caller must be one this library produced.
 bool layout_ok(const kvarn_layout_t* L) {
-  if (!L || L->version != KVARN_LAYOUT_VERSION || !supported_dim(L->head_dim)) return false;
+  if (!L || !supported_dim(L->head_dim)) return false;
+  if (L->version != KVARN_LAYOUT_VERSION && L->version != KVARN_LAYOUT_VERSION_F16_SCALES)
+    return false;
   if (L->sinkhorn_iters < 1 || L->sinkhorn_iters > 16) return false;
   kvarn_layout_t ref;
-  fill_layout(L->head_dim, L->sinkhorn_iters, &ref);
+  fill_layout(L->head_dim, L->sinkhorn_iters, scale_bytes_of(L), &ref);
   return memcmp(&ref, L, sizeof(ref)) == 0;
 }
 
@@ -70,10 +79,15 @@ int kvarn_set_launch_flags(unsigned flags) {
 unsigned kvarn_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
 int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out) {
+  return kvarn_layout_scales(head_dim, sinkhorn_iters, 32, out);
+}
+
+int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_layout_t* out) {
   if (!out) return KVARN_ERR_NULL;
-  if (!supported_dim(head_dim) || sinkhorn_iters < 1 || sinkhorn_iters > 16)
+  if (!supported_dim(head_dim) || sinkhorn_iters < 1 || sinkhorn_iters > 16 ||
+      (scale_bits != 32 && scale_bits != 16))
     return KVARN_ERR_UNSUPPORTED;
-  return fill_layout(head_dim, sinkhorn_iters, out);
+  return fill_layout(head_dim, sinkhorn_iters, scale_bits / 8, out);
 }
 
 const char* kvarn_status_string(int status) {
@@ -117,9 +131,9 @@ int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stri
   if (row_stride < D || n_rows < KVARN_TILE_TOKENS) return KVARN_ERR_BAD_ARG;
   if ((row_stride & 3) || !aligned16(k_raw) || !aligned16(v_raw) || !aligned16(tiles))
     return KVARN_ERR_ALIGN;
-  return from_cuda(kvarn::launch_compress(D, layout->sinkhorn_iters, k_raw, v_raw, row_stride,
-                                          src_row0, tiles, dst_record, n_units,
-                                          (cudaStream_t)stream));
+  return from_cuda(kvarn::launch_compress(D, layout->sinkhorn_iters, scale_bytes_of(layout),
+                                          k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
+                                          n_units, (cudaStream_t)stream));
 }
 
 int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
@@ -181,7 +195,8 @@ static int decode_prepare(const float* q, const uint8_t* tiles, const int64_t* t
     return KVARN_ERR_ALIGN;
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
   *a = kvarn::DecodeArgs{q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
-                         win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale};
+                         win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
+                         scale_bytes_of(layout)};
   return KVARN_OK;
 }
 
@@ -272,8 +287,8 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
   return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
                                          n_tiles, win_k, win_v, win_start, win_len, win_capacity,
-                                         Hq, Hkv, head_dim, softmax_scale, ws, out,
-                                         (cudaStream_t)stream));
+                                         Hq, Hkv, head_dim, softmax_scale, scale_bytes_of(layout),
+                                         ws, out, (cudaStream_t)stream));
 }
 
 int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,

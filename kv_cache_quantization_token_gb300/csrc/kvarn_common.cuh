@@ -4,6 +4,7 @@
 // layout from the method description on its own.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,25 +14,62 @@ namespace kvarn {
 
 constexpr int kTile = KVARN_TILE_TOKENS;  // tokens per compressed tile
 
-// Byte offsets of the record fields for head_dim D (same values as
-// kvarn_layout(); kept as constexpr so the kernels index without a struct).
-template <int D>
+// Byte offsets of the record fields for head_dim D with scale fields of SB
+// bytes: 4 (fp32, layout version 1) or 2 (IEEE binary16, layout version 2;
+// the same codes). Same values as kvarn_layout() / kvarn_layout_scales();
+// kept as constexpr so the kernels index without a struct.
+template <int D, int SB = 4>
 struct Rec {
+  static_assert(SB == 4 || SB == 2, "scale field width");
+  static constexpr int kSB = SB;
   static constexpr int kGv = D / (D < 128 ? D : 128);     // V groups per token
   static constexpr int kVGroup = D < 128 ? D : 128;        // channels per V group
   static constexpr int kKCodes = 0;                        // u8 [D][64]
   static constexpr int kVCodes = kKCodes + D * (kTile / 2);  // u8 [128][D/4]
   static constexpr int kKDelta = kVCodes + kTile * (D / 4);
-  static constexpr int kKLo = kKDelta + 4 * D;
-  static constexpr int kKS = kKLo + 4 * D;
-  static constexpr int kKR = kKS + 4 * D;
-  static constexpr int kVDelta = kKR + 4 * kTile;
-  static constexpr int kVLo = kVDelta + 4 * kTile * kGv;
-  static constexpr int kVR = kVLo + 4 * kTile * kGv;
-  static constexpr int kVS = kVR + 4 * kTile;
-  static constexpr int kBytes = kVS + 4 * D;
-  static_assert(kBytes == 112 * D + 1024 + 1024 * kGv, "record size");
+  static constexpr int kKLo = kKDelta + SB * D;
+  static constexpr int kKS = kKLo + SB * D;
+  static constexpr int kKR = kKS + SB * D;
+  static constexpr int kVDelta = kKR + SB * kTile;
+  static constexpr int kVLo = kVDelta + SB * kTile * kGv;
+  static constexpr int kVR = kVLo + SB * kTile * kGv;
+  static constexpr int kVS = kVR + SB * kTile;
+  static constexpr int kBytes = kVS + SB * D;
+  // stride of a record slot in shared memory (slots start on 1024-byte swizzle atoms)
+  static constexpr int kSlot = (kBytes + 1023) / 1024 * 1024;
+  static_assert(kBytes == 96 * D + SB * (4 * D + 256 + 256 * kGv), "record size");
+  static_assert(kBytes % 128 == 0, "records on 128-byte lines");
 };
+
+// Scale fields of a record, fp32 (SB = 4) or binary16 (SB = 2), read as fp32:
+// element i, the pair i, i+1 (i even) and the four i..i+3 (i a multiple of 4).
+template <int SB>
+__device__ __forceinline__ float sc_ld(const unsigned char* base, int i) {
+  if constexpr (SB == 4) return reinterpret_cast<const float*>(base)[i];
+  else return __half2float(reinterpret_cast<const __half*>(base)[i]);
+}
+template <int SB>
+__device__ __forceinline__ float2 sc_ld2(const unsigned char* base, int i) {
+  if constexpr (SB == 4) return *reinterpret_cast<const float2*>(base + 4 * i);
+  else return __half22float2(*reinterpret_cast<const __half2*>(base + 2 * i));
+}
+template <int SB>
+__device__ __forceinline__ float4 sc_ld4(const unsigned char* base, int i) {
+  if constexpr (SB == 4) {
+    return *reinterpret_cast<const float4*>(base + 4 * i);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(base + 2 * i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+}
+// Stores v into scale field i, rounded to nearest (ties to even) for binary16.
+template <int SB>
+__device__ __forceinline__ void sc_st(unsigned char* base, int i, float v) {
+  if constexpr (SB == 4) reinterpret_cast<float*>(base)[i] = v;
+  else reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
+}
 
 __device__ __forceinline__ float shfl_xor(float v, int m) {
   return __shfl_xor_sync(0xffffffffu, v, m);
@@ -81,9 +119,10 @@ struct LaunchCfg {
 // Launchers implemented in the .cu files; kvarn_abi.cu validates arguments
 // and calls them. They return a cudaError_t from cudaGetLastError().
 namespace kvarn {
-cudaError_t launch_compress(int D, int iters, const float* k_raw, const float* v_raw,
-                            int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
-                            const int64_t* dst_record, int64_t n_units, cudaStream_t st);
+cudaError_t launch_compress(int D, int iters, int scale_bytes, const float* k_raw,
+                            const float* v_raw, int64_t row_stride, const int64_t* src_row0,
+                            uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
+                            cudaStream_t st);
 cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, cudaStream_t st);
 cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
                           float* win_v, int win_capacity, const int32_t* win_start,
@@ -112,17 +151,24 @@ struct DecodeArgs {
   const int32_t* win_len;
   int win_capacity, B, Hq, Hkv, D, max_tiles;
   float scale;
+  int scale_bytes;  // record scale fields: 4 (fp32) or 2 (binary16)
 };
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p);
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                 cudaStream_t st);
+// the split kernels for records with fp32 (4) or binary16 (2) scale fields,
+// built as two translation units of decode.cu
+cudaError_t launch_decode_split_sb4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                    cudaStream_t st);
+cudaError_t launch_decode_split_sb2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                    cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
                                   float* out, cudaStream_t st);
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           void* ws, float* out, cudaStream_t st);
+                           int scale_bytes, void* ws, float* out, cudaStream_t st);
 // 128-key blocks a prefill chunk sees (tiles, and tiles + window blocks), and
 // the workspace bytes of one (block, KV head) image.
 void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, int* n_blk);

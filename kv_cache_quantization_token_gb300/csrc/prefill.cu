@@ -236,7 +236,7 @@ __device__ __forceinline__ void fwht_reg(float (&x)[N]) {
 
 template <int D>
 struct PC {
-  static constexpr int RB = Rec<D>::kBytes;
+  static constexpr int RB = Rec<D>::kBytes;             // room for a record of either scale width
   static constexpr int OPB = 128 * D * 2;                // one fp16 operand image: 128 rows x D
   static constexpr int BLK = 3 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T
   // attention kernel shared memory
@@ -279,10 +279,10 @@ struct PrefillArgs {
 
 // ---------------------------------------------------------------------------
 // dequant: block j (tile j, or window block j - n_tblk) of KV head blockIdx.y
-template <int D>
+template <int D, int SB>
 __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillArgs a) {
   using P = PC<D>;
-  using R = Rec<D>;
+  using R = Rec<D, SB>;  // scale fields fp32 (SB 4) or binary16 (SB 2)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (aligned && tid == 0) bulk_load(sm, a.tiles + off, P::RB, bar);
+    if (aligned && tid == 0) bulk_load(sm, a.tiles + off, R::kBytes, bar);
     poison = !aligned || !mbar_wait_bounded(bar, 0);
     if (__syncthreads_or(poison)) {
       // an unusable record: NaN keys make every score of this block NaN
@@ -310,19 +310,19 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
       for (int o = tid * 8; o < P::BLK / 2; o += 8 * P::NTHR)
         *reinterpret_cast<uint4*>(sKh + 2 * o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
     } else {
-      const float* kS = reinterpret_cast<const float*>(rec + R::kKS);
-      const float* kD = reinterpret_cast<const float*>(rec + R::kKDelta);
-      const float* kL = reinterpret_cast<const float*>(rec + R::kKLo);
-      const float* kR = reinterpret_cast<const float*>(rec + R::kKR);
-      const float* vS = reinterpret_cast<const float*>(rec + R::kVS);
-      const float* vR = reinterpret_cast<const float*>(rec + R::kVR);
-      const float* vD = reinterpret_cast<const float*>(rec + R::kVDelta);
-      const float* vL = reinterpret_cast<const float*>(rec + R::kVLo);
+      const unsigned char* kS = rec + R::kKS;
+      const unsigned char* kD = rec + R::kKDelta;
+      const unsigned char* kL = rec + R::kKLo;
+      const unsigned char* kR = rec + R::kKR;
+      const unsigned char* vS = rec + R::kVS;
+      const unsigned char* vR = rec + R::kVR;
+      const unsigned char* vD = rec + R::kVDelta;
+      const unsigned char* vL = rec + R::kVLo;
       // K~: thread -> channel tid % D and a contiguous share of its 128 keys
       {
         constexpr int NKG = P::NTHR / D, WPG = 16 / NKG;  // key groups, 8-key words per group
         const int c = tid % D, kg = tid / D;
-        const float s = kS[c], d = kD[c] * s, lo = kL[c] * s;
+        const float s = sc_ld<SB>(kS, c), d = sc_ld<SB>(kD, c) * s, lo = sc_ld<SB>(kL, c) * s;
         const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
         uint32_t wds[WPG];  // this thread's share of the channel row, read with 16-byte loads
 #pragma unroll
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int t = 8 * w4 + i;
-            const float v = kR[t] * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
+            const float v = sc_ld<SB>(kR, t) * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
             const __half h = __float2half_rn(v);
             const uint32_t o = sw_off(t, c, 128);
             *reinterpret_cast<__half*>(sKh + o) = h;
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
       // V~^T: thread -> key t, half of the D channels of the token row
       {
         const int t = row;
-        const float r = vR[t];
+        const float r = sc_ld<SB>(vR, t);
         const unsigned char* vrow = rec + R::kVCodes + t * (D / 4);
         constexpr int HB = D / 8;  // code bytes of half a token row (16 at D=128, 8 at D=64)
         uint32_t vw[HB / 4];       // read with one or two wide loads
@@ -367,11 +367,11 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
           const int jb = half * HB + ub;
           const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
           const int g = (4 * jb) / R::kVGroup;
-          const float d = vD[t * R::kGv + g] * r, lo = vL[t * R::kGv + g] * r;
+          const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 4 * jb + e;
-            const float v = vS[c] * fmaf(d, (float)((byte >> (2 * e)) & 3u), lo);
+            const float v = sc_ld<SB>(vS, c) * fmaf(d, (float)((byte >> (2 * e)) & 3u), lo);
             *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
           }
         }
@@ -772,7 +772,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
 }
 
-template <int D>
+template <int D, int SB>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   using P = PC<D>;
   static bool configured[64] = {};
@@ -782,13 +782,13 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_dequant_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_dequant_kernel<D, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P::DQ_SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   if (a.n_blk > 0) {
-    prefill_dequant_kernel<D><<<dim3(a.n_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
+    prefill_dequant_kernel<D, SB><<<dim3(a.n_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -819,7 +819,7 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           void* ws, float* out, cudaStream_t st) {
+                           int scale_bytes, void* ws, float* out, cudaStream_t st) {
   PrefillArgs a;
   a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
   a.ws = reinterpret_cast<uint8_t*>(ws);
@@ -827,9 +827,12 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
   a.n_tiles = n_tiles; a.table_stride = table_stride; a.win_start = win_start;
   a.win_len = win_len; a.win_cap = win_capacity; a.qscale = softmax_scale * kLog2e;
   prefill_blocks(pos0, C, n_tiles, win_len, &a.n_tblk, &a.n_blk);
-  switch (D) {
-    case 64: return launch_prefill_d<64>(a, st);
-    case 128: return launch_prefill_d<128>(a, st);
+  const int key = 10 * D + scale_bytes;
+  switch (key) {
+    case 644: return launch_prefill_d<64, 4>(a, st);
+    case 642: return launch_prefill_d<64, 2>(a, st);
+    case 1284: return launch_prefill_d<128, 4>(a, st);
+    case 1282: return launch_prefill_d<128, 2>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

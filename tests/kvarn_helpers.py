@@ -72,6 +72,36 @@ def compare_record(gpu_rec: np.ndarray, ref: dict, D: int) -> dict:
     return stats
 
 
+def compare_record_f16(gpu_rec: np.ndarray, ref: dict, D: int) -> dict:
+    """Compare a GPU record of the f16-scale layout with
+    oracle.compress_unit(..., scale_bits=16). Codes as in compare_record. Each
+    stored scale is binary16 rounded from the kernel's fp32 value, the
+    oracle's from fp64: they must be equal, except where the fp64 value lies
+    within 1e-6 (relative) of the midpoint between two binary16 neighbours,
+    where one ulp apart is allowed (counted and returned)."""
+    g = oracle.unpack_record(gpu_rec, D, 16)
+    r = oracle.unpack_record(ref["record"], D, 16)
+    stats = {"band_flips": 0, "codes": 0, "scale_flips": 0}
+    for t in ("k", "v"):
+        diff = g[f"{t}_codes"] != r[f"{t}_codes"]
+        band = band_mask(ref[f"{t}_vpre"])
+        assert not (diff & ~band).any(), f"{t} codes differ outside the rounding band"
+        stats["band_flips"] += int(diff.sum())
+        stats["codes"] += diff.size
+    for name in ("k_delta", "k_lo", "k_s", "k_r", "v_delta", "v_lo", "v_r", "v_s"):
+        got, want, exact = g[name], r[name], np.asarray(ref[name], np.float64)
+        ne = got != want
+        if ne.any():
+            gb = got[ne].astype(np.float16).view(np.uint16).astype(np.int32)
+            wb = want[ne].astype(np.float16).view(np.uint16).astype(np.int32)
+            assert np.all(np.abs(gb - wb) == 1), f"{name}: stored binary16 values more than 1 ulp apart"
+            mid = (got[ne] + want[ne]) / 2
+            assert np.all(np.abs(exact[ne] - mid) <= 1e-6 * np.abs(mid)), (
+                f"{name}: binary16 values differ away from a rounding midpoint")
+            stats["scale_flips"] += int(ne.sum())
+    return stats
+
+
 def n_tiles_for(ctx: int, W: int) -> int:
     """Promotion rule: while the window holds >= W tokens, promote 128."""
     return 0 if ctx < W else (ctx - W) // TILE + 1
@@ -81,12 +111,13 @@ class Cache:
     """A batch of KVarN caches built on the GPU through the C ABI."""
 
     def __init__(self, workload, layer, ctxs, Hkv, D, W=128, cap=None, win_start=None, dev="cuda:0",
-                 iters=4):
+                 iters=4, scale_bits=32):
         self.workload, self.layer, self.Hkv, self.D, self.W = workload, layer, Hkv, D, W
         self.dev = torch.device(dev)
         self.B = len(ctxs)
         self.ctxs = list(ctxs)
-        self.lay = kvarn.layout(D, iters)
+        self.scale_bits = scale_bits
+        self.lay = kvarn.layout(D, iters, scale_bits)
         self.rb = self.lay.record_bytes
         self.nt = [n_tiles_for(c, W) for c in ctxs]
         self.max_tiles = max(max(self.nt), 1)
@@ -143,7 +174,8 @@ class Cache:
         scale = self.D ** -0.5 if scale is None else scale
         return oracle.decode_attention(q, self.tiles.cpu().numpy(), self.tile_table.cpu().numpy(),
                                        self.nt, self.win_k.cpu().numpy(), self.win_v.cpu().numpy(),
-                                       self.starts, self.wl, scale, heads=heads)
+                                       self.starts, self.wl, scale, heads=heads,
+                                       scale_bits=self.scale_bits)
 
 
 def rel_l2(got: np.ndarray, want: np.ndarray) -> float:
@@ -163,12 +195,13 @@ class PrefillRun:
     oracle can be evaluated on the same state."""
 
     def __init__(self, workload, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
-                 dev="cuda:0", scale=None):
+                 dev="cuda:0", scale=None, scale_bits=32):
         dev = torch.device(dev)
         self.Hq, self.Hkv, self.D, self.W = Hq, Hkv, D, W
         self.k, self.v = synth.kv_layer(workload, layer, Hkv, n_tokens, D)
         self.q = synth.queries(workload, layer, (n_tokens, Hq, D))
-        self.lay = kvarn.layout(D)
+        self.scale_bits = scale_bits
+        self.lay = kvarn.layout(D, scale_bits=scale_bits)
         rb = self.rb = self.lay.record_bytes
         self.cap = cap = TILE * ((W - 1 + chunk + TILE - 1) // TILE)
         max_tiles = n_tokens // TILE + 1
@@ -213,7 +246,8 @@ class PrefillRun:
         pool = self.tiles.cpu().numpy()
         ref = oracle.prefill_attention(self.q[pos0:pos0 + s["C"]], pos0, pool,
                                        self.table.cpu().numpy(), s["n_tiles"], s["win_k"],
-                                       s["win_v"], s["start"], s["length"], self.scale, rows=rows)
+                                       s["win_v"], s["start"], s["length"], self.scale, rows=rows,
+                                       scale_bits=self.scale_bits)
         worst = 0.0
         for (i, h), r in ref.items():
             e = rel_l2(s["out"][i, h], r)

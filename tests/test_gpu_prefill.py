@@ -61,3 +61,11 @@ def test_prefill_15k_prompt_full_sampled():
         rows = [(i, h) for i in list(range(0, C, 64)) + [C - 1] for h in (0, 3, 28, 31)]
         w = run.check(p, rows)
         print(f"15.5k chunk {p}: worst rel-L2 {w:.2e}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W", [(16, 2, 128, 900, 300, 256), (8, 8, 64, 700, 256, 128)])
+def test_prefill_f16_scale_records(Hq, Hkv, D, n, chunk, W):
+    """Chunked prefill over records of the f16-scale layout."""
+    run = PrefillRun("qwen3_8b_decode", 5, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk, scale_bits=16)
+    for p in run.snap:
+        run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=19))
