@@ -335,6 +335,36 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
                             kvarn_stream_t stream);
 
 /*
+ * Chunked prefill that keeps the packed tiles' operand images in ws from one
+ * chunk to the next (same result as kvarn_prefill_attention). A prompt's
+ * tiles never change once promoted, so a caller that streams the chunks of
+ * one sequence in order can keep ws for the whole prompt and let each call
+ * convert only the tiles promoted since the previous one, plus the window
+ * blocks (which change every chunk).
+ *   ws           : [Hkv][ws_blocks] block images of kvarn_prefill_workspace_bytes(
+ *                  max_tiles, win_capacity, Hkv, head_dim) / Hkv / ws_blocks bytes
+ *                  each; ws_blocks >= the blocks any call of the sequence sees,
+ *                  e.g. max_tiles + ceil(win_capacity / 128), and the same for
+ *                  every call of the sequence.
+ *   cached_tiles : leading tiles whose images ws already holds: 0 on the first
+ *                  call, then the n_tiles of the previous call, provided that
+ *                  call's chunk was the last one appended (it then saw every
+ *                  tile), and that tiles, tile_table, layout and ws_blocks
+ *                  are unchanged. 0 <= cached_tiles <= n_tiles. Images of tiles
+ *                  [cached_tiles, n_tiles) and of the window blocks are built.
+ * Returns KVARN_ERR_BAD_ARG for ws_blocks <= 0, KVARN_ERR_WORKSPACE when
+ * ws_blocks is smaller than the blocks this chunk sees or ws_bytes smaller
+ * than ws_blocks * Hkv images; otherwise as kvarn_prefill_attention.
+ */
+int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                                   const int64_t* tile_table, int table_stride, int n_tiles,
+                                   const float* win_k, const float* win_v, int win_start,
+                                   int win_len, int win_capacity, int Hq, int Hkv, int head_dim,
+                                   float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                                   size_t ws_bytes, int ws_blocks, int cached_tiles, float* out,
+                                   kvarn_stream_t stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory. The pages
  * have no counterpart to this entry point; it exists for embedders that may
  * not call cudaMalloc where attention runs (code inside another runtime's

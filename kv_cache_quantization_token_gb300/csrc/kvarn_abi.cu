@@ -256,12 +256,12 @@ int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_di
   return KVARN_OK;
 }
 
-int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                            const int64_t* tile_table, int table_stride, int n_tiles,
-                            const float* win_k, const float* win_v, int win_start, int win_len,
-                            int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
-                            const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
-                            kvarn_stream_t stream) {
+static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                          const int64_t* tile_table, int table_stride, int n_tiles,
+                          const float* win_k, const float* win_v, int win_start, int win_len,
+                          int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
+                          const kvarn_layout_t* layout, void* ws, size_t ws_bytes, int ws_blocks,
+                          int cached_tiles, float* out, kvarn_stream_t stream) {
   if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
@@ -271,13 +271,16 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
       table_stride < n_tiles || win_len > win_capacity)
     return KVARN_ERR_BAD_ARG;
   if (pos0 + C > (int64_t)KVARN_TILE_TOKENS * n_tiles + win_len) return KVARN_ERR_BAD_ARG;
+  if (cached_tiles < 0 || cached_tiles > n_tiles || ws_blocks < 0) return KVARN_ERR_BAD_ARG;
   if (C == 0) return KVARN_OK;
   if (!q_chunk || !out) return KVARN_ERR_NULL;
   if (n_tiles > 0 && (!tiles || !tile_table)) return KVARN_ERR_NULL;
   if (win_len > 0 && (!win_k || !win_v)) return KVARN_ERR_NULL;
   int n_tblk = 0, n_blk = 0;
   kvarn::prefill_blocks(pos0, C, n_tiles, win_len, &n_tblk, &n_blk);
-  const size_t need = (size_t)n_blk * (size_t)Hkv * kvarn::prefill_block_bytes(head_dim);
+  const int stride = ws_blocks > 0 ? ws_blocks : n_blk;
+  if (stride < n_blk) return KVARN_ERR_WORKSPACE;
+  const size_t need = (size_t)stride * (size_t)Hkv * kvarn::prefill_block_bytes(head_dim);
   if (need > 0 && !ws) return KVARN_ERR_NULL;
   if (ws_bytes < need) return KVARN_ERR_WORKSPACE;
   if (!aligned16(q_chunk) || !aligned16(out) || (n_tiles > 0 && !aligned16(tiles)) ||
@@ -288,7 +291,31 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
   return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
                                          n_tiles, win_k, win_v, win_start, win_len, win_capacity,
                                          Hq, Hkv, head_dim, softmax_scale, scale_bytes_of(layout),
-                                         ws, out, (cudaStream_t)stream));
+                                         ws, stride, cached_tiles, out, (cudaStream_t)stream));
+}
+
+int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                            const int64_t* tile_table, int table_stride, int n_tiles,
+                            const float* win_k, const float* win_v, int win_start, int win_len,
+                            int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
+                            const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
+                            kvarn_stream_t stream) {
+  return prefill_common(q_chunk, C, pos0, tiles, tile_table, table_stride, n_tiles, win_k, win_v,
+                        win_start, win_len, win_capacity, Hq, Hkv, head_dim, softmax_scale, layout,
+                        ws, ws_bytes, 0, 0, out, stream);
+}
+
+int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
+                                   const int64_t* tile_table, int table_stride, int n_tiles,
+                                   const float* win_k, const float* win_v, int win_start,
+                                   int win_len, int win_capacity, int Hq, int Hkv, int head_dim,
+                                   float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                                   size_t ws_bytes, int ws_blocks, int cached_tiles, float* out,
+                                   kvarn_stream_t stream) {
+  if (ws_blocks <= 0) return KVARN_ERR_BAD_ARG;
+  return prefill_common(q_chunk, C, pos0, tiles, tile_table, table_stride, n_tiles, win_k, win_v,
+                        win_start, win_len, win_capacity, Hq, Hkv, head_dim, softmax_scale, layout,
+                        ws, ws_bytes, ws_blocks, cached_tiles, out, stream);
 }
 
 int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,

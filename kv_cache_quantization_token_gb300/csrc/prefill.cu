@@ -269,11 +269,13 @@ struct PrefillArgs {
   const int64_t* tile_table;  // [Hkv][table_stride]
   const float* win_k;
   const float* win_v;
-  uint8_t* ws;                // [Hkv][n_blk] block images
+  uint8_t* ws;                // [Hkv][ws_stride] block images
   float* out;
   int64_t pos0;
   int C, Hq, Hkv, G, n_tiles, table_stride, win_start, win_len, win_cap;
   int n_tblk, n_blk;          // tiles, and tiles + window blocks, visible to the chunk
+  int ws_stride;              // block images per KV head in ws (>= n_blk)
+  int first_blk;              // first block whose image this call builds (earlier tiles' are kept)
   float qscale;               // softmax_scale * log2(e)
 };
 
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
   unsigned char* sKl = sKh + P::OPB;
   unsigned char* sV = sKl + P::OPB;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::DQ_OFF_BAR);
-  const int j = blockIdx.x, kvh = blockIdx.y;
+  const int j = a.first_blk + blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, row = tid & 127, half = tid >> 7;
   bool poison = false;
   if (j < a.n_tblk) {
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   if (tid == 0)
-    bulk_store_wait(a.ws + ((int64_t)kvh * a.n_blk + j) * P::BLK, sKh, P::BLK);
+    bulk_store_wait(a.ws + ((int64_t)kvh * a.ws_stride + j) * P::BLK, sKh, P::BLK);
 }
 
 // ---------------------------------------------------------------------------
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   const int n_blk = n_tile_blk + n_win_blk;
   auto image = [&](int jj) -> const uint8_t* {  // workspace image of this CTA's block jj
     const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
-    return a.ws + ((int64_t)kvh * a.n_blk + widx) * P::BLK;
+    return a.ws + ((int64_t)kvh * a.ws_stride + widx) * P::BLK;
   };
 
   if (tid == 0) {
@@ -787,8 +789,8 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  if (a.n_blk > 0) {
-    prefill_dequant_kernel<D, SB><<<dim3(a.n_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
+  if (a.n_blk > a.first_blk) {
+    prefill_dequant_kernel<D, SB><<<dim3(a.n_blk - a.first_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -819,7 +821,8 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           int scale_bytes, void* ws, float* out, cudaStream_t st) {
+                           int scale_bytes, void* ws, int ws_blocks, int cached_tiles, float* out,
+                           cudaStream_t st) {
   PrefillArgs a;
   a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
   a.ws = reinterpret_cast<uint8_t*>(ws);
@@ -827,6 +830,8 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
   a.n_tiles = n_tiles; a.table_stride = table_stride; a.win_start = win_start;
   a.win_len = win_len; a.win_cap = win_capacity; a.qscale = softmax_scale * kLog2e;
   prefill_blocks(pos0, C, n_tiles, win_len, &a.n_tblk, &a.n_blk);
+  a.ws_stride = ws_blocks > 0 ? ws_blocks : a.n_blk;
+  a.first_blk = cached_tiles < a.n_tblk ? cached_tiles : a.n_tblk;
   const int key = 10 * D + scale_bytes;
   switch (key) {
     case 644: return launch_prefill_d<64, 4>(a, st);

@@ -76,6 +76,10 @@ def _L():
                                                 c_int, c_int, c_int, c_int, c_int, c_int,
                                                 ctypes.c_float, ctypes.POINTER(Layout), vp, sz, vp,
                                                 vp]
+        lib.kvarn_prefill_attention_cached.argtypes = [vp, c_int, i64, vp, vp, c_int, c_int, vp, vp,
+                                                       c_int, c_int, c_int, c_int, c_int, c_int,
+                                                       ctypes.c_float, ctypes.POINTER(Layout), vp, sz,
+                                                       c_int, c_int, vp, vp]
         lib.kvarn_prefill_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, ctypes.POINTER(sz)]
         lib.kvarn_set_launch_flags.argtypes = [ctypes.c_uint]
         lib.kvarn_get_launch_flags.argtypes = []
@@ -84,7 +88,7 @@ def _L():
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
                      "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
                      "kvarn_window_advance", "kvarn_prefill_attention", "kvarn_set_launch_flags",
-                     "kvarn_prefill_workspace_bytes"):
+                     "kvarn_prefill_workspace_bytes", "kvarn_prefill_attention_cached"):
             getattr(lib, name).restype = c_int
         _lib = lib
     return _lib
@@ -254,11 +258,15 @@ def prefill_workspace_bytes(n_tiles, win_len, Hkv, head_dim) -> int:
 
 
 def prefill_attention(q_chunk, pos0, tiles, tile_table, n_tiles, win_k, win_v, win_start,
-                      win_len, lay: Layout, softmax_scale=None, ws=None, out=None, stream=None):
+                      win_len, lay: Layout, softmax_scale=None, ws=None, out=None, stream=None,
+                      ws_blocks=None, cached_tiles=0):
     """Causal attention of a chunk of one sequence: q_chunk fp32 [C][Hq][D] at
     positions pos0 + i; tile_table int64 [Hkv][stride]; win_k/v fp32
     [Hkv][cap][D]; n_tiles, win_start, win_len host ints; ws a uint8 device
-    workspace of prefill_workspace_bytes() (allocated here when None)."""
+    workspace of prefill_workspace_bytes() (allocated here when None). With
+    ws_blocks (images per KV head of a ws kept for the whole prompt), the call
+    goes through kvarn_prefill_attention_cached and converts only the tiles
+    from cached_tiles on."""
     _dev(q_chunk, "q_chunk", torch.float32)
     C, Hq, D = q_chunk.shape
     _dev(tile_table, "tile_table", torch.int64)
@@ -271,6 +279,14 @@ def prefill_attention(q_chunk, pos0, tiles, tile_table, n_tiles, win_k, win_v, w
     if ws is None:
         need = prefill_workspace_bytes(n_tiles, win_len, Hkv, D)
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q_chunk.device)
+    if ws_blocks is not None:
+        _check("kvarn_prefill_attention_cached",
+               _L().kvarn_prefill_attention_cached(
+                   _ptr(q_chunk), C, int(pos0), _ptr(tiles), _ptr(tile_table), stride, int(n_tiles),
+                   _ptr(win_k), _ptr(win_v), int(win_start), int(win_len), cap, Hq, Hkv, D,
+                   float(softmax_scale), ctypes.byref(lay), _ptr(ws), ws.numel(), int(ws_blocks),
+                   int(cached_tiles), _ptr(out), _stream(stream)))
+        return out
     _check("kvarn_prefill_attention",
            _L().kvarn_prefill_attention(_ptr(q_chunk), C, int(pos0), _ptr(tiles), _ptr(tile_table),
                                         stride, int(n_tiles), _ptr(win_k), _ptr(win_v),

@@ -195,7 +195,7 @@ class PrefillRun:
     oracle can be evaluated on the same state."""
 
     def __init__(self, workload, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
-                 dev="cuda:0", scale=None, scale_bits=32):
+                 dev="cuda:0", scale=None, scale_bits=32, cached=False):
         dev = torch.device(dev)
         self.Hq, self.Hkv, self.D, self.W = Hq, Hkv, D, W
         self.k, self.v = synth.kv_layer(workload, layer, Hkv, n_tokens, D)
@@ -212,6 +212,12 @@ class PrefillRun:
         win_v = torch.zeros_like(win_k)
         start, length, n_tiles = 0, 0, 0
         self.snap = {}
+        # cached: one workspace for the whole prompt; each chunk converts only
+        # the tiles promoted since the previous chunk
+        ws_blocks = max_tiles + cap // TILE
+        ws = (torch.empty(kvarn.prefill_workspace_bytes(max_tiles, cap, Hkv, D), dtype=torch.uint8,
+                          device=dev) if cached else None)
+        prev_tiles = 0
         keep = set(keep if keep is not None else range(0, n_tokens, chunk))
         for pos0 in range(0, n_tokens, chunk):
             C = min(chunk, n_tokens - pos0)
@@ -230,9 +236,15 @@ class PrefillRun:
                 n_tiles += 1
                 start = (start + TILE) % cap
                 length -= TILE
-            out = kvarn.prefill_attention(torch.from_numpy(self.q[pos0:pos0 + C]).to(dev), pos0,
-                                          self.tiles, self.table, n_tiles, win_k[0], win_v[0],
-                                          start, length, self.lay, softmax_scale=scale)
+            qc = torch.from_numpy(self.q[pos0:pos0 + C]).to(dev)
+            if cached:
+                out = kvarn.prefill_attention(qc, pos0, self.tiles, self.table, n_tiles, win_k[0],
+                                              win_v[0], start, length, self.lay, softmax_scale=scale,
+                                              ws=ws, ws_blocks=ws_blocks, cached_tiles=prev_tiles)
+                prev_tiles = n_tiles
+            else:
+                out = kvarn.prefill_attention(qc, pos0, self.tiles, self.table, n_tiles, win_k[0],
+                                              win_v[0], start, length, self.lay, softmax_scale=scale)
             if pos0 in keep:
                 self.snap[pos0] = dict(C=C, n_tiles=n_tiles, start=start, length=length,
                                        win_k=win_k[0].cpu().numpy(), win_v=win_v[0].cpu().numpy(),

@@ -69,3 +69,20 @@ def test_prefill_f16_scale_records(Hq, Hkv, D, n, chunk, W):
     run = PrefillRun("qwen3_8b_decode", 5, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk, scale_bits=16)
     for p in run.snap:
         run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=19))
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W,sb", [(32, 8, 128, 2188, 512, 256, 32),
+                                                  (12, 4, 64, 650, 200, 128, 32),
+                                                  (16, 2, 128, 900, 300, 256, 16)])
+def test_prefill_cached_images_match_uncached(Hq, Hkv, D, n, chunk, W, sb):
+    """kvarn_prefill_attention_cached with one workspace for the whole prompt
+    (each chunk converts only the newly promoted tiles) gives the same bits as
+    converting every visible tile in every chunk, and matches the oracle."""
+    a = PrefillRun("qwen3_8b_prefill", 6, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk, scale_bits=sb)
+    b = PrefillRun("qwen3_8b_prefill", 6, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk, scale_bits=sb,
+                   cached=True)
+    assert a.snap.keys() == b.snap.keys()
+    for p in a.snap:
+        np.testing.assert_array_equal(a.snap[p]["out"], b.snap[p]["out"])
+    last = max(b.snap)
+    b.check(last, _rows(b.snap[last]["C"], range(0, Hq, 5), step=29))
