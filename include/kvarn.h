@@ -375,7 +375,9 @@ int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, co
  * holds that array until the process exits.
  *  - Returns KVARN_ERR_WORKSPACE (nothing enqueued) when
  *    kvarn_decode_workspace_bytes() for these sizes exceeds the array; with
- *    head_dim 128 and GQA 4 that is about B * 2,000 tiles.
+ *    head_dim 128, 32 query and 8 KV heads that allows about
+ *    B * max_tiles <= 16,000 on a 152-SM GB300 (the split plan, and with it
+ *    the workspace size, depends on the device's SM count).
  *  - The first call on a device (that device current) looks up the array's
  *    device address with cudaGetSymbolAddress and caches it; make that first
  *    call before any stream capture. It never calls cudaMalloc or cudaFree.
