@@ -289,7 +289,7 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
   if (lane == 0) qmax[h] = mx;
 }
 
-template <int D, int GP, int NW_, int WPT_>
+template <int D, int GP, int NW_, int WPT_, bool MR_ = false>
 struct DC {
   static constexpr int NW = NW_;                                // warps per CTA (2, 4 or 8)
   static constexpr int NTHR = 32 * NW;
@@ -306,8 +306,9 @@ struct DC {
   static constexpr int NCB = D / 16;                            // 16-channel blocks
   static constexpr int HB = NCB / WPT;                          // blocks whose B fragments a warp builds
   static constexpr int NS = D / 64;                             // 64-channel slices of a V row
-  // window rows staged per warp (sized by the fp32 record, whatever the scale width)
-  static constexpr int WCH0 = (TPS * Rec<D, 4>::kBytes) / (NW * 2 * D * 4);
+  // window rows staged per warp, sized by the record region of the fp32
+  // layout (two slots per group with multi-round items), whatever the scale width
+  static constexpr int WCH0 = ((MR_ ? 2 : 1) * TPS * Rec<D, 4>::kBytes) / (NW * 2 * D * 4);
   static constexpr int WCH = WCH0 >= 16 ? 16 : WCH0 >= 8 ? 8 : WCH0 >= 4 ? 4 : 2;
   static constexpr int DP = D + 8;                              // padded channel stride of the merge
   static constexpr int MRG = NW * GP * DP * 4;                  // merge region [NW][GP][DP], over records
@@ -391,7 +392,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     int rounds_arg, float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
-  using C = DC<D, GP, NW_, WPT_>;
+  using C = DC<D, GP, NW_, WPT_, MR>;
   using R = Rec<D, kSB>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
   constexpr int HB = C::HB, WPT = C::WPT, CH = C::CH;
@@ -1169,7 +1170,7 @@ cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
 template <int D, int GP, int NW, int WPT, bool MR>
 cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_ml, float* ws_acc,
                            cudaStream_t st) {
-  using C = DC<D, GP, NW, WPT>;
+  using C = DC<D, GP, NW, WPT, MR>;
   constexpr int kMaxSmem = C::smem_bytes(MR ? 2 * C::TPS : C::TPS) + 1024;
   static bool configured[64] = {};
   int dev = 0;
@@ -1267,25 +1268,31 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
   const int64_t total = (int64_t)B * Hkv * max_tiles;
   const int64_t per_sm = total / sm_count();
   const int wpt = D <= 128 ? 2 : 4;
-  int tps, rounds = 1;
-  if (D <= 128) {
-    tps = per_sm > 8 ? 2 : total >= 4LL * sm_count() ? 4 : 2;
-    if (per_sm > 8) rounds = (int)std::min<int64_t>(8, std::max<int64_t>(2, per_sm / 6));
-  } else {
-    tps = 1;
-    if (per_sm >= 12) rounds = (int)std::min<int64_t>(8, per_sm / 3);
-  }
+  const bool multi = D <= 128 ? per_sm > 8 : per_sm >= 12;
+  const int tps = D <= 128 ? (multi ? 2 : total >= 4LL * sm_count() ? 4 : 2) : 1;
   const int nw = wpt * tps;
+  // window rows per warp and per item, as DC<D, GP, NW, WPT, MR>::WCH and its NW warps
+  const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
+  const int w0 = ((multi ? 2 : 1) * tps * rb) / (nw * 2 * D * 4);
+  const int wch = w0 >= 16 ? 16 : w0 >= 8 ? 8 : w0 >= 4 ? 4 : 2;
+  p->win_items = win_capacity > 0 ? (win_capacity + nw * wch - 1) / (nw * wch) : 0;
+  // rounds: the fewest (2..8) whose grid fits one wave of the multi-round
+  // kernel's resident CTAs (3 per SM, by shared memory), so that no second,
+  // partial wave runs after the first; 8 when even that does not fit (many
+  // waves: the last one matters little).
+  int rounds = 1;
+  if (multi) {
+    const int64_t groups = (int64_t)B * Hkv, slots = 3LL * sm_count();
+    for (rounds = 2; rounds < 8; ++rounds) {
+      const int64_t ctas = groups * ((max_tiles + tps * rounds - 1) / (tps * rounds) + p->win_items);
+      if (ctas <= slots) break;
+    }
+  }
   p->tiles_per_round = tps;
   p->rounds = rounds;
   p->tiles_per_item = tps * rounds;
   p->warps_per_tile = wpt;
   p->tile_items = max_tiles > 0 ? (max_tiles + p->tiles_per_item - 1) / p->tiles_per_item : 0;
-  // window rows per warp and per item, as DC<D, GP, NW, WPT>::WCH and its NW warps
-  const int rb = 112 * D + 1024 + 1024 * (D > 128 ? D / 128 : 1);
-  const int w0 = (tps * rb) / (nw * 2 * D * 4);
-  const int wch = w0 >= 16 ? 16 : w0 >= 8 ? 8 : w0 >= 4 ? 4 : 2;
-  p->win_items = win_capacity > 0 ? (win_capacity + nw * wch - 1) / (nw * wch) : 0;
   p->items = p->tile_items + p->win_items;
   const size_t parts = (size_t)B * Hq * p->items;
   const size_t ml = (parts * 2 * sizeof(float) + 255) / 256 * 256;
