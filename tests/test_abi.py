@@ -113,3 +113,35 @@ def test_launch_flags_validation():
     assert kvarn.get_launch_flags() == 3
     kvarn.set_launch_flags(0)
     assert kvarn.get_launch_flags() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_f16_scale_layout_agrees_with_oracle(lib, D):
+    L = kvarn.layout(D, scale_bits=16)
+    assert L.version == 2 and L.record_bytes == oracle.record_bytes(D, 16)
+    assert L.record_bytes % 128 == 0 and L.off_k_delta == 96 * D
+    assert L.off_k_lo - L.off_k_delta == 2 * D and L.off_v_s + 2 * D == L.record_bytes
+    assert (L.k_bits, L.v_bits) == (4, 2)
+    M = kvarn.Layout()
+    assert lib.kvarn_layout_scales(D, 4, 8, ctypes.byref(M)) == -3
+    assert lib.kvarn_layout_scales(D, 4, 32, ctypes.byref(M)) == 0 and M.version == 1
+    # a layout claiming f16 scales with fp32 offsets is not one the library made
+    M.version = 2
+    p = ctypes.c_void_p(16)
+    assert lib.kvarn_compress_tile(p, p, D, 256, p, p, p, 1, ctypes.byref(M), None) == -3
+
+
+def test_prefill_cached_host_validation(lib):
+    L = kvarn.layout(128)
+    p = ctypes.c_void_p(4096)
+    blk = 3 * 128 * 128 * 2
+    f = lib.kvarn_prefill_attention_cached
+    f.argtypes = None
+    args = lambda wsb, wsblocks, cached, nt=10: (
+        p, 512, 1000, p, p, 64, nt, p, p, 0, 300, 768, 32, 8, 128, ctypes.c_float(0.088),
+        ctypes.byref(L), p, ctypes.c_size_t(wsb), wsblocks, cached, p, None)
+    assert f(*args(1 << 40, 0, 0)) == -4           # ws_blocks must be positive
+    assert f(*args(1 << 40, 11, 0)) == -5          # fewer images per head than the 12 blocks seen
+    assert f(*args(16 * 8 * blk - 1, 16, 0)) == -5  # workspace smaller than ws_blocks images
+    assert f(*args(1 << 40, 16, 11)) == -4         # more cached tiles than tiles
+    assert f(*args(1 << 40, 16, -1)) == -4
