@@ -77,13 +77,13 @@ def _L():
                 lib.orc_unpack_record.argtypes = [c_int, _u8p, _u8p, _u8p] + [_dp] * 8
                 lib.orc_compress_unit.argtypes = [_fp, _fp, i64, c_int, c_int, _u8p] + [_dp] * 10
                 lib.orc_dequant_record.argtypes = [c_int, _u8p, _dp, _dp]
-                lib.orc_record_bytes_sw.restype = i64
-                lib.orc_record_bytes_sw.argtypes = [c_int, c_int]
-                lib.orc_pack_record_sw.argtypes = [c_int, c_int, _u8p, _u8p] + [_dp] * 8 + [_u8p]
-                lib.orc_unpack_record_sw.argtypes = [c_int, c_int, _u8p, _u8p, _u8p] + [_dp] * 8
-                lib.orc_compress_unit_sw.argtypes = ([_fp, _fp, i64, c_int, c_int, c_int, _u8p]
-                                                     + [_dp] * 10)
-                lib.orc_dequant_record_sw.argtypes = [c_int, c_int, _u8p, _dp, _dp]
+                lib.orc_record_bytes_fmt.restype = i64
+                lib.orc_record_bytes_fmt.argtypes = [c_int, c_int, c_int]
+                lib.orc_pack_record_fmt.argtypes = [c_int, c_int, c_int, _u8p, _u8p] + [_dp] * 8 + [_u8p]
+                lib.orc_unpack_record_fmt.argtypes = [c_int, c_int, c_int, _u8p, _u8p, _u8p] + [_dp] * 8
+                lib.orc_compress_unit_fmt.argtypes = ([_fp, _fp, i64, c_int, c_int, c_int, c_int, _u8p]
+                                                      + [_dp] * 10)
+                lib.orc_dequant_record_fmt.argtypes = [c_int, c_int, c_int, _u8p, _dp, _dp]
                 lib.orc_f64_to_f16_bits.restype = ctypes.c_uint16
                 lib.orc_f64_to_f16_bits.argtypes = [ctypes.c_double]
                 lib.orc_f16_bits_to_f64.restype = ctypes.c_double
@@ -163,6 +163,8 @@ def quantize_tensor(x: np.ndarray, per_channel: bool, bits: int, iters: int = DE
 # --------------------------------------------------------------------------
 # c4 -- packed record. scale_bits = 32: the default layout (fp32 scales);
 # 16: the f16-scale layout (SharpInference issue #433, item 3), same codes.
+# v_bits = 2: the method's k4v2 preset; 4: a k4v4 variant (other K/V bit
+# widths, SharpInference issue #433 / PR #434 scope notes), same packing rule.
 def _sw(scale_bits: int) -> int:
     if scale_bits not in (16, 32):
         raise ValueError(f"scale_bits must be 16 or 32, not {scale_bits}")
@@ -178,26 +180,33 @@ def f16_value(bits: int) -> float:
     return float(_L().orc_f16_bits_to_f64(int(bits)))
 
 
-def record_bytes(D: int, scale_bits: int = 32) -> int:
-    n = _L().orc_record_bytes_sw(D, _sw(scale_bits))
+def _vb(v_bits: int) -> int:
+    if v_bits not in (2, 4):
+        raise ValueError(f"v_bits must be 2 or 4, not {v_bits}")
+    return v_bits
+
+
+def record_bytes(D: int, scale_bits: int = 32, v_bits: int = 2) -> int:
+    n = _L().orc_record_bytes_fmt(D, _sw(scale_bits), _vb(v_bits))
     if n < 0:
         raise ValueError(f"unsupported head_dim {D}")
     return int(n)
 
 
 def pack_record(D, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s,
-                scale_bits: int = 32):
-    rec = np.empty(record_bytes(D, scale_bits), np.uint8)
+                scale_bits: int = 32, v_bits: int = 2):
+    rec = np.empty(record_bytes(D, scale_bits, v_bits), np.uint8)
     args = [np.ascontiguousarray(a, dtype=np.float64) for a in
             (k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s)]
     kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
     vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
-    _check(_L().orc_pack_record_sw(D, _sw(scale_bits), _ptr(kc, _u8p), _ptr(vc, _u8p),
-                                   *[_ptr(a, _dp) for a in args], _ptr(rec, _u8p)), "pack")
+    _check(_L().orc_pack_record_fmt(D, _sw(scale_bits), _vb(v_bits), _ptr(kc, _u8p),
+                                    _ptr(vc, _u8p), *[_ptr(a, _dp) for a in args],
+                                    _ptr(rec, _u8p)), "pack")
     return rec
 
 
-def unpack_record(rec: np.ndarray, D: int, scale_bits: int = 32) -> dict:
+def unpack_record(rec: np.ndarray, D: int, scale_bits: int = 32, v_bits: int = 2) -> dict:
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     gv = D // min(D, 128)
     out = dict(k_codes=np.empty((TILE, D), np.uint8), v_codes=np.empty((TILE, D), np.uint8),
@@ -205,14 +214,14 @@ def unpack_record(rec: np.ndarray, D: int, scale_bits: int = 32) -> dict:
                v_delta=np.empty(TILE * gv), v_lo=np.empty(TILE * gv), v_r=np.empty(TILE),
                v_s=np.empty(D))
     names = ("k_delta", "k_lo", "k_s", "k_r", "v_delta", "v_lo", "v_r", "v_s")
-    _check(_L().orc_unpack_record_sw(D, _sw(scale_bits), _ptr(rec, _u8p),
-                                     _ptr(out["k_codes"], _u8p), _ptr(out["v_codes"], _u8p),
-                                     *[_ptr(out[n], _dp) for n in names]), "unpack")
+    _check(_L().orc_unpack_record_fmt(D, _sw(scale_bits), _vb(v_bits), _ptr(rec, _u8p),
+                                      _ptr(out["k_codes"], _u8p), _ptr(out["v_codes"], _u8p),
+                                      *[_ptr(out[n], _dp) for n in names]), "unpack")
     return out
 
 
 def compress_unit(k: np.ndarray, v: np.ndarray, iters: int = DEFAULT_ITERS,
-                  scale_bits: int = 32) -> dict:
+                  scale_bits: int = 32, v_bits: int = 2) -> dict:
     """Compress one (tile, KV head): k, v fp32 [128][D]. Returns the record
     bytes plus fp64 scales and pre-rounding values for the parity checks."""
     k = np.ascontiguousarray(k, dtype=np.float32)
@@ -220,25 +229,25 @@ def compress_unit(k: np.ndarray, v: np.ndarray, iters: int = DEFAULT_ITERS,
     T, D = k.shape
     assert T == TILE and v.shape == k.shape
     gv = D // min(D, 128)
-    o = dict(record=np.empty(record_bytes(D, scale_bits), np.uint8),
+    o = dict(record=np.empty(record_bytes(D, scale_bits, v_bits), np.uint8),
              k_s=np.empty(D), k_r=np.empty(T), k_delta=np.empty(D), k_lo=np.empty(D),
              k_vpre=np.empty((T, D)), v_s=np.empty(D), v_r=np.empty(T),
              v_delta=np.empty(T * gv), v_lo=np.empty(T * gv), v_vpre=np.empty((T, D)))
     names = ("k_s", "k_r", "k_delta", "k_lo", "k_vpre", "v_s", "v_r", "v_delta", "v_lo", "v_vpre")
-    _check(_L().orc_compress_unit_sw(_ptr(k, _fp), _ptr(v, _fp), D, D, iters, _sw(scale_bits),
-                                     _ptr(o["record"], _u8p), *[_ptr(o[n], _dp) for n in names]),
-           "compress")
+    _check(_L().orc_compress_unit_fmt(_ptr(k, _fp), _ptr(v, _fp), D, D, iters, _sw(scale_bits),
+                                      _vb(v_bits), _ptr(o["record"], _u8p),
+                                      *[_ptr(o[n], _dp) for n in names]), "compress")
     return o
 
 
 # --------------------------------------------------------------------------
 # c5 -- reconstruction
-def dequant_record(rec: np.ndarray, D: int, scale_bits: int = 32):
+def dequant_record(rec: np.ndarray, D: int, scale_bits: int = 32, v_bits: int = 2):
     """Unrotated fp64 K and V rows ([128][D] each) of one record."""
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     k, v = np.empty((TILE, D)), np.empty((TILE, D))
-    _check(_L().orc_dequant_record_sw(D, _sw(scale_bits), _ptr(rec, _u8p), _ptr(k, _dp),
-                                      _ptr(v, _dp)), "dequant")
+    _check(_L().orc_dequant_record_fmt(D, _sw(scale_bits), _vb(v_bits), _ptr(rec, _u8p),
+                                       _ptr(k, _dp), _ptr(v, _dp)), "dequant")
     return k, v
 
 
@@ -266,14 +275,14 @@ def window_rows(win: np.ndarray, start: int, length: int) -> np.ndarray:
 
 
 def kv_head_tokens(pool: np.ndarray, table_row, n_tiles: int, win_k, win_v, start, length, D,
-                   scale_bits: int = 32):
+                   scale_bits: int = 32, v_bits: int = 2):
     """All cached (k, v) rows of one KV head, in position order: the tiles'
     reconstructed rows, then the window's raw rows."""
     ks, vs = [], []
-    rb = record_bytes(D, scale_bits)
+    rb = record_bytes(D, scale_bits, v_bits)
     for i in range(n_tiles):
         off = int(table_row[i])
-        k, v = dequant_record(pool[off:off + rb], D, scale_bits)
+        k, v = dequant_record(pool[off:off + rb], D, scale_bits, v_bits)
         ks.append(k)
         vs.append(v)
     ks.append(window_rows(win_k, start, length))
@@ -282,7 +291,7 @@ def kv_head_tokens(pool: np.ndarray, table_row, n_tiles: int, win_k, win_v, star
 
 
 def decode_attention(q, pool, tile_table, n_tiles, win_k, win_v, win_start, win_len, scale,
-                     heads=None, scale_bits: int = 32):
+                     heads=None, scale_bits: int = 32, v_bits: int = 2):
     """Exact decode attention (c7) for every (b, h) in `heads` (default: all).
     q [B][Hq][D]; tile_table [B][Hkv][max_tiles]; win_k/v [B][Hkv][Wcap][D].
     Returns {(b, h): out[D]} in fp64."""
@@ -298,14 +307,14 @@ def decode_attention(q, pool, tile_table, n_tiles, win_k, win_v, win_start, win_
         if (b, kvh) not in cache:
             cache[(b, kvh)] = kv_head_tokens(pool, tile_table[b, kvh], int(n_tiles[b]),
                                              win_k[b, kvh], win_v[b, kvh], int(win_start[b]),
-                                             int(win_len[b]), D, scale_bits)
+                                             int(win_len[b]), D, scale_bits, v_bits)
         keys, values = cache[(b, kvh)]
         res[(b, h)] = attend(q[b, h], keys, values, scale)
     return res
 
 
 def prefill_attention(q_chunk, pos0, pool, table, n_tiles, win_k, win_v, win_start, win_len,
-                      scale, rows=None, scale_bits: int = 32):
+                      scale, rows=None, scale_bits: int = 32, v_bits: int = 2):
     """Exact causal attention (c8) of a chunk of queries of ONE sequence.
     q_chunk [C][Hq][D] at positions pos0 + i; tokens of tile k sit at positions
     [128k, 128k+128), window token j at 128*n_tiles + j; query i sees positions
@@ -322,7 +331,7 @@ def prefill_attention(q_chunk, pos0, pool, table, n_tiles, win_k, win_v, win_sta
         kvh = h // G
         if kvh not in cache:
             cache[kvh] = kv_head_tokens(pool, table[kvh], int(n_tiles), win_k[kvh], win_v[kvh],
-                                        int(win_start), int(win_len), D, scale_bits)
+                                        int(win_start), int(win_len), D, scale_bits, v_bits)
         keys, values = cache[kvh]
         visible = pos0 + i + 1
         res[(i, h)] = attend(q_chunk[i, h], keys[:visible], values[:visible], scale)

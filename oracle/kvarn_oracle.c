@@ -218,16 +218,20 @@ int orc_quantize_tensor(const float* x, int64_t row_stride, int D, int iters, in
  */
 typedef struct {
   int64_t bytes, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s;
-  int gv, sw;
+  int gv, sw, vb;
 } orc_layout;
 
-static orc_layout orc_record_layout(int D, int sw) {
+/* vb: V code width, 2 (the method's k4v2 preset) or 4 (a k4v4 variant with
+ * the same token-major packing: channel c of token t in the (c % (8/vb))-th
+ * vb-bit field of byte t * (D vb / 8) + c / (8/vb)). */
+static orc_layout orc_record_layout(int D, int sw, int vb) {
   orc_layout L;
   L.gv = D / (D < 128 ? D : 128);
   L.sw = sw;
+  L.vb = vb;
   L.k_codes = 0;
   L.v_codes = L.k_codes + (int64_t)D * (ORC_T / 2);     /* 4-bit K codes        */
-  L.k_delta = L.v_codes + (int64_t)ORC_T * (D / 4);     /* 2-bit V codes        */
+  L.k_delta = L.v_codes + (int64_t)ORC_T * (D * vb / 8); /* vb-bit V codes      */
   L.k_lo = L.k_delta + (int64_t)sw * D;
   L.k_s = L.k_lo + (int64_t)sw * D;
   L.k_r = L.k_s + (int64_t)sw * D;
@@ -240,11 +244,15 @@ static orc_layout orc_record_layout(int D, int sw) {
 }
 
 static int orc_sw_ok(int sw) { return sw == 4 || sw == 2; }
-
-int64_t orc_record_bytes_sw(int D, int sw) {
-  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
-  return orc_record_layout(D, sw).bytes;
+static int orc_fmt_ok(int D, int sw, int vb) {
+  return orc_pow2_dim(D) && D >= 4 && orc_sw_ok(sw) && (vb == 2 || vb == 4);
 }
+
+int64_t orc_record_bytes_fmt(int D, int sw, int vb) {
+  if (!orc_fmt_ok(D, sw, vb)) return -3;
+  return orc_record_layout(D, sw, vb).bytes;
+}
+int64_t orc_record_bytes_sw(int D, int sw) { return orc_record_bytes_fmt(D, sw, 2); }
 int64_t orc_record_bytes(int D) { return orc_record_bytes_sw(D, 4); }
 
 /* IEEE binary16 encoding of v, rounded to nearest with ties to even, from the
@@ -299,12 +307,13 @@ static double orc_get_scale(const uint8_t* src, int sw) {
 
 /* Writes the record from unpacked codes ([128][D], one per byte) and fp64
  * scales, which are stored rounded to the layout's scale format. */
-int orc_pack_record_sw(int D, int sw, const uint8_t* k_codes, const uint8_t* v_codes,
-                       const double* k_delta, const double* k_lo, const double* k_s,
-                       const double* k_r, const double* v_delta, const double* v_lo,
-                       const double* v_r, const double* v_s, uint8_t* rec) {
-  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
-  const orc_layout L = orc_record_layout(D, sw);
+int orc_pack_record_fmt(int D, int sw, int vb, const uint8_t* k_codes, const uint8_t* v_codes,
+                        const double* k_delta, const double* k_lo, const double* k_s,
+                        const double* k_r, const double* v_delta, const double* v_lo,
+                        const double* v_r, const double* v_s, uint8_t* rec) {
+  if (!orc_fmt_ok(D, sw, vb)) return -3;
+  const orc_layout L = orc_record_layout(D, sw, vb);
+  const int per = 8 / vb;                                /* V codes per byte */
   memset(rec, 0, (size_t)L.bytes);
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t) {
@@ -313,8 +322,8 @@ int orc_pack_record_sw(int D, int sw, const uint8_t* k_codes, const uint8_t* v_c
     }
   for (int t = 0; t < ORC_T; ++t)
     for (int c = 0; c < D; ++c) {
-      const uint8_t code = v_codes[(int64_t)t * D + c] & 0x3;
-      rec[L.v_codes + (int64_t)t * (D / 4) + c / 4] |= (uint8_t)(code << (2 * (c % 4)));
+      const uint8_t code = v_codes[(int64_t)t * D + c] & (uint8_t)((1 << vb) - 1);
+      rec[L.v_codes + (int64_t)t * (D / per) + c / per] |= (uint8_t)(code << (vb * (c % per)));
     }
   for (int c = 0; c < D; ++c) {
     orc_put_scale(rec + L.k_delta + (int64_t)sw * c, k_delta[c], sw);
@@ -332,6 +341,13 @@ int orc_pack_record_sw(int D, int sw, const uint8_t* k_codes, const uint8_t* v_c
   }
   return 0;
 }
+int orc_pack_record_sw(int D, int sw, const uint8_t* k_codes, const uint8_t* v_codes,
+                       const double* k_delta, const double* k_lo, const double* k_s,
+                       const double* k_r, const double* v_delta, const double* v_lo,
+                       const double* v_r, const double* v_s, uint8_t* rec) {
+  return orc_pack_record_fmt(D, sw, 2, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta, v_lo,
+                             v_r, v_s, rec);
+}
 int orc_pack_record(int D, const uint8_t* k_codes, const uint8_t* v_codes,
                     const double* k_delta, const double* k_lo, const double* k_s,
                     const double* k_r, const double* v_delta, const double* v_lo,
@@ -341,11 +357,12 @@ int orc_pack_record(int D, const uint8_t* k_codes, const uint8_t* v_codes,
 }
 
 /* Inverse of orc_pack_record_sw: unpacked codes and the stored scales. */
-int orc_unpack_record_sw(int D, int sw, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
-                         double* k_delta, double* k_lo, double* k_s, double* k_r,
-                         double* v_delta, double* v_lo, double* v_r, double* v_s) {
-  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
-  const orc_layout L = orc_record_layout(D, sw);
+int orc_unpack_record_fmt(int D, int sw, int vb, const uint8_t* rec, uint8_t* k_codes,
+                          uint8_t* v_codes, double* k_delta, double* k_lo, double* k_s,
+                          double* k_r, double* v_delta, double* v_lo, double* v_r, double* v_s) {
+  if (!orc_fmt_ok(D, sw, vb)) return -3;
+  const orc_layout L = orc_record_layout(D, sw, vb);
+  const int per = 8 / vb;
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t)
       k_codes[(int64_t)t * D + c] =
@@ -353,7 +370,7 @@ int orc_unpack_record_sw(int D, int sw, const uint8_t* rec, uint8_t* k_codes, ui
   for (int t = 0; t < ORC_T; ++t)
     for (int c = 0; c < D; ++c)
       v_codes[(int64_t)t * D + c] =
-          (rec[L.v_codes + (int64_t)t * (D / 4) + c / 4] >> (2 * (c % 4))) & 0x3;
+          (rec[L.v_codes + (int64_t)t * (D / per) + c / per] >> (vb * (c % per))) & ((1 << vb) - 1);
   for (int c = 0; c < D; ++c) {
     k_delta[c] = orc_get_scale(rec + L.k_delta + (int64_t)sw * c, sw);
     k_lo[c] = orc_get_scale(rec + L.k_lo + (int64_t)sw * c, sw);
@@ -370,6 +387,12 @@ int orc_unpack_record_sw(int D, int sw, const uint8_t* rec, uint8_t* k_codes, ui
   }
   return 0;
 }
+int orc_unpack_record_sw(int D, int sw, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
+                         double* k_delta, double* k_lo, double* k_s, double* k_r,
+                         double* v_delta, double* v_lo, double* v_r, double* v_s) {
+  return orc_unpack_record_fmt(D, sw, 2, rec, k_codes, v_codes, k_delta, k_lo, k_s, k_r, v_delta,
+                               v_lo, v_r, v_s);
+}
 int orc_unpack_record(int D, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_codes,
                       double* k_delta, double* k_lo, double* k_s, double* k_r,
                       double* v_delta, double* v_lo, double* v_r, double* v_s) {
@@ -380,24 +403,31 @@ int orc_unpack_record(int D, const uint8_t* rec, uint8_t* k_codes, uint8_t* v_co
 /* Full compression of one (tile, KV head) unit into a record; also returns the
  * fp64 scales and the pre-rounding values for the parity checks. The codes
  * come from the fp64 scales whatever the stored scale format. */
-int orc_compress_unit_sw(const float* k, const float* v, int64_t row_stride, int D, int iters,
-                         int sw, uint8_t* rec, double* k_s, double* k_r, double* k_delta,
-                         double* k_lo, double* k_vpre, double* v_s, double* v_r,
-                         double* v_delta, double* v_lo, double* v_vpre) {
-  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
+int orc_compress_unit_fmt(const float* k, const float* v, int64_t row_stride, int D, int iters,
+                          int sw, int vb, uint8_t* rec, double* k_s, double* k_r, double* k_delta,
+                          double* k_lo, double* k_vpre, double* v_s, double* v_r,
+                          double* v_delta, double* v_lo, double* v_vpre) {
+  if (!orc_fmt_ok(D, sw, vb)) return -3;
   uint8_t* kc = (uint8_t*)malloc((size_t)ORC_T * D);
   uint8_t* vc = (uint8_t*)malloc((size_t)ORC_T * D);
   if (!kc || !vc) { free(kc); free(vc); return -7; }
   int rc = orc_quantize_tensor(k, row_stride, D, iters, 1, 4, k_s, k_r, k_delta, k_lo, kc,
                                k_vpre);
   if (rc == 0)
-    rc = orc_quantize_tensor(v, row_stride, D, iters, 0, 2, v_s, v_r, v_delta, v_lo, vc,
+    rc = orc_quantize_tensor(v, row_stride, D, iters, 0, vb, v_s, v_r, v_delta, v_lo, vc,
                              v_vpre);
   if (rc == 0)
-    rc = orc_pack_record_sw(D, sw, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s,
-                            rec);
+    rc = orc_pack_record_fmt(D, sw, vb, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r,
+                             v_s, rec);
   free(kc); free(vc);
   return rc;
+}
+int orc_compress_unit_sw(const float* k, const float* v, int64_t row_stride, int D, int iters,
+                         int sw, uint8_t* rec, double* k_s, double* k_r, double* k_delta,
+                         double* k_lo, double* k_vpre, double* v_s, double* v_r,
+                         double* v_delta, double* v_lo, double* v_vpre) {
+  return orc_compress_unit_fmt(k, v, row_stride, D, iters, sw, 2, rec, k_s, k_r, k_delta, k_lo,
+                               k_vpre, v_s, v_r, v_delta, v_lo, v_vpre);
 }
 int orc_compress_unit(const float* k, const float* v, int64_t row_stride, int D, int iters,
                       uint8_t* rec, double* k_s, double* k_r, double* k_delta, double* k_lo,
@@ -413,9 +443,10 @@ int orc_compress_unit(const float* k, const float* v, int64_t row_stride, int D,
  * + lo_tg) with the stored scales, then each row is multiplied by H (H is its
  * own inverse).
  */
-int orc_dequant_record_sw(int D, int sw, const uint8_t* rec, double* k_out, double* v_out) {
-  if (!orc_pow2_dim(D) || D < 4 || !orc_sw_ok(sw)) return -3;
-  const orc_layout L = orc_record_layout(D, sw);
+int orc_dequant_record_fmt(int D, int sw, int vb, const uint8_t* rec, double* k_out,
+                           double* v_out) {
+  if (!orc_fmt_ok(D, sw, vb)) return -3;
+  const orc_layout L = orc_record_layout(D, sw, vb);
   const int T = ORC_T;
   uint8_t* kc = (uint8_t*)malloc((size_t)T * D);
   uint8_t* vc = (uint8_t*)malloc((size_t)T * D);
@@ -428,7 +459,7 @@ int orc_dequant_record_sw(int D, int sw, const uint8_t* rec, double* k_out, doub
   }
   double *k_delta = buf, *k_lo = k_delta + D, *k_s = k_lo + D, *v_s = k_s + D;
   double *k_r = v_s + D, *v_r = k_r + T, *v_delta = v_r + T, *v_lo = v_delta + T * L.gv;
-  orc_unpack_record_sw(D, sw, rec, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s);
+  orc_unpack_record_fmt(D, sw, vb, rec, kc, vc, k_delta, k_lo, k_s, k_r, v_delta, v_lo, v_r, v_s);
   const int gw = D < 128 ? D : 128;
   for (int t = 0; t < T; ++t)
     for (int c = 0; c < D; ++c) {
@@ -441,6 +472,9 @@ int orc_dequant_record_sw(int D, int sw, const uint8_t* rec, double* k_out, doub
   orc_wht_rows(vt, v_out, T, D);
   free(kc); free(vc); free(buf); free(kt); free(vt);
   return 0;
+}
+int orc_dequant_record_sw(int D, int sw, const uint8_t* rec, double* k_out, double* v_out) {
+  return orc_dequant_record_fmt(D, sw, 2, rec, k_out, v_out);
 }
 int orc_dequant_record(int D, const uint8_t* rec, double* k_out, double* v_out) {
   return orc_dequant_record_sw(D, 4, rec, k_out, v_out);

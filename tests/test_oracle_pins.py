@@ -448,3 +448,90 @@ def test_f16_layout_keeps_codes_and_rounds_scales(oracle, workload, D):
     vt = ub["v_r"][:, None] * ub["v_s"][None, :] * (vd * ub["v_codes"] + vl)
     np.testing.assert_allclose(kk, kt @ H, rtol=0, atol=1e-12 * np.abs(kt).max())
     np.testing.assert_allclose(vv, vt @ H, rtol=0, atol=1e-12 * np.abs(vt).max())
+
+
+# ------------------------------------------- c4 variant: 4-bit values (k4v4)
+@pytest.mark.parametrize("D,size", [(64, 11264), (128, 20480), (256, 39936)])
+def test_v4_record_size(oracle, D, size):
+    """4-bit V codes take D/2 bytes per token: 128 D code bytes in all."""
+    assert oracle.record_bytes(D, v_bits=4) == size
+    assert oracle.record_bytes(D, v_bits=4) - oracle.record_bytes(D) == 32 * D
+
+
+def test_v4_pack_bit_order_hand_built(oracle):
+    """Token-major V as in the k4v2 layout, two channels per byte: channel
+    2j + k of token t in bits 4k..4k+3 of byte j of token row t."""
+    D = 64
+    kc = np.zeros((128, D), np.uint8)
+    vc = np.zeros((128, D), np.uint8)
+    vc[0, 1] = 0xB          # token 0, channel 1 -> high nibble of V byte 0
+    vc[3, 62] = 0x6         # token 3, channel 62 -> low nibble of byte 3*32 + 31
+    z = np.zeros
+    rec = oracle.pack_record(D, kc, vc, z(D), z(D), z(D), z(128), z(128), z(128), z(128), z(D),
+                             v_bits=4)
+    voff = 64 * D
+    assert rec[voff] == 0xB0 and rec[voff + 3 * 32 + 31] == 0x06
+    assert np.count_nonzero(rec) == 2
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_v4_pack_unpack_roundtrip(oracle, D):
+    rng = np.random.default_rng(D + 4)
+    gv = D // min(D, 128)
+    f32 = lambda n: rng.standard_normal(n).astype(np.float32).astype(np.float64)
+    args = dict(k_codes=rng.integers(0, 16, (128, D)).astype(np.uint8),
+                v_codes=rng.integers(0, 16, (128, D)).astype(np.uint8),
+                k_delta=f32(D), k_lo=f32(D), k_s=f32(D), k_r=f32(128),
+                v_delta=f32(128 * gv), v_lo=f32(128 * gv), v_r=f32(128), v_s=f32(D))
+    rec = oracle.pack_record(D, v_bits=4, **args)
+    back = oracle.unpack_record(rec, D, v_bits=4)
+    for name, val in args.items():
+        np.testing.assert_array_equal(back[name], val, err_msg=name)
+
+
+@pytest.mark.parametrize("workload,D", [("qwen3_8b_decode", 128), ("batched_d256_decode", 256)])
+def test_v4_compress_keeps_keys_and_bounds_value_error(oracle, workload, D):
+    """The k4v4 record: the K half is the k4v2 record's (codes and scales);
+    V is quantised to 16 levels per token group, so every rotated, normalised
+    V element is within delta/2 of its reconstruction, the group extremes take
+    codes 0 and 15, and the V step is (max - min)/15."""
+    k, v = synth.kv_stream(workload, 2, 0, 128, D)
+    a = oracle.compress_unit(k, v)
+    b = oracle.compress_unit(k, v, v_bits=4)
+    ua = oracle.unpack_record(a["record"], D)
+    ub = oracle.unpack_record(b["record"], D, v_bits=4)
+    for name in ("k_codes", "k_delta", "k_lo", "k_s", "k_r", "v_s", "v_r"):
+        np.testing.assert_array_equal(ua[name], ub[name], err_msg=name)
+    gv = D // min(D, 128)
+    gw = D // gv
+    vpre, vc = b["v_vpre"], ub["v_codes"].astype(np.int64)
+    assert vc.max() <= 15 and vc.min() >= 0
+    y = b["v_delta"].reshape(128, gv).repeat(gw, 1) * vpre + b["v_lo"].reshape(128, gv).repeat(gw, 1)
+    recon = b["v_delta"].reshape(128, gv).repeat(gw, 1) * vc + b["v_lo"].reshape(128, gv).repeat(gw, 1)
+    half = b["v_delta"].reshape(128, gv).repeat(gw, 1) / 2
+    assert np.all(np.abs(y - recon) <= half * (1 + 1e-12) + 1e-300)
+    for t in range(0, 128, 17):
+        for g in range(gv):
+            seg = vpre[t, g * gw:(g + 1) * gw]
+            codes = vc[t, g * gw:(g + 1) * gw]
+            assert codes[np.argmin(seg)] == 0 and codes[np.argmax(seg)] == 15
+    # and the stored V offset and step are the group minimum and range / 15
+    yv = y.reshape(128, gv, gw)
+    np.testing.assert_allclose(b["v_lo"].reshape(128, gv), yv.min(-1), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(b["v_delta"].reshape(128, gv), (yv.max(-1) - yv.min(-1)) / 15,
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_v4_dequant_distortion_bound(oracle):
+    """Unrotated V rows of a k4v4 record are within the norm of the per-element
+    bounds r s delta / 2 of the exact rows (orthonormal H), and tighter than
+    the k4v2 record's on the same tile."""
+    D = 128
+    k, v = synth.kv_stream("qwen3_8b_decode", 3, 0, 128, D)
+    b = oracle.compress_unit(k, v, v_bits=4)
+    _, vv = oracle.dequant_record(b["record"], D, v_bits=4)
+    _, v2 = oracle.dequant_record(oracle.compress_unit(k, v)["record"], D)
+    bound = np.sqrt(((b["v_r"][:, None] * b["v_s"][None, :] * b["v_delta"][:, None] / 2) ** 2).sum(1))
+    err = np.linalg.norm(vv - v.astype(np.float64), axis=1)
+    assert np.all(err <= bound * (1 + 1e-9))
+    assert np.linalg.norm(vv - v) < np.linalg.norm(v2 - v)
