@@ -329,7 +329,7 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
 def run_decode_sweeps(dev, lay, peaks, peak_kind):
     """Decode split throughput beyond the headline configuration: the 8B-like
     model at 4k and 32k context, and at 16k on records of the f16-scale layout
-    (36 layers of distinct caches, split launches back to back as in the
+    and of the k4v4 variant (36 layers of distinct caches, split launches back to back as in the
     headline roofline), and batched decode with large
     heads (32 ragged sequences with contexts uniform in [8k, 32k], 16q/4kv,
     head_dim 256; one layer's cache is 0.6 GB), timed as back-to-back split
@@ -361,8 +361,8 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         return a.elapsed_time(b) / (reps * n_launch)
 
     # ---- 8B-like decode at 4k and 32k, and at 16k on f16-scale records --------
-    for ctx, sb in ((4096, 32), (32768, 32), (16384, 16)):
-        lay_s = lay if sb == 32 else kvarn.layout(D, scale_bits=sb)
+    for ctx, sb, vb in ((4096, 32, 2), (32768, 32, 2), (16384, 16, 2), (16384, 32, 4)):
+        lay_s = lay if (sb, vb) == (32, 2) else kvarn.layout(D, scale_bits=sb, v_bits=vb)
         n0, w0, cap = ctx // 128, 64, 128
         rb = lay_s.record_bytes
         max_tiles = n0 + 1
@@ -410,7 +410,7 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         assert torch.isfinite(out).all().item(), "decode produced non-finite output"
         nbytes = HKV * n0 * rb + HKV * w0 * D * 8 + HQ * D * 4
         gbs = nbytes / (split_ms * 1e-3) / 1e9
-        res[f"qwen3_8b_ctx{ctx}" + ("" if sb == 32 else "_f16_scales")] = {
+        res[f"qwen3_8b_ctx{ctx}" + ("" if sb == 32 else "_f16_scales") + ("" if vb == 2 else "_k4v4")] = {
             "record_bytes": rb,
             "split_back_to_back_ms": split_ms, "split_bytes_per_launch": nbytes,
             "split_gbs": gbs, "split_frac": gbs / hbm,

@@ -105,7 +105,7 @@ typedef struct kvarn_layout {
   int32_t tile_tokens;    /* 128                                            */
   int32_t sinkhorn_iters; /* n, the fixed Sinkhorn round count (default 4)  */
   int32_t k_bits;         /* 4                                              */
-  int32_t v_bits;         /* 2                                              */
+  int32_t v_bits;         /* 2 (4 for the k4v4 variant, kvarn_layout_ex)    */
   int32_t v_group;        /* min(D, 128) channels per V quantisation group  */
   int32_t v_groups;       /* D / v_group                                    */
   int64_t record_bytes;
@@ -135,6 +135,24 @@ int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out);
  * scale_bits.
  */
 int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_layout_t* out);
+
+/*
+ * The record layout with scale fields of scale_bits bits (32 or 16, as in
+ * kvarn_layout_scales) and v_bits-bit value codes: 2 gives the k4v2 layouts
+ * above; 4 gives a k4v4 variant (other key/value bit widths, gmlx PR #116):
+ * values quantised per token and 128-channel group to 16 levels
+ * (delta = (max - min) / 15), packed token-major like the 2-bit codes with two
+ * channels per byte: channel c of token t in bits 4 (c % 2) .. +3 of byte
+ * t * (D / 2) + c / 2 (off_v_codes, D / 2 bytes per token). The keys, the
+ * Sinkhorn factors and the field order are unchanged. record_bytes = 128 D +
+ * SB (4 D + 256 + 256 Gv), SB = scale_bits / 8: 20480 at D=128 with fp32
+ * scales. kvarn_compress_tile and the decode entry points accept it;
+ * kvarn_prefill_attention returns KVARN_ERR_UNSUPPORTED for it.
+ * Returns KVARN_ERR_UNSUPPORTED for other head dims, iteration counts,
+ * scale_bits or v_bits.
+ */
+int kvarn_layout_ex(int head_dim, int sinkhorn_iters, int scale_bits, int v_bits,
+                    kvarn_layout_t* out);
 
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char* kvarn_status_string(int status);

@@ -126,14 +126,14 @@ __device__ __forceinline__ bool usable(float var, float mean) {
   return sd > ldexpf(sqrtf(var + mean * mean), -20);
 }
 
-template <int D, int SB>
+template <int D, int SB, int VB>
 __global__ void __launch_bounds__(CC<D>::NT, (D == 256) ? 1 : 2)
 compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw,
                 int64_t row_stride, const int64_t* __restrict__ src_row0,
                 uint8_t* __restrict__ tiles, const int64_t* __restrict__ dst_record,
                 int iters) {
   using C = CC<D>;
-  using R = Rec<D, SB>;
+  using R = Rec<D, SB, VB>;
   extern __shared__ __align__(16) unsigned char smem[];
   float* xs = reinterpret_cast<float*>(smem);
   float2* red = reinterpret_cast<float2*>(smem + C::OFF_RED);
@@ -374,7 +374,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       *reinterpret_cast<uint32_t*>(stage + R::kKCodes + cb * (kTile / 2) + 4 * tg) = w1;
     }
   } else {
-    // ---------------- V: 2-bit RTN per token over 128-channel groups ---------
+    // ---------------- V: VB-bit RTN per token over 128-channel groups --------
+    constexpr int kVMax = (1 << VB) - 1;  // largest value code
     float lo[8], hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -389,7 +390,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       lo[0] = fminf(lo[0], shfl_xor(lo[0], 8));
       hi[0] = fmaxf(hi[0], shfl_xor(hi[0], 8));
     }
-    const float delta = (hi[0] - lo[0]) / 3.0f;
+    const float delta = (hi[0] - lo[0]) / (float)kVMax;
     const float inv = delta > 0.f ? 1.0f / delta : 0.f;
     const int g = (D == 256) ? ((cg >> 4) & 1) : 0;
     __syncthreads();  // every thread is past its last read of the tile
@@ -403,21 +404,54 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     for (int i = 0; i < 8; ++i) {
       const float l = __shfl_sync(0xffffffffu, lo[0], src_lane(i));
       const float iv = __shfl_sync(0xffffffffu, inv, src_lane(i));
-      unsigned long long w = 0;
       const float2 nl = f2(-l, -l), iv2 = f2(iv, iv);
+      const int t = 8 * tg + i;
+      if constexpr (VB == 2) {
+        // channel 32 (cg >> 2) + 4 m + (cg & 3) of slot m: byte 8 (cg >> 2) + m
+        // of the token row, bits 2 (cg & 3); the four lanes of a channel
+        // quadruple fill eight bytes together
+        unsigned long long w = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
-        const int c0 = min(3, max(0, __float2int_rd(u.x)));
-        const int c1 = min(3, max(0, __float2int_rd(u.y)));
-        w |= (unsigned long long)c0 << (8 * (2 * k) + 2 * (cg & 3));
-        w |= (unsigned long long)c1 << (8 * (2 * k + 1) + 2 * (cg & 3));
-      }
-      w |= __shfl_xor_sync(0xffffffffu, w, 1);
-      w |= __shfl_xor_sync(0xffffffffu, w, 2);
-      if ((i & 3) == (cg & 3)) {
-        const int t = 8 * tg + i;
-        *reinterpret_cast<unsigned long long*>(stage + R::kVCodes + t * (D / 4) + 8 * (cg >> 2)) = w;
+        for (int k = 0; k < 4; ++k) {
+          const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
+          const int c0 = min(kVMax, max(0, __float2int_rd(u.x)));
+          const int c1 = min(kVMax, max(0, __float2int_rd(u.y)));
+          w |= (unsigned long long)c0 << (8 * (2 * k) + 2 * (cg & 3));
+          w |= (unsigned long long)c1 << (8 * (2 * k + 1) + 2 * (cg & 3));
+        }
+        w |= __shfl_xor_sync(0xffffffffu, w, 1);
+        w |= __shfl_xor_sync(0xffffffffu, w, 2);
+        if ((i & 3) == (cg & 3))
+          *reinterpret_cast<unsigned long long*>(stage + R::kVCodes + t * R::kVRow + 8 * (cg >> 2)) = w;
+      } else {
+        // 4-bit codes: channel 32 (cg >> 2) + 4 m + (cg & 3) sits in byte
+        // 16 (cg >> 2) + 2 m + ((cg & 3) >> 1), nibble (cg & 3) & 1; the four
+        // lanes of a channel quadruple fill sixteen bytes together
+        const int sh = 8 * ((cg & 3) >> 1) + 4 * (cg & 1);
+        unsigned long long w0 = 0, w1 = 0;  // bytes 0..7 (slots 0..3), 8..15 (slots 4..7)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
+          const unsigned long long c0 = (unsigned long long)min(kVMax, max(0, __float2int_rd(u.x)));
+          const unsigned long long c1 = (unsigned long long)min(kVMax, max(0, __float2int_rd(u.y)));
+          if (k < 2) {
+            w0 |= c0 << (16 * (2 * k) + sh);
+            w0 |= c1 << (16 * (2 * k + 1) + sh);
+          } else {
+            w1 |= c0 << (16 * (2 * k - 4) + sh);
+            w1 |= c1 << (16 * (2 * k - 3) + sh);
+          }
+        }
+        w0 |= __shfl_xor_sync(0xffffffffu, w0, 1);
+        w1 |= __shfl_xor_sync(0xffffffffu, w1, 1);
+        w0 |= __shfl_xor_sync(0xffffffffu, w0, 2);
+        w1 |= __shfl_xor_sync(0xffffffffu, w1, 2);
+        if ((i & 3) == (cg & 3)) {
+          unsigned long long* dst =
+              reinterpret_cast<unsigned long long*>(stage + R::kVCodes + t * R::kVRow + 16 * (cg >> 2));
+          dst[0] = w0;
+          dst[1] = w1;
+        }
       }
     }
   }
@@ -435,7 +469,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     __stcs(reinterpret_cast<uint4*>(rec + o), *reinterpret_cast<const uint4*>(stage + o));
 }
 
-template <int D, int SB>
+template <int D, int SB, int VB>
 cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw, int64_t row_stride,
                               const int64_t* src_row0, uint8_t* tiles, const int64_t* dst_record,
                               int64_t n_units, cudaStream_t st) {
@@ -445,42 +479,43 @@ cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(compress_kernel<D, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(compress_kernel<D, SB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   const int64_t blocks = 2 * n_units;
-  compress_kernel<D, SB><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(
+  compress_kernel<D, SB, VB><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(
       k_raw, v_raw, row_stride, src_row0, tiles, dst_record, iters);
   return cudaGetLastError();
 }
 
-template <int SB>
+template <int SB, int VB>
 cudaError_t launch_compress_sb(int D, int iters, const float* k_raw, const float* v_raw,
                                int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
                                const int64_t* dst_record, int64_t n_units, cudaStream_t st) {
   switch (D) {
-    case 64: return launch_compress_d<64, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 128: return launch_compress_d<128, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 256: return launch_compress_d<256, SB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 64: return launch_compress_d<64, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 128: return launch_compress_d<128, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 256: return launch_compress_d<256, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_compress(int D, int iters, int scale_bytes, const float* k_raw,
+cudaError_t launch_compress(int D, int iters, int scale_bytes, int v_bits, const float* k_raw,
                             const float* v_raw, int64_t row_stride, const int64_t* src_row0,
                             uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
                             cudaStream_t st) {
-  if (scale_bytes == 2)
-    return launch_compress_sb<2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
-                                 n_units, st);
-  if (scale_bytes == 4)
-    return launch_compress_sb<4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
-                                 n_units, st);
-  return cudaErrorInvalidValue;
+  const int key = 10 * scale_bytes + v_bits;
+  switch (key) {
+    case 42: return launch_compress_sb<4, 2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 22: return launch_compress_sb<2, 2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 44: return launch_compress_sb<4, 4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 24: return launch_compress_sb<2, 4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace kvarn

@@ -35,17 +35,23 @@
 
 #include "kvarn_common.cuh"
 
-// Built twice: for records with fp32 scale fields (KVARN_SCALE_BYTES 4, the
-// default; this unit also holds the plan, the combine kernel and the
-// dispatch) and with binary16 scale fields (2).
-#ifndef KVARN_SCALE_BYTES
-#define KVARN_SCALE_BYTES 4
+// Built four times: for records with fp32 or binary16 scale fields
+// (KVARN_BUILD_SCALE_BYTES 4 or 2) and 2-bit or 4-bit value codes (KVARN_BUILD_V_BITS 2
+// or 4). The fp32 / 2-bit unit also holds the plan, the combine kernel and
+// the dispatch.
+#ifndef KVARN_BUILD_SCALE_BYTES
+#define KVARN_BUILD_SCALE_BYTES 4
 #endif
+#ifndef KVARN_BUILD_V_BITS
+#define KVARN_BUILD_V_BITS 2
+#endif
+#define KVARN_PRIMARY_UNIT (KVARN_BUILD_SCALE_BYTES == 4 && KVARN_BUILD_V_BITS == 2)
 
 namespace kvarn {
 namespace {
 
-constexpr int kSB = KVARN_SCALE_BYTES;
+constexpr int kSB = KVARN_BUILD_SCALE_BYTES;
+constexpr int kVB = KVARN_BUILD_V_BITS;
 
 constexpr float kNegInf = -INFINITY;
 constexpr float kLog2eD = 1.4426950408889634f;
@@ -296,16 +302,21 @@ struct DC {
   static constexpr int WPT = WPT_;                              // warps per tile (2 or 4)
   static constexpr int TPS = NW / WPT;                          // tiles per round
   static constexpr int CH = 4 / WPT;                            // 32-token chunks per warp
-  static constexpr int RB = Rec<D, kSB>::kBytes;                // record bytes
-  static constexpr int SLOT = Rec<D, kSB>::kSlot;               // record slot stride in shared memory
-  static constexpr int GV = Rec<D, kSB>::kGv;
+  static constexpr int RB = Rec<D, kSB, kVB>::kBytes;           // record bytes
+  static constexpr int SLOT = Rec<D, kSB, kVB>::kSlot;          // record slot stride in shared memory
+  static constexpr int GV = Rec<D, kSB, kVB>::kGv;
   static constexpr int K_BYTES = 64 * D;                        // K codes: D rows of 64 bytes
-  static constexpr int CODE_BYTES = 96 * D;                     // K + V codes, one TMA box
+  static constexpr int CODE_BYTES = (64 + 16 * kVB) * D;        // K + V codes, one TMA box
   static constexpr int CODE_LINES = CODE_BYTES / 128;           // 128-byte lines of that box
   static constexpr int NT = GP > 4 ? 2 : 1;                     // n8-tiles of (head, part) columns
   static constexpr int NCB = D / 16;                            // 16-channel blocks
   static constexpr int HB = NCB / WPT;                          // blocks whose B fragments a warp builds
-  static constexpr int NS = D / 64;                             // 64-channel slices of a V row
+  // value contraction: slices of VSL channels of a V row, MU m-blocks of 16
+  // channels each; lane group g8 owns channels VSL sl + CPL g8 + 2 mu + {0, 1}
+  static constexpr int VSL = kVB == 2 ? 64 : 32;
+  static constexpr int NS = D / VSL;
+  static constexpr int MU = kVB == 2 ? 4 : 2;
+  static constexpr int CPL = kVB == 2 ? 8 : 4;
   // window rows staged per warp, sized by the record region of the fp32
   // layout (two slots per group with multi-round items), whatever the scale width
   static constexpr int WCH0 = ((MR_ ? 2 : 1) * TPS * Rec<D, 4>::kBytes) / (NW * 2 * D * 4);
@@ -340,7 +351,7 @@ struct DC {
   }
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(SLOT % 1024 == 0 && K_BYTES % 1024 == 0, "slots and V codes on swizzle atoms");
-  static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D, kSB>::kKDelta, "code box");
+  static_assert(CODE_LINES <= 256 && CODE_BYTES == Rec<D, kSB, kVB>::kKDelta, "code box");
   static_assert(HB >= 1 && WPT * HB == NCB && (WPT == 2 || WPT == 4), "channel blocks per warp");
   static_assert(NW * GP * D * 4 <= REC_MIN, "window partials fit the record region");
 };
@@ -393,7 +404,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     int rounds_arg, float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
                     int prefetch, const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, NW_, WPT_, MR>;
-  using R = Rec<D, kSB>;
+  using R = Rec<D, kSB, kVB>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
   constexpr int HB = C::HB, WPT = C::WPT, CH = C::CH;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -626,13 +637,14 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   const int hb = g8 >> 1;
   const bool is_hi = !(g8 & 1);
   float m_run[NT], l_run[NT];
-  float out_acc[NS][4][2][NT];  // channel 64 sl + 8 g8 + 2 mu + rr, head 4nt + q4
+  constexpr int MU = C::MU;
+  float out_acc[NS][MU][2][NT];  // channel VSL sl + CPL g8 + 2 mu + rr, head 4nt + q4
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) { m_run[nt] = kNegInf; l_run[nt] = 0.f; }
 #pragma unroll
   for (int sl = 0; sl < NS; ++sl)
 #pragma unroll
-    for (int mu = 0; mu < 4; ++mu)
+    for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
@@ -871,7 +883,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int m = 4; m < 32; m <<= 1) pm[nt] = fmaxf(pm[nt], __shfl_xor_sync(0xffffffffu, pm[nt], m));
         float sc2, inv2;
-        pow2_scale(pm[nt], 4.0f, sc2, inv2);
+        pow2_scale(pm[nt], kVB == 2 ? 4.0f : 16.0f, sc2, inv2);
         float sp = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < CH; ++w2)
@@ -895,17 +907,18 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
 
-    // ---- phase B: this warp's 32 CH tokens against all channels, one 64-channel
-    // slice of the V rows at a time. M-block mu of slice sl: row g8 <-> channel
-    // 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1.
+    // ---- phase B: this warp's 32 CH tokens against all channels, one slice of
+    // VSL channels of the V rows at a time. 2-bit codes: m-block mu of slice sl
+    // row g8 <-> channel 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1;
+    // 4-bit codes: row g8 <-> channel 32 sl + 4 g8 + 2 mu, row g8 + 8 <-> + 1.
     const uint32_t vaddr0 =
-        (uint32_t)(C::K_BYTES + (32 * CH * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * (D / 4));
+        (uint32_t)(C::K_BYTES + (32 * CH * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * R::kVRow);
 #pragma unroll
     for (int sl = 0; sl < NS; ++sl) {
-      const int gv = (64 * sl) / R::kVGroup;
-      float o[4][NT][4];
+      const int gv = (C::VSL * sl) / R::kVGroup;
+      float o[MU][NT][4];
 #pragma unroll
-      for (int mu = 0; mu < 4; ++mu)
+      for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -913,33 +926,46 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
       for (int w2 = 0; w2 < CH; ++w2) {
         uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
-        ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * (D / 4) + 16 * sl)), y[0], y[1], y[2],
+        ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * R::kVRow + 16 * sl)), y[0], y[1], y[2],
                   y[3]);
         const uint32_t y8[4] = {y[0] >> 8, y[1] >> 8, y[2] >> 8, y[3] >> 8};
 #pragma unroll
-        for (int mu = 0; mu < 4; ++mu)
+        for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            // fields 2 mu and 2 mu + 1: fields 0..3 of y, or of y >> 8 for mu >= 2
-            const uint32_t ya = mu < 2 ? y[2 * j] : y8[2 * j];
-            const uint32_t yb = mu < 2 ? y[2 * j + 1] : y8[2 * j + 1];
-            const int f = 2 * (mu & 1);
-            const uint32_t a0 = v_frag(ya, f), a1 = v_frag(ya, f + 1);
-            const uint32_t a2 = v_frag(yb, f), a3 = v_frag(yb, f + 1);
+            uint32_t a0, a1, a2, a3;
+            if constexpr (kVB == 2) {
+              // fields 2 mu and 2 mu + 1: fields 0..3 of y, or of y >> 8 for mu >= 2
+              const uint32_t ya = mu < 2 ? y[2 * j] : y8[2 * j];
+              const uint32_t yb = mu < 2 ? y[2 * j + 1] : y8[2 * j + 1];
+              const int f = 2 * (mu & 1);
+              a0 = v_frag(ya, f); a1 = v_frag(ya, f + 1);
+              a2 = v_frag(yb, f); a3 = v_frag(yb, f + 1);
+            } else {
+              // nibbles 2 mu and 2 mu + 1: nibbles 0, 1 of y, or of y >> 8 for mu = 1
+              const uint32_t ya = mu == 0 ? y[2 * j] : y8[2 * j];
+              const uint32_t yb = mu == 0 ? y[2 * j + 1] : y8[2 * j + 1];
+              a0 = k_frag(ya, 0); a1 = k_frag(ya, 1);
+              a2 = k_frag(yb, 0); a3 = k_frag(yb, 1);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
           }
       }
-      // acc_c = alpha acc_c + s_c (4 2^-e (O - sum pd) + sum p r lo)
-      const float4 s0 = sc_ld4<kSB>(vS, 64 * sl + 8 * g8);
-      const float4 s1 = sc_ld4<kSB>(vS, 64 * sl + 8 * g8 + 4);
-      const float sv[4][2] = {{s0.x, s0.y}, {s0.z, s0.w}, {s1.x, s1.y}, {s1.z, s1.w}};
+      // acc_c = alpha acc_c + s_c (2^VB 2^-e (O - sum pd) + sum p r lo)
+      float sv[MU][2];
+#pragma unroll
+      for (int h4 = 0; h4 < MU / 2; ++h4) {
+        const float4 s4 = sc_ld4<kSB>(vS, C::VSL * sl + C::CPL * g8 + 4 * h4);
+        sv[2 * h4][0] = s4.x; sv[2 * h4][1] = s4.y;
+        sv[2 * h4 + 1][0] = s4.z; sv[2 * h4 + 1][1] = s4.w;
+      }
       if (k == 0) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int mu = 0; mu < 4; ++mu)
+          for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
               const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
@@ -949,7 +975,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int mu = 0; mu < 4; ++mu)
+          for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
               const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
@@ -995,8 +1021,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
       for (int sl = 0; sl < NS; ++sl)
 #pragma unroll
-        for (int mu = 0; mu < 4; ++mu)
-          *reinterpret_cast<float2*>(vred + (warp * GP + h) * C::DP + 64 * sl + 8 * g8 + 2 * mu) =
+        for (int mu = 0; mu < MU; ++mu)
+          *reinterpret_cast<float2*>(vred + (warp * GP + h) * C::DP + C::VSL * sl + C::CPL * g8 + 2 * mu) =
               make_float2(out_acc[sl][mu][0][nt], out_acc[sl][mu][1][nt]);
     }
   }
@@ -1026,7 +1052,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   }
 }
 
-#if KVARN_SCALE_BYTES == 4
+#if KVARN_PRIMARY_UNIT
 // LSE combine: one CTA of 512 threads per (query head, sequence). Each group
 // of D/4 threads reads whole item rows (float4 per thread, coalesced) of
 // every (512/(D/4))-th item in one pass, keeping its own running maximum; the
@@ -1126,7 +1152,7 @@ decode_combine_kernel(const float* __restrict__ ws_ml, const float* __restrict__
   }
 }
 
-#endif  // KVARN_SCALE_BYTES == 4
+#endif  // KVARN_PRIMARY_UNIT
 
 // cuTensorMapEncodeTiled, fetched once from the driver (the library links the
 // static CUDA runtime only).
@@ -1235,7 +1261,7 @@ void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** 
   *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
-#if KVARN_SCALE_BYTES == 4
+#if KVARN_PRIMARY_UNIT
 int sm_count() {
   static int cached[64] = {};
   int dev = 0;
@@ -1251,7 +1277,7 @@ int sm_count() {
 
 }  // namespace
 
-#if KVARN_SCALE_BYTES == 4
+#if KVARN_PRIMARY_UNIT
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
@@ -1302,9 +1328,14 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
 
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                 cudaStream_t st) {
-  if (a.scale_bytes == 4) return launch_decode_split_sb4(p, a, ws, st);
-  if (a.scale_bytes == 2) return launch_decode_split_sb2(p, a, ws, st);
-  return cudaErrorInvalidValue;
+  const int key = 10 * a.scale_bytes + a.v_bits;
+  switch (key) {
+    case 42: return launch_decode_split_sb4_v2(p, a, ws, st);
+    case 22: return launch_decode_split_sb2_v2(p, a, ws, st);
+    case 44: return launch_decode_split_sb4_v4(p, a, ws, st);
+    case 24: return launch_decode_split_sb2_v4(p, a, ws, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
@@ -1322,14 +1353,20 @@ cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, con
   }
 }
 
-#endif  // KVARN_SCALE_BYTES == 4
+#endif  // KVARN_PRIMARY_UNIT
 
-#if KVARN_SCALE_BYTES == 4
-cudaError_t launch_decode_split_sb4(const DecodePlan& p, const DecodeArgs& a, void* ws,
-                                    cudaStream_t st) {
+#if KVARN_BUILD_SCALE_BYTES == 4 && KVARN_BUILD_V_BITS == 2
+cudaError_t launch_decode_split_sb4_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
+#elif KVARN_BUILD_SCALE_BYTES == 2 && KVARN_BUILD_V_BITS == 2
+cudaError_t launch_decode_split_sb2_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
+#elif KVARN_BUILD_SCALE_BYTES == 4 && KVARN_BUILD_V_BITS == 4
+cudaError_t launch_decode_split_sb4_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
 #else
-cudaError_t launch_decode_split_sb2(const DecodePlan& p, const DecodeArgs& a, void* ws,
-                                    cudaStream_t st) {
+cudaError_t launch_decode_split_sb2_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
 #endif
   if (p.items == 0) return cudaSuccess;
   float *ml, *acc;

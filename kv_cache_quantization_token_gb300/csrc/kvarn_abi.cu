@@ -17,21 +17,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA; }
 
 // sb: bytes of each scale field, 4 (fp32, layout version 1) or 2 (binary16,
-// layout version 2); the code fields are the same in both.
-int fill_layout(int D, int iters, int sb, kvarn_layout_t* L) {
+// layout version 2); vb: value code width, 2 (the k4v2 preset) or 4 (k4v4).
+int fill_layout(int D, int iters, int sb, int vb, kvarn_layout_t* L) {
   memset(L, 0, sizeof(*L));
   L->version = sb == 2 ? KVARN_LAYOUT_VERSION_F16_SCALES : KVARN_LAYOUT_VERSION;
   L->head_dim = D;
   L->tile_tokens = KVARN_TILE_TOKENS;
   L->sinkhorn_iters = iters;
   L->k_bits = KVARN_K_BITS;
-  L->v_bits = KVARN_V_BITS;
+  L->v_bits = vb;
   L->v_group = D < 128 ? D : 128;
   L->v_groups = D / L->v_group;
   const int64_t T = KVARN_TILE_TOKENS, gv = L->v_groups;
   L->off_k_codes = 0;
   L->off_v_codes = L->off_k_codes + (int64_t)D * (T / 2);
-  L->off_k_delta = L->off_v_codes + T * (D / 4);
+  L->off_k_delta = L->off_v_codes + T * (D * vb / 8);
   L->off_k_lo = L->off_k_delta + (int64_t)sb * D;
   L->off_k_s = L->off_k_lo + (int64_t)sb * D;
   L->off_k_r = L->off_k_s + (int64_t)sb * D;
@@ -54,8 +54,9 @@ bool layout_ok(const kvarn_layout_t* L) {
   if (L->version != KVARN_LAYOUT_VERSION && L->version != KVARN_LAYOUT_VERSION_F16_SCALES)
     return false;
   if (L->sinkhorn_iters < 1 || L->sinkhorn_iters > 16) return false;
+  if (L->v_bits != 2 && L->v_bits != 4) return false;
   kvarn_layout_t ref;
-  fill_layout(L->head_dim, L->sinkhorn_iters, scale_bytes_of(L), &ref);
+  fill_layout(L->head_dim, L->sinkhorn_iters, scale_bytes_of(L), L->v_bits, &ref);
   return memcmp(&ref, L, sizeof(ref)) == 0;
 }
 
@@ -79,15 +80,20 @@ int kvarn_set_launch_flags(unsigned flags) {
 unsigned kvarn_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
 
 int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out) {
-  return kvarn_layout_scales(head_dim, sinkhorn_iters, 32, out);
+  return kvarn_layout_ex(head_dim, sinkhorn_iters, 32, KVARN_V_BITS, out);
 }
 
 int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_layout_t* out) {
+  return kvarn_layout_ex(head_dim, sinkhorn_iters, scale_bits, KVARN_V_BITS, out);
+}
+
+int kvarn_layout_ex(int head_dim, int sinkhorn_iters, int scale_bits, int v_bits,
+                    kvarn_layout_t* out) {
   if (!out) return KVARN_ERR_NULL;
   if (!supported_dim(head_dim) || sinkhorn_iters < 1 || sinkhorn_iters > 16 ||
-      (scale_bits != 32 && scale_bits != 16))
+      (scale_bits != 32 && scale_bits != 16) || (v_bits != 2 && v_bits != 4))
     return KVARN_ERR_UNSUPPORTED;
-  return fill_layout(head_dim, sinkhorn_iters, scale_bits / 8, out);
+  return fill_layout(head_dim, sinkhorn_iters, scale_bits / 8, v_bits, out);
 }
 
 const char* kvarn_status_string(int status) {
@@ -132,8 +138,8 @@ int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stri
   if ((row_stride & 3) || !aligned16(k_raw) || !aligned16(v_raw) || !aligned16(tiles))
     return KVARN_ERR_ALIGN;
   return from_cuda(kvarn::launch_compress(D, layout->sinkhorn_iters, scale_bytes_of(layout),
-                                          k_raw, v_raw, row_stride, src_row0, tiles, dst_record,
-                                          n_units, (cudaStream_t)stream));
+                                          layout->v_bits, k_raw, v_raw, row_stride, src_row0,
+                                          tiles, dst_record, n_units, (cudaStream_t)stream));
 }
 
 int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
@@ -196,7 +202,7 @@ static int decode_prepare(const float* q, const uint8_t* tiles, const int64_t* t
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
   *a = kvarn::DecodeArgs{q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
                          win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
-                         scale_bytes_of(layout)};
+                         scale_bytes_of(layout), layout->v_bits};
   return KVARN_OK;
 }
 
@@ -265,6 +271,7 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
   if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
+  if (layout->v_bits != 2) return KVARN_ERR_UNSUPPORTED;  // k4v4 records: decode only
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hkv > 65535) return KVARN_ERR_BAD_ARG;
   if (Hq / Hkv > 8) return KVARN_ERR_UNSUPPORTED;
   if (C < 0 || pos0 < 0 || n_tiles < 0 || win_len < 0 || win_capacity < 0 ||

@@ -15,18 +15,22 @@ namespace kvarn {
 constexpr int kTile = KVARN_TILE_TOKENS;  // tokens per compressed tile
 
 // Byte offsets of the record fields for head_dim D with scale fields of SB
-// bytes: 4 (fp32, layout version 1) or 2 (IEEE binary16, layout version 2;
-// the same codes). Same values as kvarn_layout() / kvarn_layout_scales();
-// kept as constexpr so the kernels index without a struct.
-template <int D, int SB = 4>
+// bytes, 4 (fp32, layout version 1) or 2 (IEEE binary16, layout version 2),
+// and VB-bit value codes, 2 (the k4v2 preset) or 4 (the k4v4 variant: the
+// same token-major packing, two channels per byte). Same values as
+// kvarn_layout_ex(); kept as constexpr so the kernels index without a struct.
+template <int D, int SB = 4, int VB = 2>
 struct Rec {
   static_assert(SB == 4 || SB == 2, "scale field width");
+  static_assert(VB == 2 || VB == 4, "value code width");
   static constexpr int kSB = SB;
+  static constexpr int kVB = VB;
   static constexpr int kGv = D / (D < 128 ? D : 128);     // V groups per token
   static constexpr int kVGroup = D < 128 ? D : 128;        // channels per V group
+  static constexpr int kVRow = D * VB / 8;                 // V code bytes per token
   static constexpr int kKCodes = 0;                        // u8 [D][64]
-  static constexpr int kVCodes = kKCodes + D * (kTile / 2);  // u8 [128][D/4]
-  static constexpr int kKDelta = kVCodes + kTile * (D / 4);
+  static constexpr int kVCodes = kKCodes + D * (kTile / 2);  // u8 [128][kVRow]
+  static constexpr int kKDelta = kVCodes + kTile * kVRow;
   static constexpr int kKLo = kKDelta + SB * D;
   static constexpr int kKS = kKLo + SB * D;
   static constexpr int kKR = kKS + SB * D;
@@ -37,7 +41,7 @@ struct Rec {
   static constexpr int kBytes = kVS + SB * D;
   // stride of a record slot in shared memory (slots start on 1024-byte swizzle atoms)
   static constexpr int kSlot = (kBytes + 1023) / 1024 * 1024;
-  static_assert(kBytes == 96 * D + SB * (4 * D + 256 + 256 * kGv), "record size");
+  static_assert(kBytes == 64 * D + 16 * VB * D + SB * (4 * D + 256 + 256 * kGv), "record size");
   static_assert(kBytes % 128 == 0, "records on 128-byte lines");
 };
 
@@ -119,7 +123,7 @@ struct LaunchCfg {
 // Launchers implemented in the .cu files; kvarn_abi.cu validates arguments
 // and calls them. They return a cudaError_t from cudaGetLastError().
 namespace kvarn {
-cudaError_t launch_compress(int D, int iters, int scale_bytes, const float* k_raw,
+cudaError_t launch_compress(int D, int iters, int scale_bytes, int v_bits, const float* k_raw,
                             const float* v_raw, int64_t row_stride, const int64_t* src_row0,
                             uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
                             cudaStream_t st);
@@ -152,16 +156,22 @@ struct DecodeArgs {
   int win_capacity, B, Hq, Hkv, D, max_tiles;
   float scale;
   int scale_bytes;  // record scale fields: 4 (fp32) or 2 (binary16)
+  int v_bits;       // value code width: 2 or 4
 };
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p);
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                 cudaStream_t st);
-// the split kernels for records with fp32 (4) or binary16 (2) scale fields,
-// built as two translation units of decode.cu
-cudaError_t launch_decode_split_sb4(const DecodePlan& p, const DecodeArgs& a, void* ws,
-                                    cudaStream_t st);
-cudaError_t launch_decode_split_sb2(const DecodePlan& p, const DecodeArgs& a, void* ws,
-                                    cudaStream_t st);
+// the split kernels for records with fp32 (sb4) or binary16 (sb2) scale
+// fields and 2-bit (v2) or 4-bit (v4) value codes, built as four translation
+// units of decode.cu
+cudaError_t launch_decode_split_sb4_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
+cudaError_t launch_decode_split_sb2_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
+cudaError_t launch_decode_split_sb4_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
+cudaError_t launch_decode_split_sb2_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
                                   float* out, cudaStream_t st);
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,

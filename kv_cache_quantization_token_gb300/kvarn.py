@@ -59,6 +59,7 @@ def _L():
         lib.kvarn_status_string.argtypes = [c_int]
         lib.kvarn_layout.argtypes = [c_int, c_int, ctypes.POINTER(Layout)]
         lib.kvarn_layout_scales.argtypes = [c_int, c_int, c_int, ctypes.POINTER(Layout)]
+        lib.kvarn_layout_ex.argtypes = [c_int, c_int, c_int, c_int, ctypes.POINTER(Layout)]
         lib.kvarn_rotate_query.argtypes = [vp, vp, i64, c_int, vp]
         lib.kvarn_compress_tile.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, ctypes.POINTER(Layout), vp]
         lib.kvarn_append_window.argtypes = [vp, vp, i64, vp, vp, c_int, vp, vp, c_int, c_int, c_int, vp]
@@ -84,7 +85,8 @@ def _L():
         lib.kvarn_set_launch_flags.argtypes = [ctypes.c_uint]
         lib.kvarn_get_launch_flags.argtypes = []
         lib.kvarn_get_launch_flags.restype = ctypes.c_uint
-        for name in ("kvarn_layout", "kvarn_layout_scales", "kvarn_rotate_query", "kvarn_compress_tile",
+        for name in ("kvarn_layout", "kvarn_layout_scales", "kvarn_layout_ex", "kvarn_rotate_query",
+                     "kvarn_compress_tile",
                      "kvarn_append_window", "kvarn_decode_workspace_bytes",
                      "kvarn_decode_attention", "kvarn_decode_split", "kvarn_decode_combine",
                      "kvarn_window_advance", "kvarn_prefill_attention", "kvarn_set_launch_flags",
@@ -127,12 +129,14 @@ def _dev(t, name, dtype):
     return t
 
 
-def layout(head_dim: int, iters: int = DEFAULT_ITERS, scale_bits: int = 32) -> Layout:
+def layout(head_dim: int, iters: int = DEFAULT_ITERS, scale_bits: int = 32,
+           v_bits: int = 2) -> Layout:
     """Record layout: fp32 scale fields (scale_bits 32, the default) or
-    binary16 ones (16, the f16-scale layout; same codes)."""
+    binary16 ones (16, the f16-scale layout; same codes), and 2-bit value
+    codes (the k4v2 preset) or 4-bit ones (v_bits 4, the k4v4 variant)."""
     L = Layout()
-    _check("kvarn_layout_scales",
-           _L().kvarn_layout_scales(head_dim, iters, scale_bits, ctypes.byref(L)))
+    _check("kvarn_layout_ex",
+           _L().kvarn_layout_ex(head_dim, iters, scale_bits, v_bits, ctypes.byref(L)))
     return L
 
 

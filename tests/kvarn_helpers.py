@@ -26,11 +26,11 @@ def band_mask(vpre: np.ndarray) -> np.ndarray:
     return np.abs(frac - 0.5) < BAND
 
 
-def compare_record(gpu_rec: np.ndarray, ref: dict, D: int) -> dict:
+def compare_record(gpu_rec: np.ndarray, ref: dict, D: int, v_bits: int = 2) -> dict:
     """Compare one GPU record with oracle.compress_unit output. Returns counts;
     raises AssertionError when a tolerance is broken."""
-    g = oracle.unpack_record(gpu_rec, D)
-    r = oracle.unpack_record(ref["record"], D)
+    g = oracle.unpack_record(gpu_rec, D, v_bits=v_bits)
+    r = oracle.unpack_record(ref["record"], D, v_bits=v_bits)
     stats = {"band_flips": 0, "codes": 0}
     for t in ("k", "v"):
         diff = g[f"{t}_codes"] != r[f"{t}_codes"]
@@ -72,15 +72,15 @@ def compare_record(gpu_rec: np.ndarray, ref: dict, D: int) -> dict:
     return stats
 
 
-def compare_record_f16(gpu_rec: np.ndarray, ref: dict, D: int) -> dict:
+def compare_record_f16(gpu_rec: np.ndarray, ref: dict, D: int, v_bits: int = 2) -> dict:
     """Compare a GPU record of the f16-scale layout with
     oracle.compress_unit(..., scale_bits=16). Codes as in compare_record. Each
     stored scale is binary16 rounded from the kernel's fp32 value, the
     oracle's from fp64: they must be equal, except where the fp64 value lies
     within 1e-6 (relative) of the midpoint between two binary16 neighbours,
     where one ulp apart is allowed (counted and returned)."""
-    g = oracle.unpack_record(gpu_rec, D, 16)
-    r = oracle.unpack_record(ref["record"], D, 16)
+    g = oracle.unpack_record(gpu_rec, D, 16, v_bits)
+    r = oracle.unpack_record(ref["record"], D, 16, v_bits)
     stats = {"band_flips": 0, "codes": 0, "scale_flips": 0}
     for t in ("k", "v"):
         diff = g[f"{t}_codes"] != r[f"{t}_codes"]
@@ -111,13 +111,13 @@ class Cache:
     """A batch of KVarN caches built on the GPU through the C ABI."""
 
     def __init__(self, workload, layer, ctxs, Hkv, D, W=128, cap=None, win_start=None, dev="cuda:0",
-                 iters=4, scale_bits=32):
+                 iters=4, scale_bits=32, v_bits=2):
         self.workload, self.layer, self.Hkv, self.D, self.W = workload, layer, Hkv, D, W
         self.dev = torch.device(dev)
         self.B = len(ctxs)
         self.ctxs = list(ctxs)
-        self.scale_bits = scale_bits
-        self.lay = kvarn.layout(D, iters, scale_bits)
+        self.scale_bits, self.v_bits = scale_bits, v_bits
+        self.lay = kvarn.layout(D, iters, scale_bits, v_bits)
         self.rb = self.lay.record_bytes
         self.nt = [n_tiles_for(c, W) for c in ctxs]
         self.max_tiles = max(max(self.nt), 1)
@@ -175,7 +175,7 @@ class Cache:
         return oracle.decode_attention(q, self.tiles.cpu().numpy(), self.tile_table.cpu().numpy(),
                                        self.nt, self.win_k.cpu().numpy(), self.win_v.cpu().numpy(),
                                        self.starts, self.wl, scale, heads=heads,
-                                       scale_bits=self.scale_bits)
+                                       scale_bits=self.scale_bits, v_bits=self.v_bits)
 
 
 def rel_l2(got: np.ndarray, want: np.ndarray) -> float:

@@ -145,3 +145,23 @@ def test_prefill_cached_host_validation(lib):
     assert f(*args(16 * 8 * blk - 1, 16, 0)) == -5  # workspace smaller than ws_blocks images
     assert f(*args(1 << 40, 16, 11)) == -4         # more cached tiles than tiles
     assert f(*args(1 << 40, 16, -1)) == -4
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_v4_layout_agrees_with_oracle(lib, D):
+    for sb in (32, 16):
+        L = kvarn.layout(D, scale_bits=sb, v_bits=4)
+        assert L.v_bits == 4 and L.record_bytes == oracle.record_bytes(D, sb, 4)
+        assert L.off_k_delta == 128 * D and L.record_bytes % 128 == 0
+    M = kvarn.Layout()
+    assert lib.kvarn_layout_ex(D, 4, 32, 3, ctypes.byref(M)) == -3
+    assert lib.kvarn_layout_ex(D, 4, 32, 8, ctypes.byref(M)) == -3
+
+
+def test_prefill_rejects_v4_records(lib):
+    L = kvarn.layout(128, v_bits=4)
+    p = ctypes.c_void_p(4096)
+    f = lib.kvarn_prefill_attention
+    f.argtypes = None
+    assert f(p, 16, 0, p, p, 64, 1, p, p, 0, 16, 768, 32, 8, 128, ctypes.c_float(0.088),
+             ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == -3

@@ -183,3 +183,25 @@ def test_f16_scale_records_multi_round():
     """The multi-round split kernel (more than 8 tiles per SM) on f16-scale records."""
     c = Cache("qwen3_8b_decode", 15, [128 * 1400 + 9], Hkv=1, D=128, scale_bits=16)
     _check(c, Hq=8, heads=[(0, h) for h in range(0, 8, 3)])
+
+
+@pytest.mark.parametrize("workload,ctxs,Hq,Hkv,D,sb", [("single_tile", [128 + 17], 1, 1, 128, 32),
+                                                      ("qwen3_8b_decode", [16384 + 40], 32, 8, 128, 32),
+                                                      ("qwen3_8b_decode", [600, 1000], 8, 1, 128, 16),
+                                                      ("batched_d256_decode", [900, 128 * 5 + 3], 16, 4, 256, 32),
+                                                      ("single_tile", [128 * 3 + 50], 4, 2, 64, 32),
+                                                      ("qwen3_8b_decode", [700], 24, 8, 128, 32)])
+def test_v4_records(workload, ctxs, Hq, Hkv, D, sb):
+    """Decode over k4v4 records (4-bit values, 20,480-byte records at
+    head_dim 128 with fp32 scales): the value contraction reads two channels
+    per code byte; the oracle dequantises the same records."""
+    c = Cache(workload, 16, ctxs, Hkv=Hkv, D=D, scale_bits=sb, v_bits=4)
+    heads = [(b, h) for b in range(len(ctxs)) for h in range(0, Hq, max(1, Hq // 4))]
+    _check(c, Hq=Hq, heads=heads)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,ctx", [(128, 8, 1, 128 * 1400 + 9), (256, 16, 4, 128 * 460 + 77)])
+def test_v4_records_multi_round(D, Hq, Hkv, ctx):
+    """The multi-round split kernel on k4v4 records."""
+    c = Cache("qwen3_8b_decode", 17, [ctx], Hkv=Hkv, D=D, v_bits=4)
+    _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])
