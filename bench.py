@@ -509,6 +509,45 @@ def workload_config():
 
 
 # --------------------------------------------------------------------------
+def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind):
+    """One compress launch over C_TILES x C_HEADS tile-heads of fresh raw K/V
+    (256 MiB of input, larger than L2), timed with CUDA events per launch."""
+    import torch
+    from kv_cache_quantization_token_gb300 import kvarn, synth
+    D, rb = lay.head_dim, lay.record_bytes
+    n_units = C_TILES * C_HEADS
+    ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * C_TILES, D)
+    ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
+    cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
+    del ks, vs
+    csrc = torch.arange(n_units, dtype=torch.int64, device=dev) * 128
+    cdst = torch.arange(n_units, dtype=torch.int64, device=dev) * rb
+    ctiles = torch.empty(n_units * rb, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
+        c_reps = 20
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(c_reps)]
+        for a, b in cev:
+            a.record()
+            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
+            b.record()
+    torch.cuda.synchronize()
+    comp_ms = float(np.mean([a.elapsed_time(b) for a, b in cev]))
+    comp_bytes = n_units * (2 * 128 * D * 4 + rb)
+    comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
+    trc = NCU_TRAFFIC["compress"]
+    ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
+    return {"tile_heads_per_launch": n_units, "ms_per_launch": comp_ms,
+            "tiles_per_s": n_units / (comp_ms * 1e-3), "gbs": comp_gbs,
+            "bytes_per_launch": comp_bytes,
+            "roofline": {"bound": "hbm", "achieved": comp_gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": comp_gbs / hbm,
+                         "traffic": ctraffic, "kernel": "compress_kernel<128>",
+                         "peak_source": peak_kind}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,7 +555,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "prefill", "decode-sweeps"],
+    ap.add_argument("--section", default="all",
+                    choices=["all", "prefill", "decode-sweeps", "compress"],
                     help="run one secondary measurement alone and print its JSON (for profiling)")
     args = ap.parse_args()
 
@@ -544,6 +584,9 @@ def main():
         peaks, peak_kind = measured_peaks()
         if args.section == "prefill":
             sec = run_prefill_bench(dev, torch.cuda.Stream(device=dev), lay, peaks, peak_kind)
+        elif args.section == "compress":
+            sec = run_compress_bench(dev, torch.cuda.Stream(device=dev), lay, args.warmup,
+                                     peaks["hbm_gbs"], peak_kind)
         else:
             sec = run_decode_sweeps(dev, lay, peaks, peak_kind)
         if rank == 0:
@@ -777,30 +820,7 @@ def main():
     assert np.isfinite(out_h.numpy()).all(), "decode produced non-finite output"
 
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
-    n_units = C_TILES * C_HEADS
-    ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * C_TILES, D)
-    ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
-    cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
-    del ks, vs
-    csrc = torch.arange(n_units, dtype=torch.int64, device=dev) * 128
-    cdst = torch.arange(n_units, dtype=torch.int64, device=dev) * rb
-    ctiles = torch.empty(n_units * rb, dtype=torch.uint8, device=dev)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
-        c_reps = 20
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(c_reps)]
-        for a, b in cev:  # input (256 MiB) is larger than L2
-            a.record()
-            kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
-            b.record()
-    torch.cuda.synchronize()
-    comp_ms = float(np.mean([a.elapsed_time(b) for a, b in cev]))
-    comp_bytes = n_units * (2 * 128 * D * 4 + rb)
-    comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
-    trc = NCU_TRAFFIC["compress"]
-    ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
+    compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
 
     # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256)
     prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
@@ -836,13 +856,7 @@ def main():
                          "kernel": "decode_split_kernel",
                          "timing": "average launch duration over back-to-back launches (see "
                                    "decode.back_to_back_timing)", "peak_source": peak_kind},
-            "compress": {"tile_heads_per_launch": n_units, "ms_per_launch": comp_ms,
-                         "tiles_per_s": n_units / (comp_ms * 1e-3), "gbs": comp_gbs,
-                         "bytes_per_launch": comp_bytes,
-                         "roofline": {"bound": "hbm", "achieved": comp_gbs, "peak": hbm,
-                                      "unit": "GB/s", "frac": comp_gbs / hbm,
-                                      "traffic": ctraffic, "kernel": "compress_kernel<128>",
-                                      "peak_source": peak_kind}},
+            "compress": compress,
             "prefill": prefill,
             "decode_sweeps": sweeps,
             "cpu_baseline": cpu,

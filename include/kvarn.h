@@ -146,8 +146,8 @@ int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_
  * t * (D / 2) + c / 2 (off_v_codes, D / 2 bytes per token). The keys, the
  * Sinkhorn factors and the field order are unchanged. record_bytes = 128 D +
  * SB (4 D + 256 + 256 Gv), SB = scale_bits / 8: 20480 at D=128 with fp32
- * scales. kvarn_compress_tile and the decode entry points accept it;
- * kvarn_prefill_attention returns KVARN_ERR_UNSUPPORTED for it.
+ * scales. kvarn_compress_tile, the decode entry points and the prefill
+ * entry points accept it.
  * Returns KVARN_ERR_UNSUPPORTED for other head dims, iteration counts,
  * scale_bits or v_bits.
  */

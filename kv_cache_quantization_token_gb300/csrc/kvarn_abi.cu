@@ -271,7 +271,6 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
   if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
-  if (layout->v_bits != 2) return KVARN_ERR_UNSUPPORTED;  // k4v4 records: decode only
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hkv > 65535) return KVARN_ERR_BAD_ARG;
   if (Hq / Hkv > 8) return KVARN_ERR_UNSUPPORTED;
   if (C < 0 || pos0 < 0 || n_tiles < 0 || win_len < 0 || win_capacity < 0 ||
@@ -298,7 +297,8 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
   return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
                                          n_tiles, win_k, win_v, win_start, win_len, win_capacity,
                                          Hq, Hkv, head_dim, softmax_scale, scale_bytes_of(layout),
-                                         ws, stride, cached_tiles, out, (cudaStream_t)stream));
+                                         layout->v_bits, ws, stride, cached_tiles, out,
+                                         (cudaStream_t)stream));
 }
 
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,

@@ -178,8 +178,8 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           int scale_bytes, void* ws, int ws_blocks, int cached_tiles, float* out,
-                           cudaStream_t st);
+                           int scale_bytes, int v_bits, void* ws, int ws_blocks, int cached_tiles,
+                           float* out, cudaStream_t st);
 // 128-key blocks a prefill chunk sees (tiles, and tiles + window blocks), and
 // the workspace bytes of one (block, KV head) image.
 void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, int* n_blk);

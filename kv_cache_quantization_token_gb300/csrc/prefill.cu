@@ -252,14 +252,19 @@ struct PC {
   static constexpr int OFF_MISC = OFF_BAR + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;     // + slack to align the base to 1024
   // dequant kernel shared memory: the packed record, then the block image
-  static constexpr int DQ_OFF_OUT = RB;                  // RB is a multiple of 1024
-  static constexpr int DQ_OFF_BAR = DQ_OFF_OUT + BLK;
-  static constexpr int DQ_SMEM = DQ_OFF_BAR + 64 + 1024;
+  // dequant kernel: the record (room for the fp32 layout of its value width),
+  // then the block image and a barrier
+  template <int VB>
+  struct DQ {
+    static constexpr int OFF_OUT = Rec<D, 4, VB>::kSlot;
+    static constexpr int OFF_BAR = OFF_OUT + BLK;
+    static constexpr int SMEM = OFF_BAR + 64 + 1024;
+  };
   static constexpr int NTHR = 256;                       // dequant: two threads per key row
   static constexpr int NTHR_ATT = 320;                   // attention: 8 softmax warps, MMA, loads
   static constexpr int TMEM_COLS = 512;                  // S: 0..127 and 128..255, O|l: 256..256+D
   static_assert(D == 64 || D == 128, "prefill head_dim");
-  static_assert(RB % 1024 == 0 && OPB % 1024 == 0 && VKB % 1024 == 0,
+  static_assert(OPB % 1024 == 0 && VKB % 1024 == 0,
                 "swizzled images on 1024-byte boundaries");
 };
 
@@ -281,18 +286,18 @@ struct PrefillArgs {
 
 // ---------------------------------------------------------------------------
 // dequant: block j (tile j, or window block j - n_tblk) of KV head blockIdx.y
-template <int D, int SB>
+template <int D, int SB, int VB>
 __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillArgs a) {
   using P = PC<D>;
-  using R = Rec<D, SB>;  // scale fields fp32 (SB 4) or binary16 (SB 2)
+  using R = Rec<D, SB, VB>;  // scale fields fp32 (SB 4) or binary16 (SB 2); VB-bit values
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
   const unsigned char* rec = sm;
-  unsigned char* sKh = sm + P::DQ_OFF_OUT;
+  unsigned char* sKh = sm + P::template DQ<VB>::OFF_OUT;
   unsigned char* sKl = sKh + P::OPB;
   unsigned char* sV = sKl + P::OPB;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::DQ_OFF_BAR);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::template DQ<VB>::OFF_BAR);
   const int j = a.first_blk + blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, row = tid & 127, half = tid >> 7;
   bool poison = false;
@@ -351,9 +356,10 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
       {
         const int t = row;
         const float r = sc_ld<SB>(vR, t);
-        const unsigned char* vrow = rec + R::kVCodes + t * (D / 4);
-        constexpr int HB = D / 8;  // code bytes of half a token row (16 at D=128, 8 at D=64)
-        uint32_t vw[HB / 4];       // read with one or two wide loads
+        const unsigned char* vrow = rec + R::kVCodes + t * R::kVRow;
+        constexpr int CPB = 8 / VB;               // channels per code byte
+        constexpr int HB = R::kVRow / 2;          // code bytes of half a token row
+        uint32_t vw[HB / 4];                      // read with wide loads
         if constexpr (HB >= 16) {
 #pragma unroll
           for (int q4 = 0; q4 < HB / 16; ++q4) {
@@ -368,12 +374,13 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
         for (int ub = 0; ub < HB; ++ub) {
           const int jb = half * HB + ub;
           const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
-          const int g = (4 * jb) / R::kVGroup;
+          const int g = (CPB * jb) / R::kVGroup;
           const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * jb + e;
-            const float v = sc_ld<SB>(vS, c) * fmaf(d, (float)((byte >> (2 * e)) & 3u), lo);
+          for (int e = 0; e < CPB; ++e) {
+            const int c = CPB * jb + e;
+            const float code = (float)((byte >> (VB * e)) & ((1u << VB) - 1u));
+            const float v = sc_ld<SB>(vS, c) * fmaf(d, code, lo);
             *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
           }
         }
@@ -774,7 +781,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
 }
 
-template <int D, int SB>
+template <int D, int SB, int VB>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   using P = PC<D>;
   static bool configured[64] = {};
@@ -784,13 +791,14 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_dequant_kernel<D, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P::DQ_SMEM);
+    e = cudaFuncSetAttribute(prefill_dequant_kernel<D, SB, VB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::template DQ<VB>::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   if (a.n_blk > a.first_blk) {
-    prefill_dequant_kernel<D, SB><<<dim3(a.n_blk - a.first_blk, a.Hkv), P::NTHR, P::DQ_SMEM, st>>>(a);
+    prefill_dequant_kernel<D, SB, VB><<<dim3(a.n_blk - a.first_blk, a.Hkv), P::NTHR,
+                                        P::template DQ<VB>::SMEM, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -821,8 +829,8 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
                            const int64_t* tile_table, int table_stride, int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
-                           int scale_bytes, void* ws, int ws_blocks, int cached_tiles, float* out,
-                           cudaStream_t st) {
+                           int scale_bytes, int v_bits, void* ws, int ws_blocks, int cached_tiles,
+                           float* out, cudaStream_t st) {
   PrefillArgs a;
   a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
   a.ws = reinterpret_cast<uint8_t*>(ws);
@@ -832,12 +840,16 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
   prefill_blocks(pos0, C, n_tiles, win_len, &a.n_tblk, &a.n_blk);
   a.ws_stride = ws_blocks > 0 ? ws_blocks : a.n_blk;
   a.first_blk = cached_tiles < a.n_tblk ? cached_tiles : a.n_tblk;
-  const int key = 10 * D + scale_bytes;
+  const int key = 100 * D + 10 * scale_bytes + v_bits;
   switch (key) {
-    case 644: return launch_prefill_d<64, 4>(a, st);
-    case 642: return launch_prefill_d<64, 2>(a, st);
-    case 1284: return launch_prefill_d<128, 4>(a, st);
-    case 1282: return launch_prefill_d<128, 2>(a, st);
+    case 6442: return launch_prefill_d<64, 4, 2>(a, st);
+    case 6422: return launch_prefill_d<64, 2, 2>(a, st);
+    case 6444: return launch_prefill_d<64, 4, 4>(a, st);
+    case 6424: return launch_prefill_d<64, 2, 4>(a, st);
+    case 12842: return launch_prefill_d<128, 4, 2>(a, st);
+    case 12822: return launch_prefill_d<128, 2, 2>(a, st);
+    case 12844: return launch_prefill_d<128, 4, 4>(a, st);
+    case 12824: return launch_prefill_d<128, 2, 4>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

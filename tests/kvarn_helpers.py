@@ -195,13 +195,13 @@ class PrefillRun:
     oracle can be evaluated on the same state."""
 
     def __init__(self, workload, layer, n_tokens, Hq, Hkv, D, W=256, chunk=512, keep=None,
-                 dev="cuda:0", scale=None, scale_bits=32, cached=False):
+                 dev="cuda:0", scale=None, scale_bits=32, cached=False, v_bits=2):
         dev = torch.device(dev)
         self.Hq, self.Hkv, self.D, self.W = Hq, Hkv, D, W
         self.k, self.v = synth.kv_layer(workload, layer, Hkv, n_tokens, D)
         self.q = synth.queries(workload, layer, (n_tokens, Hq, D))
-        self.scale_bits = scale_bits
-        self.lay = kvarn.layout(D, scale_bits=scale_bits)
+        self.scale_bits, self.v_bits = scale_bits, v_bits
+        self.lay = kvarn.layout(D, scale_bits=scale_bits, v_bits=v_bits)
         rb = self.rb = self.lay.record_bytes
         self.cap = cap = TILE * ((W - 1 + chunk + TILE - 1) // TILE)
         max_tiles = n_tokens // TILE + 1
@@ -259,7 +259,7 @@ class PrefillRun:
         ref = oracle.prefill_attention(self.q[pos0:pos0 + s["C"]], pos0, pool,
                                        self.table.cpu().numpy(), s["n_tiles"], s["win_k"],
                                        s["win_v"], s["start"], s["length"], self.scale, rows=rows,
-                                       scale_bits=self.scale_bits)
+                                       scale_bits=self.scale_bits, v_bits=self.v_bits)
         worst = 0.0
         for (i, h), r in ref.items():
             e = rel_l2(s["out"][i, h], r)

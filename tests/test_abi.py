@@ -158,10 +158,15 @@ def test_v4_layout_agrees_with_oracle(lib, D):
     assert lib.kvarn_layout_ex(D, 4, 32, 8, ctypes.byref(M)) == -3
 
 
-def test_prefill_rejects_v4_records(lib):
+def test_prefill_accepts_v4_records(lib):
+    """k4v4 records pass the prefill entry's layout check: an empty chunk is a
+    no-op and a bad head ratio is reported as such, not as an unsupported
+    record format."""
     L = kvarn.layout(128, v_bits=4)
     p = ctypes.c_void_p(4096)
     f = lib.kvarn_prefill_attention
     f.argtypes = None
-    assert f(p, 16, 0, p, p, 64, 1, p, p, 0, 16, 768, 32, 8, 128, ctypes.c_float(0.088),
-             ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == -3
+    assert f(p, 0, 0, p, p, 64, 1, p, p, 0, 16, 768, 32, 8, 128, ctypes.c_float(0.088),
+             ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == 0
+    assert f(p, 16, 0, p, p, 64, 1, p, p, 0, 16, 768, 33, 8, 128, ctypes.c_float(0.088),
+             ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == -4

@@ -86,3 +86,15 @@ def test_prefill_cached_images_match_uncached(Hq, Hkv, D, n, chunk, W, sb):
         np.testing.assert_array_equal(a.snap[p]["out"], b.snap[p]["out"])
     last = max(b.snap)
     b.check(last, _rows(b.snap[last]["C"], range(0, Hq, 5), step=29))
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W,sb,cached", [(32, 8, 128, 1400, 512, 256, 32, True),
+                                                         (8, 8, 64, 700, 256, 128, 32, False),
+                                                         (16, 2, 128, 900, 300, 256, 16, True)])
+def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
+    """Chunked prefill over k4v4 records (4-bit value codes, two channels per
+    byte), with fp32 or f16 scale fields, cached or per-chunk images."""
+    run = PrefillRun("qwen3_8b_prefill", 7, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk,
+                     scale_bits=sb, v_bits=4, cached=cached)
+    for p in run.snap:
+        run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=23))
