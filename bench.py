@@ -48,9 +48,9 @@ C_TILES, C_HEADS = 256, 8
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
     # one 16k-context layer: 17.39 MB read, nothing written back within the launch
-    "decode_split": {"src_sha": "f449e992beff7631", "bytes": 17393408},
-    # 2 x (134.30 MB read + 5.88 MB written) for 1024 tile-heads, scaled to 2048
-    "compress": {"src_sha": "92c82f58b708b8f7", "bytes": 280351744},
+    "decode_split": {"src_sha": "762da7e5fd90bbf6", "bytes": 17393920},
+    # one 2048-tile-head launch: 268.52 MB read + 17.74 MB written back within the launch
+    "compress": {"src_sha": "4eca572915d5151b", "bytes": 286262272},
 }
 
 
