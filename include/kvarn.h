@@ -341,8 +341,9 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
  *                n_tiles, win_len, Hkv, head_dim) bytes, 256-byte aligned; no
  *                initialisation needed. Calls sharing ws must not overlap.
  * Requires pos0 + C <= 128 * n_tiles + win_len (the chunk's own keys are in
- * the cache), head_dim 64 or 128 (256 returns KVARN_ERR_UNSUPPORTED) and
- * Hq / Hkv <= 8.
+ * the cache), head_dim 64, 128 or 256 and Hq / Hkv <= 8. At head_dim 256
+ * the attention streams keys in 32-key sub-blocks (the 128-row fp16 query
+ * operands fill most of shared memory); the result has the same form.
  */
 int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes);
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,

@@ -255,7 +255,7 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
 
 int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes) {
   if (!bytes) return KVARN_ERR_NULL;
-  if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVARN_ERR_UNSUPPORTED;
   if (n_tiles < 0 || win_len < 0 || Hkv <= 0) return KVARN_ERR_BAD_ARG;
   const size_t blocks = (size_t)n_tiles + (size_t)(win_len + KVARN_TILE_TOKENS - 1) / KVARN_TILE_TOKENS;
   *bytes = blocks * (size_t)Hkv * kvarn::prefill_block_bytes(head_dim);
@@ -268,7 +268,7 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
                           int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
                           const kvarn_layout_t* layout, void* ws, size_t ws_bytes, int ws_blocks,
                           int cached_tiles, float* out, kvarn_stream_t stream) {
-  if (head_dim != 64 && head_dim != 128) return KVARN_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVARN_ERR_UNSUPPORTED;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hkv > 65535) return KVARN_ERR_BAD_ARG;

@@ -236,7 +236,6 @@ __device__ __forceinline__ void fwht_reg(float (&x)[N]) {
 
 template <int D>
 struct PC {
-  static constexpr int RB = Rec<D>::kBytes;             // room for a record of either scale width
   static constexpr int OPB = 128 * D * 2;                // one fp16 operand image: 128 rows x D
   static constexpr int BLK = 3 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T
   // attention kernel shared memory
@@ -251,19 +250,21 @@ struct PC {
   static constexpr int OFF_BAR = OFF_P + 128 * 128 * 2;  // 8 mbarriers
   static constexpr int OFF_MISC = OFF_BAR + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;     // + slack to align the base to 1024
-  // dequant kernel shared memory: the packed record, then the block image
-  // dequant kernel: the record (room for the fp32 layout of its value width),
-  // then the block image and a barrier
+  // dequant kernel shared memory: the record (room for the fp32 layout of its
+  // value width), then the block image and a barrier. At head_dim 256 the
+  // image is built in two stages (K~ hi + lo, stored; then V~^T in their place)
+  static constexpr bool DQ_TWO_STAGE = D == 256;
+  static constexpr int DQ_OUT = DQ_TWO_STAGE ? 2 * OPB : BLK;
   template <int VB>
   struct DQ {
     static constexpr int OFF_OUT = Rec<D, 4, VB>::kSlot;
-    static constexpr int OFF_BAR = OFF_OUT + BLK;
+    static constexpr int OFF_BAR = OFF_OUT + DQ_OUT;
     static constexpr int SMEM = OFF_BAR + 64 + 1024;
   };
   static constexpr int NTHR = 256;                       // dequant: two threads per key row
   static constexpr int NTHR_ATT = 320;                   // attention: 8 softmax warps, MMA, loads
   static constexpr int TMEM_COLS = 512;                  // S: 0..127 and 128..255, O|l: 256..256+D
-  static_assert(D == 64 || D == 128, "prefill head_dim");
+  static_assert(D == 64 || D == 128 || D == 256, "prefill head_dim");
   static_assert(OPB % 1024 == 0 && VKB % 1024 == 0,
                 "swizzled images on 1024-byte boundaries");
 };
@@ -287,21 +288,24 @@ struct PrefillArgs {
 // ---------------------------------------------------------------------------
 // dequant: block j (tile j, or window block j - n_tblk) of KV head blockIdx.y
 template <int D, int SB, int VB>
-__global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kernel(const PrefillArgs a) {
   using P = PC<D>;
   using R = Rec<D, SB, VB>;  // scale fields fp32 (SB 4) or binary16 (SB 2); VB-bit values
+  constexpr bool kTwo = P::DQ_TWO_STAGE;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
   const unsigned char* rec = sm;
   unsigned char* sKh = sm + P::template DQ<VB>::OFF_OUT;
   unsigned char* sKl = sKh + P::OPB;
-  unsigned char* sV = sKl + P::OPB;
+  unsigned char* sV = kTwo ? sKh : sKl + P::OPB;  // two stages: V~^T replaces the stored K~
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::template DQ<VB>::OFF_BAR);
   const int j = a.first_blk + blockIdx.x, kvh = blockIdx.y;
+  uint8_t* gimg = a.ws + ((int64_t)kvh * a.ws_stride + j) * P::BLK;
   const int tid = threadIdx.x, row = tid & 127, half = tid >> 7;
+  const bool is_tile = j < a.n_tblk;  // uniform over the CTA
   bool poison = false;
-  if (j < a.n_tblk) {
+  if (is_tile) {
     const int64_t off = a.tile_table[(int64_t)kvh * a.table_stride + j];
     const bool aligned = (off & 15) == 0 && off >= 0;
     if (tid == 0) {
@@ -311,135 +315,151 @@ __global__ void __launch_bounds__(256, 2) prefill_dequant_kernel(const PrefillAr
     __syncthreads();
     if (aligned && tid == 0) bulk_load(sm, a.tiles + off, R::kBytes, bar);
     poison = !aligned || !mbar_wait_bounded(bar, 0);
-    if (__syncthreads_or(poison)) {
-      // an unusable record: NaN keys make every score of this block NaN
-      if (aligned && tid == 0) mbar_wait_bounded(bar, 0);  // let the copy land (bounded)
-      for (int o = tid * 8; o < P::BLK / 2; o += 8 * P::NTHR)
-        *reinterpret_cast<uint4*>(sKh + 2 * o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
+    poison = __syncthreads_or(poison) != 0;
+    // an unusable record: NaN keys make every score of this block NaN
+    if (poison && aligned && tid == 0) mbar_wait_bounded(bar, 0);  // let the copy land (bounded)
+  }
+  auto fill_nan = [&](unsigned char* dst, int bytes) {
+    for (int o = tid * 16; o < bytes; o += 16 * P::NTHR)
+      *reinterpret_cast<uint4*>(dst + o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
+  };
+  // window block: raw rows rotated (K into K~ hi/lo, V into V~^T); rows past
+  // the window's length are zero
+  const int wb = j - a.n_tblk;
+  const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * wb);
+  const int64_t slot = ((int64_t)a.win_start + 128 * wb + row) % a.win_cap;
+  const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
+  auto win_row = [&](const float* base, float (&x)[D]) {
+    if (row < nkeys) {
+      const float4* src = reinterpret_cast<const float4*>(base + rbase);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 v = src[c4];
+        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+      }
+      fwht_reg<D>(x);
     } else {
+#pragma unroll
+      for (int c = 0; c < D; ++c) x[c] = 0.f;
+    }
+  };
+  auto win_k = [&]() {
+    float x[D];
+    win_row(a.win_k, x);
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
+      *reinterpret_cast<uint4*>(sKh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+      *reinterpret_cast<uint4*>(sKl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+    }
+  };
+  auto win_v = [&]() {  // V row -> column `row` of V~^T
+    float x[D];
+    win_row(a.win_v, x);
+#pragma unroll
+    for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, row, D)) = __float2half_rn(x[c]);
+  };
+
+  // ---------------- K~ hi / lo
+  if (is_tile) {
+    if (poison) {
+      fill_nan(sKh, 2 * P::OPB);
+    } else {
+      // thread -> channel tid % D and a contiguous share of its 128 keys
       const unsigned char* kS = rec + R::kKS;
       const unsigned char* kD = rec + R::kKDelta;
       const unsigned char* kL = rec + R::kKLo;
       const unsigned char* kR = rec + R::kKR;
+      constexpr int NKG = P::NTHR / D, WPG = 16 / NKG;  // key groups, 8-key words per group
+      const int c = tid % D, kg = tid / D;
+      const float s = sc_ld<SB>(kS, c), d = sc_ld<SB>(kD, c) * s, lo = sc_ld<SB>(kL, c) * s;
+      const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
+      uint32_t wds[WPG];  // this thread's share of the channel row, read with 16-byte loads
+#pragma unroll
+      for (int q4 = 0; q4 < WPG / 4; ++q4) {
+        const uint4 u = reinterpret_cast<const uint4*>(crow + WPG * kg)[q4];
+        wds[4 * q4] = u.x; wds[4 * q4 + 1] = u.y; wds[4 * q4 + 2] = u.z; wds[4 * q4 + 3] = u.w;
+      }
+#pragma unroll
+      for (int u = 0; u < WPG; ++u) {
+        const int w4 = WPG * kg + u;
+        const uint32_t wd = wds[u];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = 8 * w4 + i;
+          const float v = sc_ld<SB>(kR, t) * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
+          const __half h = __float2half_rn(v);
+          const uint32_t o = sw_off(t, c, 128);
+          *reinterpret_cast<__half*>(sKh + o) = h;
+          *reinterpret_cast<__half*>(sKl + o) = __float2half_rn(v - __half2float(h));
+        }
+      }
+    }
+  } else if (half == 0) {
+    win_k();
+  } else if constexpr (!kTwo) {
+    win_v();
+  }
+  if constexpr (kTwo) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) bulk_store_wait(gimg, sKh, 2 * P::OPB);
+    __syncthreads();  // the store has read K~ before V~^T overwrites it
+  }
+
+  // ---------------- V~^T
+  if (is_tile) {
+    if (poison) {
+      fill_nan(sV, P::OPB);
+    } else {
+      // thread -> key t, half of the D channels of the token row
       const unsigned char* vS = rec + R::kVS;
       const unsigned char* vR = rec + R::kVR;
       const unsigned char* vD = rec + R::kVDelta;
       const unsigned char* vL = rec + R::kVLo;
-      // K~: thread -> channel tid % D and a contiguous share of its 128 keys
-      {
-        constexpr int NKG = P::NTHR / D, WPG = 16 / NKG;  // key groups, 8-key words per group
-        const int c = tid % D, kg = tid / D;
-        const float s = sc_ld<SB>(kS, c), d = sc_ld<SB>(kD, c) * s, lo = sc_ld<SB>(kL, c) * s;
-        const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
-        uint32_t wds[WPG];  // this thread's share of the channel row, read with 16-byte loads
+      const int t = row;
+      const float r = sc_ld<SB>(vR, t);
+      const unsigned char* vrow = rec + R::kVCodes + t * R::kVRow;
+      constexpr int CPB = 8 / VB;               // channels per code byte
+      constexpr int HB = R::kVRow / 2;          // code bytes of half a token row
+      uint32_t vw[HB / 4];                      // read with wide loads
+      if constexpr (HB >= 16) {
 #pragma unroll
-        for (int q4 = 0; q4 < WPG / 4; ++q4) {
-          const uint4 u = reinterpret_cast<const uint4*>(crow + WPG * kg)[q4];
-          wds[4 * q4] = u.x; wds[4 * q4 + 1] = u.y; wds[4 * q4 + 2] = u.z; wds[4 * q4 + 3] = u.w;
+        for (int q4 = 0; q4 < HB / 16; ++q4) {
+          const uint4 u = reinterpret_cast<const uint4*>(vrow + half * HB)[q4];
+          vw[4 * q4] = u.x; vw[4 * q4 + 1] = u.y; vw[4 * q4 + 2] = u.z; vw[4 * q4 + 3] = u.w;
         }
-#pragma unroll
-        for (int u = 0; u < WPG; ++u) {
-          const int w4 = WPG * kg + u;
-          const uint32_t wd = wds[u];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int t = 8 * w4 + i;
-            const float v = sc_ld<SB>(kR, t) * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
-            const __half h = __float2half_rn(v);
-            const uint32_t o = sw_off(t, c, 128);
-            *reinterpret_cast<__half*>(sKh + o) = h;
-            *reinterpret_cast<__half*>(sKl + o) = __float2half_rn(v - __half2float(h));
-          }
-        }
+      } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(vrow + half * HB);
+        vw[0] = u.x; vw[1] = u.y;
       }
-      // V~^T: thread -> key t, half of the D channels of the token row
-      {
-        const int t = row;
-        const float r = sc_ld<SB>(vR, t);
-        const unsigned char* vrow = rec + R::kVCodes + t * R::kVRow;
-        constexpr int CPB = 8 / VB;               // channels per code byte
-        constexpr int HB = R::kVRow / 2;          // code bytes of half a token row
-        uint32_t vw[HB / 4];                      // read with wide loads
-        if constexpr (HB >= 16) {
 #pragma unroll
-          for (int q4 = 0; q4 < HB / 16; ++q4) {
-            const uint4 u = reinterpret_cast<const uint4*>(vrow + half * HB)[q4];
-            vw[4 * q4] = u.x; vw[4 * q4 + 1] = u.y; vw[4 * q4 + 2] = u.z; vw[4 * q4 + 3] = u.w;
-          }
-        } else {
-          const uint2 u = *reinterpret_cast<const uint2*>(vrow + half * HB);
-          vw[0] = u.x; vw[1] = u.y;
-        }
+      for (int ub = 0; ub < HB; ++ub) {
+        const int jb = half * HB + ub;
+        const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
+        const int g = (CPB * jb) / R::kVGroup;
+        const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
 #pragma unroll
-        for (int ub = 0; ub < HB; ++ub) {
-          const int jb = half * HB + ub;
-          const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
-          const int g = (CPB * jb) / R::kVGroup;
-          const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
-#pragma unroll
-          for (int e = 0; e < CPB; ++e) {
-            const int c = CPB * jb + e;
-            const float code = (float)((byte >> (VB * e)) & ((1u << VB) - 1u));
-            const float v = sc_ld<SB>(vS, c) * fmaf(d, code, lo);
-            *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
-          }
+        for (int e = 0; e < CPB; ++e) {
+          const int c = CPB * jb + e;
+          const float code = (float)((byte >> (VB * e)) & ((1u << VB) - 1u));
+          const float v = sc_ld<SB>(vS, c) * fmaf(d, code, lo);
+          *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
         }
       }
     }
-  } else {
-      // window block: rotate raw rows (K into K~ hi/lo, V into V~^T)
-      const int wb = j - a.n_tblk;
-      const int nkeys = min(128, a.win_len - 128 * wb);
-      const int t = row;
-      float x[D];
-      const bool have = t < nkeys;
-      const int64_t slot = ((int64_t)a.win_start + 128 * wb + t) % a.win_cap;
-      const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
-      // K row (threads of the first half)
-      if (half == 0) {
-      if (have) {
-        const float4* src = reinterpret_cast<const float4*>(a.win_k + rbase);
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 v = src[c4];
-          x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
-        }
-        fwht_reg<D>(x);
-      } else {
-#pragma unroll
-        for (int c = 0; c < D; ++c) x[c] = 0.f;
-      }
-#pragma unroll
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        __align__(16) __half2 hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
-        *reinterpret_cast<uint4*>(sKh + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-        *reinterpret_cast<uint4*>(sKl + sw_off(t, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
-      }
-      } else {
-      // V row -> column t of V~^T (threads of the second half)
-      if (have) {
-        const float4* src = reinterpret_cast<const float4*>(a.win_v + rbase);
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 v = src[c4];
-          x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
-        }
-        fwht_reg<D>(x);
-      } else {
-#pragma unroll
-        for (int c = 0; c < D; ++c) x[c] = 0.f;
-      }
-#pragma unroll
-      for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(x[c]);
-      }
+  } else if constexpr (kTwo) {
+    if (half == 1) win_v();
   }
   // the image goes out with one bulk copy (async proxy: fence the generic writes)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
-  if (tid == 0)
-    bulk_store_wait(a.ws + ((int64_t)kvh * a.ws_stride + j) * P::BLK, sKh, P::BLK);
+  if (tid == 0) {
+    if constexpr (kTwo) bulk_store_wait(gimg + 2 * P::OPB, sV, P::OPB);
+    else bulk_store_wait(gimg, sKh, P::BLK);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -781,15 +801,392 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
 }
 
+// ---------------------------------------------------------------------------
+// attention at head_dim 256
+//
+// Q' hi and lo of 128 score rows take 128 KB of shared memory at this width,
+// so keys stream in 32-key sub-blocks (K~ hi and lo 16 KB each, one buffer)
+// and V~^T and P in 64-key halves of a block image. Roles, barriers and the
+// tensor-pipe order S(0), S(1), PV(0), S(2), PV(1), ... are those of
+// prefill_kernel, per sub-block; TMEM holds S double-buffered (columns 0-31
+// and 32-63), the row sums (column 64, from the ones row of the V operand,
+// as a separate N=16 product because O alone is 256 columns wide) and O
+// (columns 256-511). The two 128-channel halves of a row's rotation (the
+// prologue's H q and the epilogue's H o) meet through shared memory: one
+// butterfly over channel bit 7.
+struct PA256 {
+  static constexpr int D = 256;
+  static constexpr int QB = 128 * D * 2;                 // fp16 Q' hi or lo [128 rows][256]
+  static constexpr int KSB = 32 * D * 2;                 // K~ hi or lo of 32 keys: 4 x [32 rows][64 ch]
+  static constexpr int NV = D + 16;                      // V~^T rows + a ones row + 15 zero rows
+  static constexpr int VH = NV * 128;                    // V operand of 64 keys
+  static constexpr int OFF_QH = 0;
+  static constexpr int OFF_QL = OFF_QH + QB;
+  static constexpr int OFF_KH = OFF_QL + QB;
+  static constexpr int OFF_KL = OFF_KH + KSB;
+  static constexpr int OFF_V = OFF_KL + KSB;
+  static constexpr int OFF_P = OFF_V + VH;               // fp16 P [128 rows][64 keys]
+  static constexpr int OFF_BAR = OFF_P + 128 * 64 * 2;
+  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int T_L = 64;                         // row-sum column
+  static constexpr int T_O = 256;                        // O columns 256..511
+  static_assert(OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && VH % 1024 == 0,
+                "swizzled operands on 1024-byte boundaries");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(OFF_V - OFF_KH >= 32 * 1024, "prologue exchange fits the K~ buffers");
+};
+
+__global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs a) {
+  using P = PA256;
+  constexpr int D = P::D;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                       ~uintptr_t(1023));
+  unsigned char* sQh = sm + P::OFF_QH;
+  unsigned char* sQl = sm + P::OFF_QL;
+  unsigned char* sKh = sm + P::OFF_KH;
+  unsigned char* sKl = sm + P::OFF_KL;
+  unsigned char* sV = sm + P::OFF_V;
+  unsigned char* sP = sm + P::OFF_P;
+  uint64_t* bar_kh = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // K~ hi of sub-block landed
+  uint64_t* bar_kl = bar_kh + 1;   // K~ lo landed
+  uint64_t* bar_v = bar_kh + 2;    // V~^T of a 64-key half landed
+  uint64_t* bar_s = bar_kh + 3;    // [2] S(j) complete (TMEM buffer j & 1); K~ lo free
+  uint64_t* bar_khf = bar_kh + 5;  // the K~ hi products of S(j) complete: K~ hi free
+  uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: its P half read, O and l current
+  uint64_t* bar_p = bar_kh + 7;    // P(j) written and O rescaled (one arrival per softmax warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
+  volatile int* fail = reinterpret_cast<volatile int*>(sm + P::OFF_MISC + 4);
+  float4* xch = reinterpret_cast<float4*>(sm + P::OFF_KH);  // prologue exchange (32 KB)
+  float4* ych = reinterpret_cast<float4*>(sm + P::OFF_QH);  // epilogue exchange (128 KB)
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127, half = (tid >> 7) & 1;
+  const int kvh = blockIdx.y;
+  const int ppc = 128 / a.G;
+  const int i0 = blockIdx.x * ppc;
+  const int my_g = row / ppc, my_i = i0 + row % ppc;
+  const bool my_valid = my_i < a.C && my_g < a.G;
+  const int64_t my_pos = a.pos0 + my_i;
+  const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;
+  const int64_t pmin = a.pos0 + i0;
+  const int hq = kvh * a.G + min(my_g, a.G - 1);
+
+  const int64_t win_pos0 = 128LL * a.n_tiles;
+  int n_tile_blk = a.n_tiles;
+  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
+  n_tile_blk = min(n_tile_blk, a.n_tiles);
+  int n_win_blk = 0;
+  for (int w = 0; 128 * w < a.win_len; ++w)
+    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
+  const int n_blk = n_tile_blk + n_win_blk;
+  const int n_sub = 4 * n_blk;  // 32-key sub-blocks
+  auto image = [&](int jj) -> const uint8_t* {
+    const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
+    return a.ws + ((int64_t)kvh * a.ws_stride + widx) * PC<256>::BLK;
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < 7; ++i) mbar_init1(bar_kh + i);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *fail = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_slot)),
+                 "r"(P::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  const float rs2 = 0.70710678118654752f;
+  if (tid < 256) {
+    // Q' row: two threads per row, each rotating its 128 channels; the
+    // butterfly over channel bit 7 pairs them through shared memory
+    float x[128];
+    if (my_valid) {
+      const float4* src =
+          reinterpret_cast<const float4*>(a.q + ((int64_t)my_i * a.Hq + hq) * D + 128 * half);
+#pragma unroll
+      for (int c4 = 0; c4 < 32; ++c4) {
+        const float4 v = src[c4];
+        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = 0.f;
+    }
+    fwht_reg<128>(x);
+    const float sc = a.qscale * rs2;
+#pragma unroll
+    for (int pass = 0; pass < 4; ++pass) {  // 32 channels per pass through the 32 KB buffer
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4)
+        xch[c4 * 256 + tid] = make_float4(x[32 * pass + 4 * c4], x[32 * pass + 4 * c4 + 1],
+                                          x[32 * pass + 4 * c4 + 2], x[32 * pass + 4 * c4 + 3]);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      float y[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 o = xch[c4 * 256 + (tid ^ 128)];
+        const float of[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float mine = x[32 * pass + 4 * c4 + e];
+          // channel c of half 0: (a + b) / sqrt 2; channel 128 + c: (a - b) / sqrt 2
+          y[4 * c4 + e] = (half == 0 ? mine + of[e] : of[e] - mine) * sc;
+        }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(y[8 * c8 + 2 * e], y[8 * c8 + 2 * e + 1], hi[e], lo[e]);
+        const int c = 128 * half + 32 * pass + 8 * c8;
+        *reinterpret_cast<uint4*>(sQh + sw_off(row, c, 128)) = *reinterpret_cast<uint4*>(hi);
+        *reinterpret_cast<uint4*>(sQl + sw_off(row, c, 128)) = *reinterpret_cast<uint4*>(lo);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else {
+    // rows 256 .. 271 of the V operand: a row of ones (the l product sums P
+    // into TMEM column 64) and zeros
+    for (int idx = tid - 256; idx < 16 * 8; idx += 64) {
+      const int r = idx >> 3, c16 = idx & 7;
+      const uint32_t w = r == 0 ? 0x3C003C00u : 0u;
+      *reinterpret_cast<uint4*>(sV + (D + r) * 128 + c16 * 16) = make_uint4(w, w, w, w);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_o = tmem + P::T_O, t_l = tmem + P::T_L;
+
+  if (warp == 9) {
+    // ---------------- loader
+    if (lane == 0 && n_sub > 0) {
+      int nkh = 1, nkl = 1, nv = 1;
+      auto load_k = [&](unsigned char* dst, int part, int jsub, uint64_t* b) {
+        // rows 32 s .. 32 s + 31 of each 64-channel block of the image's K~ part
+        const uint8_t* src = image(jsub >> 2) + part * PC<256>::OPB + (jsub & 3) * 4096;
+        mbar_expect_tx(b, P::KSB);
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) bulk_copy_tx(dst + kb * 4096, src + kb * 16384, 4096, b);
+      };
+      auto load_v = [&](int vh) {  // 64-key half vh of the run of sub-blocks
+        const uint8_t* src = image(vh >> 1) + 2 * PC<256>::OPB + (vh & 1) * (D * 128);
+        mbar_expect_tx(bar_v, D * 128);
+        bulk_copy_tx(sV, src, D * 128, bar_v);
+      };
+      load_k(sKh, 0, 0, bar_kh);
+      load_k(sKl, 1, 0, bar_kl);
+      load_v(0);
+      for (int j = 1; j < n_sub; ++j) {
+        if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail)) break;
+        load_k(sKh, 0, j, bar_kh);
+        ++nkh;
+        if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail)) break;
+        load_k(sKl, 1, j, bar_kl);
+        ++nkl;
+        // half (j - 1) / 2 of V follows PV(j - 2), the last product of the previous half
+        if (j >= 3 && (j & 1)) {
+          if (!mbar_wait_flag(bar_o, (uint32_t)(j - 2) & 1u, fail)) break;
+          load_v((j - 1) >> 1);
+          ++nv;
+        }
+      }
+      mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u);
+      mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u);
+      mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ---------------- MMA issuer
+    if (lane == 0 && n_sub > 0) {
+      uint64_t* last = nullptr;
+      uint32_t last_par = 0;
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t t_s = tmem + 32 * (j & 1);
+        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * 32 * 128 + (kk & 3) * 32;
+          mma_f16(t_s, sdesc(su32(sQh) + off_a), sdesc(su32(sKh) + off_b), idesc<32>(), kk > 0);
+          mma_f16(t_s, sdesc(su32(sQl) + off_a), sdesc(su32(sKh) + off_b), idesc<32>(), 1);
+        }
+        mma_commit(bar_khf);
+        last = bar_khf; last_par = (uint32_t)j & 1u;
+        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * 32 * 128 + (kk & 3) * 32;
+          mma_f16(t_s, sdesc(su32(sQh) + off_a), sdesc(su32(sKl) + off_b), idesc<32>(), 1);
+        }
+        mma_commit(bar_s + (j & 1));
+        last = bar_s + (j & 1); last_par = (uint32_t)(j >> 1) & 1u;
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int j = 0; ok && j < n_sub; ++j) {
+        if (j + 1 < n_sub && !issue_s(j + 1)) break;
+        if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_v, (uint32_t)(j >> 1) & 1u, fail)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t off = (uint32_t)(2 * (j & 1) + i) * 32;  // keys 32 (j & 1) + 16 i ..
+          const uint32_t acc = (j > 0 || i > 0) ? 1u : 0u;
+          mma_f16(t_o, sdesc(su32(sP) + off), sdesc(su32(sV) + off), idesc<256>(), acc);
+          mma_f16(t_l, sdesc(su32(sP) + off), sdesc(su32(sV) + D * 128 + off), idesc<16>(), acc);
+        }
+        mma_commit(bar_o);
+        last = bar_o; last_par = (uint32_t)j & 1u;
+      }
+      if (last != nullptr && !mbar_wait_bounded(last, last_par)) *fail = 1;
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax (warps 0-7): two threads per row, 16 keys each
+    float m_ref = -INFINITY;
+    const uint32_t lb = lane_base_of(warp);
+    for (int j = 0; j < n_sub; ++j) {
+      const int jb = j >> 2, sb = j & 3;
+      const bool is_tile = jb < n_tile_blk;
+      const int64_t kpos0 = (is_tile ? 128LL * jb : win_pos0 + 128LL * (jb - n_tile_blk)) + 32 * sb;
+      const int nkeys = (is_tile ? 128 : min(128, a.win_len - 128 * (jb - n_tile_blk))) - 32 * sb;
+      const bool full_vis = kpos0 + 31 <= pmin && nkeys >= 32;
+      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
+      if (__any_sync(0xffffffffu, bad || *fail != 0)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float sv[32];
+      tmem_ld32(tmem + 32 * (j & 1) + lb, sv);
+      float mblk = -INFINITY;
+      if (full_vis) {
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) mblk = fmax3(mblk, sv[u], sv[u + 1]);
+        if (!my_valid) mblk = -INFINITY;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const bool vis = my_valid && u < nkeys && kpos0 + u <= my_pos;
+          sv[u] = vis ? sv[u] : -INFINITY;
+          mblk = fmaxf(mblk, sv[u]);
+        }
+      }
+      const bool need = mblk > m_ref + 8.0f;
+      const float m_new = need ? mblk : m_ref;
+      const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
+      m_ref = m_new;
+      const float msub = m_ref == -INFINITY ? INFINITY : m_ref;
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __half2 hp = __floats2half2_rn(ex2_ftz(sv[16 * half + 2 * e] - msub),
+                                             ex2_ftz(sv[16 * half + 2 * e + 1] - msub));
+        h[e] = *reinterpret_cast<const uint32_t*>(&hp);
+      }
+      // O and l belong to PV(j-1) until it completes
+      if (j == 0 || mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            float v[32];
+            tmem_ld32(t_o + lb + half * (D / 2) + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(t_o + lb + half * (D / 2) + c0, v);
+          }
+          if (half == 0) {
+            const float l = tmem_ld1(t_l + lb);
+            tmem_st1(t_l + lb, l * alpha);
+          }
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8)
+          *reinterpret_cast<uint4*>(sP + sw_off(row, 32 * (j & 1) + 16 * half + 8 * c8, 128)) =
+              make_uint4(h[4 * c8], h[4 * c8 + 1], h[4 * c8 + 2], h[4 * c8 + 3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const bool ok = *fail == 0;
+  // ---- epilogue: O / l, one inverse rotation (two threads per row), store
+  if (tid < 256) {
+    const uint32_t lb = lane_base_of(warp);
+    float o[128];
+    float l_row = 0.f;
+    if (n_sub > 0 && ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_o + lb + 128 * half + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c0 + i] = v[i];
+      }
+      l_row = tmem_ld1(t_l + lb);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 128; ++c) o[c] = 0.f;
+    }
+    const float inv = (l_row > 0.f ? 1.0f / l_row : 0.f) * rs2;
+#pragma unroll
+    for (int c = 0; c < 128; ++c) o[c] *= inv;
+    fwht_reg<128>(o);
+    // Q' is no longer read (the last MMA completed): its 128 KB hold the exchange
+#pragma unroll
+    for (int c4 = 0; c4 < 32; ++c4)
+      ych[c4 * 256 + tid] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (my_valid) {
+      float4* dst = reinterpret_cast<float4*>(a.out + ((int64_t)my_i * a.Hq + hq) * D + 128 * half);
+#pragma unroll
+      for (int c4 = 0; c4 < 32; ++c4) {
+        const float4 p = ych[c4 * 256 + (tid ^ 128)];
+        float4 v;
+        if (half == 0) {
+          v = make_float4(o[4 * c4] + p.x, o[4 * c4 + 1] + p.y, o[4 * c4 + 2] + p.z, o[4 * c4 + 3] + p.w);
+        } else {
+          v = make_float4(p.x - o[4 * c4], p.y - o[4 * c4 + 1], p.z - o[4 * c4 + 2], p.w - o[4 * c4 + 3]);
+        }
+        if (!ok) v = make_float4(NAN, NAN, NAN, NAN);
+        dst[c4] = v;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
+}
+
 template <int D, int SB, int VB>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   using P = PC<D>;
+  constexpr int att_smem = D == 256 ? PA256::SMEM : P::SMEM;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    if constexpr (D == 256)
+      e = cudaFuncSetAttribute(prefill_kernel_d256, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem);
+    else
+      e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prefill_dequant_kernel<D, SB, VB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::template DQ<VB>::SMEM);
@@ -804,7 +1201,10 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
-  prefill_kernel<D><<<grid, P::NTHR_ATT, P::SMEM, st>>>(a);
+  if constexpr (D == 256)
+    prefill_kernel_d256<<<grid, 320, att_smem, st>>>(a);
+  else
+    prefill_kernel<D><<<grid, P::NTHR_ATT, att_smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -850,6 +1250,10 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
     case 12822: return launch_prefill_d<128, 2, 2>(a, st);
     case 12844: return launch_prefill_d<128, 4, 4>(a, st);
     case 12824: return launch_prefill_d<128, 2, 4>(a, st);
+    case 25642: return launch_prefill_d<256, 4, 2>(a, st);
+    case 25622: return launch_prefill_d<256, 2, 2>(a, st);
+    case 25644: return launch_prefill_d<256, 4, 4>(a, st);
+    case 25624: return launch_prefill_d<256, 2, 4>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -90,7 +90,9 @@ def test_prefill_host_validation(lib):
     f.argtypes = None
     assert f(*args(512, 2000, 10, 300)) == -4          # chunk beyond the cache
     L256 = kvarn.layout(256)
-    assert f(*args(16, 0, 1, 16, D=256, lay=L256)) == -3  # head_dim 256 not yet supported
+    assert f(*args(16, 0, 1, 16, D=256, lay=L)) == -3     # layout of another head_dim
+    assert f(*args(16, 0, 1, 16, D=96, lay=L256)) == -3   # head_dim 96
+    assert f(*args(0, 0, 1, 16, D=256, lay=L256)) == 0    # head_dim 256: empty chunk
     assert f(*args(16, 0, 1, 16, Hq=80)) == -3            # GQA group of 10
     assert f(*args(0, 0, 0, 0)) == 0                      # empty chunk enqueues nothing
     # the workspace bound covers every tile and window block of 8 KV heads ...
@@ -98,6 +100,8 @@ def test_prefill_host_validation(lib):
     assert lib.kvarn_prefill_workspace_bytes(10, 300, 8, 128, ctypes.byref(need)) == 0
     blk = 3 * 128 * 128 * 2
     assert need.value == (10 + 3) * 8 * blk
+    assert lib.kvarn_prefill_workspace_bytes(10, 300, 4, 256, ctypes.byref(need)) == 0
+    assert need.value == (10 + 3) * 4 * 3 * 128 * 256 * 2
     # ... a chunk at 1000..1511 sees the 10 tiles and 2 of the window's 3 blocks
     assert f(*args(512, 1000, 10, 300, wsb=12 * 8 * blk - 1)) == -5
 

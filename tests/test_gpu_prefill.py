@@ -98,3 +98,37 @@ def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
                      scale_bits=sb, v_bits=4, cached=cached)
     for p in run.snap:
         run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=23))
+
+
+@pytest.mark.parametrize("Hq,Hkv,n,chunk,W,sb,vb,cached", [
+    (16, 4, 1400, 512, 256, 32, 2, False),   # the batched-decode head shape: 10 tiles + window
+    (16, 4, 1400, 512, 256, 32, 2, True),
+    (16, 2, 700, 256, 256, 16, 2, True),     # GQA group 8, f16 scales
+    (4, 4, 450, 100, 128, 32, 4, False),     # group 1, k4v4, ragged chunks, window wraps
+])
+def test_prefill_head_dim_256(Hq, Hkv, n, chunk, W, sb, vb, cached):
+    """head_dim 256: keys stream through the attention kernel in 32-key
+    sub-blocks, the rotations pair two threads per row."""
+    run = PrefillRun("batched_d256_decode", 8, n, Hq=Hq, Hkv=Hkv, D=256, W=W, chunk=chunk,
+                     scale_bits=sb, v_bits=vb, cached=cached)
+    for p in run.snap:
+        run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=17))
+
+
+def test_prefill_head_dim_256_chunk_of_one_equals_decode():
+    """A one-token chunk at head_dim 256 is a decode step over the same cache."""
+    n = 128 * 2 + 40
+    run = PrefillRun("batched_d256_decode", 9, n, Hq=8, Hkv=2, D=256, W=128, chunk=1, keep=[n - 1])
+    s = run.snap[n - 1]
+    dev = torch.device("cuda:0")
+    q = torch.from_numpy(run.q[n - 1:n]).to(dev)
+    dec = kvarn.decode_attention(q, run.tiles, run.table[None], torch.tensor([s["n_tiles"]],
+                                 dtype=torch.int32, device=dev),
+                                 torch.from_numpy(s["win_k"])[None].to(dev),
+                                 torch.from_numpy(s["win_v"])[None].to(dev),
+                                 torch.tensor([s["start"]], dtype=torch.int32, device=dev),
+                                 torch.tensor([s["length"]], dtype=torch.int32, device=dev),
+                                 run.lay).cpu().numpy()
+    for h in range(8):
+        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-3
+    run.check(n - 1, [(0, h) for h in range(8)])
