@@ -188,8 +188,10 @@ def run_reference(args, rank):
     print(json.dumps(out), flush=True)
 
 
-def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512, Wp=256, reps=3):
-    """One layer of the 15,500-token 8B-like prompt: per chunk append, promote, prefill
+def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512, Wp=256, reps=3,
+                      workload="qwen3_8b_prefill", hq=None, hkv=None, label="Qwen3-8B-like"):
+    """One layer of a chunked prompt (by default the 15,500-token 8B-like one,
+    32q/8kv, head_dim 128): per chunk append, promote, prefill
     attention (block dequantisation of the tiles promoted since the previous
     chunk and of the window blocks, into one workspace kept for the whole
     prompt, + tcgen05 attention). Reports prompt tokens/s
@@ -198,15 +200,17 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
     multiply-adds, counted once)."""
     import torch
     from kv_cache_quantization_token_gb300 import kvarn, synth
-    ks, vs = synth.kv_layer("qwen3_8b_prefill", 0, HKV, n_tok, D)
-    q = torch.from_numpy(synth.queries("qwen3_8b_prefill", 0, (n_tok, HQ, D))).to(dev)
+    HQ_, HKV_ = (hq or HQ), (hkv or HKV)
+    D_ = lay.head_dim
+    ks, vs = synth.kv_layer(workload, 0, HKV_, n_tok, D_)
+    q = torch.from_numpy(synth.queries(workload, 0, (n_tok, HQ_, D_))).to(dev)
     kn_all = torch.from_numpy(np.ascontiguousarray(ks.transpose(1, 0, 2))).to(dev)  # [n][Hkv][D]
     vn_all = torch.from_numpy(np.ascontiguousarray(vs.transpose(1, 0, 2))).to(dev)
     rb = lay.record_bytes
     cap = 128 * ((Wp - 1 + chunk + 127) // 128)
     max_tiles = n_tok // 128 + 1
-    tiles = torch.empty(HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
-    tab = (np.arange(HKV)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
+    tiles = torch.empty(HKV_ * max_tiles * rb, dtype=torch.uint8, device=dev)
+    tab = (np.arange(HKV_)[:, None] * max_tiles + np.arange(max_tiles)[None, :]) * rb
     table = torch.from_numpy(tab.astype(np.int64)).to(dev)
     # promotions of one chunk go out as one compress launch: the (source row,
     # destination record) pairs of every due tile and KV head, prepared ahead
@@ -217,18 +221,18 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
         length += min(chunk, n_tok - pos0)
         k = (length - Wp) // 128 + 1 if length >= Wp else 0
         if k:
-            src = [h * cap + (start + 128 * i) % cap for i in range(k) for h in range(HKV)]
-            dst = [int(tab[h, n_tiles + i]) for i in range(k) for h in range(HKV)]
+            src = [h * cap + (start + 128 * i) % cap for i in range(k) for h in range(HKV_)]
+            dst = [int(tab[h, n_tiles + i]) for i in range(k) for h in range(HKV_)]
             prom[pos0] = (k, torch.tensor(src, dtype=torch.int64, device=dev),
                           torch.tensor(dst, dtype=torch.int64, device=dev))
             start, length, n_tiles = (start + 128 * k) % cap, length - 128 * k, n_tiles + k
-    win_k = torch.zeros(1, HKV, cap, D, device=dev)
+    win_k = torch.zeros(1, HKV_, cap, D_, device=dev)
     win_v = torch.zeros_like(win_k)
     ws_start = torch.zeros(1, dtype=torch.int32, device=dev)
     ws_len = torch.zeros(1, dtype=torch.int32, device=dev)
     ws_nt = torch.zeros(1, dtype=torch.int32, device=dev)
-    out = torch.empty(n_tok, HQ, D, device=dev)
-    ws_p = torch.empty(kvarn.prefill_workspace_bytes(max_tiles, cap, HKV, D), dtype=torch.uint8,
+    out = torch.empty(n_tok, HQ_, D_, device=dev)
+    ws_p = torch.empty(kvarn.prefill_workspace_bytes(max_tiles, cap, HKV_, D_), dtype=torch.uint8,
                        device=dev)
     ev = []
 
@@ -248,7 +252,7 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
             k = 0
             if pos0 in prom:  # promote: while the window holds >= W tokens, its oldest 128
                 k, psrc, pdst = prom[pos0]
-                kvarn.compress_tile(win_k.view(-1, D), win_v.view(-1, D), psrc, tiles, pdst, lay)
+                kvarn.compress_tile(win_k.view(-1, D_), win_v.view(-1, D_), psrc, tiles, pdst, lay)
                 n_tiles += k
                 start = (start + 128 * k) % cap
                 length -= 128 * k
@@ -281,8 +285,8 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
             kvarn.window_advance(ws_start, ws_len, None, C, 0, cap)
             length += C
             while length >= Wp:
-                src = torch.tensor([h * cap + start for h in range(HKV)], dtype=torch.int64, device=dev)
-                kvarn.compress_tile(win_k.view(-1, D), win_v.view(-1, D), src, tiles,
+                src = torch.tensor([h * cap + start for h in range(HKV_)], dtype=torch.int64, device=dev)
+                kvarn.compress_tile(win_k.view(-1, D_), win_v.view(-1, D_), src, tiles,
                                     table[:, n_tiles].contiguous(), lay)
                 n_tiles += 1
                 start = (start + 128) % cap
@@ -311,19 +315,32 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
     attn_ms = float(sum(a.elapsed_time(b) for a, b in ev))
     # algorithmic multiply-adds: every visible (query, key) pair, Q.K and P.V
     vis = sum((p + 1) for p in range(n_tok))
-    macs = 2.0 * vis * HQ * D
+    macs = 2.0 * vis * HQ_ * D_
     tflops = 2.0 * macs / (attn_ms * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", 1900.0))
-    return {"workload": f"Qwen3-8B-like chunked prefill: {n_tok}-token prompt, {chunk}-token chunks, W={Wp}, "
-                        f"{HQ}q/{HKV}kv, head_dim {D}, causal; one layer",
-            "layer_ms": layer_ms, "attention_ms": attn_ms,
-            "prompt_tokens_per_s_36_layers": n_tok / (LAYERS * layer_ms * 1e-3),
-            "algorithmic_macs": macs, "achieved_tflops": tflops,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": tflops / peak_tf, "traffic": None,
-                         "kernel": "prefill_kernel<128>",
-                         "peak_source": peak_kind + " (dense bf16 burst; fp16 runs at the bf16 rate)"},
-            "mma": "tcgen05 kind::f16, Q and K split hi+lo (3 MMAs for Q.K, 1 for P.V)"}
+    res = {"workload": f"{label} chunked prefill: {n_tok}-token prompt, {chunk}-token chunks, W={Wp}, "
+                       f"{HQ_}q/{HKV_}kv, head_dim {D_}, causal; one layer",
+           "layer_ms": layer_ms, "attention_ms": attn_ms,
+           "prompt_tokens_per_s_one_layer": n_tok / (layer_ms * 1e-3),
+           "algorithmic_macs": macs, "achieved_tflops": tflops,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                        "frac": tflops / peak_tf, "traffic": None,
+                        "kernel": "prefill_kernel_d256" if D_ == 256 else f"prefill_kernel<{D_}>",
+                        "peak_source": peak_kind + " (dense bf16 burst; fp16 runs at the bf16 rate)"},
+           "mma": "tcgen05 kind::f16, Q and K split hi+lo (3 MMAs for Q.K, 1 for P.V)"
+                  + ("; keys in 32-key sub-blocks" if D_ == 256 else "")}
+    if workload == "qwen3_8b_prefill":
+        res["prompt_tokens_per_s_36_layers"] = n_tok / (LAYERS * layer_ms * 1e-3)
+    return res
+
+
+def run_prefill_d256(dev, stream, peaks, peak_kind):
+    """Chunked prefill with the batched-decode head shape (16q/4kv, head_dim
+    256): one layer of an 8,192-token prompt in 512-token chunks, W=256."""
+    from kv_cache_quantization_token_gb300 import kvarn
+    return run_prefill_bench(dev, stream, kvarn.layout(256), peaks, peak_kind, n_tok=8192,
+                             workload="batched_d256_decode", hq=16, hkv=4,
+                             label="16q/4kv head_dim-256")
 
 
 def run_decode_sweeps(dev, lay, peaks, peak_kind):
@@ -556,7 +573,7 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--section", default="all",
-                    choices=["all", "prefill", "decode-sweeps", "compress"],
+                    choices=["all", "prefill", "prefill-d256", "decode-sweeps", "compress"],
                     help="run one secondary measurement alone and print its JSON (for profiling)")
     args = ap.parse_args()
 
@@ -583,7 +600,11 @@ def main():
     if args.section != "all":
         peaks, peak_kind = measured_peaks()
         if args.section == "prefill":
-            sec = run_prefill_bench(dev, torch.cuda.Stream(device=dev), lay, peaks, peak_kind)
+            st = torch.cuda.Stream(device=dev)
+            sec = {"head_dim_128": run_prefill_bench(dev, st, lay, peaks, peak_kind),
+                   "head_dim_256": run_prefill_d256(dev, st, peaks, peak_kind)}
+        elif args.section == "prefill-d256":
+            sec = run_prefill_d256(dev, torch.cuda.Stream(device=dev), peaks, peak_kind)
         elif args.section == "compress":
             sec = run_compress_bench(dev, torch.cuda.Stream(device=dev), lay, args.warmup,
                                      peaks["hbm_gbs"], peak_kind)
@@ -822,8 +843,10 @@ def main():
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
     compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
 
-    # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256)
+    # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256), and
+    # an 8,192-token prompt with head_dim-256 heads
     prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
+    prefill_d256 = run_prefill_d256(dev, stream, peaks, peak_kind)
     # ---- decode at other contexts and batched large-head decode
     sweeps = run_decode_sweeps(dev, lay, peaks, peak_kind)
 
@@ -858,6 +881,7 @@ def main():
                                    "decode.back_to_back_timing)", "peak_source": peak_kind},
             "compress": compress,
             "prefill": prefill,
+            "prefill_d256": prefill_d256,
             "decode_sweeps": sweeps,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

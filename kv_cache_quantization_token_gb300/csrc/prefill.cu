@@ -1088,9 +1088,10 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       const float msub = m_ref == -INFINITY ? INFINITY : m_ref;
       uint32_t h[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const __half2 hp = __floats2half2_rn(ex2_ftz(sv[16 * half + 2 * e] - msub),
-                                             ex2_ftz(sv[16 * half + 2 * e + 1] - msub));
+      for (int e = 0; e < 8; ++e) {  // this thread's 16 keys (selects keep sv in registers)
+        const float s0 = half ? sv[16 + 2 * e] : sv[2 * e];
+        const float s1 = half ? sv[17 + 2 * e] : sv[2 * e + 1];
+        const __half2 hp = __floats2half2_rn(ex2_ftz(s0 - msub), ex2_ftz(s1 - msub));
         h[e] = *reinterpret_cast<const uint32_t*>(&hp);
       }
       // O and l belong to PV(j-1) until it completes
