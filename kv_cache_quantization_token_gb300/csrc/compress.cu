@@ -120,6 +120,31 @@ __device__ __forceinline__ void halve_mm(float (&lo)[8], float (&hi)[8], int mas
   }
 }
 
+// Three-input minimum / maximum (a NaN operand is ignored, as in fminf).
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// floor(u) for 0 <= u < 2^23, in the low bits of the result: u + 2^23
+// rounded toward -inf is 2^23 + floor(u) exactly (the spacing of floats in
+// [2^23, 2^24) is 1). The RTN value u = (y - lo) / delta + 1/2 lies in
+// [1/2, 2^b - 1/2] up to rounding, so its floor is the code itself.
+__device__ __forceinline__ uint32_t floor_bits(float u) {
+  return __float_as_uint(__fadd_rd(u, 8388608.0f));
+}
+// 1 / delta, or 0 when delta is 0 or subnormal (every code of the group is
+// then 0 and the group reconstructs to lo)
+__device__ __forceinline__ float rtn_inv(float delta) {
+  return delta >= 1.17549435e-38f ? 1.0f / delta : 0.f;
+}
+
 // Usable std: larger than 2^-20 times the RMS of the same group (false for NaN).
 __device__ __forceinline__ bool usable(float var, float mean) {
   const float sd = sqrtf(var);
@@ -321,9 +346,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     float lo[8], hi[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      lo[m] = y(0, m); hi[m] = y(0, m);
-#pragma unroll
-      for (int i = 1; i < 8; ++i) { lo[m] = fminf(lo[m], y(i, m)); hi[m] = fmaxf(hi[m], y(i, m)); }
+      lo[m] = fminf(min3f(min3f(min3f(y(0, m), y(1, m), y(2, m)), y(3, m), y(4, m)), y(5, m), y(6, m)), y(7, m));
+      hi[m] = fmaxf(max3f(max3f(max3f(y(0, m), y(1, m), y(2, m)), y(3, m), y(4, m)), y(5, m), y(6, m)), y(7, m));
     }
     if (C::TGW >= 1) halve_mm<8>(lo, hi, 1 << C::CG_BITS, (lane >> C::CG_BITS) & 1);
     if (C::TGW >= 2) halve_mm<4>(lo, hi, 1 << (C::CG_BITS + 1), (lane >> (C::CG_BITS + 1)) & 1);
@@ -342,7 +366,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       l = fminf(l, shfl_xor(l, 1));
       h = fmaxf(h, shfl_xor(h, 1));
       const float delta = (h - l) / 15.0f;
-      const float inv = delta > 0.f ? 1.0f / delta : 0.f;
+      const float inv = rtn_inv(delta);
       if (h_own == 0) {
         ch_a[p_own] = l;
         ch_b[p_own] = inv;
@@ -363,10 +387,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float2 u = fma2(add2(y2[i][k], nl), inv, f2(0.5f, 0.5f));
-        const int c0 = min(15, max(0, __float2int_rd(u.x)));
-        const int c1 = min(15, max(0, __float2int_rd(u.y)));
-        w0 |= (uint32_t)c0 << (4 * i);
-        w1 |= (uint32_t)c1 << (4 * i);
+        w0 |= (floor_bits(u.x) & 15u) << (4 * i);
+        w1 |= (floor_bits(u.y) & 15u) << (4 * i);
       }
       const int ca = (cg & 3) | ((2 * k) << 2) | ((cg >> 2) << 5);
       const int cb = (cg & 3) | ((2 * k + 1) << 2) | ((cg >> 2) << 5);
@@ -379,9 +401,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     float lo[8], hi[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      lo[i] = y(i, 0); hi[i] = y(i, 0);
-#pragma unroll
-      for (int m = 1; m < 8; ++m) { lo[i] = fminf(lo[i], y(i, m)); hi[i] = fmaxf(hi[i], y(i, m)); }
+      lo[i] = fminf(min3f(min3f(min3f(y(i, 0), y(i, 1), y(i, 2)), y(i, 3), y(i, 4)), y(i, 5), y(i, 6)), y(i, 7));
+      hi[i] = fmaxf(max3f(max3f(max3f(y(i, 0), y(i, 1), y(i, 2)), y(i, 3), y(i, 4)), y(i, 5), y(i, 6)), y(i, 7));
     }
     halve_mm<8>(lo, hi, 1, lane & 1);
     halve_mm<4>(lo, hi, 2, (lane >> 1) & 1);
@@ -391,7 +412,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       hi[0] = fmaxf(hi[0], shfl_xor(hi[0], 8));
     }
     const float delta = (hi[0] - lo[0]) / (float)kVMax;
-    const float inv = delta > 0.f ? 1.0f / delta : 0.f;
+    const float inv = rtn_inv(delta);
     const int g = (D == 256) ? ((cg >> 4) & 1) : 0;
     __syncthreads();  // every thread is past its last read of the tile
     if (tok_writer) {
@@ -410,15 +431,15 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
         // channel 32 (cg >> 2) + 4 m + (cg & 3) of slot m: byte 8 (cg >> 2) + m
         // of the token row, bits 2 (cg & 3); the four lanes of a channel
         // quadruple fill eight bytes together
-        unsigned long long w = 0;
+        uint32_t wl = 0, wh = 0;  // slot m's code in bits 8 (m % 4) of word m / 4
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
-          const int c0 = min(kVMax, max(0, __float2int_rd(u.x)));
-          const int c1 = min(kVMax, max(0, __float2int_rd(u.y)));
-          w |= (unsigned long long)c0 << (8 * (2 * k) + 2 * (cg & 3));
-          w |= (unsigned long long)c1 << (8 * (2 * k + 1) + 2 * (cg & 3));
+          const uint32_t c = (floor_bits(u.x) & 3u) | ((floor_bits(u.y) & 3u) << 8);
+          if (k < 2) wl |= c << (16 * k);
+          else wh |= c << (16 * (k - 2));
         }
+        unsigned long long w = (((unsigned long long)wh << 32) | wl) << (2 * (cg & 3));
         w |= __shfl_xor_sync(0xffffffffu, w, 1);
         w |= __shfl_xor_sync(0xffffffffu, w, 2);
         if ((i & 3) == (cg & 3))
@@ -428,20 +449,15 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
         // 16 (cg >> 2) + 2 m + ((cg & 3) >> 1), nibble (cg & 3) & 1; the four
         // lanes of a channel quadruple fill sixteen bytes together
         const int sh = 8 * ((cg & 3) >> 1) + 4 * (cg & 1);
-        unsigned long long w0 = 0, w1 = 0;  // bytes 0..7 (slots 0..3), 8..15 (slots 4..7)
+        uint32_t h4[4];  // slots 2q, 2q+1 in bits 0 and 16 of word q
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
-          const unsigned long long c0 = (unsigned long long)min(kVMax, max(0, __float2int_rd(u.x)));
-          const unsigned long long c1 = (unsigned long long)min(kVMax, max(0, __float2int_rd(u.y)));
-          if (k < 2) {
-            w0 |= c0 << (16 * (2 * k) + sh);
-            w0 |= c1 << (16 * (2 * k + 1) + sh);
-          } else {
-            w1 |= c0 << (16 * (2 * k - 4) + sh);
-            w1 |= c1 << (16 * (2 * k - 3) + sh);
-          }
+          h4[k] = (floor_bits(u.x) & 15u) | ((floor_bits(u.y) & 15u) << 16);
         }
+        // bytes 0..7 (slots 0..3), 8..15 (slots 4..7)
+        unsigned long long w0 = (((unsigned long long)h4[1] << 32) | h4[0]) << sh;
+        unsigned long long w1 = (((unsigned long long)h4[3] << 32) | h4[2]) << sh;
         w0 |= __shfl_xor_sync(0xffffffffu, w0, 1);
         w1 |= __shfl_xor_sync(0xffffffffu, w1, 1);
         w0 |= __shfl_xor_sync(0xffffffffu, w0, 2);
