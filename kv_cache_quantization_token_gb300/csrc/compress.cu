@@ -145,10 +145,10 @@ __device__ __forceinline__ float rtn_inv(float delta) {
   return delta >= 1.17549435e-38f ? 1.0f / delta : 0.f;
 }
 
-// Usable std: larger than 2^-20 times the RMS of the same group (false for NaN).
+// Usable std: larger than 2^-20 times the RMS of the same group, compared in
+// squares, var > 2^-40 (var + mean^2) (false for NaN).
 __device__ __forceinline__ bool usable(float var, float mean) {
-  const float sd = sqrtf(var);
-  return sd > ldexpf(sqrtf(var + mean * mean), -20);
+  return var > 0x1p-40f * fmaf(mean, mean, var);
 }
 
 template <int D, int SB, int VB>
@@ -234,7 +234,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
   for (int k = 0; k < 4; ++k) sinv2[k] = f2(1.0f / sqrt_d, 1.0f / sqrt_d);
 #pragma unroll
   for (int i = 0; i < 8; ++i) rinv2[i] = f2(1.0f, 1.0f);
-  float s_own = sqrt_d, r_own = 1.0f;
+  float s_own = sqrt_d, r_own = 1.0f;             // the factors (stored in the record)
+  float si_own = 1.0f / sqrt_d, ri_own = 1.0f;    // their reciprocals (applied to the tile)
   const int p_own = tid >> 1, h_own = tid & 1;
   // token held by this lane after the row halving: bits (cg&1, cg>>1&1, cg>>2&1) -> 4,2,1
   const int tau = ((cg & 1) << 2) | (((cg >> 1) & 1) << 1) | ((cg >> 2) & 1);
@@ -289,8 +290,11 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       }
       merge_eq(mean, m2, shfl_xor(mean, 1), shfl_xor(m2, 1), 64.f);
       const float var = m2 * (1.0f / 128.0f);
-      if (usable(var, mean)) s_own = sqrtf(var);
-      if (h_own == 0) ch_a[p_own] = 1.0f / s_own;
+      if (usable(var, mean)) {
+        s_own = sqrtf(var);
+        si_own = rsqrtf(var);
+      }
+      if (h_own == 0) ch_a[p_own] = si_own;
     }
     __syncthreads();
 #pragma unroll
@@ -320,8 +324,11 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     if (C::CG_BITS >= 5) merge_eq(rm[0], rq[0], shfl_xor(rm[0], 16), shfl_xor(rq[0], 16), 128.f);
     {
       const float var = rq[0] * (1.0f / (float)D);
-      if (usable(var, rm[0])) r_own = sqrtf(var);
-      const float ri = 1.0f / r_own;
+      if (usable(var, rm[0])) {
+        r_own = sqrtf(var);
+        ri_own = rsqrtf(var);
+      }
+      const float ri = ri_own;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float r = __shfl_sync(0xffffffffu, ri, src_lane(i));
