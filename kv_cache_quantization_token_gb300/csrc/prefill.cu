@@ -40,6 +40,7 @@
 //             inverse).
 // Every wait is bounded; a CTA that gives up writes NaN rows, frees its TMEM
 // and returns.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -48,6 +49,7 @@
 namespace kvarn {
 namespace {
 
+namespace cg = cooperative_groups;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -882,7 +884,12 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   for (int w = 0; 128 * w < a.win_len; ++w)
     if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
   const int n_blk = n_tile_blk + n_win_blk;
-  const int n_sub = 4 * n_blk;  // 32-key sub-blocks
+  // key split: with gridDim.z = 2 the two CTAs of a cluster take alternate
+  // 128-key blocks of the same rows and merge (m, l, O) at the end
+  const int rank = blockIdx.z, nsplit = gridDim.z;
+  const int n_loc = n_blk > rank ? (n_blk - rank + nsplit - 1) / nsplit : 0;
+  const int n_sub = 4 * n_loc;  // this CTA's 32-key sub-blocks
+  auto gblk = [&](int k) { return k * nsplit + rank; };  // local block -> visible block
   auto image = [&](int jj) -> const uint8_t* {
     const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
     return a.ws + ((int64_t)kvh * a.ws_stride + widx) * PC<256>::BLK;
@@ -966,19 +973,20 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_o = tmem + P::T_O, t_l = tmem + P::T_L;
 
+  float m_ref = -INFINITY;  // softmax threads: the reference maximum of their row
   if (warp == 9) {
     // ---------------- loader
     if (lane == 0 && n_sub > 0) {
       int nkh = 1, nkl = 1, nv = 1;
       auto load_k = [&](unsigned char* dst, int part, int jsub, uint64_t* b) {
         // rows 32 s .. 32 s + 31 of each 64-channel block of the image's K~ part
-        const uint8_t* src = image(jsub >> 2) + part * PC<256>::OPB + (jsub & 3) * 4096;
+        const uint8_t* src = image(gblk(jsub >> 2)) + part * PC<256>::OPB + (jsub & 3) * 4096;
         mbar_expect_tx(b, P::KSB);
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) bulk_copy_tx(dst + kb * 4096, src + kb * 16384, 4096, b);
       };
       auto load_v = [&](int vh) {  // 64-key half vh of the run of sub-blocks
-        const uint8_t* src = image(vh >> 1) + 2 * PC<256>::OPB + (vh & 1) * (D * 128);
+        const uint8_t* src = image(gblk(vh >> 1)) + 2 * PC<256>::OPB + (vh & 1) * (D * 128);
         mbar_expect_tx(bar_v, D * 128);
         bulk_copy_tx(sV, src, D * 128, bar_v);
       };
@@ -1055,10 +1063,9 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
     __syncwarp();
   } else {
     // ---------------- softmax (warps 0-7): two threads per row, 16 keys each
-    float m_ref = -INFINITY;
     const uint32_t lb = lane_base_of(warp);
     for (int j = 0; j < n_sub; ++j) {
-      const int jb = j >> 2, sb = j & 3;
+      const int jb = gblk(j >> 2), sb = j & 3;
       const bool is_tile = jb < n_tile_blk;
       const int64_t kpos0 = (is_tile ? 128LL * jb : win_pos0 + 128LL * (jb - n_tile_blk)) + 32 * sb;
       const int nkeys = (is_tile ? 128 : min(128, a.win_len - 128 * (jb - n_tile_blk))) - 32 * sb;
@@ -1125,12 +1132,12 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const bool ok = *fail == 0;
+  bool ok = *fail == 0;
   // ---- epilogue: O / l, one inverse rotation (two threads per row), store
+  const uint32_t lb = lane_base_of(warp);
+  float o[128];
+  float l_row = 0.f;
   if (tid < 256) {
-    const uint32_t lb = lane_base_of(warp);
-    float o[128];
-    float l_row = 0.f;
     if (n_sub > 0 && ok) {
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -1144,6 +1151,44 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
 #pragma unroll
       for (int c = 0; c < 128; ++c) o[c] = 0.f;
     }
+  }
+  if (nsplit > 1) {
+    // rank 1's (m, l, O) go to rank 0's shared memory: O in the Q' region, free
+    // once both CTAs' products completed (first cluster barrier)
+    cg::cluster_group cluster = cg::this_cluster();
+    float2* xml = reinterpret_cast<float2*>(sm + P::OFF_P);           // [128 rows] (m, l)
+    int* xfail = reinterpret_cast<int*>(sm + P::OFF_MISC + 8);
+    cluster.sync();
+    if (rank == 1) {
+      float4* ro = cluster.map_shared_rank(ych, 0);
+      if (tid < 256) {
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4)
+          ro[c4 * 256 + tid] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+        if (half == 0) cluster.map_shared_rank(xml, 0)[row] = make_float2(m_ref, l_row);
+      }
+      if (tid == 0) *cluster.map_shared_rank(xfail, 0) = ok ? 0 : 1;
+    }
+    cluster.sync();
+    if (rank == 0 && tid < 256) {
+      ok = ok && *xfail == 0;
+      const float2 pml = xml[row];
+      const float M = fmaxf(m_ref, pml.x);
+      const float w0 = M == -INFINITY ? 0.f : exp2f(m_ref - M);
+      const float w1 = M == -INFINITY ? 0.f : exp2f(pml.x - M);
+#pragma unroll
+      for (int c4 = 0; c4 < 32; ++c4) {
+        const float4 p = ych[c4 * 256 + tid];
+        o[4 * c4] = fmaf(o[4 * c4], w0, p.x * w1);
+        o[4 * c4 + 1] = fmaf(o[4 * c4 + 1], w0, p.y * w1);
+        o[4 * c4 + 2] = fmaf(o[4 * c4 + 2], w0, p.z * w1);
+        o[4 * c4 + 3] = fmaf(o[4 * c4 + 3], w0, p.w * w1);
+      }
+      l_row = fmaf(l_row, w0, pml.y * w1);
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the partner's O is read before reuse
+    }
+  }
+  if (rank == 0 && tid < 256) {
     const float inv = (l_row > 0.f ? 1.0f / l_row : 0.f) * rs2;
 #pragma unroll
     for (int c = 0; c < 128; ++c) o[c] *= inv;
@@ -1175,6 +1220,17 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
 }
 
+int prefill_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 template <int D, int SB, int VB>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   using P = PC<D>;
@@ -1202,10 +1258,28 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
-  if constexpr (D == 256)
-    prefill_kernel_d256<<<grid, 320, att_smem, st>>>(a);
-  else
+  if constexpr (D == 256) {
+    // a grid that leaves more than half of the SMs idle splits each row
+    // block's keys over a cluster of two CTAs
+    const int64_t ctas = (int64_t)grid.x * grid.y;
+    const int ns = 2 * ctas <= prefill_sm_count() ? 2 : 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid.x, grid.y, ns);
+    cfg.blockDim = dim3(320);
+    cfg.dynamicSmemBytes = att_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = ns;
+    cfg.attrs = attr;
+    cfg.numAttrs = ns > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel_d256, a);
+    if (e != cudaSuccess) return e;
+  } else {
     prefill_kernel<D><<<grid, P::NTHR_ATT, att_smem, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -105,10 +105,12 @@ def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
     (16, 4, 1400, 512, 256, 32, 2, True),
     (16, 2, 700, 256, 256, 16, 2, True),     # GQA group 8, f16 scales
     (4, 4, 450, 100, 128, 32, 4, False),     # group 1, k4v4, ragged chunks, window wraps
+    (32, 8, 1100, 512, 256, 32, 2, False),   # 128 row blocks: no key split
 ])
 def test_prefill_head_dim_256(Hq, Hkv, n, chunk, W, sb, vb, cached):
     """head_dim 256: keys stream through the attention kernel in 32-key
-    sub-blocks, the rotations pair two threads per row."""
+    sub-blocks, the rotations pair two threads per row; grids of at most
+    half the SMs split each row block's keys over a two-CTA cluster."""
     run = PrefillRun("batched_d256_decode", 8, n, Hq=Hq, Hkv=Hkv, D=256, W=W, chunk=chunk,
                      scale_bits=sb, v_bits=vb, cached=cached)
     for p in run.snap:
