@@ -166,6 +166,21 @@ class OracleDecodeSample:
         return LAYERS * CTX0 / (128.0 * self.n_tiles)
 
 
+def reduce_timing(elapsed_ms, units_per_rank, world, device=None):
+    """Max-over-ranks timing of a replica run (weak scaling: every rank
+    processes units_per_rank in its own elapsed_ms). The job's time is the
+    slowest rank's and its throughput the units of all ranks over that time;
+    every rank gets the same pair. world 1: the rank's own numbers."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        dist.barrier()
+    return elapsed_ms, world * units_per_rank / (elapsed_ms / 1000.0)
+
+
 def run_reference(args, rank):
     """--impl reference: the oracle timed on the host cores on this arm's metric,
     one bounded sample (every KV head of one layer over one tile) per step."""
@@ -764,14 +779,8 @@ def main():
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     gpu_launches = launches["n"]
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        dist.barrier()
+    elapsed_ms, tokens_per_s = reduce_timing(t_start.elapsed_time(t_end), B * args.steps, world, dev)
     ms_per_step = elapsed_ms / args.steps
-    tokens_per_s = world * B * args.steps / (elapsed_ms / 1000.0)
 
     # split-kernel durations: one more decode step with events around each split
     # launch, then the splits of all layers back to back
@@ -837,7 +846,7 @@ def main():
             out_h.copy_(out, non_blocking=True)
         e1.record()
     torch.cuda.synchronize()
-    e2e_tps = world * B * e2e_steps / (e0.elapsed_time(e1) / 1000.0)
+    _, e2e_tps = reduce_timing(e0.elapsed_time(e1), B * e2e_steps, world, dev)
     assert np.isfinite(out_h.numpy()).all(), "decode produced non-finite output"
 
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
