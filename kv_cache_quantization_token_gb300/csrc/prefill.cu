@@ -815,7 +815,10 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
 // as a separate N=16 product because O alone is 256 columns wide) and O
 // (columns 256-511). The two 128-channel halves of a row's rotation (the
 // prologue's H q and the epilogue's H o) meet through shared memory: one
-// butterfly over channel bit 7.
+// butterfly over channel bit 7. A chunk whose grid would leave more than half
+// of the SMs idle runs as clusters of two CTAs (gridDim.z = 2) that take
+// alternate 128-key blocks of the same rows; rank 1 hands its (m, l, O) to
+// rank 0 through distributed shared memory and rank 0 merges and stores.
 struct PA256 {
   static constexpr int D = 256;
   static constexpr int QB = 128 * D * 2;                 // fp16 Q' hi or lo [128 rows][256]
