@@ -1261,6 +1261,8 @@ void ws_split(const DecodePlan& p, int B, int Hq, void* ws, float** ml, float** 
   *acc = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + mlb);
 }
 
+}  // namespace
+
 #if KVARN_PRIMARY_UNIT
 int sm_count() {
   static int cached[64] = {};
@@ -1273,11 +1275,6 @@ int sm_count() {
   return n;
 }
 
-#endif
-
-}  // namespace
-
-#if KVARN_PRIMARY_UNIT
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p) {
   const int G = Hq / Hkv;
   p->g_pad = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;

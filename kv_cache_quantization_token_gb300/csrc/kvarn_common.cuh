@@ -99,6 +99,9 @@ __device__ __forceinline__ void pdl_trigger() {
 // Current kvarn_set_launch_flags() value.
 unsigned launch_flags();
 
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
 // cudaLaunchKernelEx configuration honouring KVARN_LAUNCH_PDL.
 struct LaunchCfg {
   cudaLaunchConfig_t cfg;

@@ -1223,17 +1223,6 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS));
 }
 
-int prefill_sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
-}
-
 template <int D, int SB, int VB>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   using P = PC<D>;
@@ -1265,7 +1254,7 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
     // a grid that leaves more than half of the SMs idle splits each row
     // block's keys over a cluster of two CTAs
     const int64_t ctas = (int64_t)grid.x * grid.y;
-    const int ns = 2 * ctas <= prefill_sm_count() ? 2 : 1;
+    const int ns = 2 * ctas <= sm_count() ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid.x, grid.y, ns);
     cfg.blockDim = dim3(320);
