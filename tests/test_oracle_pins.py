@@ -139,7 +139,7 @@ def test_sinkhorn_skips_degenerate_groups(oracle):
     assert np.all(s == 1.0) and np.all(r == 1.0) and np.all(yn == 0.0)
     rng = np.random.default_rng(9)
     Y = rng.standard_normal((128, 64))
-    Y[:, 5] = 0.1  # constant channel: in round 1 its std is pure rounding
+    Y[:, 5] = 0.1  # constant channel: in the first Sinkhorn step its std is pure rounding
     Y[:, 9] = 0.0  # zero channel: skipped in every round
     s, r, yn = oracle.sinkhorn(Y, 1)
     assert s[5] == 1.0 and s[9] == 1.0
