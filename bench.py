@@ -541,14 +541,15 @@ def workload_config():
 
 
 # --------------------------------------------------------------------------
-def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind):
-    """One compress launch over C_TILES x C_HEADS tile-heads of fresh raw K/V
-    (256 MiB of input, larger than L2), timed with CUDA events per launch."""
+def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind, tiles=C_TILES):
+    """One compress launch over tiles x C_HEADS tile-heads of fresh raw K/V
+    (256 MiB of input at the defaults, larger than L2), timed with CUDA
+    events per launch."""
     import torch
     from kv_cache_quantization_token_gb300 import kvarn, synth
     D, rb = lay.head_dim, lay.record_bytes
-    n_units = C_TILES * C_HEADS
-    ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * C_TILES, D)
+    n_units = tiles * C_HEADS
+    ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * tiles, D)
     ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
     cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
     del ks, vs
@@ -569,14 +570,15 @@ def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind):
     comp_ms = float(np.mean([a.elapsed_time(b) for a, b in cev]))
     comp_bytes = n_units * (2 * 128 * D * 4 + rb)
     comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
-    trc = NCU_TRAFFIC["compress"]
-    ctraffic = trc["bytes"] if trc["src_sha"] == src_sha("compress.cu") else None
+    trc = NCU_TRAFFIC["compress"]  # captured on the head_dim-128, 2048-tile-head launch
+    same_launch = D == 128 and n_units == C_TILES * C_HEADS
+    ctraffic = trc["bytes"] if same_launch and trc["src_sha"] == src_sha("compress.cu") else None
     return {"tile_heads_per_launch": n_units, "ms_per_launch": comp_ms,
             "tiles_per_s": n_units / (comp_ms * 1e-3), "gbs": comp_gbs,
             "bytes_per_launch": comp_bytes,
             "roofline": {"bound": "hbm", "achieved": comp_gbs, "peak": hbm,
                          "unit": "GB/s", "frac": comp_gbs / hbm,
-                         "traffic": ctraffic, "kernel": "compress_kernel<128>",
+                         "traffic": ctraffic, "kernel": f"compress_kernel<{D}>",
                          "peak_source": peak_kind}}
 
 
@@ -851,6 +853,13 @@ def main():
 
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
     compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
+    # head_dim 256: 1024 tile-heads, the same 256 MiB of input
+    try:
+        compress["head_dim_256"] = run_compress_bench(dev, stream, kvarn.layout(256), args.warmup,
+                                                      hbm, peak_kind, tiles=C_TILES // 2)
+    except Exception as e:  # a secondary measurement: report, keep the bench line
+        print(f"head_dim-256 compress measurement failed: {e!r}", file=sys.stderr)
+        compress["head_dim_256"] = {"error": repr(e)}
 
     # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256), and
     # an 8,192-token prompt with head_dim-256 heads
