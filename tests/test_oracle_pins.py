@@ -371,6 +371,31 @@ def test_prefill_chunk_of_one_equals_decode(oracle):
                 np.testing.assert_allclose(pre[(0, h)], dec[(0, h)], rtol=1e-13, atol=1e-15)
 
 
+def test_prefill_window_only_is_causal_softmax(oracle):
+    """c8 with no tiles: each chunk row i is textbook softmax attention
+    (scipy) over the raw window tokens at positions <= pos0 + i, the window a
+    ring that wraps (token w at slot (start + w) mod capacity). Pins the
+    causal bound (pos0 + i + 1 keys, not pos0 + i) and the ring order."""
+    rng = np.random.default_rng(21)
+    Hkv, Hq, D, cap, L, start = 1, 2, 64, 64, 50, 40
+    keys = rng.standard_normal((L, D)).astype(np.float32)
+    vals = rng.standard_normal((L, D)).astype(np.float32)
+    win_k = np.zeros((Hkv, cap, D), np.float32)
+    win_v = np.zeros((Hkv, cap, D), np.float32)
+    for w in range(L):
+        win_k[0, (start + w) % cap], win_v[0, (start + w) % cap] = keys[w], vals[w]
+    C, pos0, scale = 20, 30, 0.2
+    q = rng.standard_normal((C, Hq, D)).astype(np.float32)
+    out = oracle.prefill_attention(q, pos0, np.zeros(oracle.record_bytes(D), np.uint8),
+                                   np.zeros((Hkv, 1), np.int64), 0, win_k, win_v, start, L, scale)
+    K, V = keys.astype(np.float64), vals.astype(np.float64)
+    for i in range(C):
+        vis = pos0 + i + 1
+        for h in range(Hq):
+            p = scipy.special.softmax(scale * (K[:vis] @ q[i, h].astype(np.float64)))
+            np.testing.assert_allclose(out[(i, h)], p @ V[:vis], rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------- c4 variant: f16-scale layout
 def test_f16_rounding_matches_numpy(oracle):
     """The oracle's binary16 encoder (written from the format's definition)
