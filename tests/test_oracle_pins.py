@@ -396,6 +396,28 @@ def test_prefill_window_only_is_causal_softmax(oracle):
             np.testing.assert_allclose(out[(i, h)], p @ V[:vis], rtol=1e-12, atol=1e-14)
 
 
+def test_decode_gqa_groups_are_contiguous(oracle):
+    """GQA reading: query head h reads KV head h // G (contiguous groups, not
+    h mod Hkv). Window-only caches that differ per KV head and per sequence;
+    every (sequence, query head) against textbook softmax over its own KV
+    head's tokens."""
+    rng = np.random.default_rng(23)
+    B, Hkv, G, D, cap, L = 2, 3, 2, 64, 32, 9
+    Hq = Hkv * G
+    win_k = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    win_v = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    out = oracle.decode_attention(q, np.zeros(oracle.record_bytes(D), np.uint8),
+                                  np.zeros((B, Hkv, 1), np.int64), [0] * B, win_k, win_v,
+                                  [3] * B, [L] * B, 0.3)
+    for b in range(B):
+        for h in range(Hq):
+            K = win_k[b, h // G, 3:3 + L].astype(np.float64)
+            V = win_v[b, h // G, 3:3 + L].astype(np.float64)
+            p = scipy.special.softmax(0.3 * (K @ q[b, h].astype(np.float64)))
+            np.testing.assert_allclose(out[(b, h)], p @ V, rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------- c4 variant: f16-scale layout
 def test_f16_rounding_matches_numpy(oracle):
     """The oracle's binary16 encoder (written from the format's definition)
