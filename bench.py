@@ -100,9 +100,15 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=5)
+        return self.summarize(self.lines)
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock, the maximum clock and the throttle reasons seen
+        active, from nvidia-smi csv lines in FIELDS order (others skipped)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
