@@ -38,6 +38,9 @@
 //             fp16 P the MMA adds. At the end one thread per row divides by
 //             the row sum and applies the one inverse rotation (H is its own
 //             inverse).
+// head_dim 256 has its own attention kernel (prefill_kernel_d256: 32-key
+// sub-blocks, optional two-CTA cluster key split) and builds each block image
+// in two stages; the roles and the hand-offs are the same.
 // Every wait is bounded; a CTA that gives up writes NaN rows, frees its TMEM
 // and returns.
 #include <cooperative_groups.h>
