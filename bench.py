@@ -133,12 +133,12 @@ class OracleDecodeSample:
     head of the KV head's group, on host threads (the oracle's C code
     releases the GIL). Its inputs are the oracle's own compressed tiles."""
 
-    def __init__(self, n_tiles: int):
+    def __init__(self, n_tiles: int, threads: int = 0):
         import oracle
         from concurrent.futures import ThreadPoolExecutor
         from kv_cache_quantization_token_gb300 import synth
         self.oracle, self.n_tiles = oracle, n_tiles
-        self.threads = max(1, min(len(os.sched_getaffinity(0)), HKV))
+        self.threads = threads or max(1, min(len(os.sched_getaffinity(0)), HKV))
         self.pool = ThreadPoolExecutor(self.threads)
         rb = oracle.record_bytes(D)
         self.table = (np.arange(n_tiles, dtype=np.int64) * rb)[None, None, :]
@@ -885,6 +885,13 @@ def main():
         cpu = {"value": 1.0 / (sec * smp.scale), "unit": "tokens/s", "cores": smp.threads,
                "kind": "oracle", "sample": f"{smp.sample}; mean of {len(secs)} runs",
                "sample_seconds": float(np.sum(secs))}
+        # the same oracle on one host thread (a quarter of the context, ~2 s per run)
+        one = OracleDecodeSample(CTX0 // 512, threads=1)
+        secs1 = [one.run() for _ in range(3)]
+        cpu["single_thread"] = {"value": 1.0 / (float(np.mean(secs1)) * one.scale),
+                                "unit": "tokens/s", "cores": 1,
+                                "sample": f"{one.sample}; mean of 3 runs",
+                                "sample_seconds": float(np.sum(secs1))}
 
     if rank == 0:
         res = {
