@@ -243,7 +243,7 @@ template <int D>
 struct PC {
   static constexpr int OPB = 128 * D * 2;                // one fp16 operand image: 128 rows x D
   static constexpr int BLK = 3 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T
-  // attention kernel shared memory
+  // attention kernel shared memory (head_dim <= 128; head_dim 256 uses PA256)
   static constexpr int OFF_QH = 0;                       // fp16 Q' hi [128 rows][D]
   static constexpr int OFF_QL = OFF_QH + OPB;            // fp16 Q' lo (Q' - hi)
   static constexpr int OFF_KH = OFF_QL + OPB;            // fp16 K~ hi [128 keys][D]
