@@ -82,3 +82,35 @@ def test_record_round_trip_every_layout(seed, D, scale_bits, v_bits):
     for n, a in sc.items():
         want = (a.astype(np.float32) if scale_bits == 32 else a.astype(np.float16)).astype(np.float64)
         np.testing.assert_array_equal(u[n], want, err_msg=n)
+
+
+@settings(max_examples=15, deadline=None, derandomize=True)
+@given(st.lists(st.integers(1, 200), min_size=1, max_size=12), st.sampled_from([128, 256]))
+def test_tiles_independent_of_chunking(chunks, W):
+    """Any sequence of chunk sizes promotes the same tiles as token-at-a-time
+    appends (PR #434: tiles do not depend on the chunking), and the window
+    keeps its invariant: fewer than W tokens, at least W - 128 once a tile
+    was promoted."""
+    Hkv, D = 1, 64
+    n = sum(chunks)
+    ks, vs = synth_kv(n, D)
+    ref = oracle.CacheStateMachine(Hkv, D, W=W)
+    for i in range(n):
+        ref.append(ks[i:i + 1], vs[i:i + 1])
+    sm = oracle.CacheStateMachine(Hkv, D, W=W)
+    i0 = 0
+    for c in chunks:
+        sm.append(ks[i0:i0 + c], vs[i0:i0 + c])
+        i0 += c
+        assert sm.win_len < W
+        if sm.n_tiles:
+            assert sm.win_len >= W - 128
+    assert sm.n_tiles == ref.n_tiles == ((n - W) // 128 + 1 if n >= W else 0)
+    for t in range(sm.n_tiles):
+        np.testing.assert_array_equal(sm.records[t][0], ref.records[t][0])
+
+
+def synth_kv(n, D):
+    from kv_cache_quantization_token_gb300 import synth
+    k, v = synth.kv_layer("single_tile", 3, 1, n, D)
+    return k.transpose(1, 0, 2).copy(), v.transpose(1, 0, 2).copy()
