@@ -13,34 +13,39 @@
 // Two kernels per chunk:
 //   dequant   one CTA per (visible 128-key block, KV head): a packed tile is
 //             dequantised (K~ = r_t s_c (delta code + lo), V~ likewise) or a
-//             block of window rows rotated (H k, H v), into fp16 K~ hi + lo
-//             [key][channel] and V~^T [channel][key] in the 128-byte-swizzled
-//             K-major image the tensor-core operands use, built in shared
-//             memory and written to the workspace with one bulk copy. Each
+//             block of window rows rotated (H k, H v), into fp16 images of
+//             K~ [key][channel] and V~^T [channel][key], each as a hi part and
+//             a lo part (x - hi), in the 128-byte-swizzled K-major layout the
+//             tensor cores read; staged in shared memory in two halves (K~,
+//             then V~^T) and written to the workspace with bulk copies. Each
 //             block is dequantised once per chunk, not once per query CTA.
 //   attention one CTA (10 warps) per KV head and 128 score rows (the G query
 //             heads of the GQA group times 128/G positions): 8 softmax warps,
 //             one MMA warp, one copy warp, handing off through mbarriers.
-//             Per visible block: the block image is bulk-copied into shared
-//             memory (K~ hi and lo on separate barriers, each as soon as the
-//             previous block's MMAs have read it); S = Q' K~^T on tcgen05
-//             (kind::f16, fp32 accumulate into TMEM) with Q' and K~ each
-//             split into fp16 hi + lo and S = Qh Kh + Qh Kl + Ql Kh (one fp16
-//             rounding of either operand costs up to 1e-2 in the output
-//             through cancellation in q.k; the split keeps the scores to
-//             about 2^-22), double-buffered in TMEM so that the scores of
-//             block j+1 are computed while the softmax of block j runs; two
-//             threads per score row apply the causal mask and an online
-//             softmax in base 2 (the running max is only moved, and O
-//             rescaled in TMEM, when a score exceeds it by more than 8); P
-//             goes to shared memory as fp16 and [O | l] += P [V~ | 1] on
-//             tcgen05, the ones column giving the row sums of exactly the
-//             fp16 P the MMA adds. At the end one thread per row divides by
-//             the row sum and applies the one inverse rotation (H is its own
-//             inverse).
-// head_dim 256 has its own attention kernel (prefill_kernel_d256: 32-key
-// sub-blocks, optional two-CTA cluster key split) and builds each block image
-// in two stages; the roles and the hand-offs are the same.
+//             The rotated, scaled query Q' stays in tensor memory (TMEM) as
+//             fp16 hi + lo for the whole CTA, and both contractions take their
+//             A operand from TMEM (the "TS" form of tcgen05.mma), so shared
+//             memory only feeds the B operands:
+//               S  = Q'h K~h + Q'l K~h + Q'h K~l      (fp32 accumulate, TMEM)
+//               O += Ph V~h + Pl V~h + Ph V~l
+//             A single fp16 rounding of any of the four operands costs 1e-3 to
+//             1e-2 in the output (cancellation in q.k with rotated keys; in
+//             P V the weights and the values each carry 2^-11 relative), so
+//             each is carried as a pair whose sum holds about 22 bits and the
+//             lo x lo product (2^-22) is dropped. Scores are double-buffered
+//             in TMEM: S of block j+1 is formed while the softmax of block j
+//             runs. Two threads per score row apply the causal mask and a
+//             base-2 online softmax (the row maximum is exchanged between the
+//             pair through shared memory; the reference maximum is only moved,
+//             and O rescaled in TMEM, when a score exceeds it by more than 8);
+//             P goes back into the TMEM columns its scores came from, as fp16
+//             hi and lo, and the P V product reads it there. Row sums are
+//             accumulated in fp32 by the softmax threads. At the end one
+//             thread per row divides by the row sum and applies the one
+//             inverse rotation (H is its own inverse).
+// head_dim 256 has its own attention kernel (prefill_kernel_d256: 64-key
+// sub-blocks, Q'l in shared memory, optional two-CTA cluster key split); the
+// roles and the hand-offs are the same.
 // Every wait is bounded; a CTA that gives up writes NaN rows, frees its TMEM
 // and returns.
 #include <cooperative_groups.h>
@@ -83,6 +88,15 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+// The same product with the A operand (M = 128 rows, fp16 pairs packed two per
+// 32-bit column, element 2k in the low half) read from tensor memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t id,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -190,6 +204,28 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+// 32 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // One fp32 TMEM column of this thread's lane.
 __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   uint32_t r;
@@ -213,6 +249,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ void split2(float x0, float x1, __half2& hi, __half2& lo) {
   hi = __floats2half2_rn(x0, x1);
   lo = __floats2half2_rn(x0 - __low2float(hi), x1 - __high2float(hi));
+}
+
+// The pair (x0, x1) as two fp16x2 words: hi = (x0, x1) rounded, lo = the
+// rounded remainders; x0 in the low halves.
+__device__ __forceinline__ void split2w(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  __half2 h, l;
+  split2(x0, x1, h, l);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // 2^x on the special-function unit (results below 2^-126 flush to zero).
@@ -242,24 +287,22 @@ __device__ __forceinline__ void fwht_reg(float (&x)[N]) {
 template <int D>
 struct PC {
   static constexpr int OPB = 128 * D * 2;                // one fp16 operand image: 128 rows x D
-  static constexpr int BLK = 3 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T
+  static constexpr int BLK = 4 * OPB;                    // workspace block: K~ hi, K~ lo, V~^T hi, V~^T lo
   // attention kernel shared memory (head_dim <= 128; head_dim 256 uses PA256)
-  static constexpr int OFF_QH = 0;                       // fp16 Q' hi [128 rows][D]
-  static constexpr int OFF_QL = OFF_QH + OPB;            // fp16 Q' lo (Q' - hi)
-  static constexpr int OFF_KH = OFF_QL + OPB;            // fp16 K~ hi [128 keys][D]
-  static constexpr int OFF_KL = OFF_KH + OPB;            // fp16 K~ lo (contiguous with hi)
-  static constexpr int NV = D + 16;                      // V~^T rows + a ones row + 15 zero rows
-  static constexpr int VKB = NV * 128;                   // one 64-key block of the V operand
-  static constexpr int OFF_V = OFF_KL + OPB;             // fp16 [V~^T; 1; 0] [NV][128 keys]
-  static constexpr int OFF_P = OFF_V + 2 * VKB;          // fp16 P [128 rows][128 keys]
-  static constexpr int OFF_BAR = OFF_P + 128 * 128 * 2;  // 8 mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int OFF_K = 0;                        // [2 buffers][K~ hi | K~ lo], [128 keys][D]
+  static constexpr int OFF_V = 4 * OPB;                  // V~^T hi | lo, [D][128 keys]
+  static constexpr int OFF_BAR = 6 * OPB;                // 8 mbarriers
+  static constexpr int OFF_XM = OFF_BAR + 64;            // float [2][2][128]: row-max exchange
+  static constexpr int OFF_XB = OFF_XM + 2 * 2 * 128 * 4; // int [2][8]: per-warp stop flags
+  static constexpr int OFF_MISC = OFF_XB + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;     // + slack to align the base to 1024
+  // tensor memory columns: Q' hi and lo (fp16 pairs), S double buffer, O
+  static constexpr int T_QH = 0, T_QL = D / 2, T_S = D, T_O = D + 256;
+  static constexpr int TMEM_COLS = 512;
   // dequant kernel shared memory: the record (room for the fp32 layout of its
-  // value width), then the block image and a barrier. At head_dim 256 the
-  // image is built in two stages (K~ hi + lo, stored; then V~^T in their place)
-  static constexpr bool DQ_TWO_STAGE = D == 256;
-  static constexpr int DQ_OUT = DQ_TWO_STAGE ? 2 * OPB : BLK;
+  // value width), then one half of the block image (K~ hi + lo, then V~^T hi
+  // + lo in the same place) and a barrier
+  static constexpr int DQ_OUT = 2 * OPB;
   template <int VB>
   struct DQ {
     static constexpr int OFF_OUT = Rec<D, 4, VB>::kSlot;
@@ -268,10 +311,9 @@ struct PC {
   };
   static constexpr int NTHR = 256;                       // dequant: two threads per key row
   static constexpr int NTHR_ATT = 320;                   // attention: 8 softmax warps, MMA, loads
-  static constexpr int TMEM_COLS = 512;                  // S: 0..127 and 128..255, O|l: 256..256+D
   static_assert(D == 64 || D == 128 || D == 256, "prefill head_dim");
-  static_assert(OPB % 1024 == 0 && VKB % 1024 == 0,
-                "swizzled images on 1024-byte boundaries");
+  static_assert(OPB % 1024 == 0, "swizzled images on 1024-byte boundaries");
+  static_assert(D == 256 || (T_O + D <= TMEM_COLS && SMEM <= 227 * 1024), "TMEM and shared memory");
 };
 
 struct PrefillArgs {
@@ -296,14 +338,12 @@ template <int D, int SB, int VB>
 __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kernel(const PrefillArgs a) {
   using P = PC<D>;
   using R = Rec<D, SB, VB>;  // scale fields fp32 (SB 4) or binary16 (SB 2); VB-bit values
-  constexpr bool kTwo = P::DQ_TWO_STAGE;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
   const unsigned char* rec = sm;
-  unsigned char* sKh = sm + P::template DQ<VB>::OFF_OUT;
-  unsigned char* sKl = sKh + P::OPB;
-  unsigned char* sV = kTwo ? sKh : sKl + P::OPB;  // two stages: V~^T replaces the stored K~
+  unsigned char* sH = sm + P::template DQ<VB>::OFF_OUT;  // hi image (K~, then V~^T)
+  unsigned char* sL = sH + P::OPB;                        // lo image
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::template DQ<VB>::OFF_BAR);
   const int j = a.first_blk + blockIdx.x, kvh = blockIdx.y;
   uint8_t* gimg = a.ws + ((int64_t)kvh * a.ws_stride + j) * P::BLK;
@@ -328,8 +368,8 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
     for (int o = tid * 16; o < bytes; o += 16 * P::NTHR)
       *reinterpret_cast<uint4*>(dst + o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
   };
-  // window block: raw rows rotated (K into K~ hi/lo, V into V~^T); rows past
-  // the window's length are zero
+  // window block: raw rows rotated (K into K~, V into V~^T); rows past the
+  // window's length are zero
   const int wb = j - a.n_tblk;
   const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * wb);
   const int64_t slot = ((int64_t)a.win_start + 128 * wb + row) % a.win_cap;
@@ -348,29 +388,19 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
       for (int c = 0; c < D; ++c) x[c] = 0.f;
     }
   };
-  auto win_k = [&]() {
-    float x[D];
-    win_row(a.win_k, x);
-#pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-      __align__(16) __half2 hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(sKh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-      *reinterpret_cast<uint4*>(sKl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
-    }
-  };
-  auto win_v = [&]() {  // V row -> column `row` of V~^T
-    float x[D];
-    win_row(a.win_v, x);
-#pragma unroll
-    for (int c = 0; c < D; ++c) *reinterpret_cast<__half*>(sV + sw_off(c, row, D)) = __float2half_rn(x[c]);
+  // the staged half goes out with one bulk copy (async proxy: fence the
+  // generic writes first); the CTA waits until the copy has read it
+  auto store_half = [&](uint8_t* dst) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) bulk_store_wait(dst, sH, 2 * P::OPB);
+    __syncthreads();
   };
 
-  // ---------------- K~ hi / lo
+  // ---------------- K~ hi / lo  [128 keys][D]
   if (is_tile) {
     if (poison) {
-      fill_nan(sKh, 2 * P::OPB);
+      fill_nan(sH, 2 * P::OPB);
     } else {
       // thread -> channel tid % D and a contiguous share of its 128 keys
       const unsigned char* kS = rec + R::kKS;
@@ -397,27 +427,29 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
           const float v = sc_ld<SB>(kR, t) * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
           const __half h = __float2half_rn(v);
           const uint32_t o = sw_off(t, c, 128);
-          *reinterpret_cast<__half*>(sKh + o) = h;
-          *reinterpret_cast<__half*>(sKl + o) = __float2half_rn(v - __half2float(h));
+          *reinterpret_cast<__half*>(sH + o) = h;
+          *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
         }
       }
     }
   } else if (half == 0) {
-    win_k();
-  } else if constexpr (!kTwo) {
-    win_v();
+    float x[D];
+    win_row(a.win_k, x);
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      __align__(16) __half2 hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
+      *reinterpret_cast<uint4*>(sH + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
+      *reinterpret_cast<uint4*>(sL + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+    }
   }
-  if constexpr (kTwo) {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (tid == 0) bulk_store_wait(gimg, sKh, 2 * P::OPB);
-    __syncthreads();  // the store has read K~ before V~^T overwrites it
-  }
+  store_half(gimg);
 
-  // ---------------- V~^T
+  // ---------------- V~^T hi / lo  [D][128 keys]
   if (is_tile) {
     if (poison) {
-      fill_nan(sV, P::OPB);
+      fill_nan(sH, 2 * P::OPB);
     } else {
       // thread -> key t, half of the D channels of the token row
       const unsigned char* vS = rec + R::kVS;
@@ -451,51 +483,83 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
           const int c = CPB * jb + e;
           const float code = (float)((byte >> (VB * e)) & ((1u << VB) - 1u));
           const float v = sc_ld<SB>(vS, c) * fmaf(d, code, lo);
-          *reinterpret_cast<__half*>(sV + sw_off(c, t, D)) = __float2half_rn(v);
+          const __half h = __float2half_rn(v);
+          const uint32_t o = sw_off(c, t, D);
+          *reinterpret_cast<__half*>(sH + o) = h;
+          *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
         }
       }
     }
-  } else if constexpr (kTwo) {
-    if (half == 1) win_v();
+  } else if (half == 1) {  // V row -> column `row` of V~^T
+    float x[D];
+    win_row(a.win_v, x);
+#pragma unroll
+    for (int c = 0; c < D; ++c) {
+      const __half h = __float2half_rn(x[c]);
+      const uint32_t o = sw_off(c, row, D);
+      *reinterpret_cast<__half*>(sH + o) = h;
+      *reinterpret_cast<__half*>(sL + o) = __float2half_rn(x[c] - __half2float(h));
+    }
   }
-  // the image goes out with one bulk copy (async proxy: fence the generic writes)
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
-  if (tid == 0) {
-    if constexpr (kTwo) bulk_store_wait(gimg + 2 * P::OPB, sV, P::OPB);
-    else bulk_store_wait(gimg, sKh, P::BLK);
-  }
+  store_half(gimg + 2 * P::OPB);
+}
+
+// Key blocks visible to some row of a CTA whose query positions span
+// [pmin, pmax]: tiles, then 128-token window blocks (a CTA that sees a window
+// block sees every tile).
+struct Visible {
+  int n_tile_blk, n_blk;
+};
+__device__ __forceinline__ Visible visible_blocks(const PrefillArgs& a, int64_t pmax) {
+  const int64_t win_pos0 = 128LL * a.n_tiles;
+  int n_tile_blk = a.n_tiles;
+  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
+  n_tile_blk = min(n_tile_blk, a.n_tiles);
+  int n_win_blk = 0;
+  for (int w = 0; 128 * w < a.win_len; ++w)
+    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
+  return Visible{n_tile_blk, n_tile_blk + n_win_blk};
+}
+
+// Row maximum of a score row split over two threads (warps w and w + 4, the
+// same TMEM lanes): each publishes its half's maximum and reads the other's
+// after a barrier of the two warps, and the pair agrees on whether to go on:
+// false when either warp gave up (`bad` is uniform over a warp). Slots
+// alternate with the block parity, so a thread's next write never lands
+// before its partner has read this one.
+__device__ __forceinline__ bool pair_max(float mloc, bool bad, float* xm, int* xb, int par, int half,
+                                         int row, int warp, float& mblk) {
+  xm[(par * 2 + half) * 128 + row] = mloc;
+  if ((threadIdx.x & 31) == 0) xb[par * 8 + warp] = bad ? 1 : 0;
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + (warp & 3)) : "memory");
+  mblk = fmaxf(mloc, xm[(par * 2 + (half ^ 1)) * 128 + row]);
+  return !bad && xb[par * 8 + (warp ^ 4)] == 0;
 }
 
 // ---------------------------------------------------------------------------
-// attention over the block images of the chunk
+// attention over the block images of the chunk (head_dim 64 or 128)
 //
 // Warp roles: warps 0-7 run the softmax (two threads per score row) and the
 // epilogue, warp 8 issues the tcgen05 MMAs (one thread), warp 9 the bulk
-// copies (one thread). Scores are double-buffered in TMEM, so S of block j+1
-// is computed while the softmax of block j runs. The tensor pipe runs, in
-// order, S(0), S(1), PV(0), S(2), PV(1), ...; K~ hi and K~ lo have their own
-// barriers, so the next block's hi half streams in while this block's
-// Qh Kl product is still being accumulated.
+// copies (one thread). K~ is double-buffered in shared memory, V~^T single;
+// S is double-buffered in TMEM. The tensor pipe runs, in order, S(0), S(1),
+// PV(0), S(2), PV(1), ...; S(j+2) overwrites the TMEM columns that held P(j)
+// only after PV(j), which the pipe completes first.
 template <int D>
 __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   using P = PC<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
-  unsigned char* sQh = sm + P::OFF_QH;
-  unsigned char* sQl = sm + P::OFF_QL;
-  unsigned char* sKh = sm + P::OFF_KH;
-  unsigned char* sKl = sm + P::OFF_KL;
+  unsigned char* sK = sm + P::OFF_K;
   unsigned char* sV = sm + P::OFF_V;
-  unsigned char* sP = sm + P::OFF_P;
-  uint64_t* bar_kh = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // K~ hi landed
-  uint64_t* bar_kl = bar_kh + 1;   // K~ lo landed
-  uint64_t* bar_v = bar_kh + 2;    // V~^T landed
-  uint64_t* bar_s = bar_kh + 3;    // [2] S(j) complete (TMEM buffer j & 1); K~ lo free
-  uint64_t* bar_khf = bar_kh + 5;  // the K~ hi products of S(j) complete: K~ hi free
-  uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: P and V~ free, O current
-  uint64_t* bar_p = bar_kh + 7;    // P(j) written and O rescaled (one arrival per softmax warp)
+  uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // [2] K~ of block j in buffer j & 1
+  uint64_t* bar_v = bar_k + 2;     // V~^T of block j landed
+  uint64_t* bar_s = bar_k + 3;     // [2] S(j) complete: scores ready, K~ buffer j & 1 free
+  uint64_t* bar_o = bar_k + 5;     // PV(j) complete: V~^T free, O current
+  uint64_t* bar_p = bar_k + 6;     // P(j) in TMEM, O rescaled (one arrival per softmax warp)
+  float* xm = reinterpret_cast<float*>(sm + P::OFF_XM);
+  int* xb = reinterpret_cast<int*>(sm + P::OFF_XB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
   volatile int* fail = reinterpret_cast<volatile int*>(sm + P::OFF_MISC + 4);
 
@@ -513,24 +577,16 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;  // largest query position of the CTA
   const int64_t pmin = a.pos0 + i0;                       // smallest
   const int hq = kvh * a.G + min(my_g, a.G - 1);
-
-  // key blocks visible to some row of this CTA: tiles, then 128-token window
-  // blocks (a CTA that sees a window block sees every tile)
   const int64_t win_pos0 = 128LL * a.n_tiles;
-  int n_tile_blk = a.n_tiles;
-  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
-  n_tile_blk = min(n_tile_blk, a.n_tiles);
-  int n_win_blk = 0;
-  for (int w = 0; 128 * w < a.win_len; ++w)
-    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
-  const int n_blk = n_tile_blk + n_win_blk;
+  const Visible vis_blk = visible_blocks(a, pmax);
+  const int n_tile_blk = vis_blk.n_tile_blk, n_blk = vis_blk.n_blk;
   auto image = [&](int jj) -> const uint8_t* {  // workspace image of this CTA's block jj
     const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
     return a.ws + ((int64_t)kvh * a.ws_stride + widx) * P::BLK;
   };
 
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init1(bar_kh + i);
+    for (int i = 0; i < 6; ++i) mbar_init1(bar_k + i);
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
@@ -541,7 +597,30 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
                  "r"(P::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // Q' row: rotate, scale, fp16 into the swizzled A operand (one thread per row)
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_o = tmem + P::T_O;
+  const uint32_t lb = lane_base_of(warp);
+
+  // the first copies go out while the query rows are prepared
+  int nk[2] = {0, 0}, nv = 0;  // copies issued per barrier (loader thread)
+  auto load_k = [&](int jj) {
+    const int b = jj & 1;
+    bulk_load(sK + b * 2 * P::OPB, image(jj), 2 * P::OPB, bar_k + b);
+    ++nk[b];
+  };
+  auto load_v = [&](int jj) {
+    bulk_load(sV, image(jj) + 2 * P::OPB, 2 * P::OPB, bar_v);
+    ++nv;
+  };
+  if (warp == 9 && lane == 0 && n_blk > 0) {
+    load_k(0);
+    if (n_blk > 1) load_k(1);
+    load_v(0);
+  }
+  // Q' row into TMEM: rotate, scale, fp16 hi + lo (one thread per row)
   if (tid < 128) {
     float x[D];
     if (my_valid) {
@@ -557,65 +636,39 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     }
     fwht_reg<D>(x);
 #pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-      __align__(16) __half2 hi[4], lo[4];
+    for (int c0 = 0; c0 < D; c0 += 64) {
+      uint32_t hw[32], lw[32];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        split2(x[8 * c8 + 2 * e] * a.qscale, x[8 * c8 + 2 * e + 1] * a.qscale, hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(sQh + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-      *reinterpret_cast<uint4*>(sQl + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+      for (int e = 0; e < 32; ++e)
+        split2w(x[c0 + 2 * e] * a.qscale, x[c0 + 2 * e + 1] * a.qscale, hw[e], lw[e]);
+      tmem_st32_nowait(tmem + lb + P::T_QH + c0 / 2, hw);
+      tmem_st32_nowait(tmem + lb + P::T_QL + c0 / 2, lw);
     }
-    // the MMA (async proxy) reads what these generic stores wrote
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  } else if (tid < 256) {
-    // rows D .. D+15 of both key blocks of the V operand: a row of ones (the
-    // PV MMA then also sums P into column D of O) and zeros
-    for (int idx = tid - 128; idx < 2 * 16 * 8; idx += 128) {
-      const int kb = idx >> 7, r = (idx >> 3) & 15, c16 = idx & 7;
-      const uint32_t w = r == 0 ? 0x3C003C00u : 0u;
-      *reinterpret_cast<uint4*>(sV + kb * P::VKB + (D + r) * 128 + c16 * 16) = make_uint4(w, w, w, w);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tmem_wait_st();
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t t_o = tmem + 256;
 
+  float m_ref = -INFINITY, l_part = 0.f;  // softmax threads: reference max, half-row sum
   if (warp == 9) {
     // ---------------- loader: block images into shared memory
     if (lane == 0 && n_blk > 0) {
-      int nkh = 1, nkl = 1, nv = 1;
-      auto load_v = [&](int jj) {  // the image holds two 64-key blocks of D rows each
-        mbar_expect_tx(bar_v, P::OPB);
-        bulk_copy_tx(sV, image(jj) + 2 * P::OPB, P::OPB / 2, bar_v);
-        bulk_copy_tx(sV + P::VKB, image(jj) + 2 * P::OPB + P::OPB / 2, P::OPB / 2, bar_v);
-      };
-      bulk_load(sKh, image(0), P::OPB, bar_kh);
-      bulk_load(sKl, image(0) + P::OPB, P::OPB, bar_kl);
-      load_v(0);
-      // waits follow the tensor pipe's completion order: S(j-1) hi part,
-      // S(j-1), PV(j-2)
-      for (int j = 1; j <= n_blk; ++j) {
-        if (j < n_blk) {
-          if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail)) break;
-          bulk_load(sKh, image(j), P::OPB, bar_kh);
-          ++nkh;
-          if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail)) break;
-          bulk_load(sKl, image(j) + P::OPB, P::OPB, bar_kl);
-          ++nkl;
+      // completion order of the tensor pipe: S(j) before PV(j)
+      for (int j = 0; j < n_blk; ++j) {
+        if (j + 2 < n_blk) {
+          if (!mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
+          load_k(j + 2);
         }
-        if (j >= 2) {
-          if (!mbar_wait_flag(bar_o, (uint32_t)(j - 2) & 1u, fail)) break;
-          load_v(j - 1);
-          ++nv;
+        if (j + 1 < n_blk) {
+          if (!mbar_wait_flag(bar_o, (uint32_t)j & 1u, fail)) break;
+          load_v(j + 1);
         }
       }
       // every copy issued has landed before the CTA can retire
-      mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u);
-      mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u);
-      mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
+      for (int b = 0; b < 2; ++b)
+        if (nk[b] > 0) mbar_wait_bounded(bar_k + b, (uint32_t)(nk[b] - 1) & 1u);
+      if (nv > 0) mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -624,42 +677,40 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       uint64_t* last = nullptr;  // the most recent commit, drained on the way out
       uint32_t last_par = 0;
       auto issue_s = [&](int j) -> bool {
-        const uint32_t t_s = tmem + 128 * (j & 1);
-        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail)) return false;
+        const int b = j & 1;
+        if (!mbar_wait_flag(bar_k + b, (uint32_t)(j >> 1) & 1u, fail)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t t_s = tmem + P::T_S + 128 * b;
+        const uint32_t kh = su32(sK + b * 2 * P::OPB), kl = kh + P::OPB;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKh) + off), idesc<128>(), kk > 0);
-          mma_f16(t_s, sdesc(su32(sQl) + off), sdesc(su32(sKh) + off), idesc<128>(), 1);
+          const uint32_t qh = tmem + P::T_QH + 8 * kk, ql = tmem + P::T_QL + 8 * kk;
+          mma_f16_ts(t_s, qh, sdesc(kh + off), idesc<128>(), kk > 0);
+          mma_f16_ts(t_s, ql, sdesc(kh + off), idesc<128>(), 1);
+          mma_f16_ts(t_s, qh, sdesc(kl + off), idesc<128>(), 1);
         }
-        mma_commit(bar_khf);
-        last = bar_khf; last_par = (uint32_t)j & 1u;
-        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail)) return false;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          mma_f16(t_s, sdesc(su32(sQh) + off), sdesc(su32(sKl) + off), idesc<128>(), 1);
-        }
-        mma_commit(bar_s + (j & 1));
-        last = bar_s + (j & 1); last_par = (uint32_t)(j >> 1) & 1u;
+        mma_commit(bar_s + b);
+        last = bar_s + b; last_par = (uint32_t)(j >> 1) & 1u;
         return true;
       };
       bool ok = issue_s(0);
       for (int j = 0; ok && j < n_blk; ++j) {
-        // S(j+1) goes in ahead of PV(j): its TMEM buffer was read by the softmax
-        // of block j-1, which PV(j-1) already waited for
+        // S(j+1) goes in ahead of PV(j): its TMEM buffer held P(j-1), which
+        // PV(j-1), issued earlier, reads first
         if (j + 1 < n_blk && !issue_s(j + 1)) break;
         if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
         if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t t_p = tmem + P::T_S + 128 * (j & 1);
+        const uint32_t vh = su32(sV), vl = vh + P::OPB;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          const uint32_t off_b = (kk >> 2) * P::VKB + (kk & 3) * 32;
-          mma_f16(t_o, sdesc(su32(sP) + off_a), sdesc(su32(sV) + off_b), idesc<P::NV>(),
-                  (j > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk) {  // 16 keys each; keys 64 h .. are thread half h's
+          const uint32_t ph = t_p + 64 * (kk >> 2) + 8 * (kk & 3), pl = ph + 32;
+          const uint32_t off = (kk >> 2) * D * 128 + (kk & 3) * 32;
+          mma_f16_ts(t_o, ph, sdesc(vh + off), idesc<D>(), (j > 0 || kk > 0));
+          mma_f16_ts(t_o, pl, sdesc(vh + off), idesc<D>(), 1);
+          mma_f16_ts(t_o, ph, sdesc(vl + off), idesc<D>(), 1);
         }
         mma_commit(bar_o);
         last = bar_o; last_par = (uint32_t)j & 1u;
@@ -669,75 +720,63 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     }
     __syncwarp();
   } else {
-    // ---------------- softmax (warps 0-7)
-    // Each thread reads its whole score row for the row maximum (no exchange
-    // between the two threads of a row) and exponentiates its half. Row sums
-    // come out of the PV MMA (column D of O, from the ones row of the V operand).
-    float m_ref = -INFINITY;
-    const uint32_t lb = lane_base_of(warp);
+    // ---------------- softmax (warps 0-7): two threads per row, 64 keys each
     for (int j = 0; j < n_blk; ++j) {
       const bool is_tile = j < n_tile_blk;
       const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
       const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
       const bool full_vis = kpos0 + 127 <= pmin && nkeys == 128;  // uniform over the CTA
       bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
-      if (__any_sync(0xffffffffu, bad || *fail != 0)) break;  // the warp leaves together
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t t_s = tmem + 128 * (j & 1) + lb;
+      bad = __any_sync(0xffffffffu, bad || *fail != 0);  // the warp (and its pair) leave together
+      const uint32_t t_s = tmem + P::T_S + 128 * (j & 1) + lb + 64 * half;
       float sv[64];
-      tmem_ld32(t_s + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
-      tmem_ld32(t_s + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
-      float mblk = -INFINITY;
-      if (full_vis) {
+      float mloc = -INFINITY;
+      if (!bad) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tmem_ld32(t_s, *reinterpret_cast<float(*)[32]>(sv));
+        tmem_ld32(t_s + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+        if (full_vis) {
 #pragma unroll
-        for (int u = 0; u < 64; u += 2) mblk = fmax3(mblk, sv[u], sv[u + 1]);
+          for (int u = 0; u < 64; u += 2) mloc = fmax3(mloc, sv[u], sv[u + 1]);
+          if (!my_valid) mloc = -INFINITY;
+        } else {
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {  // the other half of the row
-          float v[32];
-          tmem_ld32(t_s + 64 * (1 - half) + c0, v);
-#pragma unroll
-          for (int u = 0; u < 32; u += 2) mblk = fmax3(mblk, v[u], v[u + 1]);
-        }
-        if (!my_valid) mblk = -INFINITY;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 64; ++u) {
-          const int t = 64 * half + u;
-          const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
-          sv[u] = vis ? sv[u] : -INFINITY;
-          mblk = fmaxf(mblk, sv[u]);
-        }
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          float v[32];
-          tmem_ld32(t_s + 64 * (1 - half) + c0, v);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int t = 64 * (1 - half) + c0 + u;
+          for (int u = 0; u < 64; ++u) {
+            const int t = 64 * half + u;
             const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
-            mblk = vis ? fmaxf(mblk, v[u]) : mblk;
+            sv[u] = vis ? sv[u] : -INFINITY;
+            mloc = fmaxf(mloc, sv[u]);
           }
         }
       }
-      // move the reference max (and rescale O and l) only when a score exceeds
-      // it by more than 8; both threads of a row see the same values
+      float mblk;
+      if (!pair_max(mloc, bad, xm, xb, j & 1, half, row, warp, mblk)) break;
+      // move the reference max (and rescale O and the row sum) only when a
+      // score exceeds it by more than 8; both threads of a row see the same
+      // values
       const bool need = mblk > m_ref + 8.0f;
       const float m_new = need ? mblk : m_ref;
       const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
       m_ref = m_new;
-      // exp2 of a non-positive argument (up to +8); results below 2^-126 flush to
-      // zero (they are below fp16 resolution too); a row with no visible key yet
-      // subtracts +inf and gets 0
+      // exp2 of a non-positive argument (up to +8); results below 2^-126 flush
+      // to zero; a row with no visible key yet subtracts +inf and gets 0
       const float msub = m_ref == -INFINITY ? INFINITY : m_ref;
-      uint32_t h[32];
+      uint32_t hw[32], lw[32];
+      float ls = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const __half2 hp = __floats2half2_rn(ex2_ftz(sv[2 * e] - msub), ex2_ftz(sv[2 * e + 1] - msub));
-        h[e] = *reinterpret_cast<const uint32_t*>(&hp);
+        const float p0 = ex2_ftz(sv[2 * e] - msub), p1 = ex2_ftz(sv[2 * e + 1] - msub);
+        ls += p0 + p1;
+        split2w(p0, p1, hw[e], lw[e]);
       }
-      // P and O belong to PV(j-1) until it completes
-      if (j == 0 || mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+      l_part = fmaf(l_part, alpha, ls);
+      // P(j) replaces this thread's scores: hi in the first 32 columns of its
+      // half, lo in the next 32
+      tmem_st32_nowait(t_s, hw);
+      tmem_st32_nowait(t_s + 32, lw);
+      // O belongs to PV(j-1) until it completes
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
           for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -747,18 +786,10 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
             for (int i = 0; i < 32; ++i) v[i] *= alpha;
             tmem_st32(t_o + lb + half * (D / 2) + c0, v);
           }
-          if (half == 0) {
-            const float l = tmem_ld1(t_o + lb + D);
-            tmem_st1(t_o + lb + D, l * alpha);
-          }
         }
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(sP + sw_off(row, 64 * half + 8 * c8, 128)) =
-              make_uint4(h[4 * c8], h[4 * c8 + 1], h[4 * c8 + 2], h[4 * c8 + 3]);
+        // (a failed wait leaves O alone; the next block's check stops the warp)
       }
-      // (a failed wait leaves P and O alone; the next block's check stops the warp)
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
@@ -768,19 +799,21 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const bool ok = *fail == 0;
+  // row sums of the two halves meet in shared memory
+  if (tid < 256) xm[half * 128 + row] = l_part;
+  __syncthreads();
   // ---- epilogue: O / l, one inverse rotation, store (one thread per row)
   if (tid < 128) {
     float o[D];
-    float l_row = 0.f;
+    const float l_row = xm[row] + xm[128 + row];
     if (n_blk > 0 && ok) {
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float v[32];
-        tmem_ld32(t_o + lane_base_of(warp) + c0, v);
+        tmem_ld32(t_o + lb + c0, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c0 + i] = v[i];
       }
-      l_row = tmem_ld1(t_o + lane_base_of(warp) + D);
     } else {
 #pragma unroll
       for (int c = 0; c < D; ++c) o[c] = 0.f;
@@ -809,41 +842,42 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
 // ---------------------------------------------------------------------------
 // attention at head_dim 256
 //
-// Q' hi and lo of 128 score rows take 128 KB of shared memory at this width,
-// so keys stream in 32-key sub-blocks (K~ hi and lo 16 KB each, one buffer)
-// and V~^T and P in 64-key halves of a block image. Roles, barriers and the
-// tensor-pipe order S(0), S(1), PV(0), S(2), PV(1), ... are those of
-// prefill_kernel, per sub-block; TMEM holds S double-buffered (columns 0-31
-// and 32-63), the row sums (column 64, from the ones row of the V operand,
-// as a separate N=16 product because O alone is 256 columns wide) and O
-// (columns 256-511). The two 128-channel halves of a row's rotation (the
-// prologue's H q and the epilogue's H o) meet through shared memory: one
-// butterfly over channel bit 7. A chunk whose grid would leave more than half
-// of the SMs idle runs as clusters of two CTAs (gridDim.z = 2) that take
-// alternate 128-key blocks of the same rows; rank 1 hands its (m, l, O) to
-// rank 0 through distributed shared memory and rank 0 merges and stores.
+// TMEM cannot hold Q' hi and lo (256 columns each) beside O (256 columns), so
+// Q' hi stays in TMEM and Q' lo in shared memory (the Q'l K~h product takes
+// both operands from shared memory). Keys stream in 64-key sub-blocks: K~ hi
+// and lo of a sub-block (32 KB each, one buffer, each half on its own
+// barrier so the next sub-block's hi half streams in while this one's
+// Q'h K~l product runs) and V~^T hi and lo (32 KB each). TMEM: Q' hi in
+// columns 0-127, S double-buffered in 128-191 and 192-255 (N = 64), O in
+// 256-511. Roles, barriers and the tensor-pipe order S(0), S(1), PV(0), S(2),
+// PV(1), ... are those of prefill_kernel, per sub-block. The two 128-channel
+// halves of a row's rotation (the prologue's H q and the epilogue's H o) meet
+// through shared memory: one butterfly over channel bit 7. A chunk whose grid
+// would leave more than half of the SMs idle runs as clusters of two CTAs
+// (gridDim.z = 2) that take alternate 128-key blocks of the same rows; rank 1
+// hands its (m, l, O) to rank 0 through distributed shared memory and rank 0
+// merges and stores.
 struct PA256 {
   static constexpr int D = 256;
-  static constexpr int QB = 128 * D * 2;                 // fp16 Q' hi or lo [128 rows][256]
-  static constexpr int KSB = 32 * D * 2;                 // K~ hi or lo of 32 keys: 4 x [32 rows][64 ch]
-  static constexpr int NV = D + 16;                      // V~^T rows + a ones row + 15 zero rows
-  static constexpr int VH = NV * 128;                    // V operand of 64 keys
-  static constexpr int OFF_QH = 0;
-  static constexpr int OFF_QL = OFF_QH + QB;
+  static constexpr int QB = 128 * D * 2;                 // fp16 Q' lo [128 rows][256]
+  static constexpr int KSB = 64 * D * 2;                 // K~ hi or lo of 64 keys: 4 x [64 rows][64 ch]
+  static constexpr int VSB = D * 64 * 2;                 // V~^T hi or lo of 64 keys: [256 rows][64 keys]
+  static constexpr int OFF_QL = 0;
   static constexpr int OFF_KH = OFF_QL + QB;
   static constexpr int OFF_KL = OFF_KH + KSB;
-  static constexpr int OFF_V = OFF_KL + KSB;
-  static constexpr int OFF_P = OFF_V + VH;               // fp16 P [128 rows][64 keys]
-  static constexpr int OFF_BAR = OFF_P + 128 * 64 * 2;
-  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int OFF_VH = OFF_KL + KSB;
+  static constexpr int OFF_VL = OFF_VH + VSB;
+  static constexpr int OFF_BAR = OFF_VL + VSB;
+  static constexpr int OFF_XM = OFF_BAR + 64;            // float [2][2][128]
+  static constexpr int OFF_XB = OFF_XM + 2 * 2 * 128 * 4; // int [2][8]
+  static constexpr int OFF_MISC = OFF_XB + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int T_L = 64;                         // row-sum column
-  static constexpr int T_O = 256;                        // O columns 256..511
-  static_assert(OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && VH % 1024 == 0,
-                "swizzled operands on 1024-byte boundaries");
+  static constexpr int T_QH = 0, T_S = 128, T_O = 256;
+  static_assert(OFF_KH % 1024 == 0 && OFF_VH % 1024 == 0 && OFF_VL % 1024 == 0, "swizzle atoms");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(OFF_V - OFF_KH >= 32 * 1024, "prologue exchange fits the K~ buffers");
+  static_assert(OFF_VH >= 128 * 1024, "epilogue exchange fits Q'l and the K~ buffers");
+  static_assert(OFF_BAR - OFF_KH >= 32 * 1024, "prologue exchange fits the K~ buffers");
 };
 
 __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs a) {
@@ -852,23 +886,23 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                        ~uintptr_t(1023));
-  unsigned char* sQh = sm + P::OFF_QH;
   unsigned char* sQl = sm + P::OFF_QL;
   unsigned char* sKh = sm + P::OFF_KH;
   unsigned char* sKl = sm + P::OFF_KL;
-  unsigned char* sV = sm + P::OFF_V;
-  unsigned char* sP = sm + P::OFF_P;
+  unsigned char* sVh = sm + P::OFF_VH;
   uint64_t* bar_kh = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // K~ hi of sub-block landed
   uint64_t* bar_kl = bar_kh + 1;   // K~ lo landed
-  uint64_t* bar_v = bar_kh + 2;    // V~^T of a 64-key half landed
+  uint64_t* bar_v = bar_kh + 2;    // V~^T hi + lo landed
   uint64_t* bar_s = bar_kh + 3;    // [2] S(j) complete (TMEM buffer j & 1); K~ lo free
   uint64_t* bar_khf = bar_kh + 5;  // the K~ hi products of S(j) complete: K~ hi free
-  uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: its P half read, O and l current
-  uint64_t* bar_p = bar_kh + 7;    // P(j) written and O rescaled (one arrival per softmax warp)
+  uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: V~^T free, O current
+  uint64_t* bar_p = bar_kh + 7;    // P(j) in TMEM, O rescaled (one arrival per softmax warp)
+  float* xm = reinterpret_cast<float*>(sm + P::OFF_XM);
+  int* xb = reinterpret_cast<int*>(sm + P::OFF_XB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
   volatile int* fail = reinterpret_cast<volatile int*>(sm + P::OFF_MISC + 4);
   float4* xch = reinterpret_cast<float4*>(sm + P::OFF_KH);  // prologue exchange (32 KB)
-  float4* ych = reinterpret_cast<float4*>(sm + P::OFF_QH);  // epilogue exchange (128 KB)
+  float4* ych = reinterpret_cast<float4*>(sm + P::OFF_QL);  // epilogue exchange (128 KB)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid & 127, half = (tid >> 7) & 1;
@@ -881,20 +915,14 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   const int64_t pmax = a.pos0 + min(a.C, i0 + ppc) - 1;
   const int64_t pmin = a.pos0 + i0;
   const int hq = kvh * a.G + min(my_g, a.G - 1);
-
   const int64_t win_pos0 = 128LL * a.n_tiles;
-  int n_tile_blk = a.n_tiles;
-  if (n_tile_blk > 0 && 128LL * (n_tile_blk - 1) > pmax) n_tile_blk = (int)(pmax / 128) + 1;
-  n_tile_blk = min(n_tile_blk, a.n_tiles);
-  int n_win_blk = 0;
-  for (int w = 0; 128 * w < a.win_len; ++w)
-    if (win_pos0 + 128 * w <= pmax) n_win_blk = w + 1;
-  const int n_blk = n_tile_blk + n_win_blk;
+  const Visible vis_blk = visible_blocks(a, pmax);
+  const int n_tile_blk = vis_blk.n_tile_blk, n_blk = vis_blk.n_blk;
   // key split: with gridDim.z = 2 the two CTAs of a cluster take alternate
   // 128-key blocks of the same rows and merge (m, l, O) at the end
   const int rank = blockIdx.z, nsplit = gridDim.z;
   const int n_loc = n_blk > rank ? (n_blk - rank + nsplit - 1) / nsplit : 0;
-  const int n_sub = 4 * n_loc;  // this CTA's 32-key sub-blocks
+  const int n_sub = 2 * n_loc;  // this CTA's 64-key sub-blocks
   auto gblk = [&](int k) { return k * nsplit + rank; };  // local block -> visible block
   auto image = [&](int jj) -> const uint8_t* {
     const int widx = jj < n_tile_blk ? jj : a.n_tblk + (jj - n_tile_blk);
@@ -913,10 +941,17 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
                  "r"(P::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_o = tmem + P::T_O;
+  const uint32_t lb = lane_base_of(warp);
   const float rs2 = 0.70710678118654752f;
   if (tid < 256) {
     // Q' row: two threads per row, each rotating its 128 channels; the
-    // butterfly over channel bit 7 pairs them through shared memory
+    // butterfly over channel bit 7 pairs them through shared memory. Q' hi
+    // goes to TMEM (columns 64 half ..), Q' lo to shared memory.
     float x[128];
     if (my_valid) {
       const float4* src =
@@ -952,53 +987,46 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
+      uint32_t hw[16];
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
-        __align__(16) __half2 hi[4], lo[4];
+        uint32_t lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split2(y[8 * c8 + 2 * e], y[8 * c8 + 2 * e + 1], hi[e], lo[e]);
+        for (int e = 0; e < 4; ++e) split2w(y[8 * c8 + 2 * e], y[8 * c8 + 2 * e + 1], hw[4 * c8 + e], lo[e]);
         const int c = 128 * half + 32 * pass + 8 * c8;
-        *reinterpret_cast<uint4*>(sQh + sw_off(row, c, 128)) = *reinterpret_cast<uint4*>(hi);
-        *reinterpret_cast<uint4*>(sQl + sw_off(row, c, 128)) = *reinterpret_cast<uint4*>(lo);
+        *reinterpret_cast<uint4*>(sQl + sw_off(row, c, 128)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      tmem_st16_nowait(tmem + lb + P::T_QH + 64 * half + 16 * pass, hw);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  } else {
-    // rows 256 .. 271 of the V operand: a row of ones (the l product sums P
-    // into TMEM column 64) and zeros
-    for (int idx = tid - 256; idx < 16 * 8; idx += 64) {
-      const int r = idx >> 3, c16 = idx & 7;
-      const uint32_t w = r == 0 ? 0x3C003C00u : 0u;
-      *reinterpret_cast<uint4*>(sV + (D + r) * 128 + c16 * 16) = make_uint4(w, w, w, w);
-    }
+    tmem_wait_st();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t t_o = tmem + P::T_O, t_l = tmem + P::T_L;
 
-  float m_ref = -INFINITY;  // softmax threads: the reference maximum of their row
+  float m_ref = -INFINITY, l_part = 0.f;  // softmax threads: reference max, half-row sum
   if (warp == 9) {
     // ---------------- loader
     if (lane == 0 && n_sub > 0) {
       int nkh = 1, nkl = 1, nv = 1;
       auto load_k = [&](unsigned char* dst, int part, int jsub, uint64_t* b) {
-        // rows 32 s .. 32 s + 31 of each 64-channel block of the image's K~ part
-        const uint8_t* src = image(gblk(jsub >> 2)) + part * PC<256>::OPB + (jsub & 3) * 4096;
+        // rows 64 s .. 64 s + 63 of each 64-channel block of the image's K~ part
+        const uint8_t* src = image(gblk(jsub >> 1)) + part * PC<256>::OPB + (jsub & 1) * 8192;
         mbar_expect_tx(b, P::KSB);
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) bulk_copy_tx(dst + kb * 4096, src + kb * 16384, 4096, b);
+        for (int kb = 0; kb < 4; ++kb) bulk_copy_tx(dst + kb * 8192, src + kb * 16384, 8192, b);
       };
-      auto load_v = [&](int vh) {  // 64-key half vh of the run of sub-blocks
-        const uint8_t* src = image(gblk(vh >> 1)) + 2 * PC<256>::OPB + (vh & 1) * (D * 128);
-        mbar_expect_tx(bar_v, D * 128);
-        bulk_copy_tx(sV, src, D * 128, bar_v);
+      auto load_v = [&](int jsub) {  // key half jsub & 1 of the block's V~^T hi and lo
+        const uint8_t* src = image(gblk(jsub >> 1)) + 2 * PC<256>::OPB + (jsub & 1) * P::VSB;
+        mbar_expect_tx(bar_v, 2 * P::VSB);
+        bulk_copy_tx(sVh, src, P::VSB, bar_v);
+        bulk_copy_tx(sVh + P::VSB, src + PC<256>::OPB, P::VSB, bar_v);
       };
       load_k(sKh, 0, 0, bar_kh);
       load_k(sKl, 1, 0, bar_kl);
       load_v(0);
+      // completion order of the tensor pipe: S(j-1) hi part, S(j-1), PV(j-1)
       for (int j = 1; j < n_sub; ++j) {
         if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail)) break;
         load_k(sKh, 0, j, bar_kh);
@@ -1006,12 +1034,9 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail)) break;
         load_k(sKl, 1, j, bar_kl);
         ++nkl;
-        // half (j - 1) / 2 of V follows PV(j - 2), the last product of the previous half
-        if (j >= 3 && (j & 1)) {
-          if (!mbar_wait_flag(bar_o, (uint32_t)(j - 2) & 1u, fail)) break;
-          load_v((j - 1) >> 1);
-          ++nv;
-        }
+        if (!mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) break;
+        load_v(j);
+        ++nv;
       }
       mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u);
       mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u);
@@ -1024,15 +1049,16 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
       auto issue_s = [&](int j) -> bool {
-        const uint32_t t_s = tmem + 32 * (j & 1);
+        const uint32_t t_s = tmem + P::T_S + 64 * (j & 1);
         if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          const uint32_t off_b = (kk >> 2) * 32 * 128 + (kk & 3) * 32;
-          mma_f16(t_s, sdesc(su32(sQh) + off_a), sdesc(su32(sKh) + off_b), idesc<32>(), kk > 0);
-          mma_f16(t_s, sdesc(su32(sQl) + off_a), sdesc(su32(sKh) + off_b), idesc<32>(), 1);
+          const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
+          const uint32_t qh = tmem + P::T_QH + 8 * kk;
+          mma_f16_ts(t_s, qh, sdesc(su32(sKh) + off_b), idesc<64>(), kk > 0);
+          mma_f16(t_s, sdesc(su32(sQl) + off_a), sdesc(su32(sKh) + off_b), idesc<64>(), 1);
         }
         mma_commit(bar_khf);
         last = bar_khf; last_par = (uint32_t)j & 1u;
@@ -1040,9 +1066,8 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          const uint32_t off_b = (kk >> 2) * 32 * 128 + (kk & 3) * 32;
-          mma_f16(t_s, sdesc(su32(sQh) + off_a), sdesc(su32(sKl) + off_b), idesc<32>(), 1);
+          const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
+          mma_f16_ts(t_s, tmem + P::T_QH + 8 * kk, sdesc(su32(sKl) + off_b), idesc<64>(), 1);
         }
         mma_commit(bar_s + (j & 1));
         last = bar_s + (j & 1); last_par = (uint32_t)(j >> 1) & 1u;
@@ -1052,14 +1077,17 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       for (int j = 0; ok && j < n_sub; ++j) {
         if (j + 1 < n_sub && !issue_s(j + 1)) break;
         if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
-        if (!mbar_wait_flag(bar_v, (uint32_t)(j >> 1) & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t t_p = tmem + P::T_S + 64 * (j & 1);
+        const uint32_t vh = su32(sVh), vl = vh + P::VSB;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint32_t off = (uint32_t)(2 * (j & 1) + i) * 32;  // keys 32 (j & 1) + 16 i ..
-          const uint32_t acc = (j > 0 || i > 0) ? 1u : 0u;
-          mma_f16(t_o, sdesc(su32(sP) + off), sdesc(su32(sV) + off), idesc<256>(), acc);
-          mma_f16(t_l, sdesc(su32(sP) + off), sdesc(su32(sV) + D * 128 + off), idesc<16>(), acc);
+        for (int kk = 0; kk < 4; ++kk) {  // 16 keys each; keys 32 h .. are thread half h's
+          const uint32_t ph = t_p + 32 * (kk >> 1) + 8 * (kk & 1), pl = ph + 16;
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          mma_f16_ts(t_o, ph, sdesc(vh + 32 * kk), idesc<256>(), acc);
+          mma_f16_ts(t_o, pl, sdesc(vh + 32 * kk), idesc<256>(), 1);
+          mma_f16_ts(t_o, ph, sdesc(vl + 32 * kk), idesc<256>(), 1);
         }
         mma_commit(bar_o);
         last = bar_o; last_par = (uint32_t)j & 1u;
@@ -1068,48 +1096,56 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
     }
     __syncwarp();
   } else {
-    // ---------------- softmax (warps 0-7): two threads per row, 16 keys each
-    const uint32_t lb = lane_base_of(warp);
+    // ---------------- softmax (warps 0-7): two threads per row, 32 keys each
     for (int j = 0; j < n_sub; ++j) {
-      const int jb = gblk(j >> 2), sb = j & 3;
+      const int jb = gblk(j >> 1), sb = j & 1;
       const bool is_tile = jb < n_tile_blk;
-      const int64_t kpos0 = (is_tile ? 128LL * jb : win_pos0 + 128LL * (jb - n_tile_blk)) + 32 * sb;
-      const int nkeys = (is_tile ? 128 : min(128, a.win_len - 128 * (jb - n_tile_blk))) - 32 * sb;
-      const bool full_vis = kpos0 + 31 <= pmin && nkeys >= 32;
+      const int64_t kpos0 = (is_tile ? 128LL * jb : win_pos0 + 128LL * (jb - n_tile_blk)) + 64 * sb;
+      const int nkeys = (is_tile ? 128 : min(128, a.win_len - 128 * (jb - n_tile_blk))) - 64 * sb;
+      const bool full_vis = kpos0 + 63 <= pmin && nkeys >= 64;
       bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
-      if (__any_sync(0xffffffffu, bad || *fail != 0)) break;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      bad = __any_sync(0xffffffffu, bad || *fail != 0);
+      const uint32_t t_s = tmem + P::T_S + 64 * (j & 1) + lb + 32 * half;
       float sv[32];
-      tmem_ld32(tmem + 32 * (j & 1) + lb, sv);
-      float mblk = -INFINITY;
-      if (full_vis) {
+      float mloc = -INFINITY;
+      if (!bad) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tmem_ld32(t_s, sv);
+        if (full_vis) {
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) mblk = fmax3(mblk, sv[u], sv[u + 1]);
-        if (!my_valid) mblk = -INFINITY;
-      } else {
+          for (int u = 0; u < 32; u += 2) mloc = fmax3(mloc, sv[u], sv[u + 1]);
+          if (!my_valid) mloc = -INFINITY;
+        } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const bool vis = my_valid && u < nkeys && kpos0 + u <= my_pos;
-          sv[u] = vis ? sv[u] : -INFINITY;
-          mblk = fmaxf(mblk, sv[u]);
+          for (int u = 0; u < 32; ++u) {
+            const int t = 32 * half + u;
+            const bool vis = my_valid && t < nkeys && kpos0 + t <= my_pos;
+            sv[u] = vis ? sv[u] : -INFINITY;
+            mloc = fmaxf(mloc, sv[u]);
+          }
         }
       }
+      float mblk;
+      if (!pair_max(mloc, bad, xm, xb, j & 1, half, row, warp, mblk)) break;
       const bool need = mblk > m_ref + 8.0f;
       const float m_new = need ? mblk : m_ref;
       const float alpha = (need && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.0f;
       m_ref = m_new;
       const float msub = m_ref == -INFINITY ? INFINITY : m_ref;
-      uint32_t h[8];
+      uint32_t hw[16], lw[16];
+      float ls = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {  // this thread's 16 keys (selects keep sv in registers)
-        const float s0 = half ? sv[16 + 2 * e] : sv[2 * e];
-        const float s1 = half ? sv[17 + 2 * e] : sv[2 * e + 1];
-        const __half2 hp = __floats2half2_rn(ex2_ftz(s0 - msub), ex2_ftz(s1 - msub));
-        h[e] = *reinterpret_cast<const uint32_t*>(&hp);
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = ex2_ftz(sv[2 * e] - msub), p1 = ex2_ftz(sv[2 * e + 1] - msub);
+        ls += p0 + p1;
+        split2w(p0, p1, hw[e], lw[e]);
       }
-      // O and l belong to PV(j-1) until it completes
-      if (j == 0 || mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+      l_part = fmaf(l_part, alpha, ls);
+      tmem_st16_nowait(t_s, hw);
+      tmem_st16_nowait(t_s + 16, lw);
+      // O belongs to PV(j-1) until it completes
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
           for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -1119,17 +1155,9 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
             for (int i = 0; i < 32; ++i) v[i] *= alpha;
             tmem_st32(t_o + lb + half * (D / 2) + c0, v);
           }
-          if (half == 0) {
-            const float l = tmem_ld1(t_l + lb);
-            tmem_st1(t_l + lb, l * alpha);
-          }
         }
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8)
-          *reinterpret_cast<uint4*>(sP + sw_off(row, 32 * (j & 1) + 16 * half + 8 * c8, 128)) =
-              make_uint4(h[4 * c8], h[4 * c8 + 1], h[4 * c8 + 2], h[4 * c8 + 3]);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
@@ -1139,11 +1167,13 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   bool ok = *fail == 0;
+  if (tid < 256) xm[half * 128 + row] = l_part;
+  __syncthreads();
   // ---- epilogue: O / l, one inverse rotation (two threads per row), store
-  const uint32_t lb = lane_base_of(warp);
   float o[128];
   float l_row = 0.f;
   if (tid < 256) {
+    l_row = xm[row] + xm[128 + row];
     if (n_sub > 0 && ok) {
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -1152,17 +1182,16 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[c0 + i] = v[i];
       }
-      l_row = tmem_ld1(t_l + lb);
     } else {
 #pragma unroll
       for (int c = 0; c < 128; ++c) o[c] = 0.f;
     }
   }
   if (nsplit > 1) {
-    // rank 1's (m, l, O) go to rank 0's shared memory: O in the Q' region, free
-    // once both CTAs' products completed (first cluster barrier)
+    // rank 1's (m, l, O) go to rank 0's shared memory: O in the Q'l and K~
+    // region, free once both CTAs' products completed (first cluster barrier)
     cg::cluster_group cluster = cg::this_cluster();
-    float2* xml = reinterpret_cast<float2*>(sm + P::OFF_P);           // [128 rows] (m, l)
+    float2* xml = reinterpret_cast<float2*>(sm + P::OFF_VH);           // [128 rows] (m, l)
     int* xfail = reinterpret_cast<int*>(sm + P::OFF_MISC + 8);
     cluster.sync();
     if (rank == 1) {
@@ -1199,7 +1228,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
 #pragma unroll
     for (int c = 0; c < 128; ++c) o[c] *= inv;
     fwht_reg<128>(o);
-    // Q' is no longer read (the last MMA completed): its 128 KB hold the exchange
+    // Q'l and K~ are no longer read (the last MMA completed): they hold the exchange
 #pragma unroll
     for (int c4 = 0; c4 < 32; ++c4)
       ych[c4 * 256 + tid] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
@@ -1293,7 +1322,7 @@ void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, 
   *n_blk = nt + nw;
 }
 
-size_t prefill_block_bytes(int D) { return (size_t)3 * 128 * D * 2; }
+size_t prefill_block_bytes(int D) { return (size_t)4 * 128 * D * 2; }
 
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
                            const int64_t* tile_table, int table_stride, int n_tiles,

@@ -185,7 +185,7 @@ def rel_l2(got: np.ndarray, want: np.ndarray) -> float:
     return float(np.linalg.norm(got.astype(np.float64) - want) / den)
 
 
-PREFILL_RTOL = 2e-3  # tensor-core prefill (fp16 operands, fp32 accumulation)
+PREFILL_RTOL = 1e-4  # tensor-core prefill: fp16 hi + lo operand pairs, fp32 accumulation
 
 
 class PrefillRun:

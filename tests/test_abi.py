@@ -98,10 +98,10 @@ def test_prefill_host_validation(lib):
     # the workspace bound covers every tile and window block of 8 KV heads ...
     need = ctypes.c_size_t()
     assert lib.kvarn_prefill_workspace_bytes(10, 300, 8, 128, ctypes.byref(need)) == 0
-    blk = 3 * 128 * 128 * 2
+    blk = 4 * 128 * 128 * 2
     assert need.value == (10 + 3) * 8 * blk
     assert lib.kvarn_prefill_workspace_bytes(10, 300, 4, 256, ctypes.byref(need)) == 0
-    assert need.value == (10 + 3) * 4 * 3 * 128 * 256 * 2
+    assert need.value == (10 + 3) * 4 * 4 * 128 * 256 * 2
     # ... a chunk at 1000..1511 sees the 10 tiles and 2 of the window's 3 blocks
     assert f(*args(512, 1000, 10, 300, wsb=12 * 8 * blk - 1)) == -5
 
@@ -138,7 +138,7 @@ def test_f16_scale_layout_agrees_with_oracle(lib, D):
 def test_prefill_cached_host_validation(lib):
     L = kvarn.layout(128)
     p = ctypes.c_void_p(4096)
-    blk = 3 * 128 * 128 * 2
+    blk = 4 * 128 * 128 * 2
     f = lib.kvarn_prefill_attention_cached
     f.argtypes = None
     args = lambda wsb, wsblocks, cached, nt=10: (

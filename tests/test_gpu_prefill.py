@@ -32,7 +32,8 @@ def test_prefill_shapes(Hq, Hkv, D, n, chunk, W):
 
 
 def test_prefill_chunk_of_one_equals_decode():
-    """A one-token chunk is a decode step over the same cache."""
+    """A one-token chunk is a decode step over the same cache (both within
+    1e-4 of the oracle, so within 2e-4 of each other)."""
     n = 128 * 3 + 40
     run = PrefillRun("qwen3_8b_decode", 2, n, Hq=8, Hkv=2, D=128, W=128, chunk=1, keep=[n - 1])
     s = run.snap[n - 1]
@@ -46,7 +47,7 @@ def test_prefill_chunk_of_one_equals_decode():
                                  torch.tensor([s["length"]], dtype=torch.int32, device=dev),
                                  run.lay).cpu().numpy()
     for h in range(8):
-        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-3
+        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-4
     run.check(n - 1, [(0, h) for h in range(8)])
 
 
@@ -108,7 +109,7 @@ def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
     (32, 8, 1100, 512, 256, 32, 2, False),   # 128 row blocks: no key split
 ])
 def test_prefill_head_dim_256(Hq, Hkv, n, chunk, W, sb, vb, cached):
-    """head_dim 256: keys stream through the attention kernel in 32-key
+    """head_dim 256: keys stream through the attention kernel in 64-key
     sub-blocks, the rotations pair two threads per row; grids of at most
     half the SMs split each row block's keys over a two-CTA cluster."""
     run = PrefillRun("batched_d256_decode", 8, n, Hq=Hq, Hkv=Hkv, D=256, W=W, chunk=chunk,
@@ -132,5 +133,5 @@ def test_prefill_head_dim_256_chunk_of_one_equals_decode():
                                  torch.tensor([s["length"]], dtype=torch.int32, device=dev),
                                  run.lay).cpu().numpy()
     for h in range(8):
-        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-3
+        assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-4
     run.check(n - 1, [(0, h) for h in range(8)])
