@@ -348,8 +348,9 @@ def run_prefill_bench(dev, stream, lay, peaks, peak_kind, n_tok=15500, chunk=512
                         "frac": tflops / peak_tf, "traffic": None,
                         "kernel": "prefill_kernel_d256" if D_ == 256 else f"prefill_kernel<{D_}>",
                         "peak_source": peak_kind + " (dense bf16 burst; fp16 runs at the bf16 rate)"},
-           "mma": "tcgen05 kind::f16, Q and K split hi+lo (3 MMAs for Q.K, 1 for P.V)"
-                  + ("; keys in 32-key sub-blocks" if D_ == 256 else "")}
+           "mma": "tcgen05 kind::f16, A operand from TMEM; Q', K~, P and V~ each an fp16 hi+lo "
+                  "pair (3 MMAs for Q.K, 3 for P.V)"
+                  + ("; keys in 64-key sub-blocks" if D_ == 256 else "")}
     if workload == "qwen3_8b_prefill":
         res["prompt_tokens_per_s_36_layers"] = n_tok / (LAYERS * layer_ms * 1e-3)
     return res

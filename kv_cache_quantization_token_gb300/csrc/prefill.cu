@@ -557,7 +557,10 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   uint64_t* bar_v = bar_k + 2;     // V~^T of block j landed
   uint64_t* bar_s = bar_k + 3;     // [2] S(j) complete: scores ready, K~ buffer j & 1 free
   uint64_t* bar_o = bar_k + 5;     // PV(j) complete: V~^T free, O current
-  uint64_t* bar_p = bar_k + 6;     // P(j) in TMEM, O rescaled (one arrival per softmax warp)
+  // [2] P(j) in TMEM and O rescaled: one arrival per softmax warp, on the
+  // barrier of the block's parity (a warp may run one block ahead of the
+  // others; its arrival must not count toward the block before)
+  uint64_t* bar_p = bar_k + 6;
   float* xm = reinterpret_cast<float*>(sm + P::OFF_XM);
   int* xb = reinterpret_cast<int*>(sm + P::OFF_XB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
@@ -587,7 +590,8 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) mbar_init1(bar_k + i);
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p)) : "memory");
+    for (int i = 0; i < 2; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
   }
@@ -699,7 +703,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
         // S(j+1) goes in ahead of PV(j): its TMEM buffer held P(j-1), which
         // PV(j-1), issued earlier, reads first
         if (j + 1 < n_blk && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
         if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 128 * (j & 1);
@@ -792,7 +796,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       tmem_wait_st();
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
+      if (lane == 0) mbar_arrive(bar_p + (j & 1));
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -867,8 +871,8 @@ struct PA256 {
   static constexpr int OFF_KL = OFF_KH + KSB;
   static constexpr int OFF_VH = OFF_KL + KSB;
   static constexpr int OFF_VL = OFF_VH + VSB;
-  static constexpr int OFF_BAR = OFF_VL + VSB;
-  static constexpr int OFF_XM = OFF_BAR + 64;            // float [2][2][128]
+  static constexpr int OFF_BAR = OFF_VL + VSB;          // 9 mbarriers
+  static constexpr int OFF_XM = OFF_BAR + 128;           // float [2][2][128]
   static constexpr int OFF_XB = OFF_XM + 2 * 2 * 128 * 4; // int [2][8]
   static constexpr int OFF_MISC = OFF_XB + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
@@ -896,7 +900,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
   uint64_t* bar_s = bar_kh + 3;    // [2] S(j) complete (TMEM buffer j & 1); K~ lo free
   uint64_t* bar_khf = bar_kh + 5;  // the K~ hi products of S(j) complete: K~ hi free
   uint64_t* bar_o = bar_kh + 6;    // PV(j) complete: V~^T free, O current
-  uint64_t* bar_p = bar_kh + 7;    // P(j) in TMEM, O rescaled (one arrival per softmax warp)
+  uint64_t* bar_p = bar_kh + 7;    // [2] P(j) in TMEM, O rescaled (per block parity, as above)
   float* xm = reinterpret_cast<float*>(sm + P::OFF_XM);
   int* xb = reinterpret_cast<int*>(sm + P::OFF_XB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
@@ -931,7 +935,8 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
 
   if (tid == 0) {
     for (int i = 0; i < 7; ++i) mbar_init1(bar_kh + i);
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p)) : "memory");
+    for (int i = 0; i < 2; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *fail = 0;
   }
@@ -1076,7 +1081,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       bool ok = issue_s(0);
       for (int j = 0; ok && j < n_sub; ++j) {
         if (j + 1 < n_sub && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
         if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 64 * (j & 1);
@@ -1160,7 +1165,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       tmem_wait_st();
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
+      if (lane == 0) mbar_arrive(bar_p + (j & 1));
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

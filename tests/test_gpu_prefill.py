@@ -135,3 +135,14 @@ def test_prefill_head_dim_256_chunk_of_one_equals_decode():
     for h in range(8):
         assert rel_l2(s["out"][0, h], dec[0, h].astype(np.float64)) <= 2e-4
     run.check(n - 1, [(0, h) for h in range(8)])
+
+
+def test_prefill_repeat_is_bit_identical():
+    """The same 6,000-token prompt twice: every chunk's output is bit-identical
+    (the warp roles hand off through barriers only; nothing depends on timing)."""
+    a = PrefillRun("qwen3_8b_prefill", 10, 6000, Hq=32, Hkv=8, D=128, cached=True)
+    b = PrefillRun("qwen3_8b_prefill", 10, 6000, Hq=32, Hkv=8, D=128, cached=True)
+    for p in a.snap:
+        np.testing.assert_array_equal(a.snap[p]["out"], b.snap[p]["out"])
+    last = max(a.snap)
+    a.check(last, _rows(a.snap[last]["C"], (0, 7, 30), step=41))
