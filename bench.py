@@ -54,6 +54,12 @@ NCU_TRAFFIC = {
 }
 
 
+# launch flags of the timed decode calls: programmatic dependent launch with
+# record prefetch (nothing inside a step writes records, tables or tile counts;
+# promotions run between steps)
+FAST = 3  # KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH
+
+
 def src_sha(name: str) -> str:
     with open(os.path.join(ROOT, "kv_cache_quantization_token_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -378,7 +384,6 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
     from kv_cache_quantization_token_gb300 import kvarn, synth
     hbm = float(peaks["hbm_gbs"])
     res = {}
-    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
     stream = torch.cuda.Stream(device=dev)
 
     def back_to_back(launch, n_launch, reps=10):
@@ -437,11 +442,13 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
 
         def splits():
             for l in range(LAYERS):
-                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws)
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws,
+                                   flags=FAST)
 
         def steps():
             for l in range(LAYERS):
-                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws)
+                kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws,
+                                   flags=FAST)
                 kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
 
         split_ms = back_to_back(splits, LAYERS)
@@ -505,7 +512,7 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
     ev_f, ev_j = torch.cuda.Event(), torch.cuda.Event()
 
     def split1():
-        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws)
+        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws, flags=FAST)
 
     def step_conc():
         cur = torch.cuda.current_stream()
@@ -514,8 +521,8 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         with torch.cuda.stream(side):
             kvarn.compress_tile(kd, vd, psrc, ptiles, pdst, layb)
         ev_j.record(side)
-        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws)
-        kvarn.decode_combine(ws, out, Hkvb, max_tiles, capb)
+        kvarn.decode_split(q, tiles, table, nt, win_k, win_v, wst, wl, layb, ws, flags=FAST)
+        kvarn.decode_combine(ws, out, Hkvb, max_tiles, capb, flags=FAST)
         cur.wait_event(ev_j)
 
     split_ms = back_to_back(lambda: [split1() for _ in range(8)], 8)
@@ -533,7 +540,6 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         "tokens_per_s_per_layer": Bb / (step_ms * 1e-3),
         "concurrent_compress_tile_heads_per_step": n_prom,
         "peak_source": peak_kind}
-    kvarn.set_launch_flags(0)
     return res
 
 
@@ -597,8 +603,10 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--section", default="all",
-                    choices=["all", "prefill", "prefill-d256", "decode-sweeps", "compress"],
-                    help="run one secondary measurement alone and print its JSON (for profiling)")
+                    choices=["all", "decode", "prefill", "prefill-d256", "decode-sweeps", "compress"],
+                    help="decode: the headline decode step alone (no secondary measurements); "
+                         "the others run one secondary measurement alone and print its JSON "
+                         "(for profiling)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -621,7 +629,7 @@ def main():
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     lay = kvarn.layout(D)
-    if args.section != "all":
+    if args.section not in ("all", "decode"):
         peaks, peak_kind = measured_peaks()
         if args.section == "prefill":
             st = torch.cuda.Stream(device=dev)
@@ -640,8 +648,10 @@ def main():
     rb = lay.record_bytes
     B = 1
     cap = 128
-    # the window starts part-filled so promotions fall inside the timed steps
-    w0 = 64
+    # the window starts part-filled so that it reaches W = 128, and the first
+    # promotion falls, right after the first timed step (1 + warmup tokens are
+    # appended before the timed region); further ones follow every 128 steps
+    w0 = (126 - args.warmup) % 128
     e2e_steps = max(10, args.steps // 5)
     total_steps = 1 + args.warmup + args.steps + e2e_steps
     max_tiles = CTX0 // 128 + (w0 + total_steps) // 128 + 1
@@ -719,24 +729,24 @@ def main():
         side.wait_event(ev_fork)
         with torch.cuda.stream(side):
             for l in range(LAYERS):
-                kvarn.append_window(kn[l], vn[l], win_k[l], win_v[l], win_start, win_len)
+                kvarn.append_window(kn[l], vn[l], win_k[l], win_v[l], win_start, win_len,
+                                    flags=FAST)
         ev_join.record(side)
         for l in range(LAYERS):
             if record_events:
                 ev_split[l][0].record()
             kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
-                               win_len, lay, ws)
+                               win_len, lay, ws, flags=FAST)
             if record_events:
                 ev_split[l][1].record()
-            kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
+            kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap, flags=FAST)
         cur.wait_event(ev_join)
-        kvarn.window_advance(win_start, win_len, None, 1, 0, cap)
+        kvarn.window_advance(win_start, win_len, None, 1, 0, cap, flags=FAST)
 
     per_step_launches = 3 * LAYERS + 1
     # kernels of a step chain by programmatic dependent launch; the split kernels
     # stream their records in before waiting on the previous kernel (nothing in
     # the step writes records, tables or tile counts: promotions run between steps)
-    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
@@ -757,7 +767,7 @@ def main():
     with torch.cuda.graph(graph_split, stream=stream):
         for l in range(LAYERS):
             kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
-                               win_len, lay, ws)
+                               win_len, lay, ws, flags=FAST)
 
     def run_steps(n):
         for _ in range(n):
@@ -808,7 +818,7 @@ def main():
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 kvarn.decode_split(q[l], tiles, table[l], n_tiles, win_k[l], win_v[l], win_start,
-                                   win_len, lay, ws)
+                                   win_len, lay, ws, flags=FAST)
                 b.record()
                 evs.append((a, b))
         torch.cuda.synchronize()
@@ -858,25 +868,29 @@ def main():
     _, e2e_tps = reduce_timing(e0.elapsed_time(e1), B * e2e_steps, world, dev)
     assert np.isfinite(out_h.numpy()).all(), "decode produced non-finite output"
 
+    secondary = args.section == "all"
+    compress = prefill = prefill_d256 = sweeps = None
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
-    compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
-    # head_dim 256: 1024 tile-heads, the same 256 MiB of input
-    try:
-        compress["head_dim_256"] = run_compress_bench(dev, stream, kvarn.layout(256), args.warmup,
-                                                      hbm, peak_kind, tiles=C_TILES // 2)
-    except Exception as e:  # a secondary measurement: report, keep the bench line
-        print(f"head_dim-256 compress measurement failed: {e!r}", file=sys.stderr)
-        compress["head_dim_256"] = {"error": repr(e)}
+    if secondary:
+        compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
+        # head_dim 256: 1024 tile-heads, the same 256 MiB of input
+        try:
+            compress["head_dim_256"] = run_compress_bench(dev, stream, kvarn.layout(256),
+                                                          args.warmup, hbm, peak_kind,
+                                                          tiles=C_TILES // 2)
+        except Exception as e:  # a secondary measurement: report, keep the bench line
+            print(f"head_dim-256 compress measurement failed: {e!r}", file=sys.stderr)
+            compress["head_dim_256"] = {"error": repr(e)}
 
-    # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256), and
-    # an 8,192-token prompt with head_dim-256 heads
-    prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
-    prefill_d256 = run_prefill_d256(dev, stream, peaks, peak_kind)
-    # ---- decode at other contexts and batched large-head decode
-    sweeps = run_decode_sweeps(dev, lay, peaks, peak_kind)
+        # ---- chunked prefill (15,500-token prompt, 512-token chunks, W=256), and
+        # an 8,192-token prompt with head_dim-256 heads
+        prefill = run_prefill_bench(dev, stream, lay, peaks, peak_kind)
+        prefill_d256 = run_prefill_d256(dev, stream, peaks, peak_kind)
+        # ---- decode at other contexts and batched large-head decode
+        sweeps = run_decode_sweeps(dev, lay, peaks, peak_kind)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and secondary:
         # layer 0's whole 16k-token cache, repeated for about 10 s of host work
         smp = OracleDecodeSample(CTX0 // 128)
         secs, t_all = [], time.perf_counter()

@@ -25,9 +25,19 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every array argument is a DEVICE pointer owned by the caller, unless the
- *    argument says "host". The library never allocates device memory and keeps
- *    no state between calls: scratch space is passed in as a workspace.
- *  - Work is enqueued asynchronously on the given stream; nothing synchronises.
+ *    argument says "host". The library never allocates device memory and
+ *    keeps no state between calls: scratch space is passed in as a workspace,
+ *    and how a call's kernels are launched is an argument of that call
+ *    (launch_flags). The two exceptions are the sticky device error word
+ *    (kvarn_get_device_error) and the fixed scratch array of
+ *    kvarn_decode_attention_noalloc.
+ *  - Work is enqueued asynchronously on the given stream; nothing synchronises
+ *    except kvarn_get_device_error.
+ *  - Calls that read packed records take the record pool's size (tiles_bytes);
+ *    a record whose offset is negative, misaligned or runs past the pool is
+ *    not read: the kernel poisons what depends on it with NaN and sets
+ *    KVARN_DEVERR_RECORD in the device error word. Writes are bounded the
+ *    same way (kvarn_compress_tile).
  *  - All floating-point data is IEEE fp32, little-endian.
  *  - The return value is a kvarn_status_t. Argument errors are detected on the
  *    host before anything is launched and nothing is enqueued in that case.
@@ -71,6 +81,50 @@ typedef enum kvarn_status {
 #define KVARN_LAYOUT_VERSION 1
 #define KVARN_LAYOUT_VERSION_F16_SCALES 2
 #define KVARN_DEFAULT_SINKHORN_ITERS 4
+
+/*
+ * Launch flags of the calls on the decode path (kvarn_append_window,
+ * kvarn_window_advance, kvarn_decode_split, kvarn_decode_combine,
+ * kvarn_decode_attention, kvarn_decode_attention_noalloc), per call. The pages
+ * have no counterpart: this is how the kernels are chained on this GPU.
+ *   0                      plain stream-ordered launches.
+ *   KVARN_LAUNCH_PDL       programmatic dependent launch: the kernel may be
+ *                          scheduled while the previous kernel on the stream
+ *                          is still running and waits for it on the device
+ *                          before touching memory, which hides the launch
+ *                          gap. Results are identical to 0.
+ *   KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH
+ *                          as above, and the split kernel reads n_tiles, the
+ *                          tile table and the packed records BEFORE that wait
+ *                          (so a layer's records stream in while the previous
+ *                          kernels finish). The caller guarantees that no
+ *                          kernel still running ahead of it on the stream
+ *                          writes those three (e.g. promotions are enqueued
+ *                          between graph replays, not inside the step).
+ * Other bits, or PREFETCH without PDL, give KVARN_ERR_BAD_ARG.
+ */
+#define KVARN_LAUNCH_PDL 1u
+#define KVARN_LAUNCH_PREFETCH 2u
+
+/*
+ * Device error bits (kvarn_get_device_error). A kernel that gives up on
+ * something sets its bit and writes NaN where the result depends on it; it
+ * never traps, so the CUDA context stays usable.
+ *   KVARN_DEVERR_WAIT      a wait for an asynchronous copy or tensor-core
+ *                          product of the same kernel ran out of time
+ *                          (200 ms): the hardware did not complete it.
+ *   KVARN_DEVERR_RECORD    a tile-table entry (or a compress destination)
+ *                          was negative, misaligned or ran past tiles_bytes;
+ *                          a compress source ran past n_rows.
+ *   KVARN_DEVERR_WINDOW    kvarn_append_window would have overfilled a
+ *                          sequence's ring (win_len + n_new > win_capacity);
+ *                          that sequence's rows were not written.
+ *   KVARN_DEVERR_SELFTEST  set by kvarn_selftest_bounded_wait.
+ */
+#define KVARN_DEVERR_WAIT 1u
+#define KVARN_DEVERR_RECORD 2u
+#define KVARN_DEVERR_WINDOW 4u
+#define KVARN_DEVERR_SELFTEST 8u
 
 /*
  * Packed tile record: one record per (tile, KV head), headerless, all fields
@@ -158,6 +212,27 @@ int kvarn_layout_ex(int head_dim, int sinkhorn_iters, int scale_bits, int v_bits
 const char* kvarn_status_string(int status);
 
 /*
+ * Reads the current device's error word (KVARN_DEVERR_* bits set by kernels
+ * of this library since it was last cleared) into *bits (host pointer) and,
+ * if clear is non-zero, clears it. The pages have no counterpart: it is how
+ * a kernel that gave up reports it. Synchronises the current device (a
+ * blocking copy), so do not call it inside stream capture. The first call on
+ * a device, like the first launch of any call that reports, looks the word's
+ * address up once (cudaGetSymbolAddress); make that first call outside
+ * stream capture.
+ */
+int kvarn_get_device_error(unsigned* bits, int clear);
+
+/*
+ * Self-check of the device failure path: one kernel waits on an mbarrier
+ * that nothing will complete, gives up after timeout_us microseconds
+ * (1..1000000), sets KVARN_DEVERR_SELFTEST in the error word and returns
+ * normally. Lets a caller (or a test) confirm that a device wait that runs
+ * out is reported without faulting the context. No counterpart on the pages.
+ */
+int kvarn_selftest_bounded_wait(unsigned timeout_us, kvarn_stream_t stream);
+
+/*
  * Query rotation (PR #434, commit 0d7cd28, llm_kvarn_rotate_query; issue #180
  * Algorithm step 1): q_rot[i] = H q[i] for every row i, H the orthonormal
  * Sylvester Walsh-Hadamard matrix of order D (symmetric, so self-inverse).
@@ -180,17 +255,21 @@ int kvarn_rotate_query(const float* q, float* q_rot, int64_t n_rows, int head_di
  * depend on which other units share the launch or on their order.
  *   k_raw, v_raw  : fp32, n_rows rows of row_stride elements, 16-byte aligned.
  *   row_stride    : elements between rows, >= D and a multiple of 4.
- *   n_rows        : rows in k_raw and v_raw; every src_row0[u] + 128 <= n_rows
- *                   is the caller's promise (not checked on the device).
+ *   n_rows        : rows in k_raw and v_raw. A unit whose rows run past
+ *                   n_rows (src_row0[u] < 0 or src_row0[u] + 128 > n_rows)
+ *                   is skipped and KVARN_DEVERR_RECORD set.
  *   src_row0      : int64 [n_units], device.
- *   tiles         : u8 base of the record pool, 16-byte aligned.
+ *   tiles         : u8 base of the record pool, 16-byte aligned, tiles_bytes
+ *                   long.
  *   dst_record    : int64 [n_units] byte offsets, device, multiples of 16;
- *                   records of one launch must not overlap.
+ *                   records of one launch must not overlap. A unit whose
+ *                   record would not lie inside the pool (or is misaligned)
+ *                   is skipped and KVARN_DEVERR_RECORD set.
  *   layout        : host pointer from kvarn_layout().
  */
 int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stride,
                         int64_t n_rows, const int64_t* src_row0, uint8_t* tiles,
-                        const int64_t* dst_record, int64_t n_units,
+                        int64_t tiles_bytes, const int64_t* dst_record, int64_t n_units,
                         const kvarn_layout_t* layout, kvarn_stream_t stream);
 
 /*
@@ -202,7 +281,11 @@ int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stri
  *   win_start,
  *   win_len       : int32 [n_seq], device. New token i of sequence s goes to
  *                   ring slot (win_start[s] + win_len[s] + i) % win_capacity.
- *                   The caller guarantees win_len[s] + n_new <= win_capacity.
+ *                   win_len[s] + n_new must not exceed win_capacity (the ring
+ *                   would overwrite rows not yet promoted): a sequence for
+ *                   which it would is left unwritten and KVARN_DEVERR_WINDOW
+ *                   is set.
+ *   launch_flags  : 0 or KVARN_LAUNCH_PDL (PREFETCH has no effect here).
  * The library does not change win_start or win_len: the caller applies the
  * promotion rule (while win_len >= W, compress the oldest 128 tokens with
  * kvarn_compress_tile, then win_start += 128, win_len -= 128) and advances
@@ -212,7 +295,7 @@ int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stri
 int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new,
                         float* win_k, float* win_v, int win_capacity,
                         const int32_t* win_start, const int32_t* win_len,
-                        int n_seq, int n_kv_heads, int head_dim,
+                        int n_seq, int n_kv_heads, int head_dim, unsigned launch_flags,
                         kvarn_stream_t stream);
 
 /*
@@ -227,37 +310,15 @@ int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new,
  * the oldest 128 tokens" and has already compressed those tokens with
  * kvarn_compress_tile. win_start, win_len, n_tiles: int32 [n_seq], device
  * (n_tiles may be NULL when promote == 0). win_capacity must be a positive
- * multiple of 128. One tiny launch; it lets a whole decode step be captured.
+ * multiple of 128. d_len and promote apply to every sequence of the call: a
+ * ragged batch whose sequences promote at different steps advances each
+ * sequence with its own call (pointers offset to that sequence, n_seq = 1).
+ * One tiny launch; it lets a whole decode step be captured.
+ * launch_flags: 0 or KVARN_LAUNCH_PDL.
  */
 int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
-                         int d_len, int promote, int win_capacity, kvarn_stream_t stream);
-
-/*
- * Launch mode of the decode-path kernels (kvarn_append_window,
- * kvarn_window_advance, kvarn_decode_split, kvarn_decode_combine,
- * kvarn_decode_attention). Process-wide; applies to launches enqueued after
- * the call, including launches captured into CUDA graphs. The pages have no
- * counterpart: this is how the kernels are chained on this GPU.
- *   0                      plain stream-ordered launches (the default).
- *   KVARN_LAUNCH_PDL       programmatic dependent launch: each kernel may be
- *                          scheduled while the previous kernel on the stream
- *                          is still running and waits for it on the device
- *                          before touching memory, which hides the launch
- *                          gap. Results are identical to mode 0.
- *   KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH
- *                          as above, and the split kernel reads n_tiles, the
- *                          tile table and the packed records BEFORE that wait
- *                          (so a layer's records stream in while the previous
- *                          kernels finish). The caller guarantees that no
- *                          kernel still running ahead of it on the stream
- *                          writes those three (e.g. promotions are enqueued
- *                          between graph replays, not inside the step).
- * Returns KVARN_ERR_BAD_ARG for unknown bits or PREFETCH without PDL.
- */
-#define KVARN_LAUNCH_PDL 1u
-#define KVARN_LAUNCH_PREFETCH 2u
-int kvarn_set_launch_flags(unsigned flags);
-unsigned kvarn_get_launch_flags(void);
+                         int d_len, int promote, int win_capacity, unsigned launch_flags,
+                         kvarn_stream_t stream);
 
 /*
  * Decode attention over the compressed cache (PR #434, commits 0d7cd28 and
@@ -280,12 +341,13 @@ unsigned kvarn_get_launch_flags(void);
  * over every cached token j of KV head h / G: the tiles' tokens (k_j, v_j
  * reconstructed as described at kvarn_layout_t) and then the window's raw rows.
  *   q          : fp32 [B][Hq][D], unrotated. Hq / Hkv = G must be 1..8.
- *   tiles      : u8 base of the record pool.
+ *   tiles      : u8 base of the record pool, tiles_bytes long.
  *   tile_table : int64 [B][Hkv][max_tiles] record byte offsets, multiples of
  *                128 (record_bytes is a multiple of 128, so a pool of whole
- *                records qualifies; another offset makes that head's output
- *                NaN);
- *                entries at or past n_tiles[b] are never read.
+ *                records qualifies); an entry that is misaligned, negative or
+ *                runs past tiles_bytes makes that head's output NaN and sets
+ *                KVARN_DEVERR_RECORD; entries at or past n_tiles[b] are never
+ *                read.
  *   n_tiles    : int32 [B], 0 <= n_tiles[b] <= max_tiles (clamped on device).
  *   win_k/v    : fp32 [B][Hkv][win_capacity][D]; win_start/win_len int32 [B]
  *                as in kvarn_append_window (win_len clamped to win_capacity).
@@ -294,26 +356,29 @@ unsigned kvarn_get_launch_flags(void);
  *   ws         : device workspace of at least kvarn_decode_workspace_bytes()
  *                bytes, 256-byte aligned; it holds the per-item partials and
  *                needs no initialisation. Calls sharing ws must not overlap.
+ *   launch_flags : KVARN_LAUNCH_* bits, see above.
  * The grids depend only on (B, Hq, Hkv, D, max_tiles, win_capacity, device),
  * so the calls can be captured in a CUDA graph and replayed while n_tiles and
  * the windows change. Results are deterministic (bit-identical on repeat).
  */
 int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_tiles,
                                  int win_capacity, size_t* bytes);
-int kvarn_decode_split(const float* q, const uint8_t* tiles, const int64_t* tile_table,
-                       const int32_t* n_tiles, const float* win_k, const float* win_v,
-                       const int32_t* win_start, const int32_t* win_len, int win_capacity, int B,
-                       int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
-                       const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
-                       kvarn_stream_t stream);
+int kvarn_decode_split(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
+                       const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
+                       const float* win_v, const int32_t* win_start, const int32_t* win_len,
+                       int win_capacity, int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                       float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                       size_t ws_bytes, unsigned launch_flags, kvarn_stream_t stream);
 int kvarn_decode_combine(const void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int head_dim,
-                         int max_tiles, int win_capacity, float* out, kvarn_stream_t stream);
-int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
-                           const int32_t* n_tiles, const float* win_k, const float* win_v,
-                           const int32_t* win_start, const int32_t* win_len,
-                           int win_capacity, int B, int Hq, int Hkv, int head_dim,
-                           int max_tiles, float softmax_scale, const kvarn_layout_t* layout,
-                           void* ws, size_t ws_bytes, float* out, kvarn_stream_t stream);
+                         int max_tiles, int win_capacity, float* out, unsigned launch_flags,
+                         kvarn_stream_t stream);
+int kvarn_decode_attention(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
+                           const int64_t* tile_table, const int32_t* n_tiles,
+                           const float* win_k, const float* win_v, const int32_t* win_start,
+                           const int32_t* win_len, int win_capacity, int B, int Hq, int Hkv,
+                           int head_dim, int max_tiles, float softmax_scale,
+                           const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
+                           unsigned launch_flags, kvarn_stream_t stream);
 
 /*
  * Chunked-prefill attention (PR #434, commit 99c3773, llm_kvarn_prefill_attention:
@@ -325,16 +390,21 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
  * over the keys j of KV head h / G whose position is <= pos0 + i, where tile
  * k holds positions [128 k, 128 k + 128) and window token w (w < win_len)
  * sits at position 128 * n_tiles + w.
- * The two contractions run on tcgen05 tensor cores with fp16 operands and
- * fp32 accumulation. Two kernels: every 128-key block the chunk sees (packed
- * tiles dequantised, window rows rotated into the same space) is written once
- * per KV head into ws as fp16 operand images, then one attention kernel per
- * (KV head, 128 score rows) streams those images through shared memory; the
- * softmax, causal mask and final inverse rotation run on CUDA cores.
+ * The two contractions run on tcgen05 tensor cores with fp32 accumulation;
+ * each operand (rotated query, keys, probabilities, values) is carried as a
+ * pair of fp16 values whose sum holds about 22 bits, so the result meets the
+ * same 1e-4 relative bound as decode. Two kernels: every 128-key block the
+ * chunk sees (packed tiles dequantised, window rows rotated into the same
+ * space) is written once per KV head into ws as fp16 operand images, then one
+ * attention kernel per (KV head, 128 score rows) streams those images through
+ * shared memory; the softmax, causal mask and final inverse rotation run on
+ * CUDA cores.
  *   q_chunk    : fp32 [C][Hq][D], unrotated; out: fp32 [C][Hq][D].
+ *   tiles      : u8 base of the record pool, tiles_bytes long.
  *   tile_table : int64 [Hkv][table_stride] record byte offsets (multiples of
- *                16; another offset makes the keys of that tile NaN) of this
- *                sequence's tiles; table_stride >= n_tiles.
+ *                16, inside the pool; another offset makes the keys of that
+ *                tile NaN and sets KVARN_DEVERR_RECORD) of this sequence's
+ *                tiles; table_stride >= n_tiles.
  *   win_k/v    : fp32 [Hkv][win_capacity][D] ring of this sequence;
  *                win_start, win_len, n_tiles: host integers.
  *   ws         : device workspace of at least kvarn_prefill_workspace_bytes(
@@ -342,12 +412,13 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* 
  *                initialisation needed. Calls sharing ws must not overlap.
  * Requires pos0 + C <= 128 * n_tiles + win_len (the chunk's own keys are in
  * the cache), head_dim 64, 128 or 256 and Hq / Hkv <= 8. At head_dim 256
- * the attention streams keys in 32-key sub-blocks (the 128-row fp16 query
- * operands fill most of shared memory); the result has the same form.
+ * the attention streams keys in 64-key sub-blocks (the query operands fill
+ * much of the tensor memory); the result has the same form.
  */
 int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes);
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                            const int64_t* tile_table, int table_stride, int n_tiles,
+                            int64_t tiles_bytes, const int64_t* tile_table, int table_stride,
+                            int n_tiles,
                             const float* win_k, const float* win_v, int win_start, int win_len,
                             int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
                             const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
@@ -376,7 +447,8 @@ int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uin
  * than ws_blocks * Hkv images; otherwise as kvarn_prefill_attention.
  */
 int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                                   const int64_t* tile_table, int table_stride, int n_tiles,
+                                   int64_t tiles_bytes, const int64_t* tile_table,
+                                   int table_stride, int n_tiles,
                                    const float* win_k, const float* win_v, int win_start,
                                    int win_len, int win_capacity, int Hq, int Hkv, int head_dim,
                                    float softmax_scale, const kvarn_layout_t* layout, void* ws,
@@ -405,14 +477,14 @@ int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, co
  *    GPU (different streams, or different host threads) race on it.
  */
 #define KVARN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
-int kvarn_decode_attention_noalloc(const float* q, const uint8_t* tiles,
+int kvarn_decode_attention_noalloc(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
                                    const int64_t* tile_table, const int32_t* n_tiles,
                                    const float* win_k, const float* win_v,
                                    const int32_t* win_start, const int32_t* win_len,
                                    int win_capacity, int B, int Hq, int Hkv, int head_dim,
                                    int max_tiles, float softmax_scale,
                                    const kvarn_layout_t* layout, float* out,
-                                   kvarn_stream_t stream);
+                                   unsigned launch_flags, kvarn_stream_t stream);
 
 #ifdef __cplusplus
 }

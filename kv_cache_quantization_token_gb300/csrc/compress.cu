@@ -154,9 +154,9 @@ __device__ __forceinline__ bool usable(float var, float mean) {
 template <int D, int SB, int VB>
 __global__ void __launch_bounds__(CC<D>::NT, (D == 256) ? 1 : 2)
 compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw,
-                int64_t row_stride, const int64_t* __restrict__ src_row0,
-                uint8_t* __restrict__ tiles, const int64_t* __restrict__ dst_record,
-                int iters) {
+                int64_t row_stride, int64_t n_rows, const int64_t* __restrict__ src_row0,
+                uint8_t* __restrict__ tiles, int64_t tiles_bytes,
+                const int64_t* __restrict__ dst_record, int iters, unsigned* err) {
   using C = CC<D>;
   using R = Rec<D, SB, VB>;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -169,7 +169,13 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t unit = blockIdx.x >> 1;
   const bool is_v = blockIdx.x & 1;
-  const float* src = (is_v ? v_raw : k_raw) + src_row0[unit] * row_stride;
+  // a unit whose rows or record lie outside the buffers is skipped (and reported)
+  const int64_t row0 = src_row0[unit], dst = dst_record[unit];
+  if (row0 < 0 || row0 > n_rows - 128 || dst < 0 || (dst & 15) || dst > tiles_bytes - R::kBytes) {
+    if (tid == 0 && !is_v) report(err, KVARN_DEVERR_RECORD);
+    return;
+  }
+  const float* src = (is_v ? v_raw : k_raw) + row0 * row_stride;
 
   // ---------------- phase 1: coalesced loads + butterflies of bits 0,1,5.. --
   {
@@ -481,7 +487,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
   __syncthreads();
 
   // ---------------- copy the staged halves of the record out --------------
-  uint8_t* rec = tiles + dst_record[unit];
+  uint8_t* rec = tiles + dst;
   const int a0 = is_v ? R::kVCodes : R::kKCodes;
   const int a1 = is_v ? R::kKDelta : R::kVCodes;
   const int b0 = is_v ? R::kVDelta : R::kKDelta;
@@ -494,8 +500,9 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 
 template <int D, int SB, int VB>
 cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw, int64_t row_stride,
-                              const int64_t* src_row0, uint8_t* tiles, const int64_t* dst_record,
-                              int64_t n_units, cudaStream_t st) {
+                              int64_t n_rows, const int64_t* src_row0, uint8_t* tiles,
+                              int64_t tiles_bytes, const int64_t* dst_record, int64_t n_units,
+                              unsigned* err, cudaStream_t st) {
   using C = CC<D>;
   static bool configured[64] = {};  // the smem opt-in is set once per device
   int dev = 0;
@@ -509,18 +516,19 @@ cudaError_t launch_compress_d(int iters, const float* k_raw, const float* v_raw,
   }
   const int64_t blocks = 2 * n_units;
   compress_kernel<D, SB, VB><<<(unsigned)blocks, C::NT, C::SMEM, st>>>(
-      k_raw, v_raw, row_stride, src_row0, tiles, dst_record, iters);
+      k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, iters, err);
   return cudaGetLastError();
 }
 
 template <int SB, int VB>
 cudaError_t launch_compress_sb(int D, int iters, const float* k_raw, const float* v_raw,
-                               int64_t row_stride, const int64_t* src_row0, uint8_t* tiles,
-                               const int64_t* dst_record, int64_t n_units, cudaStream_t st) {
+                               int64_t row_stride, int64_t n_rows, const int64_t* src_row0,
+                               uint8_t* tiles, int64_t tiles_bytes, const int64_t* dst_record,
+                               int64_t n_units, unsigned* err, cudaStream_t st) {
   switch (D) {
-    case 64: return launch_compress_d<64, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 128: return launch_compress_d<128, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 256: return launch_compress_d<256, SB, VB>(iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 64: return launch_compress_d<64, SB, VB>(iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 128: return launch_compress_d<128, SB, VB>(iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 256: return launch_compress_d<256, SB, VB>(iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -528,15 +536,16 @@ cudaError_t launch_compress_sb(int D, int iters, const float* k_raw, const float
 }  // namespace
 
 cudaError_t launch_compress(int D, int iters, int scale_bytes, int v_bits, const float* k_raw,
-                            const float* v_raw, int64_t row_stride, const int64_t* src_row0,
-                            uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
+                            const float* v_raw, int64_t row_stride, int64_t n_rows,
+                            const int64_t* src_row0, uint8_t* tiles, int64_t tiles_bytes,
+                            const int64_t* dst_record, int64_t n_units, unsigned* err,
                             cudaStream_t st) {
   const int key = 10 * scale_bytes + v_bits;
   switch (key) {
-    case 42: return launch_compress_sb<4, 2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 22: return launch_compress_sb<2, 2>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 44: return launch_compress_sb<4, 4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
-    case 24: return launch_compress_sb<2, 4>(D, iters, k_raw, v_raw, row_stride, src_row0, tiles, dst_record, n_units, st);
+    case 42: return launch_compress_sb<4, 2>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 22: return launch_compress_sb<2, 2>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 44: return launch_compress_sb<4, 4>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 24: return launch_compress_sb<2, 4>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
     default: return cudaErrorInvalidValue;
   }
 }

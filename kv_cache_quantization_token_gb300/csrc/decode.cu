@@ -78,21 +78,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: gives up (returns false) instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+// Bounded wait for a copy: gives up after a fixed time (reporting
+// KVARN_DEVERR_WAIT) instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_timed(bar, parity, err, KVARN_DEVERR_WAIT);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -402,7 +391,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
                     const int32_t* __restrict__ win_start, const int32_t* __restrict__ win_len,
                     int cap, int Hq, int Hkv, int G, int max_tiles, int items, int tile_items,
                     int rounds_arg, float scale, float* __restrict__ ws_ml, float* __restrict__ ws_acc,
-                    int prefetch, const __grid_constant__ CUtensorMap tmap) {
+                    int prefetch, int64_t tiles_bytes, unsigned* err,
+                    const __grid_constant__ CUtensorMap tmap) {
   using C = DC<D, GP, NW_, WPT_, MR>;
   using R = Rec<D, kSB, kVB>;
   constexpr int NW = C::NW, NT = C::NT, GV = C::GV, NCB = C::NCB, NS = C::NS, TPS = C::TPS;
@@ -482,7 +472,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     __syncthreads();
     const int k = warp;
     const bool have = k < nslot;
-    bool ok = have && mbar_wait(&bar[k], 0);
+    bool ok = have && mbar_wait(&bar[k], 0, err);
     const float* Kw = reinterpret_cast<const float*>(rec + k * (2 * C::WCH * D * 4));
     const float* Vw = Kw + C::WCH * D;
     const int wn = min(C::WCH, wlen - (wj0 + C::WCH * k));
@@ -598,10 +588,13 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   // Copies a packed tile into a record slot (one TMA box of codes plus one bulk
   // copy of the scales, completing on the slot's barrier); okf[slot] tells
   // the group whether a copy was issued (record offsets must be multiples of
-  // 128 bytes; others poison the result).
+  // 128 bytes and the record must lie inside the pool; others poison the
+  // result and are reported).
   auto issue = [&](int li, int slot) {
     const int64_t off = trow[li];
-    const bool aligned = (off & 127) == 0 && off >= 0 && (off >> 7) < 0x7FFFFFFFLL;
+    const bool aligned = (off & 127) == 0 && off >= 0 && off <= tiles_bytes - C::RB &&
+                         (off >> 7) < 0x7FFFFFFFLL;
+    if (!aligned) report(err, KVARN_DEVERR_RECORD);
     okf[slot] = aligned;
     if (aligned) {
       mbar_expect_tx(&bar[slot], C::RB);
@@ -657,7 +650,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     const uint32_t par = dbuf ? (uint32_t)((k >> 1) & 1) : 0u;
     const unsigned char* Rk = rec + slot * C::SLOT;
     const uint32_t rk = smem_u32(Rk);
-    const bool landed = okf[slot] && mbar_wait(&bar[slot], par);
+    const bool landed = okf[slot] && mbar_wait(&bar[slot], par, err);
     if (!landed) bad = 1;  // computed on, result poisoned
     if (issuer && landed) {
       if (k & 1) pend1 = 0; else pend0 = 0;
@@ -999,8 +992,8 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   bad = __syncthreads_or(bad);
   if (bad && issuer)  // let every copy that was issued land before the CTA exits (bounded)
   {
-    if (pend0) mbar_wait(&bar[pair], (uint32_t)(pend0 - 1));
-    if (pend1) mbar_wait(&bar[pair + TPS], (uint32_t)(pend1 - 1));
+    if (pend0) mbar_wait(&bar[pair], (uint32_t)(pend0 - 1), err);
+    if (pend1) mbar_wait(&bar[pair + TPS], (uint32_t)(pend1 - 1), err);
   }
 
   // ---------------- merge the warps' (m, l, acc) ---------------------------
@@ -1177,13 +1170,15 @@ EncodeTiledFn encode_tiled() {
 // Tensor map over the record pool seen as rows of 128 bytes: a box of
 // code_lines rows starting at row offset/128 is the K and V codes of the
 // record at that offset, copied with 128-byte swizzling. The row count is the
-// largest a coordinate can address; only rows of real records are read.
-cudaError_t code_map(CUtensorMap* m, const void* tiles, int code_lines) {
+// pool's, so no box reaches past it (rows beyond are zero-filled; the kernel
+// also refuses offsets whose record would not fit).
+cudaError_t code_map(CUtensorMap* m, const void* tiles, int64_t tiles_bytes, int code_lines) {
   memset(m, 0, sizeof(*m));
-  if (!tiles) return cudaSuccess;  // no tile items: the map is never used
+  if (!tiles || tiles_bytes < 128) return cudaSuccess;  // no record can be read: the map is never used
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {128, 0x7FFFFFFFull};
+  const int64_t rows = tiles_bytes / 128 < 0x7FFFFFFF ? tiles_bytes / 128 : 0x7FFFFFFF;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {128};
   const cuuint32_t box[2] = {128, (cuuint32_t)code_lines};
   const cuuint32_t estr[2] = {1, 1};
@@ -1209,16 +1204,16 @@ cudaError_t launch_split_t(const DecodePlan& p, const DecodeArgs& a, float* ws_m
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   CUtensorMap tmap;
-  e = code_map(&tmap, p.tile_items > 0 ? a.tiles : nullptr, C::CODE_LINES);
+  e = code_map(&tmap, p.tile_items > 0 ? a.tiles : nullptr, a.tiles_bytes, C::CODE_LINES);
   if (e != cudaSuccess) return e;
-  const unsigned fl = launch_flags();
+  const unsigned fl = a.flags;
   const int prefetch = (fl & KVARN_LAUNCH_PDL) && (fl & KVARN_LAUNCH_PREFETCH);
   const int slots = MR && p.rounds > 1 ? 2 * C::TPS : C::TPS;
-  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::smem_bytes(slots) + 1024, st);
+  LaunchCfg L(dim3(p.items, a.Hkv, a.B), dim3(C::NTHR), C::smem_bytes(slots) + 1024, st, fl);
   return cudaLaunchKernelEx(&L.cfg, decode_split_kernel<D, GP, NW, WPT, MR>, a.q, a.tiles, a.tile_table,
                             a.n_tiles, a.win_k, a.win_v, a.win_start, a.win_len, a.win_capacity,
                             a.Hq, a.Hkv, a.Hq / a.Hkv, a.max_tiles, p.items, p.tile_items, p.rounds,
-                            a.scale, ws_ml, ws_acc, prefetch, tmap);
+                            a.scale, ws_ml, ws_acc, prefetch, a.tiles_bytes, a.err, tmap);
 }
 
 template <int D, int GP>
@@ -1336,10 +1331,10 @@ cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* 
 }
 
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
-                                  float* out, cudaStream_t st) {
+                                  float* out, unsigned flags, cudaStream_t st) {
   float *ml, *acc;
   ws_split(p, B, Hq, const_cast<void*>(ws), &ml, &acc);
-  LaunchCfg L(dim3(Hq, B), dim3(512), 0, st);
+  LaunchCfg L(dim3(Hq, B), dim3(512), 0, st, flags);
   const float* cml = ml;
   const float* cacc = acc;
   switch (D) {

@@ -43,20 +43,27 @@ void* scratch_on_current_device() {
 }  // namespace
 
 extern "C" int kvarn_decode_attention_noalloc(const float* q, const uint8_t* tiles,
-                                              const int64_t* tile_table, const int32_t* n_tiles,
-                                              const float* win_k, const float* win_v,
-                                              const int32_t* win_start, const int32_t* win_len,
-                                              int win_capacity, int B, int Hq, int Hkv,
-                                              int head_dim, int max_tiles, float softmax_scale,
-                                              const kvarn_layout_t* layout, float* out,
+                                              int64_t tiles_bytes, const int64_t* tile_table,
+                                              const int32_t* n_tiles, const float* win_k,
+                                              const float* win_v, const int32_t* win_start,
+                                              const int32_t* win_len, int win_capacity, int B,
+                                              int Hq, int Hkv, int head_dim, int max_tiles,
+                                              float softmax_scale, const kvarn_layout_t* layout,
+                                              float* out, unsigned launch_flags,
                                               kvarn_stream_t stream) {
+  // argument errors are reported before the scratch array is looked up
+  if ((launch_flags & ~(KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH)) ||
+      ((launch_flags & KVARN_LAUNCH_PREFETCH) && !(launch_flags & KVARN_LAUNCH_PDL)) ||
+      tiles_bytes < 0)
+    return KVARN_ERR_BAD_ARG;
   size_t need = 0;
   int rc = kvarn_decode_workspace_bytes(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &need);
   if (rc != KVARN_OK) return rc;
   if (need > kScratchBytes) return KVARN_ERR_WORKSPACE;  // the request is larger than the array
   void* ws = scratch_on_current_device();
   if (!ws) return KVARN_ERR_CUDA;
-  return kvarn_decode_attention(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
-                                win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
-                                layout, ws, kScratchBytes, out, stream);
+  return kvarn_decode_attention(q, tiles, tiles_bytes, tile_table, n_tiles, win_k, win_v,
+                                win_start, win_len, win_capacity, B, Hq, Hkv, head_dim, max_tiles,
+                                softmax_scale, layout, ws, kScratchBytes, out, launch_flags,
+                                stream);
 }

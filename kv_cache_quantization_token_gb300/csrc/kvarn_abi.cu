@@ -6,7 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "kvarn_common.cuh"
 
@@ -60,24 +60,56 @@ bool layout_ok(const kvarn_layout_t* L) {
   return memcmp(&ref, L, sizeof(ref)) == 0;
 }
 
-std::atomic<unsigned> g_launch_flags{0};
+bool flags_ok(unsigned flags) {
+  if (flags & ~(KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH)) return false;
+  return !((flags & KVARN_LAUNCH_PREFETCH) && !(flags & KVARN_LAUNCH_PDL));
+}
+
+// The device error word: KVARN_DEVERR_* bits that kernels OR in when they give
+// up on something. One word per device (each device that loads the library
+// has its own copy of this file-scope variable); kernels get its address as an
+// argument.
+__device__ unsigned g_device_error;
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
 
 }  // namespace
 
 namespace kvarn {
-unsigned launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+unsigned* device_error_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
 }  // namespace kvarn
 
 extern "C" {
 
-int kvarn_set_launch_flags(unsigned flags) {
-  if (flags & ~(KVARN_LAUNCH_PDL | KVARN_LAUNCH_PREFETCH)) return KVARN_ERR_BAD_ARG;
-  if ((flags & KVARN_LAUNCH_PREFETCH) && !(flags & KVARN_LAUNCH_PDL)) return KVARN_ERR_BAD_ARG;
-  g_launch_flags.store(flags, std::memory_order_relaxed);
+int kvarn_get_device_error(unsigned* bits, int clear) {
+  if (!bits) return KVARN_ERR_NULL;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return KVARN_ERR_CUDA;
+  *bits = v;
+  if (clear && v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return KVARN_ERR_CUDA;
+  }
   return KVARN_OK;
 }
 
-unsigned kvarn_get_launch_flags(void) { return g_launch_flags.load(std::memory_order_relaxed); }
+int kvarn_selftest_bounded_wait(unsigned timeout_us, kvarn_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return KVARN_ERR_BAD_ARG;
+  unsigned* err = kvarn::device_error_word();
+  if (!err) return KVARN_ERR_CUDA;
+  return from_cuda(kvarn::launch_selftest_wait((uint64_t)timeout_us * 1000, err, (cudaStream_t)stream));
+}
 
 int kvarn_layout(int head_dim, int sinkhorn_iters, kvarn_layout_t* out) {
   return kvarn_layout_ex(head_dim, sinkhorn_iters, 32, KVARN_V_BITS, out);
@@ -104,7 +136,7 @@ const char* kvarn_status_string(int status) {
     case KVARN_ERR_UNSUPPORTED: return "unsupported head_dim, GQA group or iteration count";
     case KVARN_ERR_BAD_ARG: return "a size or count is negative or inconsistent";
     case KVARN_ERR_WORKSPACE: return "workspace smaller than the _workspace_bytes query";
-    case KVARN_ERR_CUDA: return "the CUDA runtime rejected a launch";
+    case KVARN_ERR_CUDA: return "the CUDA runtime rejected a launch or a copy";
     default: return "unknown kvarn status";
   }
 }
@@ -126,27 +158,30 @@ int kvarn_rotate_query(const float* q, float* q_rot, int64_t n_rows, int head_di
 
 int kvarn_compress_tile(const float* k_raw, const float* v_raw, int64_t row_stride,
                         int64_t n_rows, const int64_t* src_row0, uint8_t* tiles,
-                        const int64_t* dst_record, int64_t n_units, const kvarn_layout_t* layout,
-                        kvarn_stream_t stream) {
+                        int64_t tiles_bytes, const int64_t* dst_record, int64_t n_units,
+                        const kvarn_layout_t* layout, kvarn_stream_t stream) {
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout)) return KVARN_ERR_UNSUPPORTED;
   const int D = layout->head_dim;
-  if (n_units < 0 || n_units > 0x3fffffff || n_rows < 0) return KVARN_ERR_BAD_ARG;
+  if (n_units < 0 || n_units > 0x3fffffff || n_rows < 0 || tiles_bytes < 0) return KVARN_ERR_BAD_ARG;
   if (n_units == 0) return KVARN_OK;
   if (!k_raw || !v_raw || !src_row0 || !tiles || !dst_record) return KVARN_ERR_NULL;
-  if (row_stride < D || n_rows < KVARN_TILE_TOKENS) return KVARN_ERR_BAD_ARG;
+  if (row_stride < D || n_rows < KVARN_TILE_TOKENS || tiles_bytes < layout->record_bytes)
+    return KVARN_ERR_BAD_ARG;
   if ((row_stride & 3) || !aligned16(k_raw) || !aligned16(v_raw) || !aligned16(tiles))
     return KVARN_ERR_ALIGN;
   return from_cuda(kvarn::launch_compress(D, layout->sinkhorn_iters, scale_bytes_of(layout),
-                                          layout->v_bits, k_raw, v_raw, row_stride, src_row0,
-                                          tiles, dst_record, n_units, (cudaStream_t)stream));
+                                          layout->v_bits, k_raw, v_raw, row_stride, n_rows,
+                                          src_row0, tiles, tiles_bytes, dst_record, n_units,
+                                          kvarn::device_error_word(), (cudaStream_t)stream));
 }
 
 int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
                         float* win_v, int win_capacity, const int32_t* win_start,
                         const int32_t* win_len, int n_seq, int n_kv_heads, int head_dim,
-                        kvarn_stream_t stream) {
+                        unsigned launch_flags, kvarn_stream_t stream) {
   if (!supported_dim(head_dim)) return KVARN_ERR_UNSUPPORTED;
+  if (!flags_ok(launch_flags)) return KVARN_ERR_BAD_ARG;
   if (n_new < 0 || n_seq < 0 || n_kv_heads <= 0 || win_capacity <= 0) return KVARN_ERR_BAD_ARG;
   if (n_new > win_capacity) return KVARN_ERR_BAD_ARG;
   if (n_new == 0 || n_seq == 0) return KVARN_OK;
@@ -155,6 +190,7 @@ int kvarn_append_window(const float* k_new, const float* v_new, int64_t n_new, f
     return KVARN_ERR_ALIGN;
   return from_cuda(kvarn::launch_append(k_new, v_new, n_new, win_k, win_v, win_capacity,
                                         win_start, win_len, n_seq, n_kv_heads, head_dim,
+                                        launch_flags, kvarn::device_error_word(),
                                         (cudaStream_t)stream));
 }
 
@@ -178,14 +214,16 @@ int kvarn_decode_workspace_bytes(int B, int Hq, int Hkv, int head_dim, int max_t
   return KVARN_OK;
 }
 
-static int decode_prepare(const float* q, const uint8_t* tiles, const int64_t* tile_table,
-                          const int32_t* n_tiles, const float* win_k, const float* win_v,
-                          const int32_t* win_start, const int32_t* win_len, int win_capacity,
-                          int B, int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
-                          const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
-                          kvarn::DecodePlan* p, kvarn::DecodeArgs* a) {
+static int decode_prepare(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
+                          const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
+                          const float* win_v, const int32_t* win_start, const int32_t* win_len,
+                          int win_capacity, int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                          float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                          size_t ws_bytes, unsigned launch_flags, kvarn::DecodePlan* p,
+                          kvarn::DecodeArgs* a) {
   int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
   if (rc != KVARN_OK) return rc;
+  if (!flags_ok(launch_flags) || tiles_bytes < 0) return KVARN_ERR_BAD_ARG;
   if (!layout) return KVARN_ERR_NULL;
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
   kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, p);
@@ -202,55 +240,61 @@ static int decode_prepare(const float* q, const uint8_t* tiles, const int64_t* t
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
   *a = kvarn::DecodeArgs{q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
                          win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
-                         scale_bytes_of(layout), layout->v_bits};
+                         scale_bytes_of(layout), layout->v_bits, tiles_bytes, launch_flags,
+                         kvarn::device_error_word()};
   return KVARN_OK;
 }
 
-int kvarn_decode_split(const float* q, const uint8_t* tiles, const int64_t* tile_table,
-                       const int32_t* n_tiles, const float* win_k, const float* win_v,
-                       const int32_t* win_start, const int32_t* win_len, int win_capacity, int B,
-                       int Hq, int Hkv, int head_dim, int max_tiles, float softmax_scale,
-                       const kvarn_layout_t* layout, void* ws, size_t ws_bytes,
-                       kvarn_stream_t stream) {
+int kvarn_decode_split(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
+                       const int64_t* tile_table, const int32_t* n_tiles, const float* win_k,
+                       const float* win_v, const int32_t* win_start, const int32_t* win_len,
+                       int win_capacity, int B, int Hq, int Hkv, int head_dim, int max_tiles,
+                       float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                       size_t ws_bytes, unsigned launch_flags, kvarn_stream_t stream) {
   kvarn::DecodePlan p;
   kvarn::DecodeArgs a;
-  const int rc = decode_prepare(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
-                                win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
-                                layout, ws, ws_bytes, &p, &a);
+  const int rc = decode_prepare(q, tiles, tiles_bytes, tile_table, n_tiles, win_k, win_v,
+                                win_start, win_len, win_capacity, B, Hq, Hkv, head_dim, max_tiles,
+                                softmax_scale, layout, ws, ws_bytes, launch_flags, &p, &a);
   if (rc != KVARN_OK || B == 0) return rc;
   return from_cuda(kvarn::launch_decode_split(p, a, ws, (cudaStream_t)stream));
 }
 
 int kvarn_decode_combine(const void* ws, size_t ws_bytes, int B, int Hq, int Hkv, int head_dim,
-                         int max_tiles, int win_capacity, float* out, kvarn_stream_t stream) {
+                         int max_tiles, int win_capacity, float* out, unsigned launch_flags,
+                         kvarn_stream_t stream) {
   const int rc = decode_check(B, Hq, Hkv, head_dim, max_tiles, win_capacity);
   if (rc != KVARN_OK) return rc;
+  if (!flags_ok(launch_flags)) return KVARN_ERR_BAD_ARG;
   if (B == 0) return KVARN_OK;
   kvarn::DecodePlan p;
   kvarn::decode_plan(B, Hq, Hkv, head_dim, max_tiles, win_capacity, &p);
   if (!out || (p.ws_bytes > 0 && !ws)) return KVARN_ERR_NULL;
   if (ws_bytes < p.ws_bytes) return KVARN_ERR_WORKSPACE;
   if (!aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255)) return KVARN_ERR_ALIGN;
-  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
+  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, launch_flags,
+                                                (cudaStream_t)stream));
 }
 
-int kvarn_decode_attention(const float* q, const uint8_t* tiles, const int64_t* tile_table,
-                           const int32_t* n_tiles, const float* win_k, const float* win_v,
-                           const int32_t* win_start, const int32_t* win_len, int win_capacity,
-                           int B, int Hq, int Hkv, int head_dim, int max_tiles,
-                           float softmax_scale, const kvarn_layout_t* layout, void* ws,
-                           size_t ws_bytes, float* out, kvarn_stream_t stream) {
+int kvarn_decode_attention(const float* q, const uint8_t* tiles, int64_t tiles_bytes,
+                           const int64_t* tile_table, const int32_t* n_tiles,
+                           const float* win_k, const float* win_v, const int32_t* win_start,
+                           const int32_t* win_len, int win_capacity, int B, int Hq, int Hkv,
+                           int head_dim, int max_tiles, float softmax_scale,
+                           const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
+                           unsigned launch_flags, kvarn_stream_t stream) {
   kvarn::DecodePlan p;
   kvarn::DecodeArgs a;
-  int rc = decode_prepare(q, tiles, tile_table, n_tiles, win_k, win_v, win_start, win_len,
-                          win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale, layout, ws,
-                          ws_bytes, &p, &a);
+  int rc = decode_prepare(q, tiles, tiles_bytes, tile_table, n_tiles, win_k, win_v, win_start,
+                          win_len, win_capacity, B, Hq, Hkv, head_dim, max_tiles, softmax_scale,
+                          layout, ws, ws_bytes, launch_flags, &p, &a);
   if (rc != KVARN_OK || B == 0) return rc;
   if (!out) return KVARN_ERR_NULL;
   if (!aligned16(out)) return KVARN_ERR_ALIGN;
   rc = from_cuda(kvarn::launch_decode_split(p, a, ws, (cudaStream_t)stream));
   if (rc != KVARN_OK) return rc;
-  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, (cudaStream_t)stream));
+  return from_cuda(kvarn::launch_decode_combine(p, B, Hq, head_dim, ws, out, launch_flags,
+                                                (cudaStream_t)stream));
 }
 
 int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_dim, size_t* bytes) {
@@ -263,7 +307,8 @@ int kvarn_prefill_workspace_bytes(int n_tiles, int win_len, int Hkv, int head_di
 }
 
 static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                          const int64_t* tile_table, int table_stride, int n_tiles,
+                          int64_t tiles_bytes, const int64_t* tile_table, int table_stride,
+                          int n_tiles,
                           const float* win_k, const float* win_v, int win_start, int win_len,
                           int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
                           const kvarn_layout_t* layout, void* ws, size_t ws_bytes, int ws_blocks,
@@ -273,7 +318,7 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
   if (!layout_ok(layout) || layout->head_dim != head_dim) return KVARN_ERR_UNSUPPORTED;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || Hkv > 65535) return KVARN_ERR_BAD_ARG;
   if (Hq / Hkv > 8) return KVARN_ERR_UNSUPPORTED;
-  if (C < 0 || pos0 < 0 || n_tiles < 0 || win_len < 0 || win_capacity < 0 ||
+  if (C < 0 || pos0 < 0 || n_tiles < 0 || win_len < 0 || win_capacity < 0 || tiles_bytes < 0 ||
       table_stride < n_tiles || win_len > win_capacity)
     return KVARN_ERR_BAD_ARG;
   if (pos0 + C > (int64_t)KVARN_TILE_TOKENS * n_tiles + win_len) return KVARN_ERR_BAD_ARG;
@@ -294,45 +339,51 @@ static int prefill_common(const float* q_chunk, int C, int64_t pos0, const uint8
       (reinterpret_cast<uintptr_t>(ws) & 255))
     return KVARN_ERR_ALIGN;
   if (!(softmax_scale == softmax_scale)) return KVARN_ERR_BAD_ARG;
-  return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tile_table, table_stride,
-                                         n_tiles, win_k, win_v, win_start, win_len, win_capacity,
-                                         Hq, Hkv, head_dim, softmax_scale, scale_bytes_of(layout),
-                                         layout->v_bits, ws, stride, cached_tiles, out,
+  return from_cuda(kvarn::launch_prefill(q_chunk, C, pos0, tiles, tiles_bytes, tile_table,
+                                         table_stride, n_tiles, win_k, win_v, win_start, win_len,
+                                         win_capacity, Hq, Hkv, head_dim, softmax_scale,
+                                         scale_bytes_of(layout), layout->v_bits, ws, stride,
+                                         cached_tiles, out, kvarn::device_error_word(),
                                          (cudaStream_t)stream));
 }
 
 int kvarn_prefill_attention(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                            const int64_t* tile_table, int table_stride, int n_tiles,
-                            const float* win_k, const float* win_v, int win_start, int win_len,
-                            int win_capacity, int Hq, int Hkv, int head_dim, float softmax_scale,
-                            const kvarn_layout_t* layout, void* ws, size_t ws_bytes, float* out,
-                            kvarn_stream_t stream) {
-  return prefill_common(q_chunk, C, pos0, tiles, tile_table, table_stride, n_tiles, win_k, win_v,
+                            int64_t tiles_bytes, const int64_t* tile_table, int table_stride,
+                            int n_tiles, const float* win_k, const float* win_v, int win_start,
+                            int win_len, int win_capacity, int Hq, int Hkv, int head_dim,
+                            float softmax_scale, const kvarn_layout_t* layout, void* ws,
+                            size_t ws_bytes, float* out, kvarn_stream_t stream) {
+  return prefill_common(q_chunk, C, pos0, tiles, tiles_bytes, tile_table, table_stride, n_tiles,
+                        win_k, win_v,
                         win_start, win_len, win_capacity, Hq, Hkv, head_dim, softmax_scale, layout,
                         ws, ws_bytes, 0, 0, out, stream);
 }
 
 int kvarn_prefill_attention_cached(const float* q_chunk, int C, int64_t pos0, const uint8_t* tiles,
-                                   const int64_t* tile_table, int table_stride, int n_tiles,
-                                   const float* win_k, const float* win_v, int win_start,
-                                   int win_len, int win_capacity, int Hq, int Hkv, int head_dim,
+                                   int64_t tiles_bytes, const int64_t* tile_table,
+                                   int table_stride, int n_tiles, const float* win_k,
+                                   const float* win_v, int win_start, int win_len,
+                                   int win_capacity, int Hq, int Hkv, int head_dim,
                                    float softmax_scale, const kvarn_layout_t* layout, void* ws,
                                    size_t ws_bytes, int ws_blocks, int cached_tiles, float* out,
                                    kvarn_stream_t stream) {
   if (ws_blocks <= 0) return KVARN_ERR_BAD_ARG;
-  return prefill_common(q_chunk, C, pos0, tiles, tile_table, table_stride, n_tiles, win_k, win_v,
+  return prefill_common(q_chunk, C, pos0, tiles, tiles_bytes, tile_table, table_stride, n_tiles,
+                        win_k, win_v,
                         win_start, win_len, win_capacity, Hq, Hkv, head_dim, softmax_scale, layout,
                         ws, ws_bytes, ws_blocks, cached_tiles, out, stream);
 }
 
 int kvarn_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles, int n_seq,
-                         int d_len, int promote, int win_capacity, kvarn_stream_t stream) {
-  if (n_seq < 0 || promote < 0 || win_capacity <= 0 || (win_capacity % KVARN_TILE_TOKENS))
+                         int d_len, int promote, int win_capacity, unsigned launch_flags,
+                         kvarn_stream_t stream) {
+  if (n_seq < 0 || promote < 0 || win_capacity <= 0 || (win_capacity % KVARN_TILE_TOKENS) ||
+      !flags_ok(launch_flags))
     return KVARN_ERR_BAD_ARG;
   if (n_seq == 0 || (d_len == 0 && promote == 0)) return KVARN_OK;
   if (!win_start || !win_len || (promote > 0 && !n_tiles)) return KVARN_ERR_NULL;
   return from_cuda(kvarn::launch_window_advance(win_start, win_len, n_tiles, n_seq, d_len, promote,
-                                                win_capacity, (cudaStream_t)stream));
+                                                win_capacity, launch_flags, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -96,17 +96,20 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Current kvarn_set_launch_flags() value.
-unsigned launch_flags();
-
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
-// cudaLaunchKernelEx configuration honouring KVARN_LAUNCH_PDL.
+// Device address of the library's error word on the current device (looked
+// up once per device), or NULL if it cannot be found; kernels given NULL
+// report nothing.
+unsigned* device_error_word();
+
+// cudaLaunchKernelEx configuration honouring the KVARN_LAUNCH_PDL bit of the
+// call's launch flags.
 struct LaunchCfg {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st, unsigned flags) {
     cfg = cudaLaunchConfig_t{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -115,11 +118,60 @@ struct LaunchCfg {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (launch_flags() & KVARN_LAUNCH_PDL) ? 1 : 0;
+    cfg.numAttrs = (flags & KVARN_LAUNCH_PDL) ? 1 : 0;
   }
   LaunchCfg(const LaunchCfg&) = delete;
   LaunchCfg& operator=(const LaunchCfg&) = delete;
 };
+
+// ---------------------------------------------------------------------------
+// Device-side failure reporting. A kernel that gives up (a wait that ran out
+// of time, an input it refuses to touch) sets its KVARN_DEVERR_* bit in the
+// library's error word and poisons the affected output with NaN; the word is
+// read (and cleared) on the host with kvarn_get_device_error().
+__device__ __forceinline__ void report(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Every wait on an mbarrier gives up after this long (a copy or a product of
+// the same kernel completes within microseconds).
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+
+__device__ __forceinline__ bool mbar_test_parity(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"((uint32_t)__cvta_generic_to_shared(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits until the phase of `bar` with the given parity has completed, for at
+// most limit_ns (and a fixed number of polls, should the timer not move);
+// returns false, after setting `bit` in *err, when it gives up. If `stop` is
+// given, the wait also gives up (without reporting) once *stop is non-zero,
+// and a wait that runs out sets *stop.
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity, unsigned* err,
+                                                unsigned bit, volatile int* stop = nullptr,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test_parity(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (int it = 0; it < (1 << 20); ++it) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test_parity(bar, parity)) return true;
+    if (stop && *stop) return false;
+    if (global_ns() - t0 > limit_ns) break;
+  }
+  if (stop) *stop = 1;
+  report(err, bit);
+  return false;
+}
 
 }  // namespace kvarn
 
@@ -127,14 +179,16 @@ struct LaunchCfg {
 // and calls them. They return a cudaError_t from cudaGetLastError().
 namespace kvarn {
 cudaError_t launch_compress(int D, int iters, int scale_bytes, int v_bits, const float* k_raw,
-                            const float* v_raw, int64_t row_stride, const int64_t* src_row0,
-                            uint8_t* tiles, const int64_t* dst_record, int64_t n_units,
+                            const float* v_raw, int64_t row_stride, int64_t n_rows,
+                            const int64_t* src_row0, uint8_t* tiles, int64_t tiles_bytes,
+                            const int64_t* dst_record, int64_t n_units, unsigned* err,
                             cudaStream_t st);
 cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, cudaStream_t st);
 cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
                           float* win_v, int win_capacity, const int32_t* win_start,
                           const int32_t* win_len, int n_seq, int n_kv_heads, int D,
-                          cudaStream_t st);
+                          unsigned flags, unsigned* err, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, unsigned* err, cudaStream_t st);
 
 struct DecodePlan {
   int tiles_per_round;  // packed tiles a split CTA works on at once (one per warp group)
@@ -160,6 +214,9 @@ struct DecodeArgs {
   float scale;
   int scale_bytes;  // record scale fields: 4 (fp32) or 2 (binary16)
   int v_bits;       // value code width: 2 or 4
+  int64_t tiles_bytes;  // size of the record pool
+  unsigned flags;       // KVARN_LAUNCH_* bits of the call
+  unsigned* err;        // device error word (may be NULL)
 };
 int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, DecodePlan* p);
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
@@ -176,18 +233,19 @@ cudaError_t launch_decode_split_sb4_v4(const DecodePlan& p, const DecodeArgs& a,
 cudaError_t launch_decode_split_sb2_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
-                                  float* out, cudaStream_t st);
+                                  float* out, unsigned flags, cudaStream_t st);
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
-                           const int64_t* tile_table, int table_stride, int n_tiles,
+                           int64_t tiles_bytes, const int64_t* tile_table, int table_stride,
+                           int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
                            int scale_bytes, int v_bits, void* ws, int ws_blocks, int cached_tiles,
-                           float* out, cudaStream_t st);
+                           float* out, unsigned* err, cudaStream_t st);
 // 128-key blocks a prefill chunk sees (tiles, and tiles + window blocks), and
 // the workspace bytes of one (block, KV head) image.
 void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, int* n_blk);
 size_t prefill_block_bytes(int D);
 cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
                                   int n_seq, int d_len, int promote, int win_capacity,
-                                  cudaStream_t st);
+                                  unsigned flags, cudaStream_t st);
 }  // namespace kvarn

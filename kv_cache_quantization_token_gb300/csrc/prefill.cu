@@ -106,30 +106,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void mbar_init1(uint64_t* bar) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
+// Bounded waits (a fixed time limit; running out reports KVARN_DEVERR_WAIT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_timed(bar, parity, err, KVARN_DEVERR_WAIT);
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i)
-    if (mbar_poll(bar, parity)) return true;
-  return false;
-}
-// Bounded wait that also gives up once another thread of the CTA has raised
-// `fail`; a wait that runs out raises it.
-__device__ __forceinline__ bool mbar_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail) {
-  for (int i = 0; i < (1 << 22); ++i) {
-    if (mbar_poll(bar, parity)) return true;
-    if ((i & 63) == 63 && *fail) return false;
-  }
-  *fail = 1;
-  return false;
+// The same wait, which also gives up once another thread of the CTA has
+// raised `fail`; a wait that runs out raises it.
+__device__ __forceinline__ bool mbar_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail,
+                                               unsigned* err) {
+  return mbar_wait_timed(bar, parity, err, KVARN_DEVERR_WAIT, fail);
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
@@ -330,6 +315,8 @@ struct PrefillArgs {
   int ws_stride;              // block images per KV head in ws (>= n_blk)
   int first_blk;              // first block whose image this call builds (earlier tiles' are kept)
   float qscale;               // softmax_scale * log2(e)
+  int64_t tiles_bytes;        // size of the record pool
+  unsigned* err;              // device error word (may be NULL)
 };
 
 // ---------------------------------------------------------------------------
@@ -352,17 +339,18 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
   bool poison = false;
   if (is_tile) {
     const int64_t off = a.tile_table[(int64_t)kvh * a.table_stride + j];
-    const bool aligned = (off & 15) == 0 && off >= 0;
+    const bool aligned = (off & 15) == 0 && off >= 0 && off <= a.tiles_bytes - R::kBytes;
     if (tid == 0) {
       mbar_init1(bar);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      if (!aligned) report(a.err, KVARN_DEVERR_RECORD);
     }
     __syncthreads();
     if (aligned && tid == 0) bulk_load(sm, a.tiles + off, R::kBytes, bar);
-    poison = !aligned || !mbar_wait_bounded(bar, 0);
+    poison = !aligned || !mbar_wait_bounded(bar, 0, a.err);
     poison = __syncthreads_or(poison) != 0;
     // an unusable record: NaN keys make every score of this block NaN
-    if (poison && aligned && tid == 0) mbar_wait_bounded(bar, 0);  // let the copy land (bounded)
+    if (poison && aligned && tid == 0) mbar_wait_bounded(bar, 0, nullptr);  // let the copy land (bounded)
   }
   auto fill_nan = [&](unsigned char* dst, int bytes) {
     for (int o = tid * 16; o < bytes; o += 16 * P::NTHR)
@@ -661,18 +649,18 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       // completion order of the tensor pipe: S(j) before PV(j)
       for (int j = 0; j < n_blk; ++j) {
         if (j + 2 < n_blk) {
-          if (!mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
+          if (!mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
           load_k(j + 2);
         }
         if (j + 1 < n_blk) {
-          if (!mbar_wait_flag(bar_o, (uint32_t)j & 1u, fail)) break;
+          if (!mbar_wait_flag(bar_o, (uint32_t)j & 1u, fail, a.err)) break;
           load_v(j + 1);
         }
       }
       // every copy issued has landed before the CTA can retire
       for (int b = 0; b < 2; ++b)
-        if (nk[b] > 0) mbar_wait_bounded(bar_k + b, (uint32_t)(nk[b] - 1) & 1u);
-      if (nv > 0) mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
+        if (nk[b] > 0) mbar_wait_bounded(bar_k + b, (uint32_t)(nk[b] - 1) & 1u, a.err);
+      if (nv > 0) mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u, a.err);
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -682,7 +670,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       uint32_t last_par = 0;
       auto issue_s = [&](int j) -> bool {
         const int b = j & 1;
-        if (!mbar_wait_flag(bar_k + b, (uint32_t)(j >> 1) & 1u, fail)) return false;
+        if (!mbar_wait_flag(bar_k + b, (uint32_t)(j >> 1) & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_s = tmem + P::T_S + 128 * b;
         const uint32_t kh = su32(sK + b * 2 * P::OPB), kl = kh + P::OPB;
@@ -703,8 +691,8 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
         // S(j+1) goes in ahead of PV(j): its TMEM buffer held P(j-1), which
         // PV(j-1), issued earlier, reads first
         if (j + 1 < n_blk && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
-        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
+        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail, a.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 128 * (j & 1);
         const uint32_t vh = su32(sV), vl = vh + P::OPB;
@@ -720,7 +708,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
         last = bar_o; last_par = (uint32_t)j & 1u;
       }
       // the tensor pipe completes in order: the last commit covers everything
-      if (last != nullptr && !mbar_wait_bounded(last, last_par)) *fail = 1;
+      if (last != nullptr && !mbar_wait_bounded(last, last_par, a.err)) *fail = 1;
     }
     __syncwarp();
   } else {
@@ -730,7 +718,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       const int64_t kpos0 = is_tile ? 128LL * j : win_pos0 + 128LL * (j - n_tile_blk);
       const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * (j - n_tile_blk));
       const bool full_vis = kpos0 + 127 <= pmin && nkeys == 128;  // uniform over the CTA
-      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
+      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err);
       bad = __any_sync(0xffffffffu, bad || *fail != 0);  // the warp (and its pair) leave together
       const uint32_t t_s = tmem + P::T_S + 128 * (j & 1) + lb + 64 * half;
       float sv[64];
@@ -780,7 +768,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
       tmem_st32_nowait(t_s + 32, lw);
       // O belongs to PV(j-1) until it completes
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
+        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail, a.err)) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
           for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -1033,19 +1021,19 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       load_v(0);
       // completion order of the tensor pipe: S(j-1) hi part, S(j-1), PV(j-1)
       for (int j = 1; j < n_sub; ++j) {
-        if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail, a.err)) break;
         load_k(sKh, 0, j, bar_kh);
         ++nkh;
-        if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail, a.err)) break;
         load_k(sKl, 1, j, bar_kl);
         ++nkl;
-        if (!mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail, a.err)) break;
         load_v(j);
         ++nv;
       }
-      mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u);
-      mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u);
-      mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u);
+      mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u, a.err);
+      mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u, a.err);
+      mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u, a.err);
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -1055,7 +1043,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       uint32_t last_par = 0;
       auto issue_s = [&](int j) -> bool {
         const uint32_t t_s = tmem + P::T_S + 64 * (j & 1);
-        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail)) return false;
+        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -1067,7 +1055,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         }
         mma_commit(bar_khf);
         last = bar_khf; last_par = (uint32_t)j & 1u;
-        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail)) return false;
+        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -1081,8 +1069,8 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       bool ok = issue_s(0);
       for (int j = 0; ok && j < n_sub; ++j) {
         if (j + 1 < n_sub && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail)) break;
-        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail)) break;
+        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
+        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail, a.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 64 * (j & 1);
         const uint32_t vh = su32(sVh), vl = vh + P::VSB;
@@ -1097,7 +1085,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         mma_commit(bar_o);
         last = bar_o; last_par = (uint32_t)j & 1u;
       }
-      if (last != nullptr && !mbar_wait_bounded(last, last_par)) *fail = 1;
+      if (last != nullptr && !mbar_wait_bounded(last, last_par, a.err)) *fail = 1;
     }
     __syncwarp();
   } else {
@@ -1108,7 +1096,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       const int64_t kpos0 = (is_tile ? 128LL * jb : win_pos0 + 128LL * (jb - n_tile_blk)) + 64 * sb;
       const int nkeys = (is_tile ? 128 : min(128, a.win_len - 128 * (jb - n_tile_blk))) - 64 * sb;
       const bool full_vis = kpos0 + 63 <= pmin && nkeys >= 64;
-      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail);
+      bool bad = !mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err);
       bad = __any_sync(0xffffffffu, bad || *fail != 0);
       const uint32_t t_s = tmem + P::T_S + 64 * (j & 1) + lb + 32 * half;
       float sv[32];
@@ -1150,7 +1138,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       tmem_st16_nowait(t_s + 16, lw);
       // O belongs to PV(j-1) until it completes
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail)) {
+        if (mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail, a.err)) {
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
           for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -1330,17 +1318,19 @@ void prefill_blocks(int64_t pos0, int C, int n_tiles, int win_len, int* n_tblk, 
 size_t prefill_block_bytes(int D) { return (size_t)4 * 128 * D * 2; }
 
 cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* tiles,
-                           const int64_t* tile_table, int table_stride, int n_tiles,
+                           int64_t tiles_bytes, const int64_t* tile_table, int table_stride,
+                           int n_tiles,
                            const float* win_k, const float* win_v, int win_start, int win_len,
                            int win_capacity, int Hq, int Hkv, int D, float softmax_scale,
                            int scale_bytes, int v_bits, void* ws, int ws_blocks, int cached_tiles,
-                           float* out, cudaStream_t st) {
+                           float* out, unsigned* err, cudaStream_t st) {
   PrefillArgs a;
   a.q = q; a.tiles = tiles; a.tile_table = tile_table; a.win_k = win_k; a.win_v = win_v;
   a.ws = reinterpret_cast<uint8_t*>(ws);
   a.out = out; a.pos0 = pos0; a.C = C; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
   a.n_tiles = n_tiles; a.table_stride = table_stride; a.win_start = win_start;
   a.win_len = win_len; a.win_cap = win_capacity; a.qscale = softmax_scale * kLog2e;
+  a.tiles_bytes = tiles_bytes; a.err = err;
   prefill_blocks(pos0, C, n_tiles, win_len, &a.n_tblk, &a.n_blk);
   a.ws_stride = ws_blocks > 0 ? ws_blocks : a.n_blk;
   a.first_blk = cached_tiles < a.n_tblk ? cached_tiles : a.n_tblk;

@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const float* q, float* q_ro
 __global__ void append_kernel(const float4* __restrict__ k_new, const float4* __restrict__ v_new,
                               int64_t n_new, float4* __restrict__ win_k, float4* __restrict__ win_v,
                               int cap, const int32_t* __restrict__ win_start,
-                              const int32_t* __restrict__ win_len, int n_seq, int hkv, int d4) {
+                              const int32_t* __restrict__ win_len, int n_seq, int hkv, int d4,
+                              unsigned* err) {
   pdl_trigger();
   pdl_wait();
   const int64_t total = (int64_t)n_seq * n_new * hkv * d4;
@@ -64,7 +65,13 @@ __global__ void append_kernel(const float4* __restrict__ k_new, const float4* __
     r /= hkv;
     const int64_t i = r % n_new;
     const int s = (int)(r / n_new);
-    int64_t slot = ((int64_t)win_start[s] + win_len[s] + i) % cap;
+    // a ring that would overflow keeps its rows (none of them promoted yet)
+    const int len = win_len[s];
+    if (len < 0 || (int64_t)len + n_new > cap) {
+      if (i == 0 && h == 0 && c4 == 0) report(err, KVARN_DEVERR_WINDOW);
+      continue;
+    }
+    int64_t slot = ((int64_t)win_start[s] + len + i) % cap;
     if (slot < 0) slot += cap;
     const int64_t dst = (((int64_t)s * hkv + h) * cap + slot) * d4 + c4;
     win_k[dst] = k_new[idx];
@@ -89,12 +96,31 @@ __global__ void advance_kernel(int32_t* win_start, int32_t* win_len, int32_t* n_
   win_len[s] = len;
 }
 
+// Waits on an mbarrier that nothing completes, for at most timeout_ns, then
+// reports KVARN_DEVERR_SELFTEST: the device failure path, run on purpose.
+__global__ void selftest_wait_kernel(uint64_t timeout_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar))
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_timed(&bar, 0, err, KVARN_DEVERR_SELFTEST, nullptr, timeout_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, unsigned* err, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(timeout_ns, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_window_advance(int32_t* win_start, int32_t* win_len, int32_t* n_tiles,
                                   int n_seq, int d_len, int promote, int win_capacity,
-                                  cudaStream_t st) {
-  LaunchCfg L(dim3((n_seq + 127) / 128), dim3(128), 0, st);
+                                  unsigned flags, cudaStream_t st) {
+  LaunchCfg L(dim3((n_seq + 127) / 128), dim3(128), 0, st, flags);
   return cudaLaunchKernelEx(&L.cfg, advance_kernel, win_start, win_len, n_tiles, n_seq, d_len,
                             promote, win_capacity);
 }
@@ -113,15 +139,15 @@ cudaError_t launch_rotate(const float* q, float* q_rot, int64_t n_rows, int D, c
 cudaError_t launch_append(const float* k_new, const float* v_new, int64_t n_new, float* win_k,
                           float* win_v, int win_capacity, const int32_t* win_start,
                           const int32_t* win_len, int n_seq, int n_kv_heads, int D,
-                          cudaStream_t st) {
+                          unsigned flags, unsigned* err, cudaStream_t st) {
   const int64_t total = (int64_t)n_seq * n_new * n_kv_heads * (D / 4);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 32) blocks = 152 * 32;
-  LaunchCfg L(dim3((unsigned)blocks), dim3(256), 0, st);
+  LaunchCfg L(dim3((unsigned)blocks), dim3(256), 0, st, flags);
   return cudaLaunchKernelEx(&L.cfg, append_kernel, reinterpret_cast<const float4*>(k_new),
                             reinterpret_cast<const float4*>(v_new), n_new,
                             reinterpret_cast<float4*>(win_k), reinterpret_cast<float4*>(win_v),
-                            win_capacity, win_start, win_len, n_seq, n_kv_heads, D / 4);
+                            win_capacity, win_start, win_len, n_seq, n_kv_heads, D / 4, err);
 }
 
 }  // namespace kvarn

@@ -56,36 +56,45 @@ def test_host_validation_rejects_before_launch(lib):
     L = kvarn.layout(128)
     p = ctypes.c_void_p(16)
     bad = ctypes.c_void_p(8)
-    # compress: null, misaligned, bad stride
-    assert lib.kvarn_compress_tile(None, p, 128, 256, p, p, p, 1, ctypes.byref(L), None) == -1
-    assert lib.kvarn_compress_tile(bad, p, 128, 256, p, p, p, 1, ctypes.byref(L), None) == -2
-    assert lib.kvarn_compress_tile(p, p, 130, 256, p, p, p, 1, ctypes.byref(L), None) == -2
-    assert lib.kvarn_compress_tile(p, p, 64, 256, p, p, p, 1, ctypes.byref(L), None) == -4
-    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, p, 0, ctypes.byref(L), None) == 0
+    # compress: null, misaligned, bad stride, a pool smaller than one record
+    rb = L.record_bytes
+    assert lib.kvarn_compress_tile(None, p, 128, 256, p, p, rb, p, 1, ctypes.byref(L), None) == -1
+    assert lib.kvarn_compress_tile(bad, p, 128, 256, p, p, rb, p, 1, ctypes.byref(L), None) == -2
+    assert lib.kvarn_compress_tile(p, p, 130, 256, p, p, rb, p, 1, ctypes.byref(L), None) == -2
+    assert lib.kvarn_compress_tile(p, p, 64, 256, p, p, rb, p, 1, ctypes.byref(L), None) == -4
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, rb - 16, p, 1, ctypes.byref(L), None) == -4
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, -1, p, 1, ctypes.byref(L), None) == -4
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, rb, p, 0, ctypes.byref(L), None) == 0
     tampered = kvarn.layout(128)
     tampered.record_bytes += 16
-    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, p, 1, ctypes.byref(tampered), None) == -3
+    assert lib.kvarn_compress_tile(p, p, 128, 256, p, p, rb, p, 1, ctypes.byref(tampered), None) == -3
     # rotate: unsupported dim, overlap
     assert lib.kvarn_rotate_query(p, p, 4, 96, None) == -3
     assert lib.kvarn_rotate_query(ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 256), 4, 128, None) == -4
-    # append: too many new tokens for the ring
-    assert lib.kvarn_append_window(p, p, 300, p, p, 256, p, p, 1, 8, 128, None) == -4
+    # append: too many new tokens for the ring; unknown launch flags
+    assert lib.kvarn_append_window(p, p, 300, p, p, 256, p, p, 1, 8, 128, 0, None) == -4
+    assert lib.kvarn_append_window(p, p, 3, p, p, 256, p, p, 1, 8, 128, 8, None) == -4
     # decode: GQA group too large, non-divisible heads, workspace too small
     n = ctypes.c_size_t()
     assert lib.kvarn_decode_workspace_bytes(1, 32, 2, 128, 8, 128, ctypes.byref(n)) == -3
     assert lib.kvarn_decode_workspace_bytes(1, 30, 8, 128, 8, 128, ctypes.byref(n)) == -4
     assert lib.kvarn_decode_workspace_bytes(1, 32, 8, 128, 8, 128, ctypes.byref(n)) == 0
     assert n.value > 0
-    args = [p] * 8 + [128, 1, 32, 8, 128, 8, ctypes.c_float(0.088), ctypes.byref(L), p, 16, p, None]
-    assert lib.kvarn_decode_attention(*args) == -5
+    def dargs(ws_bytes=16, flags=0, tiles_bytes=1 << 30):
+        return ([p, p, tiles_bytes] + [p] * 6 + [128, 1, 32, 8, 128, 8, ctypes.c_float(0.088),
+                                                 ctypes.byref(L), p, ws_bytes, p, flags, None])
+    assert lib.kvarn_decode_attention(*dargs()) == -5
+    assert lib.kvarn_decode_attention(*dargs(1 << 30, flags=4)) == -4   # unknown flag bit
+    assert lib.kvarn_decode_attention(*dargs(1 << 30, tiles_bytes=-1)) == -4
+    assert lib.kvarn_decode_attention_noalloc(*(dargs(flags=2)[:17] + [p, 2, None])) == -4
 
 
 def test_prefill_host_validation(lib):
     L = kvarn.layout(128)
     p = ctypes.c_void_p(4096)
     args = lambda C, pos0, nt, wl, D=128, Hq=32, lay=L, wsb=1 << 40: (
-        p, C, pos0, p, p, 64, nt, p, p, 0, wl, 768, Hq, 8, D, ctypes.c_float(0.088),
-        ctypes.byref(lay), p, ctypes.c_size_t(wsb), p, None)
+        p, C, pos0, p, ctypes.c_int64(1 << 40), p, 64, nt, p, p, 0, wl, 768, Hq, 8, D,
+        ctypes.c_float(0.088), ctypes.byref(lay), p, ctypes.c_size_t(wsb), p, None)
     f = lib.kvarn_prefill_attention
     f.argtypes = None
     assert f(*args(512, 2000, 10, 300)) == -4          # chunk beyond the cache
@@ -107,16 +116,25 @@ def test_prefill_host_validation(lib):
 
 
 
-def test_launch_flags_validation():
-    assert kvarn.get_launch_flags() == 0
-    with pytest.raises(kvarn.KvarnError):
-        kvarn.set_launch_flags(kvarn.LAUNCH_PREFETCH)  # prefetch needs programmatic launch
-    with pytest.raises(kvarn.KvarnError):
-        kvarn.set_launch_flags(8)
-    kvarn.set_launch_flags(kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH)
-    assert kvarn.get_launch_flags() == 3
-    kvarn.set_launch_flags(0)
-    assert kvarn.get_launch_flags() == 0
+def test_launch_flags_are_per_call(lib):
+    """Launch flags are an argument of each decode-path call: unknown bits and
+    PREFETCH without PDL are refused by that call, and nothing is left set
+    between calls."""
+    p = ctypes.c_void_p(4096)
+    adv = lib.kvarn_window_advance
+    assert adv(p, p, p, 1, 1, 0, 128, kvarn.LAUNCH_PREFETCH, None) == -4
+    assert adv(p, p, p, 1, 1, 0, 128, 8, None) == -4
+    assert adv(p, p, p, 0, 1, 0, 128, kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH, None) == 0
+    assert lib.kvarn_decode_combine(p, 1 << 30, 1, 32, 8, 128, 8, 128, p, 16, None) == -4
+    assert not hasattr(kvarn, "set_launch_flags")
+    raw = ctypes.CDLL(_build.LIB)
+    assert not hasattr(raw, "kvarn_set_launch_flags")
+
+
+def test_device_error_api_rejects_bad_arguments(lib):
+    assert lib.kvarn_get_device_error(None, 0) == -1
+    assert lib.kvarn_selftest_bounded_wait(0, None) == -4
+    assert lib.kvarn_selftest_bounded_wait(2000000, None) == -4
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
@@ -132,7 +150,7 @@ def test_f16_scale_layout_agrees_with_oracle(lib, D):
     # a layout claiming f16 scales with fp32 offsets is not one the library made
     M.version = 2
     p = ctypes.c_void_p(16)
-    assert lib.kvarn_compress_tile(p, p, D, 256, p, p, p, 1, ctypes.byref(M), None) == -3
+    assert lib.kvarn_compress_tile(p, p, D, 256, p, p, 1 << 20, p, 1, ctypes.byref(M), None) == -3
 
 
 def test_prefill_cached_host_validation(lib):
@@ -142,8 +160,8 @@ def test_prefill_cached_host_validation(lib):
     f = lib.kvarn_prefill_attention_cached
     f.argtypes = None
     args = lambda wsb, wsblocks, cached, nt=10: (
-        p, 512, 1000, p, p, 64, nt, p, p, 0, 300, 768, 32, 8, 128, ctypes.c_float(0.088),
-        ctypes.byref(L), p, ctypes.c_size_t(wsb), wsblocks, cached, p, None)
+        p, 512, 1000, p, ctypes.c_int64(1 << 40), p, 64, nt, p, p, 0, 300, 768, 32, 8, 128,
+        ctypes.c_float(0.088), ctypes.byref(L), p, ctypes.c_size_t(wsb), wsblocks, cached, p, None)
     assert f(*args(1 << 40, 0, 0)) == -4           # ws_blocks must be positive
     assert f(*args(1 << 40, 11, 0)) == -5          # fewer images per head than the 12 blocks seen
     assert f(*args(16 * 8 * blk - 1, 16, 0)) == -5  # workspace smaller than ws_blocks images
@@ -170,7 +188,8 @@ def test_prefill_accepts_v4_records(lib):
     p = ctypes.c_void_p(4096)
     f = lib.kvarn_prefill_attention
     f.argtypes = None
-    assert f(p, 0, 0, p, p, 64, 1, p, p, 0, 16, 768, 32, 8, 128, ctypes.c_float(0.088),
+    big = ctypes.c_int64(1 << 40)
+    assert f(p, 0, 0, p, big, p, 64, 1, p, p, 0, 16, 768, 32, 8, 128, ctypes.c_float(0.088),
              ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == 0
-    assert f(p, 16, 0, p, p, 64, 1, p, p, 0, 16, 768, 33, 8, 128, ctypes.c_float(0.088),
+    assert f(p, 16, 0, p, big, p, 64, 1, p, p, 0, 16, 768, 33, 8, 128, ctypes.c_float(0.088),
              ctypes.byref(L), p, ctypes.c_size_t(1 << 40), p, None) == -4

@@ -38,6 +38,6 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert need > (16 << 20)
     p = ctypes.c_void_p(256)
     fn = kvarn._L().kvarn_decode_attention_noalloc
-    rc = fn(p, p, p, p, p, p, p, p, 128, 64, 32, 8, 128, 8192, ctypes.c_float(0.088),
-            ctypes.byref(lay), p, None)
+    rc = fn(p, p, 1 << 40, p, p, p, p, p, p, 128, 64, 32, 8, 128, 8192, ctypes.c_float(0.088),
+            ctypes.byref(lay), p, 0, None)
     assert rc == -5  # KVARN_ERR_WORKSPACE, nothing enqueued
