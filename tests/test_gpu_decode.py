@@ -90,10 +90,12 @@ def test_offset_not_multiple_of_128_poisons_only_that_head():
     pool[n + 16:n + 16 + c.rb] = c.tiles[int(c.tile_table[0, 1, 0]):int(c.tile_table[0, 1, 0]) + c.rb]
     table = c.tile_table.clone()
     table[0, 1, 0] = n + 16  # 16-byte aligned, not a multiple of 128
+    kvarn.device_error(clear=True)
     out = kvarn.decode_attention(q, pool, table, c.n_tiles, c.win_k, c.win_v, c.win_start,
                                  c.win_len, c.lay).cpu().numpy()
     assert np.isnan(out[0, 4:]).all()          # query heads of KV head 1
     assert np.array_equal(out[0, :4], good[0, :4])
+    assert kvarn.device_error(clear=True) == kvarn.DEVERR_RECORD  # reported, then cleared
 
 
 @pytest.mark.parametrize("workload,Hq,Hkv,D,ctx", [("single_tile", 8, 8, 64, 128 * 80 + 33),
@@ -205,3 +207,4 @@ def test_v4_records_multi_round(D, Hq, Hkv, ctx):
     """The multi-round split kernel on k4v4 records."""
     c = Cache("qwen3_8b_decode", 17, [ctx], Hkv=Hkv, D=D, v_bits=4)
     _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])
+

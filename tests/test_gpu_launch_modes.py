@@ -109,7 +109,7 @@ class _DecodeState:
         self.win_len = torch.tensor(self.wl, dtype=torch.int32, device=DEV)
         self.n_tiles = torch.tensor(self.nt, dtype=torch.int32, device=DEV)
         self.host_start = [0] * B
-        self.ws = torch.empty(kvarn.decode_workspace_bytes(B, self.HQ, HKV, D, self.max_tiles, CAP),
+        self.ws = torch.zeros(kvarn.decode_workspace_bytes(B, self.HQ, HKV, D, self.max_tiles, CAP),
                               dtype=torch.uint8, device=DEV)
         self.q = torch.empty(L, B, self.HQ, D, device=DEV)
         self.kn = torch.empty(L, B, 1, HKV, D, device=DEV)
@@ -157,6 +157,8 @@ def test_graph_replay_matches_direct_path_across_promotions():
     every output of every step, before and after each sequence's window
     crosses 128 tokens and is promoted into a tile."""
     ctxs = [128 * 5 + 124, 128 * 3 + 126]
+    torch.cuda.synchronize()
+    kvarn.device_error(clear=True)
     eager, graphed = _DecodeState(ctxs), _DecodeState(ctxs)
     fast = kvarn.LAUNCH_PDL | kvarn.LAUNCH_PREFETCH
     graphed.kn.zero_()
