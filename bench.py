@@ -47,10 +47,11 @@ C_TILES, C_HEADS = 256, 8
 # DRAM bytes per launch from an ncu capture, keyed by the kernel source they
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
-    # one 16k-context layer: 17.39 MB read, nothing written back within the launch
-    "decode_split": {"src_sha": "e83c81fb6e8c2756", "bytes": 17394176},
-    # one 2048-tile-head launch: 268.52 MB read + 17.65 MB written back within the launch
-    "compress": {"src_sha": "9915dbe10f8fdd8c", "bytes": 286166016},
+    # one 16k-context layer (128 tiles x 8 KV heads + a 124-token window): 17.88 MB
+    # read, nothing written back within the launch
+    "decode_split": {"src_sha": "ed8b1bb7bfbbec11", "bytes": 17877248},
+    # one 2048-tile-head launch: 268.51 MB read + 17.56 MB written back within the launch
+    "compress": {"src_sha": "39ae76a024c4acbb", "bytes": 286073856},
 }
 
 
@@ -176,6 +177,104 @@ class OracleDecodeSample:
     @property
     def scale(self) -> float:
         return LAYERS * CTX0 / (128.0 * self.n_tiles)
+
+
+def oracle_compress_baseline(sample: dict) -> dict:
+    """The oracle's tile compression timed on host threads (1 and all cores)
+    over the first units of the bulk-compress input, and the GPU records of
+    the same units compared with the oracle's: codes that differ, of which
+    inside the rounding band (|frac(v) - 1/2| < 1e-5 of the oracle's
+    pre-rounding value v) and outside it, and the largest relative scale
+    difference. The oracle's codes are exact only up to that band."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    k, v, recs, rb = sample["k"], sample["v"], sample["records"], sample["record_bytes"]
+    n = k.shape[0] // 128
+    unit = lambda u: oracle.compress_unit(k[128 * u:128 * u + 128], v[128 * u:128 * u + 128])
+    t0 = time.perf_counter()
+    for u in range(4):
+        unit(u)
+    t1 = (time.perf_counter() - t0) / 4
+    cores = max(1, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(cores) as pool:
+        t0 = time.perf_counter()
+        refs = list(pool.map(unit, range(n)))
+        tn = (time.perf_counter() - t0) / n
+    codes = differ = in_band = outside = 0
+    worst = 0.0
+    for u, ref in enumerate(refs):
+        got = oracle.unpack_record(recs[u * rb:(u + 1) * rb], D)
+        want = oracle.unpack_record(ref["record"], D)
+        for t in ("k", "v"):
+            d = got[f"{t}_codes"] != want[f"{t}_codes"]
+            vpre = ref[f"{t}_vpre"]
+            band = np.abs(vpre - np.floor(vpre) - 0.5) < 1e-5
+            codes += d.size
+            differ += int(d.sum())
+            in_band += int((d & band).sum())
+            outside += int((d & ~band).sum())
+            for f in ("delta", "s", "r"):
+                w = np.asarray(ref[f"{t}_{f}"], np.float64)
+                g = got[f"{t}_{f}"].astype(np.float64)
+                worst = max(worst, float(np.max(np.abs(g - w) / np.maximum(np.abs(w), 1e-30))))
+    return {"oracle_tile_heads_per_s_1_core": 1.0 / t1,
+            "oracle_tile_heads_per_s_all_cores": 1.0 / tn, "cores": cores,
+            "sample": f"{n} tile-heads of the bulk-compress input (head_dim {D}); 4 on one thread",
+            "gpu_vs_oracle": {"codes": codes, "differing": differ, "in_rounding_band": in_band,
+                              "outside_rounding_band": outside,
+                              "scale_rel_err_max": worst,
+                              "note": "GPU records of the same units, decoded by the oracle; "
+                                      "delta, s and r compared relative to the oracle's value"}}
+
+
+def oracle_prefill_baseline(rows_every: int = 16) -> dict:
+    """The oracle's causal prefill attention timed on host threads over the
+    last 512-token chunk of a 2,048-token prefix of the 8B-like prompt (32q/8kv,
+    head_dim 128, W=256): every rows_every-th row, all 32 query heads, over
+    tiles the oracle compressed itself; scaled by visible (query, key) pairs to
+    the whole prefix's attention."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from kv_cache_quantization_token_gb300 import synth
+    n_tok, Wp, Hq, Hkv = 2048, 256, 32, 8
+    k, v = synth.kv_layer("qwen3_8b_prefill", 0, Hkv, n_tok, D)
+    q = synth.queries("qwen3_8b_prefill", 0, (n_tok, Hq, D))
+    nt = (n_tok - Wp) // 128 + 1                       # tiles after the last promotion
+    rb = oracle.record_bytes(D)
+    cores = max(1, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(cores) as pool:
+        recs = list(pool.map(lambda hu: oracle.compress_unit(
+            k[hu[0], 128 * hu[1]:128 * hu[1] + 128], v[hu[0], 128 * hu[1]:128 * hu[1] + 128])["record"],
+            [(h, i) for h in range(Hkv) for i in range(nt)]))
+    pool_b = np.concatenate(recs)
+    table = (np.arange(Hkv)[:, None] * nt + np.arange(nt)[None, :]).astype(np.int64) * rb
+    wl = n_tok - 128 * nt
+    cap = 512
+    wk = np.zeros((Hkv, cap, D), np.float32)
+    wv = np.zeros_like(wk)
+    wk[:, :wl] = k[:, 128 * nt:]
+    wv[:, :wl] = v[:, 128 * nt:]
+    pos0 = n_tok - 512
+    rows = list(range(0, 512, rows_every))
+
+    def one(i):
+        return oracle.prefill_attention(q[pos0:pos0 + 512], pos0, pool_b, table, nt, wk, wv, 0, wl,
+                                        D ** -0.5, rows=[(i, h) for h in range(Hq)])
+    out = {}
+    for label, workers in (("1_core", 1), ("all_cores", cores)):
+        sample_rows = rows[:4] if workers == 1 else rows
+        with ThreadPoolExecutor(workers) as pool:
+            t0 = time.perf_counter()
+            list(pool.map(one, sample_rows))
+            sec = time.perf_counter() - t0
+        pairs = sum(pos0 + i + 1 for i in sample_rows)
+        total = n_tok * (n_tok + 1) // 2
+        layer_s = sec * total / pairs
+        out[f"prompt_tokens_per_s_one_layer_{label}"] = n_tok / layer_s
+    out.update({"cores": cores, "sample": f"rows 0, {rows_every}, ... of positions {pos0}..{n_tok - 1} "
+                                          f"(4 rows on one thread), all {Hq} query heads; scaled "
+                                          f"by visible (query, key) pairs to the {n_tok}-token prefix"})
+    return out
 
 
 def reduce_timing(elapsed_ms, units_per_rank, world, device=None):
@@ -375,7 +474,8 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
     """Decode split throughput beyond the headline configuration: the 8B-like
     model at 4k and 32k context, and at 16k on records of the f16-scale layout
     and of the k4v4 variant (36 layers of distinct caches, split launches back to back as in the
-    headline roofline), and batched decode with large
+    headline roofline); the 0.6B-like model (16q/8kv, 28 layers, 3072 + 77
+    tokens); and batched decode with large
     heads (32 ragged sequences with contexts uniform in [8k, 32k], 16q/4kv,
     head_dim 256; one layer's cache is 0.6 GB), timed as back-to-back split
     launches and as decode steps (split + combine) with a concurrent compress
@@ -404,25 +504,31 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / (reps * n_launch)
 
-    # ---- 8B-like decode at 4k and 32k, and at 16k on f16-scale records --------
-    for ctx, sb, vb in ((4096, 32, 2), (32768, 32, 2), (16384, 16, 2), (16384, 32, 4)):
+    # ---- 8B-like decode at 4k and 32k, and at 16k on f16-scale and k4v4
+    # records; and the 0.6B-like model (16q/8kv, 28 layers) at 3072 + 77 tokens
+    points = [("qwen3_8b_ctx4096", WORKLOAD, HQ, LAYERS, 4096, 64, 32, 2),
+              ("qwen3_8b_ctx32768", WORKLOAD, HQ, LAYERS, 32768, 64, 32, 2),
+              ("qwen3_8b_ctx16384_f16_scales", WORKLOAD, HQ, LAYERS, 16384, 64, 16, 2),
+              ("qwen3_8b_ctx16384_k4v4", WORKLOAD, HQ, LAYERS, 16384, 64, 32, 4),
+              ("qwen3_0p6b_ctx3072", "qwen3_0p6b_decode", 16, 28, 3072, 77, 32, 2)]
+    for name, wl_name, hq, n_layers, ctx, w0, sb, vb in points:
         lay_s = lay if (sb, vb) == (32, 2) else kvarn.layout(D, scale_bits=sb, v_bits=vb)
-        n0, w0, cap = ctx // 128, 64, 128
+        n0, cap = ctx // 128, 128
         rb = lay_s.record_bytes
         max_tiles = n0 + 1
-        tiles = torch.empty(LAYERS * HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
-        table = torch.empty(LAYERS, 1, HKV, max_tiles, dtype=torch.int64, device=dev)
-        win_k = torch.zeros(LAYERS, 1, HKV, cap, D, device=dev)
+        tiles = torch.empty(n_layers * HKV * max_tiles * rb, dtype=torch.uint8, device=dev)
+        table = torch.empty(n_layers, 1, HKV, max_tiles, dtype=torch.int64, device=dev)
+        win_k = torch.zeros(n_layers, 1, HKV, cap, D, device=dev)
         win_v = torch.zeros_like(win_k)
         raw = []
-        for r in range(2):  # two distinct layers of values, stored at 36 distinct addresses
-            ks, vs = synth.kv_layer(WORKLOAD, 200 + r, HKV, ctx + w0, D)
+        for r in range(2):  # two distinct layers of values, stored at n_layers distinct addresses
+            ks, vs = synth.kv_layer(wl_name, 200 + r, HKV, ctx + w0, D)
             raw.append((torch.from_numpy(ks.reshape(-1, D)).to(dev),
                         torch.from_numpy(vs.reshape(-1, D)).to(dev), ks[:, ctx:], vs[:, ctx:]))
             del ks, vs
         src = torch.from_numpy((np.arange(HKV)[:, None] * (ctx + w0)
                                 + 128 * np.arange(n0)[None, :]).reshape(-1).astype(np.int64)).to(dev)
-        for l in range(LAYERS):
+        for l in range(n_layers):
             tab = ((l * HKV) * max_tiles + np.arange(HKV)[:, None] * max_tiles
                    + np.arange(max_tiles)[None, :]) * rb
             table[l, 0] = torch.from_numpy(tab.astype(np.int64))
@@ -432,36 +538,37 @@ def run_decode_sweeps(dev, lay, peaks, peak_kind):
             win_k[l, 0, :, :w0] = torch.from_numpy(kw).to(dev)
             win_v[l, 0, :, :w0] = torch.from_numpy(vw).to(dev)
         del raw
-        q = torch.from_numpy(synth.queries(WORKLOAD, 3, (LAYERS, 1, HQ, D))).to(dev)
-        ws = torch.empty(kvarn.decode_workspace_bytes(1, HQ, HKV, D, max_tiles, cap) + 256,
+        q = torch.from_numpy(synth.queries(wl_name, 3, (n_layers, 1, hq, D))).to(dev)
+        ws = torch.empty(kvarn.decode_workspace_bytes(1, hq, HKV, D, max_tiles, cap) + 256,
                          dtype=torch.uint8, device=dev)
-        out = torch.empty(LAYERS, 1, HQ, D, device=dev)
+        out = torch.empty(n_layers, 1, hq, D, device=dev)
         wst = torch.zeros(1, dtype=torch.int32, device=dev)
         wl = torch.full((1,), w0, dtype=torch.int32, device=dev)
         nt = torch.full((1,), n0, dtype=torch.int32, device=dev)
 
         def splits():
-            for l in range(LAYERS):
+            for l in range(n_layers):
                 kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws,
                                    flags=FAST)
 
         def steps():
-            for l in range(LAYERS):
+            for l in range(n_layers):
                 kvarn.decode_split(q[l], tiles, table[l], nt, win_k[l], win_v[l], wst, wl, lay_s, ws,
                                    flags=FAST)
-                kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap)
+                kvarn.decode_combine(ws, out[l], HKV, max_tiles, cap, flags=FAST)
 
-        split_ms = back_to_back(splits, LAYERS)
-        layer_ms = back_to_back(steps, LAYERS)
+        split_ms = back_to_back(splits, n_layers)
+        layer_ms = back_to_back(steps, n_layers)
         assert torch.isfinite(out).all().item(), "decode produced non-finite output"
-        nbytes = HKV * n0 * rb + HKV * w0 * D * 8 + HQ * D * 4
+        nbytes = HKV * n0 * rb + HKV * w0 * D * 8 + hq * D * 4
         gbs = nbytes / (split_ms * 1e-3) / 1e9
-        res[f"qwen3_8b_ctx{ctx}" + ("" if sb == 32 else "_f16_scales") + ("" if vb == 2 else "_k4v4")] = {
-            "record_bytes": rb,
+        res[name] = {
+            "record_bytes": rb, "q_heads": hq, "kv_heads": HKV, "layers": n_layers,
+            "context": ctx + w0,
             "split_back_to_back_ms": split_ms, "split_bytes_per_launch": nbytes,
             "split_gbs": gbs, "split_frac": gbs / hbm,
             "attention_ms_per_layer": layer_ms,
-            "tokens_per_s_36_layers": 1.0 / (LAYERS * layer_ms * 1e-3)}
+            f"tokens_per_s_{n_layers}_layers": 1.0 / (n_layers * layer_ms * 1e-3)}
         del tiles, table, win_k, win_v, ws
 
     # ---- batched decode, head_dim 256 ------------------------------------------
@@ -554,10 +661,11 @@ def workload_config():
 
 
 # --------------------------------------------------------------------------
-def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind, tiles=C_TILES):
+def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind, tiles=C_TILES, keep=None):
     """One compress launch over tiles x C_HEADS tile-heads of fresh raw K/V
     (256 MiB of input at the defaults, larger than L2), timed with CUDA
-    events per launch."""
+    events per launch. With `keep` (a dict), the raw rows and the GPU records
+    of the first 32 units are left there for the host-side baseline leg."""
     import torch
     from kv_cache_quantization_token_gb300 import kvarn, synth
     D, rb = lay.head_dim, lay.record_bytes
@@ -565,6 +673,9 @@ def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind, tiles=C_TILES):
     ks, vs = synth.kv_layer(WORKLOAD, 99, C_HEADS, 128 * tiles, D)
     ck = torch.from_numpy(ks.reshape(-1, D)).to(dev)
     cv = torch.from_numpy(vs.reshape(-1, D)).to(dev)
+    if keep is not None:
+        keep["k"] = ks.reshape(-1, D)[:32 * 128].copy()
+        keep["v"] = vs.reshape(-1, D)[:32 * 128].copy()
     del ks, vs
     csrc = torch.arange(n_units, dtype=torch.int64, device=dev) * 128
     cdst = torch.arange(n_units, dtype=torch.int64, device=dev) * rb
@@ -580,6 +691,9 @@ def run_compress_bench(dev, stream, lay, warmup, hbm, peak_kind, tiles=C_TILES):
             kvarn.compress_tile(ck, cv, csrc, ctiles, cdst, lay)
             b.record()
     torch.cuda.synchronize()
+    if keep is not None:
+        keep["records"] = ctiles[:32 * rb].cpu().numpy()
+        keep["record_bytes"] = rb
     comp_ms = float(np.mean([a.elapsed_time(b) for a, b in cev]))
     comp_bytes = n_units * (2 * 128 * D * 4 + rb)
     comp_gbs = comp_bytes / (comp_ms * 1e-3) / 1e9
@@ -872,7 +986,9 @@ def main():
     compress = prefill = prefill_d256 = sweeps = None
     # ---- compress bulk (32k-token 8B-like caches) ------------------------------
     if secondary:
-        compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind)
+        compress_sample = {}
+        compress = run_compress_bench(dev, stream, lay, args.warmup, hbm, peak_kind,
+                                      keep=compress_sample)
         # head_dim 256: 1024 tile-heads, the same 256 MiB of input
         try:
             compress["head_dim_256"] = run_compress_bench(dev, stream, kvarn.layout(256),
@@ -907,6 +1023,8 @@ def main():
                                 "unit": "tokens/s", "cores": 1,
                                 "sample": f"{one.sample}; mean of 3 runs",
                                 "sample_seconds": float(np.sum(secs1))}
+        cpu["compress"] = oracle_compress_baseline(compress_sample)
+        cpu["prefill_2048_prefix"] = oracle_prefill_baseline()
 
     if rank == 0:
         res = {
