@@ -163,8 +163,10 @@ def quantize_tensor(x: np.ndarray, per_channel: bool, bits: int, iters: int = DE
 # --------------------------------------------------------------------------
 # c4 -- packed record. scale_bits = 32: the default layout (fp32 scales);
 # 16: the f16-scale layout (SharpInference issue #433, item 3), same codes.
-# v_bits = 2: the method's k4v2 preset; 4: a k4v4 variant (other K/V bit
-# widths, SharpInference issue #433 / PR #434 scope notes), same packing rule.
+# v_bits = 2: the method's k4v2 preset; 3 and 4: k4v3 and k4v4 variants (other
+# K/V bit widths, gmlx PR #116), the same packing rule: each token's V codes
+# are a little-endian bit stream, channel c at bits v_bits*c .. (a 3-bit code
+# can straddle two bytes).
 def _sw(scale_bits: int) -> int:
     if scale_bits not in (16, 32):
         raise ValueError(f"scale_bits must be 16 or 32, not {scale_bits}")
@@ -181,8 +183,8 @@ def f16_value(bits: int) -> float:
 
 
 def _vb(v_bits: int) -> int:
-    if v_bits not in (2, 4):
-        raise ValueError(f"v_bits must be 2 or 4, not {v_bits}")
+    if v_bits not in (2, 3, 4):
+        raise ValueError(f"v_bits must be 2, 3 or 4, not {v_bits}")
     return v_bits
 
 

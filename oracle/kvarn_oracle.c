@@ -221,9 +221,12 @@ typedef struct {
   int gv, sw, vb;
 } orc_layout;
 
-/* vb: V code width, 2 (the method's k4v2 preset) or 4 (a k4v4 variant with
- * the same token-major packing: channel c of token t in the (c % (8/vb))-th
- * vb-bit field of byte t * (D vb / 8) + c / (8/vb)). */
+/* vb: V code width, 2 (the method's k4v2 preset), 3 or 4 (variants with
+ * other value widths). Packing: the V codes of token t form a little-endian
+ * bit stream of D * vb / 8 bytes starting at byte t * (D vb / 8); channel c
+ * occupies stream bits vb*c .. vb*c + vb - 1, stream bit i being bit i % 8 of
+ * byte i / 8. For vb = 2 and 4 that is the (c % (8/vb))-th vb-bit field of
+ * byte c / (8/vb); a 3-bit code may straddle two bytes. */
 static orc_layout orc_record_layout(int D, int sw, int vb) {
   orc_layout L;
   L.gv = D / (D < 128 ? D : 128);
@@ -245,7 +248,8 @@ static orc_layout orc_record_layout(int D, int sw, int vb) {
 
 static int orc_sw_ok(int sw) { return sw == 4 || sw == 2; }
 static int orc_fmt_ok(int D, int sw, int vb) {
-  return orc_pow2_dim(D) && D >= 4 && orc_sw_ok(sw) && (vb == 2 || vb == 4);
+  return orc_pow2_dim(D) && D >= 4 && orc_sw_ok(sw) && (vb == 2 || vb == 3 || vb == 4) &&
+         (D * vb) % 8 == 0;
 }
 
 int64_t orc_record_bytes_fmt(int D, int sw, int vb) {
@@ -313,7 +317,7 @@ int orc_pack_record_fmt(int D, int sw, int vb, const uint8_t* k_codes, const uin
                         const double* v_r, const double* v_s, uint8_t* rec) {
   if (!orc_fmt_ok(D, sw, vb)) return -3;
   const orc_layout L = orc_record_layout(D, sw, vb);
-  const int per = 8 / vb;                                /* V codes per byte */
+  const int64_t row = (int64_t)D * vb / 8;               /* V code bytes per token */
   memset(rec, 0, (size_t)L.bytes);
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t) {
@@ -322,8 +326,11 @@ int orc_pack_record_fmt(int D, int sw, int vb, const uint8_t* k_codes, const uin
     }
   for (int t = 0; t < ORC_T; ++t)
     for (int c = 0; c < D; ++c) {
-      const uint8_t code = v_codes[(int64_t)t * D + c] & (uint8_t)((1 << vb) - 1);
-      rec[L.v_codes + (int64_t)t * (D / per) + c / per] |= (uint8_t)(code << (vb * (c % per)));
+      const unsigned code = v_codes[(int64_t)t * D + c] & ((1u << vb) - 1u);
+      for (int b = 0; b < vb; ++b) {  /* one stream bit at a time */
+        const int64_t bit = (int64_t)vb * c + b;
+        rec[L.v_codes + t * row + bit / 8] |= (uint8_t)(((code >> b) & 1u) << (bit % 8));
+      }
     }
   for (int c = 0; c < D; ++c) {
     orc_put_scale(rec + L.k_delta + (int64_t)sw * c, k_delta[c], sw);
@@ -362,15 +369,20 @@ int orc_unpack_record_fmt(int D, int sw, int vb, const uint8_t* rec, uint8_t* k_
                           double* k_r, double* v_delta, double* v_lo, double* v_r, double* v_s) {
   if (!orc_fmt_ok(D, sw, vb)) return -3;
   const orc_layout L = orc_record_layout(D, sw, vb);
-  const int per = 8 / vb;
+  const int64_t row = (int64_t)D * vb / 8;
   for (int c = 0; c < D; ++c)
     for (int t = 0; t < ORC_T; ++t)
       k_codes[(int64_t)t * D + c] =
           (rec[L.k_codes + (int64_t)c * (ORC_T / 2) + t / 2] >> (4 * (t & 1))) & 0xF;
   for (int t = 0; t < ORC_T; ++t)
-    for (int c = 0; c < D; ++c)
-      v_codes[(int64_t)t * D + c] =
-          (rec[L.v_codes + (int64_t)t * (D / per) + c / per] >> (vb * (c % per))) & ((1 << vb) - 1);
+    for (int c = 0; c < D; ++c) {
+      unsigned code = 0;
+      for (int b = 0; b < vb; ++b) {
+        const int64_t bit = (int64_t)vb * c + b;
+        code |= (unsigned)((rec[L.v_codes + t * row + bit / 8] >> (bit % 8)) & 1u) << b;
+      }
+      v_codes[(int64_t)t * D + c] = (uint8_t)code;
+    }
   for (int c = 0; c < D; ++c) {
     k_delta[c] = orc_get_scale(rec + L.k_delta + (int64_t)sw * c, sw);
     k_lo[c] = orc_get_scale(rec + L.k_lo + (int64_t)sw * c, sw);

@@ -582,3 +582,97 @@ def test_v4_dequant_distortion_bound(oracle):
     err = np.linalg.norm(vv - v.astype(np.float64), axis=1)
     assert np.all(err <= bound * (1 + 1e-9))
     assert np.linalg.norm(vv - v) < np.linalg.norm(v2 - v)
+
+
+# ------------------------------------------- c4 variant: 3-bit values (k4v3)
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_v3_record_size(oracle, D):
+    """Token rows of 3 D / 8 bytes: 16 D bytes more than the k4v2 record."""
+    assert oracle.record_bytes(D, v_bits=3) - oracle.record_bytes(D) == 16 * D
+    assert oracle.record_bytes(128, v_bits=3) == 18432
+
+
+def test_v3_pack_bit_order_hand_built(oracle):
+    """Each token's V codes are a little-endian bit stream, channel c at bits
+    3c..3c+2: code 5 = 0b101 at channel 2 of token 0 sets stream bits 6 and 8
+    (bit 6 of byte 0, bit 0 of byte 1: a code straddling two bytes); code 6 =
+    0b110 at the last channel of token 3 sets the top two bits of that row's
+    last byte."""
+    D = 128
+    z = lambda n: np.zeros(n)
+    vc = np.zeros((128, D), np.uint8)
+    vc[0, 2] = 5
+    vc[3, D - 1] = 6
+    rec = oracle.pack_record(D, np.zeros((128, D), np.uint8), vc, z(D), z(D), z(D), z(128),
+                             z(128), z(128), z(128), z(D), v_bits=3)
+    voff = 64 * D
+    row = 3 * D // 8
+    assert rec[voff] == 0x40 and rec[voff + 1] == 0x01
+    assert rec[voff + 3 * row + row - 1] == 0xC0
+    assert np.count_nonzero(rec) == 3
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("scale_bits", [32, 16])
+def test_v3_pack_unpack_roundtrip(oracle, D, scale_bits):
+    rng = np.random.default_rng(D + 3 + scale_bits)
+    gv = D // min(D, 128)
+    f32 = lambda n: rng.standard_normal(n).astype(np.float16).astype(np.float64)
+    args = dict(k_codes=rng.integers(0, 16, (128, D)).astype(np.uint8),
+                v_codes=rng.integers(0, 8, (128, D)).astype(np.uint8),
+                k_delta=f32(D), k_lo=f32(D), k_s=f32(D), k_r=f32(128),
+                v_delta=f32(128 * gv), v_lo=f32(128 * gv), v_r=f32(128), v_s=f32(D))
+    rec = oracle.pack_record(D, scale_bits=scale_bits, v_bits=3, **args)
+    assert rec.size == oracle.record_bytes(D, scale_bits, 3)
+    back = oracle.unpack_record(rec, D, scale_bits, v_bits=3)
+    for name, val in args.items():
+        np.testing.assert_array_equal(back[name], val, err_msg=name)
+
+
+@pytest.mark.parametrize("workload,D", [("qwen3_8b_decode", 128), ("batched_d256_decode", 256)])
+def test_v3_compress_keeps_keys_and_bounds_value_error(oracle, workload, D):
+    """The k4v3 record: the K half is the k4v2 record's; V is quantised to 8
+    levels per token group (step (max - min)/7), every normalised V element
+    is within delta/2 of its reconstruction, and the group extremes take
+    codes 0 and 7."""
+    k, v = synth.kv_stream(workload, 4, 0, 128, D)
+    a = oracle.compress_unit(k, v)
+    b = oracle.compress_unit(k, v, v_bits=3)
+    ua = oracle.unpack_record(a["record"], D)
+    ub = oracle.unpack_record(b["record"], D, v_bits=3)
+    for name in ("k_codes", "k_delta", "k_lo", "k_s", "k_r", "v_s", "v_r"):
+        np.testing.assert_array_equal(ua[name], ub[name], err_msg=name)
+    gv = D // min(D, 128)
+    gw = D // gv
+    vpre, vc = b["v_vpre"], ub["v_codes"].astype(np.int64)
+    assert vc.max() <= 7 and vc.min() >= 0
+    dl = b["v_delta"].reshape(128, gv).repeat(gw, 1)
+    lo = b["v_lo"].reshape(128, gv).repeat(gw, 1)
+    y, recon = dl * vpre + lo, dl * vc + lo
+    assert np.all(np.abs(y - recon) <= dl / 2 * (1 + 1e-12) + 1e-300)
+    for t in range(0, 128, 13):
+        for g in range(gv):
+            seg, codes = vpre[t, g * gw:(g + 1) * gw], vc[t, g * gw:(g + 1) * gw]
+            assert codes[np.argmin(seg)] == 0 and codes[np.argmax(seg)] == 7
+    yv = y.reshape(128, gv, gw)
+    np.testing.assert_allclose(b["v_delta"].reshape(128, gv), (yv.max(-1) - yv.min(-1)) / 7,
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_v3_distortion_between_v2_and_v4(oracle):
+    """Unrotated V rows of a k4v3 record are within the norm of r s delta / 2
+    of the exact rows, and their error lies between the k4v2 and k4v4
+    records' on the same tile."""
+    D = 128
+    k, v = synth.kv_stream("qwen3_8b_decode", 5, 0, 128, D)
+    err = {}
+    for vb in (2, 3, 4):
+        b = oracle.compress_unit(k, v, v_bits=vb)
+        _, vv = oracle.dequant_record(b["record"], D, v_bits=vb)
+        e = np.linalg.norm(vv - v.astype(np.float64), axis=1)
+        if vb == 3:
+            bound = np.sqrt(((b["v_r"][:, None] * b["v_s"][None, :] * b["v_delta"][:, None] / 2)
+                             ** 2).sum(1))
+            assert np.all(e <= bound * (1 + 1e-9))
+        err[vb] = np.linalg.norm(e)
+    assert err[4] < err[3] < err[2]
