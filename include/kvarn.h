@@ -159,7 +159,7 @@ typedef struct kvarn_layout {
   int32_t tile_tokens;    /* 128                                            */
   int32_t sinkhorn_iters; /* n, the fixed Sinkhorn round count (default 4)  */
   int32_t k_bits;         /* 4                                              */
-  int32_t v_bits;         /* 2 (4 for the k4v4 variant, kvarn_layout_ex)    */
+  int32_t v_bits;         /* 2 (3 or 4 for the variants of kvarn_layout_ex) */
   int32_t v_group;        /* min(D, 128) channels per V quantisation group  */
   int32_t v_groups;       /* D / v_group                                    */
   int64_t record_bytes;
@@ -192,16 +192,19 @@ int kvarn_layout_scales(int head_dim, int sinkhorn_iters, int scale_bits, kvarn_
 
 /*
  * The record layout with scale fields of scale_bits bits (32 or 16, as in
- * kvarn_layout_scales) and v_bits-bit value codes: 2 gives the k4v2 layouts
- * above; 4 gives a k4v4 variant (other key/value bit widths, gmlx PR #116):
- * values quantised per token and 128-channel group to 16 levels
- * (delta = (max - min) / 15), packed token-major like the 2-bit codes with two
- * channels per byte: channel c of token t in bits 4 (c % 2) .. +3 of byte
- * t * (D / 2) + c / 2 (off_v_codes, D / 2 bytes per token). The keys, the
- * Sinkhorn factors and the field order are unchanged. record_bytes = 128 D +
- * SB (4 D + 256 + 256 Gv), SB = scale_bits / 8: 20480 at D=128 with fp32
- * scales. kvarn_compress_tile, the decode entry points and the prefill
- * entry points accept it.
+ * kvarn_layout_scales) and v_bits-bit value codes (other key/value bit
+ * widths, gmlx PR #116): 2 gives the k4v2 layouts above; 3 and 4 give k4v3
+ * and k4v4 variants, values quantised per token and 128-channel group to
+ * 2^v_bits levels (delta = (max - min) / (2^v_bits - 1)). Every width packs
+ * a token's value codes as a little-endian bit stream of D * v_bits / 8
+ * bytes at off_v_codes + t * D * v_bits / 8: channel c occupies stream bits
+ * v_bits * c .. v_bits * c + v_bits - 1, stream bit i being bit i % 8 of
+ * byte i / 8 (for 2 and 4 bits: the (c % (8 / v_bits))-th field of byte
+ * c / (8 / v_bits); a 3-bit code can straddle two bytes). The keys, the
+ * Sinkhorn factors and the field order are unchanged. record_bytes = 64 D +
+ * 16 v_bits D + SB (4 D + 256 + 256 Gv), SB = scale_bits / 8: 18432 (k4v3)
+ * and 20480 (k4v4) at D=128 with fp32 scales. kvarn_compress_tile, the
+ * decode entry points and the prefill entry points accept all of them.
  * Returns KVARN_ERR_UNSUPPORTED for other head dims, iteration counts,
  * scale_bits or v_bits.
  */

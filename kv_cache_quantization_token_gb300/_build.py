@@ -11,13 +11,15 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkvarn.so")
-# (source, object, extra flags): decode.cu is built four times, for records
-# with fp32 or binary16 scale fields and with 2-bit or 4-bit value codes.
+# (source, object, extra flags): decode.cu is built six times, for records
+# with fp32 or binary16 scale fields and with 2-, 3- or 4-bit value codes.
 UNITS = [("kvarn_abi.cu", "kvarn_abi.o", []), ("compress.cu", "compress.o", []),
          ("window.cu", "window.o", []), ("decode.cu", "decode.o", []),
          ("decode.cu", "decode_sb2.o", ["-DKVARN_BUILD_SCALE_BYTES=2"]),
          ("decode.cu", "decode_v4.o", ["-DKVARN_BUILD_V_BITS=4"]),
          ("decode.cu", "decode_sb2_v4.o", ["-DKVARN_BUILD_SCALE_BYTES=2", "-DKVARN_BUILD_V_BITS=4"]),
+         ("decode.cu", "decode_v3.o", ["-DKVARN_BUILD_V_BITS=3"]),
+         ("decode.cu", "decode_sb2_v3.o", ["-DKVARN_BUILD_SCALE_BYTES=2", "-DKVARN_BUILD_V_BITS=3"]),
          ("decode_noalloc.cu", "decode_noalloc.o", []), ("prefill.cu", "prefill.o", [])]
 SOURCES = sorted({u[0] for u in UNITS})
 HEADERS = [os.path.join(CSRC, "kvarn_common.cuh"), os.path.join(ROOT, "include", "kvarn.h")]

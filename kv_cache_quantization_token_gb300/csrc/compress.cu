@@ -5,7 +5,7 @@
 // steps 1-3; SharpInference PR #434, commit 82efc4f):
 //   1. Walsh-Hadamard rotation of each token row along head_dim,
 //   2. n rounds of dual-axis std normalisation, channel step first,
-//   3. asymmetric RTN: K 4-bit per channel over the tile's tokens, V 2-bit per
+//   3. asymmetric RTN: K 4-bit per channel over the tile's tokens, V 2-bit (3 or 4 in the variants) per
 //      token over 128-channel groups; codes packed into the record.
 //
 // GPU formulation (same result up to rounding as the log-space statement):
@@ -457,6 +457,40 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
         w |= __shfl_xor_sync(0xffffffffu, w, 2);
         if ((i & 3) == (cg & 3))
           *reinterpret_cast<unsigned long long*>(stage + R::kVCodes + t * R::kVRow + 8 * (cg >> 2)) = w;
+      } else if constexpr (VB == 3) {
+        // 3-bit codes: the token row is a bit stream, channel c at bits 3 c.
+        // Channel 32 (cg >> 2) + 4 m + q (q = cg & 3) of slot m sits at bit
+        // 12 m + 3 q of the 96-bit run of its 32-channel block, which starts
+        // at byte 12 (cg >> 2) of the row; the four lanes of a channel
+        // quadruple assemble the run together (bits 0..63 and 64..95).
+        const int q = cg & 3;
+        unsigned long long lo64 = 0ull;
+        uint32_t hi32 = 0u;
+        auto place = [&](uint32_t c, int m) {
+          const int b = 12 * m + 3 * q;
+          if (b < 64) {
+            lo64 |= (unsigned long long)c << b;
+            if (b > 61) hi32 |= c >> (64 - b);  // the code straddles bit 64
+          } else {
+            hi32 |= c << (b - 64);
+          }
+        };
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
+          place(floor_bits(u.x) & 7u, 2 * k);
+          place(floor_bits(u.y) & 7u, 2 * k + 1);
+        }
+        lo64 |= __shfl_xor_sync(0xffffffffu, lo64, 1);
+        hi32 |= __shfl_xor_sync(0xffffffffu, hi32, 1);
+        lo64 |= __shfl_xor_sync(0xffffffffu, lo64, 2);
+        hi32 |= __shfl_xor_sync(0xffffffffu, hi32, 2);
+        if ((i & 3) == q) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(stage + R::kVCodes + t * R::kVRow + 12 * (cg >> 2));
+          dst[0] = (uint32_t)lo64;
+          dst[1] = (uint32_t)(lo64 >> 32);
+          dst[2] = hi32;
+        }
       } else {
         // 4-bit codes: channel 32 (cg >> 2) + 4 m + (cg & 3) sits in byte
         // 16 (cg >> 2) + 2 m + ((cg & 3) >> 1), nibble (cg & 3) & 1; the four
@@ -546,6 +580,8 @@ cudaError_t launch_compress(int D, int iters, int scale_bytes, int v_bits, const
     case 22: return launch_compress_sb<2, 2>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
     case 44: return launch_compress_sb<4, 4>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
     case 24: return launch_compress_sb<2, 4>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 43: return launch_compress_sb<4, 3>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
+    case 23: return launch_compress_sb<2, 3>(D, iters, k_raw, v_raw, row_stride, n_rows, src_row0, tiles, tiles_bytes, dst_record, n_units, err, st);
     default: return cudaErrorInvalidValue;
   }
 }

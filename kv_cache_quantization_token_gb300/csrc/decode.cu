@@ -35,10 +35,10 @@
 
 #include "kvarn_common.cuh"
 
-// Built four times: for records with fp32 or binary16 scale fields
-// (KVARN_BUILD_SCALE_BYTES 4 or 2) and 2-bit or 4-bit value codes (KVARN_BUILD_V_BITS 2
-// or 4). The fp32 / 2-bit unit also holds the plan, the combine kernel and
-// the dispatch.
+// Built six times: for records with fp32 or binary16 scale fields
+// (KVARN_BUILD_SCALE_BYTES 4 or 2) and 2-, 3- or 4-bit value codes
+// (KVARN_BUILD_V_BITS). The fp32 / 2-bit unit also holds the plan, the
+// combine kernel and the dispatch.
 #ifndef KVARN_BUILD_SCALE_BYTES
 #define KVARN_BUILD_SCALE_BYTES 4
 #endif
@@ -52,6 +52,9 @@ namespace {
 
 constexpr int kSB = KVARN_BUILD_SCALE_BYTES;
 constexpr int kVB = KVARN_BUILD_V_BITS;
+// Width of the value codes the value contraction reads: 3-bit records are
+// repacked into 4-bit codes in shared memory first (see repack_v3_to_v4).
+constexpr int kVF = kVB == 3 ? 4 : kVB;
 
 constexpr float kNegInf = -INFINITY;
 constexpr float kLog2eD = 1.4426950408889634f;
@@ -284,6 +287,36 @@ __device__ __forceinline__ void rotate_head_pairs(const float* qh, bool valid, f
   if (lane == 0) qmax[h] = mx;
 }
 
+// Eight 3-bit fields of x (bits 3i..3i+2) to eight 4-bit ones (bits 4i..).
+__device__ __forceinline__ uint32_t spread3to4(uint32_t x) {
+  uint32_t y = (x & 0xFFFu) | ((x & 0xFFF000u) << 4);     // fields 4-7 to the high half-word
+  y = (y & 0x003F003Fu) | ((y & 0x0FC00FC0u) << 2);        // fields 2, 3 (6, 7) to the next byte
+  return (y & 0x07070707u) | ((y & 0x38383838u) << 1);     // the odd field of each byte up a bit
+}
+
+// 3-bit value codes of a landed record (token rows of 3 D / 8 bytes at 64 D,
+// a little-endian bit stream per row) rewritten as 4-bit rows of D / 2 bytes
+// at offset 0, over the K codes; both regions carry the record box's 128-byte
+// swizzle (64 D is a multiple of 1024, so offsets map alike). Thread `id` of
+// `nth` converts 32-channel blocks: 12 bytes in, 16 bytes out.
+template <int D>
+__device__ __forceinline__ void repack_v3_to_v4(unsigned char* slot, int id, int nth) {
+  constexpr int CB = D / 32;  // 32-channel blocks per token
+  for (int u = id; u < 128 * CB; u += nth) {
+    const int t = u / CB, cb = u % CB;
+    const uint32_t src = (uint32_t)(64 * D + t * (3 * D / 8) + 12 * cb);
+    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(slot + swz128(src));
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(slot + swz128(src + 4));
+    const uint32_t w2 = *reinterpret_cast<const uint32_t*>(slot + swz128(src + 8));
+    uint4 o;
+    o.x = spread3to4(w0 & 0xFFFFFFu);
+    o.y = spread3to4((w0 >> 24) | ((w1 & 0xFFFFu) << 8));
+    o.z = spread3to4((w1 >> 16) | ((w2 & 0xFFu) << 16));
+    o.w = spread3to4(w2 >> 8);
+    *reinterpret_cast<uint4*>(slot + swz128((uint32_t)(t * (D / 2) + 16 * cb))) = o;
+  }
+}
+
 template <int D, int GP, int NW_, int WPT_, bool MR_ = false>
 struct DC {
   static constexpr int NW = NW_;                                // warps per CTA (2, 4 or 8)
@@ -302,10 +335,15 @@ struct DC {
   static constexpr int HB = NCB / WPT;                          // blocks whose B fragments a warp builds
   // value contraction: slices of VSL channels of a V row, MU m-blocks of 16
   // channels each; lane group g8 owns channels VSL sl + CPL g8 + 2 mu + {0, 1}
-  static constexpr int VSL = kVB == 2 ? 64 : 32;
+  static constexpr int VSL = kVF == 2 ? 64 : 32;
   static constexpr int NS = D / VSL;
-  static constexpr int MU = kVB == 2 ? 4 : 2;
-  static constexpr int CPL = kVB == 2 ? 8 : 4;
+  static constexpr int MU = kVF == 2 ? 4 : 2;
+  static constexpr int CPL = kVF == 2 ? 8 : 4;
+  // where the value contraction finds its codes in a record slot, and the
+  // bytes per token row there: 3-bit codes are repacked into 4-bit rows over
+  // the K codes (dead once the scores are formed; the same 64 D bytes)
+  static constexpr int V_OFF = kVB == 3 ? 0 : K_BYTES;
+  static constexpr int V_ROW = kVF * D / 8;
   // window rows staged per warp, sized by the record region of the fp32
   // layout (two slots per group with multi-round items), whatever the scale width
   static constexpr int WCH0 = ((MR_ ? 2 : 1) * TPS * Rec<D, 4>::kBytes) / (NW * 2 * D * 4);
@@ -876,7 +914,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int m = 4; m < 32; m <<= 1) pm[nt] = fmaxf(pm[nt], __shfl_xor_sync(0xffffffffu, pm[nt], m));
         float sc2, inv2;
-        pow2_scale(pm[nt], kVB == 2 ? 4.0f : 16.0f, sc2, inv2);
+        pow2_scale(pm[nt], kVF == 2 ? 4.0f : 16.0f, sc2, inv2);
         float sp = 0.f;
 #pragma unroll
         for (int w2 = 0; w2 < CH; ++w2)
@@ -900,12 +938,20 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       }
     }
 
+    if constexpr (kVB == 3) {
+      // every warp of the group is past its reads of the K codes: the value
+      // codes go over them as 4-bit rows, then the group reads those
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");
+      repack_v3_to_v4<D>(const_cast<unsigned char*>(Rk), 32 * half + lane, 32 * WPT);
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");
+    }
+
     // ---- phase B: this warp's 32 CH tokens against all channels, one slice of
     // VSL channels of the V rows at a time. 2-bit codes: m-block mu of slice sl
     // row g8 <-> channel 64 sl + 8 g8 + 2 mu, row g8 + 8 <-> that channel + 1;
     // 4-bit codes: row g8 <-> channel 32 sl + 4 g8 + 2 mu, row g8 + 8 <-> + 1.
     const uint32_t vaddr0 =
-        (uint32_t)(C::K_BYTES + (32 * CH * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * R::kVRow);
+        (uint32_t)(C::V_OFF + (32 * CH * half + 4 * ri + 2 * (mi >> 1) + (mi & 1)) * C::V_ROW);
 #pragma unroll
     for (int sl = 0; sl < NS; ++sl) {
       const int gv = (C::VSL * sl) / R::kVGroup;
@@ -919,7 +965,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
       for (int w2 = 0; w2 < CH; ++w2) {
         uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
-        ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * R::kVRow + 16 * sl)), y[0], y[1], y[2],
+        ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * C::V_ROW + 16 * sl)), y[0], y[1], y[2],
                   y[3]);
         const uint32_t y8[4] = {y[0] >> 8, y[1] >> 8, y[2] >> 8, y[3] >> 8};
 #pragma unroll
@@ -927,7 +973,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint32_t a0, a1, a2, a3;
-            if constexpr (kVB == 2) {
+            if constexpr (kVF == 2) {
               // fields 2 mu and 2 mu + 1: fields 0..3 of y, or of y >> 8 for mu >= 2
               const uint32_t ya = mu < 2 ? y[2 * j] : y8[2 * j];
               const uint32_t yb = mu < 2 ? y[2 * j + 1] : y8[2 * j + 1];
@@ -1326,6 +1372,8 @@ cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* 
     case 22: return launch_decode_split_sb2_v2(p, a, ws, st);
     case 44: return launch_decode_split_sb4_v4(p, a, ws, st);
     case 24: return launch_decode_split_sb2_v4(p, a, ws, st);
+    case 43: return launch_decode_split_sb4_v3(p, a, ws, st);
+    case 23: return launch_decode_split_sb2_v3(p, a, ws, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1356,8 +1404,14 @@ cudaError_t launch_decode_split_sb2_v2(const DecodePlan& p, const DecodeArgs& a,
 #elif KVARN_BUILD_SCALE_BYTES == 4 && KVARN_BUILD_V_BITS == 4
 cudaError_t launch_decode_split_sb4_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st) {
-#else
+#elif KVARN_BUILD_SCALE_BYTES == 2 && KVARN_BUILD_V_BITS == 4
 cudaError_t launch_decode_split_sb2_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
+#elif KVARN_BUILD_SCALE_BYTES == 4 && KVARN_BUILD_V_BITS == 3
+cudaError_t launch_decode_split_sb4_v3(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st) {
+#else
+cudaError_t launch_decode_split_sb2_v3(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st) {
 #endif
   if (p.items == 0) return cudaSuccess;

@@ -54,7 +54,7 @@ bool layout_ok(const kvarn_layout_t* L) {
   if (L->version != KVARN_LAYOUT_VERSION && L->version != KVARN_LAYOUT_VERSION_F16_SCALES)
     return false;
   if (L->sinkhorn_iters < 1 || L->sinkhorn_iters > 16) return false;
-  if (L->v_bits != 2 && L->v_bits != 4) return false;
+  if (L->v_bits < 2 || L->v_bits > 4) return false;
   kvarn_layout_t ref;
   fill_layout(L->head_dim, L->sinkhorn_iters, scale_bytes_of(L), L->v_bits, &ref);
   return memcmp(&ref, L, sizeof(ref)) == 0;
@@ -123,7 +123,7 @@ int kvarn_layout_ex(int head_dim, int sinkhorn_iters, int scale_bits, int v_bits
                     kvarn_layout_t* out) {
   if (!out) return KVARN_ERR_NULL;
   if (!supported_dim(head_dim) || sinkhorn_iters < 1 || sinkhorn_iters > 16 ||
-      (scale_bits != 32 && scale_bits != 16) || (v_bits != 2 && v_bits != 4))
+      (scale_bits != 32 && scale_bits != 16) || v_bits < 2 || v_bits > 4)
     return KVARN_ERR_UNSUPPORTED;
   return fill_layout(head_dim, sinkhorn_iters, scale_bits / 8, v_bits, out);
 }

@@ -16,13 +16,14 @@ constexpr int kTile = KVARN_TILE_TOKENS;  // tokens per compressed tile
 
 // Byte offsets of the record fields for head_dim D with scale fields of SB
 // bytes, 4 (fp32, layout version 1) or 2 (IEEE binary16, layout version 2),
-// and VB-bit value codes, 2 (the k4v2 preset) or 4 (the k4v4 variant: the
-// same token-major packing, two channels per byte). Same values as
+// and VB-bit value codes, 2 (the k4v2 preset), 3 or 4 (the k4v3 and k4v4
+// variants): each token's value codes are a little-endian bit stream, channel
+// c at bits VB*c .. (a 3-bit code can straddle two bytes). Same values as
 // kvarn_layout_ex(); kept as constexpr so the kernels index without a struct.
 template <int D, int SB = 4, int VB = 2>
 struct Rec {
   static_assert(SB == 4 || SB == 2, "scale field width");
-  static_assert(VB == 2 || VB == 4, "value code width");
+  static_assert(VB == 2 || VB == 3 || VB == 4, "value code width");
   static constexpr int kSB = SB;
   static constexpr int kVB = VB;
   static constexpr int kGv = D / (D < 128 ? D : 128);     // V groups per token
@@ -222,8 +223,8 @@ int decode_plan(int B, int Hq, int Hkv, int D, int max_tiles, int win_capacity, 
 cudaError_t launch_decode_split(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                 cudaStream_t st);
 // the split kernels for records with fp32 (sb4) or binary16 (sb2) scale
-// fields and 2-bit (v2) or 4-bit (v4) value codes, built as four translation
-// units of decode.cu
+// fields and 2-, 3- or 4-bit (v2, v3, v4) value codes, built as six
+// translation units of decode.cu
 cudaError_t launch_decode_split_sb4_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st);
 cudaError_t launch_decode_split_sb2_v2(const DecodePlan& p, const DecodeArgs& a, void* ws,
@@ -231,6 +232,10 @@ cudaError_t launch_decode_split_sb2_v2(const DecodePlan& p, const DecodeArgs& a,
 cudaError_t launch_decode_split_sb4_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st);
 cudaError_t launch_decode_split_sb2_v4(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
+cudaError_t launch_decode_split_sb4_v3(const DecodePlan& p, const DecodeArgs& a, void* ws,
+                                       cudaStream_t st);
+cudaError_t launch_decode_split_sb2_v3(const DecodePlan& p, const DecodeArgs& a, void* ws,
                                        cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodePlan& p, int B, int Hq, int D, const void* ws,
                                   float* out, unsigned flags, cudaStream_t st);

@@ -447,6 +447,30 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
       const int t = row;
       const float r = sc_ld<SB>(vR, t);
       const unsigned char* vrow = rec + R::kVCodes + t * R::kVRow;
+      if constexpr (VB == 3) {
+        // 3-bit codes: the row is a little-endian bit stream, eight channels
+        // in every three bytes; this thread's half of the channels starts at
+        // byte 3 D / 16 half
+        constexpr int HC = D / 2;
+        const unsigned char* hb = vrow + half * (3 * HC / 8);
+#pragma unroll 4
+        for (int j8 = 0; j8 < HC / 8; ++j8) {
+          const uint32_t w = (uint32_t)hb[3 * j8] | ((uint32_t)hb[3 * j8 + 1] << 8) |
+                             ((uint32_t)hb[3 * j8 + 2] << 16);
+          const int c0 = half * HC + 8 * j8;
+          const int g = c0 / R::kVGroup;
+          const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int c = c0 + e;
+            const float v = sc_ld<SB>(vS, c) * fmaf(d, (float)((w >> (3 * e)) & 7u), lo);
+            const __half h = __float2half_rn(v);
+            const uint32_t o = sw_off(c, t, D);
+            *reinterpret_cast<__half*>(sH + o) = h;
+            *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
+          }
+        }
+      } else {
       constexpr int CPB = 8 / VB;               // channels per code byte
       constexpr int HB = R::kVRow / 2;          // code bytes of half a token row
       uint32_t vw[HB / 4];                      // read with wide loads
@@ -476,6 +500,7 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
           *reinterpret_cast<__half*>(sH + o) = h;
           *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
         }
+      }
       }
     }
   } else if (half == 1) {  // V row -> column `row` of V~^T
@@ -1348,6 +1373,12 @@ cudaError_t launch_prefill(const float* q, int C, int64_t pos0, const uint8_t* t
     case 25622: return launch_prefill_d<256, 2, 2>(a, st);
     case 25644: return launch_prefill_d<256, 4, 4>(a, st);
     case 25624: return launch_prefill_d<256, 2, 4>(a, st);
+    case 6443: return launch_prefill_d<64, 4, 3>(a, st);
+    case 6423: return launch_prefill_d<64, 2, 3>(a, st);
+    case 12843: return launch_prefill_d<128, 4, 3>(a, st);
+    case 12823: return launch_prefill_d<128, 2, 3>(a, st);
+    case 25643: return launch_prefill_d<256, 4, 3>(a, st);
+    case 25623: return launch_prefill_d<256, 2, 3>(a, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -176,8 +176,18 @@ def test_v4_layout_agrees_with_oracle(lib, D):
         assert L.v_bits == 4 and L.record_bytes == oracle.record_bytes(D, sb, 4)
         assert L.off_k_delta == 128 * D and L.record_bytes % 128 == 0
     M = kvarn.Layout()
-    assert lib.kvarn_layout_ex(D, 4, 32, 3, ctypes.byref(M)) == -3
+    assert lib.kvarn_layout_ex(D, 4, 32, 1, ctypes.byref(M)) == -3
     assert lib.kvarn_layout_ex(D, 4, 32, 8, ctypes.byref(M)) == -3
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_v3_layout_agrees_with_oracle(lib, D):
+    """k4v3: token rows of 3 D / 8 bytes (a bit stream); the library's layout
+    and the oracle's record size agree."""
+    for sb in (32, 16):
+        L = kvarn.layout(D, scale_bits=sb, v_bits=3)
+        assert L.v_bits == 3 and L.record_bytes == oracle.record_bytes(D, sb, 3)
+        assert L.off_k_delta == 112 * D and L.record_bytes % 128 == 0
 
 
 def test_prefill_accepts_v4_records(lib):

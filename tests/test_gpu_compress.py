@@ -171,3 +171,31 @@ def test_compress_v4_matches_oracle(workload, D, n_heads, n_tiles, sb):
         st = compare_record(rec, ref, D, v_bits=4) if sb == 32 else compare_record_f16(rec, ref, D, 4)
         flips += st["band_flips"]
     print(f"{workload} D{D} k4v4 sb{sb}: {flips} boundary-band flips")
+
+
+@pytest.mark.parametrize("workload,D,n_heads,n_tiles,sb", [("qwen3_8b_decode", 128, 2, 4, 32),
+                                                          ("batched_d256_decode", 256, 2, 3, 32),
+                                                          ("single_tile", 64, 1, 2, 32),
+                                                          ("qwen3_8b_decode", 128, 1, 3, 16)])
+def test_compress_v3_matches_oracle(workload, D, n_heads, n_tiles, sb):
+    """The k4v3 variant: 3-bit values (8 levels per token group), each token
+    row a bit stream in which 3-bit codes straddle bytes; keys as in k4v2."""
+    from tests.kvarn_helpers import compare_record_f16
+    ks, vs = synth.kv_layer(workload, 9, n_heads, 128 * n_tiles, D)
+    k_rows, v_rows = ks.reshape(-1, D), vs.reshape(-1, D)
+    units = [128 * i for i in range(n_heads * n_tiles)]
+    lay = kvarn.layout(D, scale_bits=sb, v_bits=3)
+    rb = lay.record_bytes
+    assert rb == oracle.record_bytes(D, sb, 3)
+    tiles = torch.full((len(units) * rb,), 0xAB, dtype=torch.uint8, device=DEV)
+    kvarn.compress_tile(torch.from_numpy(k_rows).to(DEV), torch.from_numpy(v_rows).to(DEV),
+                        torch.tensor(units, dtype=torch.int64, device=DEV), tiles,
+                        torch.arange(len(units), dtype=torch.int64, device=DEV) * rb, lay)
+    host = tiles.cpu().numpy()
+    flips = 0
+    for i, u in enumerate(units):
+        ref = oracle.compress_unit(k_rows[u:u + 128], v_rows[u:u + 128], scale_bits=sb, v_bits=3)
+        rec = host[i * rb:(i + 1) * rb]
+        st = compare_record(rec, ref, D, v_bits=3) if sb == 32 else compare_record_f16(rec, ref, D, 3)
+        flips += st["band_flips"]
+    print(f"{workload} D{D} k4v3 sb{sb}: {flips} boundary-band flips")

@@ -208,3 +208,24 @@ def test_v4_records_multi_round(D, Hq, Hkv, ctx):
     c = Cache("qwen3_8b_decode", 17, [ctx], Hkv=Hkv, D=D, v_bits=4)
     _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])
 
+
+@pytest.mark.parametrize("workload,ctxs,Hq,Hkv,D,sb", [("single_tile", [128 + 17], 1, 1, 128, 32),
+                                                      ("qwen3_8b_decode", [16384 + 40], 32, 8, 128, 32),
+                                                      ("qwen3_8b_decode", [600, 1000], 8, 1, 128, 16),
+                                                      ("batched_d256_decode", [900, 128 * 5 + 3], 16, 4, 256, 32),
+                                                      ("single_tile", [128 * 3 + 50], 4, 2, 64, 32)])
+def test_v3_records(workload, ctxs, Hq, Hkv, D, sb):
+    """Decode over k4v3 records (3-bit values straddling bytes, 18,432-byte
+    records at head_dim 128 with fp32 scales): after the scores, the warp
+    group rewrites a record's value codes as 4-bit rows over its K codes and
+    the value contraction reads those; the oracle dequantises the records."""
+    c = Cache(workload, 18, ctxs, Hkv=Hkv, D=D, scale_bits=sb, v_bits=3)
+    heads = [(b, h) for b in range(len(ctxs)) for h in range(0, Hq, max(1, Hq // 4))]
+    _check(c, Hq=Hq, heads=heads)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,ctx", [(128, 8, 1, 128 * 1400 + 9), (256, 16, 4, 128 * 460 + 77)])
+def test_v3_records_multi_round(D, Hq, Hkv, ctx):
+    """The multi-round split kernel (records double-buffered) on k4v3 records."""
+    c = Cache("qwen3_8b_decode", 19, [ctx], Hkv=Hkv, D=D, v_bits=3)
+    _check(c, Hq=Hq, heads=[(0, h) for h in range(0, Hq, 5)])

@@ -89,14 +89,17 @@ def test_prefill_cached_images_match_uncached(Hq, Hkv, D, n, chunk, W, sb):
     b.check(last, _rows(b.snap[last]["C"], range(0, Hq, 5), step=29))
 
 
-@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W,sb,cached", [(32, 8, 128, 1400, 512, 256, 32, True),
-                                                         (8, 8, 64, 700, 256, 128, 32, False),
-                                                         (16, 2, 128, 900, 300, 256, 16, True)])
-def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W,sb,cached,vb", [(32, 8, 128, 1400, 512, 256, 32, True, 4),
+                                                            (8, 8, 64, 700, 256, 128, 32, False, 4),
+                                                            (16, 2, 128, 900, 300, 256, 16, True, 4),
+                                                            (32, 8, 128, 1400, 512, 256, 32, True, 3),
+                                                            (8, 8, 64, 700, 256, 128, 16, False, 3)])
+def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached, vb):
     """Chunked prefill over k4v4 records (4-bit value codes, two channels per
-    byte), with fp32 or f16 scale fields, cached or per-chunk images."""
+    byte) and k4v3 records (3-bit codes straddling bytes), with fp32 or f16
+    scale fields, cached or per-chunk images."""
     run = PrefillRun("qwen3_8b_prefill", 7, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk,
-                     scale_bits=sb, v_bits=4, cached=cached)
+                     scale_bits=sb, v_bits=vb, cached=cached)
     for p in run.snap:
         run.check(p, _rows(run.snap[p]["C"], range(0, Hq, 3), step=23))
 
@@ -106,6 +109,7 @@ def test_prefill_v4_records(Hq, Hkv, D, n, chunk, W, sb, cached):
     (16, 4, 1400, 512, 256, 32, 2, True),
     (16, 2, 700, 256, 256, 16, 2, True),     # GQA group 8, f16 scales
     (4, 4, 450, 100, 128, 32, 4, False),     # group 1, k4v4, ragged chunks, window wraps
+    (8, 4, 700, 256, 256, 32, 3, True),      # k4v3 records
     (32, 8, 1100, 512, 256, 32, 2, False),   # 128 row blocks: no key split
 ])
 def test_prefill_head_dim_256(Hq, Hkv, n, chunk, W, sb, vb, cached):
