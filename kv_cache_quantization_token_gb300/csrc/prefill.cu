@@ -76,6 +76,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// The descriptor of the operand `bytes` further on (16-byte multiple): the
+// start address field holds address / 16 in 14 bits, and every shared
+// address here stays below 256 KB, so the sum never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
 // Instruction descriptor, kind::f16: D f32, A and B f16, both K-major, M = 128.
 template <int N>
 __device__ __forceinline__ uint32_t idesc() {
@@ -98,6 +104,19 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uin
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
       "r"(tmem_a), "l"(b), "r"(id), "r"(accumulate));
 }
+// The TS product that always accumulates into D.
+__device__ __forceinline__ void mma_f16_ts_acc(uint32_t tmem_d, uint32_t tmem_a, uint64_t b,
+                                               uint32_t id) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;\n" ::"r"(tmem_d),
+               "r"(tmem_a), "l"(b), "r"(id));
+}
+// One lane of a converged warp (the same lane every time the warp is whole).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(pred));
+  return pred != 0;
+}
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    su32(bar))
@@ -115,6 +134,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ bool mbar_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail,
                                                unsigned* err) {
   return mbar_wait_timed(bar, parity, err, KVARN_DEVERR_WAIT, fail);
+}
+// mbar_wait_flag for a whole warp: one elected lane polls (32 lanes polling
+// one barrier cost the MMA issuer more than the product queue holds), the
+// warp leaves together, and __syncwarp orders the other lanes after the
+// elected lane's acquire. True when the phase completed.
+__device__ __forceinline__ bool warp_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail,
+                                               unsigned* err) {
+  bool ok = true;
+  if (elect_one()) ok = mbar_wait_flag(bar, parity, fail, err);
+  ok = __ballot_sync(0xffffffffu, !ok) == 0u;
+  __syncwarp();
+  return ok;
+}
+// The same for two barriers at once.
+__device__ __forceinline__ bool warp_wait_flag2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1,
+                                                uint32_t parity1, volatile int* fail, unsigned* err) {
+  bool ok = true;
+  if (elect_one())
+    ok = mbar_wait_flag(bar0, parity0, fail, err) && mbar_wait_flag(bar1, parity1, fail, err);
+  ok = __ballot_sync(0xffffffffu, !ok) == 0u;
+  __syncwarp();
+  return ok;
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
@@ -689,25 +730,33 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ---------------- MMA issuer
-    if (lane == 0 && n_blk > 0) {
+    // ---------------- MMA issuer. The whole warp runs the loop, so operand
+    // addresses stay warp-uniform, and one elected lane issues each group of
+    // products with its commit: a lone lane computing them while two softmax
+    // warps share its scheduler falls behind an N = 128 product chain.
+    if (n_blk > 0) {
       uint64_t* last = nullptr;  // the most recent commit, drained on the way out
       uint32_t last_par = 0;
+      const uint64_t dk = sdesc(su32(sK)), dvh = sdesc(su32(sV)), dvl = sdesc_add(dvh, P::OPB);
       auto issue_s = [&](int j) -> bool {
         const int b = j & 1;
-        if (!mbar_wait_flag(bar_k + b, (uint32_t)(j >> 1) & 1u, fail, a.err)) return false;
+        if (!warp_wait_flag(bar_k + b, (uint32_t)(j >> 1) & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_s = tmem + P::T_S + 128 * b;
-        const uint32_t kh = su32(sK + b * 2 * P::OPB), kl = kh + P::OPB;
+        const uint64_t kh = sdesc_add(dk, b * 2 * P::OPB), kl = sdesc_add(kh, P::OPB);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          const uint32_t qh = tmem + P::T_QH + 8 * kk, ql = tmem + P::T_QL + 8 * kk;
-          mma_f16_ts(t_s, qh, sdesc(kh + off), idesc<128>(), kk > 0);
-          mma_f16_ts(t_s, ql, sdesc(kh + off), idesc<128>(), 1);
-          mma_f16_ts(t_s, qh, sdesc(kl + off), idesc<128>(), 1);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+            const uint32_t qh = tmem + P::T_QH + 8 * kk, ql = tmem + P::T_QL + 8 * kk;
+            if (kk == 0) mma_f16_ts(t_s, qh, kh, idesc<128>(), 0);
+            else mma_f16_ts_acc(t_s, qh, sdesc_add(kh, off), idesc<128>());
+            mma_f16_ts_acc(t_s, ql, sdesc_add(kh, off), idesc<128>());
+            mma_f16_ts_acc(t_s, qh, sdesc_add(kl, off), idesc<128>());
+          }
+          mma_commit(bar_s + b);
         }
-        mma_commit(bar_s + b);
+        __syncwarp();
         last = bar_s + b; last_par = (uint32_t)(j >> 1) & 1u;
         return true;
       };
@@ -716,24 +765,30 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
         // S(j+1) goes in ahead of PV(j): its TMEM buffer held P(j-1), which
         // PV(j-1), issued earlier, reads first
         if (j + 1 < n_blk && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
-        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail, a.err)) break;
+        if (!warp_wait_flag2(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, bar_v, (uint32_t)j & 1u, fail,
+                             a.err))
+          break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 128 * (j & 1);
-        const uint32_t vh = su32(sV), vl = vh + P::OPB;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 16 keys each; keys 64 h .. are thread half h's
-          const uint32_t ph = t_p + 64 * (kk >> 2) + 8 * (kk & 3), pl = ph + 32;
-          const uint32_t off = (kk >> 2) * D * 128 + (kk & 3) * 32;
-          mma_f16_ts(t_o, ph, sdesc(vh + off), idesc<D>(), (j > 0 || kk > 0));
-          mma_f16_ts(t_o, pl, sdesc(vh + off), idesc<D>(), 1);
-          mma_f16_ts(t_o, ph, sdesc(vl + off), idesc<D>(), 1);
+          for (int kk = 0; kk < 8; ++kk) {  // 16 keys each; keys 64 h .. are thread half h's
+            const uint32_t ph = t_p + 64 * (kk >> 2) + 8 * (kk & 3), pl = ph + 32;
+            const uint32_t off = (kk >> 2) * D * 128 + (kk & 3) * 32;
+            if (kk == 0) mma_f16_ts(t_o, ph, dvh, idesc<D>(), j > 0);
+            else mma_f16_ts_acc(t_o, ph, sdesc_add(dvh, off), idesc<D>());
+            mma_f16_ts_acc(t_o, pl, sdesc_add(dvh, off), idesc<D>());
+            mma_f16_ts_acc(t_o, ph, sdesc_add(dvl, off), idesc<D>());
+          }
+          mma_commit(bar_o);
         }
-        mma_commit(bar_o);
+        __syncwarp();
         last = bar_o; last_par = (uint32_t)j & 1u;
       }
       // the tensor pipe completes in order: the last commit covers everything
-      if (last != nullptr && !mbar_wait_bounded(last, last_par, a.err)) *fail = 1;
+      if (last != nullptr &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(last, last_par, a.err)))
+        *fail = 1;
     }
     __syncwarp();
   } else {
@@ -1062,55 +1117,70 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ---------------- MMA issuer
-    if (lane == 0 && n_sub > 0) {
+    // ---------------- MMA issuer: the whole warp runs the loop and one
+    // elected lane issues (operand addresses stay warp-uniform)
+    if (n_sub > 0) {
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
+      const uint64_t dql = sdesc(su32(sQl)), dkh = sdesc(su32(sKh)), dkl = sdesc(su32(sKl));
+      const uint64_t dvh = sdesc(su32(sVh)), dvl = sdesc_add(dvh, P::VSB);
       auto issue_s = [&](int j) -> bool {
         const uint32_t t_s = tmem + P::T_S + 64 * (j & 1);
-        if (!mbar_wait_flag(bar_kh, (uint32_t)j & 1u, fail, a.err)) return false;
+        if (!warp_wait_flag(bar_kh, (uint32_t)j & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
-          const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
-          const uint32_t qh = tmem + P::T_QH + 8 * kk;
-          mma_f16_ts(t_s, qh, sdesc(su32(sKh) + off_b), idesc<64>(), kk > 0);
-          mma_f16(t_s, sdesc(su32(sQl) + off_a), sdesc(su32(sKh) + off_b), idesc<64>(), 1);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_a = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+            const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
+            const uint32_t qh = tmem + P::T_QH + 8 * kk;
+            if (kk == 0) mma_f16_ts(t_s, qh, dkh, idesc<64>(), 0);
+            else mma_f16_ts_acc(t_s, qh, sdesc_add(dkh, off_b), idesc<64>());
+            mma_f16(t_s, sdesc_add(dql, off_a), sdesc_add(dkh, off_b), idesc<64>(), 1);
+          }
+          mma_commit(bar_khf);
         }
-        mma_commit(bar_khf);
+        __syncwarp();
         last = bar_khf; last_par = (uint32_t)j & 1u;
-        if (!mbar_wait_flag(bar_kl, (uint32_t)j & 1u, fail, a.err)) return false;
+        if (!warp_wait_flag(bar_kl, (uint32_t)j & 1u, fail, a.err)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
-          mma_f16_ts(t_s, tmem + P::T_QH + 8 * kk, sdesc(su32(sKl) + off_b), idesc<64>(), 1);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_b = (kk >> 2) * 64 * 128 + (kk & 3) * 32;
+            mma_f16_ts_acc(t_s, tmem + P::T_QH + 8 * kk, sdesc_add(dkl, off_b), idesc<64>());
+          }
+          mma_commit(bar_s + (j & 1));
         }
-        mma_commit(bar_s + (j & 1));
+        __syncwarp();
         last = bar_s + (j & 1); last_par = (uint32_t)(j >> 1) & 1u;
         return true;
       };
       bool ok = issue_s(0);
       for (int j = 0; ok && j < n_sub; ++j) {
         if (j + 1 < n_sub && !issue_s(j + 1)) break;
-        if (!mbar_wait_flag(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
-        if (!mbar_wait_flag(bar_v, (uint32_t)j & 1u, fail, a.err)) break;
+        if (!warp_wait_flag2(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, bar_v, (uint32_t)j & 1u, fail,
+                             a.err))
+          break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 64 * (j & 1);
-        const uint32_t vh = su32(sVh), vl = vh + P::VSB;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 16 keys each; keys 32 h .. are thread half h's
-          const uint32_t ph = t_p + 32 * (kk >> 1) + 8 * (kk & 1), pl = ph + 16;
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          mma_f16_ts(t_o, ph, sdesc(vh + 32 * kk), idesc<256>(), acc);
-          mma_f16_ts(t_o, pl, sdesc(vh + 32 * kk), idesc<256>(), 1);
-          mma_f16_ts(t_o, ph, sdesc(vl + 32 * kk), idesc<256>(), 1);
+          for (int kk = 0; kk < 4; ++kk) {  // 16 keys each; keys 32 h .. are thread half h's
+            const uint32_t ph = t_p + 32 * (kk >> 1) + 8 * (kk & 1), pl = ph + 16;
+            if (kk == 0) mma_f16_ts(t_o, ph, dvh, idesc<256>(), j > 0);
+            else mma_f16_ts_acc(t_o, ph, sdesc_add(dvh, 32 * kk), idesc<256>());
+            mma_f16_ts_acc(t_o, pl, sdesc_add(dvh, 32 * kk), idesc<256>());
+            mma_f16_ts_acc(t_o, ph, sdesc_add(dvl, 32 * kk), idesc<256>());
+          }
+          mma_commit(bar_o);
         }
-        mma_commit(bar_o);
+        __syncwarp();
         last = bar_o; last_par = (uint32_t)j & 1u;
       }
-      if (last != nullptr && !mbar_wait_bounded(last, last_par, a.err)) *fail = 1;
+      if (last != nullptr &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(last, last_par, a.err)))
+        *fail = 1;
     }
     __syncwarp();
   } else {
