@@ -135,27 +135,16 @@ __device__ __forceinline__ bool mbar_wait_flag(uint64_t* bar, uint32_t parity, v
                                                unsigned* err) {
   return mbar_wait_timed(bar, parity, err, KVARN_DEVERR_WAIT, fail);
 }
-// mbar_wait_flag for a whole warp: one elected lane polls (32 lanes polling
-// one barrier cost the MMA issuer more than the product queue holds), the
-// warp leaves together, and __syncwarp orders the other lanes after the
-// elected lane's acquire. True when the phase completed.
+// mbar_wait_flag for a whole warp, which leaves together: true only when
+// every lane saw the phase complete.
 __device__ __forceinline__ bool warp_wait_flag(uint64_t* bar, uint32_t parity, volatile int* fail,
                                                unsigned* err) {
-  bool ok = true;
-  if (elect_one()) ok = mbar_wait_flag(bar, parity, fail, err);
-  ok = __ballot_sync(0xffffffffu, !ok) == 0u;
-  __syncwarp();
-  return ok;
+  return __all_sync(0xffffffffu, mbar_wait_flag(bar, parity, fail, err));
 }
-// The same for two barriers at once.
+// The same for two barriers, one after the other.
 __device__ __forceinline__ bool warp_wait_flag2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1,
                                                 uint32_t parity1, volatile int* fail, unsigned* err) {
-  bool ok = true;
-  if (elect_one())
-    ok = mbar_wait_flag(bar0, parity0, fail, err) && mbar_wait_flag(bar1, parity1, fail, err);
-  ok = __ballot_sync(0xffffffffu, !ok) == 0u;
-  __syncwarp();
-  return ok;
+  return warp_wait_flag(bar0, parity0, fail, err) && warp_wait_flag(bar1, parity1, fail, err);
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
@@ -317,8 +306,8 @@ struct PC {
   // attention kernel shared memory (head_dim <= 128; head_dim 256 uses PA256)
   static constexpr int OFF_K = 0;                        // [2 buffers][K~ hi | K~ lo], [128 keys][D]
   static constexpr int OFF_V = 4 * OPB;                  // V~^T hi | lo, [D][128 keys]
-  static constexpr int OFF_BAR = 6 * OPB;                // 8 mbarriers
-  static constexpr int OFF_XM = OFF_BAR + 64;            // float [2][2][128]: row-max exchange
+  static constexpr int OFF_BAR = 6 * OPB;                // 10 mbarriers
+  static constexpr int OFF_XM = OFF_BAR + 128;           // float [2][2][128]: row-max exchange
   static constexpr int OFF_XB = OFF_XM + 2 * 2 * 128 * 4; // int [2][8]: per-warp stop flags
   static constexpr int OFF_MISC = OFF_XB + 64;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;     // + slack to align the base to 1024
@@ -594,11 +583,14 @@ __device__ __forceinline__ bool pair_max(float mloc, bool bad, float* xm, int* x
 // attention over the block images of the chunk (head_dim 64 or 128)
 //
 // Warp roles: warps 0-7 run the softmax (two threads per score row) and the
-// epilogue, warp 8 issues the tcgen05 MMAs (one thread), warp 9 the bulk
-// copies (one thread). K~ is double-buffered in shared memory, V~^T single;
-// S is double-buffered in TMEM. The tensor pipe runs, in order, S(0), S(1),
-// PV(0), S(2), PV(1), ...; S(j+2) overwrites the TMEM columns that held P(j)
-// only after PV(j), which the pipe completes first.
+// epilogue, warp 8 issues the tcgen05 MMAs (one elected lane), warp 9 the
+// bulk copies (one thread). K~ is double-buffered in shared memory, V~^T
+// single but in two 64-key halves with barriers of their own: PV(j) commits
+// after its first half, and the first half of V~^T(j+1) streams in while the
+// second half of PV(j) runs. S is double-buffered in TMEM. The tensor pipe
+// runs, in order, S(0), S(1), PV(0), S(2), PV(1), ...; S(j+2) overwrites the
+// TMEM columns that held P(j) only after PV(j), which the pipe completes
+// first.
 template <int D>
 __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   using P = PC<D>;
@@ -608,13 +600,14 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   unsigned char* sK = sm + P::OFF_K;
   unsigned char* sV = sm + P::OFF_V;
   uint64_t* bar_k = reinterpret_cast<uint64_t*>(sm + P::OFF_BAR);  // [2] K~ of block j in buffer j & 1
-  uint64_t* bar_v = bar_k + 2;     // V~^T of block j landed
-  uint64_t* bar_s = bar_k + 3;     // [2] S(j) complete: scores ready, K~ buffer j & 1 free
-  uint64_t* bar_o = bar_k + 5;     // PV(j) complete: V~^T free, O current
+  uint64_t* bar_v = bar_k + 2;     // [2] key half h of V~^T(j) landed
+  uint64_t* bar_s = bar_k + 4;     // [2] S(j) complete: scores ready, K~ buffer j & 1 free
+  uint64_t* bar_o = bar_k + 6;     // PV(j) complete: V~^T free, O current
+  uint64_t* bar_vh = bar_k + 7;    // the first half of PV(j) complete: V~^T half 0 free
   // [2] P(j) in TMEM and O rescaled: one arrival per softmax warp, on the
   // barrier of the block's parity (a warp may run one block ahead of the
   // others; its arrival must not count toward the block before)
-  uint64_t* bar_p = bar_k + 6;
+  uint64_t* bar_p = bar_k + 8;
   float* xm = reinterpret_cast<float*>(sm + P::OFF_XM);
   int* xb = reinterpret_cast<int*>(sm + P::OFF_XB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P::OFF_MISC);
@@ -643,7 +636,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   };
 
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init1(bar_k + i);
+    for (int i = 0; i < 8; ++i) mbar_init1(bar_k + i);
     for (int i = 0; i < 2; ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(bar_p + i)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -663,20 +656,26 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
   const uint32_t lb = lane_base_of(warp);
 
   // the first copies go out while the query rows are prepared
-  int nk[2] = {0, 0}, nv = 0;  // copies issued per barrier (loader thread)
+  int nk[2] = {0, 0}, nv[2] = {0, 0};  // copies issued per barrier (loader thread)
   auto load_k = [&](int jj) {
     const int b = jj & 1;
     bulk_load(sK + b * 2 * P::OPB, image(jj), 2 * P::OPB, bar_k + b);
     ++nk[b];
   };
-  auto load_v = [&](int jj) {
-    bulk_load(sV, image(jj) + 2 * P::OPB, 2 * P::OPB, bar_v);
-    ++nv;
+  // keys 64 h .. 64 h + 63 of V~^T hi and lo: the h-th 64-key block of each
+  constexpr uint32_t kVHalf = D * 128;
+  auto load_v = [&](int jj, int h) {
+    const uint8_t* src = image(jj) + 2 * P::OPB + h * kVHalf;
+    mbar_expect_tx(bar_v + h, 2 * kVHalf);
+    bulk_copy_tx(sV + h * kVHalf, src, kVHalf, bar_v + h);
+    bulk_copy_tx(sV + P::OPB + h * kVHalf, src + P::OPB, kVHalf, bar_v + h);
+    ++nv[h];
   };
   if (warp == 9 && lane == 0 && n_blk > 0) {
     load_k(0);
     if (n_blk > 1) load_k(1);
-    load_v(0);
+    load_v(0, 0);
+    load_v(0, 1);
   }
   // Q' row into TMEM: rotate, scale, fp16 hi + lo (one thread per row)
   if (tid < 128) {
@@ -719,14 +718,17 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
           load_k(j + 2);
         }
         if (j + 1 < n_blk) {
+          if (!mbar_wait_flag(bar_vh, (uint32_t)j & 1u, fail, a.err)) break;
+          load_v(j + 1, 0);
           if (!mbar_wait_flag(bar_o, (uint32_t)j & 1u, fail, a.err)) break;
-          load_v(j + 1);
+          load_v(j + 1, 1);
         }
       }
       // every copy issued has landed before the CTA can retire
-      for (int b = 0; b < 2; ++b)
+      for (int b = 0; b < 2; ++b) {
         if (nk[b] > 0) mbar_wait_bounded(bar_k + b, (uint32_t)(nk[b] - 1) & 1u, a.err);
-      if (nv > 0) mbar_wait_bounded(bar_v, (uint32_t)(nv - 1) & 1u, a.err);
+        if (nv[b] > 0) mbar_wait_bounded(bar_v + b, (uint32_t)(nv[b] - 1) & 1u, a.err);
+      }
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -765,25 +767,33 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
         // S(j+1) goes in ahead of PV(j): its TMEM buffer held P(j-1), which
         // PV(j-1), issued earlier, reads first
         if (j + 1 < n_blk && !issue_s(j + 1)) break;
-        if (!warp_wait_flag2(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, bar_v, (uint32_t)j & 1u, fail,
-                             a.err))
-          break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_p = tmem + P::T_S + 128 * (j & 1);
-        if (elect_one()) {
+        bool pv_ok = true;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 keys each; keys 64 h .. are thread half h's
-            const uint32_t ph = t_p + 64 * (kk >> 2) + 8 * (kk & 3), pl = ph + 32;
-            const uint32_t off = (kk >> 2) * D * 128 + (kk & 3) * 32;
-            if (kk == 0) mma_f16_ts(t_o, ph, dvh, idesc<D>(), j > 0);
-            else mma_f16_ts_acc(t_o, ph, sdesc_add(dvh, off), idesc<D>());
-            mma_f16_ts_acc(t_o, pl, sdesc_add(dvh, off), idesc<D>());
-            mma_f16_ts_acc(t_o, ph, sdesc_add(dvl, off), idesc<D>());
+        for (int h = 0; h < 2; ++h) {  // key half h: P columns of thread half h, V~^T half h
+          if (!(h == 0 ? warp_wait_flag2(bar_p + (j & 1), (uint32_t)(j >> 1) & 1u, bar_v,
+                                         (uint32_t)j & 1u, fail, a.err)
+                       : warp_wait_flag(bar_v + 1, (uint32_t)j & 1u, fail, a.err))) {
+            pv_ok = false;
+            break;
           }
-          mma_commit(bar_o);
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          if (elect_one()) {
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {  // 16 keys each
+              const uint32_t ph = t_p + 64 * h + 8 * kq, pl = ph + 32;
+              const uint32_t off = h * kVHalf + kq * 32;
+              if (h == 0 && kq == 0) mma_f16_ts(t_o, ph, dvh, idesc<D>(), j > 0);
+              else mma_f16_ts_acc(t_o, ph, sdesc_add(dvh, off), idesc<D>());
+              mma_f16_ts_acc(t_o, pl, sdesc_add(dvh, off), idesc<D>());
+              mma_f16_ts_acc(t_o, ph, sdesc_add(dvl, off), idesc<D>());
+            }
+            mma_commit(h == 0 ? bar_vh : bar_o);
+          }
+          __syncwarp();
+          last = h == 0 ? bar_vh : bar_o; last_par = (uint32_t)j & 1u;
         }
-        __syncwarp();
-        last = bar_o; last_par = (uint32_t)j & 1u;
+        if (!pv_ok) break;
       }
       // the tensor pipe completes in order: the last commit covers everything
       if (last != nullptr &&
