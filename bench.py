@@ -49,7 +49,7 @@ C_TILES, C_HEADS = 256, 8
 NCU_TRAFFIC = {
     # one 16k-context layer (128 tiles x 8 KV heads + a 124-token window): 17.88 MB
     # read, nothing written back within the launch
-    "decode_split": {"src_sha": "ed8b1bb7bfbbec11", "bytes": 17877248},
+    "decode_split": {"src_sha": "3fb3a5f88e862cc2", "bytes": 17877760},
     # one 2048-tile-head launch: 268.51 MB read + 17.56 MB written back within the launch
     "compress": {"src_sha": "39ae76a024c4acbb", "bytes": 286073856},
 }
