@@ -386,26 +386,6 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
     for (int o = tid * 16; o < bytes; o += 16 * P::NTHR)
       *reinterpret_cast<uint4*>(dst + o) = make_uint4(0x7E007E00u, 0x7E007E00u, 0x7E007E00u, 0x7E007E00u);
   };
-  // window block: raw rows rotated (K into K~, V into V~^T); rows past the
-  // window's length are zero
-  const int wb = j - a.n_tblk;
-  const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * wb);
-  const int64_t slot = ((int64_t)a.win_start + 128 * wb + row) % a.win_cap;
-  const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
-  auto win_row = [&](const float* base, float (&x)[D]) {
-    if (row < nkeys) {
-      const float4* src = reinterpret_cast<const float4*>(base + rbase);
-#pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4) {
-        const float4 v = src[c4];
-        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
-      }
-      fwht_reg<D>(x);
-    } else {
-#pragma unroll
-      for (int c = 0; c < D; ++c) x[c] = 0.f;
-    }
-  };
   // the staged half goes out with one bulk copy (async proxy: fence the
   // generic writes first); the CTA waits until the copy has read it
   auto store_half = [&](uint8_t* dst) {
@@ -414,52 +394,115 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
     if (tid == 0) bulk_store_wait(dst, sH, 2 * P::OPB);
     __syncthreads();
   };
+  // Tile images are written in blocks of 8 channels x 8 keys, one 16-byte
+  // chunk (8 consecutive elements of a swizzled row) per store. Thread ->
+  // block maps keep the 8 lanes of each store phase on 8 distinct chunk
+  // positions of their rows: the K~ lanes differ in the channel group (rows
+  // are keys), the V~^T lanes in the key group (rows are channels).
+  constexpr int NCG8 = D / 8;  // 8-channel groups
+
+  // window block: raw rows, rotated (K into K~, V into V~^T); rows past the
+  // window's length are zero. Two threads per row (its two channel halves)
+  // rotate their half in registers and meet for the butterfly over the top
+  // channel bit through a padded fp32 staging area over the (unused) record
+  // and image region, which the images then overwrite.
+  const int wb = j - a.n_tblk;
+  const int nkeys = is_tile ? 128 : min(128, a.win_len - 128 * wb);
+  const int64_t slot = ((int64_t)a.win_start + 128 * wb + row) % a.win_cap;
+  const int64_t rbase = ((int64_t)kvh * a.win_cap + slot) * D;
+  constexpr int HD = D / 2, XS = D + 4;  // half a row; staging row stride (floats)
+  static_assert(128 * XS * 4 <= P::template DQ<VB>::OFF_BAR, "window staging fits");
+  auto win_rotate = [&](const float* base, float (&x)[HD]) {
+    if (row < nkeys) {
+      const float4* src = reinterpret_cast<const float4*>(base + rbase + half * HD);
+#pragma unroll
+      for (int c4 = 0; c4 < HD / 4; ++c4) {
+        const float4 v = src[c4];
+        x[4 * c4] = v.x; x[4 * c4 + 1] = v.y; x[4 * c4 + 2] = v.z; x[4 * c4 + 3] = v.w;
+      }
+#pragma unroll
+      for (int h = 1; h < HD; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < HD; ++i)
+          if (!(i & h)) {
+            const float u = x[i], w = x[i | h];
+            x[i] = u + w;
+            x[i | h] = u - w;
+          }
+    } else {
+#pragma unroll
+      for (int c = 0; c < HD; ++c) x[c] = 0.f;
+    }
+    float* xb = reinterpret_cast<float*>(sm);
+#pragma unroll
+    for (int c4 = 0; c4 < HD / 4; ++c4)
+      *reinterpret_cast<float4*>(xb + row * XS + half * HD + 4 * c4) =
+          make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+    __syncthreads();
+    const float sc = 1.0f / sqrtf((float)D);
+#pragma unroll
+    for (int c4 = 0; c4 < HD / 4; ++c4) {
+      const float4 y = *reinterpret_cast<const float4*>(xb + row * XS + (half ^ 1) * HD + 4 * c4);
+      const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * c4 + e;
+        x[c] = (half == 0 ? x[c] + yv[e] : yv[e] - x[c]) * sc;  // low half: a + b, high: a - b
+      }
+    }
+    __syncthreads();  // the staging area is read before the images overwrite it
+  };
 
   // ---------------- K~ hi / lo  [128 keys][D]
   if (is_tile) {
     if (poison) {
       fill_nan(sH, 2 * P::OPB);
     } else {
-      // thread -> channel tid % D and a contiguous share of its 128 keys
       const unsigned char* kS = rec + R::kKS;
       const unsigned char* kD = rec + R::kKDelta;
       const unsigned char* kL = rec + R::kKLo;
       const unsigned char* kR = rec + R::kKR;
-      constexpr int NKG = P::NTHR / D, WPG = 16 / NKG;  // key groups, 8-key words per group
-      const int c = tid % D, kg = tid / D;
-      const float s = sc_ld<SB>(kS, c), d = sc_ld<SB>(kD, c) * s, lo = sc_ld<SB>(kL, c) * s;
-      const uint32_t* crow = reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64);
-      uint32_t wds[WPG];  // this thread's share of the channel row, read with 16-byte loads
+      for (int blk = tid; blk < 16 * NCG8; blk += P::NTHR) {
+        const int cg = blk % NCG8, kg = blk / NCG8;  // channels 8 cg .., keys 8 kg ..
+        float dd[8], ll[8];
+        uint32_t cw[8];  // nibble i of cw[e]: the code of key 8 kg + i, channel 8 cg + e
 #pragma unroll
-      for (int q4 = 0; q4 < WPG / 4; ++q4) {
-        const uint4 u = reinterpret_cast<const uint4*>(crow + WPG * kg)[q4];
-        wds[4 * q4] = u.x; wds[4 * q4 + 1] = u.y; wds[4 * q4 + 2] = u.z; wds[4 * q4 + 3] = u.w;
-      }
-#pragma unroll
-      for (int u = 0; u < WPG; ++u) {
-        const int w4 = WPG * kg + u;
-        const uint32_t wd = wds[u];
+        for (int e = 0; e < 8; ++e) {
+          const int c = 8 * cg + e;
+          const float sc = sc_ld<SB>(kS, c);
+          dd[e] = sc_ld<SB>(kD, c) * sc;
+          ll[e] = sc_ld<SB>(kL, c) * sc;
+          cw[e] = *reinterpret_cast<const uint32_t*>(rec + R::kKCodes + c * 64 + 4 * kg);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int t = 8 * w4 + i;
-          const float v = sc_ld<SB>(kR, t) * fmaf(d, (float)((wd >> (4 * i)) & 15u), lo);
-          const __half h = __float2half_rn(v);
-          const uint32_t o = sw_off(t, c, 128);
-          *reinterpret_cast<__half*>(sH + o) = h;
-          *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
+          const int t = 8 * kg + i;
+          const float r = sc_ld<SB>(kR, t);
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float v0 = r * fmaf(dd[2 * e2], (float)((cw[2 * e2] >> (4 * i)) & 15u), ll[2 * e2]);
+            const float v1 =
+                r * fmaf(dd[2 * e2 + 1], (float)((cw[2 * e2 + 1] >> (4 * i)) & 15u), ll[2 * e2 + 1]);
+            split2w(v0, v1, hw[e2], lw[e2]);
+          }
+          const uint32_t o = sw_off(t, 8 * cg, 128);
+          *reinterpret_cast<uint4*>(sH + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sL + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
     }
-  } else if (half == 0) {
-    float x[D];
-    win_row(a.win_k, x);
+  } else {
+    float x[HD];
+    win_rotate(a.win_k, x);
 #pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-      __align__(16) __half2 hi[4], lo[4];
+    for (int c8 = 0; c8 < HD / 8; ++c8) {
+      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split2(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(sH + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(hi);
-      *reinterpret_cast<uint4*>(sL + sw_off(row, 8 * c8, 128)) = *reinterpret_cast<uint4*>(lo);
+      for (int e2 = 0; e2 < 4; ++e2) split2w(x[8 * c8 + 2 * e2], x[8 * c8 + 2 * e2 + 1], hw[e2], lw[e2]);
+      const uint32_t o = sw_off(row, half * HD + 8 * c8, 128);
+      *reinterpret_cast<uint4*>(sH + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sL + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   }
   store_half(gimg);
@@ -469,77 +512,49 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
     if (poison) {
       fill_nan(sH, 2 * P::OPB);
     } else {
-      // thread -> key t, half of the D channels of the token row
       const unsigned char* vS = rec + R::kVS;
       const unsigned char* vR = rec + R::kVR;
       const unsigned char* vD = rec + R::kVDelta;
       const unsigned char* vL = rec + R::kVLo;
-      const int t = row;
-      const float r = sc_ld<SB>(vR, t);
-      const unsigned char* vrow = rec + R::kVCodes + t * R::kVRow;
-      if constexpr (VB == 3) {
-        // 3-bit codes: the row is a little-endian bit stream, eight channels
-        // in every three bytes; this thread's half of the channels starts at
-        // byte 3 D / 16 half
-        constexpr int HC = D / 2;
-        const unsigned char* hb = vrow + half * (3 * HC / 8);
-#pragma unroll 4
-        for (int j8 = 0; j8 < HC / 8; ++j8) {
-          const uint32_t w = (uint32_t)hb[3 * j8] | ((uint32_t)hb[3 * j8 + 1] << 8) |
-                             ((uint32_t)hb[3 * j8 + 2] << 16);
-          const int c0 = half * HC + 8 * j8;
-          const int g = c0 / R::kVGroup;
+      constexpr uint32_t kMask = (1u << VB) - 1u;
+      for (int blk = tid; blk < 16 * NCG8; blk += P::NTHR) {
+        const int tg = blk % 16, cg = blk / 16;  // keys 8 tg .., channels 8 cg ..
+        const int g = (8 * cg) / R::kVGroup;     // the channels' value group
+        float sv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sv[e] = sc_ld<SB>(vS, 8 * cg + e);
+        float vals[8][8];  // [channel e][key i]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int t = 8 * tg + i;
+          const float r = sc_ld<SB>(vR, t);
           const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
+          // the 8 codes of channels 8 cg .. form VB bytes of the row's bit stream
+          const unsigned char* cb = rec + R::kVCodes + t * R::kVRow + VB * cg;
+          uint32_t w = 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = c0 + e;
-            const float v = sc_ld<SB>(vS, c) * fmaf(d, (float)((w >> (3 * e)) & 7u), lo);
-            const __half h = __float2half_rn(v);
-            const uint32_t o = sw_off(c, t, D);
-            *reinterpret_cast<__half*>(sH + o) = h;
-            *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
-          }
+          for (int q = 0; q < VB; ++q) w |= (uint32_t)cb[q] << (8 * q);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vals[e][i] = sv[e] * fmaf(d, (float)((w >> (VB * e)) & kMask), lo);
         }
-      } else {
-      constexpr int CPB = 8 / VB;               // channels per code byte
-      constexpr int HB = R::kVRow / 2;          // code bytes of half a token row
-      uint32_t vw[HB / 4];                      // read with wide loads
-      if constexpr (HB >= 16) {
 #pragma unroll
-        for (int q4 = 0; q4 < HB / 16; ++q4) {
-          const uint4 u = reinterpret_cast<const uint4*>(vrow + half * HB)[q4];
-          vw[4 * q4] = u.x; vw[4 * q4 + 1] = u.y; vw[4 * q4 + 2] = u.z; vw[4 * q4 + 3] = u.w;
+        for (int e = 0; e < 8; ++e) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) split2w(vals[e][2 * i2], vals[e][2 * i2 + 1], hw[i2], lw[i2]);
+          const uint32_t o = sw_off(8 * cg + e, 8 * tg, D);
+          *reinterpret_cast<uint4*>(sH + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sL + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-      } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(vrow + half * HB);
-        vw[0] = u.x; vw[1] = u.y;
-      }
-#pragma unroll
-      for (int ub = 0; ub < HB; ++ub) {
-        const int jb = half * HB + ub;
-        const uint32_t byte = (vw[ub >> 2] >> (8 * (ub & 3))) & 0xFFu;
-        const int g = (CPB * jb) / R::kVGroup;
-        const float d = sc_ld<SB>(vD, t * R::kGv + g) * r, lo = sc_ld<SB>(vL, t * R::kGv + g) * r;
-#pragma unroll
-        for (int e = 0; e < CPB; ++e) {
-          const int c = CPB * jb + e;
-          const float code = (float)((byte >> (VB * e)) & ((1u << VB) - 1u));
-          const float v = sc_ld<SB>(vS, c) * fmaf(d, code, lo);
-          const __half h = __float2half_rn(v);
-          const uint32_t o = sw_off(c, t, D);
-          *reinterpret_cast<__half*>(sH + o) = h;
-          *reinterpret_cast<__half*>(sL + o) = __float2half_rn(v - __half2float(h));
-        }
-      }
       }
     }
-  } else if (half == 1) {  // V row -> column `row` of V~^T
-    float x[D];
-    win_row(a.win_v, x);
+  } else {  // V row -> column `row` of V~^T (this thread's channel half)
+    float x[HD];
+    win_rotate(a.win_v, x);
 #pragma unroll
-    for (int c = 0; c < D; ++c) {
+    for (int c = 0; c < HD; ++c) {
       const __half h = __float2half_rn(x[c]);
-      const uint32_t o = sw_off(c, row, D);
+      const uint32_t o = sw_off(half * HD + c, row, D);
       *reinterpret_cast<__half*>(sH + o) = h;
       *reinterpret_cast<__half*>(sL + o) = __float2half_rn(x[c] - __half2float(h));
     }
