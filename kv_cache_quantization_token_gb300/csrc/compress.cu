@@ -139,6 +139,13 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t floor_bits(float u) {
   return __float_as_uint(__fadd_rd(u, 8388608.0f));
 }
+// base with its bits pos .. pos + len - 1 replaced by the low len bits of
+// field (one bit-field insert)
+__device__ __forceinline__ uint32_t bfi(uint32_t field, uint32_t base, uint32_t pos, uint32_t len) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, %4;" : "=r"(r) : "r"(field), "r"(base), "r"(pos), "r"(len));
+  return r;
+}
 // 1 / delta, or 0 when delta is 0 or subnormal (every code of the group is
 // then 0 and the group reconstructs to lo)
 __device__ __forceinline__ float rtn_inv(float delta) {
@@ -296,9 +303,9 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
       }
       merge_eq(mean, m2, shfl_xor(mean, 1), shfl_xor(m2, 1), 64.f);
       const float var = m2 * (1.0f / 128.0f);
-      if (usable(var, mean)) {
-        s_own = sqrtf(var);
+      if (usable(var, mean)) {  // the std and its reciprocal from one rsqrt
         si_own = rsqrtf(var);
+        s_own = var * si_own;
       }
       if (h_own == 0) ch_a[p_own] = si_own;
     }
@@ -331,8 +338,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
     {
       const float var = rq[0] * (1.0f / (float)D);
       if (usable(var, rm[0])) {
-        r_own = sqrtf(var);
         ri_own = rsqrtf(var);
+        r_own = var * ri_own;
       }
       const float ri = ri_own;
 #pragma unroll
@@ -400,8 +407,8 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float2 u = fma2(add2(y2[i][k], nl), inv, f2(0.5f, 0.5f));
-        w0 |= (floor_bits(u.x) & 15u) << (4 * i);
-        w1 |= (floor_bits(u.y) & 15u) << (4 * i);
+        w0 = bfi(floor_bits(u.x), w0, 4 * i, 4);
+        w1 = bfi(floor_bits(u.y), w1, 4 * i, 4);
       }
       const int ca = (cg & 3) | ((2 * k) << 2) | ((cg >> 2) << 5);
       const int cb = (cg & 3) | ((2 * k + 1) << 2) | ((cg >> 2) << 5);
@@ -448,9 +455,13 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
-          const uint32_t c = (floor_bits(u.x) & 3u) | ((floor_bits(u.y) & 3u) << 8);
-          if (k < 2) wl |= c << (16 * k);
-          else wh |= c << (16 * (k - 2));
+          if (k < 2) {
+            wl = bfi(floor_bits(u.x), wl, 16 * k, 2);
+            wl = bfi(floor_bits(u.y), wl, 16 * k + 8, 2);
+          } else {
+            wh = bfi(floor_bits(u.x), wh, 16 * (k - 2), 2);
+            wh = bfi(floor_bits(u.y), wh, 16 * (k - 2) + 8, 2);
+          }
         }
         unsigned long long w = (((unsigned long long)wh << 32) | wl) << (2 * (cg & 3));
         w |= __shfl_xor_sync(0xffffffffu, w, 1);
@@ -500,7 +511,7 @@ compress_kernel(const float* __restrict__ k_raw, const float* __restrict__ v_raw
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 u = fma2(add2(y2[i][k], nl), iv2, f2(0.5f, 0.5f));
-          h4[k] = (floor_bits(u.x) & 15u) | ((floor_bits(u.y) & 15u) << 16);
+          h4[k] = bfi(floor_bits(u.y), floor_bits(u.x) & 15u, 16, 4);
         }
         // bytes 0..7 (slots 0..3), 8..15 (slots 4..7)
         unsigned long long w0 = (((unsigned long long)h4[1] << 32) | h4[0]) << sh;
