@@ -1124,17 +1124,24 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
       load_k(sKh, 0, 0, bar_kh);
       load_k(sKl, 1, 0, bar_kl);
       load_v(0);
-      // completion order of the tensor pipe: S(j-1) hi part, S(j-1), PV(j-1)
-      for (int j = 1; j < n_sub; ++j) {
-        if (!mbar_wait_flag(bar_khf, (uint32_t)(j - 1) & 1u, fail, a.err)) break;
-        load_k(sKh, 0, j, bar_kh);
-        ++nkh;
-        if (!mbar_wait_flag(bar_s + ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, fail, a.err)) break;
-        load_k(sKl, 1, j, bar_kl);
-        ++nkl;
-        if (!mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail, a.err)) break;
-        load_v(j);
-        ++nv;
+      // in the tensor pipe's completion order -- the K~ hi products of S(j),
+      // S(j), then PV(j-1) (S(j+1) goes in ahead of PV(j)) -- so that K~ hi of
+      // the next sub-block is requested as soon as its buffer is free, not
+      // after the P.V before it
+      for (int j = 0; j < n_sub; ++j) {
+        if (j + 1 < n_sub) {
+          if (!mbar_wait_flag(bar_khf, (uint32_t)j & 1u, fail, a.err)) break;
+          load_k(sKh, 0, j + 1, bar_kh);
+          ++nkh;
+          if (!mbar_wait_flag(bar_s + (j & 1), (uint32_t)(j >> 1) & 1u, fail, a.err)) break;
+          load_k(sKl, 1, j + 1, bar_kl);
+          ++nkl;
+        }
+        if (j >= 1) {
+          if (!mbar_wait_flag(bar_o, (uint32_t)(j - 1) & 1u, fail, a.err)) break;
+          load_v(j);
+          ++nv;
+        }
       }
       mbar_wait_bounded(bar_kh, (uint32_t)(nkh - 1) & 1u, a.err);
       mbar_wait_bounded(bar_kl, (uint32_t)(nkl - 1) & 1u, a.err);
