@@ -1066,18 +1066,31 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += C::NTHR) {
-    const int h = idx / D, c = idx % D;
-    float M = kNegInf;
+  {
+    // each thread takes channels of one head, so that the head's maximum and
+    // the warps' weights are formed once per thread, not once per channel
+    constexpr int TPH = C::NTHR / GP;  // threads per head slot
+    const int h = tid / TPH;
+    if (h < G) {
+      float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
-    float s = 0.f;
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w * 32 + h]);
+      float f[NW];
+      unsigned has = 0u;  // warps with a tile (m = -inf: none)
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float mw = red[w * 32 + h];  // -inf: a warp without a tile
-      if (mw != kNegInf) s = fmaf(vred[(w * GP + h) * C::DP + c], ex2_approx(mw - M), s);
+      for (int w = 0; w < NW; ++w) {
+        const float mw = red[w * 32 + h];
+        f[w] = ex2_approx(mw - M);
+        if (mw != kNegInf) has |= 1u << w;
+      }
+      for (int c = tid % TPH; c < D; c += TPH) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+          if (has & (1u << w)) s = fmaf(vred[(w * GP + h) * C::DP + c], f[w], s);
+        ws_acc[(part + (int64_t)h * items) * D + c] = bad ? NAN : s;
+      }
     }
-    ws_acc[(part + (int64_t)h * items) * D + c] = bad ? NAN : s;
   }
   if (tid < G) {
     float M = kNegInf, L = 0.f;
