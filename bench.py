@@ -202,6 +202,13 @@ def oracle_compress_baseline(sample: dict) -> dict:
         tn = (time.perf_counter() - t0) / n
     codes = differ = in_band = outside = 0
     worst = 0.0
+    # the offsets lo: how many meet 1e-6 relative to |lo| itself, how many only
+    # relative to max(|lo|, delta, RMS of the normalised tile) (the bound the
+    # parity tests apply: a constant group can put lo at a near-zero Walsh
+    # coefficient), and how many neither
+    lo_n = lo_plain = lo_widened_only = lo_out = 0
+    lo_worst = 0.0
+    gv = D // min(D, 128)
     for u, ref in enumerate(refs):
         got = oracle.unpack_record(recs[u * rb:(u + 1) * rb], D)
         want = oracle.unpack_record(ref["record"], D)
@@ -217,14 +224,37 @@ def oracle_compress_baseline(sample: dict) -> dict:
                 w = np.asarray(ref[f"{t}_{f}"], np.float64)
                 g = got[f"{t}_{f}"].astype(np.float64)
                 worst = max(worst, float(np.max(np.abs(g - w) / np.maximum(np.abs(w), 1e-30))))
+            lw = np.asarray(ref[f"{t}_lo"], np.float64)
+            dw = np.asarray(ref[f"{t}_delta"], np.float64)
+            if t == "k":
+                norm = dw[None, :] * vpre + lw[None, :]
+            else:
+                norm = (np.repeat(dw.reshape(128, gv), D // gv, axis=1) * vpre
+                        + np.repeat(lw.reshape(128, gv), D // gv, axis=1))
+            rms = float(np.sqrt(np.mean(norm ** 2)))
+            diff = np.abs(got[f"{t}_lo"].astype(np.float64) - lw)
+            plain = diff / np.maximum(np.abs(lw), 1e-30)
+            wide = diff / np.maximum(np.maximum(np.abs(lw), np.abs(dw)), max(rms, 1e-30))
+            plain[diff == 0] = 0.0
+            wide[diff == 0] = 0.0
+            lo_n += lw.size
+            lo_plain += int((plain <= 1e-6).sum())
+            lo_widened_only += int(((plain > 1e-6) & (wide <= 1e-6)).sum())
+            lo_out += int((wide > 1e-6).sum())
+            lo_worst = max(lo_worst, float(wide.max()))
     return {"oracle_tile_heads_per_s_1_core": 1.0 / t1,
             "oracle_tile_heads_per_s_all_cores": 1.0 / tn, "cores": cores,
             "sample": f"{n} tile-heads of the bulk-compress input (head_dim {D}); 4 on one thread",
             "gpu_vs_oracle": {"codes": codes, "differing": differ, "in_rounding_band": in_band,
                               "outside_rounding_band": outside,
                               "scale_rel_err_max": worst,
+                              "lo": {"values": lo_n, "within_1e-6_of_lo": lo_plain,
+                                     "within_1e-6_only_widened": lo_widened_only,
+                                     "outside_1e-6": lo_out, "widened_rel_err_max": lo_worst},
                               "note": "GPU records of the same units, decoded by the oracle; "
-                                      "delta, s and r compared relative to the oracle's value"}}
+                                      "delta, s and r compared relative to the oracle's value; "
+                                      "lo relative to |lo|, and to max(|lo|, delta, RMS of "
+                                      "the normalised tile)"}}
 
 
 def oracle_prefill_baseline(rows_every: int = 16) -> dict:
