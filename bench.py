@@ -47,11 +47,14 @@ C_TILES, C_HEADS = 256, 8
 # DRAM bytes per launch from an ncu capture, keyed by the kernel source they
 # were measured on (None until captured; ignored once the source changes).
 NCU_TRAFFIC = {
-    # one 16k-context layer (128 tiles x 8 KV heads + a 124-token window): 17.88 MB
-    # read, nothing written back within the launch
-    "decode_split": {"src_sha": "3fb3a5f88e862cc2", "bytes": 17877760},
-    # one 2048-tile-head launch: 268.51 MB read + 17.56 MB written back within the launch
-    "compress": {"src_sha": "3a34651e8ff2c571", "bytes": 286177792},
+    # one split launch of the decode section (128 tiles x 8 KV heads + a
+    # 124-token window, 17,809,408 algorithmic bytes): 17.88 MB read, nothing
+    # written back within the launch. The bench's timed launches run at a
+    # longer context, so the figure is scaled by their algorithmic bytes.
+    "decode_split": {"src_sha": "b497a42a471b3749", "bytes": 17876736, "algorithmic": 17809408},
+    # one 2048-tile-head launch (the one the bench times): 268.51 MB read +
+    # 17.58 MB written back within the launch
+    "compress": {"src_sha": "c4499b18558919c0", "bytes": 286092032},
 }
 
 
@@ -987,7 +990,8 @@ def main():
     split_gbs = split_bytes / (split_ms * 1e-3) / 1e9
     seq_gbs = split_bytes / (split_seq_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC["decode_split"]
-    traffic = tr["bytes"] if tr["src_sha"] == src_sha("decode.cu") else None
+    traffic = (round(tr["bytes"] * split_bytes / tr["algorithmic"])
+               if tr["src_sha"] == src_sha("decode.cu") else None)
 
     # ---- e2e: host buffers through the public API ---------------------------
     q_h = q.cpu().pin_memory()
@@ -1075,6 +1079,9 @@ def main():
                        "launch_flags": "PDL|PREFETCH"},
             "roofline": {"bound": "hbm", "achieved": seq_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": seq_gbs / hbm, "traffic": traffic,
+                         "traffic_source": "ncu DRAM read + write bytes of one split launch at "
+                                           "16.5k context (1.004 x its algorithmic bytes), scaled "
+                                           "to this launch's algorithmic bytes",
                          "kernel": "decode_split_kernel",
                          "timing": "average launch duration over back-to-back launches (see "
                                    "decode.back_to_back_timing)", "peak_source": peak_kind},
