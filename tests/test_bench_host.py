@@ -28,3 +28,35 @@ def test_traffic_table_names_existing_sources():
         entry = bench.NCU_TRAFFIC[name]
         assert len(entry["src_sha"]) == 16 and entry["bytes"] > 0
         assert len(bench.src_sha(src)) == 16
+
+
+def test_compress_parity_sample_counts():
+    """The bench's compress parity sample, fed the oracle's own records as the
+    device's: no code differs, scales agree to fp32 storage, every offset lo
+    meets 1e-6 relative to |lo| itself; a perturbed lo is counted as outside."""
+    import numpy as np
+    import oracle
+    from kv_cache_quantization_token_gb300 import synth
+    D = bench.D
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 0, 1, 128 * 4, D)
+    k, v = np.ascontiguousarray(ks[0]), np.ascontiguousarray(vs[0])
+    refs = [oracle.compress_unit(k[128 * u:128 * u + 128], v[128 * u:128 * u + 128]) for u in range(4)]
+    recs = np.frombuffer(b"".join(bytes(r["record"]) for r in refs), np.uint8).copy()
+    rb = recs.size // 4
+    got = bench.oracle_compress_baseline({"k": k, "v": v, "records": recs, "record_bytes": rb})
+    cmp_ = got["gpu_vs_oracle"]
+    assert cmp_["codes"] == 4 * 2 * 128 * D and cmp_["differing"] == 0
+    assert cmp_["scale_rel_err_max"] < 1e-6
+    lo = cmp_["lo"]
+    assert lo["values"] == 4 * (D + 128 * (D // min(D, 128)))
+    assert lo["within_1e-6_of_lo"] == lo["values"] and lo["outside_1e-6"] == 0
+    # one K offset of unit 0 moved by 1e-3 of the tile's scale: counted
+    # outside the bound, and nothing else changes
+    f = oracle.unpack_record(recs[:rb], D)
+    f["k_lo"][0] += 1e-3 * max(abs(f["k_lo"][0]), abs(f["k_delta"][0]), 1.0)
+    recs[:rb] = oracle.pack_record(D, f["k_codes"], f["v_codes"], f["k_delta"], f["k_lo"], f["k_s"],
+                                   f["k_r"], f["v_delta"], f["v_lo"], f["v_r"], f["v_s"])
+    got2 = bench.oracle_compress_baseline({"k": k, "v": v, "records": recs, "record_bytes": rb})
+    lo2 = got2["gpu_vs_oracle"]["lo"]
+    assert lo2["outside_1e-6"] == 1 and lo2["within_1e-6_only_widened"] == 0
+    assert got2["gpu_vs_oracle"]["differing"] == 0
