@@ -160,11 +160,20 @@ __device__ __forceinline__ void rotate_head_to_smem(const float* qh, bool valid,
 // ---------------------------------------------------------------------------
 // Tensor-core (mma.sync m16n8k16, fp16 x fp16 -> fp32) formulation of the two
 // contractions of a packed tile, with fragments built straight from the codes:
-//  scores  S[t][n] = sum_c A[t][c] B[c][n]   A = 1 + code/16 (exact in fp16),
-//                                            B = the folded query, split hi+lo
-//          sum_c wd_c code_tc = 16 (S - sum_c wd_c)
-//  values  O[c][n] = sum_t A[c][t] B[t][n]   A = 1 + code/4, B = p r delta hi+lo
-//          sum_t pd_t code_tc = 4 (O - sum_t pd_t)
+//  scores  S[t][n] = sum_c A[t][c] B[c][n]   A = code 2^-20 (an fp16 subnormal,
+//                                            exact), B = the folded query,
+//                                            split hi+lo
+//          sum_c wd_c code_tc = 2^20 S
+//  values  O[c][n] = sum_t A[c][t] B[t][n]   A = code 2^-18 (2-bit codes) or
+//                                            code 2^-20 (4-bit), B = p r delta
+//                                            hi+lo
+//          sum_t pd_t code_tc = 2^18 O or 2^20 O
+// A code moved to the top of the mantissa bits of its 16-bit half (bits 4..7
+// for a nibble, 6..7 for a 2-bit field) and masked is a subnormal, so a
+// fragment register is at most one shift and one AND of the loaded codes. The
+// tensor core sums subnormal products in a window placed as if each were as
+// large as the smallest normal, so codes sit near the top of the subnormal
+// range: low in the mantissa they would lose up to 12 bits of the sum.
 // Columns n are (query head, hi/lo part) pairs, 8 per n-tile. Each B operand is
 // scaled by a power of two per head (exact) so the fp16 parts stay in range.
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -175,25 +184,21 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// y * m + c on the integer multiply-add unit (keeps these off the logic pipe,
-// which the masks already occupy).
-__device__ __forceinline__ uint32_t imad(uint32_t y, uint32_t m, uint32_t c) {
-  uint32_t r;
-  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(y), "r"(m), "r"(c));
-  return r;
+// fp16 pair {c_lo 2^-20, c_hi 2^-20} (subnormals) from nibble n (0..3) of the
+// low and of the high 16-bit half of x: the nibble moved to bits 4..7.
+__device__ __forceinline__ uint32_t k_frag(uint32_t x, int n) {
+  const uint32_t y = n == 0 ? x << 4 : n == 1 ? x : x >> (4 * n - 4);
+  return y & 0x00F000F0u;
 }
-// fp16 pair {1 + c_lo/16, 1 + c_hi/16} from nibble j (0 or 1) of the low and of
-// the high 16-bit half of x (the code goes to mantissa bits 9..6); nibbles 2
-// and 3 are taken as nibbles 0 and 1 of x >> 8.
-__device__ __forceinline__ uint32_t k_frag(uint32_t x, int j) {
-  return imad(x & (j == 0 ? 0x000F000Fu : 0x00F000F0u), j == 0 ? 64u : 4u, 0x3C003C00u);
+// fp16 pair {c_lo 2^-18, c_hi 2^-18} (subnormals) from 2-bit field f (0..7) of
+// each 16-bit half of x: the field moved to bits 6..7.
+__device__ __forceinline__ uint32_t v_frag(uint32_t x, int f) {
+  const uint32_t y = f < 3 ? x << (6 - 2 * f) : f == 3 ? x : x >> (2 * f - 6);
+  return y & 0x00C000C0u;
 }
-// fp16 pair {1 + c_lo/4, 1 + c_hi/4} from 2-bit field m (0..3) of each 16-bit
-// half of x (the code goes to mantissa bits 9..8); fields 4..7 are taken as
-// fields 0..3 of x >> 8.
-__device__ __forceinline__ uint32_t v_frag(uint32_t x, int m) {
-  return imad(x & (0x00030003u << (2 * m)), 1u << (8 - 2 * m), 0x3C003C00u);
-}
+// 2^20 and 2^18: the inverse scale of a fragment's codes
+constexpr float kKCodeInv = 1048576.0f;
+constexpr float kVCodeInv = kVF == 2 ? 262144.0f : 1048576.0f;
 // Physical offset of logical byte o of a 1024-byte aligned region written by a
 // TMA copy with 128-byte swizzling (16-byte chunk index XOR 128-byte line index).
 __device__ __forceinline__ uint32_t swz128(uint32_t o) { return o ^ (((o >> 7) & 7u) << 4); }
@@ -363,8 +368,8 @@ struct DC {
   static constexpr int OFF_BX = OFF_QMAX + 32;
   static constexpr int OFF_SCW = OFF_BX;
   static constexpr int OFF_WRED = OFF_BX + SCW_BYTES;
-  static constexpr int OFF_PT = OFF_BX + (BX_BYTES > WIN_BYTES ? BX_BYTES : WIN_BYTES);  // (sum wd, bias) [TPS][WPT][GP]
-  static constexpr int OFF_FLG = OFF_PT + TPS * WPT * GP * 8;   // int [2 TPS]: slot copy issued / parity pending
+  static constexpr int OFF_PT = OFF_BX + (BX_BYTES > WIN_BYTES ? BX_BYTES : WIN_BYTES);  // bias [TPS][WPT][GP]
+  static constexpr int OFF_FLG = OFF_PT + TPS * WPT * GP * 4;   // int [2 TPS]: slot copy issued / parity pending
   static constexpr int NBAR = 2 * TPS > NW ? 2 * TPS : NW;       // one per record slot, or per window chunk
   static constexpr int OFF_BAR = (OFF_FLG + 2 * TPS * 4 + 7) / 8 * 8;
   static constexpr int OFF_REC = (OFF_BAR + NBAR * 8 + 1023) / 1024 * 1024;
@@ -621,7 +626,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
   const bool dbuf = MR && rounds > 1;              // two record slots per group
   float* qmax = reinterpret_cast<float*>(smem + C::OFF_QMAX);
   uint2* bx = reinterpret_cast<uint2*>(smem + C::OFF_BX);     // [TPS][NCB][NT][32]
-  float2* pt = reinterpret_cast<float2*>(smem + C::OFF_PT);   // [TPS][WPT][GP]
+  float* pt = reinterpret_cast<float*>(smem + C::OFF_PT);     // [TPS][WPT][GP]
   const bool issuer = lane == 0 && half == 0;                 // the group's copy issuer
   // Copies a packed tile into a record slot (one TMA box of codes plus one bulk
   // copy of the scales, completing on the slot's barrier); okf[slot] tells
@@ -711,19 +716,19 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
       float s_, i_;
       const float qb = 4 * nt + hb < GP ? qmax[4 * nt + hb] : 0.f;
       const float qa = 4 * nt + q4 < GP ? qmax[4 * nt + q4] : 0.f;
-      pow2_scale(qb * mf, 16.0f, scB[nt], i_);
-      pow2_scale(qa * mf, 16.0f, s_, invA[nt]);
+      pow2_scale(qb * mf, 1.0f, scB[nt], i_);
+      pow2_scale(qa * mf, 1.0f, s_, invA[nt]);
     }
     // this warp's share of the channel blocks: B fragments to shared memory, and
-    // per-head partial sums of wd (fp32) and of the bias q' s lo. In block cb,
+    // per-head partial sums of the bias q' s lo. In block cb,
     // lane (g8, q4) forms both fp16 parts of wd for head 4nt + hb on the channel
     // pair 16 cb + 2 q4 + 8 (g8 & 1) and swaps one part with lane ^ 4, which
     // took the other pair of the same head: the hi lane keeps both hi parts,
     // the lo lane both lo parts.
     const int hl = g8 & 1;
-    float2 wsum[NT], bsum[NT];
+    float2 bsum[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) { wsum[nt] = make_float2(0.f, 0.f); bsum[nt] = wsum[nt]; }
+    for (int nt = 0; nt < NT; ++nt) bsum[nt] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < HB; ++u) {
       const int cb = HB * half + u;
@@ -738,7 +743,6 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         const float2 qv = h < GP ? *reinterpret_cast<const float2*>(qs + ((c >> 1) * GP + h) * 2)
                                  : make_float2(0.f, 0.f);
         const float2 x = __fmul2_rn(qv, sd);
-        wsum[nt] = __fadd2_rn(wsum[nt], x);
         bsum[nt] = __ffma2_rn(qv, sl, bsum[nt]);
         const float2 xs = __fmul2_rn(x, make_float2(scB[nt], scB[nt]));
         const __half2 hi = __floats2half2_rn(xs.x, xs.y);
@@ -752,32 +756,24 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float ws = wsum[nt].x + wsum[nt].y, bs = bsum[nt].x + bsum[nt].y;
+      float bs = bsum[nt].x + bsum[nt].y;
 #pragma unroll
-      for (int m = 1; m <= 4; m <<= 1) {  // over q4 and the hi/lo lane: all channels of this warp's share
-        ws += __shfl_xor_sync(0xffffffffu, ws, m);
+      for (int m = 1; m <= 4; m <<= 1)  // over q4 and the hi/lo lane: all channels of this warp's share
         bs += __shfl_xor_sync(0xffffffffu, bs, m);
-      }
-      if (q4 == 0 && is_hi && 4 * nt + hb < GP)
-        pt[(kk * WPT + half) * GP + 4 * nt + hb] = make_float2(ws, bs);
+      if (q4 == 0 && is_hi && 4 * nt + hb < GP) pt[(kk * WPT + half) * GP + 4 * nt + hb] = bs;
     }
     asm volatile("bar.sync %0, %1;" ::"r"(1 + pair), "n"(32 * WPT) : "memory");  // the group's barrier
 
-    // sum_c wd_c code_tc = S inv - 16 sum_c wd_c: per-head constants of the
-    // accumulator view (head 4nt + q4)
+    // the bias sum_c q'_c s_c lo_c per head of the accumulator view (head 4nt + q4)
     float cstA[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float ws = 0.f, bs = 0.f;
+      float bs = 0.f;
       if (4 * nt + q4 < GP) {
 #pragma unroll
-        for (int w = 0; w < WPT; ++w) {
-          const float2 v = pt[(kk * WPT + w) * GP + 4 * nt + q4];
-          ws += v.x;
-          bs += v.y;
-        }
+        for (int w = 0; w < WPT; ++w) bs += pt[(kk * WPT + w) * GP + 4 * nt + q4];
       }
-      cstA[nt] = bs - 16.0f * ws;
+      cstA[nt] = bs;
     }
 
     // ---- phase A: scores of this warp's 32 CH tokens. Chunk w4 = tokens 32 w4 ..
@@ -808,9 +804,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         ldsm_x4_t(rk + swz128(kaddr0 + (uint32_t)(cp * 16 * 64 + 16 * w2)), x[0], x[1], x[2], x[3]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const uint32_t xl = x[2 * u], xh = x[2 * u + 1], xl8 = xl >> 8, xh8 = xh >> 8;
+          const uint32_t xl = x[2 * u], xh = x[2 * u + 1];
           const uint32_t a00 = k_frag(xl, 0), a01 = k_frag(xl, 1), a02 = k_frag(xh, 0), a03 = k_frag(xh, 1);
-          const uint32_t a10 = k_frag(xl8, 0), a11 = k_frag(xl8, 1), a12 = k_frag(xh8, 0), a13 = k_frag(xh8, 1);
+          const uint32_t a10 = k_frag(xl, 2), a11 = k_frag(xl, 3), a12 = k_frag(xh, 2), a13 = k_frag(xh, 3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(acc[w2][0][nt], a00, a01, a02, a03, bf[u][nt].x, bf[u][nt].y);
@@ -832,8 +828,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            z[w2][j][rr][nt] = rt[j][rr] * fmaf(acc[w2][j][nt][2 * rr] + acc[w2][j][nt][2 * rr + 1],
-                                                invA[nt], cstA[nt]);
+            z[w2][j][rr][nt] =
+                rt[j][rr] * fmaf((acc[w2][j][nt][2 * rr] + acc[w2][j][nt][2 * rr + 1]) * kKCodeInv,
+                                 invA[nt], cstA[nt]);
     }
     // streaming state of the warp: the running maximum moves to mn, earlier
     // sums are rescaled by alpha (0 on the group's first tile)
@@ -914,14 +911,12 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
 #pragma unroll
         for (int m = 4; m < 32; m <<= 1) pm[nt] = fmaxf(pm[nt], __shfl_xor_sync(0xffffffffu, pm[nt], m));
         float sc2, inv2;
-        pow2_scale(pm[nt], kVF == 2 ? 4.0f : 16.0f, sc2, inv2);
-        float sp = 0.f;
+        pow2_scale(pm[nt], 1.0f, sc2, inv2);
 #pragma unroll
         for (int w2 = 0; w2 < CH; ++w2)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const float xa = pd[w2][j][0][nt] * sc2, xb = pd[w2][j][1][nt] * sc2;
-            sp += xa + xb;
             const uint32_t xl = hilo_one(xa);  // row g8: token 4 g8 + 2j
             const uint32_t xh = hilo_one(xb);  // token 4 g8 + 2j + 1
             bB[gv][w2][j][nt][0] = movmatrix_t(xl);
@@ -929,12 +924,9 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           }
         float l2 = lt[nt];
 #pragma unroll
-        for (int m = 4; m < 32; m <<= 1) {
-          sp += __shfl_xor_sync(0xffffffffu, sp, m);
-          l2 += __shfl_xor_sync(0xffffffffu, l2, m);
-        }
+        for (int m = 4; m < 32; m <<= 1) l2 += __shfl_xor_sync(0xffffffffu, l2, m);
         invP[gv][nt] = inv2;
-        cstP[gv][nt] = fmaf(-sp, inv2, l2);
+        cstP[gv][nt] = l2;
       }
     }
 
@@ -967,32 +959,24 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
         uint32_t y[4];  // (K-block j, b0/b1 tokens) = (0,0), (0,1), (1,0), (1,1)
         ldsm_x4_t(rk + swz128(vaddr0 + (uint32_t)(32 * w2 * C::V_ROW + 16 * sl)), y[0], y[1], y[2],
                   y[3]);
-        const uint32_t y8[4] = {y[0] >> 8, y[1] >> 8, y[2] >> 8, y[3] >> 8};
 #pragma unroll
         for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             uint32_t a0, a1, a2, a3;
-            if constexpr (kVF == 2) {
-              // fields 2 mu and 2 mu + 1: fields 0..3 of y, or of y >> 8 for mu >= 2
-              const uint32_t ya = mu < 2 ? y[2 * j] : y8[2 * j];
-              const uint32_t yb = mu < 2 ? y[2 * j + 1] : y8[2 * j + 1];
-              const int f = 2 * (mu & 1);
-              a0 = v_frag(ya, f); a1 = v_frag(ya, f + 1);
-              a2 = v_frag(yb, f); a3 = v_frag(yb, f + 1);
-            } else {
-              // nibbles 2 mu and 2 mu + 1: nibbles 0, 1 of y, or of y >> 8 for mu = 1
-              const uint32_t ya = mu == 0 ? y[2 * j] : y8[2 * j];
-              const uint32_t yb = mu == 0 ? y[2 * j + 1] : y8[2 * j + 1];
-              a0 = k_frag(ya, 0); a1 = k_frag(ya, 1);
-              a2 = k_frag(yb, 0); a3 = k_frag(yb, 1);
+            if constexpr (kVF == 2) {  // fields 2 mu and 2 mu + 1
+              a0 = v_frag(y[2 * j], 2 * mu); a1 = v_frag(y[2 * j], 2 * mu + 1);
+              a2 = v_frag(y[2 * j + 1], 2 * mu); a3 = v_frag(y[2 * j + 1], 2 * mu + 1);
+            } else {  // nibbles 2 mu and 2 mu + 1
+              a0 = k_frag(y[2 * j], 2 * mu); a1 = k_frag(y[2 * j], 2 * mu + 1);
+              a2 = k_frag(y[2 * j + 1], 2 * mu); a3 = k_frag(y[2 * j + 1], 2 * mu + 1);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816(o[mu][nt], a0, a1, a2, a3, bB[gv][w2][j][nt][0], bB[gv][w2][j][nt][1]);
           }
       }
-      // acc_c = alpha acc_c + s_c (2^VB 2^-e (O - sum pd) + sum p r lo)
+      // acc_c = alpha acc_c + s_c (2^-e 2^18 O + sum p r lo) (2^20 for 4-bit codes)
       float sv[MU][2];
 #pragma unroll
       for (int h4 = 0; h4 < MU / 2; ++h4) {
@@ -1007,7 +991,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-              const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
+              const float O = (o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1]) * kVCodeInv;
               out_acc[sl][mu][rr][nt] = sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]);
             }
       } else {
@@ -1017,7 +1001,7 @@ decode_split_kernel(const float* __restrict__ q, const uint8_t* __restrict__ til
           for (int mu = 0; mu < MU; ++mu)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-              const float O = o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1];
+              const float O = (o[mu][nt][2 * rr] + o[mu][nt][2 * rr + 1]) * kVCodeInv;
               out_acc[sl][mu][rr][nt] = fmaf(out_acc[sl][mu][rr][nt], alpha[nt],
                                              sv[mu][rr] * fmaf(O, invP[gv][nt], cstP[gv][nt]));
             }
