@@ -350,6 +350,9 @@ __global__ void __launch_bounds__(256, (D == 256) ? 1 : 2) prefill_dequant_kerne
   unsigned char* sL = sH + P::OPB;                        // lo image
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + P::template DQ<VB>::OFF_BAR);
   const int j = a.first_blk + blockIdx.x, kvh = blockIdx.y;
+  // the attention kernel may start now: it prepares its query rows and waits
+  // for this grid before it reads an image
+  pdl_trigger();
   uint8_t* gimg = a.ws + ((int64_t)kvh * a.ws_stride + j) * P::BLK;
   const int tid = threadIdx.x, row = tid & 127, half = tid >> 7;
   const bool is_tile = j < a.n_tblk;  // uniform over the CTA
@@ -674,6 +677,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel(const PrefillArgs a) {
     ++nv[h];
   };
   if (warp == 9 && lane == 0 && n_blk > 0) {
+    pdl_wait();  // the images of this call's dequantisation grid are complete
     load_k(0);
     if (n_blk > 1) load_k(1);
     load_v(0, 0);
@@ -1108,6 +1112,7 @@ __global__ void __launch_bounds__(320, 1) prefill_kernel_d256(const PrefillArgs 
         bulk_copy_tx(sVh, src, P::VSB, bar_v);
         bulk_copy_tx(sVh + P::VSB, src + PC<256>::OPB, P::VSB, bar_v);
       };
+      pdl_wait();  // the images of this call's dequantisation grid are complete
       load_k(sKh, 0, 0, bar_kh);
       load_k(sKl, 1, 0, bar_kl);
       load_v(0);
@@ -1381,7 +1386,14 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  if (a.n_blk > a.first_blk) {
+  // With a dequantisation grid in front, the attention kernel is a programmatic
+  // dependent of it: its CTAs may take the SMs the dequantisation leaves free
+  // and rotate their query rows meanwhile; the loader waits for the grid before
+  // its first image copy. The dequantisation grid itself starts only after all
+  // earlier work on the stream, so everything else the attention kernel reads
+  // (the queries) is complete either way.
+  const bool dq = a.n_blk > a.first_blk;
+  if (dq) {
     prefill_dequant_kernel<D, SB, VB><<<dim3(a.n_blk - a.first_blk, a.Hkv), P::NTHR,
                                         P::template DQ<VB>::SMEM, st>>>(a);
     e = cudaGetLastError();
@@ -1389,28 +1401,41 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t st) {
   }
   const int ppc = 128 / a.G;
   dim3 grid((a.C + ppc - 1) / ppc, a.Hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(P::NTHR_ATT);
+  cfg.dynamicSmemBytes = att_smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (dq) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if constexpr (D == 256) {
     // a grid that leaves more than half of the SMs idle splits each row
     // block's keys over a cluster of two CTAs
     const int64_t ctas = (int64_t)grid.x * grid.y;
     const int ns = 2 * ctas <= sm_count() ? 2 : 1;
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid.x, grid.y, ns);
     cfg.blockDim = dim3(320);
-    cfg.dynamicSmemBytes = att_smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = ns;
+    if (ns > 1) {
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = 1;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = ns;
+      ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = ns > 1 ? 1 : 0;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, prefill_kernel_d256, a);
-    if (e != cudaSuccess) return e;
   } else {
-    prefill_kernel<D><<<grid, P::NTHR_ATT, att_smem, st>>>(a);
+    cfg.gridDim = grid;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, a);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
