@@ -401,7 +401,10 @@ int kvarn_decode_attention(const float* q, const uint8_t* tiles, int64_t tiles_b
  * space) is written once per KV head into ws as fp16 operand images, then one
  * attention kernel per (KV head, 128 score rows) streams those images through
  * shared memory; the softmax, causal mask and final inverse rotation run on
- * CUDA cores.
+ * CUDA cores. The call as a whole is ordered after earlier work on the
+ * stream. Within it, the attention kernel is a programmatic dependent of the
+ * dequantisation kernel: it may rotate its query rows while the images are
+ * being written, and reads an image only after they all are.
  *   q_chunk    : fp32 [C][Hq][D], unrotated; out: fp32 [C][Hq][D].
  *   tiles      : u8 base of the record pool, tiles_bytes long.
  *   tile_table : int64 [Hkv][table_stride] record byte offsets (multiples of
