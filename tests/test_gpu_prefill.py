@@ -150,3 +150,47 @@ def test_prefill_repeat_is_bit_identical():
         np.testing.assert_array_equal(a.snap[p]["out"], b.snap[p]["out"])
     last = max(a.snap)
     a.check(last, _rows(a.snap[last]["C"], (0, 7, 30), step=41))
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,chunk,W", [(32, 8, 128, 1400, 512, 256), (16, 4, 256, 1100, 512, 256)])
+def test_prefill_graph_replay_matches_direct_call(Hq, Hkv, D, n, chunk, W):
+    """A prefill call captured in a CUDA graph (its attention kernel a
+    programmatic dependent of its dequantisation grid; at head_dim 256 also a
+    two-CTA cluster) replays to the direct call's output bit for bit: with
+    every block converted, with only the window blocks converted, and with
+    nothing to convert (a one-token chunk at the last tile position: no
+    dequantisation grid in front, a plain launch)."""
+    run = PrefillRun("qwen3_8b_prefill", 11, n, Hq=Hq, Hkv=Hkv, D=D, W=W, chunk=chunk)
+    last = max(run.snap)
+    s = run.snap[last]
+    dev = torch.device("cuda:0")
+    q_last = torch.from_numpy(run.q[last:last + s["C"]]).to(dev)
+    p_tile = 128 * s["n_tiles"] - 1
+    q_tile = torch.from_numpy(run.q[p_tile:p_tile + 1]).to(dev)
+    wk = torch.from_numpy(s["win_k"]).to(dev)
+    wv = torch.from_numpy(s["win_v"]).to(dev)
+    cap = wk.shape[1]
+    ws_blocks = s["n_tiles"] + cap // 128
+    ws = torch.empty(kvarn.prefill_workspace_bytes(s["n_tiles"], cap, Hkv, D), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(q, pos0, out, cached):
+        return kvarn.prefill_attention(q, pos0, run.tiles, run.table, s["n_tiles"], wk, wv,
+                                       s["start"], s["length"], run.lay, ws=ws, out=out,
+                                       ws_blocks=ws_blocks, cached_tiles=cached)
+
+    for q, pos0, cached in [(q_last, last, 0), (q_last, last, s["n_tiles"]),
+                            (q_tile, p_tile, s["n_tiles"])]:
+        direct = torch.full(q.shape, float("nan"), device=dev)
+        replay = torch.full(q.shape, float("nan"), device=dev)
+        with torch.cuda.stream(stream):
+            call(q, pos0, direct, 0)  # every image rebuilt: the reference output
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(q, pos0, replay, cached)
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(direct, replay), f"pos0={pos0} cached={cached}: graph replay differs"
+        if pos0 == last:
+            np.testing.assert_array_equal(replay.cpu().numpy(), s["out"])
