@@ -676,3 +676,30 @@ def test_v3_distortion_between_v2_and_v4(oracle):
             assert np.all(e <= bound * (1 + 1e-9))
         err[vb] = np.linalg.norm(e)
     assert err[4] < err[3] < err[2]
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("scale_bits", [32, 16])
+@pytest.mark.parametrize("v_bits", [2, 3, 4])
+def test_dequant_is_the_scaled_affine_code_rotated_back(oracle, D, scale_bits, v_bits):
+    """Issue #180, "Algorithm (per 128-token tile)": a stored row is rebuilt as
+    r_t s_c (delta code + lo) in the rotated space, keys with per-channel
+    (delta, lo), values with per-token (delta, lo) for each 128-channel group,
+    then rotated back by the orthonormal Sylvester-Hadamard matrix (scipy).
+    Written here from the record's unpacked fields, at every value width and
+    both scale widths."""
+    k, v = synth.kv_stream("batched_d256_decode" if D == 256 else "qwen3_8b_decode", 3, 1, 128, D)
+    rec = oracle.compress_unit(k, v, scale_bits=scale_bits, v_bits=v_bits)["record"]
+    u = oracle.unpack_record(rec, D, scale_bits, v_bits)
+    kh, vh = oracle.dequant_record(rec, D, scale_bits, v_bits)
+    H = scipy.linalg.hadamard(D) / np.sqrt(D)
+    kc, vc = u["k_codes"].astype(np.float64), u["v_codes"].astype(np.float64)
+    k_rot = u["k_r"][:, None] * u["k_s"][None, :] * (u["k_delta"][None, :] * kc + u["k_lo"][None, :])
+    gv = D // 128
+    g = np.arange(D) // 128
+    vd = u["v_delta"].reshape(128, gv)[:, g]
+    vl = u["v_lo"].reshape(128, gv)[:, g]
+    v_rot = u["v_r"][:, None] * u["v_s"][None, :] * (vd * vc + vl)
+    assert vc.max() <= 2 ** v_bits - 1 and kc.max() <= 15
+    np.testing.assert_allclose(kh, k_rot @ H, rtol=1e-10, atol=1e-12 * np.abs(kh).max())
+    np.testing.assert_allclose(vh, v_rot @ H, rtol=1e-10, atol=1e-12 * np.abs(vh).max())
