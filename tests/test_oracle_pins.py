@@ -703,3 +703,43 @@ def test_dequant_is_the_scaled_affine_code_rotated_back(oracle, D, scale_bits, v
     assert vc.max() <= 2 ** v_bits - 1 and kc.max() <= 15
     np.testing.assert_allclose(kh, k_rot @ H, rtol=1e-10, atol=1e-12 * np.abs(kh).max())
     np.testing.assert_allclose(vh, v_rot @ H, rtol=1e-10, atol=1e-12 * np.abs(vh).max())
+
+
+def test_prefill_window_token_sits_after_the_tiles(oracle):
+    """c8 positions with tiles and a window: tile k holds positions
+    [128k, 128k + 128), window token j position 128 n_tiles + j (PR #434,
+    commit 6040076: the window stages the newest tokens). Perturbing window
+    token j leaves every query row at an earlier position bit-identical,
+    including rows inside the tiles. With a zero query (equal weights over the
+    visible tokens) a row at position p >= 128 n_tiles + j moves by exactly
+    the value's change divided by p + 1."""
+    Hkv, Hq, D, n = 1, 2, 64, 424
+    ks, vs = synth.kv_layer("qwen3_8b_decode", 1, Hkv, n, D)
+    sm = oracle.CacheStateMachine(Hkv, D, W=128)
+    for pos in range(n):
+        sm.append(ks[:, pos:pos + 1].transpose(1, 0, 2), vs[:, pos:pos + 1].transpose(1, 0, 2))
+    assert sm.n_tiles == 3 and sm.win_len == 40
+    rb = oracle.record_bytes(D)
+    pool = np.concatenate([r[0] for r in sm.records])
+    table = (np.arange(sm.n_tiles, dtype=np.int64) * rb)[None, :]
+    wk, wv = sm.window(0)
+    win_k = np.zeros((1, 64, D), np.float32)
+    win_v = np.zeros((1, 64, D), np.float32)
+    win_k[0, :40], win_v[0, :40] = wk, wv
+    pos0, C = 300, n - 300
+    q = synth.queries("qwen3_8b_decode", 1, (C, Hq, D))
+    q[:, 0] = 0.0  # head 0: equal weights
+    base = oracle.prefill_attention(q, pos0, pool, table, sm.n_tiles, win_k, win_v, 0, 40, 1 / 8)
+    j = 10
+    pk, pv = win_k.copy(), win_v.copy()
+    pk[0, j] += 3.0
+    pv[0, j] -= 5.0
+    moved = oracle.prefill_attention(q, pos0, pool, table, sm.n_tiles, pk, pv, 0, 40, 1 / 8)
+    p_j = 128 * sm.n_tiles + j
+    dv = pv[0, j].astype(np.float64) - win_v[0, j].astype(np.float64)
+    for (i, h), o in base.items():
+        p = pos0 + i
+        if p < p_j:
+            np.testing.assert_array_equal(moved[(i, h)], o)
+        elif h == 0:
+            np.testing.assert_allclose(moved[(i, h)] - o, dv / (p + 1), rtol=1e-9, atol=1e-13)
