@@ -743,3 +743,44 @@ def test_prefill_window_token_sits_after_the_tiles(oracle):
             np.testing.assert_array_equal(moved[(i, h)], o)
         elif h == 0:
             np.testing.assert_allclose(moved[(i, h)] - o, dv / (p + 1), rtol=1e-9, atol=1e-13)
+
+
+def test_decode_batch_rows_are_independent(oracle):
+    """c7 over a batch: each sequence reads only its own table row, tile count,
+    window ring, start and length. Two sequences with different tile counts,
+    windows and ring starts give, head by head, the result of decoding each
+    sequence alone."""
+    Hkv, G, D, cap = 2, 2, 64, 256
+    Hq = Hkv * G
+    rb = oracle.record_bytes(D)
+    seqs = []
+    for b, (n, start) in enumerate([(128 * 3 + 37, 200), (128 + 5, 17)]):
+        ks, vs = synth.kv_layer("qwen3_8b_decode", 5 + b, Hkv, n, D)
+        sm = oracle.CacheStateMachine(Hkv, D, W=128)
+        sm.append(ks.transpose(1, 0, 2), vs.transpose(1, 0, 2))
+        win_k = np.zeros((Hkv, cap, D), np.float32)
+        win_v = np.zeros((Hkv, cap, D), np.float32)
+        for h in range(Hkv):
+            wk, wv = sm.window(h)
+            for w in range(sm.win_len):
+                win_k[h, (start + w) % cap], win_v[h, (start + w) % cap] = wk[w], wv[w]
+        seqs.append((sm, win_k, win_v, start))
+    max_tiles = max(s[0].n_tiles for s in seqs)
+    # one pool: sequence b's tile t of KV head h at record ((b * Hkv + h) * max_tiles + t)
+    pool = np.zeros(2 * Hkv * max_tiles * rb, np.uint8)
+    table = np.zeros((2, Hkv, max_tiles), np.int64)
+    for b, (sm, _, _, _) in enumerate(seqs):
+        for t in range(sm.n_tiles):
+            for h in range(Hkv):
+                off = ((b * Hkv + h) * max_tiles + t) * rb
+                pool[off:off + rb] = sm.records[t][h]
+                table[b, h, t] = off
+    q = synth.queries("qwen3_8b_decode", 9, (2, Hq, D))
+    both = oracle.decode_attention(q, pool, table, [s[0].n_tiles for s in seqs],
+                                   np.stack([s[1] for s in seqs]), np.stack([s[2] for s in seqs]),
+                                   [s[3] for s in seqs], [s[0].win_len for s in seqs], 1 / 8)
+    for b, (sm, win_k, win_v, start) in enumerate(seqs):
+        alone = oracle.decode_attention(q[b:b + 1], pool, table[b:b + 1], [sm.n_tiles],
+                                        win_k[None], win_v[None], [start], [sm.win_len], 1 / 8)
+        for h in range(Hq):
+            np.testing.assert_array_equal(both[(b, h)], alone[(0, h)])
